@@ -1,0 +1,526 @@
+"""CPU oracle for the DFlash block-diffusion draft round.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+link this module: it is used by tests/, by the smoke check in
+__graft_entry__.py and by bench.py's cpu_baseline / reference legs, and by
+nothing else.  It shares no code with the CUDA library.
+
+What it computes, step by step, in float64 with plain numpy (one row at a
+time, so every row's arithmetic is independent of how many rows share a
+call):
+
+  * committed / takePending / commitBlock / flush / propose / selectBlock:
+    the drafter session state machine of ollama's ``mlxrunner/dflash.go``
+    (gitea mirror; functions of the same names);
+  * the context path aux_hidden_norms -> fc -> hidden_norm, then each
+    layer's input_layernorm before a K/V-only projection (mlxcel PR #1771
+    "add the Laguna DFlash drafter": summary and "Where the landed code and
+    the issue text disagree");
+  * the block forward over [anchor, mask x n] with the anchor row dropped
+    before the unembedding ("Ollama DFlash block-diffusion draft model in
+    mlxrunner", Facts; dflash.go propose/selectBlock);
+  * sampling from one batched distribution (dflash.go selectBlock), done as
+    Gumbel-max with a counter-based generator so that the CUDA side can draw
+    the same token;
+  * speculative verification: accepted prefix plus a bonus token, exact
+    with respect to the target because it uses the actual proposal
+    probabilities (dflash.go propose comment; DFlash2 commit note), as in
+    Leviathan, Kalman & Matias (2023) and Chen et al. (2023).
+
+Readings where the pages are silent (each listed in the design doc):
+  R1 norm gains are inputs (random 1 + N(0, 0.02) in tests);
+  R3 eps = 1e-6;  R4 one RMSNorm per tap over that tap's slice;
+  R5 per-head RMSNorm on q and k;  R6 rotate-half RoPE on pairs (j, j+d/2);
+  R7 a query at position p sees a key at r iff p - r < W;
+  R8 fused qkv rows are ordered q | k | v;  R9 one sigmoid gate per query
+  head from g_proj;  R10 bidirectional attention inside the block unless the
+  config says causal;  R11 block K/V never persist (rewound before any write);
+  R13 full-vocabulary distributions (no top-k / top-p);  R15 if the
+  residual max(0, p - q) sums to zero, the bonus is drawn from p.
+
+Storage rounding: for bf16 configs the values that the CUDA path stores in
+bf16 are rounded to the nearest bf16 here too (u, c, the layer inputs fed to
+matrix products, q, the cache K/V, the attention output, the residual h after
+each add, the SwiGLU product, the final-norm output); fp32 configs round the
+same points to fp32.  Everything between two storage points stays float64.
+
+Parity pins: see tests/test_oracle_*.py.  Parity is unpinned only for the
+architecture readings above (they are choices, not facts of the pages) and
+for proposal probabilities of trained weights (none exist here).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+PENDING_FLUSH_TOKENS = 256   # dflash.go: dflashPendingFlushTokens
+
+
+class ContextGap(Exception):
+    """A committed run starts past the buffered frontier (dflash.go committed)."""
+
+
+# ---------------------------------------------------------------------------
+# Number formats
+# ---------------------------------------------------------------------------
+
+def round_bf16(x) -> np.ndarray:
+    """Nearest bf16 value (ties to even) of float64 input, returned as float64.
+
+    bf16 keeps 8 significant bits, so 45 of float64's 53 are dropped.  Values
+    are assumed to lie in bf16's normal range (true for every tensor here).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    b = x.view(np.uint64)
+    lsb = (b >> np.uint64(45)) & np.uint64(1)
+    b = (b + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)
+    return b.view(np.float64)
+
+
+def storage_round(dtype: str):
+    if dtype == "bf16":
+        return round_bf16
+    if dtype == "f32":
+        return lambda x: np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+# ---------------------------------------------------------------------------
+# Counter-based random numbers: Philox4x32-10
+# Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+# SC'11.  Each round multiplies words 0 and 2 by two constants, keeps the
+# 64-bit products' halves, and xors the high halves with words 1/3 and the
+# key; the key is bumped by two Weyl constants between rounds.
+# ---------------------------------------------------------------------------
+
+_PHILOX_M0 = np.uint64(0xD2511F53)
+_PHILOX_M1 = np.uint64(0xCD9E8D57)
+_PHILOX_W0 = np.uint64(0x9E3779B9)
+_PHILOX_W1 = np.uint64(0xBB67AE85)
+_MASK32 = np.uint64(0xFFFFFFFF)
+
+
+def philox4x32_10(c0, c1, c2, c3, k0, k1):
+    """Vectorised Philox4x32 with 10 rounds; all arguments uint32-valued arrays."""
+    c0, c1, c2, c3 = (np.asarray(v, dtype=np.uint64) & _MASK32 for v in (c0, c1, c2, c3))
+    k0 = np.asarray(k0, dtype=np.uint64) & _MASK32
+    k1 = np.asarray(k1, dtype=np.uint64) & _MASK32
+    c0, c1, c2, c3, k0, k1 = np.broadcast_arrays(c0, c1, c2, c3, k0, k1)
+    k0 = k0.copy(); k1 = k1.copy()
+    for r in range(10):
+        if r > 0:
+            k0 = (k0 + _PHILOX_W0) & _MASK32
+            k1 = (k1 + _PHILOX_W1) & _MASK32
+        p0 = _PHILOX_M0 * c0          # < 2^64: no overflow in uint64
+        p1 = _PHILOX_M1 * c2
+        hi0, lo0 = p0 >> np.uint64(32), p0 & _MASK32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & _MASK32
+        c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0
+    return c0, c1, c2, c3
+
+
+def random_u32(seed: int, rnd: int, stream: int, seq: int, row: int, v):
+    """Word 0 of Philox4x32-10 at counter (v, row | stream<<16, seq, round),
+    key (low 32 bits of seed, high 32 bits of seed)."""
+    seed = int(seed) & (2**64 - 1)
+    u64 = lambda a: np.asarray(a, dtype=np.uint64)
+    ctr1 = (u64(row) & np.uint64(0xFFFF)) | ((u64(stream) & np.uint64(0xFFFF)) << np.uint64(16))
+    x, _, _, _ = philox4x32_10(v, ctr1, u64(seq), u64(rnd), seed & 0xFFFFFFFF, seed >> 32)
+    return x
+
+
+def uniform_open(x_u32) -> np.ndarray:
+    """u = ((x >> 9) + 0.5) * 2^-23, strictly inside (0, 1) and exact in fp32."""
+    x = np.asarray(x_u32, dtype=np.uint64) >> np.uint64(9)
+    return (x.astype(np.float64) + 0.5) * 2.0 ** -23
+
+
+def gumbel(seed, rnd, stream, seq, row, v) -> np.ndarray:
+    u = uniform_open(random_u32(seed, rnd, stream, seq, row, v))
+    return -np.log(-np.log(u))
+
+
+STREAM_DRAFT = 0    # Gumbel noise of the draft's token choice
+STREAM_ACCEPT = 1   # acceptance uniforms of the verify
+STREAM_BONUS = 2    # Gumbel noise of the bonus / residual draw
+
+
+# ---------------------------------------------------------------------------
+# Elementary steps
+# ---------------------------------------------------------------------------
+
+def rmsnorm(x, g, eps):
+    """x / sqrt(mean(x^2) + eps) * g over the last axis."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * g
+
+
+def rope(x, pos, theta):
+    """Rotate-half RoPE: pairs (j, j + d/2) turned by pos * theta^(-2j/d).
+
+    x: [..., d]; pos: scalar or array broadcasting against x[..., 0].
+    """
+    d = x.shape[-1]
+    half = d // 2
+    inv = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / d)
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * inv
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def linear(w, x):
+    """Rows of x times w^T, one matrix-vector product per row."""
+    x = np.atleast_2d(x)
+    return np.stack([w @ row for row in x]) if len(x) else np.zeros((0, w.shape[0]))
+
+
+def silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+def sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def logsumexp(s):
+    m = np.max(s)
+    return m + np.log(np.sum(np.exp(s - m)))
+
+
+def softmax(s):
+    e = np.exp(s - np.max(s))
+    return e / np.sum(e)
+
+
+# ---------------------------------------------------------------------------
+# The draft model
+# ---------------------------------------------------------------------------
+
+class OracleDraft:
+    """Draft weights in float64 plus the forward steps of the round.
+
+    ``cfg`` needs the attributes of synthetic.DraftConfig; ``weights`` maps
+    the tensor names of synthetic.weight_shapes to arrays holding exact
+    storage values.
+    """
+
+    def __init__(self, cfg, weights):
+        self.cfg = cfg
+        self.w = {k: np.asarray(v, dtype=np.float64) for k, v in weights.items()}
+        self.st = storage_round(cfg.dtype)
+        self.group = cfg.n_q_heads // cfg.n_kv_heads
+
+    # -- context path (Laguna PR: aux_hidden_norms + fc + hidden_norm, then
+    #    each layer's input_layernorm before a K/V-only projection) ---------
+    def context_hidden(self, feats):
+        """c = hidden_norm(fc([aux_norm_k(f_k)]_k)) for rows of target features."""
+        c = self.cfg
+        f = np.asarray(feats, dtype=np.float64).reshape(-1, c.n_taps, c.target_hidden)
+        u = self.st(rmsnorm(f, self.w["aux_norms"], c.rms_eps)).reshape(len(f), -1)
+        return self.st(rmsnorm(linear(self.w["w_fc"], u), self.w["hidden_norm"], c.rms_eps))
+
+    def context_kv(self, feats, slots):
+        """Per-layer K, V [rows, Hkv, d] of context rows at absolute slots."""
+        c = self.cfg
+        hid = self.context_hidden(feats)
+        slots = np.asarray(slots, dtype=np.float64)
+        qd = c.n_q_heads * c.head_dim
+        kd = c.n_kv_heads * c.head_dim
+        Ks, Vs = [], []
+        for l in range(c.n_layers):
+            p = f"layers.{l}."
+            x = self.st(rmsnorm(hid, self.w[p + "in_norm"], c.rms_eps))
+            wkv = self.w[p + "w_qkv"][qd:qd + 2 * kd]       # K/V rows only
+            kv = linear(wkv, x)
+            k = kv[:, :kd].reshape(-1, c.n_kv_heads, c.head_dim)
+            v = kv[:, kd:].reshape(-1, c.n_kv_heads, c.head_dim)
+            k = rope(rmsnorm(k, self.w[p + "k_norm"], c.rms_eps), slots[:, None], c.rope_theta)
+            Ks.append(self.st(k))
+            Vs.append(self.st(v))
+        return Ks, Vs
+
+    # -- block forward -----------------------------------------------------
+    def visible(self, qpos, kpos, q_row, k_row):
+        """Key visibility for one query: window limit (R7) and the in-block mask."""
+        c = self.cfg
+        ok = np.ones(np.shape(kpos), dtype=bool)
+        if c.window:
+            ok &= (qpos - np.asarray(kpos)) < c.window
+        if k_row is not None and c.causal_block:
+            ok &= np.asarray(k_row) <= q_row
+        return ok
+
+    def attention(self, q, k, v, pos, ck, cv, cpos):
+        """softmax(q.k / sqrt(d)) . v for every block row and query head.
+
+        Keys are the visible context rows followed by the visible block rows;
+        query head hq reads KV head hq // (Hq / Hkv) (grouped-query attention).
+        q [nb, Hq, d]; k, v [nb, Hkv, d]; ck, cv [N, Hkv, d]; pos [nb]; cpos [N].
+        """
+        c = self.cfg
+        nb = len(q)
+        scale = 1.0 / np.sqrt(c.head_dim)
+        o = np.zeros((nb, c.n_q_heads, c.head_dim))
+        for i in range(nb):
+            cvis = self.visible(pos[i], cpos, i, None)
+            bvis = self.visible(pos[i], pos, i, np.arange(nb))
+            for hq in range(c.n_q_heads):
+                hk = hq // self.group
+                keys = np.concatenate([ck[cvis, hk, :], k[bvis, hk, :]])
+                vals = np.concatenate([cv[cvis, hk, :], v[bvis, hk, :]])
+                o[i, hq] = softmax((keys @ q[i, hq]) * scale) @ vals
+        return o
+
+    def block_forward(self, tokens, F, ctx):
+        """Forward of [anchor, mask x n] at positions F..F+n against context.
+
+        ctx: dict with 'pos' [N] and per-layer 'k', 'v' lists of [N, Hkv, d].
+        Returns the final residual h [n+1, H].
+        """
+        c, w, st = self.cfg, self.w, self.st
+        nb = len(tokens)
+        pos = F + np.arange(nb, dtype=np.float64)
+        h = np.stack([w["embed"][int(t)] for t in tokens])
+        qd = c.n_q_heads * c.head_dim
+        kd = c.n_kv_heads * c.head_dim
+        cpos = np.asarray(ctx["pos"], dtype=np.float64)
+        for l in range(c.n_layers):
+            p = f"layers.{l}."
+            x = st(rmsnorm(h, w[p + "in_norm"], c.rms_eps))
+            qkv = linear(w[p + "w_qkv"], x)
+            q = qkv[:, :qd].reshape(nb, c.n_q_heads, c.head_dim)
+            k = qkv[:, qd:qd + kd].reshape(nb, c.n_kv_heads, c.head_dim)
+            v = qkv[:, qd + kd:].reshape(nb, c.n_kv_heads, c.head_dim)
+            q = st(rope(rmsnorm(q, w[p + "q_norm"], c.rms_eps), pos[:, None], c.rope_theta))
+            k = st(rope(rmsnorm(k, w[p + "k_norm"], c.rms_eps), pos[:, None], c.rope_theta))
+            v = st(v)
+            gate = sigmoid(linear(w[p + "w_g"], x)) if c.gated_attention else None
+            o = self.attention(q, k, v, pos, ctx["k"][l], ctx["v"][l], cpos)
+            if gate is not None:
+                o = o * gate[:, :, None]
+            o = st(o.reshape(nb, qd))
+            h = st(h + linear(w[p + "w_o"], o))
+            y = st(rmsnorm(h, w[p + "post_norm"], c.rms_eps))
+            a = st(silu(linear(w[p + "w_gate"], y)) * linear(w[p + "w_up"], y))
+            h = st(h + linear(w[p + "w_down"], a))
+        return h
+
+    def unembed(self, h_rows):
+        """Raw draft logits of block rows (final norm, then the unembedding)."""
+        z = self.st(rmsnorm(h_rows, self.w["final_norm"], self.cfg.rms_eps))
+        return linear(self.w["unembed"], z)
+
+
+# ---------------------------------------------------------------------------
+# Sampling and verification
+# ---------------------------------------------------------------------------
+
+def sample_rows(logits, temperature, seed, rnd, seq):
+    """One batched draw for rows 1..n of a block (dflash.go selectBlock).
+
+    T == 0: argmax (lowest index on ties), q(token) = 1.
+    T > 0: token = argmax_v(l_v/T + Gumbel_v), which is an exact draw from
+    softmax(l/T); q(token) = exp(l_token/T - logsumexp(l/T)).
+    Returns tokens [n], q(token) [n], lse [n] (nan when T == 0).
+    """
+    logits = np.atleast_2d(np.asarray(logits, dtype=np.float64))
+    n, V = logits.shape
+    toks = np.zeros(n, dtype=np.int64)
+    qtok = np.ones(n)
+    lse = np.full(n, np.nan)
+    for i in range(n):
+        if temperature == 0:
+            toks[i] = int(np.argmax(logits[i]))
+            continue
+        s = logits[i] / temperature
+        lse[i] = logsumexp(s)
+        g = gumbel(seed, rnd, STREAM_DRAFT, seq, i + 1, np.arange(V))
+        toks[i] = int(np.argmax(s + g))
+        qtok[i] = np.exp(s[toks[i]] - lse[i])
+    return toks, qtok, lse
+
+
+def proposal_distribution(draft_logits_row, draft_temperature, proposed_token):
+    """q of one block row: softmax(l/T) at T > 0, one-hot of the proposal at T == 0."""
+    if draft_temperature == 0:
+        q = np.zeros(len(draft_logits_row))
+        q[int(proposed_token)] = 1.0
+        return q
+    return softmax(np.asarray(draft_logits_row, dtype=np.float64) / draft_temperature)
+
+
+def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_temperature,
+           temperature, seed, rnd, seq):
+    """Accepted prefix length a and bonus token b.
+
+    target_logits [n+1, V]: row r scores the token after [current, d_1..d_r].
+    draft_tokens [n]: the tokens under test (normally the proposal).
+    draft_logits [n, V], proposed_tokens [n], draft_temperature: what the last
+    propose drew from; q_i is that distribution.
+
+    T == 0: accept while argmax(target row i-1) == d_i; b = argmax(row a).
+    T > 0: accept d_i iff r_i * q_i(d_i) < p_i(d_i) (that is r_i < p/q), with
+    p_i = softmax(target row i-1 / T); at the first rejection draw b from
+    max(0, p_i - q_i) (from p_i if that is all zero, R15); if all n pass,
+    draw b from p of row n.
+    """
+    tl = np.atleast_2d(np.asarray(target_logits, dtype=np.float64))
+    n = len(draft_tokens)
+    V = tl.shape[1]
+    if temperature == 0:
+        a = 0
+        while a < n and int(np.argmax(tl[a])) == int(draft_tokens[a]):
+            a += 1
+        return a, int(np.argmax(tl[a]))
+    for i in range(1, n + 1):
+        p = softmax(tl[i - 1] / temperature)
+        q = proposal_distribution(draft_logits[i - 1], draft_temperature, proposed_tokens[i - 1])
+        d = int(draft_tokens[i - 1])
+        r = uniform_open(random_u32(seed, rnd, STREAM_ACCEPT, seq, i, 0))
+        if r * q[d] < p[d]:
+            continue
+        res = np.maximum(p - q, 0.0)
+        if not np.sum(res) > 0:
+            res = p
+        with np.errstate(divide="ignore"):
+            score = np.log(res) + gumbel(seed, rnd, STREAM_BONUS, seq, i, np.arange(V))
+        return i - 1, int(np.argmax(score))
+    p = softmax(tl[n] / temperature)
+    with np.errstate(divide="ignore"):
+        score = np.log(p) + gumbel(seed, rnd, STREAM_BONUS, seq, n + 1, np.arange(V))
+    return n, int(np.argmax(score))
+
+
+# ---------------------------------------------------------------------------
+# The drafter session (dflash.go: open / committed / takePending /
+# commitBlock / flush / propose / selectBlock)
+# ---------------------------------------------------------------------------
+
+class OracleSession:
+    """One request's drafting state.
+
+    F (ctxOffset) is the slot after the last feature row written to the
+    cache; P rows are buffered past it, so F + P is the slot after the last
+    reported token.  The cache maps slot -> (K [L,Hkv,d], V [L,Hkv,d]).
+    """
+
+    def __init__(self, draft: OracleDraft, restored_offset: int = 0, seq: int = 0,
+                 restored_cache=None):
+        self.draft = draft
+        self.cfg = draft.cfg
+        self.F = int(restored_offset)
+        self.pending = []
+        self.P = 0
+        self.block_outstanding = False
+        self.block_kv = None           # the outstanding block's K/V (never persisted)
+        self.cache = dict(restored_cache or {})
+        self.seq = seq
+        self.last = None               # what the last propose drew from
+        self.stats = dict(rounds=0, proposed=0, accepted=0)
+
+    # dflash.go draftLimit
+    @property
+    def draft_limit(self) -> int:
+        return self.cfg.block_size - 1
+
+    def committed(self, features, position: int):
+        """Append the rows of a committed run that the session does not hold yet."""
+        features = np.atleast_2d(features)
+        n = len(features)
+        start = self.F + self.P - int(position)
+        if start < 0:
+            raise ContextGap(f"committed run at {position} leaves a context gap at {self.F + self.P}")
+        if start < n:
+            self.pending.append(np.asarray(features[start:n]))
+            self.P += n - start
+            if self.P >= PENDING_FLUSH_TOKENS:
+                self.flush()
+
+    def take_pending(self):
+        if not self.pending:
+            return None, self.F
+        rows = np.concatenate(self.pending)
+        first = self.F
+        self.pending = []
+        self.F += self.P
+        self.P = 0
+        return rows, first
+
+    def commit_block(self):
+        """Rewind the outstanding block: the cache keeps only context rows."""
+        if not self.block_outstanding:
+            return
+        self.block_kv = None
+        self.block_outstanding = False
+
+    def _write_context(self, rows, first):
+        """Context-only forward of rows at slots first.. (drops rows no future
+        query can see when the draft has a window: Laguna PR, window drop)."""
+        if rows is None or len(rows) == 0:
+            return
+        slots = first + np.arange(len(rows))
+        if self.cfg.window:
+            keep = slots > self.F - self.cfg.window
+            rows, slots = rows[keep], slots[keep]
+            for s in [s for s in self.cache if s <= self.F - self.cfg.window]:
+                del self.cache[s]
+            if len(rows) == 0:
+                return
+        Ks, Vs = self.draft.context_kv(rows, slots)
+        for j, s in enumerate(slots):
+            self.cache[int(s)] = (np.stack([K[j] for K in Ks]), np.stack([V[j] for V in Vs]))
+
+    def flush(self):
+        self.commit_block()
+        if not self.pending:
+            return
+        rows, first = self.take_pending()
+        self._write_context(rows, first)
+
+    def context(self):
+        """Cached context rows below F as arrays for the attention."""
+        c = self.cfg
+        slots = sorted(s for s in self.cache if s < self.F)
+        L = c.n_layers
+        if not slots:
+            z = np.zeros((0, c.n_kv_heads, c.head_dim))
+            return dict(pos=np.zeros(0), k=[z] * L, v=[z] * L)
+        K = np.stack([self.cache[s][0] for s in slots])   # [N, L, Hkv, d]
+        V = np.stack([self.cache[s][1] for s in slots])
+        return dict(pos=np.asarray(slots, dtype=np.float64),
+                    k=[K[:, l] for l in range(L)], v=[V[:, l] for l in range(L)])
+
+    def propose(self, current: int, max_tokens: int, temperature: float = 0.0,
+                seed: int = 0, rnd: int = 0):
+        """Draft n = min(max_tokens, B_s - 1) tokens after `current`.
+
+        Returns None (the pages' nil) when n <= 0 or nothing has been
+        committed; otherwise dict(tokens, q, logits, lse, hidden).
+        """
+        c = self.cfg
+        n = min(int(max_tokens), c.block_size - 1)
+        if n <= 0 or self.F + self.P == 0:
+            return None
+        self.commit_block()
+        rows, first = self.take_pending()
+        self._write_context(rows, first)
+        self.block_outstanding = True
+        tokens = [int(current)] + [c.mask_token] * n
+        h = self.draft.block_forward(tokens, self.F, self.context())
+        logits = self.draft.unembed(h[1:])          # the anchor row is unused
+        toks, q, lse = sample_rows(logits, temperature, seed, rnd, self.seq)
+        self.last = dict(tokens=toks, logits=logits, temperature=temperature)
+        self.stats["rounds"] += 1
+        self.stats["proposed"] += n
+        return dict(tokens=toks, q=q, logits=logits, lse=lse, hidden=h, n=n)
+
+    def verify(self, target_logits, draft_tokens, temperature, seed=0, rnd=0):
+        if self.last is None:
+            raise RuntimeError("verify without a proposal")
+        a, b = verify(target_logits, draft_tokens, self.last["logits"], self.last["tokens"],
+                      self.last["temperature"], temperature, seed, rnd, self.seq)
+        self.stats["accepted"] += a
+        return a, b
+
+    def close(self):
+        self.flush()
