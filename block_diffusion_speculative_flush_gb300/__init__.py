@@ -1,0 +1,206 @@
+"""Python binding of the GB300-native DFlash draft round (libdflash.so).
+
+Each function has the name of the C entry point it marshals and does nothing
+else: tensors become device pointers, lists of sessions become host arrays,
+negative status codes become DFlashError.  Every step of the round runs in
+the CUDA library; if the library is missing, importing this package fails.
+
+PyTorch is used only for device memory (the tensors passed in) and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _abi
+from ._abi import (DFLASH_DTYPE_BF16, DFLASH_DTYPE_F32, DFLASH_ERR_CAPACITY, DFLASH_ERR_CONTEXT_GAP,
+                   DFLASH_ERR_CUDA, DFLASH_ERR_DEVICE, DFLASH_ERR_INVALID_ARG, DFLASH_ERR_OOM, DFLASH_ERR_SHAPE,
+                   DFLASH_ERR_STATE, DFLASH_FLAG_SIMT_GEMM, DFLASH_OK, DFLASH_PENDING_FLUSH_TOKENS)
+
+lib = _abi.load()
+
+__all__ = [
+    "DFlashError", "Model", "Session", "lib", "torch_dtype",
+    "dflash_model_create", "dflash_model_destroy", "dflash_draft_limit", "dflash_device_status", "dflash_open",
+    "dflash_committed", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
+    "dflash_close", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
+    "dflash_version", "dflash_last_error",
+]
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"dflash status {status}: {message}")
+        self.status = status
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise DFlashError(rc, lib.dflash_last_error().decode(errors="replace"))
+    return rc
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def torch_dtype(cfg) -> torch.dtype:
+    return torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+
+
+class Model:
+    """Handle of a dflash_model; keeps the weight tensors alive."""
+
+    def __init__(self, handle: int, cfg, tensors: dict, layer_structs):
+        self.handle = handle
+        self.cfg = cfg
+        self._tensors = tensors
+        self._layers = layer_structs
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            lib.dflash_model_destroy(self.handle)
+            self.handle = None
+
+
+class Session:
+    def __init__(self, handle: int, model: Model):
+        self.handle = handle
+        self.model = model
+
+
+def _sessions(sessions):
+    if isinstance(sessions, Session):
+        sessions = [sessions]
+    arr = (C.c_void_p * len(sessions))(*[s.handle for s in sessions])
+    return arr, len(sessions)
+
+
+def dflash_version() -> int:
+    return lib.dflash_version()
+
+
+def dflash_last_error() -> str:
+    return lib.dflash_last_error().decode(errors="replace")
+
+
+def dflash_model_create(cfg, weights: dict, flags: int = 0) -> Model:
+    """cfg: an object with the fields of synthetic.DraftConfig; weights: name ->
+    CUDA tensor in the storage type (names as synthetic.weight_shapes)."""
+    c = _abi.dflash_config(
+        dtype=DFLASH_DTYPE_BF16 if cfg.dtype == "bf16" else DFLASH_DTYPE_F32, n_taps=cfg.n_taps,
+        target_hidden=cfg.target_hidden, hidden=cfg.hidden, n_layers=cfg.n_layers, n_q_heads=cfg.n_q_heads,
+        n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, intermediate=cfg.intermediate, vocab=cfg.vocab,
+        block_size=cfg.block_size, mask_token=cfg.mask_token, window=cfg.window,
+        causal_block=int(cfg.causal_block), gated_attention=int(cfg.gated_attention), flags=flags,
+        rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps)
+    t = {k: v.contiguous() for k, v in weights.items()}
+    layers = (_abi.dflash_layer_weights * cfg.n_layers)()
+    for l in range(cfg.n_layers):
+        p = f"layers.{l}."
+        g = t.get(p + "w_g")
+        layers[l] = _abi.dflash_layer_weights(
+            _ptr(t[p + "in_norm"]), _ptr(t[p + "w_qkv"]), _ptr(t[p + "q_norm"]), _ptr(t[p + "k_norm"]), _ptr(g),
+            _ptr(t[p + "w_o"]), _ptr(t[p + "post_norm"]), _ptr(t[p + "w_gate"]), _ptr(t[p + "w_up"]),
+            _ptr(t[p + "w_down"]))
+    w = _abi.dflash_weights(_ptr(t["aux_norms"]), _ptr(t["w_fc"]), _ptr(t["hidden_norm"]), _ptr(t["final_norm"]),
+                            _ptr(t["embed"]), _ptr(t["unembed"]), layers)
+    out = C.c_void_p()
+    _check(lib.dflash_model_create(C.byref(c), C.byref(w), C.byref(out)))
+    return Model(out.value, cfg, t, layers)
+
+
+def dflash_model_destroy(model: Model) -> None:
+    if model.handle:
+        _check(lib.dflash_model_destroy(model.handle))
+        model.handle = None
+
+
+def dflash_draft_limit(model: Model) -> int:
+    return _check(lib.dflash_draft_limit(model.handle))
+
+
+def dflash_device_status(model: Model) -> None:
+    _check(lib.dflash_device_status(model.handle))
+
+
+def dflash_open(model: Model, restored_offset: int = 0, max_ctx: int = 4096, stream=None) -> Session:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    out = C.c_void_p()
+    _check(lib.dflash_open(model.handle, restored_offset, max_ctx, C.c_void_p(stream.cuda_stream), C.byref(out)))
+    return Session(out.value, model)
+
+
+def dflash_committed(session: Session, features: torch.Tensor, position: int) -> None:
+    """features: CUDA tensor [n_rows, K*H_t] (row stride from the tensor)."""
+    if features.dim() != 2 or features.stride(1) != 1:
+        raise ValueError("features must be 2-D with unit column stride")
+    _check(lib.dflash_committed(session.handle, _ptr(features), features.stride(0), features.shape[0], position))
+
+
+def dflash_flush(sessions) -> None:
+    arr, n = _sessions(sessions)
+    _check(lib.dflash_flush(arr, n))
+
+
+def dflash_settle(session: Session) -> None:
+    _check(lib.dflash_settle(session.handle))
+
+
+def dflash_commit_block(sessions) -> None:
+    arr, n = _sessions(sessions)
+    _check(lib.dflash_commit_block(arr, n))
+
+
+def dflash_propose(sessions, current: torch.Tensor, max_tokens: int, temperature: float, seed: int, rnd: int,
+                   out_tokens: torch.Tensor, out_q: torch.Tensor, out_logits: torch.Tensor | None = None) -> list:
+    """Returns out_n per session (0 where the pages return nil)."""
+    arr, n = _sessions(sessions)
+    out_n = (C.c_int32 * n)()
+    _check(lib.dflash_propose(arr, n, _ptr(current), max_tokens, float(temperature), seed, rnd, _ptr(out_tokens),
+                              _ptr(out_q), _ptr(out_logits), out_n))
+    return list(out_n)
+
+
+def dflash_verify(sessions, target_logits: torch.Tensor, draft_tokens: torch.Tensor, n: int, temperature: float,
+                  seed: int, rnd: int, out_accept: torch.Tensor, out_bonus: torch.Tensor) -> None:
+    arr, b = _sessions(sessions)
+    dt = DFLASH_DTYPE_BF16 if target_logits.dtype == torch.bfloat16 else DFLASH_DTYPE_F32
+    if target_logits.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("target logits must be fp32 or bf16")
+    _check(lib.dflash_verify(arr, b, _ptr(target_logits), dt, _ptr(draft_tokens), n, float(temperature), seed, rnd,
+                             _ptr(out_accept), _ptr(out_bonus)))
+
+
+def dflash_close(session: Session) -> None:
+    if session.handle:
+        _check(lib.dflash_close(session.handle))
+        session.handle = None
+
+
+def dflash_stats(session: Session) -> dict:
+    c = _abi.dflash_counters()
+    _check(lib.dflash_stats(session.handle, C.byref(c)))
+    return {k: getattr(c, k) for k, _ in c._fields_}
+
+
+def dflash_session_state(session: Session) -> tuple:
+    F, P, B = C.c_int64(), C.c_int32(), C.c_int32()
+    _check(lib.dflash_session_state(session.handle, C.byref(F), C.byref(P), C.byref(B)))
+    return F.value, P.value, bool(B.value)
+
+
+def dflash_kv_export(session: Session, layer: int, first_slot: int, n_rows: int, k_out: torch.Tensor,
+                     v_out: torch.Tensor) -> None:
+    _check(lib.dflash_kv_export(session.handle, layer, first_slot, n_rows, _ptr(k_out), _ptr(v_out)))
+
+
+def dflash_kv_import(session: Session, layer: int, first_slot: int, n_rows: int, k_in: torch.Tensor,
+                     v_in: torch.Tensor) -> None:
+    _check(lib.dflash_kv_import(session.handle, layer, first_slot, n_rows, _ptr(k_in), _ptr(v_in)))

@@ -1,0 +1,125 @@
+// Device helpers shared by the DFlash kernels: storage conversions, warp and
+// block reductions, the counter-based random numbers the round draws, and the
+// RMSNorm row statistic.  Written for sm_103a.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dfl {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------------------
+// storage <-> fp32
+// ---------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sum over the whole block; every thread gets the result.  `red` must hold
+// at least blockDim.x / 32 floats.  Summation order is fixed by the block
+// shape, never by the data or by other rows.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int i = 0; i < nw; ++i) s += red[i];
+  return s;
+}
+
+// (value, index) argmax with the lowest index winning ties.
+struct ArgMax {
+  float v;
+  int32_t i;
+};
+__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ArgMax b;
+    b.v = __shfl_xor_sync(0xffffffffu, a.v, o);
+    b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+    a = better(a, b);
+  }
+  return a;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10: Salmon, Moraes, Dror & Shaw, "Parallel Random Numbers: As
+// Easy as 1, 2, 3" (SC'11).  Ten rounds of two 32x32->64 multiplies by the
+// paper's constants; the high halves are xored with the other two counter
+// words and the key, the key advancing by the two Weyl constants between
+// rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k.x += 0x9E3779B9u;
+      k.y += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+  }
+  return c;
+}
+
+enum : uint32_t { kStreamDraft = 0, kStreamAccept = 1, kStreamBonus = 2 };
+
+// Word 0 of Philox at counter (v, row | stream << 16, seq, round), key = seed.
+__device__ __forceinline__ uint32_t rand_u32(uint64_t seed, uint32_t rnd, uint32_t stream,
+                                             uint32_t seq, uint32_t row, uint32_t v) {
+  const uint4 c = make_uint4(v, (row & 0xFFFFu) | (stream << 16), seq, rnd);
+  const uint2 k = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+  return philox4x32_10(c, k).x;
+}
+
+// u = ((x >> 9) + 0.5) * 2^-23: strictly inside (0, 1) and exact in fp32.
+__device__ __forceinline__ float uniform_open(uint32_t x) {
+  return ((float)(x >> 9) + 0.5f) * 1.1920928955078125e-07f;
+}
+
+__device__ __forceinline__ float gumbel(uint64_t seed, uint32_t rnd, uint32_t stream, uint32_t seq,
+                                        uint32_t row, uint32_t v) {
+  const float u = uniform_open(rand_u32(seed, rnd, stream, seq, row, v));
+  return -logf(-logf(u));
+}
+
+// ---------------------------------------------------------------------------
+// Bounded waits: a spin that runs past its limit records where it gave up in
+// a device error word that the host reads after the call.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+}  // namespace dfl

@@ -1,0 +1,903 @@
+// Host runtime behind the C ABI of include/dflash.h: model validation, the
+// drafter session state machine, workspace management and the launch
+// sequence of one batched flush / propose / verify.
+//
+// The session cursors follow ollama's mlxrunner/dflash.go (committed,
+// takePending, commitBlock, flush, propose): ctxOffset F is the slot after
+// the last feature row written; P rows are held past it; F + P is the slot
+// after the last reported token.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "dflash.h"
+#include "gemm_tc.h"
+#include "kernels.h"
+
+using namespace dfl;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CU_TRY(expr)                                                                              \
+  do {                                                                                            \
+    cudaError_t e_ = (expr);                                                                      \
+    if (e_ != cudaSuccess)                                                                        \
+      return fail(e_ == cudaErrorMemoryAllocation ? DFLASH_ERR_OOM : DFLASH_ERR_CUDA, "%s: %s (%s:%d)", #expr, \
+                  cudaGetErrorString(e_), __FILE__, __LINE__);                                    \
+  } while (0)
+
+#define ST_TRY(expr)        \
+  do {                      \
+    int s_ = (expr);        \
+    if (s_ != DFLASH_OK) return s_; \
+  } while (0)
+
+inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// A device buffer that only grows.  Growing waits for the stream so that no
+// queued kernel still reads the old allocation.
+struct Buf {
+  void* p = nullptr;
+  size_t cap = 0;
+  int ensure(size_t bytes, cudaStream_t st) {
+    if (bytes <= cap) return DFLASH_OK;
+    if (p) {
+      CU_TRY(cudaStreamSynchronize(st));
+      CU_TRY(cudaFree(p));
+      p = nullptr;
+      cap = 0;
+    }
+    size_t want = std::max<size_t>(bytes, 4096);
+    want = (size_t)align_up((int64_t)want + want / 4, 256);
+    CU_TRY(cudaMalloc(&p, want));
+    CU_TRY(cudaMemsetAsync(p, 0, want, st));
+    cap = want;
+    return DFLASH_OK;
+  }
+  void release() {
+    if (p) cudaFree(p);
+    p = nullptr;
+    cap = 0;
+  }
+  template <typename T> T* as() const { return (T*)p; }
+};
+
+// Packs the small per-call tables into one host block, uploaded with a single
+// copy.  The host side is a ring of pinned slots guarded by events so that a
+// slot is never rewritten while its copy is still queued.
+struct TablePack {
+  std::vector<char> host;
+  size_t add(const void* src, size_t bytes) {
+    const size_t off = (size_t)align_up((int64_t)host.size(), 16);
+    host.resize(off + bytes);
+    if (bytes) memcpy(host.data() + off, src, bytes);
+    return off;
+  }
+  template <typename T> size_t add(const std::vector<T>& v) { return add(v.data(), v.size() * sizeof(T)); }
+};
+
+struct HostRing {
+  static constexpr int kSlots = 8;
+  char* slot[kSlots] = {};
+  size_t cap[kSlots] = {};
+  cudaEvent_t ev[kSlots] = {};
+  int next = 0;
+  int upload(const TablePack& t, Buf& dev, cudaStream_t st) {
+    const size_t bytes = std::max<size_t>(t.host.size(), 16);
+    ST_TRY(dev.ensure(bytes, st));
+    const int i = next;
+    next = (next + 1) % kSlots;
+    if (!ev[i]) CU_TRY(cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming));
+    CU_TRY(cudaEventSynchronize(ev[i]));
+    if (cap[i] < bytes) {
+      if (slot[i]) cudaFreeHost(slot[i]);
+      slot[i] = nullptr;
+      const size_t want = (size_t)align_up((int64_t)bytes * 2, 4096);
+      CU_TRY(cudaMallocHost((void**)&slot[i], want));
+      cap[i] = want;
+    }
+    memcpy(slot[i], t.host.data(), t.host.size());
+    CU_TRY(cudaMemcpyAsync(dev.p, slot[i], t.host.size(), cudaMemcpyHostToDevice, st));
+    CU_TRY(cudaEventRecord(ev[i], st));
+    return DFLASH_OK;
+  }
+  void release() {
+    for (int i = 0; i < kSlots; ++i) {
+      if (ev[i]) {
+        cudaEventSynchronize(ev[i]);
+        cudaEventDestroy(ev[i]);
+      }
+      if (slot[i]) cudaFreeHost(slot[i]);
+      ev[i] = nullptr;
+      slot[i] = nullptr;
+    }
+  }
+};
+
+struct LayerW {
+  const void *in_norm, *w_qkv, *q_norm, *k_norm, *w_g, *w_o, *post_norm, *w_gate, *w_up, *w_down;
+  void* w_qkvg = nullptr;  // owned: [w_qkv ; w_g] rows, one product for q, k, v and the gate
+};
+
+}  // namespace
+
+struct dflash_model {
+  dflash_config cfg{};
+  DT dt = DT::F32;
+  size_t esz = 4;
+  const void *aux_norms, *w_fc, *hidden_norm, *final_norm, *embed, *unembed;
+  std::vector<LayerW> layers;
+  int qkv_rows = 0;   // (Hq + 2 Hkv) d
+  int qkv_cols = 0;   // qkv_rows (+ Hq for the gate)
+  int num_sms = 0;
+  bool use_tc = false;
+  int32_t* d_err = nullptr;
+  TcContext* tc = nullptr;
+  // workspace
+  Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart;
+  HostRing ring;
+};
+
+struct dflash_session {
+  dflash_model* m = nullptr;
+  cudaStream_t stream = nullptr;
+  int64_t F = 0;      // ctxOffset
+  int32_t P = 0;      // pendingCount
+  bool block_outstanding = false;
+  int64_t max_ctx = 0, cap = 0;
+  void* kv = nullptr;       // [L][2][Hkv][cap][d]
+  void* pending = nullptr;  // [PENDING_FLUSH_TOKENS][K*H_t]
+  float* plogits = nullptr; // [B_s-1][V] logits of the last proposal
+  float* plse = nullptr;    // [B_s-1]
+  int32_t* ptok = nullptr;  // [B_s-1]
+  long long* d_accepted = nullptr;
+  bool has_prop = false;
+  int last_n = 0;
+  float last_T = 0.f;
+  int64_t rounds = 0, proposed = 0, flushes = 0, flushed_rows = 0;
+};
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+int check_config(const dflash_config& c) {
+  if (c.dtype != DFLASH_DTYPE_F32 && c.dtype != DFLASH_DTYPE_BF16) return fail(DFLASH_ERR_INVALID_ARG, "dtype %d", c.dtype);
+  if (c.n_taps < 1 || c.target_hidden < 1 || c.hidden < 1 || c.n_layers < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1 ||
+      c.intermediate < 1 || c.vocab < 2)
+    return fail(DFLASH_ERR_SHAPE, "non-positive dimension in config");
+  if (c.block_size < 2 || c.block_size > 512) return fail(DFLASH_ERR_SHAPE, "block_size %d outside 2..512", c.block_size);
+  if (c.window != 0 && (c.window < 2 || c.window > (1 << 20)))
+    return fail(DFLASH_ERR_SHAPE, "window %d outside 2..2^20", c.window);
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(DFLASH_ERR_SHAPE, "head_dim %d (64 or 128 supported)", c.head_dim);
+  if (c.n_q_heads % c.n_kv_heads) return fail(DFLASH_ERR_SHAPE, "n_q_heads %d not a multiple of n_kv_heads %d", c.n_q_heads, c.n_kv_heads);
+  if (c.n_q_heads / c.n_kv_heads * c.block_size > 512)
+    return fail(DFLASH_ERR_SHAPE, "query rows per KV head (group x block) above 512");
+  if (c.mask_token < 0 || c.mask_token >= c.vocab) return fail(DFLASH_ERR_SHAPE, "mask_token %d outside vocab", c.mask_token);
+  if (c.causal_block != 0 && c.causal_block != 1) return fail(DFLASH_ERR_INVALID_ARG, "causal_block must be 0 or 1");
+  if (c.gated_attention != 0 && c.gated_attention != 1) return fail(DFLASH_ERR_INVALID_ARG, "gated_attention must be 0 or 1");
+  if (!(c.rope_theta > 1.f) || !(c.rms_eps >= 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "rope_theta / rms_eps");
+  if (c.dtype == DFLASH_DTYPE_BF16) {
+    const int w[] = {c.target_hidden, c.hidden, c.intermediate, c.n_q_heads * c.head_dim};
+    for (int x : w)
+      if (x % 64) return fail(DFLASH_ERR_SHAPE, "bf16 widths must be multiples of 64 (got %d)", x);
+  }
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// matrix products: Y[M][N] (fp32) = X[M][K] . W[N][K]^T
+// ---------------------------------------------------------------------------
+int gemm(dflash_model* m, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy, int M, int N,
+         int K, cudaStream_t st) {
+  if (M <= 0) return DFLASH_OK;
+  if (m->use_tc) {
+    const int rc = tc_gemm(m->tc, X, ldx, W, ldw, Y, ldy, M, N, K, st);
+    if (rc) return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
+  } else {
+    launch_gemm_simt(m->dt, X, ldx, W, ldw, Y, ldy, M, N, K, st);
+  }
+  return DFLASH_OK;
+}
+
+int launch_check(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// one batched forward: context rows (flush) and optionally block rows
+// ---------------------------------------------------------------------------
+struct CtxRow {
+  const void* src;  // feature row
+  int32_t sess;     // compact session index
+  int64_t pos;      // slot
+};
+
+struct Forward {
+  std::vector<dflash_session*> sess;  // compact sessions
+  std::vector<CtxRow> ctx;
+  // block part
+  int n = 0;                          // block rows are n + 1 per session (0: flush only)
+  const int32_t* current = nullptr;   // device [batch]
+  std::vector<int32_t> sess_map;      // compact -> caller index
+  float temperature = 0.f;
+  uint64_t seed = 0;
+  uint64_t rnd = 0;
+  int32_t* out_tokens = nullptr;
+  float* out_q = nullptr;
+  float* out_logits = nullptr;
+};
+
+int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
+  const dflash_config& c = m->cfg;
+  const int Bc = (int)fw.sess.size();
+  const int Mc = (int)fw.ctx.size();
+  const bool block = fw.n > 0;
+  const int nrows = fw.n + 1;
+  const int Mb = block ? Bc * nrows : 0;
+  const int M = Mc + Mb;
+  if (M == 0) return DFLASH_OK;
+  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, I = c.intermediate, V = c.vocab;
+  const int KHt = c.n_taps * c.target_hidden;
+  const size_t es = m->esz;
+
+  // ---- per-call tables ---------------------------------------------------
+  TablePack tp;
+  std::vector<const void*> rowsrc(Mc);
+  std::vector<RowMeta> meta(M);
+  for (int r = 0; r < Mc; ++r) {
+    rowsrc[r] = fw.ctx[r].src;
+    meta[r] = RowMeta{fw.ctx[r].sess, -1, fw.ctx[r].pos};
+  }
+  std::vector<void*> kvb(Bc);
+  std::vector<int64_t> capv(Bc), front(Bc);
+  std::vector<int32_t> seqv(Bc);
+  for (int j = 0; j < Bc; ++j) {
+    kvb[j] = fw.sess[j]->kv;
+    capv[j] = fw.sess[j]->cap;
+    front[j] = fw.sess[j]->F;
+    seqv[j] = block ? fw.sess_map[j] : j;
+  }
+  for (int j = 0; j < Bc && block; ++j)
+    for (int i = 0; i < nrows; ++i) meta[Mc + j * nrows + i] = RowMeta{j, j * nrows + i, fw.sess[j]->F + i};
+  // attention work items: split every (session, KV head) key range in chunks
+  std::vector<AttnItem> items;
+  std::vector<int32_t> ifirst(Bc), icount(Bc);
+  if (block) {
+    int64_t total = 0;
+    std::vector<int64_t> k0v(Bc), k1v(Bc);
+    for (int j = 0; j < Bc; ++j) {
+      const int64_t F = fw.sess[j]->F;
+      k0v[j] = c.window ? std::max<int64_t>(0, F - c.window + 1) : 0;
+      k1v[j] = F + nrows;
+      total += (k1v[j] - k0v[j]) * Hkv;
+    }
+    int64_t chunk = align_up(std::max<int64_t>(1, total / std::max(1, 2 * m->num_sms)), 64);
+    chunk = std::min<int64_t>(std::max<int64_t>(chunk, 64), 4096);
+    for (int j = 0; j < Bc; ++j) {
+      const int S = (int)((k1v[j] - k0v[j] + chunk - 1) / chunk);
+      ifirst[j] = (int32_t)items.size();
+      icount[j] = S;
+      for (int h = 0; h < Hkv; ++h)
+        for (int s = 0; s < S; ++s)
+          items.push_back(AttnItem{j, h, k0v[j] + s * chunk, std::min(k1v[j], k0v[j] + (s + 1) * chunk)});
+    }
+  }
+  const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
+               o_front = tp.add(front), o_seq = tp.add(seqv), o_items = tp.add(items), o_ifirst = tp.add(ifirst),
+               o_icount = tp.add(icount), o_map = tp.add(fw.sess_map);
+  ST_TRY(m->ring.upload(tp, m->tables, st));
+  char* tb = m->tables.as<char>();
+  SessTables tabs{(void* const*)(tb + o_kv), (const int64_t*)(tb + o_cap), (const int64_t*)(tb + o_front),
+                  (const int32_t*)(tb + o_seq)};
+  const RowMeta* dmeta = (const RowMeta*)(tb + o_meta);
+
+  // ---- buffers -----------------------------------------------------------
+  ST_TRY(m->x.ensure((size_t)M * H * es, st));
+  ST_TRY(m->qkv.ensure((size_t)M * m->qkv_cols * 4, st));
+  ST_TRY(m->rope.ensure((size_t)M * (d / 2) * sizeof(float2), st));
+  if (Mc) {
+    ST_TRY(m->u.ensure((size_t)Mc * KHt * es, st));
+    ST_TRY(m->fcout.ensure((size_t)Mc * H * 4, st));
+    ST_TRY(m->c.ensure((size_t)Mc * H * es, st));
+  }
+  if (block) {
+    ST_TRY(m->h.ensure((size_t)Mb * H * es, st));
+    ST_TRY(m->Q.ensure((size_t)Mb * Hq * d * es, st));
+    ST_TRY(m->G.ensure((size_t)Mb * Hq * 4, st));
+    ST_TRY(m->O.ensure((size_t)Mb * Hq * d * es, st));
+    ST_TRY(m->tmp.ensure((size_t)Mb * std::max(H, 2 * I) * 4, st));
+    ST_TRY(m->y.ensure((size_t)Mb * H * es, st));
+    ST_TRY(m->a.ensure((size_t)Mb * I * es, st));
+    ST_TRY(m->z.ensure((size_t)Bc * fw.n * H * es, st));
+    const int R = nrows * (Hq / Hkv);
+    ST_TRY(m->apart.ensure(std::max<size_t>(items.size(), 1) * R * (d + 2) * 4, st));
+  }
+
+  // ---- context path: aux_hidden_norms -> fc -> hidden_norm ----------------
+  if (Mc) {
+    launch_tap_norm(m->dt, (const void* const*)(tb + o_rowsrc), Mc, m->aux_norms, m->u.p, c.n_taps, c.target_hidden,
+                    c.rms_eps, st);
+    ST_TRY(gemm(m, m->u.p, KHt, m->w_fc, KHt, m->fcout.as<float>(), H, Mc, H, KHt, st));
+    launch_rmsnorm(m->dt, true, m->fcout.p, Mc, nullptr, H, m->hidden_norm, m->c.p, H, Mc, H, Mc, 0, 0, c.rms_eps, st);
+  }
+  if (block)
+    launch_embed(m->dt, m->embed, fw.current, (const int32_t*)(tb + o_map), c.mask_token, V, Bc, nrows, H, m->h.p,
+                 m->d_err, st);
+  launch_rope_table(dmeta, M, d, c.rope_theta, m->rope.as<float2>(), st);
+  ST_TRY(launch_check("context path"));
+
+  AttnParams ap{Hq, Hkv, d, nrows, c.window, c.causal_block, c.n_layers, 0, 1.f / std::sqrt((float)d)};
+  const int qd = Hq * d, kd = Hkv * d;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& w = m->layers[l];
+    // input_layernorm over [context rows ; block rows]
+    launch_rmsnorm(m->dt, false, m->c.p, Mc, m->h.p, H, w.in_norm, m->x.p, H, M, H, M, 0, 0, c.rms_eps, st);
+    if (block) {
+      const void* wq = w.w_qkvg ? w.w_qkvg : w.w_qkv;
+      ST_TRY(gemm(m, m->x.p, H, wq, H, m->qkv.as<float>(), m->qkv_cols, M, m->qkv_cols, H, st));
+    } else {
+      // context-only forward: the K/V rows of the fused projection only
+      const char* wkv = (const char*)w.w_qkv + (size_t)qd * H * es;
+      ST_TRY(gemm(m, m->x.p, H, wkv, H, m->qkv.as<float>() + qd, m->qkv_cols, M, 2 * kd, H, st));
+    }
+    launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, m->rope.as<float2>(), w.q_norm, w.k_norm, Hq,
+                    Hkv, d, c.gated_attention, c.rms_eps, tabs, c.n_layers, l, m->Q.p, m->G.as<float>(), st);
+    ST_TRY(launch_check("qkv"));
+    if (!block) continue;
+    ap.layer = l;
+    launch_attention_simt(m->dt, m->Q.p, (const AttnItem*)(tb + o_items), (int)items.size(), tabs, ap,
+                          m->apart.as<float>(), st);
+    launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
+                             (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
+                             m->O.p, st);
+    ST_TRY(launch_check("attention"));
+    ST_TRY(gemm(m, m->O.p, qd, w.w_o, qd, m->tmp.as<float>(), H, Mb, H, qd, st));
+    launch_residual(m->dt, m->h.p, m->tmp.as<float>(), H, Mb, H, st);
+    launch_rmsnorm(m->dt, false, m->h.p, Mb, nullptr, H, w.post_norm, m->y.p, H, Mb, H, Mb, 0, 0, c.rms_eps, st);
+    ST_TRY(gemm(m, m->y.p, H, w.w_gate, H, m->tmp.as<float>(), 2 * I, Mb, I, H, st));
+    ST_TRY(gemm(m, m->y.p, H, w.w_up, H, m->tmp.as<float>() + I, 2 * I, Mb, I, H, st));
+    launch_swiglu(m->dt, m->tmp.as<float>(), 2 * I, Mb, I, I, m->a.p, st);
+    ST_TRY(gemm(m, m->a.p, I, w.w_down, I, m->tmp.as<float>(), H, Mb, H, I, st));
+    launch_residual(m->dt, m->h.p, m->tmp.as<float>(), H, Mb, H, st);
+    ST_TRY(launch_check("mlp"));
+  }
+  if (!block) return DFLASH_OK;
+
+  // ---- rows 1..n: final norm, unembedding, one batched draw ----------------
+  const int n = fw.n, Rz = Bc * n;
+  launch_rmsnorm(m->dt, false, m->h.p, Mb, nullptr, H, m->final_norm, m->z.p, H, Rz, H, n, nrows, 1, c.rms_eps, st);
+  float* lg;
+  if (Bc == 1) {
+    lg = fw.sess[0]->plogits;
+  } else {
+    ST_TRY(m->logits.ensure((size_t)Rz * V * 4, st));
+    lg = m->logits.as<float>();
+  }
+  ST_TRY(gemm(m, m->z.p, H, m->unembed, H, lg, V, Rz, V, H, st));
+  const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
+  ST_TRY(m->spart.ensure((size_t)Rz * chunks * sizeof(float4), st));
+  ST_TRY(m->vstat.ensure((size_t)Rz * 8, st));
+  SampleArgs sa{};
+  sa.logits = lg;
+  sa.ld = V;
+  sa.rows = Rz;
+  sa.V = V;
+  sa.in_bf16 = 0;
+  sa.temperature = fw.temperature;
+  sa.gumbel = fw.temperature > 0.f;
+  sa.seed = fw.seed;
+  sa.rnd = (uint32_t)fw.rnd;
+  sa.rows_per_seq = n;
+  sa.row_offset = 1;
+  sa.seq_ids = tabs.seq;
+  launch_sample_partials(sa, chunk, m->spart.as<float4>(), st);
+  int32_t* tok = m->vstat.as<int32_t>();
+  float* lse = (float*)(tok + Rz);
+  launch_sample_combine(sa, chunks, m->spart.as<float4>(), tok, nullptr, lse, st);
+  // outputs in caller order
+  sa.out_map = (const int32_t*)(tb + o_map);
+  launch_sample_combine(sa, chunks, m->spart.as<float4>(), fw.out_tokens, fw.out_q, nullptr, st);
+  ST_TRY(launch_check("sample"));
+  for (int j = 0; j < Bc; ++j) {
+    dflash_session* s = fw.sess[j];
+    if (Bc > 1) CU_TRY(cudaMemcpyAsync(s->plogits, lg + (size_t)j * n * V, (size_t)n * V * 4, cudaMemcpyDeviceToDevice, st));
+    CU_TRY(cudaMemcpyAsync(s->plse, lse + j * n, n * 4, cudaMemcpyDeviceToDevice, st));
+    CU_TRY(cudaMemcpyAsync(s->ptok, tok + j * n, n * 4, cudaMemcpyDeviceToDevice, st));
+    if (fw.out_logits)
+      CU_TRY(cudaMemcpyAsync(fw.out_logits + (size_t)fw.sess_map[j] * n * V, s->plogits, (size_t)n * V * 4,
+                             cudaMemcpyDeviceToDevice, st));
+  }
+  return DFLASH_OK;
+}
+
+// Context rows of one session's held features (and optionally extra rows
+// straight from the caller), with the window drop applied.  F advances
+// past every row; P returns to zero.
+void take_pending(dflash_session* s, int32_t sess_idx, const void* extra, int64_t extra_stride, int extra_rows,
+                  std::vector<CtxRow>& out) {
+  const dflash_config& c = s->m->cfg;
+  const size_t rowb = (size_t)c.n_taps * c.target_hidden * s->m->esz;
+  const int64_t first = s->F;
+  const int total = s->P + extra_rows;
+  const int64_t Fnew = first + total;
+  for (int r = 0; r < total; ++r) {
+    const int64_t slot = first + r;
+    if (c.window && slot <= Fnew - c.window) continue;  // no later query can see it
+    const void* src = r < s->P ? (const char*)s->pending + (size_t)r * rowb
+                               : (const char*)extra + (size_t)(r - s->P) * extra_stride * s->m->esz;
+    out.push_back(CtxRow{src, sess_idx, slot});
+  }
+  s->flushed_rows += total;
+  s->F = Fnew;
+  s->P = 0;
+}
+
+void commit_block(dflash_session* s) {
+  if (!s->block_outstanding) return;
+  s->block_outstanding = false;  // the block's slots past F are free again
+}
+
+int check_sessions(dflash_session* const* s, int32_t batch) {
+  if (!s || batch < 1) return fail(DFLASH_ERR_INVALID_ARG, "null session array or batch < 1");
+  for (int b = 0; b < batch; ++b) {
+    if (!s[b]) return fail(DFLASH_ERR_INVALID_ARG, "session %d is null", b);
+    if (s[b]->m != s[0]->m) return fail(DFLASH_ERR_INVALID_ARG, "sessions of different models in one batch");
+    for (int j = 0; j < b; ++j)
+      if (s[j] == s[b]) return fail(DFLASH_ERR_INVALID_ARG, "session %d repeated in batch", b);
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* dflash_last_error(void) { return g_err.c_str(); }
+int dflash_version(void) { return 100; }
+
+int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflash_model** out) {
+  if (!cfg || !w || !out) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  ST_TRY(check_config(*cfg));
+  const dflash_config& c = *cfg;
+  if (!w->aux_norms || !w->w_fc || !w->hidden_norm || !w->final_norm || !w->embed || !w->unembed || !w->layers)
+    return fail(DFLASH_ERR_INVALID_ARG, "null model weight");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    if (!lw.in_norm || !lw.w_qkv || !lw.q_norm || !lw.k_norm || !lw.w_o || !lw.post_norm || !lw.w_gate || !lw.w_up ||
+        !lw.w_down)
+      return fail(DFLASH_ERR_INVALID_ARG, "null weight in layer %d", l);
+    if (c.gated_attention && !lw.w_g) return fail(DFLASH_ERR_SHAPE, "layer %d: gated attention without g_proj", l);
+    if (!c.gated_attention && lw.w_g) return fail(DFLASH_ERR_SHAPE, "layer %d: g_proj given but gating is off", l);
+  }
+  dflash_model* m = new dflash_model();
+  m->cfg = c;
+  m->dt = c.dtype == DFLASH_DTYPE_BF16 ? DT::BF16 : DT::F32;
+  m->esz = dt_size(m->dt);
+  m->aux_norms = w->aux_norms;
+  m->w_fc = w->w_fc;
+  m->hidden_norm = w->hidden_norm;
+  m->final_norm = w->final_norm;
+  m->embed = w->embed;
+  m->unembed = w->unembed;
+  m->qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  m->qkv_cols = m->qkv_rows + (c.gated_attention ? c.n_q_heads : 0);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaMalloc(&m->d_err, 16);
+  if (e == cudaSuccess) e = cudaMemset(m->d_err, 0, 16);
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(DFLASH_ERR_CUDA, "device setup: %s", cudaGetErrorString(e));
+  }
+  m->layers.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    LayerW& L = m->layers[l];
+    L = LayerW{lw.in_norm, lw.w_qkv, lw.q_norm, lw.k_norm, lw.w_g, lw.w_o, lw.post_norm, lw.w_gate, lw.w_up, lw.w_down,
+               nullptr};
+    if (c.gated_attention) {
+      // one product for q | k | v | gate: a packed copy of the two matrices
+      const size_t a = (size_t)m->qkv_rows * c.hidden * m->esz, g = (size_t)c.n_q_heads * c.hidden * m->esz;
+      e = cudaMalloc(&L.w_qkvg, a + g);
+      if (e == cudaSuccess) e = cudaMemcpy(L.w_qkvg, lw.w_qkv, a, cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess) e = cudaMemcpy((char*)L.w_qkvg + a, lw.w_g, g, cudaMemcpyDeviceToDevice);
+      if (e != cudaSuccess) {
+        dflash_model_destroy(m);
+        return fail(e == cudaErrorMemoryAllocation ? DFLASH_ERR_OOM : DFLASH_ERR_CUDA, "packing qkv+g: %s",
+                    cudaGetErrorString(e));
+      }
+    }
+  }
+  m->use_tc = m->dt == DT::BF16 && !(c.flags & DFLASH_FLAG_SIMT_GEMM);
+  if (m->use_tc) {
+    if (tc_create(&m->tc, m->num_sms, m->d_err)) {
+      const std::string msg = tc_last_error();
+      dflash_model_destroy(m);
+      return fail(DFLASH_ERR_CUDA, "tcgen05 setup: %s", msg.c_str());
+    }
+  }
+  *out = m;
+  return DFLASH_OK;
+}
+
+int dflash_model_destroy(dflash_model* m) {
+  if (!m) return fail(DFLASH_ERR_INVALID_ARG, "null model");
+  cudaDeviceSynchronize();
+  for (auto& L : m->layers)
+    if (L.w_qkvg) cudaFree(L.w_qkvg);
+  Buf* bufs[] = {&m->tables, &m->u, &m->fcout, &m->c, &m->h, &m->x, &m->qkv, &m->rope, &m->Q, &m->G,
+                 &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart};
+  for (Buf* b : bufs) b->release();
+  m->ring.release();
+  if (m->d_err) cudaFree(m->d_err);
+  if (m->tc) tc_destroy(m->tc);
+  delete m;
+  return DFLASH_OK;
+}
+
+int dflash_draft_limit(const dflash_model* m) {
+  if (!m) return fail(DFLASH_ERR_INVALID_ARG, "null model");
+  return m->cfg.block_size - 1;
+}
+
+int dflash_device_status(dflash_model* m) {
+  if (!m) return fail(DFLASH_ERR_INVALID_ARG, "null model");
+  int32_t e = 0;
+  CU_TRY(cudaDeviceSynchronize());
+  CU_TRY(cudaMemcpy(&e, m->d_err, 4, cudaMemcpyDeviceToHost));
+  CU_TRY(cudaMemset(m->d_err, 0, 4));
+  if (e) {
+    std::string why;
+    if (e & 1) why += "anchor token id outside the vocabulary; ";
+    if (e & 2) why += "draft token id outside the vocabulary; ";
+    if (e & 4) why += "tensor-core pipeline wait expired; ";
+    return fail(DFLASH_ERR_DEVICE, "device reported: %s", why.c_str());
+  }
+  return DFLASH_OK;
+}
+
+int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void* stream, dflash_session** out) {
+  if (!m || !out) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  const dflash_config& c = m->cfg;
+  if (max_ctx < 1 || restored_offset < 0 || restored_offset > max_ctx)
+    return fail(DFLASH_ERR_INVALID_ARG, "max_ctx %lld / restored_offset %lld", (long long)max_ctx,
+                (long long)restored_offset);
+  dflash_session* s = new dflash_session();
+  s->m = m;
+  s->stream = (cudaStream_t)stream;
+  s->F = restored_offset;
+  s->max_ctx = max_ctx;
+  s->cap = c.window ? align_up((int64_t)c.window + c.block_size, 64) : align_up(max_ctx + c.block_size, 64);
+  const size_t kvb = (size_t)c.n_layers * 2 * c.n_kv_heads * s->cap * c.head_dim * m->esz;
+  const size_t pend = (size_t)DFLASH_PENDING_FLUSH_TOKENS * c.n_taps * c.target_hidden * m->esz;
+  const size_t nb = (size_t)(c.block_size - 1);
+  cudaError_t e = cudaMalloc(&s->kv, kvb);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->kv, 0, kvb, s->stream);
+  if (e == cudaSuccess) e = cudaMalloc(&s->pending, pend);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&s->plogits, nb * c.vocab * 4);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&s->plse, nb * 4);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&s->ptok, nb * 4);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&s->d_accepted, 8);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->d_accepted, 0, 8, s->stream);
+  if (e != cudaSuccess) {
+    cudaFree(s->kv);
+    cudaFree(s->pending);
+    cudaFree(s->plogits);
+    cudaFree(s->plse);
+    cudaFree(s->ptok);
+    cudaFree(s->d_accepted);
+    delete s;
+    return fail(e == cudaErrorMemoryAllocation ? DFLASH_ERR_OOM : DFLASH_ERR_CUDA, "session buffers: %s",
+                cudaGetErrorString(e));
+  }
+  *out = s;
+  return DFLASH_OK;
+}
+
+int dflash_committed(dflash_session* s, const void* features, int64_t row_stride, int32_t n_rows, int64_t position) {
+  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+  const dflash_config& c = s->m->cfg;
+  const int64_t width = (int64_t)c.n_taps * c.target_hidden;
+  if (n_rows < 0 || position < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_rows %d / position %lld", n_rows, (long long)position);
+  if (n_rows > 0 && (!features || row_stride < width))
+    return fail(DFLASH_ERR_INVALID_ARG, "features null or row_stride %lld < %lld", (long long)row_stride, (long long)width);
+  const int64_t start = s->F + s->P - position;
+  if (start < 0)
+    return fail(DFLASH_ERR_CONTEXT_GAP, "committed run at %lld leaves a context gap at %lld", (long long)position,
+                (long long)(s->F + s->P));
+  if (start >= n_rows) return DFLASH_OK;  // restored prefix: nothing new
+  const int add = (int)(n_rows - start);
+  if (s->F + s->P + add > s->max_ctx)
+    return fail(DFLASH_ERR_CAPACITY, "context would reach %lld rows, max_ctx %lld", (long long)(s->F + s->P + add),
+                (long long)s->max_ctx);
+  const size_t es = s->m->esz;
+  const char* src = (const char*)features + (size_t)start * row_stride * es;
+  if (s->P + add < DFLASH_PENDING_FLUSH_TOKENS) {
+    CU_TRY(cudaMemcpy2DAsync((char*)s->pending + (size_t)s->P * width * es, width * es, src, row_stride * es, width * es,
+                             add, cudaMemcpyDeviceToDevice, s->stream));
+    s->P += add;
+    return DFLASH_OK;
+  }
+  // the held rows reach the flush threshold: one context-only forward over
+  // the staged rows and the new rows read in place
+  commit_block(s);
+  Forward fw;
+  fw.sess = {s};
+  const int64_t F0 = s->F;
+  const int32_t P0 = s->P;
+  take_pending(s, 0, src, row_stride, add, fw.ctx);
+  const int rc = run_forward(s->m, fw, s->stream);
+  if (rc != DFLASH_OK) {
+    s->F = F0;
+    s->P = P0;
+    return rc;
+  }
+  s->flushes++;
+  return DFLASH_OK;
+}
+
+int dflash_commit_block(dflash_session* const* s, int32_t batch) {
+  ST_TRY(check_sessions(s, batch));
+  for (int b = 0; b < batch; ++b) commit_block(s[b]);
+  return DFLASH_OK;
+}
+
+int dflash_flush(dflash_session* const* s, int32_t batch) {
+  ST_TRY(check_sessions(s, batch));
+  Forward fw;
+  std::vector<int64_t> F0(batch);
+  std::vector<int32_t> P0(batch);
+  for (int b = 0; b < batch; ++b) {
+    commit_block(s[b]);
+    F0[b] = s[b]->F;
+    P0[b] = s[b]->P;
+    if (s[b]->P == 0) continue;
+    const int32_t j = (int32_t)fw.sess.size();
+    fw.sess.push_back(s[b]);
+    take_pending(s[b], j, nullptr, 0, 0, fw.ctx);
+  }
+  if (fw.sess.empty()) return DFLASH_OK;
+  const int rc = run_forward(s[0]->m, fw, s[0]->stream);
+  if (rc != DFLASH_OK) {
+    for (int b = 0; b < batch; ++b) {
+      s[b]->F = F0[b];
+      s[b]->P = P0[b];
+    }
+    return rc;
+  }
+  for (auto* x : fw.sess) x->flushes++;
+  return DFLASH_OK;
+}
+
+int dflash_settle(dflash_session* s) { return dflash_flush(&s, 1); }
+
+int dflash_propose(dflash_session* const* s, int32_t batch, const int32_t* current, int32_t max_tokens,
+                   float temperature, uint64_t seed, uint64_t round, int32_t* out_tokens, float* out_q,
+                   float* out_logits, int32_t* out_n) {
+  ST_TRY(check_sessions(s, batch));
+  if (!out_n) return fail(DFLASH_ERR_INVALID_ARG, "out_n is null");
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(DFLASH_ERR_INVALID_ARG, "temperature");
+  dflash_model* m = s[0]->m;
+  const int n = std::min<int>(max_tokens, m->cfg.block_size - 1);
+  for (int b = 0; b < batch; ++b) out_n[b] = 0;
+  if (n <= 0) return DFLASH_OK;
+  if (!current || !out_tokens || !out_q) return fail(DFLASH_ERR_INVALID_ARG, "null current / out_tokens / out_q");
+  Forward fw;
+  fw.n = n;
+  fw.current = current;
+  fw.temperature = temperature;
+  fw.seed = seed;
+  fw.rnd = round;
+  fw.out_tokens = out_tokens;
+  fw.out_q = out_q;
+  fw.out_logits = out_logits;
+  struct Saved { int64_t F; int32_t P; bool bo, hp; };
+  std::vector<Saved> saved(batch);
+  for (int b = 0; b < batch; ++b) {
+    dflash_session* x = s[b];
+    saved[b] = Saved{x->F, x->P, x->block_outstanding, x->has_prop};
+    if (x->F + x->P == 0) continue;  // nothing committed yet: nil
+    if (x->F + x->P + n >= x->cap && !m->cfg.window)
+      return fail(DFLASH_ERR_CAPACITY, "session %d: block would pass the cache end", b);
+    commit_block(x);
+    const int32_t j = (int32_t)fw.sess.size();
+    fw.sess.push_back(x);
+    fw.sess_map.push_back(b);
+    take_pending(x, j, nullptr, 0, 0, fw.ctx);
+  }
+  if (fw.sess.empty()) return DFLASH_OK;
+  const int rc = run_forward(m, fw, s[0]->stream);
+  if (rc != DFLASH_OK) {
+    for (int b = 0; b < batch; ++b) {
+      s[b]->F = saved[b].F;
+      s[b]->P = saved[b].P;
+      s[b]->block_outstanding = saved[b].bo;
+      s[b]->has_prop = saved[b].hp;
+    }
+    return rc;
+  }
+  for (size_t j = 0; j < fw.sess.size(); ++j) {
+    dflash_session* x = fw.sess[j];
+    x->block_outstanding = true;
+    x->has_prop = true;
+    x->last_n = n;
+    x->last_T = temperature;
+    x->rounds++;
+    x->proposed += n;
+    out_n[fw.sess_map[j]] = n;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_logits, int32_t logits_dtype,
+                  const int32_t* draft_tokens, int32_t n, float temperature, uint64_t seed, uint64_t round,
+                  int32_t* out_accept, int32_t* out_bonus) {
+  ST_TRY(check_sessions(s, batch));
+  if (!target_logits || !draft_tokens || !out_accept || !out_bonus) return fail(DFLASH_ERR_INVALID_ARG, "null pointer");
+  if (logits_dtype != DFLASH_DTYPE_F32 && logits_dtype != DFLASH_DTYPE_BF16)
+    return fail(DFLASH_ERR_INVALID_ARG, "logits_dtype %d", logits_dtype);
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(DFLASH_ERR_INVALID_ARG, "temperature");
+  dflash_model* m = s[0]->m;
+  if (n < 1 || n > m->cfg.block_size - 1) return fail(DFLASH_ERR_INVALID_ARG, "n = %d", n);
+  for (int b = 0; b < batch; ++b)
+    if (temperature > 0.f && (!s[b]->has_prop || s[b]->last_n != n))
+      return fail(DFLASH_ERR_STATE, "session %d has no proposal of %d tokens to verify against", b, n);
+  cudaStream_t st = s[0]->stream;
+  const int V = m->cfg.vocab, rows = batch * (n + 1);
+  TablePack tp;
+  std::vector<const float*> dl(batch), dlse(batch);
+  std::vector<const int32_t*> dtok(batch);
+  std::vector<float> dT(batch);
+  std::vector<long long*> acc(batch);
+  std::vector<int32_t> seqv(batch);
+  for (int b = 0; b < batch; ++b) {
+    dl[b] = s[b]->plogits;
+    dlse[b] = s[b]->plse;
+    dtok[b] = s[b]->ptok;
+    dT[b] = s[b]->last_T;
+    acc[b] = s[b]->d_accepted;
+    seqv[b] = b;
+  }
+  const size_t o_dl = tp.add(dl), o_dlse = tp.add(dlse), o_dtok = tp.add(dtok), o_dT = tp.add(dT), o_acc = tp.add(acc),
+               o_seq = tp.add(seqv);
+  ST_TRY(m->ring.upload(tp, m->tables, st));
+  char* tb = m->tables.as<char>();
+  const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
+  ST_TRY(m->vpart.ensure((size_t)rows * chunks * sizeof(float4), st));
+  ST_TRY(m->vstat.ensure((size_t)rows * 8, st));
+  int32_t* amax = m->vstat.as<int32_t>();
+  float* lse = (float*)(amax + rows);
+  SampleArgs sa{};
+  sa.logits = target_logits;
+  sa.ld = V;
+  sa.rows = rows;
+  sa.V = V;
+  sa.in_bf16 = logits_dtype == DFLASH_DTYPE_BF16;
+  sa.temperature = temperature;
+  sa.gumbel = 0;
+  sa.rows_per_seq = n + 1;
+  sa.row_offset = 0;
+  launch_sample_partials(sa, chunk, m->vpart.as<float4>(), st);
+  launch_sample_combine(sa, chunks, m->vpart.as<float4>(), amax, nullptr, lse, st);
+  VerifyArgs va{};
+  va.target = target_logits;
+  va.in_bf16 = sa.in_bf16;
+  va.B = batch;
+  va.n = n;
+  va.V = V;
+  va.temperature = temperature;
+  va.seed = seed;
+  va.rnd = (uint32_t)round;
+  va.seq_ids = (const int32_t*)(tb + o_seq);
+  va.draft = draft_tokens;
+  va.lse_t = lse;
+  va.amax_t = amax;
+  va.dlogits = (const float* const*)(tb + o_dl);
+  va.dlse = (const float* const*)(tb + o_dlse);
+  va.dtok = (const int32_t* const*)(tb + o_dtok);
+  va.dtemp = (const float*)(tb + o_dT);
+  va.accept = out_accept;
+  va.bonus = out_bonus;
+  va.accepted_total = (long long* const*)(tb + o_acc);
+  va.err = m->d_err;
+  launch_verify_accept(va, st);
+  return launch_check("verify");
+}
+
+int dflash_close(dflash_session* s) {
+  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+  const int rc = dflash_flush(&s, 1);
+  cudaStreamSynchronize(s->stream);
+  cudaFree(s->kv);
+  cudaFree(s->pending);
+  cudaFree(s->plogits);
+  cudaFree(s->plse);
+  cudaFree(s->ptok);
+  cudaFree(s->d_accepted);
+  delete s;
+  return rc;
+}
+
+int dflash_stats(const dflash_session* s, dflash_counters* out) {
+  if (!s || !out) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  long long acc = 0;
+  CU_TRY(cudaStreamSynchronize(s->stream));
+  CU_TRY(cudaMemcpy(&acc, s->d_accepted, 8, cudaMemcpyDeviceToHost));
+  out->rounds = s->rounds;
+  out->proposed = s->proposed;
+  out->accepted = acc;
+  out->flushes = s->flushes;
+  out->flushed_rows = s->flushed_rows;
+  return DFLASH_OK;
+}
+
+int dflash_session_state(const dflash_session* s, int64_t* ctx_offset, int32_t* pending, int32_t* block_outstanding) {
+  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+  if (ctx_offset) *ctx_offset = s->F;
+  if (pending) *pending = s->P;
+  if (block_outstanding) *block_outstanding = s->block_outstanding ? 1 : 0;
+  return DFLASH_OK;
+}
+
+static int kv_range_ok(const dflash_session* s, int32_t layer, int64_t first, int32_t n) {
+  const dflash_config& c = s->m->cfg;
+  if (layer < 0 || layer >= c.n_layers || first < 0 || n < 0) return fail(DFLASH_ERR_INVALID_ARG, "layer / range");
+  if (first + n > s->max_ctx + c.block_size) return fail(DFLASH_ERR_CAPACITY, "rows past the cache");
+  if (c.window && n > s->cap) return fail(DFLASH_ERR_CAPACITY, "more rows than the ring holds");
+  return DFLASH_OK;
+}
+
+int dflash_kv_export(const dflash_session* s, int32_t layer, int64_t first_slot, int32_t n_rows, void* k_out,
+                     void* v_out) {
+  if (!s || !k_out || !v_out) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  ST_TRY(kv_range_ok(s, layer, first_slot, n_rows));
+  const dflash_config& c = s->m->cfg;
+  const size_t plane = (size_t)c.n_kv_heads * s->cap * c.head_dim * s->m->esz;
+  const char* base = (const char*)s->kv + (size_t)(2 * layer) * plane;
+  launch_kv_copy(s->m->dt, k_out, n_rows, 0, base, s->cap, first_slot, n_rows, c.n_kv_heads, c.head_dim, s->stream);
+  launch_kv_copy(s->m->dt, v_out, n_rows, 0, base + plane, s->cap, first_slot, n_rows, c.n_kv_heads, c.head_dim,
+                 s->stream);
+  return launch_check("kv_export");
+}
+
+int dflash_kv_import(dflash_session* s, int32_t layer, int64_t first_slot, int32_t n_rows, const void* k_in,
+                     const void* v_in) {
+  if (!s || !k_in || !v_in) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  ST_TRY(kv_range_ok(s, layer, first_slot, n_rows));
+  const dflash_config& c = s->m->cfg;
+  const size_t plane = (size_t)c.n_kv_heads * s->cap * c.head_dim * s->m->esz;
+  char* base = (char*)s->kv + (size_t)(2 * layer) * plane;
+  launch_kv_copy(s->m->dt, base, s->cap, first_slot, k_in, n_rows, 0, n_rows, c.n_kv_heads, c.head_dim, s->stream);
+  launch_kv_copy(s->m->dt, base + plane, s->cap, first_slot, v_in, n_rows, 0, n_rows, c.n_kv_heads, c.head_dim,
+                 s->stream);
+  return launch_check("kv_import");
+}
+
+}  // extern "C"

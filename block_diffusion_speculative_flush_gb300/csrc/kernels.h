@@ -1,0 +1,115 @@
+// Internal launch interface of the DFlash kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dfl {
+
+enum class DT : int { F32 = 0, BF16 = 1 };
+
+inline size_t dt_size(DT t) { return t == DT::F32 ? 4 : 2; }
+
+// One row of a layer's fused QKV product: a context row being flushed or a
+// block row being drafted.
+struct RowMeta {
+  int32_t sess;  // index into the call's per-session tables
+  int32_t blk;   // block row index into the Q / gate buffers, -1 for context rows
+  int64_t pos;   // absolute position; also the cache slot (modulo the ring)
+};
+
+// Per-session device tables of one batched call.
+struct SessTables {
+  void* const* kv;         // [B] session cache base: [L][2][Hkv][cap][d] in the storage type
+  const int64_t* cap;      // [B] cache slots (ring size when the draft has a window)
+  const int64_t* frontier; // [B] F: position of the block's anchor row
+  const int32_t* seq;      // [B] seq id used by the random streams
+};
+
+// One attention work item: keys [k0, k1) (positions) of one session / KV head.
+struct AttnItem {
+  int32_t sess, kvh;
+  int64_t k0, k1;
+};
+
+struct AttnParams {
+  int Hq, Hkv, d, nrows;    // nrows = n + 1 block rows per session
+  int window, causal;
+  int L, layer;
+  float scale;
+};
+
+// --- portable kernels (any storage type) ----------------------------------
+void launch_tap_norm(DT dt, const void* const* src, int rows, const void* aux, void* u, int K, int Ht,
+                     float eps, cudaStream_t st);
+// out[j] = rmsnorm(in[map(j)]) * g, in rows taken from in0 for map < rows0 else in1.
+// map(j) = (j / a) * b + (j % a) + c.   in_f32: inputs are fp32, else storage type.
+void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* in1, int64_t ld_in,
+                    const void* g, void* out, int64_t ld_out, int rows, int H, int a, int b, int c, float eps,
+                    cudaStream_t st);
+// current[sess_map[j]] is the anchor of compact session j; ids outside
+// [0, V) set bit 1 of *err and read row 0.
+void launch_embed(DT dt, const void* E, const int32_t* current, const int32_t* sess_map, int mask_token, int V,
+                  int B, int nrows, int H, void* h, int32_t* err, cudaStream_t st);
+void launch_rope_table(const RowMeta* meta, int M, int d, float theta, float2* table, cudaStream_t st);
+void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
+                     const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
+                     SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st);
+void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_items, SessTables tabs,
+                           AttnParams p, float* part, cudaStream_t st);
+void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count,
+                              int B, AttnParams p, const float* G, void* O, cudaStream_t st);
+void launch_residual(DT dt, void* h, const float* delta, int64_t ld_delta, int rows, int H, cudaStream_t st);
+void launch_swiglu(DT dt, const float* gu, int64_t ld, int rows, int I, int up_offset, void* a,
+                   cudaStream_t st);
+void launch_gemm_simt(DT dt, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy,
+                      int M, int N, int K, cudaStream_t st);
+void launch_kv_copy(DT dt, void* dst, int64_t dst_cap, int64_t dst_first, const void* src, int64_t src_cap,
+                    int64_t src_first, int n_rows, int Hkv, int d, cudaStream_t st);
+
+// Sampling: per (row, chunk) partials over a row of logits, then a merge.
+struct SampleArgs {
+  const void* logits;      // [rows][V] fp32 or bf16 (in_bf16)
+  int64_t ld;
+  int rows, V;
+  int in_bf16;
+  float temperature;       // 0: argmax
+  int gumbel;              // add the draft's Gumbel noise (T > 0)
+  uint64_t seed;
+  uint32_t rnd;
+  int rows_per_seq;        // rows of one session (seq id = row / rows_per_seq)
+  int row_offset;          // Philox row of a session's first row
+  const int32_t* seq_ids;  // [B] seq id per session
+  const int32_t* out_map;  // [B] output row block of each session (NULL: identity)
+};
+void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st);
+// Writes tok[row], q[row] (probability of the token at T), lse[row] (log-sum-exp of logits/T).
+void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, int32_t* tok, float* qtok,
+                           float* lse, cudaStream_t st);
+
+struct VerifyArgs {
+  const void* target;      // [B][n+1][V]
+  int in_bf16;
+  int B, n, V;
+  float temperature;
+  uint64_t seed;
+  uint32_t rnd;
+  const int32_t* seq_ids;  // [B]
+  const int32_t* draft;    // [B][n] tokens under test
+  const float* lse_t;      // [B][n+1] target log-sum-exp of logits/T
+  const int32_t* amax_t;   // [B][n+1] target argmax
+  const float* const* dlogits;  // [B] -> [n][V] fp32 draft logits of the last proposal
+  const float* const* dlse;     // [B] -> [n]
+  const int32_t* const* dtok;   // [B] -> [n] proposed tokens
+  const float* dtemp;           // [B] temperature of that proposal
+  int32_t* accept;              // [B]
+  int32_t* bonus;               // [B]
+  long long* const* accepted_total;  // [B] -> running counter of each session
+  int32_t* err;                 // bit 2: a draft token id outside [0, V)
+};
+void launch_verify_accept(const VerifyArgs& a, cudaStream_t st);
+
+// --- tensor-core path (bf16, sm_103a) --------------------------------------
+struct TcGemmPlan;  // opaque, defined in gemm_tc.cu
+
+}  // namespace dfl

@@ -1,0 +1,650 @@
+// Portable kernels of the DFlash draft round: every step that is not a
+// weight-streaming matrix product.  Each is templated on the storage type
+// (fp32 for the tiny config, bf16 otherwise) and accumulates in fp32.
+//
+// Steps and the passages they follow:
+//   tap_norm       aux_hidden_norms: one RMSNorm per target tap (Laguna PR #1771)
+//   rmsnorm        hidden_norm / input_layernorm / post-attention / final norms
+//   embed          the block [anchor, mask x n] (dflash.go propose)
+//   rope_table     rotary angles per row, computed in double
+//   qkv_post       per-head q/k norm + RoPE, cache write of context and block
+//                  K/V at their own slots (dflash.go: a context entry at slot S
+//                  derives only from the features at S)
+//   attention      block queries against [context | block] keys, GQA, window,
+//                  causal or bidirectional block mask, split over keys
+//   sample         one batched distribution over rows 1..n (dflash.go selectBlock)
+//   verify_accept  accepted prefix + bonus token from the target logits and
+//                  the proposal probabilities (DFlash2 commit note)
+#include <float.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dfl {
+
+namespace {
+
+template <typename T>
+__global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict__ aux, T* __restrict__ u,
+                           int K, int Ht, float eps) {
+  __shared__ float red[32];
+  const int r = blockIdx.x, k = blockIdx.y;
+  const T* f = src[r] + (size_t)k * Ht;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < Ht; j += blockDim.x) {
+    const float x = to_f(f[j]);
+    ss += x * x;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)Ht + eps);
+  const T* g = aux + (size_t)k * Ht;
+  T* o = u + (size_t)r * K * Ht + (size_t)k * Ht;
+  for (int j = threadIdx.x; j < Ht; j += blockDim.x) o[j] = from_f<T>(to_f(f[j]) * inv * to_f(g[j]));
+}
+
+template <typename TIn, typename T>
+__global__ void k_rmsnorm(const TIn* __restrict__ in0, int rows0, const TIn* __restrict__ in1, int64_t ld_in,
+                          const T* __restrict__ g, T* __restrict__ out, int64_t ld_out, int H, int a, int b,
+                          int c, float eps) {
+  __shared__ float red[32];
+  const int j = blockIdx.x;
+  const int src = (j / a) * b + (j % a) + c;
+  const TIn* x = src < rows0 ? in0 + (int64_t)src * ld_in : in1 + (int64_t)(src - rows0) * ld_in;
+  float ss = 0.f;
+  for (int t = threadIdx.x; t < H; t += blockDim.x) {
+    const float v = to_f(x[t]);
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)H + eps);
+  T* o = out + (int64_t)j * ld_out;
+  for (int t = threadIdx.x; t < H; t += blockDim.x) o[t] = from_f<T>(to_f(x[t]) * inv * to_f(g[t]));
+}
+
+template <typename T>
+__global__ void k_embed(const T* __restrict__ E, const int32_t* __restrict__ current,
+                        const int32_t* __restrict__ sess_map, int mask_token, int V, int nrows, int H,
+                        T* __restrict__ h, int32_t* __restrict__ err) {
+  const int r = blockIdx.x;
+  const int b = r / nrows, i = r % nrows;
+  int tok = i == 0 ? current[sess_map ? sess_map[b] : b] : mask_token;
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) atomicOr(err, 1);
+    tok = 0;
+  }
+  const T* e = E + (int64_t)tok * H;
+  T* o = h + (int64_t)r * H;
+  for (int t = threadIdx.x; t < H; t += blockDim.x) o[t] = e[t];
+}
+
+// cos / sin of pos * theta^(-2j/d), the angle formed and reduced in double so
+// that large positions keep full fp32 accuracy.
+__global__ void k_rope_table(const RowMeta* __restrict__ meta, int d, float theta, float2* __restrict__ table) {
+  const int m = blockIdx.x, j = threadIdx.x;
+  if (j >= d / 2) return;
+  const double inv = pow((double)theta, -2.0 * (double)j / (double)d);
+  const double ang = (double)meta[m].pos * inv;
+  double s, c;
+  sincos(ang, &s, &c);
+  table[(int64_t)m * (d / 2) + j] = make_float2((float)c, (float)s);
+}
+
+// One warp per head of one row.  Lane l holds elements l + 32u of the head,
+// so RoPE partners (j, j + d/2) sit in the same lane.
+template <typename T, int DU>  // DU = d / 32
+__global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const RowMeta* __restrict__ meta,
+                           const float2* __restrict__ rope, const T* __restrict__ q_norm,
+                           const T* __restrict__ k_norm, int Hq, int Hkv, int gated, float eps, SessTables tabs,
+                           int layer, T* __restrict__ Q, float* __restrict__ G) {
+  constexpr int d = DU * 32;
+  const int m = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int hh = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const RowMeta rm = meta[m];
+  const float* row = qkv + (int64_t)m * ldq;
+  if (gated && rm.blk >= 0 && blockIdx.y == 0) {
+    for (int hq = threadIdx.x; hq < Hq; hq += blockDim.x) {
+      const float x = row[(Hq + 2 * Hkv) * d + hq];
+      G[(int64_t)rm.blk * Hq + hq] = 1.f / (1.f + expf(-x));
+    }
+  }
+  if (hh >= Hq + Hkv) return;
+  const bool is_q = hh < Hq;
+  if (is_q && rm.blk < 0) return;  // context rows need only K and V
+  const int kh = hh - Hq;
+  const float* x = row + (int64_t)hh * d;
+  float y[DU];
+  float ss = 0.f;
+#pragma unroll
+  for (int u = 0; u < DU; ++u) {
+    y[u] = x[lane + 32 * u];
+    ss += y[u] * y[u];
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  const T* gn = is_q ? q_norm : k_norm;
+#pragma unroll
+  for (int u = 0; u < DU; ++u) y[u] = y[u] * inv * to_f(gn[lane + 32 * u]);
+  const float2* rt = rope + (int64_t)m * (d / 2);
+#pragma unroll
+  for (int u = 0; u < DU / 2; ++u) {
+    const float2 cs = rt[lane + 32 * u];
+    const float a = y[u], b = y[u + DU / 2];
+    y[u] = a * cs.x - b * cs.y;
+    y[u + DU / 2] = b * cs.x + a * cs.y;
+  }
+  if (is_q) {
+    T* q = Q + ((int64_t)rm.blk * Hq + hh) * d;
+#pragma unroll
+    for (int u = 0; u < DU; ++u) q[lane + 32 * u] = from_f<T>(y[u]);
+    return;
+  }
+  const int64_t cap = tabs.cap[rm.sess];
+  const int64_t slot = rm.pos % cap;
+  T* base = (T*)tabs.kv[rm.sess];
+  T* kd = base + (((int64_t)(2 * layer) * Hkv + kh) * cap + slot) * d;
+  T* vd = base + (((int64_t)(2 * layer + 1) * Hkv + kh) * cap + slot) * d;
+  const float* xv = row + (int64_t)(Hq + Hkv + kh) * d;
+#pragma unroll
+  for (int u = 0; u < DU; ++u) {
+    kd[lane + 32 * u] = from_f<T>(y[u]);
+    vd[lane + 32 * u] = from_f<T>(xv[lane + 32 * u]);
+  }
+}
+
+// Key visibility for block row i (position F + i) and key position r.
+__device__ __forceinline__ bool key_visible(int64_t F, int i, int64_t r, int window, int causal) {
+  if (window && (F + i) - r >= window) return false;
+  if (causal && r >= F && (r - F) > i) return false;
+  return true;
+}
+
+// Split-key attention on CUDA cores: one CTA per work item (session, KV head,
+// key range); all n+1 rows x group query heads of that KV head at once.
+// Partial (max, sum, acc[d]) per query row; merged by k_attn_combine.
+template <typename T>
+__global__ void k_attn_simt(const T* __restrict__ Q, const AttnItem* __restrict__ items, SessTables tabs,
+                            AttnParams p, float* __restrict__ part) {
+  extern __shared__ float sm[];
+  const int d = p.d, G = p.Hq / p.Hkv, R = p.nrows * G;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float* qs = sm;                      // [R][d]
+  float* ks = qs + R * d;              // [32][d+1]
+  float* vs = ks + 32 * (d + 1);       // [32][d]
+  float* ms = vs + 32 * d;             // [R]
+  float* ls = ms + R;                  // [R]
+  float* acc = ls + R;                 // [R][d]
+  const AttnItem it = items[blockIdx.x];
+  const int64_t F = tabs.frontier[it.sess], cap = tabs.cap[it.sess];
+  const T* Kb = (const T*)tabs.kv[it.sess] + ((int64_t)(2 * p.layer) * p.Hkv + it.kvh) * cap * d;
+  const T* Vb = (const T*)tabs.kv[it.sess] + ((int64_t)(2 * p.layer + 1) * p.Hkv + it.kvh) * cap * d;
+  for (int e = threadIdx.x; e < R * d; e += blockDim.x) {
+    const int rr = e / d, t = e % d;
+    const int i = rr / G, g = rr % G;
+    qs[e] = to_f(Q[(((int64_t)it.sess * p.nrows + i) * p.Hq + it.kvh * G + g) * d + t]) * p.scale;
+    acc[e] = 0.f;
+  }
+  for (int rr = threadIdx.x; rr < R; rr += blockDim.x) {
+    ms[rr] = -INFINITY;
+    ls[rr] = 0.f;
+  }
+  __syncthreads();
+  for (int64_t kt = it.k0; kt < it.k1; kt += 32) {
+    for (int e = threadIdx.x; e < 32 * d; e += blockDim.x) {
+      const int j = e / d, t = e % d;
+      const int64_t r = kt + j;
+      float kv = 0.f, vv = 0.f;
+      if (r < it.k1) {
+        const int64_t slot = r % cap;
+        kv = to_f(Kb[slot * d + t]);
+        vv = to_f(Vb[slot * d + t]);
+      }
+      ks[j * (d + 1) + t] = kv;
+      vs[j * d + t] = vv;
+    }
+    __syncthreads();
+    for (int rr = warp; rr < R; rr += nw) {
+      const int i = rr / G;
+      const int64_t r = kt + lane;
+      const bool vis = r < it.k1 && key_visible(F, i, r, p.window, p.causal);
+      float s = -INFINITY;
+      if (vis) {
+        float a = 0.f;
+        for (int t = 0; t < d; ++t) a += qs[rr * d + t] * ks[lane * (d + 1) + t];
+        s = a;
+      }
+      const float mt = warp_max(s);
+      if (mt == -INFINITY) continue;
+      const float m_old = ms[rr];
+      const float m_new = fmaxf(m_old, mt);
+      const float pj = vis ? expf(s - m_new) : 0.f;
+      const float corr = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
+      const float psum = warp_sum(pj);
+      for (int t = lane; t < d; t += 32) {
+        float a = acc[rr * d + t] * corr;
+        for (int j = 0; j < 32; ++j) a += __shfl_sync(0xffffffffu, pj, j) * vs[j * d + t];
+        acc[rr * d + t] = a;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        ms[rr] = m_new;
+        ls[rr] = ls[rr] * corr + psum;
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+  }
+  float* out = part + (int64_t)blockIdx.x * R * (d + 2);
+  for (int e = threadIdx.x; e < R * (d + 2); e += blockDim.x) {
+    const int rr = e / (d + 2), t = e % (d + 2);
+    out[e] = t == 0 ? ms[rr] : (t == 1 ? ls[rr] : acc[rr * d + t - 2]);
+  }
+}
+
+template <typename T>
+__global__ void k_attn_combine(const float* __restrict__ part, const int32_t* __restrict__ item_first,
+                               const int32_t* __restrict__ item_count, AttnParams p, const float* __restrict__ Gt,
+                               T* __restrict__ O) {
+  const int d = p.d, G = p.Hq / p.Hkv, R = p.nrows * G;
+  const int b = blockIdx.x / p.nrows, i = blockIdx.x % p.nrows;
+  const int hq = blockIdx.y, kvh = hq / G, g = hq % G, rr = i * G + g;
+  const int S = item_count[b];
+  const int first = item_first[b] + kvh * S;
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, part[((int64_t)(first + s) * R + rr) * (d + 2)]);
+  float L = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float* ps = part + ((int64_t)(first + s) * R + rr) * (d + 2);
+    if (ps[0] != -INFINITY) L += ps[1] * expf(ps[0] - M);
+  }
+  const float gate = Gt ? Gt[((int64_t)b * p.nrows + i) * p.Hq + hq] : 1.f;
+  for (int t = threadIdx.x; t < d; t += blockDim.x) {
+    float o = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float* ps = part + ((int64_t)(first + s) * R + rr) * (d + 2);
+      if (ps[0] != -INFINITY) o += ps[2 + t] * expf(ps[0] - M);
+    }
+    o = o / L * gate;
+    O[(((int64_t)b * p.nrows + i) * p.Hq + hq) * d + t] = from_f<T>(o);
+  }
+}
+
+template <typename T>
+__global__ void k_residual(T* __restrict__ h, const float* __restrict__ delta, int64_t ld, int H) {
+  const int r = blockIdx.x;
+  for (int t = threadIdx.x; t < H; t += blockDim.x) {
+    T* p = h + (int64_t)r * H + t;
+    *p = from_f<T>(to_f(*p) + delta[(int64_t)r * ld + t]);
+  }
+}
+
+template <typename T>
+__global__ void k_swiglu(const float* __restrict__ gu, int64_t ld, int I, int up_off, T* __restrict__ a) {
+  const int r = blockIdx.x;
+  for (int t = threadIdx.x; t < I; t += blockDim.x) {
+    const float g = gu[(int64_t)r * ld + t], u = gu[(int64_t)r * ld + up_off + t];
+    a[(int64_t)r * I + t] = from_f<T>(g / (1.f + expf(-g)) * u);
+  }
+}
+
+// Y[M][N] = X[M][K] . W[N][K]^T on CUDA cores, fp32 accumulation with a
+// fixed k order (independent of M).  64x64 tiles, 4x4 outputs per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) k_gemm_simt(const T* __restrict__ X, int64_t ldx, const T* __restrict__ W,
+                                                   int64_t ldw, float* __restrict__ Y, int64_t ldy, int M, int N,
+                                                   int K) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float c[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int e = threadIdx.x; e < 64 * 16; e += 256) {
+      const int r = e / 16, kk = e % 16;
+      const int gm = m0 + r, gn = n0 + r, gk = k0 + kk;
+      As[kk][r] = (gm < M && gk < K) ? to_f(X[(int64_t)gm * ldx + gk]) : 0.f;
+      Bs[kk][r] = (gn < N && gk < K) ? to_f(W[(int64_t)gn * ldw + gk]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = As[kk][ty + 16 * i];
+        b[i] = Bs[kk][tx + 16 * i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[i][j] = fmaf(a[i], b[j], c[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gm = m0 + ty + 16 * i, gn = n0 + tx + 16 * j;
+      if (gm < M && gn < N) Y[(int64_t)gm * ldy + gn] = c[i][j];
+    }
+}
+
+template <typename T>
+__global__ void k_kv_copy(T* __restrict__ dst, int64_t dcap, int64_t dfirst, const T* __restrict__ src,
+                          int64_t scap, int64_t sfirst, int n, int d) {
+  const int h = blockIdx.y, r = blockIdx.x;
+  const T* s = src + ((int64_t)h * scap + (sfirst + r) % scap) * d;
+  T* o = dst + ((int64_t)h * dcap + (dfirst + r) % dcap) * d;
+  for (int t = threadIdx.x; t < d; t += blockDim.x) o[t] = s[t];
+}
+
+// ---------------------------------------------------------------------------
+// sampling
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float load_logit(const void* p, int in_bf16, int64_t idx) {
+  return in_bf16 ? __bfloat162float(((const bf16*)p)[idx]) : ((const float*)p)[idx];
+}
+
+// part[row][chunk] = (max of l/T, sum exp(l/T - max), best score, best index)
+// where the score is l/T + Gumbel (draft draw) or l/T (argmax / row stats).
+__global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
+  __shared__ float sm_m[32], sm_l[32], sm_s[32];
+  __shared__ int32_t sm_i[32];
+  const int row = blockIdx.x, c = blockIdx.y, nch = gridDim.y;
+  const int v0 = c * chunk, v1 = min(a.V, v0 + chunk);
+  const float invT = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
+  const int b = row / a.rows_per_seq;
+  const uint32_t prow = (uint32_t)(row % a.rows_per_seq + a.row_offset);
+  const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
+  float m = -INFINITY, l = 0.f;
+  ArgMax best{-INFINITY, INT32_MAX};
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    const float s = load_logit(a.logits, a.in_bf16, (int64_t)row * a.ld + v) * invT;
+    if (s > m) {
+      l = l * expf(m - s) + 1.f;
+      m = s;
+    } else {
+      l += expf(s - m);
+    }
+    float score = s;
+    if (a.gumbel) score += gumbel(a.seed, a.rnd, kStreamDraft, seq, prow, (uint32_t)v);
+    best = better(best, ArgMax{score, v});
+  }
+  // warp merge
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    const float M = fmaxf(m, m2);
+    l = (m == -INFINITY ? 0.f : l * expf(m - M)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - M));
+    m = M;
+  }
+  best = warp_argmax(best);
+  if (lane == 0) {
+    sm_m[w] = m;
+    sm_l[w] = l;
+    sm_s[w] = best.v;
+    sm_i[w] = best.i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int i = 0; i < nw; ++i) M = fmaxf(M, sm_m[i]);
+    float L = 0.f;
+    ArgMax bb{-INFINITY, INT32_MAX};
+    for (int i = 0; i < nw; ++i) {
+      if (sm_m[i] != -INFINITY) L += sm_l[i] * expf(sm_m[i] - M);
+      bb = better(bb, ArgMax{sm_s[i], sm_i[i]});
+    }
+    part[(int64_t)row * nch + c] = make_float4(M, L, bb.v, __int_as_float(bb.i));
+  }
+}
+
+__global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restrict__ part, int32_t* __restrict__ tok,
+                                 float* __restrict__ qtok, float* __restrict__ lse) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= a.rows) return;
+  float M = -INFINITY;
+  for (int c = 0; c < chunks; ++c) M = fmaxf(M, part[(int64_t)row * chunks + c].x);
+  float L = 0.f;
+  ArgMax bb{-INFINITY, INT32_MAX};
+  for (int c = 0; c < chunks; ++c) {
+    const float4 pc = part[(int64_t)row * chunks + c];
+    if (pc.x != -INFINITY) L += pc.y * expf(pc.x - M);
+    bb = better(bb, ArgMax{pc.z, __float_as_int(pc.w)});
+  }
+  const float ls = M + logf(L);
+  int orow = row;
+  if (a.out_map) orow = a.out_map[row / a.rows_per_seq] * a.rows_per_seq + row % a.rows_per_seq;
+  if (tok) tok[orow] = bb.i;
+  if (lse) lse[orow] = ls;
+  if (qtok) {
+    if (a.temperature > 0.f) {
+      const float x = load_logit(a.logits, a.in_bf16, (int64_t)row * a.ld + bb.i) / a.temperature;
+      qtok[orow] = expf(x - ls);
+    } else {
+      qtok[orow] = 1.f;
+    }
+  }
+}
+
+// One CTA per session: the sequential acceptance scan, then (T > 0) one pass
+// over the vocabulary for the bonus draw.
+__global__ void __launch_bounds__(1024) k_verify_accept(VerifyArgs a) {
+  __shared__ int s_rej;
+  __shared__ float sm_sum[32];
+  __shared__ float sm_rs[32], sm_ps[32];
+  __shared__ int32_t sm_ri[32], sm_pi[32];
+  const int b = blockIdx.x;
+  const int n = a.n, V = a.V;
+  const int64_t tbase = (int64_t)b * (n + 1) * V;
+  const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
+  if (a.temperature <= 0.f) {
+    if (threadIdx.x == 0) {
+      int acc = 0;
+      while (acc < n && a.amax_t[b * (n + 1) + acc] == a.draft[b * n + acc]) ++acc;
+      a.accept[b] = acc;
+      a.bonus[b] = a.amax_t[b * (n + 1) + acc];
+      if (a.accepted_total) *a.accepted_total[b] += acc;
+    }
+    return;
+  }
+  const float invT = 1.f / a.temperature;
+  const float Tq = a.dtemp[b];
+  const float* dl = a.dlogits[b];
+  const float* dlse = a.dlse[b];
+  const int32_t* dtok = a.dtok[b];
+  if (threadIdx.x == 0) {
+    int rej = 0;
+    for (int i = 1; i <= n; ++i) {
+      int dtk = a.draft[b * n + i - 1];
+      if (dtk < 0 || dtk >= V) {
+        atomicOr(a.err, 2);
+        dtk = 0;
+      }
+      const float p = expf(load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT -
+                           a.lse_t[b * (n + 1) + i - 1]);
+      const float q = Tq > 0.f ? expf(dl[(int64_t)(i - 1) * V + dtk] / Tq - dlse[i - 1])
+                               : (dtk == dtok[i - 1] ? 1.f : 0.f);
+      const float r = uniform_open(rand_u32(a.seed, a.rnd, kStreamAccept, seq, (uint32_t)i, 0u));
+      if (!(r * q < p)) {
+        rej = i;
+        break;
+      }
+    }
+    s_rej = rej;
+  }
+  __syncthreads();
+  const int rej = s_rej;
+  const int trow = rej ? rej - 1 : n;                 // target row of the bonus draw
+  const uint32_t prow = rej ? (uint32_t)rej : (uint32_t)(n + 1);
+  const float lse = a.lse_t[b * (n + 1) + trow];
+  float rsum = 0.f;
+  ArgMax bres{-INFINITY, INT32_MAX}, bp{-INFINITY, INT32_MAX};
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float lp = load_logit(a.target, a.in_bf16, tbase + (int64_t)trow * V + v) * invT - lse;
+    const float g = gumbel(a.seed, a.rnd, kStreamBonus, seq, prow, (uint32_t)v);
+    bp = better(bp, ArgMax{lp + g, v});
+    if (rej) {
+      const float p = expf(lp);
+      const float q = Tq > 0.f ? expf(dl[(int64_t)(rej - 1) * V + v] / Tq - dlse[rej - 1])
+                               : (v == dtok[rej - 1] ? 1.f : 0.f);
+      const float res = fmaxf(p - q, 0.f);
+      rsum += res;
+      if (res > 0.f) bres = better(bres, ArgMax{logf(res) + g, v});
+    }
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  rsum = warp_sum(rsum);
+  bres = warp_argmax(bres);
+  bp = warp_argmax(bp);
+  if (lane == 0) {
+    sm_sum[w] = rsum;
+    sm_rs[w] = bres.v;
+    sm_ri[w] = bres.i;
+    sm_ps[w] = bp.v;
+    sm_pi[w] = bp.i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float S = 0.f;
+    ArgMax R{-INFINITY, INT32_MAX}, P{-INFINITY, INT32_MAX};
+    for (int i = 0; i < nw; ++i) {
+      S += sm_sum[i];
+      R = better(R, ArgMax{sm_rs[i], sm_ri[i]});
+      P = better(P, ArgMax{sm_ps[i], sm_pi[i]});
+    }
+    const int accn = rej ? rej - 1 : n;
+    a.accept[b] = accn;
+    a.bonus[b] = (rej && S > 0.f) ? R.i : P.i;
+    if (a.accepted_total) *a.accepted_total[b] += accn;
+  }
+}
+
+inline unsigned cdiv(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+#define DFL_DISPATCH(dt, ...)                 \
+  do {                                        \
+    if ((dt) == DT::F32) {                    \
+      using T = float;                        \
+      __VA_ARGS__;                            \
+    } else {                                  \
+      using T = bf16;                         \
+      __VA_ARGS__;                            \
+    }                                         \
+  } while (0)
+
+void launch_tap_norm(DT dt, const void* const* src, int rows, const void* aux, void* u, int K, int Ht, float eps,
+                     cudaStream_t st) {
+  if (rows <= 0) return;
+  DFL_DISPATCH(dt, k_tap_norm<T><<<dim3(rows, K), 256, 0, st>>>((const T* const*)src, (const T*)aux, (T*)u, K,
+                                                                   Ht, eps));
+}
+
+void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* in1, int64_t ld_in, const void* g,
+                    void* out, int64_t ld_out, int rows, int H, int a, int b, int c, float eps, cudaStream_t st) {
+  if (rows <= 0) return;
+  if (in_f32) {
+    DFL_DISPATCH(dt, k_rmsnorm<float, T><<<rows, 256, 0, st>>>((const float*)in0, rows0, (const float*)in1, ld_in,
+                                                                (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
+  } else {
+    DFL_DISPATCH(dt, k_rmsnorm<T, T><<<rows, 256, 0, st>>>((const T*)in0, rows0, (const T*)in1, ld_in,
+                                                            (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
+  }
+}
+
+void launch_embed(DT dt, const void* E, const int32_t* current, const int32_t* sess_map, int mask_token, int V,
+                  int B, int nrows, int H, void* h, int32_t* err, cudaStream_t st) {
+  if (B <= 0) return;
+  DFL_DISPATCH(dt, k_embed<T><<<B * nrows, 128, 0, st>>>((const T*)E, current, sess_map, mask_token, V, nrows, H,
+                                                          (T*)h, err));
+}
+
+void launch_rope_table(const RowMeta* meta, int M, int d, float theta, float2* table, cudaStream_t st) {
+  if (M <= 0) return;
+  k_rope_table<<<M, d / 2, 0, st>>>(meta, d, theta, table);
+}
+
+void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
+                     const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
+                     SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st) {
+  (void)L;
+  if (M <= 0) return;
+  const int heads = Hq + Hkv;
+  dim3 grid(M, cdiv(heads, 4));
+  if (d == 64) {
+    DFL_DISPATCH(dt, k_qkv_post<T, 2><<<grid, 128, 0, st>>>(qkv, ldq, meta, rope, (const T*)q_norm,
+                                                              (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
+                                                              (T*)Q, G));
+  } else {
+    DFL_DISPATCH(dt, k_qkv_post<T, 4><<<grid, 128, 0, st>>>(qkv, ldq, meta, rope, (const T*)q_norm,
+                                                              (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
+                                                              (T*)Q, G));
+  }
+}
+
+void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p,
+                           float* part, cudaStream_t st) {
+  if (n_items <= 0) return;
+  const int R = p.nrows * (p.Hq / p.Hkv);
+  const size_t smem = sizeof(float) * ((size_t)R * p.d * 2 + 32 * (p.d + 1) + 32 * p.d + 2 * R);
+  DFL_DISPATCH(dt, {
+    cudaFuncSetAttribute(k_attn_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_attn_simt<T><<<n_items, 256, smem, st>>>((const T*)Q, items, tabs, p, part);
+  });
+}
+
+void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count, int B,
+                              AttnParams p, const float* G, void* O, cudaStream_t st) {
+  DFL_DISPATCH(dt, k_attn_combine<T><<<dim3(B * p.nrows, p.Hq), p.d, 0, st>>>(part, item_first, item_count, p, G,
+                                                                               (T*)O));
+}
+
+void launch_residual(DT dt, void* h, const float* delta, int64_t ld, int rows, int H, cudaStream_t st) {
+  if (rows <= 0) return;
+  DFL_DISPATCH(dt, k_residual<T><<<rows, 256, 0, st>>>((T*)h, delta, ld, H));
+}
+
+void launch_swiglu(DT dt, const float* gu, int64_t ld, int rows, int I, int up_off, void* a, cudaStream_t st) {
+  if (rows <= 0) return;
+  DFL_DISPATCH(dt, k_swiglu<T><<<rows, 256, 0, st>>>(gu, ld, I, up_off, (T*)a));
+}
+
+void launch_gemm_simt(DT dt, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy, int M,
+                      int N, int K, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return;
+  dim3 grid(cdiv(N, 64), cdiv(M, 64));
+  DFL_DISPATCH(dt, k_gemm_simt<T><<<grid, 256, 0, st>>>((const T*)X, ldx, (const T*)W, ldw, Y, ldy, M, N, K));
+}
+
+void launch_kv_copy(DT dt, void* dst, int64_t dcap, int64_t dfirst, const void* src, int64_t scap, int64_t sfirst,
+                    int n, int Hkv, int d, cudaStream_t st) {
+  if (n <= 0) return;
+  DFL_DISPATCH(dt, k_kv_copy<T><<<dim3(n, Hkv), 128, 0, st>>>((T*)dst, dcap, dfirst, (const T*)src, scap, sfirst,
+                                                               n, d));
+}
+
+void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st) {
+  if (a.rows <= 0) return;
+  k_sample_partials<<<dim3(a.rows, cdiv(a.V, chunk)), 256, 0, st>>>(a, chunk, part);
+}
+
+void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, int32_t* tok, float* qtok, float* lse,
+                           cudaStream_t st) {
+  if (a.rows <= 0) return;
+  k_sample_combine<<<cdiv(a.rows, 128), 128, 0, st>>>(a, chunks, part, tok, qtok, lse);
+}
+
+void launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
+  if (a.B <= 0) return;
+  k_verify_accept<<<a.B, 1024, 0, st>>>(a);
+}
+
+}  // namespace dfl

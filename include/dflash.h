@@ -1,0 +1,245 @@
+/*
+ * dflash.h — C ABI of the GB300-native DFlash block-diffusion draft round.
+ *
+ * One draft round has four parts, each an entry point below:
+ *   1. committed / flush:  buffered target feature rows (the concatenated
+ *      hidden taps of the target's layers) pass aux_hidden_norms, fc and
+ *      hidden_norm, then each layer's input norm and a K/V-only projection,
+ *      and land in the draft K/V cache at their own slots.
+ *   2. propose:  one forward of [anchor, mask x n] against that cache; the
+ *      anchor row is dropped, rows 1..n are unembedded and sampled from one
+ *      batched distribution.
+ *   3. commit_block:  the block's rows are rewound out of the cache before
+ *      any write; a committed run that starts past the buffered frontier is
+ *      refused as a context gap.
+ *   4. verify:  accepted prefix plus a bonus token from the target logits
+ *      and the proposal probabilities.
+ *
+ * Sources (web pages): "Ollama DFlash block-diffusion draft model in
+ * mlxrunner" (Facts); ollama mlxrunner/dflash.go (gitea mirror: committed,
+ * settle, close, takePending, commitBlock, flush, propose, selectBlock, and
+ * the DFlash2 commit note); mlxcel PR #1771 "feat(speculative): add the
+ * Laguna DFlash drafter" (summary, review commits, "Where the landed code
+ * and the issue text disagree").
+ *
+ * Conventions
+ *   - Every call returns DFLASH_OK (0) or a negative status.  On error no
+ *     session or model state changes, and dflash_last_error() returns a
+ *     message for the calling thread.  Nothing aborts the process (the
+ *     pages panic on a context gap; here it is a status).
+ *   - Pointers are DEVICE pointers unless marked (host).  Device work is
+ *     enqueued on the session's stream (batched calls: the stream of the
+ *     first session) and is asynchronous unless stated otherwise.
+ *   - Matrices are row-major [out, in]; activations are row-major
+ *     [rows, width].  Storage type is fp32 or bf16 per the model config.
+ *   - A batched call takes a HOST array of sessions of one model.  The
+ *     random streams use the session's index in that array as its seq id.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define DFLASH_OK 0
+#define DFLASH_ERR_INVALID_ARG (-1) /* null pointer, negative size, bad enum */
+#define DFLASH_ERR_SHAPE (-2)       /* config or weight geometry inconsistent / unsupported */
+#define DFLASH_ERR_CONTEXT_GAP (-3) /* committed run starts past the buffered frontier */
+#define DFLASH_ERR_CAPACITY (-4)    /* would exceed the session's max_ctx */
+#define DFLASH_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
+#define DFLASH_ERR_OOM (-6)         /* device allocation failed */
+#define DFLASH_ERR_STATE (-7)       /* call not valid in this state (e.g. verify without propose) */
+#define DFLASH_ERR_DEVICE (-8)      /* a kernel reported a bad input (see dflash_device_status) */
+
+#define DFLASH_DTYPE_F32 0
+#define DFLASH_DTYPE_BF16 1
+
+/* Feature rows held between flushes (dflash.go dflashPendingFlushTokens). */
+#define DFLASH_PENDING_FLUSH_TOKENS 256
+
+/* dflash_config.flags */
+#define DFLASH_FLAG_SIMT_GEMM 1u /* bf16 models: use the CUDA-core GEMM instead of tcgen05 (testing) */
+
+typedef struct dflash_model dflash_model;
+typedef struct dflash_session dflash_session;
+
+/* Draft geometry and block parameters.  Bounds checked by dflash_model_create
+ * (the Laguna PR treats the drafter config as untrusted): block_size in
+ * 2..512, window 0 (full attention) or 2..2^20, head_dim 64 or 128,
+ * n_q_heads a multiple of n_kv_heads, bf16 widths multiples of 64. */
+typedef struct dflash_config {
+  int32_t dtype;           /* DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16 */
+  int32_t n_taps;          /* K: tapped target layers */
+  int32_t target_hidden;   /* H_t: width of one tap; a feature row is K*H_t wide */
+  int32_t hidden;          /* H */
+  int32_t n_layers;        /* L */
+  int32_t n_q_heads;       /* Hq */
+  int32_t n_kv_heads;      /* Hkv */
+  int32_t head_dim;        /* d */
+  int32_t intermediate;    /* I, SwiGLU width */
+  int32_t vocab;           /* V */
+  int32_t block_size;      /* B_s; draft limit is B_s - 1 */
+  int32_t mask_token;      /* m */
+  int32_t window;          /* W: a query at p sees keys r with p - r < W; 0 = unlimited */
+  int32_t causal_block;    /* 1: causal inside the block; 0: bidirectional */
+  int32_t gated_attention; /* 1: per-head sigmoid gate from g_proj on the attention output */
+  uint32_t flags;          /* DFLASH_FLAG_* */
+  float rope_theta;        /* RoPE base (rotate-half pairs j, j + d/2) */
+  float rms_eps;           /* RMSNorm epsilon */
+} dflash_config;
+
+/* Per-layer weights, device pointers in the storage type.  Borrowed: they
+ * must stay valid until dflash_model_destroy. */
+typedef struct dflash_layer_weights {
+  const void* in_norm;   /* [H] input_layernorm, applied to context and block rows */
+  const void* w_qkv;     /* [(Hq + 2 Hkv) d, H] fused projection, rows q | k | v */
+  const void* q_norm;    /* [d] per-head RMSNorm of q */
+  const void* k_norm;    /* [d] per-head RMSNorm of k */
+  const void* w_g;       /* [Hq, H] g_proj (gated_attention) or NULL */
+  const void* w_o;       /* [H, Hq d] */
+  const void* post_norm; /* [H] */
+  const void* w_gate;    /* [I, H] */
+  const void* w_up;      /* [I, H] */
+  const void* w_down;    /* [H, I] */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  const void* aux_norms;   /* [K, H_t] one RMSNorm gain per tap (aux_hidden_norms) */
+  const void* w_fc;        /* [H, K H_t] */
+  const void* hidden_norm; /* [H] */
+  const void* final_norm;  /* [H] */
+  const void* embed;       /* [V, H] token embeddings of the block */
+  const void* unembed;     /* [V, H] */
+  const dflash_layer_weights* layers; /* (host) array of n_layers */
+} dflash_weights;
+
+typedef struct dflash_counters {
+  int64_t rounds;       /* proposals made */
+  int64_t proposed;     /* tokens proposed */
+  int64_t accepted;     /* tokens accepted by dflash_verify (reads device memory: synchronises) */
+  int64_t flushes;      /* context-only forwards */
+  int64_t flushed_rows; /* feature rows written to the cache */
+} dflash_counters;
+
+/* Message of the calling thread's last failed call ("" if none). */
+DFLASH_API const char* dflash_last_error(void);
+/* ABI version (major * 100 + minor). */
+DFLASH_API int dflash_version(void);
+
+/* Validates the config and weight geometry and builds the model.  *out is
+ * owned by the caller and released with dflash_model_destroy.
+ * Errors: INVALID_ARG, SHAPE (out-of-bounds config, e.g. block_size outside
+ * 2..512 or a head geometry that does not divide), OOM, CUDA. */
+DFLASH_API int dflash_model_create(const dflash_config* cfg /*host*/, const dflash_weights* w /*host*/,
+                        dflash_model** out /*host*/);
+DFLASH_API int dflash_model_destroy(dflash_model* m);
+
+/* blockSize - 1 (dflash.go draftLimit); negative status on a null model. */
+DFLASH_API int dflash_draft_limit(const dflash_model* m);
+
+/* Reads (synchronously) and clears the model's device error word: 0 if no
+ * kernel saw a bad input since the last call, else DFLASH_ERR_DEVICE with
+ * the reason in dflash_last_error (token id out of range, ...). */
+DFLASH_API int dflash_device_status(dflash_model* m);
+
+/* Opens a session whose cache already holds `restored_offset` context rows
+ * (dflash.go open: ctxOffset = the caches' restored offset; the rows are
+ * supplied with dflash_kv_import).  max_ctx bounds the context rows the
+ * session may ever hold (its cache holds max_ctx + block_size slots, or a
+ * ring of window + block_size slots when the draft has a window).
+ * stream: a cudaStream_t (NULL = legacy default stream). */
+DFLASH_API int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void* stream,
+                dflash_session** out /*host*/);
+
+/* dflash.go committed: `features` holds n_rows target feature rows
+ * [n_rows, K*H_t] (row_stride elements apart) for tokens at positions
+ * position..position+n_rows-1.  Rows the session already holds (a
+ * restored prefix) are skipped; start = F + P - position < 0 is a context
+ * gap (DFLASH_ERR_CONTEXT_GAP, nothing changes).  New rows are staged (a
+ * device copy made on the stream, so `features` may be reused once the
+ * stream reaches this call); when the held rows reach
+ * DFLASH_PENDING_FLUSH_TOKENS they are flushed in one context-only forward.
+ * Errors: INVALID_ARG, CONTEXT_GAP, CAPACITY (F + P + new rows > max_ctx). */
+DFLASH_API int dflash_committed(dflash_session* s, const void* features, int64_t row_stride, int32_t n_rows,
+                     int64_t position);
+
+/* dflash.go flush: rewinds each session's outstanding block, then writes all
+ * held rows in one batched context-only forward.  When the draft has a
+ * window, rows that no later query can see (slot <= F_new - W) are dropped
+ * before aux_hidden_norms and fc (Laguna PR), while F still advances past
+ * them. */
+DFLASH_API int dflash_flush(dflash_session* const* s /*host [batch]*/, int32_t batch);
+/* dflash.go settle: the same as flushing the one session. */
+DFLASH_API int dflash_settle(dflash_session* s);
+
+/* dflash.go commitBlock: if a block is outstanding, rewind it (the cache
+ * keeps only context rows; the block's K/V slots become free).  Every write
+ * path (committed, flush, propose) runs this first. */
+DFLASH_API int dflash_commit_block(dflash_session* const* s /*host [batch]*/, int32_t batch);
+
+/* dflash.go propose + selectBlock, batched.  n = min(max_tokens, B_s - 1).
+ * A session gets out_n[b] = 0 (the pages' nil) when n <= 0 or it has no
+ * context yet (F + P == 0); the others draft n tokens:
+ *   commitBlock; the held rows become context (written first, at slots
+ *   F..F+P-1); the block [current[b], mask x n] runs at positions F..F+n;
+ *   rows 1..n are unembedded; temperature 0 takes the argmax, T > 0 draws
+ *   argmax(l/T + Gumbel) with Philox4x32-10 keyed by `seed` at counter
+ *   (v, row | 0 << 16, b, round).
+ * current: [batch] int32.  Outputs (device): out_tokens [batch, n] int32,
+ * out_q [batch, n] fp32 (probability of each token under softmax(l/T); 1 at
+ * T = 0), out_logits [batch, n, V] fp32 or NULL.  out_n: (host) [batch].
+ * The session keeps the logits, log-sum-exp and tokens for dflash_verify. */
+DFLASH_API int dflash_propose(dflash_session* const* s /*host [batch]*/, int32_t batch, const int32_t* current,
+                   int32_t max_tokens, float temperature, uint64_t seed, uint64_t round, int32_t* out_tokens,
+                   float* out_q, float* out_logits, int32_t* out_n /*host*/);
+
+/* Speculative verification of each session's last proposal.
+ * target_logits [batch, n+1, V] (fp32 or bf16 per logits_dtype): row r
+ * scores the token after [current, d_1..d_r].  draft_tokens [batch, n]: the
+ * tokens under test (normally the proposal; tests may force others).
+ * T == 0: accept while argmax(row i-1) == d_i; bonus = argmax(row a).
+ * T > 0: accept d_i iff u_i * q_i(d_i) < p_i(d_i), u_i uniform from stream 1;
+ * at the first rejection the bonus is drawn from max(0, p_i - q_i) (from p_i
+ * if that is all zero), after n acceptances from p of row n (stream 2).
+ * q_i is the proposal's distribution softmax(l_i / T_propose) (one-hot of
+ * the proposed token if that proposal was greedy).
+ * Outputs: out_accept [batch] int32 in 0..n, out_bonus [batch] int32.
+ * Errors: STATE if a session has no proposal with this n. */
+DFLASH_API int dflash_verify(dflash_session* const* s /*host [batch]*/, int32_t batch, const void* target_logits,
+                  int32_t logits_dtype, const int32_t* draft_tokens, int32_t n, float temperature, uint64_t seed,
+                  uint64_t round, int32_t* out_accept, int32_t* out_bonus);
+
+/* dflash.go close: flush, then release the session (synchronises its stream). */
+DFLASH_API int dflash_close(dflash_session* s);
+
+DFLASH_API int dflash_stats(const dflash_session* s, dflash_counters* out /*host*/);
+
+/* Host view of the cursors: F (ctxOffset), P (pendingCount), outstanding block. */
+DFLASH_API int dflash_session_state(const dflash_session* s, int64_t* ctx_offset /*host*/, int32_t* pending /*host*/,
+                         int32_t* block_outstanding /*host*/);
+
+/* Copies context rows [first_slot, first_slot + n_rows) of one layer out of
+ * / into the session cache.  k, v: [Hkv, n_rows, d] in the storage type.
+ * Rows must lie below F + block_size (and, with a window, inside the ring).
+ * Used for checkpoint / resume (restored prefixes) and inspection. */
+DFLASH_API int dflash_kv_export(const dflash_session* s, int32_t layer, int64_t first_slot, int32_t n_rows, void* k_out,
+                     void* v_out);
+DFLASH_API int dflash_kv_import(dflash_session* s, int32_t layer, int64_t first_slot, int32_t n_rows, const void* k_in,
+                     const void* v_in);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

@@ -1,0 +1,346 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on
+the same seeded inputs, at sizes the oracle finishes in seconds that still
+span several GEMM tiles, ragged vocabulary tails, GQA groups and the window
+ring."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+from oracle import dflash_oracle as O
+from synthetic.target import SyntheticTarget
+from tests.gpu_util import (MARGIN, TOL_LOGITS, TOL_Q, Pair, assert_tokens, export_kv, lib, oracle_scores)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny_fp32", "small_bf16", "small_laguna_bf16"]
+
+
+@pytest.fixture(scope="module")
+def D():
+    return lib()
+
+
+@pytest.fixture(scope="module", params=SMALL)
+def pair(request):
+    return Pair(S.CONFIGS[request.param])
+
+
+def _oracle_session(p, feats):
+    s = O.OracleSession(p.oracle)
+    s.committed(feats, 0)
+    return s
+
+
+@pytest.mark.parametrize("rows", [37, 300])
+def test_flush_writes_oracle_kv(D, pair, rows):
+    """Context-only forward: every cached K/V row equals the oracle's row at
+    its slot (rows no query can see are dropped under a window)."""
+    cfg = pair.cfg
+    f_np, f = pair.feats(rows, seed=1)
+    s = D.dflash_open(pair.model, max_ctx=1024)
+    D.dflash_committed(s, f, 0)
+    D.dflash_flush([s])
+    assert D.dflash_session_state(s) == (rows, 0, False)
+    os_ = _oracle_session(pair, f_np)
+    os_.flush()
+    lo = max(0, rows - cfg.window + 1) if cfg.window else 0
+    tol = TOL_LOGITS[cfg.dtype]
+    for l in range(cfg.n_layers):
+        k, v = export_kv(D, s, cfg, l, lo, rows - lo)
+        ok = np.stack([os_.cache[j][0][l] for j in range(lo, rows)], axis=1)
+        ov = np.stack([os_.cache[j][1][l] for j in range(lo, rows)], axis=1)
+        assert np.max(np.abs(k - ok)) <= tol and np.max(np.abs(v - ov)) <= tol
+        if cfg.dtype == "bf16":   # storage values agree except for rare rounding-boundary flips
+            assert np.mean(k != ok) < 0.02 and np.mean(v != ov) < 0.02
+    D.dflash_close(s)
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_propose_matches_oracle(D, pair, T):
+    """Two rounds: propose over held rows, then commit more rows (rewinding
+    the block) and propose again.  Logits, tokens and q against the oracle."""
+    cfg = pair.cfg
+    n = cfg.block_size - 1
+    V = cfg.vocab
+    f_np, f = pair.feats(90, seed=2)
+    s = D.dflash_open(pair.model, max_ctx=1024)
+    D.dflash_committed(s, f[:80], 0)
+    os_ = _oracle_session(pair, f_np[:80])
+    cur = torch.tensor([5], dtype=torch.int32, device="cuda")
+    tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+    lg = torch.empty((1, n, V), dtype=torch.float32, device="cuda")
+    for rnd in range(2):
+        if rnd == 1:
+            D.dflash_committed(s, f[80:90], 80)
+            os_.committed(f_np[80:90], 80)
+        out_n = D.dflash_propose([s], cur, 100, T, 1234, rnd, tok, q, lg)
+        assert out_n == [n]
+        ref = os_.propose(5, 100, T, 1234, rnd)
+        torch.cuda.synchronize()
+        g_lg = lg[0].double().cpu().numpy()
+        err = np.max(np.abs(g_lg - ref["logits"]))
+        assert err <= TOL_LOGITS[cfg.dtype], err
+        _, margins = oracle_scores(ref["logits"], T, 1234, rnd, 0)
+        g_tok = tok[0].cpu().numpy()
+        assert_tokens(g_tok, ref["tokens"], margins)
+        same = g_tok == ref["tokens"]
+        assert np.max(np.abs(q[0].cpu().numpy()[same] - ref["q"][same])) <= TOL_Q
+        assert D.dflash_session_state(s) == (os_.F, 0, True)
+    D.dflash_device_status(pair.model)
+    D.dflash_close(s)
+
+
+def test_nil_proposals(D):
+    p = Pair(S.CONFIGS["tiny_fp32"])
+    s = D.dflash_open(p.model, max_ctx=64)
+    cur = torch.tensor([1], dtype=torch.int32, device="cuda")
+    tok = torch.empty((1, 7), dtype=torch.int32, device="cuda")
+    q = torch.empty((1, 7), dtype=torch.float32, device="cuda")
+    assert D.dflash_propose([s], cur, 4, 0.0, 0, 0, tok, q) == [0]      # nothing committed
+    _, f = p.feats(3)
+    D.dflash_committed(s, f, 0)
+    assert D.dflash_propose([s], cur, 0, 0.0, 0, 0, tok, q) == [0]      # n <= 0
+    assert D.dflash_propose([s], cur, 3, 0.0, 0, 0, tok, q) == [3]
+    assert D.dflash_draft_limit(p.model) == 7
+    D.dflash_close(s)
+
+
+def test_context_gap_is_refused(D):
+    p = Pair(S.CONFIGS["tiny_fp32"])
+    s = D.dflash_open(p.model, max_ctx=64)
+    _, f = p.feats(10)
+    D.dflash_committed(s, f[:4], 0)
+    with pytest.raises(D.DFlashError) as e:
+        D.dflash_committed(s, f[4:6], 5)
+    assert e.value.status == D.DFLASH_ERR_CONTEXT_GAP
+    assert D.dflash_session_state(s) == (0, 4, False)
+    D.dflash_committed(s, f[2:6], 2)          # rows 2, 3 held already
+    assert D.dflash_session_state(s) == (0, 6, False)
+    with pytest.raises(D.DFlashError) as e:
+        D.dflash_committed(s, p.feats(60)[1], 6)
+    assert e.value.status == D.DFLASH_ERR_CAPACITY
+    D.dflash_close(s)
+
+
+def test_pending_rows_flush_at_256(D):
+    p = Pair(S.CONFIGS["tiny_fp32"])
+    s = D.dflash_open(p.model, max_ctx=1024)
+    _, f = p.feats(300)
+    D.dflash_committed(s, f[:255], 0)
+    assert D.dflash_session_state(s) == (0, 255, False)
+    D.dflash_committed(s, f[255:256], 255)
+    assert D.dflash_session_state(s) == (256, 0, False)
+    D.dflash_committed(s, f[256:], 256)
+    assert D.dflash_session_state(s) == (256, 44, False)
+    D.dflash_close(s)
+
+
+@pytest.mark.parametrize("cfg_name", ["tiny_fp32", "small_bf16"])
+def test_incremental_flush_is_bit_identical(D, cfg_name):
+    """A context entry depends only on its own features: flushing in pieces
+    gives the same cache bytes as one flush."""
+    p = Pair(S.CONFIGS[cfg_name])
+    cfg = p.cfg
+    _, f = p.feats(120, seed=4)
+    a = D.dflash_open(p.model, max_ctx=512)
+    D.dflash_committed(a, f, 0)
+    D.dflash_flush([a])
+    b = D.dflash_open(p.model, max_ctx=512)
+    for lo, hi in [(0, 1), (1, 9), (9, 70), (70, 120)]:
+        D.dflash_committed(b, f[lo:hi], lo)
+        D.dflash_flush([b])
+    for l in range(cfg.n_layers):
+        ka, va = export_kv(D, a, cfg, l, 0, 120)
+        kb, vb = export_kv(D, b, cfg, l, 0, 120)
+        assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    D.dflash_close(a)
+    D.dflash_close(b)
+
+
+@pytest.mark.parametrize("cfg_name", ["tiny_fp32", "small_bf16"])
+def test_rewind_then_flush_equals_never_drafting(D, cfg_name):
+    p = Pair(S.CONFIGS[cfg_name])
+    cfg = p.cfg
+    _, f = p.feats(40, seed=5)
+    n = cfg.block_size - 1
+    a = D.dflash_open(p.model, max_ctx=256)
+    D.dflash_committed(a, f[:30], 0)
+    cur = torch.tensor([2], dtype=torch.int32, device="cuda")
+    tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+    D.dflash_propose([a], cur, n, 0.0, 0, 0, tok, q)
+    assert D.dflash_session_state(a) == (30, 0, True)
+    D.dflash_committed(a, f[30:33], 30)      # fewer rows than the block: stale block slots stay past F
+    D.dflash_flush([a])
+    assert D.dflash_session_state(a) == (33, 0, False)
+    b = D.dflash_open(p.model, max_ctx=256)
+    D.dflash_committed(b, f[:33], 0)
+    D.dflash_flush([b])
+    for l in range(cfg.n_layers):
+        ka, va = export_kv(D, a, cfg, l, 0, 33)
+        kb, vb = export_kv(D, b, cfg, l, 0, 33)
+        assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    D.dflash_close(a)
+    D.dflash_close(b)
+
+
+def test_tensor_core_gemm_matches_cuda_core_gemm(D):
+    """The tcgen05 path and the CUDA-core path give the same round."""
+    cfg = S.CONFIGS["small_bf16"]
+    w = S.make_weights(cfg, seed=0)
+    outs = []
+    for flags in (0, D.DFLASH_FLAG_SIMT_GEMM):
+        p = Pair(cfg, weights=w, flags=flags)
+        _, f = p.feats(50, seed=6)
+        s = D.dflash_open(p.model, max_ctx=256)
+        D.dflash_committed(s, f, 0)
+        n = cfg.block_size - 1
+        cur = torch.tensor([7], dtype=torch.int32, device="cuda")
+        tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+        q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+        lg = torch.empty((1, n, cfg.vocab), dtype=torch.float32, device="cuda")
+        D.dflash_propose([s], cur, n, 0.0, 0, 0, tok, q, lg)
+        torch.cuda.synchronize()
+        outs.append(lg.double().cpu().numpy())
+        D.dflash_close(s)
+    assert np.max(np.abs(outs[0] - outs[1])) < 1e-2
+
+
+@pytest.mark.parametrize("cfg_name", ["tiny_fp32", "small_bf16"])
+@pytest.mark.parametrize("T", [0.0, 0.7])
+def test_batched_propose_and_verify(D, cfg_name, T):
+    """Three sessions with different context lengths in one batched propose
+    and verify; each against its own oracle session (seq id = batch index)."""
+    p = Pair(S.CONFIGS[cfg_name])
+    cfg = p.cfg
+    n = cfg.block_size - 1
+    V = cfg.vocab
+    lens = [20, 75, 130]
+    sess, oss = [], []
+    for b, L in enumerate(lens):
+        f_np, f = p.feats(L, seed=10 + b)
+        s = D.dflash_open(p.model, max_ctx=512)
+        D.dflash_committed(s, f, 0)
+        o = O.OracleSession(p.oracle, seq=b)
+        o.committed(f_np, 0)
+        sess.append(s)
+        oss.append(o)
+    cur_np = np.array([3, 9, 1], dtype=np.int32)
+    cur = torch.from_numpy(cur_np).cuda()
+    tok = torch.empty((3, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((3, n), dtype=torch.float32, device="cuda")
+    lg = torch.empty((3, n, V), dtype=torch.float32, device="cuda")
+    assert D.dflash_propose(sess, cur, n, T, 77, 5, tok, q, lg) == [n] * 3
+    refs = [o.propose(int(c), n, T, 77, 5) for o, c in zip(oss, cur_np)]
+    torch.cuda.synchronize()
+    for b in range(3):
+        assert np.max(np.abs(lg[b].double().cpu().numpy() - refs[b]["logits"])) <= TOL_LOGITS[cfg.dtype]
+        _, margins = oracle_scores(refs[b]["logits"], T, 77, 5, b)
+        assert_tokens(tok[b].cpu().numpy(), refs[b]["tokens"], margins)
+    # verify the oracle's proposal tokens on both sides against synthetic target logits
+    d_np = np.stack([r["tokens"] for r in refs]).astype(np.int32)
+    tl_np = S.make_target_logits(3, n + 1, V, d_np, seed=3, std=1.0, boost=4.0)
+    acc = torch.empty(3, dtype=torch.int32, device="cuda")
+    bon = torch.empty(3, dtype=torch.int32, device="cuda")
+    D.dflash_verify(sess, torch.from_numpy(tl_np).cuda(), torch.from_numpy(d_np).cuda(), n, T, 99, 5, acc, bon)
+    torch.cuda.synchronize()
+    for b in range(3):
+        a_ref, b_ref = oss[b].verify(tl_np[b].astype(np.float64), d_np[b], T, 99, 5)
+        a_gpu, b_gpu = int(acc[b]), int(bon[b])
+        if T == 0:
+            assert (a_gpu, b_gpu) == (a_ref, b_ref)
+        else:
+            # decisions within 1e-3 of the acceptance threshold may flip
+            close = _near_threshold(oss[b], tl_np[b], d_np[b], T, 99, 5, b)
+            if not close:
+                assert a_gpu == a_ref
+                if a_gpu == a_ref:
+                    assert b_gpu == b_ref or _bonus_margin_small(oss[b], tl_np[b], d_np[b], a_ref, T, 99, 5, b)
+    D.dflash_device_status(p.model)
+    for s in sess:
+        D.dflash_close(s)
+
+
+def _near_threshold(o, tl, d, T, seed, rnd, seq):
+    n = len(d)
+    for i in range(1, n + 1):
+        p = O.softmax(tl[i - 1].astype(np.float64) / T)
+        q = O.proposal_distribution(o.last["logits"][i - 1], o.last["temperature"], o.last["tokens"][i - 1])
+        r = O.uniform_open(O.random_u32(seed, rnd, O.STREAM_ACCEPT, seq, i, 0))
+        x, y = r * q[d[i - 1]], p[d[i - 1]]
+        if abs(x - y) <= 1e-3 * max(abs(y), 1e-30):
+            return True
+        if not x < y:
+            return False
+    return False
+
+
+def _bonus_margin_small(o, tl, d, a, T, seed, rnd, seq):
+    n = len(d)
+    row = a if a == n else a
+    p = O.softmax(tl[row].astype(np.float64) / T)
+    if a < n:
+        q = O.proposal_distribution(o.last["logits"][a], o.last["temperature"], o.last["tokens"][a])
+        res = np.maximum(p - q, 0)
+        w = res if res.sum() > 0 else p
+        prow = a + 1
+    else:
+        w, prow = p, n + 1
+    with np.errstate(divide="ignore"):
+        s = np.log(w) + O.gumbel(seed, rnd, O.STREAM_BONUS, seq, prow, np.arange(len(p)))
+    top = np.sort(s)[-2:]
+    return top[1] - top[0] < MARGIN
+
+
+def test_greedy_speculative_output_equals_greedy_decode(D):
+    """The tiny fp32 draft on the GPU drives greedy rounds against the
+    synthetic 2-layer target for 128 tokens: the output equals plain greedy
+    decoding of the target, with the real draft and with forced accept
+    lengths 0, 1, 2 and full."""
+    p = Pair(S.CONFIGS["tiny_fp32"])
+    cfg = p.cfg
+    n = cfg.block_size - 1
+    tgt = SyntheticTarget(seed=1)
+    prompt = list(S.rng_for(0, "prompt").integers(0, 32, size=8))
+    ref = tgt.greedy_decode(prompt, 200)
+    plan = [0, 1, 2, n]
+    for forced in (False, True):
+        tgt.reset()
+        logits, taps = tgt.forward(prompt, 0)
+        s = D.dflash_open(p.model, max_ctx=512)
+        D.dflash_committed(s, torch.from_numpy(taps).cuda(), 0)
+        out = [int(np.argmax(logits[-1]))]
+        pos = len(prompt)
+        cur = torch.empty(1, dtype=torch.int32, device="cuda")
+        tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+        q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+        acc = torch.empty(1, dtype=torch.int32, device="cuda")
+        bon = torch.empty(1, dtype=torch.int32, device="cuda")
+        rnd = 0
+        while len(out) < 128:
+            cur.fill_(out[-1])
+            assert D.dflash_propose([s], cur, n, 0.0, 0, rnd, tok, q) == [n]
+            d = tok[0].cpu().tolist()
+            k = None
+            if forced:
+                k = plan[rnd % len(plan)]
+                t = len(out)
+                d = [ref[t + j] for j in range(k)] + ([(ref[t + k] + 1) % 32] if k < n else [])
+                d += [0] * (n - len(d))
+            tl, tt = tgt.forward([out[-1]] + d, pos)
+            D.dflash_verify([s], torch.from_numpy(tl[None]).cuda(), torch.tensor([d], dtype=torch.int32).cuda(),
+                            n, 0.0, 0, rnd, acc, bon)
+            a, b = int(acc[0]), int(bon[0])
+            if forced:
+                assert a == k and b == ref[len(out) + a]
+            tgt.trim(pos + a + 1)
+            D.dflash_committed(s, torch.from_numpy(tt[:a + 1]).cuda(), pos)
+            out += d[:a] + [b]
+            pos += a + 1
+            rnd += 1
+        assert out[:128] == ref[:128]
+        st = D.dflash_stats(s)
+        assert st["rounds"] == rnd and st["proposed"] == rnd * n
+        D.dflash_close(s)
