@@ -1,0 +1,518 @@
+#!/usr/bin/env python3
+"""Throughput of the DFlash draft round on GB300.
+
+One step is one whole round of the hot path for one sequence of the
+Qwen3-8B-shaped bf16 draft (5 layers, hidden 4096, 32 Q / 8 KV heads of 128,
+SwiGLU 12288, vocab 151936, block 16 so n = 15, temperature 1.0):
+
+  committed   4 new target feature rows [4, 5 x 4096] (the steady-state
+              accepted + bonus rows of a round), appended at the frontier
+  propose     commit_block rewind, the 4 held rows pass aux norms / fc /
+              hidden norm / per-layer K/V into the cache, the 16-row block
+              forward against the context, unembedding of rows 1..15 and
+              one batched Gumbel-max draw
+  verify      accept length and bonus token from target logits [16, 151936]
+
+The context starts at 4096 - 4 (W + K/2) rows filled by a real flush, so the
+mean context over the K timed steps is 4096.  Weights (3.4 GB) are read every
+step, far more than the 129 MB L2, so no L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (under torchrun): N independent replicas, one sequence per GPU, no
+collective on the data path (weak scaling); rank 0 prints the line with the
+max time over ranks.  --impl reference times the CPU oracle (this method has
+no other reference implementation) on bounded samples of the same round.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft rounds/sec & proposed tok/s (bs1, bs64); flush rows/s; % HBM roofline"
+UNIT = "draft rounds/s"
+CFG_NAME = "qwen3_8b_bf16"
+CTX = 4096
+P_ROWS = 4
+TEMP = 1.0
+SEED = 20260201
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# ranks (replicas only: the barrier and the max over ranks are the only
+# cross-rank traffic)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r for r in csv.reader(io.StringIO(open(self.path).read())) if len(r) >= 9]
+        os.unlink(self.path)
+        sm, smax, reasons, samples = [], None, set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            samples += 1
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": samples}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def traffic_from_profile(kernel_src: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "k_gemm_tc_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    digest = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    if kv.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def round_bytes(cfg, ctx, P):
+    """Algorithmic bytes of one bs1 round: every weight read once, the context
+    K/V read once per layer, the features read once, the new K/V written once,
+    the logits written and read once, the target logits read once."""
+    H, I, V = cfg.hidden, cfg.intermediate, cfg.vocab
+    qkv = cfg.qkv_rows * H
+    per_layer = qkv + H * cfg.n_q_heads * cfg.head_dim + 3 * H * I
+    weights = 2 * (cfg.n_layers * per_layer + V * H + (H * cfg.feature_width if P else 0))
+    nb = cfg.block_size
+    kv_row = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * cfg.n_layers
+    kv = (ctx + nb) * kv_row + (P + nb) * kv_row
+    feats = P * cfg.feature_width * 2
+    logits = (nb - 1) * V * 4 * 2 + nb * V * 4
+    return weights + kv + feats + logits
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def gpu_weights(cfg, seed, device):
+    import torch
+
+    import synthetic as S
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out = {}
+    for name, shape in S.weight_shapes(cfg).items():
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 0.02
+        if name.endswith("norm") or name == "aux_norms":
+            x += 1.0
+        out[name] = x.to(torch.bfloat16)
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import block_diffusion_speculative_flush_gb300 as D
+    import synthetic as S
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist_init(world, "nccl")
+    cfg = S.CONFIGS[CFG_NAME]
+    K, W = args.steps, args.warmup
+    n = cfg.block_size - 1
+    V = cfg.vocab
+    stream = torch.cuda.Stream(device=dev)
+    weights = gpu_weights(cfg, SEED + rank, dev)
+    model = D.dflash_model_create(cfg, weights)
+    start_ctx = CTX - P_ROWS * (W + K // 2)
+    assert start_ctx > 0, "too many steps for the 4096-row mean context"
+    max_ctx = start_ctx + P_ROWS * (W + K + 8)
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 1000 + rank)
+    sessions = []
+    with torch.cuda.stream(stream):
+        for _ in range(2):   # one for the kernel-only loop, one for the end-to-end loop
+            s = D.dflash_open(model, max_ctx=max_ctx, stream=stream)
+            for lo in range(0, start_ctx, 1024):
+                hi = min(start_ctx, lo + 1024)
+                f = torch.randn((hi - lo, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+                D.dflash_committed(s, f, lo)
+                del f
+            D.dflash_flush([s])
+            sessions.append(s)
+        feats = torch.randn((W + K, P_ROWS, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+        tl = (torch.randn((1, n + 1, V), generator=g, device=dev) * 3.0).contiguous()
+        cur = torch.full((1,), 17, dtype=torch.int32, device=dev)
+        tok = torch.empty((1, n), dtype=torch.int32, device=dev)
+        q = torch.empty((1, n), dtype=torch.float32, device=dev)
+        acc = torch.empty(1, dtype=torch.int32, device=dev)
+        bon = torch.empty(1, dtype=torch.int32, device=dev)
+    stream.synchronize()
+
+    def step(s, i, f, logits):
+        D.dflash_committed(s, f, start_ctx + P_ROWS * i)
+        D.dflash_propose([s], cur, n, TEMP, SEED, i, tok, q)
+        D.dflash_verify([s], logits, tok, n, TEMP, SEED, i, acc, bon)
+
+    # ---- kernel-only timed region: inputs resident in HBM ----
+    sa = sessions[0]
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(sa, i, feats[i], tl)
+    stream.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    D.dflash_timing_enable(model, True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(W, W + K):
+            step(sa, i, feats[i], tl)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    timing = D.dflash_timing_read(model)
+    D.dflash_timing_enable(model, False)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world, dev)
+
+    # ---- end to end through the public API with host buffers ----
+    sb = sessions[1]
+    feats_h = feats.cpu().pin_memory()
+    tl_h = tl.cpu().pin_memory()
+    f_dev = torch.empty((P_ROWS, cfg.feature_width), dtype=torch.bfloat16, device=dev)
+    tl_dev = torch.empty_like(tl)
+    tok_h = torch.empty((1, n), dtype=torch.int32).pin_memory()
+    acc_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    bon_h = torch.empty(1, dtype=torch.int32).pin_memory()
+
+    def e2e_step(i):
+        f_dev.copy_(feats_h[i], non_blocking=True)
+        tl_dev.copy_(tl_h, non_blocking=True)
+        step(sb, i, f_dev, tl_dev)
+        tok_h.copy_(tok, non_blocking=True)
+        acc_h.copy_(acc, non_blocking=True)
+        bon_h.copy_(bon, non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            e2e_step(i)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(W, W + K):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+    barrier(world)
+    e2e_max = max_over_ranks(e2e_s, world, dev)
+    D.dflash_device_status(model)
+    h2d = P_ROWS * cfg.feature_width * 2 + tl.numel() * 4
+    d2h = n * 4 + 4 + 4
+
+    result = None
+    if rank == 0:
+        peaks, peak_kind = measured_peaks()
+        gt = timing.get("gemm_tc", {})
+        achieved = gt["bytes"] / (gt["total_ms"] * 1e-3) / 1e9 if gt.get("total_ms") else None
+        launches = gt.get("launches", 0)
+        traffic = traffic_from_profile(os.path.join(ROOT, "block_diffusion_speculative_flush_gb300", "csrc",
+                                                    "gemm_tc.cu"))
+        value = world * K / (ms_max * 1e-3)
+        rb = round_bytes(cfg, CTX, P_ROWS)
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init draft weights, N(0,1) features, "
+                                                          "N(0,3) target logits)",
+            "config": {"workload": "qwen3_8b_bf16 draft round, bs1, block 16 (n=15), mean ctx 4096, "
+                                   "4 committed rows per round, T=1.0",
+                       "model": "Qwen3-8B-shaped DFlash draft (5 layers, H 4096, 32/8 heads x 128, I 12288, "
+                                "V 151936)",
+                       "global_batch": world, "seq_len": CTX, "parallelism": f"replicas x{world}",
+                       "l2": "no flush: 3.4 GB of weights streamed per step (L2 is 129 MB)"},
+            "proposed_tok_s": round(value * n, 1),
+            "round_roofline": {"bound": "hbm", "algorithmic_bytes": rb,
+                               "achieved_gbs": round(rb / (ms_max / K * 1e-3) / 1e9, 1),
+                               "peak_gbs": peaks["hbm_gbs"],
+                               "frac": round(rb / (ms_max / K * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+            "roofline": {"kernel": "k_gemm_tc (tcgen05 weight-streaming GEMM)", "bound": "hbm",
+                         "achieved": round(achieved, 1) if achieved else None, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
+                         "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": round(gt["bytes"] / launches) if launches else None,
+                         "traffic": traffic, "launches": launches},
+            "kernel_classes": {k: {"launches": v["launches"], "ms_per_step": round(v["total_ms"] / K, 4),
+                                   "gbs": round(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 1)
+                                   if v["total_ms"] else None}
+                               for k, v in timing.items()},
+            "gpu_launches": int(timing.get("all", {}).get("launches", 0)),
+            "clocks": clk,
+            "e2e": {"value": round(world * K / e2e_max, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+        }
+    # weights for the CPU baseline are read before the GPU state goes away
+    host_w = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_w = {k: v.float().cpu().numpy() for k, v in weights.items()}
+    for s in sessions:
+        D.dflash_close(s)
+    del model, weights
+    torch.cuda.empty_cache()
+    if result is not None and host_w is not None:
+        result["cpu_baseline"] = cpu_baseline(cfg, host_w)
+    return result
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle: baseline leg and reference arm
+# ---------------------------------------------------------------------------
+def _oracle_setup(cfg, host_w):
+    import numpy as np
+
+    import synthetic as S
+    from oracle import dflash_oracle as O
+    d = O.OracleDraft(cfg, host_w)
+    Kc = S.make_kv(cfg, CTX, SEED, "ctx_k").astype(np.float64)
+    Vc = S.make_kv(cfg, CTX, SEED, "ctx_v").astype(np.float64)
+    cache = {s: (Kc[:, :, s, :], Vc[:, :, s, :]) for s in range(CTX)}
+    feats = S.make_features(cfg, P_ROWS, seed=SEED)
+    n = cfg.block_size - 1
+    tl = np.random.default_rng(SEED).standard_normal((n + 1, cfg.vocab)) * 3.0
+    return O, d, cache, feats, tl
+
+
+def _threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count() or 1])
+    except ImportError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, host_w):
+    """One whole round of the oracle on the host: 4 held rows through the
+    context path, the 16-row block at ctx 4096 (context K/V seeded directly),
+    the unembedding, the draw, and the verify."""
+    O, d, cache, feats, tl = _oracle_setup(cfg, host_w)
+    n = cfg.block_size - 1
+    s = O.OracleSession(d, restored_offset=CTX - P_ROWS, restored_cache={k: v for k, v in cache.items()
+                                                                          if k < CTX - P_ROWS})
+    s.committed(feats, CTX - P_ROWS)
+    t0 = time.perf_counter()
+    out = s.propose(17, n, TEMP, SEED, 0)
+    s.verify(tl, out["tokens"], TEMP, SEED, 0)
+    dt = time.perf_counter() - t0
+    return {"value": round(1.0 / dt, 5), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+            "sample": f"one whole round on the host ({dt:.1f} s): 4 held rows, 16-row block at ctx 4096 "
+                      "(context K/V seeded directly), unembedding, draw and verify; float64 numpy"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host's cores.  The round is cut
+    into its oracle calls in order (context hidden rows, then per layer the
+    new rows' K/V and the block layer, then vocabulary slices of the
+    unembedding, then the draw and the verify); the K timed steps share those
+    calls out in order, so together they run exactly one round and
+    value = 1 / (sum of the K step times) rounds/s.  The W warm-up steps run
+    one more round the same way.  The whole run costs about two rounds."""
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import synthetic as S
+    cfg = S.CONFIGS[CFG_NAME]
+    rng = np.random.default_rng(SEED)
+    host_w = {}
+    for name, shape in S.weight_shapes(cfg).items():
+        x = rng.standard_normal(shape, dtype=np.float32) * np.float32(0.02)
+        if name.endswith("norm") or name == "aux_norms":
+            x += np.float32(1.0)
+        host_w[name] = S.to_dtype_values(x, "bf16")
+    O, d, cache, feats, tl = _oracle_setup(cfg, host_w)
+    L, n, V = cfg.n_layers, cfg.block_size - 1, cfg.vocab
+    F0 = CTX - P_ROWS
+    ctx_pos = np.arange(CTX, dtype=np.float64)
+    slots = np.arange(F0, CTX)
+    tokens = [17] + [cfg.mask_token] * n
+    pos = CTX + np.arange(n + 1, dtype=np.float64)
+    ctx_k = [np.stack([cache[s][0][l] for s in range(F0)]) for l in range(L)]
+    ctx_v = [np.stack([cache[s][1][l] for s in range(F0)]) for l in range(L)]
+    st = {}
+
+    def start(rnd):
+        st["rnd"] = rnd
+        st["hid"] = d.context_hidden(feats)
+        st["h"] = d.w.rows("embed", tokens)
+        st["logits"] = np.zeros((n, V))
+
+    def layer(l):
+        ck, cv = d.context_layer_kv(l, st["hid"], slots)
+        st["h"] = d.block_layer(l, st["h"], pos, np.concatenate([ctx_k[l], ck]), np.concatenate([ctx_v[l], cv]),
+                                ctx_pos)
+
+    def unembed(j, J):
+        lo, hi = j * V // J, (j + 1) * V // J
+        st["logits"][:, lo:hi] = d.unembed(st["h"][1:], lo, hi)
+
+    def finish():
+        toks, _, _ = O.sample_rows(st["logits"], TEMP, SEED, st["rnd"], 0)
+        O.verify(tl, toks, st["logits"], toks, TEMP, TEMP, SEED, st["rnd"], 0)
+
+    J = 8
+    calls = [start] + [(lambda l=l: layer(l)) for l in range(L)] + [(lambda j=j: unembed(j, J)) for j in range(J)] \
+        + [finish]
+
+    def run_round(rnd, steps):
+        """Runs one round as `steps` steps; returns each step's seconds."""
+        st["rnd_arg"] = rnd
+        times = []
+        c = 0
+        for k in range(steps):
+            hi = (k + 1) * len(calls) // steps
+            t0 = time.perf_counter()
+            while c < hi:
+                f = calls[c]
+                f(rnd) if f is start else f()
+                c += 1
+            times.append(time.perf_counter() - t0)
+        return times
+
+    run_round(0, max(1, args.warmup))
+    times = run_round(1, args.steps)
+    per_round = sum(times)
+    value = 1.0 / per_round
+    sample = (f"the {args.steps} timed steps together run one whole round ({per_round:.1f} s): 4 held rows, "
+              f"16-row block at ctx 4096 (context K/V seeded directly), unembedding, draw and verify, "
+              f"each step a contiguous slice of the round's oracle calls; float64 numpy")
+    return {
+        "metric": METRIC, "value": round(value, 5), "unit": UNIT, "impl": "reference", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_round * 1e3 / args.steps, 2),
+        "ms_per_round": round(per_round * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (random-init draft weights, N(0,1) features, N(0,3) target logits)",
+        "config": {"workload": "qwen3_8b_bf16 draft round, bs1, block 16 (n=15), ctx 4096, "
+                               "4 committed rows per round, T=1.0", "l2": "host run"},
+        "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

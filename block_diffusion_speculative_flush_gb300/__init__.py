@@ -25,7 +25,7 @@ __all__ = [
     "dflash_model_create", "dflash_model_destroy", "dflash_draft_limit", "dflash_device_status", "dflash_open",
     "dflash_committed", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
     "dflash_close", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
-    "dflash_version", "dflash_last_error",
+    "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read",
 ]
 
 
@@ -204,3 +204,16 @@ def dflash_kv_export(session: Session, layer: int, first_slot: int, n_rows: int,
 def dflash_kv_import(session: Session, layer: int, first_slot: int, n_rows: int, k_in: torch.Tensor,
                      v_in: torch.Tensor) -> None:
     _check(lib.dflash_kv_import(session.handle, layer, first_slot, n_rows, _ptr(k_in), _ptr(v_in)))
+
+
+def dflash_timing_enable(model: Model, on: bool) -> None:
+    _check(lib.dflash_timing_enable(model.handle, 1 if on else 0))
+
+
+def dflash_timing_read(model: Model) -> dict:
+    """kernel class -> dict(launches, total_ms, bytes, flops); synchronises."""
+    arr = (_abi.dflash_kernel_time * 16)()
+    n = C.c_int32()
+    _check(lib.dflash_timing_read(model.handle, arr, 16, C.byref(n)))
+    return {arr[i].name.decode(): dict(launches=arr[i].launches, total_ms=arr[i].total_ms, bytes=arr[i].bytes,
+                                       flops=arr[i].flops) for i in range(n.value)}

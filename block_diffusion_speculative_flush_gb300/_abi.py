@@ -49,6 +49,11 @@ class dflash_counters(C.Structure):
                 ("flushes", C.c_int64), ("flushed_rows", C.c_int64)]
 
 
+class dflash_kernel_time(C.Structure):
+    _fields_ = [("name", C.c_char * 24), ("launches", C.c_int64), ("total_ms", C.c_double),
+                ("bytes", C.c_double), ("flops", C.c_double)]
+
+
 P = C.c_void_p
 SessArr = C.POINTER(C.c_void_p)
 
@@ -74,6 +79,8 @@ SIGNATURES = {
     "dflash_session_state": (C.c_int, [P, C.POINTER(C.c_int64), C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "dflash_kv_export": (C.c_int, [P, C.c_int32, C.c_int64, C.c_int32, P, P]),
     "dflash_kv_import": (C.c_int, [P, C.c_int32, C.c_int64, C.c_int32, P, P]),
+    "dflash_timing_enable": (C.c_int, [P, C.c_int32]),
+    "dflash_timing_read": (C.c_int, [P, C.POINTER(dflash_kernel_time), C.c_int32, C.POINTER(C.c_int32)]),
 }
 
 

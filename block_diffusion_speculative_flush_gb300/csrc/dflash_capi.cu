@@ -152,8 +152,15 @@ struct dflash_model {
   bool use_tc = false;
   int32_t* d_err = nullptr;
   TcContext* tc = nullptr;
+  // measurement
+  bool timing = false;
+  int64_t launches = 0;
+  struct Rec { cudaEvent_t e0, e1; int cls; double bytes, flops; };
+  std::vector<Rec> recs;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_pool;
+  size_t ev_used = 0;
   // workspace
-  Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart;
+  Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart, vbonus;
   HostRing ring;
 };
 
@@ -177,6 +184,33 @@ struct dflash_session {
 };
 
 namespace {
+
+// ---------------------------------------------------------------------------
+// measurement: CUDA events around instrumented launches
+// ---------------------------------------------------------------------------
+enum TimeClass { kGemmTc = 0, kGemmSimt, kAttention, kSample, kVerify, kClasses };
+const char* const kClassNames[kClasses] = {"gemm_tc", "gemm_simt", "attention", "sample", "verify"};
+
+struct Timed {
+  dflash_model* m;
+  cudaStream_t st;
+  size_t idx = (size_t)-1;
+  Timed(dflash_model* m_, int cls, double bytes, double flops, cudaStream_t st_) : m(m_), st(st_) {
+    if (!m->timing) return;
+    if (m->ev_used == m->ev_pool.size()) {
+      cudaEvent_t a = nullptr, b = nullptr;
+      if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return;
+      m->ev_pool.push_back({a, b});
+    }
+    auto ev = m->ev_pool[m->ev_used++];
+    idx = m->recs.size();
+    m->recs.push_back(dflash_model::Rec{ev.first, ev.second, cls, bytes, flops});
+    cudaEventRecord(ev.first, st);
+  }
+  ~Timed() {
+    if (idx != (size_t)-1) cudaEventRecord(m->recs[idx].e1, st);
+  }
+};
 
 // ---------------------------------------------------------------------------
 // validation
@@ -211,12 +245,53 @@ int check_config(const dflash_config& c) {
 int gemm(dflash_model* m, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy, int M, int N,
          int K, cudaStream_t st) {
   if (M <= 0) return DFLASH_OK;
+  const double bytes = (double)N * K * m->esz + (double)M * K * m->esz + (double)M * N * 4;
+  Timed tm(m, m->use_tc ? kGemmTc : kGemmSimt, bytes, 2.0 * M * N * K, st);
+  m->launches++;
   if (m->use_tc) {
-    const int rc = tc_gemm(m->tc, X, ldx, W, ldw, Y, ldy, M, N, K, st);
+    const int rc = tc_gemm(m->tc, X, ldx, W, nullptr, ldw, Y, ldy, M, N, K, kF32, st);
     if (rc) return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
   } else {
     launch_gemm_simt(m->dt, X, ldx, W, ldw, Y, ldy, M, N, K, st);
   }
+  return DFLASH_OK;
+}
+
+// h[M][N] = storage(h + X W^T): the residual add after the attention output
+// and after the MLP down projection.
+int gemm_resid(dflash_model* m, const void* X, int64_t ldx, const void* W, void* h, float* tmp, int M, int N, int K,
+               cudaStream_t st) {
+  if (M <= 0) return DFLASH_OK;
+  if (!m->use_tc) {
+    ST_TRY(gemm(m, X, ldx, W, K, tmp, N, M, N, K, st));
+    launch_residual(m->dt, h, tmp, N, M, N, st);
+    m->launches++;
+    return DFLASH_OK;
+  }
+  const double bytes = (double)N * K * 2 + (double)M * K * 2 + (double)M * N * 4;
+  Timed tm(m, kGemmTc, bytes, 2.0 * M * N * K, st);
+  m->launches++;
+  if (tc_gemm(m->tc, X, ldx, W, nullptr, K, h, N, M, N, K, kResidBf16, st))
+    return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
+  return DFLASH_OK;
+}
+
+// a[M][I] = storage(silu(Y Wg^T) * (Y Wu^T)).
+int gemm_swiglu(dflash_model* m, const void* Y, const void* Wg, const void* Wu, void* a, float* tmp, int M, int I,
+                int H, cudaStream_t st) {
+  if (M <= 0) return DFLASH_OK;
+  if (!m->use_tc) {
+    ST_TRY(gemm(m, Y, H, Wg, H, tmp, 2 * I, M, I, H, st));
+    ST_TRY(gemm(m, Y, H, Wu, H, tmp + I, 2 * I, M, I, H, st));
+    launch_swiglu(m->dt, tmp, 2 * I, M, I, I, a, st);
+    m->launches++;
+    return DFLASH_OK;
+  }
+  const double bytes = 2.0 * I * H * 2 + (double)M * H * 2 + (double)M * I * 2;
+  Timed tm(m, kGemmTc, bytes, 4.0 * M * I * H, st);
+  m->launches++;
+  if (tc_gemm(m->tc, Y, H, Wg, Wu, H, a, I, M, I, H, kSwigluBf16, st))
+    return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
   return DFLASH_OK;
 }
 
@@ -294,8 +369,10 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       k1v[j] = F + nrows;
       total += (k1v[j] - k0v[j]) * Hkv;
     }
-    int64_t chunk = align_up(std::max<int64_t>(1, total / std::max(1, 2 * m->num_sms)), 64);
-    chunk = std::min<int64_t>(std::max<int64_t>(chunk, 64), 4096);
+    // about one work item per SM: fewer, longer key ranges keep the split
+    // partials (R x (d + 4) floats per item) small next to the K/V bytes
+    int64_t chunk = align_up(std::max<int64_t>(1, total / std::max(1, m->num_sms)), 64);
+    chunk = std::min<int64_t>(std::max<int64_t>(chunk, 128), 8192);
     for (int j = 0; j < Bc; ++j) {
       const int S = (int)((k1v[j] - k0v[j] + chunk - 1) / chunk);
       ifirst[j] = (int32_t)items.size();
@@ -333,7 +410,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     ST_TRY(m->a.ensure((size_t)Mb * I * es, st));
     ST_TRY(m->z.ensure((size_t)Bc * fw.n * H * es, st));
     const int R = nrows * (Hq / Hkv);
-    ST_TRY(m->apart.ensure(std::max<size_t>(items.size(), 1) * R * (d + 2) * 4, st));
+    ST_TRY(m->apart.ensure(std::max<size_t>(items.size(), 1) * R * (d + 4) * 4, st));
   }
 
   // ---- context path: aux_hidden_norms -> fc -> hidden_norm ----------------
@@ -342,19 +419,30 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
                     c.rms_eps, st);
     ST_TRY(gemm(m, m->u.p, KHt, m->w_fc, KHt, m->fcout.as<float>(), H, Mc, H, KHt, st));
     launch_rmsnorm(m->dt, true, m->fcout.p, Mc, nullptr, H, m->hidden_norm, m->c.p, H, Mc, H, Mc, 0, 0, c.rms_eps, st);
+    m->launches += 2;
   }
-  if (block)
+  if (block) {
     launch_embed(m->dt, m->embed, fw.current, (const int32_t*)(tb + o_map), c.mask_token, V, Bc, nrows, H, m->h.p,
                  m->d_err, st);
+    m->launches++;
+  }
   launch_rope_table(dmeta, M, d, c.rope_theta, m->rope.as<float2>(), st);
+  m->launches++;
   ST_TRY(launch_check("context path"));
 
   AttnParams ap{Hq, Hkv, d, nrows, c.window, c.causal_block, c.n_layers, 0, 1.f / std::sqrt((float)d)};
+  double attn_bytes = 0, attn_flops = 0;  // per layer: K/V read once, Q read, O written
+  for (const AttnItem& it : items) {
+    attn_bytes += (double)(it.k1 - it.k0) * d * 2 * es;
+    attn_flops += 4.0 * (it.k1 - it.k0) * d * nrows * (Hq / Hkv);
+  }
+  attn_bytes += 2.0 * Mb * Hq * d * es;
   const int qd = Hq * d, kd = Hkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& w = m->layers[l];
     // input_layernorm over [context rows ; block rows]
     launch_rmsnorm(m->dt, false, m->c.p, Mc, m->h.p, H, w.in_norm, m->x.p, H, M, H, M, 0, 0, c.rms_eps, st);
+    m->launches++;
     if (block) {
       const void* wq = w.w_qkvg ? w.w_qkvg : w.w_qkv;
       ST_TRY(gemm(m, m->x.p, H, wq, H, m->qkv.as<float>(), m->qkv_cols, M, m->qkv_cols, H, st));
@@ -365,23 +453,27 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     }
     launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, m->rope.as<float2>(), w.q_norm, w.k_norm, Hq,
                     Hkv, d, c.gated_attention, c.rms_eps, tabs, c.n_layers, l, m->Q.p, m->G.as<float>(), st);
+    m->launches++;
     ST_TRY(launch_check("qkv"));
     if (!block) continue;
     ap.layer = l;
-    launch_attention_simt(m->dt, m->Q.p, (const AttnItem*)(tb + o_items), (int)items.size(), tabs, ap,
-                          m->apart.as<float>(), st);
-    launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
-                             (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
-                             m->O.p, st);
+    {
+      Timed tm(m, kAttention, attn_bytes, attn_flops, st);
+      const AttnItem* ditems = (const AttnItem*)(tb + o_items);
+      if (m->dt != DT::BF16 ||
+          !launch_attention_mma(m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), st))
+        launch_attention_simt(m->dt, m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), st);
+      launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
+                               (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
+                               m->O.p, st);
+      m->launches += 2;
+    }
     ST_TRY(launch_check("attention"));
-    ST_TRY(gemm(m, m->O.p, qd, w.w_o, qd, m->tmp.as<float>(), H, Mb, H, qd, st));
-    launch_residual(m->dt, m->h.p, m->tmp.as<float>(), H, Mb, H, st);
+    ST_TRY(gemm_resid(m, m->O.p, qd, w.w_o, m->h.p, m->tmp.as<float>(), Mb, H, qd, st));
     launch_rmsnorm(m->dt, false, m->h.p, Mb, nullptr, H, w.post_norm, m->y.p, H, Mb, H, Mb, 0, 0, c.rms_eps, st);
-    ST_TRY(gemm(m, m->y.p, H, w.w_gate, H, m->tmp.as<float>(), 2 * I, Mb, I, H, st));
-    ST_TRY(gemm(m, m->y.p, H, w.w_up, H, m->tmp.as<float>() + I, 2 * I, Mb, I, H, st));
-    launch_swiglu(m->dt, m->tmp.as<float>(), 2 * I, Mb, I, I, m->a.p, st);
-    ST_TRY(gemm(m, m->a.p, I, w.w_down, I, m->tmp.as<float>(), H, Mb, H, I, st));
-    launch_residual(m->dt, m->h.p, m->tmp.as<float>(), H, Mb, H, st);
+    m->launches++;
+    ST_TRY(gemm_swiglu(m, m->y.p, w.w_gate, w.w_up, m->a.p, m->tmp.as<float>(), Mb, I, H, st));
+    ST_TRY(gemm_resid(m, m->a.p, I, w.w_down, m->h.p, m->tmp.as<float>(), Mb, H, I, st));
     ST_TRY(launch_check("mlp"));
   }
   if (!block) return DFLASH_OK;
@@ -389,6 +481,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   // ---- rows 1..n: final norm, unembedding, one batched draw ----------------
   const int n = fw.n, Rz = Bc * n;
   launch_rmsnorm(m->dt, false, m->h.p, Mb, nullptr, H, m->final_norm, m->z.p, H, Rz, H, n, nrows, 1, c.rms_eps, st);
+  m->launches++;
   float* lg;
   if (Bc == 1) {
     lg = fw.sess[0]->plogits;
@@ -413,13 +506,17 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   sa.rows_per_seq = n;
   sa.row_offset = 1;
   sa.seq_ids = tabs.seq;
-  launch_sample_partials(sa, chunk, m->spart.as<float4>(), st);
   int32_t* tok = m->vstat.as<int32_t>();
   float* lse = (float*)(tok + Rz);
-  launch_sample_combine(sa, chunks, m->spart.as<float4>(), tok, nullptr, lse, st);
-  // outputs in caller order
-  sa.out_map = (const int32_t*)(tb + o_map);
-  launch_sample_combine(sa, chunks, m->spart.as<float4>(), fw.out_tokens, fw.out_q, nullptr, st);
+  {
+    Timed tm(m, kSample, (double)Rz * V * 4, 6.0 * Rz * V, st);
+    launch_sample_partials(sa, chunk, m->spart.as<float4>(), st);
+    launch_sample_combine(sa, chunks, m->spart.as<float4>(), tok, nullptr, lse, st);
+    // outputs in caller order
+    sa.out_map = (const int32_t*)(tb + o_map);
+    launch_sample_combine(sa, chunks, m->spart.as<float4>(), fw.out_tokens, fw.out_q, nullptr, st);
+    m->launches += 3;
+  }
   ST_TRY(launch_check("sample"));
   for (int j = 0; j < Bc; ++j) {
     dflash_session* s = fw.sess[j];
@@ -553,9 +650,14 @@ int dflash_model_destroy(dflash_model* m) {
   for (auto& L : m->layers)
     if (L.w_qkvg) cudaFree(L.w_qkvg);
   Buf* bufs[] = {&m->tables, &m->u, &m->fcout, &m->c, &m->h, &m->x, &m->qkv, &m->rope, &m->Q, &m->G,
-                 &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart};
+                 &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart,
+                 &m->vbonus};
   for (Buf* b : bufs) b->release();
   m->ring.release();
+  for (auto& e : m->ev_pool) {
+    cudaEventDestroy(e.first);
+    cudaEventDestroy(e.second);
+  }
   if (m->d_err) cudaFree(m->d_err);
   if (m->tc) tc_destroy(m->tc);
   delete m;
@@ -804,8 +906,11 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   sa.gumbel = 0;
   sa.rows_per_seq = n + 1;
   sa.row_offset = 0;
+  const double tbytes = (double)rows * V * (sa.in_bf16 ? 2 : 4) + (double)batch * V * 4;
+  Timed tm(m, kVerify, tbytes, 4.0 * rows * V, st);
   launch_sample_partials(sa, chunk, m->vpart.as<float4>(), st);
   launch_sample_combine(sa, chunks, m->vpart.as<float4>(), amax, nullptr, lse, st);
+  m->launches += 3;
   VerifyArgs va{};
   va.target = target_logits;
   va.in_bf16 = sa.in_bf16;
@@ -827,7 +932,10 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   va.bonus = out_bonus;
   va.accepted_total = (long long* const*)(tb + o_acc);
   va.err = m->d_err;
-  launch_verify_accept(va, st);
+  ST_TRY(m->vbonus.ensure((size_t)batch * chunks * sizeof(VerifyPart) + (size_t)batch * 4, st));
+  va.rej = (int32_t*)(m->vbonus.as<char>() + (size_t)batch * chunks * sizeof(VerifyPart));
+  launch_verify_accept(va, m->vbonus.as<VerifyPart>(), st);
+  m->launches += temperature > 0.f ? 1 : 0;
   return launch_check("verify");
 }
 
@@ -898,6 +1006,41 @@ int dflash_kv_import(dflash_session* s, int32_t layer, int64_t first_slot, int32
   launch_kv_copy(s->m->dt, base + plane, s->cap, first_slot, v_in, n_rows, 0, n_rows, c.n_kv_heads, c.head_dim,
                  s->stream);
   return launch_check("kv_import");
+}
+
+int dflash_timing_enable(dflash_model* m, int32_t on) {
+  if (!m) return fail(DFLASH_ERR_INVALID_ARG, "null model");
+  if (on) {
+    CU_TRY(cudaDeviceSynchronize());
+    m->recs.clear();
+    m->ev_used = 0;
+    m->launches = 0;
+  }
+  m->timing = on != 0;
+  return DFLASH_OK;
+}
+
+int dflash_timing_read(dflash_model* m, dflash_kernel_time* out, int32_t max_entries, int32_t* n_entries) {
+  if (!m || !out || !n_entries || max_entries < 0) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  CU_TRY(cudaDeviceSynchronize());
+  dflash_kernel_time acc[kClasses + 1];
+  memset(acc, 0, sizeof acc);
+  for (int k = 0; k < kClasses; ++k) snprintf(acc[k].name, sizeof acc[k].name, "%s", kClassNames[k]);
+  snprintf(acc[kClasses].name, sizeof acc[kClasses].name, "all");
+  acc[kClasses].launches = m->launches;
+  for (const auto& r : m->recs) {
+    float ms = 0.f;
+    CU_TRY(cudaEventElapsedTime(&ms, r.e0, r.e1));
+    acc[r.cls].launches++;
+    acc[r.cls].total_ms += ms;
+    acc[r.cls].bytes += r.bytes;
+    acc[r.cls].flops += r.flops;
+  }
+  int n = 0;
+  for (int k = 0; k <= kClasses && n < max_entries; ++k)
+    if (acc[k].launches) out[n++] = acc[k];
+  *n_entries = n;
+  return DFLASH_OK;
 }
 
 }  // extern "C"

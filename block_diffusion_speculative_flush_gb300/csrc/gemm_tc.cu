@@ -34,6 +34,8 @@ namespace dfl {
 
 namespace {
 
+using bf16 = __nv_bfloat16;
+
 thread_local std::string g_tc_err;
 
 constexpr int BM = 128;  // weight rows per tile (MMA M)
@@ -41,14 +43,17 @@ constexpr int BK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct TcParams {
-  float* Y;
+  void* Y;         // fp32 output, bf16 residual stream, or bf16 SwiGLU product
   int64_t ldy;
-  int M, N;
+  int M, N;        // activation rows; output features
+  int mode;        // TcMode
   int n_tiles, splits, kb_total;
   float* ws;       // split partials [tile][split][BN][BM]
   int* counters;   // [tile] arrivals, returned to zero by the last CTA
   int* err;
 };
+
+constexpr int kMaxSplits = 16;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -175,14 +180,18 @@ __host__ __device__ constexpr size_t smem_bytes() {
   return (size_t)stages_for<BN>() * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
 }
 
-template <int BN>
+// SWI: the 128-row weight tile is 64 gate rows then the 64 matching up rows
+// (two TMA boxes from two matrices), and the epilogue writes silu(g) * u.
+template <int BN, bool SWI>
 __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmW,
+                                                    const __grid_constant__ CUtensorMap tmW2,
                                                     const __grid_constant__ CUtensorMap tmX, TcParams p) {
   constexpr int STAGES = stages_for<BN>();
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr uint32_t TX = A_BYTES + B_BYTES;
   constexpr int CH = BN < 32 ? BN : 32;
+  static_assert((size_t)BN * BM * 4 <= (size_t)STAGES * (A_BYTES + B_BYTES), "epilogue tile must fit the pipeline");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -213,6 +222,7 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmW) : "memory");
+    if (SWI) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmW2) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmX) : "memory");
   }
   if (warp == 1) {
@@ -241,7 +251,12 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
         break;
       }
       mbar_expect_tx(&full[s], TX);
-      tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM, pol_w);
+      if (SWI) {
+        tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, m_tile * (BM / 2), pol_w);
+        tma_load_2d(sA + s * A_BYTES + A_BYTES / 2, &tmW2, &full[s], (kb0 + i) * BK, m_tile * (BM / 2), pol_w);
+      } else {
+        tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM, pol_w);
+      }
       tma_load_2d(sB + s * B_BYTES, &tmX, &full[s], (kb0 + i) * BK, n_tile * BN, pol_x);
       ++issued;
     }
@@ -286,20 +301,20 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
     }
   }
   tc_fence_after();
-  const int row = warp * 32 + lane;
-  const int feat = m_tile * BM + row;
+  const int row = warp * 32 + lane;   // TMEM lane = weight row within the tile
   const int tok0 = n_tile * BN;
   const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  // The pipeline buffers are idle once every MMA has completed: the final
+  // tile is staged there as S[col][row] (fp32) for a coalesced store.
+  float* S = reinterpret_cast<float*>(smem);
+  bool store = true;
   if (p.splits == 1) {
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += CH) {
       float v[CH];
       tmem_ld<CH>(taddr + c0, v);
 #pragma unroll
-      for (int j = 0; j < CH; ++j) {
-        const int t = tok0 + c0 + j;
-        if (t < p.M && feat < p.N) p.Y[(int64_t)t * p.ldy + feat] = v[j];
-      }
+      for (int j = 0; j < CH; ++j) S[(c0 + j) * BM + row] = v[j];
     }
   } else {
     const int tile = m_tile * p.n_tiles + n_tile;
@@ -315,17 +330,62 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
     __syncthreads();
     if (threadIdx.x == 0) *last_flag = atomicAdd(&p.counters[tile], 1) == p.splits - 1;
     __syncthreads();
-    if (*last_flag) {
+    store = *last_flag != 0;
+    if (store) {
+      // the last CTA of the tile sums the partials in split order; all loads
+      // of a column group are issued before the adds
       __threadfence();
-      const float* base = p.ws + (int64_t)tile * p.splits * BN * BM;
+      const float* base = p.ws + (int64_t)tile * p.splits * BN * BM + row;
 #pragma unroll 1
-      for (int c = 0; c < BN; ++c) {
-        const int t = tok0 + c;
-        float acc = 0.f;
-        for (int s = 0; s < p.splits; ++s) acc += __ldcg(base + ((int64_t)s * BN + c) * BM + row);
-        if (t < p.M && feat < p.N) p.Y[(int64_t)t * p.ldy + feat] = acc;
+      for (int c0 = 0; c0 < BN; c0 += 4) {
+        float v[kMaxSplits][4];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[sp][j] = sp < p.splits ? __ldcg(base + ((int64_t)sp * BN + c0 + j) * BM) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float acc = 0.f;
+#pragma unroll
+          for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) acc += v[sp][j];
+          S[(c0 + j) * BM + row] = acc;
+        }
       }
       if (threadIdx.x == 0) p.counters[tile] = 0;
+    }
+  }
+  __syncthreads();
+  if (store) {
+    if (SWI) {
+      // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
+      bf16* out = reinterpret_cast<bf16*>(p.Y);
+      for (int e = threadIdx.x; e < BN * (BM / 2); e += blockDim.x) {
+        const int c = e / (BM / 2), f = e % (BM / 2);
+        const int t = tok0 + c, feat = m_tile * (BM / 2) + f;
+        if (t < p.M && feat < p.N) {
+          const float g = S[c * BM + f], u = S[c * BM + BM / 2 + f];
+          out[(int64_t)t * p.ldy + feat] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+        }
+      }
+    } else if (p.mode == kResidBf16) {
+      bf16* h = reinterpret_cast<bf16*>(p.Y);
+      for (int e = threadIdx.x; e < BN * BM; e += blockDim.x) {
+        const int c = e / BM, f = e % BM;
+        const int t = tok0 + c, feat = m_tile * BM + f;
+        if (t < p.M && feat < p.N) {
+          bf16* hp = h + (int64_t)t * p.ldy + feat;
+          *hp = __float2bfloat16_rn(__bfloat162float(*hp) + S[c * BM + f]);
+        }
+      }
+    } else {
+      float* Y = reinterpret_cast<float*>(p.Y);
+      for (int e = threadIdx.x; e < BN * BM; e += blockDim.x) {
+        const int c = e / BM, f = e % BM;
+        const int t = tok0 + c, feat = m_tile * BM + f;
+        if (t < p.M && feat < p.N) Y[(int64_t)t * p.ldy + feat] = S[c * BM + f];
+      }
     }
   }
   tc_fence_before();
@@ -347,7 +407,7 @@ struct TcContext {
   int* counters = nullptr;
   size_t cnt_cap = 0;
   int* err = nullptr;
-  bool attr_set[9] = {};
+  bool attr_set[10] = {};
 };
 
 const char* tc_last_error() { return g_tc_err.c_str(); }
@@ -399,32 +459,36 @@ static int encode_2d(TcContext* c, CUtensorMap* map, const void* base, uint64_t 
   return 0;
 }
 
-template <int BN>
-static int launch_bn(TcContext* c, const CUtensorMap& mw, const CUtensorMap& mx, const TcParams& p, int grid,
-                     cudaStream_t st, int slot) {
+template <int BN, bool SWI>
+static int launch_bn(TcContext* c, const CUtensorMap& mw, const CUtensorMap& mw2, const CUtensorMap& mx,
+                     const TcParams& p, int grid, cudaStream_t st, int slot) {
   const size_t smem = smem_bytes<BN>();
   if (!c->attr_set[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, SWI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return tc_fail("smem attribute", e);
     c->attr_set[slot] = true;
   }
-  k_gemm_tc<BN><<<grid, 128, smem, st>>>(mw, mx, p);
+  k_gemm_tc<BN, SWI><<<grid, 128, smem, st>>>(mw, mw2, mx, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return tc_fail("k_gemm_tc launch", e);
   return 0;
 }
 
-int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy, int M, int N,
-            int K, cudaStream_t st) {
+int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y,
+            int64_t ldy, int M, int N, int K, int mode, cudaStream_t st) {
   if (M <= 0 || N <= 0) return 0;
-  if (K % BK || ldx % 8 || ldw % 8 || ((uintptr_t)X & 15) || ((uintptr_t)W & 15))
+  const bool swi = mode == kSwigluBf16;
+  if (K % BK || ldx % 8 || ldw % 8 || ((uintptr_t)X & 15) || ((uintptr_t)W & 15) || (swi && ((uintptr_t)W2 & 15)))
     return tc_fail("tc_gemm: K must be a multiple of 64, strides multiples of 8, operands 16-byte aligned");
+  if (mode < kF32 || mode > kSwigluBf16) return tc_fail("tc_gemm: unknown mode");
   const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-  const int m_tiles = (N + BM - 1) / BM, n_tiles = (M + BN - 1) / BN, kb_total = K / BK;
-  // split K so that the weight tiles alone give about two CTAs per SM; the
-  // split depends on N and K only
-  int splits = (2 * c->num_sms + m_tiles / 2) / m_tiles;
-  splits = std::max(1, std::min(splits, std::max(1, kb_total / 2)));
+  const int rows_per_tile = swi ? BM / 2 : BM;
+  const int m_tiles = (N + rows_per_tile - 1) / rows_per_tile, n_tiles = (M + BN - 1) / BN, kb_total = K / BK;
+  // Split K so that the weight tiles fill one wave of resident CTAs (two per
+  // SM up to BN = 128, one at 256); the split depends on N and K only.
+  const int slots = c->num_sms * (BN <= 128 ? 2 : 1);
+  int splits = slots / m_tiles;
+  splits = std::max(1, std::min({splits, kMaxSplits, std::max(1, kb_total / 2)}));
   const int tiles = m_tiles * n_tiles;
   if (splits > 1) {
     const size_t need = (size_t)tiles * splits * BN * BM * sizeof(float);
@@ -449,17 +513,31 @@ int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, int64_t ldw
       c->cnt_cap = want;
     }
   }
-  CUtensorMap mw, mx;
-  if (encode_2d(c, &mw, W, (uint64_t)K, (uint64_t)N, ldw, BM)) return -1;
+  CUtensorMap mw, mw2, mx;
+  if (encode_2d(c, &mw, W, (uint64_t)K, (uint64_t)N, ldw, (uint32_t)rows_per_tile)) return -1;
+  if (swi) {
+    if (encode_2d(c, &mw2, W2, (uint64_t)K, (uint64_t)N, ldw, (uint32_t)rows_per_tile)) return -1;
+  } else {
+    mw2 = mw;
+  }
   if (encode_2d(c, &mx, X, (uint64_t)K, (uint64_t)M, ldx, (uint32_t)BN)) return -1;
-  TcParams p{Y, ldy, M, N, n_tiles, splits, kb_total, c->ws, c->counters, c->err};
+  TcParams p{Y, ldy, M, N, mode, n_tiles, splits, kb_total, c->ws, c->counters, c->err};
   const int grid = tiles * splits;
+  if (swi) {
+    switch (BN) {
+      case 16: return launch_bn<16, true>(c, mw, mw2, mx, p, grid, st, 5);
+      case 32: return launch_bn<32, true>(c, mw, mw2, mx, p, grid, st, 6);
+      case 64: return launch_bn<64, true>(c, mw, mw2, mx, p, grid, st, 7);
+      case 128: return launch_bn<128, true>(c, mw, mw2, mx, p, grid, st, 8);
+      default: return launch_bn<256, true>(c, mw, mw2, mx, p, grid, st, 9);
+    }
+  }
   switch (BN) {
-    case 16: return launch_bn<16>(c, mw, mx, p, grid, st, 0);
-    case 32: return launch_bn<32>(c, mw, mx, p, grid, st, 1);
-    case 64: return launch_bn<64>(c, mw, mx, p, grid, st, 2);
-    case 128: return launch_bn<128>(c, mw, mx, p, grid, st, 3);
-    default: return launch_bn<256>(c, mw, mx, p, grid, st, 4);
+    case 16: return launch_bn<16, false>(c, mw, mw2, mx, p, grid, st, 0);
+    case 32: return launch_bn<32, false>(c, mw, mw2, mx, p, grid, st, 1);
+    case 64: return launch_bn<64, false>(c, mw, mw2, mx, p, grid, st, 2);
+    case 128: return launch_bn<128, false>(c, mw, mw2, mx, p, grid, st, 3);
+    default: return launch_bn<256, false>(c, mw, mw2, mx, p, grid, st, 4);
   }
 }
 

@@ -14,12 +14,18 @@ int tc_create(TcContext** out, int num_sms, int* err);
 void tc_destroy(TcContext* c);
 const char* tc_last_error();
 
-// Y[M][N] (fp32, row stride ldy) = X[M][K] . W[N][K]^T with bf16 X and W.
-// Needs K % 64 == 0, ldx and ldw multiples of 8 elements and 16-byte aligned
-// X / W; any M >= 1 and N >= 1.  The k order of every output element
-// depends on N and K only (never on M), so a row's result does not change
-// with the number of rows in the call.
-int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy, int M, int N,
-            int K, cudaStream_t st);
+enum TcMode {
+  kF32 = 0,        // Y fp32 [M][ldy]: Y = X W^T
+  kResidBf16 = 1,  // Y bf16 [M][ldy]: Y = bf16(Y + X W^T), the residual add
+  kSwigluBf16 = 2  // Y bf16 [M][ldy]: Y = bf16(silu(X Wg^T) * (X Wu^T)), W = Wg, W2 = Wu
+};
+
+// Weight-streaming product with bf16 X [M][K] and W [N][K] (and W2 for
+// SwiGLU, N = the intermediate width).  Needs K % 64 == 0, ldx and ldw
+// multiples of 8 elements and 16-byte aligned operands; any M, N >= 1.  The
+// k order of every output element depends on N and K only (never on M), so
+// a row's result does not change with the number of rows in the call.
+int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y, int64_t ldy,
+            int M, int N, int K, int mode, cudaStream_t st);
 
 }  // namespace dfl

@@ -57,6 +57,10 @@ void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, 
                      SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st);
 void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_items, SessTables tabs,
                            AttnParams p, float* part, cudaStream_t st);
+// bf16 block attention on mma.sync tensor cores; false if the shape is not
+// supported (head_dim other than 64/128, more than 128 query rows per KV head).
+bool launch_attention_mma(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p,
+                          float* part, cudaStream_t st);
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count,
                               int B, AttnParams p, const float* G, void* O, cudaStream_t st);
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld_delta, int rows, int H, cudaStream_t st);
@@ -106,8 +110,20 @@ struct VerifyArgs {
   int32_t* bonus;               // [B]
   long long* const* accepted_total;  // [B] -> running counter of each session
   int32_t* err;                 // bit 2: a draft token id outside [0, V)
+  int32_t* rej;                 // [B] scratch: first rejected position (0: none)
 };
-void launch_verify_accept(const VerifyArgs& a, cudaStream_t st);
+// Bonus-draw partial of one vocabulary chunk of one session.
+struct VerifyPart {
+  float rsum;      // sum of max(0, p - q)
+  float rv;        // best log(max(0, p - q)) + Gumbel
+  int32_t ri;
+  float pv;        // best log p + Gumbel
+  int32_t pi;
+};
+// T > 0: one grid of (session, vocabulary chunk) CTAs for the bonus draw,
+// then the per-session finish; T == 0: the finish alone.  part holds
+// B * ceil(V / 4096) entries.
+void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st);
 
 // --- tensor-core path (bf16, sm_103a) --------------------------------------
 struct TcGemmPlan;  // opaque, defined in gemm_tc.cu

@@ -43,23 +43,38 @@ __global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict
   for (int j = threadIdx.x; j < Ht; j += blockDim.x) o[j] = from_f<T>(to_f(f[j]) * inv * to_f(g[j]));
 }
 
+// One CTA per output row; the row stays in registers between the sum of
+// squares and the scaled write (up to 8 x blockDim.x elements per row).
 template <typename TIn, typename T>
-__global__ void k_rmsnorm(const TIn* __restrict__ in0, int rows0, const TIn* __restrict__ in1, int64_t ld_in,
-                          const T* __restrict__ g, T* __restrict__ out, int64_t ld_out, int H, int a, int b,
-                          int c, float eps) {
+__global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, int rows0, const TIn* __restrict__ in1,
+                                                 int64_t ld_in, const T* __restrict__ g, T* __restrict__ out,
+                                                 int64_t ld_out, int H, int a, int b, int c, float eps) {
   __shared__ float red[32];
   const int j = blockIdx.x;
   const int src = (j / a) * b + (j % a) + c;
   const TIn* x = src < rows0 ? in0 + (int64_t)src * ld_in : in1 + (int64_t)(src - rows0) * ld_in;
+  constexpr int MAXV = 8;
+  float v[MAXV];
   float ss = 0.f;
-  for (int t = threadIdx.x; t < H; t += blockDim.x) {
-    const float v = to_f(x[t]);
-    ss += v * v;
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int t = threadIdx.x + k * blockDim.x;
+    v[k] = t < H ? to_f(x[t]) : 0.f;
+    ss += v[k] * v[k];
+  }
+  for (int t = threadIdx.x + MAXV * blockDim.x; t < H; t += blockDim.x) {  // rows wider than the registers
+    const float y = to_f(x[t]);
+    ss += y * y;
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)H + eps);
   T* o = out + (int64_t)j * ld_out;
-  for (int t = threadIdx.x; t < H; t += blockDim.x) o[t] = from_f<T>(to_f(x[t]) * inv * to_f(g[t]));
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int t = threadIdx.x + k * blockDim.x;
+    if (t < H) o[t] = from_f<T>(v[k] * inv * to_f(g[t]));
+  }
+  for (int t = threadIdx.x + MAXV * blockDim.x; t < H; t += blockDim.x) o[t] = from_f<T>(to_f(x[t]) * inv * to_f(g[t]));
 }
 
 template <typename T>
@@ -235,38 +250,62 @@ __global__ void k_attn_simt(const T* __restrict__ Q, const AttnItem* __restrict_
     }
     __syncthreads();
   }
-  float* out = part + (int64_t)blockIdx.x * R * (d + 2);
-  for (int e = threadIdx.x; e < R * (d + 2); e += blockDim.x) {
-    const int rr = e / (d + 2), t = e % (d + 2);
-    out[e] = t == 0 ? ms[rr] : (t == 1 ? ls[rr] : acc[rr * d + t - 2]);
+  float* out = part + (int64_t)blockIdx.x * R * (d + 4);
+  for (int e = threadIdx.x; e < R * (d + 4); e += blockDim.x) {
+    const int rr = e / (d + 4), t = e % (d + 4);
+    out[e] = t == 0 ? ms[rr] : (t == 1 ? ls[rr] : (t < 4 ? 0.f : acc[rr * d + t - 4]));
   }
 }
 
+// Merge of the key splits of one (block row, query head) per warp:
+// M = max m_s, L = sum l_s e^(m_s - M), o = sum O_s e^(m_s - M) / L, then
+// the per-head gate.  Partial rows are [m, l, -, -, O[d]] (16-byte aligned O).
 template <typename T>
-__global__ void k_attn_combine(const float* __restrict__ part, const int32_t* __restrict__ item_first,
-                               const int32_t* __restrict__ item_count, AttnParams p, const float* __restrict__ Gt,
-                               T* __restrict__ O) {
-  const int d = p.d, G = p.Hq / p.Hkv, R = p.nrows * G;
-  const int b = blockIdx.x / p.nrows, i = blockIdx.x % p.nrows;
-  const int hq = blockIdx.y, kvh = hq / G, g = hq % G, rr = i * G + g;
+__global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part,
+                                                      const int32_t* __restrict__ item_first,
+                                                      const int32_t* __restrict__ item_count, AttnParams p, int total,
+                                                      const float* __restrict__ Gt, T* __restrict__ O) {
+  __shared__ float wsm[4][64];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int gw = blockIdx.x * 4 + wl;  // (b, i, hq) flattened
+  if (gw >= total) return;
+  const int d = p.d, G = p.Hq / p.Hkv, R = p.nrows * G, PD = d + 4;
+  const int hq = gw % p.Hq, bi = gw / p.Hq;
+  const int b = bi / p.nrows, i = bi % p.nrows;
+  const int kvh = hq / G, rr = i * G + hq % G;
   const int S = item_count[b];
-  const int first = item_first[b] + kvh * S;
+  const float* base = part + ((int64_t)(item_first[b] + kvh * S) * R + rr) * PD;
+  const int64_t sstride = (int64_t)R * PD;
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, part[((int64_t)(first + s) * R + rr) * (d + 2)]);
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, base[s * sstride]);
+  M = warp_max(M);
   float L = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float* ps = part + ((int64_t)(first + s) * R + rr) * (d + 2);
-    if (ps[0] != -INFINITY) L += ps[1] * expf(ps[0] - M);
+  for (int s = lane; s < S; s += 32) {
+    const float m = base[s * sstride];
+    const float w = m == -INFINITY ? 0.f : expf(m - M);
+    L += base[s * sstride + 1] * w;
+    if (s < 64) wsm[wl][s] = w;
   }
-  const float gate = Gt ? Gt[((int64_t)b * p.nrows + i) * p.Hq + hq] : 1.f;
-  for (int t = threadIdx.x; t < d; t += blockDim.x) {
-    float o = 0.f;
+  L = warp_sum(L);
+  __syncwarp();
+  const float gate = Gt ? Gt[(int64_t)bi * p.Hq + hq] : 1.f;
+  const float scale = gate / L;
+  T* out = O + ((int64_t)bi * p.Hq + hq) * d;
+  for (int t4 = lane * 4; t4 < d; t4 += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < S; ++s) {
-      const float* ps = part + ((int64_t)(first + s) * R + rr) * (d + 2);
-      if (ps[0] != -INFINITY) o += ps[2 + t] * expf(ps[0] - M);
+      const float m = s < 64 ? 0.f : base[s * sstride];
+      const float w = s < 64 ? wsm[wl][s] : (m == -INFINITY ? 0.f : expf(m - M));
+      const float4 v = *reinterpret_cast<const float4*>(base + s * sstride + 4 + t4);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
     }
-    o = o / L * gate;
-    O[(((int64_t)b * p.nrows + i) * p.Hq + hq) * d + t] = from_f<T>(o);
+    out[t4] = from_f<T>(acc.x * scale);
+    out[t4 + 1] = from_f<T>(acc.y * scale);
+    out[t4 + 2] = from_f<T>(acc.z * scale);
+    out[t4 + 3] = from_f<T>(acc.w * scale);
   }
 }
 
@@ -430,60 +469,63 @@ __global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restr
   }
 }
 
-// One CTA per session: the sequential acceptance scan, then (T > 0) one pass
-// over the vocabulary for the bonus draw.
-__global__ void __launch_bounds__(1024) k_verify_accept(VerifyArgs a) {
-  __shared__ int s_rej;
-  __shared__ float sm_sum[32];
-  __shared__ float sm_rs[32], sm_ps[32];
-  __shared__ int32_t sm_ri[32], sm_pi[32];
-  const int b = blockIdx.x;
+// Acceptance scan of one session (T > 0): the first i in 1..n whose draft
+// token fails u_i * q_i(d_i) < p_i(d_i), or 0 if all n pass.
+__device__ int verify_scan(const VerifyArgs& a, int b) {
   const int n = a.n, V = a.V;
   const int64_t tbase = (int64_t)b * (n + 1) * V;
   const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
-  if (a.temperature <= 0.f) {
-    if (threadIdx.x == 0) {
-      int acc = 0;
-      while (acc < n && a.amax_t[b * (n + 1) + acc] == a.draft[b * n + acc]) ++acc;
-      a.accept[b] = acc;
-      a.bonus[b] = a.amax_t[b * (n + 1) + acc];
-      if (a.accepted_total) *a.accepted_total[b] += acc;
-    }
-    return;
-  }
   const float invT = 1.f / a.temperature;
   const float Tq = a.dtemp[b];
   const float* dl = a.dlogits[b];
   const float* dlse = a.dlse[b];
   const int32_t* dtok = a.dtok[b];
-  if (threadIdx.x == 0) {
-    int rej = 0;
-    for (int i = 1; i <= n; ++i) {
-      int dtk = a.draft[b * n + i - 1];
-      if (dtk < 0 || dtk >= V) {
-        atomicOr(a.err, 2);
-        dtk = 0;
-      }
-      const float p = expf(load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT -
-                           a.lse_t[b * (n + 1) + i - 1]);
-      const float q = Tq > 0.f ? expf(dl[(int64_t)(i - 1) * V + dtk] / Tq - dlse[i - 1])
-                               : (dtk == dtok[i - 1] ? 1.f : 0.f);
-      const float r = uniform_open(rand_u32(a.seed, a.rnd, kStreamAccept, seq, (uint32_t)i, 0u));
-      if (!(r * q < p)) {
-        rej = i;
-        break;
-      }
+  for (int i = 1; i <= n; ++i) {
+    int dtk = a.draft[b * n + i - 1];
+    if (dtk < 0 || dtk >= V) {
+      atomicOr(a.err, 2);
+      dtk = 0;
     }
-    s_rej = rej;
+    const float p = expf(load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT -
+                         a.lse_t[b * (n + 1) + i - 1]);
+    const float q = Tq > 0.f ? expf(dl[(int64_t)(i - 1) * V + dtk] / Tq - dlse[i - 1])
+                             : (dtk == dtok[i - 1] ? 1.f : 0.f);
+    const float r = uniform_open(rand_u32(a.seed, a.rnd, kStreamAccept, seq, (uint32_t)i, 0u));
+    if (!(r * q < p)) return i;
+  }
+  return 0;
+}
+
+// Bonus draw partials (T > 0), grid (session, vocabulary chunk): over the
+// chunk of the target row after the accepted prefix, the residual mass
+// sum max(0, p - q), the best log(max(0, p - q)) + Gumbel and the best
+// log p + Gumbel.
+__global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__ part) {
+  __shared__ int s_rej;
+  __shared__ float sm_sum[32], sm_rs[32], sm_ps[32];
+  __shared__ int32_t sm_ri[32], sm_pi[32];
+  const int b = blockIdx.x, c = blockIdx.y, nch = gridDim.y;
+  const int n = a.n, V = a.V;
+  if (threadIdx.x == 0) {
+    s_rej = verify_scan(a, b);
+    if (c == 0) a.rej[b] = s_rej;
   }
   __syncthreads();
   const int rej = s_rej;
+  const int64_t tbase = (int64_t)b * (n + 1) * V;
+  const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
+  const float invT = 1.f / a.temperature;
+  const float Tq = a.dtemp[b];
+  const float* dl = a.dlogits[b];
+  const float* dlse = a.dlse[b];
+  const int32_t* dtok = a.dtok[b];
   const int trow = rej ? rej - 1 : n;                 // target row of the bonus draw
   const uint32_t prow = rej ? (uint32_t)rej : (uint32_t)(n + 1);
   const float lse = a.lse_t[b * (n + 1) + trow];
+  const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   float rsum = 0.f;
   ArgMax bres{-INFINITY, INT32_MAX}, bp{-INFINITY, INT32_MAX};
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
     const float lp = load_logit(a.target, a.in_bf16, tbase + (int64_t)trow * V + v) * invT - lse;
     const float g = gumbel(a.seed, a.rnd, kStreamBonus, seq, prow, (uint32_t)v);
     bp = better(bp, ArgMax{lp + g, v});
@@ -509,18 +551,48 @@ __global__ void __launch_bounds__(1024) k_verify_accept(VerifyArgs a) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
+    VerifyPart o{0.f, -INFINITY, INT32_MAX, -INFINITY, INT32_MAX};
+    for (int i = 0; i < nw; ++i) {
+      o.rsum += sm_sum[i];
+      const ArgMax r = better(ArgMax{o.rv, o.ri}, ArgMax{sm_rs[i], sm_ri[i]});
+      const ArgMax q = better(ArgMax{o.pv, o.pi}, ArgMax{sm_ps[i], sm_pi[i]});
+      o.rv = r.v;
+      o.ri = r.i;
+      o.pv = q.v;
+      o.pi = q.i;
+    }
+    part[(int64_t)b * nch + c] = o;
+  }
+}
+
+// Accept length and bonus per session.  T == 0: accept while the target's
+// argmax equals the draft token; bonus = argmax of row a.  T > 0: merge the
+// bonus partials in chunk order.
+__global__ void k_verify_finish(VerifyArgs a, int chunks, const VerifyPart* __restrict__ part) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.B) return;
+  const int n = a.n;
+  int accn, bonus;
+  if (a.temperature <= 0.f) {
+    accn = 0;
+    while (accn < n && a.amax_t[b * (n + 1) + accn] == a.draft[b * n + accn]) ++accn;
+    bonus = a.amax_t[b * (n + 1) + accn];
+  } else {
+    const int rej = a.rej[b];
     float S = 0.f;
     ArgMax R{-INFINITY, INT32_MAX}, P{-INFINITY, INT32_MAX};
-    for (int i = 0; i < nw; ++i) {
-      S += sm_sum[i];
-      R = better(R, ArgMax{sm_rs[i], sm_ri[i]});
-      P = better(P, ArgMax{sm_ps[i], sm_pi[i]});
+    for (int c = 0; c < chunks; ++c) {
+      const VerifyPart o = part[(int64_t)b * chunks + c];
+      S += o.rsum;
+      R = better(R, ArgMax{o.rv, o.ri});
+      P = better(P, ArgMax{o.pv, o.pi});
     }
-    const int accn = rej ? rej - 1 : n;
-    a.accept[b] = accn;
-    a.bonus[b] = (rej && S > 0.f) ? R.i : P.i;
-    if (a.accepted_total) *a.accepted_total[b] += accn;
+    accn = rej ? rej - 1 : n;
+    bonus = (rej && S > 0.f) ? R.i : P.i;
   }
+  a.accept[b] = accn;
+  a.bonus[b] = bonus;
+  if (a.accepted_total) *a.accepted_total[b] += accn;
 }
 
 inline unsigned cdiv(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
@@ -552,10 +624,10 @@ void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* 
                     void* out, int64_t ld_out, int rows, int H, int a, int b, int c, float eps, cudaStream_t st) {
   if (rows <= 0) return;
   if (in_f32) {
-    DFL_DISPATCH(dt, k_rmsnorm<float, T><<<rows, 256, 0, st>>>((const float*)in0, rows0, (const float*)in1, ld_in,
+    DFL_DISPATCH(dt, k_rmsnorm<float, T><<<rows, 512, 0, st>>>((const float*)in0, rows0, (const float*)in1, ld_in,
                                                                 (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
   } else {
-    DFL_DISPATCH(dt, k_rmsnorm<T, T><<<rows, 256, 0, st>>>((const T*)in0, rows0, (const T*)in1, ld_in,
+    DFL_DISPATCH(dt, k_rmsnorm<T, T><<<rows, 512, 0, st>>>((const T*)in0, rows0, (const T*)in1, ld_in,
                                                             (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
   }
 }
@@ -603,8 +675,9 @@ void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_it
 
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count, int B,
                               AttnParams p, const float* G, void* O, cudaStream_t st) {
-  DFL_DISPATCH(dt, k_attn_combine<T><<<dim3(B * p.nrows, p.Hq), p.d, 0, st>>>(part, item_first, item_count, p, G,
-                                                                               (T*)O));
+  const int total = B * p.nrows * p.Hq;
+  DFL_DISPATCH(dt, k_attn_combine<T><<<cdiv(total, 4), 128, 0, st>>>(part, item_first, item_count, p, total, G,
+                                                                      (T*)O));
 }
 
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld, int rows, int H, cudaStream_t st) {
@@ -642,9 +715,11 @@ void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, 
   k_sample_combine<<<cdiv(a.rows, 128), 128, 0, st>>>(a, chunks, part, tok, qtok, lse);
 }
 
-void launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
+void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st) {
   if (a.B <= 0) return;
-  k_verify_accept<<<a.B, 1024, 0, st>>>(a);
+  const int chunk = 4096, chunks = (int)cdiv(a.V, chunk);
+  if (a.temperature > 0.f) k_verify_bonus<<<dim3(a.B, chunks), 256, 0, st>>>(a, chunk, part);
+  k_verify_finish<<<cdiv(a.B, 64), 64, 0, st>>>(a, chunks, part);
 }
 
 }  // namespace dfl

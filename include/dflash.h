@@ -238,6 +238,26 @@ DFLASH_API int dflash_kv_export(const dflash_session* s, int32_t layer, int64_t 
 DFLASH_API int dflash_kv_import(dflash_session* s, int32_t layer, int64_t first_slot, int32_t n_rows, const void* k_in,
                      const void* v_in);
 
+/* ---- measurement ---------------------------------------------------------
+ * Not part of the round.  While timing is on, the runtime brackets every
+ * launch of the matrix-product, attention, sampling and verify kernels with
+ * CUDA events on the launching stream and records the launch's algorithmic
+ * bytes (each operand read once, each output written once) and flops; every
+ * kernel launch of the model is also counted. */
+typedef struct dflash_kernel_time {
+  char name[24];     /* kernel class: "gemm_tc", "gemm_simt", "attention", "sample", "verify", "all" */
+  int64_t launches;  /* kernel launches of this class */
+  double total_ms;   /* sum of event-measured durations (0 for "all") */
+  double bytes;      /* algorithmic bytes of those launches */
+  double flops;      /* algorithmic flops of those launches */
+} dflash_kernel_time;
+
+/* on != 0 clears the records and starts recording; on == 0 stops. */
+DFLASH_API int dflash_timing_enable(dflash_model* m, int32_t on);
+/* Synchronises the device, then writes up to max_entries classes to out
+ * (host) and their number to *n_entries (host). */
+DFLASH_API int dflash_timing_read(dflash_model* m, dflash_kernel_time* out, int32_t max_entries, int32_t* n_entries);
+
 #ifdef __cplusplus
 }
 #endif

@@ -196,6 +196,31 @@ def softmax(s):
 # The draft model
 # ---------------------------------------------------------------------------
 
+class _Float64View:
+    """Weights as given (exact storage values in any float array type), read
+    as float64 when used; vectors are converted once, matrices per use so
+    that a large draft never needs a full float64 copy."""
+
+    def __init__(self, weights):
+        self.src = dict(weights)
+        self.small = {}
+
+    def __getitem__(self, name):
+        a = self.src[name]
+        if a.ndim == 2 and a.size > (1 << 22):
+            return np.asarray(a, dtype=np.float64)
+        if name not in self.small:
+            self.small[name] = np.asarray(a, dtype=np.float64)
+        return self.small[name]
+
+    def __contains__(self, name):
+        return name in self.src
+
+    def rows(self, name, idx):
+        """Selected rows only (embedding lookup)."""
+        return np.asarray(self.src[name][np.asarray(idx, dtype=np.int64)], dtype=np.float64)
+
+
 class OracleDraft:
     """Draft weights in float64 plus the forward steps of the round.
 
@@ -206,7 +231,7 @@ class OracleDraft:
 
     def __init__(self, cfg, weights):
         self.cfg = cfg
-        self.w = {k: np.asarray(v, dtype=np.float64) for k, v in weights.items()}
+        self.w = _Float64View(weights)
         self.st = storage_round(cfg.dtype)
         self.group = cfg.n_q_heads // cfg.n_kv_heads
 
@@ -219,24 +244,30 @@ class OracleDraft:
         u = self.st(rmsnorm(f, self.w["aux_norms"], c.rms_eps)).reshape(len(f), -1)
         return self.st(rmsnorm(linear(self.w["w_fc"], u), self.w["hidden_norm"], c.rms_eps))
 
-    def context_kv(self, feats, slots):
-        """Per-layer K, V [rows, Hkv, d] of context rows at absolute slots."""
+    def context_layer_kv(self, l, hid, slots):
+        """Layer l's K, V [rows, Hkv, d] of context rows (hidden `hid`) at slots:
+        input_layernorm, the K/V rows of the fused projection, k norm, RoPE."""
         c = self.cfg
-        hid = self.context_hidden(feats)
-        slots = np.asarray(slots, dtype=np.float64)
+        p = f"layers.{l}."
         qd = c.n_q_heads * c.head_dim
         kd = c.n_kv_heads * c.head_dim
+        x = self.st(rmsnorm(hid, self.w[p + "in_norm"], c.rms_eps))
+        wkv = self.w[p + "w_qkv"][qd:qd + 2 * kd]       # K/V rows only
+        kv = linear(wkv, x)
+        k = kv[:, :kd].reshape(-1, c.n_kv_heads, c.head_dim)
+        v = kv[:, kd:].reshape(-1, c.n_kv_heads, c.head_dim)
+        slots = np.asarray(slots, dtype=np.float64)
+        k = rope(rmsnorm(k, self.w[p + "k_norm"], c.rms_eps), slots[:, None], c.rope_theta)
+        return self.st(k), self.st(v)
+
+    def context_kv(self, feats, slots):
+        """Per-layer K, V [rows, Hkv, d] of context rows at absolute slots."""
+        hid = self.context_hidden(feats)
         Ks, Vs = [], []
-        for l in range(c.n_layers):
-            p = f"layers.{l}."
-            x = self.st(rmsnorm(hid, self.w[p + "in_norm"], c.rms_eps))
-            wkv = self.w[p + "w_qkv"][qd:qd + 2 * kd]       # K/V rows only
-            kv = linear(wkv, x)
-            k = kv[:, :kd].reshape(-1, c.n_kv_heads, c.head_dim)
-            v = kv[:, kd:].reshape(-1, c.n_kv_heads, c.head_dim)
-            k = rope(rmsnorm(k, self.w[p + "k_norm"], c.rms_eps), slots[:, None], c.rope_theta)
-            Ks.append(self.st(k))
-            Vs.append(self.st(v))
+        for l in range(self.cfg.n_layers):
+            k, v = self.context_layer_kv(l, hid, slots)
+            Ks.append(k)
+            Vs.append(v)
         return Ks, Vs
 
     # -- block forward -----------------------------------------------------
@@ -271,44 +302,51 @@ class OracleDraft:
                 o[i, hq] = softmax((keys @ q[i, hq]) * scale) @ vals
         return o
 
+    def block_layer(self, l, h, pos, ck, cv, cpos):
+        """One draft layer over the block rows h [nb, H] at positions pos,
+        against context K/V ck, cv [N, Hkv, d] at positions cpos."""
+        c, w, st = self.cfg, self.w, self.st
+        nb = len(h)
+        qd = c.n_q_heads * c.head_dim
+        kd = c.n_kv_heads * c.head_dim
+        p = f"layers.{l}."
+        x = st(rmsnorm(h, w[p + "in_norm"], c.rms_eps))
+        qkv = linear(w[p + "w_qkv"], x)
+        q = qkv[:, :qd].reshape(nb, c.n_q_heads, c.head_dim)
+        k = qkv[:, qd:qd + kd].reshape(nb, c.n_kv_heads, c.head_dim)
+        v = qkv[:, qd + kd:].reshape(nb, c.n_kv_heads, c.head_dim)
+        q = st(rope(rmsnorm(q, w[p + "q_norm"], c.rms_eps), pos[:, None], c.rope_theta))
+        k = st(rope(rmsnorm(k, w[p + "k_norm"], c.rms_eps), pos[:, None], c.rope_theta))
+        v = st(v)
+        gate = sigmoid(linear(w[p + "w_g"], x)) if c.gated_attention else None
+        o = self.attention(q, k, v, pos, ck, cv, cpos)
+        if gate is not None:
+            o = o * gate[:, :, None]
+        o = st(o.reshape(nb, qd))
+        h = st(h + linear(w[p + "w_o"], o))
+        y = st(rmsnorm(h, w[p + "post_norm"], c.rms_eps))
+        a = st(silu(linear(w[p + "w_gate"], y)) * linear(w[p + "w_up"], y))
+        return st(h + linear(w[p + "w_down"], a))
+
     def block_forward(self, tokens, F, ctx):
         """Forward of [anchor, mask x n] at positions F..F+n against context.
 
         ctx: dict with 'pos' [N] and per-layer 'k', 'v' lists of [N, Hkv, d].
         Returns the final residual h [n+1, H].
         """
-        c, w, st = self.cfg, self.w, self.st
-        nb = len(tokens)
-        pos = F + np.arange(nb, dtype=np.float64)
-        h = np.stack([w["embed"][int(t)] for t in tokens])
-        qd = c.n_q_heads * c.head_dim
-        kd = c.n_kv_heads * c.head_dim
+        pos = F + np.arange(len(tokens), dtype=np.float64)
+        h = self.w.rows("embed", [int(t) for t in tokens])
         cpos = np.asarray(ctx["pos"], dtype=np.float64)
-        for l in range(c.n_layers):
-            p = f"layers.{l}."
-            x = st(rmsnorm(h, w[p + "in_norm"], c.rms_eps))
-            qkv = linear(w[p + "w_qkv"], x)
-            q = qkv[:, :qd].reshape(nb, c.n_q_heads, c.head_dim)
-            k = qkv[:, qd:qd + kd].reshape(nb, c.n_kv_heads, c.head_dim)
-            v = qkv[:, qd + kd:].reshape(nb, c.n_kv_heads, c.head_dim)
-            q = st(rope(rmsnorm(q, w[p + "q_norm"], c.rms_eps), pos[:, None], c.rope_theta))
-            k = st(rope(rmsnorm(k, w[p + "k_norm"], c.rms_eps), pos[:, None], c.rope_theta))
-            v = st(v)
-            gate = sigmoid(linear(w[p + "w_g"], x)) if c.gated_attention else None
-            o = self.attention(q, k, v, pos, ctx["k"][l], ctx["v"][l], cpos)
-            if gate is not None:
-                o = o * gate[:, :, None]
-            o = st(o.reshape(nb, qd))
-            h = st(h + linear(w[p + "w_o"], o))
-            y = st(rmsnorm(h, w[p + "post_norm"], c.rms_eps))
-            a = st(silu(linear(w[p + "w_gate"], y)) * linear(w[p + "w_up"], y))
-            h = st(h + linear(w[p + "w_down"], a))
+        for l in range(self.cfg.n_layers):
+            h = self.block_layer(l, h, pos, ctx["k"][l], ctx["v"][l], cpos)
         return h
 
-    def unembed(self, h_rows):
-        """Raw draft logits of block rows (final norm, then the unembedding)."""
+    def unembed(self, h_rows, lo=0, hi=None):
+        """Raw draft logits of block rows (final norm, then the unembedding);
+        lo/hi select a slice of the vocabulary."""
         z = self.st(rmsnorm(h_rows, self.w["final_norm"], self.cfg.rms_eps))
-        return linear(self.w["unembed"], z)
+        U = self.w.src["unembed"]
+        return linear(np.asarray(U[lo:hi], dtype=np.float64), z)
 
 
 # ---------------------------------------------------------------------------

@@ -50,24 +50,39 @@ def export_kv(D, sess, cfg, layer, first, n):
 
 
 def oracle_scores(logits, T, seed, rnd, seq):
-    """The score whose argmax is the drawn token, and its top-2 margin, per row."""
-    logits = np.atleast_2d(logits)
-    out, margins = [], []
+    """The oracle's score whose argmax is the drawn token, per row: l/T plus
+    the draft's Gumbel noise at T > 0, the raw logits at T = 0."""
+    logits = np.atleast_2d(np.asarray(logits, dtype=np.float64))
+    out = []
     for i, row in enumerate(logits):
-        s = row / T if T > 0 else row.copy()
         if T > 0:
-            s = s + O.gumbel(seed, rnd, O.STREAM_DRAFT, seq, i + 1, np.arange(len(row)))
-        top = np.sort(s)[-2:]
-        out.append(s)
-        margins.append(top[1] - top[0])
-    return np.array(out), np.array(margins)
+            out.append(row / T + O.gumbel(seed, rnd, O.STREAM_DRAFT, seq, i + 1, np.arange(len(row))))
+        else:
+            out.append(row.copy())
+    return np.array(out)
 
 
-def assert_tokens(gpu_tok, ora_tok, margins, margin=MARGIN):
+def check_tokens(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq):
+    """Token ids must equal the oracle's.  The one exemption is a row where the
+    two sides' logits differ by delta and the oracle's score of the GPU's
+    token is within max(1e-3, 2 delta / T) of the oracle's top score: there
+    the choice is decided by rounding, not by the method (bf16 storage at the
+    same points on both sides still leaves logits up to ~1e-2 apart).
+    Returns the number of exempted rows."""
     gpu_tok = np.asarray(gpu_tok).reshape(-1)
-    ora_tok = np.asarray(ora_tok).reshape(-1)
-    margins = np.asarray(margins).reshape(-1)
-    bad = (gpu_tok != ora_tok) & (margins >= margin)
-    assert not bad.any(), f"token mismatch at rows {np.nonzero(bad)[0]}: gpu {gpu_tok[bad]} oracle {ora_tok[bad]} " \
-                          f"margins {margins[bad]}"
-    return int(((gpu_tok != ora_tok)).sum())
+    gl = np.atleast_2d(np.asarray(gpu_logits, dtype=np.float64))
+    ol = np.atleast_2d(np.asarray(ora_logits, dtype=np.float64))
+    sc = oracle_scores(ol, T, seed, rnd, seq)
+    teff = T if T > 0 else 1.0
+    exempt = 0
+    for i in range(len(gpu_tok)):
+        top = int(np.argmax(sc[i]))
+        g = int(gpu_tok[i])
+        if g == top:
+            continue
+        delta = float(np.max(np.abs(gl[i] - ol[i])))
+        bound = max(MARGIN, 2.0 * delta / teff)
+        gap = sc[i][top] - sc[i][g]
+        assert gap <= bound, f"row {i}: gpu token {g}, oracle {top}, score gap {gap:.3g} > bound {bound:.3g}"
+        exempt += 1
+    return exempt
