@@ -25,7 +25,7 @@ __all__ = [
     "dflash_model_create", "dflash_model_destroy", "dflash_draft_limit", "dflash_device_status", "dflash_open",
     "dflash_committed", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
     "dflash_close", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
-    "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read",
+    "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read", "dflash_verify_noalloc",
 ]
 
 
@@ -176,6 +176,18 @@ def dflash_verify(sessions, target_logits: torch.Tensor, draft_tokens: torch.Ten
         raise ValueError("target logits must be fp32 or bf16")
     _check(lib.dflash_verify(arr, b, _ptr(target_logits), dt, _ptr(draft_tokens), n, float(temperature), seed, rnd,
                              _ptr(out_accept), _ptr(out_bonus)))
+
+
+def dflash_verify_noalloc(sessions, target_logits: torch.Tensor, draft_tokens: torch.Tensor, n: int,
+                          temperature: float, seed: int, rnd: int, out_accept: torch.Tensor,
+                          out_bonus: torch.Tensor) -> None:
+    """dflash_verify on the library's static scratch (no device allocation)."""
+    arr, b = _sessions(sessions)
+    if target_logits.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("target logits must be fp32 or bf16")
+    dt = DFLASH_DTYPE_BF16 if target_logits.dtype == torch.bfloat16 else DFLASH_DTYPE_F32
+    _check(lib.dflash_verify_noalloc(arr, b, _ptr(target_logits), dt, _ptr(draft_tokens), n, float(temperature), seed,
+                                     rnd, _ptr(out_accept), _ptr(out_bonus)))
 
 
 def dflash_close(session: Session) -> None:

@@ -74,6 +74,8 @@ SIGNATURES = {
                                  C.POINTER(C.c_int32)]),
     "dflash_verify": (C.c_int, [SessArr, C.c_int32, P, C.c_int32, P, C.c_int32, C.c_float, C.c_uint64, C.c_uint64,
                                 P, P]),
+    "dflash_verify_noalloc": (C.c_int, [SessArr, C.c_int32, P, C.c_int32, P, C.c_int32, C.c_float, C.c_uint64,
+                                        C.c_uint64, P, P]),
     "dflash_close": (C.c_int, [P]),
     "dflash_stats": (C.c_int, [P, C.POINTER(dflash_counters)]),
     "dflash_session_state": (C.c_int, [P, C.POINTER(C.c_int64), C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),

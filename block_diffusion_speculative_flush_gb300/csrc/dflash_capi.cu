@@ -575,6 +575,27 @@ int check_sessions(dflash_session* const* s, int32_t batch) {
 // ===========================================================================
 extern "C" {
 
+// Internal accessors for the allocation-free verify (verify_noalloc.cu);
+// hidden symbols, not part of the ABI.
+int dflash__set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+int dflash__session_proposal(const dflash_session* s, const float** logits, const float** lse,
+                             const int32_t** tokens, float* temperature, int32_t* n, long long** accepted,
+                             void** stream, int32_t* vocab, int32_t* draft_limit, int32_t** err, const void** model) {
+  *logits = s->plogits;
+  *lse = s->plse;
+  *tokens = s->ptok;
+  *temperature = s->last_T;
+  *n = s->has_prop ? s->last_n : 0;
+  *accepted = s->d_accepted;
+  *stream = (void*)s->stream;
+  *vocab = s->m->cfg.vocab;
+  *draft_limit = s->m->cfg.block_size - 1;
+  *err = s->m->d_err;
+  *model = s->m;
+  return DFLASH_OK;
+}
+
 const char* dflash_last_error(void) { return g_err.c_str(); }
 int dflash_version(void) { return 100; }
 

@@ -220,6 +220,28 @@ DFLASH_API int dflash_verify(dflash_session* const* s /*host [batch]*/, int32_t 
                   int32_t logits_dtype, const int32_t* draft_tokens, int32_t n, float temperature, uint64_t seed,
                   uint64_t round, int32_t* out_accept, int32_t* out_bonus);
 
+/* The same verification as dflash_verify, for callers that may not allocate
+ * device memory: a serving runtime that hands out all GPU memory up front
+ * under a fixed budget, or a decode loop that cannot take cudaMalloc's
+ * implicit device synchronisation between rounds.  (The pages have no
+ * counterpart; this is a property of this library.)  dflash_verify grows a
+ * model workspace with cudaMalloc on demand; this call never calls cudaMalloc,
+ * cudaFree or an allocating routine.  Its scratch is a 4 MiB array inside the
+ * library image, present on every GPU that loads the library until the
+ * process exits.  Limits: at most 128 sessions per call, and
+ * batch * (n + 1) * ceil(V / 4096) 16-byte row partials plus the bonus
+ * partials must fit the 4 MiB (about 200k partials); larger calls return
+ * DFLASH_ERR_CAPACITY and change nothing.  The first call on a device looks
+ * up the scratch's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call
+ * shares the one scratch area, so calls that overlap on the GPU (different
+ * streams, no ordering between them) race; issue them in stream order.
+ * Arguments, outputs and errors otherwise as dflash_verify. */
+DFLASH_API int dflash_verify_noalloc(dflash_session* const* s /*host [batch]*/, int32_t batch,
+                                     const void* target_logits, int32_t logits_dtype, const int32_t* draft_tokens,
+                                     int32_t n, float temperature, uint64_t seed, uint64_t round,
+                                     int32_t* out_accept, int32_t* out_bonus);
+
 /* dflash.go close: flush, then release the session (synchronises its stream). */
 DFLASH_API int dflash_close(dflash_session* s);
 
