@@ -58,6 +58,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["round", "flush", "laguna", "batched"], default="round",
+                    help="round: the bs1 Qwen3-8B-shaped round (the default line); flush: 8 sequences x 256-row "
+                         "context flushes; laguna: window-512 gated draft, bs1, blocks 16 and 8; batched: 64 "
+                         "sequences, contexts 1k-16k, propose + rejection-sampling verify at T=0.7")
     return ap.parse_args(argv)
 
 
@@ -174,8 +178,10 @@ def round_bytes(cfg, ctx, P):
     K/V read once per layer, the features read once, the new K/V written once,
     the logits written and read once, the target logits read once."""
     H, I, V = cfg.hidden, cfg.intermediate, cfg.vocab
-    qkv = cfg.qkv_rows * H
+    qkv = (cfg.qkv_rows + (cfg.n_q_heads if cfg.gated_attention else 0)) * H
     per_layer = qkv + H * cfg.n_q_heads * cfg.head_dim + 3 * H * I
+    if cfg.window:
+        ctx = min(ctx, cfg.window - 1)
     weights = 2 * (cfg.n_layers * per_layer + V * H + (H * cfg.feature_width if P else 0))
     nb = cfg.block_size
     kv_row = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * cfg.n_layers
@@ -226,7 +232,7 @@ def run_ours(args, rank, world, local_rank):
     g.manual_seed(SEED + 1000 + rank)
     sessions = []
     with torch.cuda.stream(stream):
-        for _ in range(2):   # one for the kernel-only loop, one for the end-to-end loop
+        for _ in range(3):   # kernel-only loop, end-to-end loop, instrumented loop
             s = D.dflash_open(model, max_ctx=max_ctx, stream=stream)
             for lo in range(0, start_ctx, 1024):
                 hi = min(start_ctx, lo + 1024)
@@ -254,12 +260,12 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for i in range(W):
             step(sa, i, feats[i], tl)
+            step(sessions[2], i, feats[i], tl)
     stream.synchronize()
     clocks = ClockSampler(local_rank)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    D.dflash_timing_enable(model, True)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -270,10 +276,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    timing = D.dflash_timing_read(model)
-    D.dflash_timing_enable(model, False)
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, world, dev)
+
+    # ---- the same steps again with CUDA events around every instrumented
+    # launch (per-kernel-class durations for the roofline; the events break
+    # the launch overlap, so this pass is not the one that gives `value`)
+    sc = sessions[2]
+    D.dflash_timing_enable(model, True)
+    with torch.cuda.stream(stream):
+        for i in range(W, W + K):
+            step(sc, i, feats[i], tl)
+    timing = D.dflash_timing_read(model)
+    D.dflash_timing_enable(model, False)
 
     # ---- end to end through the public API with host buffers ----
     sb = sessions[1]
@@ -342,7 +357,7 @@ def run_ours(args, rank, world, local_rank):
                          "peak_kind": f"{peak_kind} HBM copy bandwidth",
                          "algorithmic_bytes_per_launch": round(gt["bytes"] / launches) if launches else None,
                          "traffic": traffic, "launches": launches},
-            "kernel_classes": {k: {"launches": v["launches"], "ms_per_step": round(v["total_ms"] / K, 4),
+            "kernel_classes_instrumented": {k: {"launches": v["launches"], "ms_per_step": round(v["total_ms"] / K, 4),
                                    "gbs": round(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 1)
                                    if v["total_ms"] else None}
                                for k, v in timing.items()},
@@ -362,6 +377,208 @@ def run_ours(args, rank, world, local_rank):
     if result is not None and host_w is not None:
         result["cpu_baseline"] = cpu_baseline(cfg, host_w)
     return result
+
+
+# ---------------------------------------------------------------------------
+# further workloads (one JSON line each; the default line is the round above)
+# ---------------------------------------------------------------------------
+def _timed(torch, stream, fn, K, W, local_rank, world, dev):
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            fn(i)
+    stream.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(W, W + K):
+            fn(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    return max_over_ranks(e0.elapsed_time(e1), world, dev), clk
+
+
+def _line(metric, unit, value, world, K, W, ms, dtype, config, extra, clk):
+    out = {"metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K, "warmup": W,
+           "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": dtype, "data": "synthetic (random-init draft weights, N(0,1) features and K/V)",
+           "config": config, "clocks": clk}
+    out.update(extra)
+    return out
+
+
+def run_workload(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import block_diffusion_speculative_flush_gb300 as D
+    import synthetic as S
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist_init(world, "nccl")
+    K, W = args.steps, args.warmup
+    stream = torch.cuda.Stream(device=dev)
+    peaks, peak_kind = measured_peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 7 + rank)
+
+    if args.workload == "flush":
+        # 8 sequences at context offsets 0, 1k, ..., 7k; each step every
+        # sequence commits 256 new feature rows, which reach the pending
+        # threshold and flush in one context-only forward (M = 256)
+        cfg = S.CONFIGS[CFG_NAME]
+        rows, nseq = 256, 8
+        model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED + rank, dev))
+        with torch.cuda.stream(stream):
+            sess = [D.dflash_open(model, restored_offset=1024 * j, max_ctx=1024 * j + rows * (2 * K + W + 8),
+                                  stream=stream) for j in range(nseq)]
+            feats = torch.randn((rows, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+            n = cfg.block_size - 1
+            cur = torch.full((1,), 3, dtype=torch.int32, device=dev)
+            tok = torch.empty((1, n), dtype=torch.int32, device=dev)
+            q = torch.empty((1, n), dtype=torch.float32, device=dev)
+            for s_ in sess[1:]:      # an outstanding block that the first flush rewinds
+                D.dflash_propose([s_], cur, n, 0.0, 0, 0, tok, q)
+
+        def step(i):
+            for j, s_ in enumerate(sess):
+                D.dflash_committed(s_, feats, 1024 * j + rows * i)
+
+        ms, clk = _timed(torch, stream, step, K, W, local_rank, world, dev)
+        for j, s_ in enumerate(sess):       # cursor consistency after every rewind + flush
+            assert D.dflash_session_state(s_) == (1024 * j + rows * (K + W), 0, False)
+        # the same rows as one batched flush: 255 staged rows per sequence, one forward of 2040 rows
+        def step_b(i):
+            for j, s_ in enumerate(sess):
+                D.dflash_committed(s_, feats[:rows - 1], 1024 * j + rows * (K + W) + (rows - 1) * i)
+            D.dflash_flush(sess)
+
+        Kb = max(1, K // 2)
+        ms_b, _ = _timed(torch, stream, step_b, Kb, 1, local_rank, world, dev)
+        kv_params = 2 * cfg.n_kv_heads * cfg.head_dim * cfg.hidden * cfg.n_layers
+        fc_params = cfg.hidden * cfg.feature_width
+        flops = 2.0 * rows * nseq * (fc_params + kv_params)
+        tflops = flops / (ms / K * 1e-3) / 1e12
+        peak_t = peaks.get("bf16_tflops_sustained", 1700.0)
+        for s_ in sess:
+            D.dflash_close(s_)
+        return _line("flush rows/s (8 sequences x 256 pending rows, Qwen3-8B-shaped draft)", "rows/s",
+                     world * rows * nseq / (ms / K * 1e-3), world, K, W, ms, "bf16",
+                     {"workload": "8 x committed(256 rows [256, 20480]) at context offsets 0..7k, each a "
+                                  "context-only forward after a block rewind", "l2": "252 MB of fc/K/V weights "
+                                  "per flush; features 10.5 MB resident"},
+                     {"roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak_t,
+                                   "unit": "TFLOP/s", "frac": round(tflops / peak_t, 4),
+                                   "peak_kind": f"{peak_kind} bf16 (sustained)"},
+                      "batched_flush_rows_s": round(world * (rows - 1) * nseq / (ms_b / Kb * 1e-3), 1),
+                      "gpu_launches": None}, clk)
+
+    if args.workload == "laguna":
+        res = {}
+        for bs in (16, 8):
+            cfg = S.CONFIGS["laguna_bf16"].replace(block_size=bs)
+            n = bs - 1
+            model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED + rank, dev))
+            T = 32768
+            with torch.cuda.stream(stream):
+                s_ = D.dflash_open(model, max_ctx=T + P_ROWS * (K + W + 4) + 64, stream=stream)
+                for lo in range(0, T, 4096):      # rows older than the window are dropped before the fc
+                    f = torch.randn((4096, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+                    D.dflash_committed(s_, f, lo)
+                    del f
+                D.dflash_flush([s_])
+                feats = torch.randn((W + K, P_ROWS, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+                tl = (torch.randn((1, n + 1, cfg.vocab), generator=g, device=dev) * 3.0).contiguous()
+                cur = torch.full((1,), 17, dtype=torch.int32, device=dev)
+                tok = torch.empty((1, n), dtype=torch.int32, device=dev)
+                q = torch.empty((1, n), dtype=torch.float32, device=dev)
+                acc = torch.empty(1, dtype=torch.int32, device=dev)
+                bon = torch.empty(1, dtype=torch.int32, device=dev)
+
+            def step(i):
+                D.dflash_committed(s_, feats[i], T + P_ROWS * i)
+                D.dflash_propose([s_], cur, n, TEMP, SEED, i, tok, q)
+                D.dflash_verify([s_], tl, tok, n, TEMP, SEED, i, acc, bon)
+
+            ms, clk = _timed(torch, stream, step, K, W, local_rank, world, dev)
+            rb = round_bytes(cfg, T, P_ROWS)
+            res[bs] = (world * K / (ms * 1e-3), ms, clk, rb)
+            D.dflash_close(s_)
+            del model
+            torch.cuda.empty_cache()
+        v16, ms16, clk16, rb16 = res[16]
+        gbs = rb16 / (ms16 / K * 1e-3) / 1e9
+        return _line("draft rounds/s (Laguna-style gated window-512 draft, bs1, block 16)", "draft rounds/s", v16,
+                     world, K, W, ms16, "bf16",
+                     {"workload": "laguna_bf16: 4 layers, H 3072, 24/8 heads x 128, I 8192 (assumed), V 100352, "
+                                  "window 512 over a 32768-row temporal context, 4 committed rows per round, T=1.0",
+                      "l2": "no flush: 2.1 GB of weights streamed per round"},
+                     {"round_roofline": {"bound": "hbm", "algorithmic_bytes": rb16, "achieved_gbs": round(gbs, 1),
+                                         "peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)},
+                      "block8_rounds_s": round(res[8][0], 2),
+                      "block8_round_roofline_frac": round(res[8][3] / (res[8][1] / K * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                                          4)}, clk16)
+
+    # batched serving mix
+    cfg = S.CONFIGS[CFG_NAME]
+    B, n, Tb = 64, cfg.block_size - 1, 0.7
+    ctxs = np.random.default_rng(0).integers(1024, 16385, size=B)
+    model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED + rank, dev))
+    with torch.cuda.stream(stream):
+        sess = []
+        for b in range(B):
+            c = int(ctxs[b])
+            s_ = D.dflash_open(model, restored_offset=c, max_ctx=c + P_ROWS * (K + W + 4) + 64, stream=stream)
+            for l in range(cfg.n_layers):      # restored context: seeded K/V rows
+                kk = torch.randn((cfg.n_kv_heads, c, cfg.head_dim), generator=g, device=dev).to(torch.bfloat16)
+                vv = torch.randn((cfg.n_kv_heads, c, cfg.head_dim), generator=g, device=dev).to(torch.bfloat16)
+                D.dflash_kv_import(s_, l, 0, c, kk, vv)
+                del kk, vv
+            sess.append(s_)
+        feats = torch.randn((B, P_ROWS, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+        tl = (torch.randn((B, n + 1, cfg.vocab), generator=g, device=dev) * 3.0).contiguous()
+        cur = torch.randint(0, cfg.vocab, (B,), generator=g, device=dev, dtype=torch.int32)
+        tok = torch.empty((B, n), dtype=torch.int32, device=dev)
+        q = torch.empty((B, n), dtype=torch.float32, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        bon = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def step(i):
+        for b, s_ in enumerate(sess):
+            D.dflash_committed(s_, feats[b], int(ctxs[b]) + P_ROWS * i)
+        D.dflash_propose(sess, cur, n, Tb, SEED, i, tok, q)
+        D.dflash_verify(sess, tl, tok, n, Tb, SEED, i, acc, bon)
+
+    ms, clk = _timed(torch, stream, step, K, W, local_rank, world, dev)
+    H, I, V = cfg.hidden, cfg.intermediate, cfg.vocab
+    per_layer = cfg.qkv_rows * H + H * cfg.n_q_heads * cfg.head_dim + 3 * H * I
+    gemm_flops = 2.0 * (B * (n + 1) * (cfg.n_layers * per_layer) + B * n * V * H +
+                        B * P_ROWS * (H * cfg.feature_width + cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * H))
+    kv_bytes = float(sum(int(c) + 2 * P_ROWS * (K + W) // 2 + n + 1 for c in ctxs)) * cfg.n_layers * 2 * \
+        cfg.n_kv_heads * cfg.head_dim * 2
+    t_step = ms / K * 1e-3
+    ideal = gemm_flops / (peaks.get("bf16_tflops_sustained", 1700.0) * 1e12) + \
+        (kv_bytes + B * (n + 1) * V * 4) / (peaks["hbm_gbs"] * 1e9)
+    D.dflash_device_status(model)
+    for s_ in sess:
+        D.dflash_close(s_)
+    return _line("proposed tok/s (bs64 serving mix, Qwen3-8B-shaped draft, block 16, ctx 1k-16k)", "proposed tok/s",
+                 world * B * n / t_step, world, K, W, ms, "bf16",
+                 {"workload": "64 sequences, contexts uniform 1k-16k (seeded K/V), 4 committed rows each per round, "
+                              "batched propose + rejection-sampling verify at T=0.7 on N(0,3) target logits "
+                              "[64,16,151936]", "l2": "no flush: 11+ GB of K/V and 3.4 GB of weights per round"},
+                 {"rounds_s": round(world / t_step, 2),
+                  "roofline": {"bound": "mixed (GEMMs tensor, attention and verify HBM)",
+                               "ideal_ms_per_step": round(ideal * 1e3, 3), "frac": round(ideal / t_step, 4),
+                               "gemm_tflop_per_step": round(gemm_flops / 1e12, 3),
+                               "kv_gb_per_step": round(kv_bytes / 1e9, 2)}}, clk)
 
 
 # ---------------------------------------------------------------------------
@@ -504,6 +721,8 @@ def main(argv=None):
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
+    elif args.workload != "round":
+        out = run_workload(args, rank, world, local_rank)
     else:
         out = run_ours(args, rank, world, local_rank)
     if rank == 0 and out is not None:

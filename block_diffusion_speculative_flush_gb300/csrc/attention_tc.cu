@@ -1,0 +1,357 @@
+// Block attention on the sm_103a tensor cores (tcgen05 + TMEM + TMA) for bf16
+// drafts with head_dim 128: the n+1 block rows x the group's query heads of
+// one KV head attend over one range of key positions (context, then the
+// block's own rows), with the window limit and the causal / bidirectional
+// in-block mask applied per query row (Laguna PR: the window is a per-query
+// limit over [context | block]).
+//
+// One CTA per work item (session, KV head, key range starting on a multiple
+// of 64).  Query rows (at most 128, zero padded) form the MMA's M = 128 side.
+//   warp 8        TMA: a 64-key K tile [64 keys][128 d] and the matching
+//                 V^T tile [128 d][64 keys] per stage (3 stages); the cache
+//                 keeps V transposed so that both are K-major operand tiles.
+//   warp 9        MMA: S = Q K^T into one of two TMEM buffers, then
+//                 O += P V^T (P as a bf16 hi + lo pair, ~16 bits of the
+//                 probabilities) into the TMEM accumulator.
+//   warps 0..7    softmax, two threads per query row (warps w and w + 4 read
+//                 the same TMEM lanes; each takes 32 keys of a tile and 64
+//                 columns of O): S from TMEM, mask against the row's visible
+//                 key range, online max in the exp2 domain with lazy
+//                 rescaling (O and the sum are rescaled only when the row max
+//                 grows by more than 2^8, so P <= 256), P written to shared
+//                 memory as the next MMA's A operand; finally O and
+//                 (max, sum) go out as this key range's partial.
+// Every wait is bounded; an expired wait sets bit 8 of the error word.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace dfl {
+
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;                       // head dim
+constexpr int KT = 64;                       // keys per tile (MMA N of S)
+constexpr int ST = 3;                        // K/V stages in flight
+constexpr int QBYTES = 128 * D * 2;          // Q: two [128 rows][64 d] swizzled blocks
+constexpr int KBYTES = KT * D * 2;           // K tile: two [64 keys][64 d] blocks
+constexpr int VBYTES = D * KT * 2;           // V^T tile: one [128 d][64 keys] block
+constexpr int PBYTES = 128 * KT * 2;         // P tile: one [128 rows][64 keys] block
+constexpr int DATA_BYTES = QBYTES + ST * (KBYTES + VBYTES) + 4 * PBYTES;  // + barriers and 1 KB exchange
+constexpr int THREADS = 320;
+constexpr int SOFTMAX_THREADS = 256;
+constexpr uint32_t TMEM_COLS = 256;          // O [0,128), S0 [128,192), S1 [192,256)
+
+__device__ __forceinline__ bool visible(int64_t F, int i, int64_t r, int window, int causal) {
+  if (window && (F + i) - r >= window) return false;
+  if (causal && r >= F && (r - F) > i) return false;
+  return true;
+}
+
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// byte offset of 16-byte chunk c of row r inside a [rows][128 B] swizzled block
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__ Q, const AttnItem* __restrict__ items,
+                                                        SessTables tabs, AttnParams p, float* __restrict__ part,
+                                                        int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + QBYTES;
+  uint8_t* sV = sK + ST * KBYTES;
+  uint8_t* sP = sV + ST * VBYTES;  // [2 buffers][hi, lo]
+  uint64_t* kv_full = (uint64_t*)(sP + 4 * PBYTES);
+  uint64_t* kv_empty = kv_full + ST;
+  uint64_t* s_full = kv_empty + ST;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* o_done = pv_done + 2;
+  uint32_t* tmem_slot = (uint32_t*)(o_done + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  // [3][2][128]: per-half row max (one buffer per tile parity, so a thread
+  // never overwrites a value its partner has not read) and the final sum
+  float* xch = (float*)(tmem_slot + 4);
+
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const AttnItem it = items[blockIdx.x];
+  const int G = p.Hq / p.Hkv, R = p.nrows * G;
+  const int64_t F = tabs.frontier[it.sess], cap = tabs.cap[it.sess];
+  const CUtensorMap* kmap = tabs.kvmaps[it.sess];
+  const CUtensorMap* vmap = kmap + 1;
+  const int planeK = 2 * p.layer * p.Hkv + it.kvh, planeV = (2 * p.layer + 1) * p.Hkv + it.kvh;
+  const int T = (int)((it.k1 - it.k0 + KT - 1) / KT);
+
+  if (tid == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], SOFTMAX_THREADS);
+      mbar_init(&p_full[b], SOFTMAX_THREADS);
+      mbar_init(&pv_done[b], 1);
+    }
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)kmap) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)vmap) : "memory");
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    fence_before();
+  }
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // Q and the block's K/V come from the previous kernel
+
+  // ---- Q rows of this KV head, zero padded to 128, as the MMA's A tile
+  if (warp < 8) {
+    // all 8 loads of a thread are issued before the first store
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = tid + SOFTMAX_THREADS * k, r = e >> 4, c = e & 15;
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        const int i = r / G, g = r % G;
+        v[k] = __ldg(reinterpret_cast<const uint4*>(
+            Q + (((int64_t)it.sess * p.nrows + i) * p.Hq + it.kvh * G + g) * D + c * 8));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = tid + SOFTMAX_THREADS * k, r = e >> 4, c = e & 15;
+      *reinterpret_cast<uint4*>(sQ + (c >> 3) * (QBYTES / 2) + swz(r, c & 7)) = v[k];
+    }
+    fence_proxy_async();
+  }
+  __syncthreads();
+
+  if (warp == 8) {
+    if (lane == 0) {
+      // ---- TMA producer
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % ST;
+        if (t >= ST && !mbar_wait(&kv_empty[s], (uint32_t)((t / ST) - 1) & 1u, abort_flag)) {
+          atomicOr(err, 8);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_expect_tx(&kv_full[s], KBYTES + VBYTES);
+        const int slot0 = (int)((it.k0 + (int64_t)t * KT) % cap);
+        tma_load_3d(sK + s * KBYTES, kmap, &kv_full[s], 0, slot0, planeK);
+        tma_load_3d(sK + s * KBYTES + KBYTES / 2, kmap, &kv_full[s], 64, slot0, planeK);
+        tma_load_3d(sV + s * VBYTES, vmap, &kv_full[s], slot0, 0, planeV);
+        ++issued;
+      }
+      if (*abort_flag) {  // let this CTA's own copies land before leaving
+        for (int t = issued - ST > 0 ? issued - ST : 0; t < issued; ++t) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&kv_full[t % ST], (uint32_t)(t / ST) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      constexpr uint32_t idS = idesc_bf16(128, KT), idPV = idesc_bf16(128, D);
+      const uint32_t tO = tmem;
+      auto issue_pv = [&](int u) -> bool {
+        const int pb = u & 1, s = u % ST;
+        if (!mbar_wait(&p_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag)) return false;
+        fence_after();
+        const uint32_t ph = smem_u32(sP + pb * 2 * PBYTES), pl = ph + PBYTES, v0 = smem_u32(sV + s * VBYTES);
+#pragma unroll
+        for (int ks = 0; ks < KT / 16; ++ks)
+          umma_bf16(tO, sdesc_sw128(ph + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, (u > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < KT / 16; ++ks) umma_bf16(tO, sdesc_sw128(pl + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, 1u);
+        umma_commit(&pv_done[pb]);
+        umma_commit(&kv_empty[s]);
+        return true;
+      };
+      bool ok = true;
+      for (int t = 0; t < T && ok; ++t) {
+        const int s = t % ST, sb = t & 1;
+        if (!mbar_wait(&kv_full[s], (uint32_t)(t / ST) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (t >= 2 && !mbar_wait(&s_free[sb], (uint32_t)((t >> 1) - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + s * KBYTES);
+        const uint32_t tS = tmem + 128 + sb * KT;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_bf16(tS, sdesc_sw128(q0 + (ks >> 2) * (QBYTES / 2) + (ks & 3) * 32),
+                    sdesc_sw128(k0 + (ks >> 2) * (KBYTES / 2) + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
+        umma_commit(&s_full[sb]);
+        if (t >= 1) ok = issue_pv(t - 1);
+      }
+      if (ok && T > 0) ok = issue_pv(T - 1);
+      if (!ok) {
+        atomicOr(err, 8);
+        *abort_flag = 1;
+      }
+      umma_commit(o_done);  // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ---- softmax: two threads per query row (row = TMEM lane)
+    const int r = (warp & 3) * 32 + lane;
+    const int half = warp >> 2;                // keys [32 half, +32) of a tile, O columns [64 half, +64)
+    const bool rv = r < R;
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+    const float sl2 = p.scale * 1.4426950408889634f;
+    // the row's visible key positions form one interval [vlo, vhi]
+    int64_t vlo = it.k0, vhi = it.k1 - 1;
+    if (rv) {
+      const int64_t qpos = F + r / G;
+      if (p.window) vlo = vlo > qpos - p.window + 1 ? vlo : qpos - p.window + 1;
+      if (p.causal) vhi = vhi < qpos ? vhi : qpos;
+    } else {
+      vlo = 1;
+      vhi = 0;
+    }
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int sb = t & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, abort_flag));
+      if (!ok) break;
+      fence_after();
+      float s[32];
+      tmem_ld32(tmem + lrow + 128 + sb * KT + 32 * half, s);
+      fence_before();
+      mbar_arrive(&s_free[sb]);
+      const int64_t kt = it.k0 + (int64_t)t * KT + 32 * half;
+      const int64_t lo64 = vlo - kt, hi64 = vhi - kt;
+      const int lo = lo64 < 0 ? 0 : (lo64 > 32 ? 32 : (int)lo64);
+      const int hi = hi64 < -1 ? -1 : (hi64 > 31 ? 31 : (int)hi64);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        s[j] = (j >= lo && j <= hi) ? s[j] * sl2 : -INFINITY;
+        mt = fmaxf(mt, s[j]);
+      }
+      // both threads of a row agree on the tile max
+      float* xt = xch + (t & 1) * 256;
+      xt[half * 128 + r] = mt;
+      asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
+      mt = fmaxf(mt, xt[(half ^ 1) * 128 + r]);
+      // lazy rescale: move the reference max only when it grows past 2^8
+      const bool grow = mt > m_used + 8.f;
+      const float m_new = grow ? mt : m_used;
+      const float f = (grow && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
+      if (__any_sync(0xffffffffu, f != 1.f)) {
+        // O must hold every earlier tile's product before it is scaled
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag));
+        if (!ok) break;
+        fence_after();
+#pragma unroll 1
+        for (int c = 64 * half; c < 64 * half + 64; c += 32) {
+          float o[32];
+          tmem_ld32(tmem + lrow + c, o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] *= f;
+          tmem_st32(tmem + lrow + c, o);
+        }
+      }
+      l *= f;
+      m_used = m_new;
+      uint32_t hi2[16], lo2[16];
+      float ls = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float p0 = exp2f(s[j] - m_used), p1 = exp2f(s[j + 1] - m_used);  // exp2(-inf) = 0
+        ls += p0 + p1;
+        split_pack(p0, p1, hi2[j / 2], lo2[j / 2]);
+      }
+      l += ls;
+      const int pb = t & 1;
+      if (t >= 2) {  // the P buffer is free once the product of tile t-2 is done
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[pb], (uint32_t)((t >> 1) - 1) & 1u, abort_flag));
+        if (!ok) break;
+      }
+      uint8_t* ph = sP + pb * 2 * PBYTES;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int cc = 4 * half + c;
+        *reinterpret_cast<uint4*>(ph + swz(r, cc)) = make_uint4(hi2[4 * c], hi2[4 * c + 1], hi2[4 * c + 2], hi2[4 * c + 3]);
+        *reinterpret_cast<uint4*>(ph + PBYTES + swz(r, cc)) =
+            make_uint4(lo2[4 * c], lo2[4 * c + 1], lo2[4 * c + 2], lo2[4 * c + 3]);
+      }
+      fence_proxy_async();
+      fence_before();
+      mbar_arrive(&p_full[pb]);
+    }
+    if (!ok) {
+      atomicOr(err, 8);
+      *abort_flag = 1;
+    }
+    // ---- partial of this key range: (max in natural-log units, sum, -, -, O)
+    if (!mbar_wait(o_done, 0, abort_flag) && !mbar_wait(o_done, 0, abort_flag)) atomicOr(err, 8);
+    fence_after();
+    float* xl = xch + 2 * 256;
+    xl[half * 128 + r] = l;
+    asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
+    float* pr = part + ((int64_t)blockIdx.x * R + (rv ? r : 0)) * (D + 4);
+    if (rv && half == 0) {
+      *reinterpret_cast<float4*>(pr) = make_float4(m_used == -INFINITY ? -INFINITY : m_used * 0.6931471805599453f,
+                                                   xl[r] + xl[128 + r], 0.f, 0.f);
+    }
+#pragma unroll 1
+    for (int c = 64 * half; c < 64 * half + 64; c += 32) {
+      float o[32];
+      tmem_ld32(tmem + lrow + c, o);
+      if (rv) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(pr + 4 + c + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+bool launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
+                         int* err, cudaStream_t st) {
+  const int R = p.nrows * (p.Hq / p.Hkv);
+  if (p.d != D || R > 128 || !tabs.kvmaps) return false;
+  if (n_items <= 0) return true;
+  const size_t smem = (size_t)DATA_BYTES + 1024 + 256 + 3 * 1024;
+  cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_k(k_attn_tc, n_items, THREADS, smem, st, (const bf16*)Q, items, tabs, p, part, err);
+  return true;
+}
+
+}  // namespace dfl

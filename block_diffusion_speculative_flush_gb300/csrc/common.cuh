@@ -122,4 +122,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: every kernel lets the next one in the stream
+// be scheduled early (trigger) and waits for the previous one to finish and
+// flush its memory before reading anything it produced (wait).  Without the
+// launch attribute both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace dfl

@@ -177,6 +177,7 @@ struct dflash_session {
   float* plse = nullptr;    // [B_s-1]
   int32_t* ptok = nullptr;  // [B_s-1]
   long long* d_accepted = nullptr;
+  CUtensorMap* d_maps = nullptr;  // {K planes, V^T planes} for the tensor-core attention, or NULL
   bool has_prop = false;
   int last_n = 0;
   float last_T = 0.f;
@@ -347,9 +348,13 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     meta[r] = RowMeta{fw.ctx[r].sess, -1, fw.ctx[r].pos};
   }
   std::vector<void*> kvb(Bc);
+  std::vector<const CUtensorMap*> mapv(Bc);
   std::vector<int64_t> capv(Bc), front(Bc);
   std::vector<int32_t> seqv(Bc);
+  bool have_maps = true;
   for (int j = 0; j < Bc; ++j) {
+    mapv[j] = fw.sess[j]->d_maps;
+    have_maps = have_maps && mapv[j] != nullptr;
     kvb[j] = fw.sess[j]->kv;
     capv[j] = fw.sess[j]->cap;
     front[j] = fw.sess[j]->F;
@@ -365,7 +370,9 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     std::vector<int64_t> k0v(Bc), k1v(Bc);
     for (int j = 0; j < Bc; ++j) {
       const int64_t F = fw.sess[j]->F;
-      k0v[j] = c.window ? std::max<int64_t>(0, F - c.window + 1) : 0;
+      // ranges start on a multiple of 64 (a whole tensor-core key tile);
+      // positions before the window are masked per query
+      k0v[j] = (c.window ? std::max<int64_t>(0, F - c.window + 1) : 0) & ~(int64_t)63;
       k1v[j] = F + nrows;
       total += (k1v[j] - k0v[j]) * Hkv;
     }
@@ -384,11 +391,11 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   }
   const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
                o_front = tp.add(front), o_seq = tp.add(seqv), o_items = tp.add(items), o_ifirst = tp.add(ifirst),
-               o_icount = tp.add(icount), o_map = tp.add(fw.sess_map);
+               o_icount = tp.add(icount), o_map = tp.add(fw.sess_map), o_maps = tp.add(mapv);
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
   SessTables tabs{(void* const*)(tb + o_kv), (const int64_t*)(tb + o_cap), (const int64_t*)(tb + o_front),
-                  (const int32_t*)(tb + o_seq)};
+                  (const int32_t*)(tb + o_seq), have_maps ? (const CUtensorMap* const*)(tb + o_maps) : nullptr};
   const RowMeta* dmeta = (const RowMeta*)(tb + o_meta);
 
   // ---- buffers -----------------------------------------------------------
@@ -461,7 +468,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       Timed tm(m, kAttention, attn_bytes, attn_flops, st);
       const AttnItem* ditems = (const AttnItem*)(tb + o_items);
       if (m->dt != DT::BF16 ||
-          !launch_attention_mma(m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), st))
+          !launch_attention_tc(m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), m->d_err, st))
         launch_attention_simt(m->dt, m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), st);
       launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
                                (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
@@ -700,7 +707,8 @@ int dflash_device_status(dflash_model* m) {
     std::string why;
     if (e & 1) why += "anchor token id outside the vocabulary; ";
     if (e & 2) why += "draft token id outside the vocabulary; ";
-    if (e & 4) why += "tensor-core pipeline wait expired; ";
+    if (e & 4) why += "tensor-core GEMM pipeline wait expired; ";
+    if (e & 8) why += "tensor-core attention pipeline wait expired; ";
     return fail(DFLASH_ERR_DEVICE, "device reported: %s", why.c_str());
   }
   return DFLASH_OK;
@@ -729,6 +737,15 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->ptok, nb * 4);
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->d_accepted, 8);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->d_accepted, 0, 8, s->stream);
+  if (e == cudaSuccess && m->use_tc && c.head_dim == 128) {
+    CUtensorMap maps[2];
+    if (tc_encode_kv_maps(m->tc, s->kv, s->cap, c.head_dim, 2 * c.n_layers * c.n_kv_heads, maps) != 0) {
+      e = cudaErrorInvalidValue;
+    } else {
+      e = cudaMalloc((void**)&s->d_maps, sizeof maps);
+      if (e == cudaSuccess) e = cudaMemcpy(s->d_maps, maps, sizeof maps, cudaMemcpyHostToDevice);
+    }
+  }
   if (e != cudaSuccess) {
     cudaFree(s->kv);
     cudaFree(s->pending);
@@ -736,6 +753,7 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
     cudaFree(s->plse);
     cudaFree(s->ptok);
     cudaFree(s->d_accepted);
+    cudaFree(s->d_maps);
     delete s;
     return fail(e == cudaErrorMemoryAllocation ? DFLASH_ERR_OOM : DFLASH_ERR_CUDA, "session buffers: %s",
                 cudaGetErrorString(e));
@@ -953,8 +971,9 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   va.bonus = out_bonus;
   va.accepted_total = (long long* const*)(tb + o_acc);
   va.err = m->d_err;
-  ST_TRY(m->vbonus.ensure((size_t)batch * chunks * sizeof(VerifyPart) + (size_t)batch * 4, st));
-  va.rej = (int32_t*)(m->vbonus.as<char>() + (size_t)batch * chunks * sizeof(VerifyPart));
+  const int bchunks = verify_bonus_chunks(V);
+  ST_TRY(m->vbonus.ensure((size_t)batch * bchunks * sizeof(VerifyPart) + (size_t)batch * 4, st));
+  va.rej = (int32_t*)(m->vbonus.as<char>() + (size_t)batch * bchunks * sizeof(VerifyPart));
   launch_verify_accept(va, m->vbonus.as<VerifyPart>(), st);
   m->launches += temperature > 0.f ? 1 : 0;
   return launch_check("verify");
@@ -970,6 +989,7 @@ int dflash_close(dflash_session* s) {
   cudaFree(s->plse);
   cudaFree(s->ptok);
   cudaFree(s->d_accepted);
+  cudaFree(s->d_maps);
   delete s;
   return rc;
 }
@@ -1009,9 +1029,9 @@ int dflash_kv_export(const dflash_session* s, int32_t layer, int64_t first_slot,
   ST_TRY(kv_range_ok(s, layer, first_slot, n_rows));
   const dflash_config& c = s->m->cfg;
   const size_t plane = (size_t)c.n_kv_heads * s->cap * c.head_dim * s->m->esz;
-  const char* base = (const char*)s->kv + (size_t)(2 * layer) * plane;
-  launch_kv_copy(s->m->dt, k_out, n_rows, 0, base, s->cap, first_slot, n_rows, c.n_kv_heads, c.head_dim, s->stream);
-  launch_kv_copy(s->m->dt, v_out, n_rows, 0, base + plane, s->cap, first_slot, n_rows, c.n_kv_heads, c.head_dim,
+  char* base = (char*)s->kv + (size_t)(2 * layer) * plane;
+  launch_kv_copy(s->m->dt, base, s->cap, first_slot, k_out, n_rows, c.n_kv_heads, c.head_dim, false, false, s->stream);
+  launch_kv_copy(s->m->dt, base + plane, s->cap, first_slot, v_out, n_rows, c.n_kv_heads, c.head_dim, false, true,
                  s->stream);
   return launch_check("kv_export");
 }
@@ -1023,9 +1043,10 @@ int dflash_kv_import(dflash_session* s, int32_t layer, int64_t first_slot, int32
   const dflash_config& c = s->m->cfg;
   const size_t plane = (size_t)c.n_kv_heads * s->cap * c.head_dim * s->m->esz;
   char* base = (char*)s->kv + (size_t)(2 * layer) * plane;
-  launch_kv_copy(s->m->dt, base, s->cap, first_slot, k_in, n_rows, 0, n_rows, c.n_kv_heads, c.head_dim, s->stream);
-  launch_kv_copy(s->m->dt, base + plane, s->cap, first_slot, v_in, n_rows, 0, n_rows, c.n_kv_heads, c.head_dim,
-                 s->stream);
+  launch_kv_copy(s->m->dt, base, s->cap, first_slot, const_cast<void*>(k_in), n_rows, c.n_kv_heads, c.head_dim, true,
+                 false, s->stream);
+  launch_kv_copy(s->m->dt, base + plane, s->cap, first_slot, const_cast<void*>(v_in), n_rows, c.n_kv_heads, c.head_dim,
+                 true, true, s->stream);
   return launch_check("kv_import");
 }
 

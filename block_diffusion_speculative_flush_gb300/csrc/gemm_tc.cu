@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "gemm_tc.h"
+#include "launch.h"
 
 namespace dfl {
 
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
   const int kb1 = (int)((int64_t)(split + 1) * p.kb_total / p.splits);
   const int nkb = kb1 - kb0;
 
+  pdl_trigger();  // the next kernel may be scheduled as this one's CTAs retire
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -241,22 +243,35 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
     uint64_t pol_w, pol_x;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
-    int issued = 0;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % STAGES;
-      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-      if (i >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
-        atomicOr(p.err, 4);
-        *abort_flag = 1;
-        break;
-      }
-      mbar_expect_tx(&full[s], TX);
+    auto load_w = [&](int i, int s) {
       if (SWI) {
         tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, m_tile * (BM / 2), pol_w);
         tma_load_2d(sA + s * A_BYTES + A_BYTES / 2, &tmW2, &full[s], (kb0 + i) * BK, m_tile * (BM / 2), pol_w);
       } else {
         tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM, pol_w);
       }
+    };
+    // Weights do not depend on the previous kernel: the first stages of them
+    // are requested before waiting for it, so the weight stream starts while
+    // the previous kernel drains.
+    const int pre = nkb < STAGES ? nkb : STAGES;
+    for (int i = 0; i < pre; ++i) {
+      mbar_expect_tx(&full[i], TX);
+      load_w(i, i);
+    }
+    pdl_wait();
+    for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * B_BYTES, &tmX, &full[i], (kb0 + i) * BK, n_tile * BN, pol_x);
+    int issued = pre;
+    for (int i = pre; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
+        atomicOr(p.err, 4);
+        *abort_flag = 1;
+        break;
+      }
+      mbar_expect_tx(&full[s], TX);
+      load_w(i, s);
       tma_load_2d(sB + s * B_BYTES, &tmX, &full[s], (kb0 + i) * BK, n_tile * BN, pol_x);
       ++issued;
     }
@@ -291,6 +306,7 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
     umma_commit(done);  // arrives once every MMA issued above has completed
   }
   __syncwarp();
+  pdl_wait();  // the epilogue reads (residual) and writes memory the previous kernels use
 
   // ---- epilogue: TMEM -> registers -> global ----
   const uint64_t t0 = globaltimer_ns();
@@ -459,6 +475,32 @@ static int encode_2d(TcContext* c, CUtensorMap* map, const void* base, uint64_t 
   return 0;
 }
 
+int tc_encode_kv_maps(TcContext* c, const void* kv, int64_t cap, int d, int planes, CUtensorMap* out) {
+  // K planes: [planes][cap][d], box {64 channels, 64 positions, 1 plane}
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)cap, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)cap * d * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (c->encode(&out[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return tc_fail("K plane tensor map");
+  }
+  // V^T planes: [planes][d][cap], box {64 positions, d channels, 1 plane}
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)cap, (cuuint64_t)d, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)cap * 2, (cuuint64_t)cap * d * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)d, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (c->encode(&out[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return tc_fail("V plane tensor map");
+  }
+  return 0;
+}
+
 template <int BN, bool SWI>
 static int launch_bn(TcContext* c, const CUtensorMap& mw, const CUtensorMap& mw2, const CUtensorMap& mx,
                      const TcParams& p, int grid, cudaStream_t st, int slot) {
@@ -468,8 +510,7 @@ static int launch_bn(TcContext* c, const CUtensorMap& mw, const CUtensorMap& mw2
     if (e != cudaSuccess) return tc_fail("smem attribute", e);
     c->attr_set[slot] = true;
   }
-  k_gemm_tc<BN, SWI><<<grid, 128, smem, st>>>(mw, mw2, mx, p);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_k(k_gemm_tc<BN, SWI>, grid, 128, smem, st, mw, mw2, mx, p);
   if (e != cudaSuccess) return tc_fail("k_gemm_tc launch", e);
   return 0;
 }

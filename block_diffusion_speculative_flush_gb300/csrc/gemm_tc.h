@@ -2,6 +2,7 @@
 // TMEM accumulators, operands staged by TMA).  Internal interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,5 +28,10 @@ enum TcMode {
 // a row's result does not change with the number of rows in the call.
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y, int64_t ldy,
             int M, int N, int K, int mode, cudaStream_t st);
+
+// TMA maps of a session's K/V cache for the attention kernel: out[0] views
+// the K planes ([planes][cap][d], 64 x 64 boxes), out[1] the V^T planes
+// ([planes][d][cap], 64-position x d boxes).  cap must be a multiple of 64.
+int tc_encode_kv_maps(TcContext* c, const void* kv, int64_t cap, int d, int planes, CUtensorMap* out);
 
 }  // namespace dfl

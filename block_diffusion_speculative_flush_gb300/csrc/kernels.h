@@ -1,6 +1,7 @@
 // Internal launch interface of the DFlash kernels (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,11 +20,17 @@ struct RowMeta {
 };
 
 // Per-session device tables of one batched call.
+// Cache layout of one session, per layer l and KV head h: the K plane
+// (2l)*Hkv + h holds [cap slots][d] (row per position) and the V plane
+// (2l+1)*Hkv + h holds [d][cap slots] (V transposed, row per channel), so
+// that a 64-position tile of either is a K-major operand tile for the
+// tensor cores.
 struct SessTables {
-  void* const* kv;         // [B] session cache base: [L][2][Hkv][cap][d] in the storage type
+  void* const* kv;         // [B] session cache base: 2 * L * Hkv planes of cap * d elements
   const int64_t* cap;      // [B] cache slots (ring size when the draft has a window)
   const int64_t* frontier; // [B] F: position of the block's anchor row
   const int32_t* seq;      // [B] seq id used by the random streams
+  const CUtensorMap* const* kvmaps;  // [B] -> {K planes, V^T planes} TMA maps (bf16, d = 128), or NULL
 };
 
 // One attention work item: keys [k0, k1) (positions) of one session / KV head.
@@ -57,10 +64,11 @@ void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, 
                      SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st);
 void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_items, SessTables tabs,
                            AttnParams p, float* part, cudaStream_t st);
-// bf16 block attention on mma.sync tensor cores; false if the shape is not
-// supported (head_dim other than 64/128, more than 128 query rows per KV head).
-bool launch_attention_mma(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p,
-                          float* part, cudaStream_t st);
+// bf16 block attention on tcgen05 tensor cores (key ranges must start on a
+// multiple of 64); false if the shape is not supported (head_dim other than
+// 128, more than 128 query rows per KV head, no tensor maps).
+bool launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
+                         int* err, cudaStream_t st);
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count,
                               int B, AttnParams p, const float* G, void* O, cudaStream_t st);
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld_delta, int rows, int H, cudaStream_t st);
@@ -68,8 +76,10 @@ void launch_swiglu(DT dt, const float* gu, int64_t ld, int rows, int I, int up_o
                    cudaStream_t st);
 void launch_gemm_simt(DT dt, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy,
                       int M, int N, int K, cudaStream_t st);
-void launch_kv_copy(DT dt, void* dst, int64_t dst_cap, int64_t dst_first, const void* src, int64_t src_cap,
-                    int64_t src_first, int n_rows, int Hkv, int d, cudaStream_t st);
+// Rows between a cache plane set and a flat [Hkv][n][d] buffer.  to_cache:
+// flat -> cache.  transposed: the cache planes are V^T ([d][cap]).
+void launch_kv_copy(DT dt, void* cache, int64_t cap, int64_t first, void* flat, int n_rows, int Hkv, int d,
+                    bool to_cache, bool transposed, cudaStream_t st);
 
 // Sampling: per (row, chunk) partials over a row of logits, then a merge.
 struct SampleArgs {
@@ -122,7 +132,9 @@ struct VerifyPart {
 };
 // T > 0: one grid of (session, vocabulary chunk) CTAs for the bonus draw,
 // then the per-session finish; T == 0: the finish alone.  part holds
-// B * ceil(V / 4096) entries.
+// B * verify_bonus_chunks(V) entries.
+constexpr int kVerifyBonusChunk = 2048;
+inline int verify_bonus_chunks(int V) { return (V + kVerifyBonusChunk - 1) / kVerifyBonusChunk; }
 void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st);
 
 // --- tensor-core path (bf16, sm_103a) --------------------------------------

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 
 namespace dfl {
 
@@ -28,6 +29,8 @@ namespace {
 template <typename T>
 __global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict__ aux, T* __restrict__ u,
                            int K, int Ht, float eps) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int r = blockIdx.x, k = blockIdx.y;
   const T* f = src[r] + (size_t)k * Ht;
@@ -49,6 +52,8 @@ template <typename TIn, typename T>
 __global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, int rows0, const TIn* __restrict__ in1,
                                                  int64_t ld_in, const T* __restrict__ g, T* __restrict__ out,
                                                  int64_t ld_out, int H, int a, int b, int c, float eps) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int j = blockIdx.x;
   const int src = (j / a) * b + (j % a) + c;
@@ -77,10 +82,13 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, in
   for (int t = threadIdx.x + MAXV * blockDim.x; t < H; t += blockDim.x) o[t] = from_f<T>(to_f(x[t]) * inv * to_f(g[t]));
 }
 
+// Block rows [anchor, mask x n]: rows of E copied 16 bytes at a time.
 template <typename T>
 __global__ void k_embed(const T* __restrict__ E, const int32_t* __restrict__ current,
                         const int32_t* __restrict__ sess_map, int mask_token, int V, int nrows, int H,
                         T* __restrict__ h, int32_t* __restrict__ err) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int b = r / nrows, i = r % nrows;
   int tok = i == 0 ? current[sess_map ? sess_map[b] : b] : mask_token;
@@ -88,14 +96,17 @@ __global__ void k_embed(const T* __restrict__ E, const int32_t* __restrict__ cur
     if (threadIdx.x == 0) atomicOr(err, 1);
     tok = 0;
   }
-  const T* e = E + (int64_t)tok * H;
-  T* o = h + (int64_t)r * H;
-  for (int t = threadIdx.x; t < H; t += blockDim.x) o[t] = e[t];
+  const uint4* e = reinterpret_cast<const uint4*>(E + (int64_t)tok * H);
+  uint4* o = reinterpret_cast<uint4*>(h + (int64_t)r * H);
+  const int nv = (int)(H * sizeof(T) / 16);
+  for (int t = threadIdx.x; t < nv; t += blockDim.x) o[t] = e[t];
 }
 
 // cos / sin of pos * theta^(-2j/d), the angle formed and reduced in double so
 // that large positions keep full fp32 accuracy.
 __global__ void k_rope_table(const RowMeta* __restrict__ meta, int d, float theta, float2* __restrict__ table) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x, j = threadIdx.x;
   if (j >= d / 2) return;
   const double inv = pow((double)theta, -2.0 * (double)j / (double)d);
@@ -112,6 +123,8 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
                            const float2* __restrict__ rope, const T* __restrict__ q_norm,
                            const T* __restrict__ k_norm, int Hq, int Hkv, int gated, float eps, SessTables tabs,
                            int layer, T* __restrict__ Q, float* __restrict__ G) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int d = DU * 32;
   const int m = blockIdx.x;
   const int lane = threadIdx.x & 31;
@@ -159,12 +172,12 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
   const int64_t slot = rm.pos % cap;
   T* base = (T*)tabs.kv[rm.sess];
   T* kd = base + (((int64_t)(2 * layer) * Hkv + kh) * cap + slot) * d;
-  T* vd = base + (((int64_t)(2 * layer + 1) * Hkv + kh) * cap + slot) * d;
+  T* vd = base + ((int64_t)(2 * layer + 1) * Hkv + kh) * cap * d + slot;  // V^T plane: [d][cap]
   const float* xv = row + (int64_t)(Hq + Hkv + kh) * d;
 #pragma unroll
   for (int u = 0; u < DU; ++u) {
     kd[lane + 32 * u] = from_f<T>(y[u]);
-    vd[lane + 32 * u] = from_f<T>(xv[lane + 32 * u]);
+    vd[(int64_t)(lane + 32 * u) * cap] = from_f<T>(xv[lane + 32 * u]);
   }
 }
 
@@ -181,6 +194,8 @@ __device__ __forceinline__ bool key_visible(int64_t F, int i, int64_t r, int win
 template <typename T>
 __global__ void k_attn_simt(const T* __restrict__ Q, const AttnItem* __restrict__ items, SessTables tabs,
                             AttnParams p, float* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm[];
   const int d = p.d, G = p.Hq / p.Hkv, R = p.nrows * G;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -213,7 +228,7 @@ __global__ void k_attn_simt(const T* __restrict__ Q, const AttnItem* __restrict_
       if (r < it.k1) {
         const int64_t slot = r % cap;
         kv = to_f(Kb[slot * d + t]);
-        vv = to_f(Vb[slot * d + t]);
+        vv = to_f(Vb[(int64_t)t * cap + slot]);
       }
       ks[j * (d + 1) + t] = kv;
       vs[j * d + t] = vv;
@@ -265,6 +280,8 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
                                                       const int32_t* __restrict__ item_first,
                                                       const int32_t* __restrict__ item_count, AttnParams p, int total,
                                                       const float* __restrict__ Gt, T* __restrict__ O) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float wsm[4][64];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int gw = blockIdx.x * 4 + wl;  // (b, i, hq) flattened
@@ -293,14 +310,29 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
   T* out = O + ((int64_t)bi * p.Hq + hq) * d;
   for (int t4 = lane * 4; t4 < d; t4 += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-      const float m = s < 64 ? 0.f : base[s * sstride];
-      const float w = s < 64 ? wsm[wl][s] : (m == -INFINITY ? 0.f : expf(m - M));
-      const float4 v = *reinterpret_cast<const float4*>(base + s * sstride + 4 + t4);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+    // eight splits' loads in flight at a time; the sum keeps split order
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = s0 + k < S ? __ldg(reinterpret_cast<const float4*>(base + (s0 + k) * sstride + 4 + t4))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int s = s0 + k;
+        if (s >= S) break;
+        float w;
+        if (s < 64) {
+          w = wsm[wl][s];
+        } else {
+          const float m = base[s * sstride];
+          w = m == -INFINITY ? 0.f : expf(m - M);
+        }
+        acc.x += w * v[k].x;
+        acc.y += w * v[k].y;
+        acc.z += w * v[k].z;
+        acc.w += w * v[k].w;
+      }
     }
     out[t4] = from_f<T>(acc.x * scale);
     out[t4 + 1] = from_f<T>(acc.y * scale);
@@ -311,6 +343,8 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
 
 template <typename T>
 __global__ void k_residual(T* __restrict__ h, const float* __restrict__ delta, int64_t ld, int H) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   for (int t = threadIdx.x; t < H; t += blockDim.x) {
     T* p = h + (int64_t)r * H + t;
@@ -320,6 +354,8 @@ __global__ void k_residual(T* __restrict__ h, const float* __restrict__ delta, i
 
 template <typename T>
 __global__ void k_swiglu(const float* __restrict__ gu, int64_t ld, int I, int up_off, T* __restrict__ a) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   for (int t = threadIdx.x; t < I; t += blockDim.x) {
     const float g = gu[(int64_t)r * ld + t], u = gu[(int64_t)r * ld + up_off + t];
@@ -333,6 +369,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_gemm_simt(const T* __restrict__ X, int64_t ldx, const T* __restrict__ W,
                                                    int64_t ldw, float* __restrict__ Y, int64_t ldy, int M, int N,
                                                    int K) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -371,12 +409,21 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const T* __restrict__ X, int6
 }
 
 template <typename T>
-__global__ void k_kv_copy(T* __restrict__ dst, int64_t dcap, int64_t dfirst, const T* __restrict__ src,
-                          int64_t scap, int64_t sfirst, int n, int d) {
+__global__ void k_kv_copy(T* __restrict__ cache, int64_t cap, int64_t first, T* __restrict__ flat, int n, int d,
+                          int to_cache, int transposed) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.y, r = blockIdx.x;
-  const T* s = src + ((int64_t)h * scap + (sfirst + r) % scap) * d;
-  T* o = dst + ((int64_t)h * dcap + (dfirst + r) % dcap) * d;
-  for (int t = threadIdx.x; t < d; t += blockDim.x) o[t] = s[t];
+  const int64_t slot = (first + r) % cap;
+  T* plane = cache + (int64_t)h * cap * d;
+  T* f = flat + ((int64_t)h * n + r) * d;
+  for (int t = threadIdx.x; t < d; t += blockDim.x) {
+    T* c = transposed ? plane + (int64_t)t * cap + slot : plane + slot * d + t;
+    if (to_cache)
+      *c = f[t];
+    else
+      f[t] = *c;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -389,6 +436,8 @@ __device__ __forceinline__ float load_logit(const void* p, int in_bf16, int64_t 
 // part[row][chunk] = (max of l/T, sum exp(l/T - max), best score, best index)
 // where the score is l/T + Gumbel (draft draw) or l/T (argmax / row stats).
 __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sm_m[32], sm_l[32], sm_s[32];
   __shared__ int32_t sm_i[32];
   const int row = blockIdx.x, c = blockIdx.y, nch = gridDim.y;
@@ -443,6 +492,8 @@ __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ 
 
 __global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restrict__ part, int32_t* __restrict__ tok,
                                  float* __restrict__ qtok, float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= a.rows) return;
   float M = -INFINITY;
@@ -501,6 +552,8 @@ __device__ int verify_scan(const VerifyArgs& a, int b) {
 // sum max(0, p - q), the best log(max(0, p - q)) + Gumbel and the best
 // log p + Gumbel.
 __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int s_rej;
   __shared__ float sm_sum[32], sm_rs[32], sm_ps[32];
   __shared__ int32_t sm_ri[32], sm_pi[32];
@@ -569,6 +622,8 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
 // argmax equals the draft token; bonus = argmax of row a.  T > 0: merge the
 // bonus partials in chunk order.
 __global__ void k_verify_finish(VerifyArgs a, int chunks, const VerifyPart* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.B) return;
   const int n = a.n;
@@ -616,7 +671,7 @@ inline unsigned cdiv(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b);
 void launch_tap_norm(DT dt, const void* const* src, int rows, const void* aux, void* u, int K, int Ht, float eps,
                      cudaStream_t st) {
   if (rows <= 0) return;
-  DFL_DISPATCH(dt, k_tap_norm<T><<<dim3(rows, K), 256, 0, st>>>((const T* const*)src, (const T*)aux, (T*)u, K,
+  DFL_DISPATCH(dt, launch_k(k_tap_norm<T>, dim3(rows, K), 256, 0, st, (const T* const*)src, (const T*)aux, (T*)u, K,
                                                                    Ht, eps));
 }
 
@@ -624,10 +679,10 @@ void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* 
                     void* out, int64_t ld_out, int rows, int H, int a, int b, int c, float eps, cudaStream_t st) {
   if (rows <= 0) return;
   if (in_f32) {
-    DFL_DISPATCH(dt, k_rmsnorm<float, T><<<rows, 512, 0, st>>>((const float*)in0, rows0, (const float*)in1, ld_in,
+    DFL_DISPATCH(dt, launch_k(k_rmsnorm<float, T>, rows, 512, 0, st, (const float*)in0, rows0, (const float*)in1, ld_in,
                                                                 (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
   } else {
-    DFL_DISPATCH(dt, k_rmsnorm<T, T><<<rows, 512, 0, st>>>((const T*)in0, rows0, (const T*)in1, ld_in,
+    DFL_DISPATCH(dt, launch_k(k_rmsnorm<T, T>, rows, 512, 0, st, (const T*)in0, rows0, (const T*)in1, ld_in,
                                                             (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
   }
 }
@@ -635,13 +690,13 @@ void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* 
 void launch_embed(DT dt, const void* E, const int32_t* current, const int32_t* sess_map, int mask_token, int V,
                   int B, int nrows, int H, void* h, int32_t* err, cudaStream_t st) {
   if (B <= 0) return;
-  DFL_DISPATCH(dt, k_embed<T><<<B * nrows, 128, 0, st>>>((const T*)E, current, sess_map, mask_token, V, nrows, H,
+  DFL_DISPATCH(dt, launch_k(k_embed<T>, B * nrows, 128, 0, st, (const T*)E, current, sess_map, mask_token, V, nrows, H,
                                                           (T*)h, err));
 }
 
 void launch_rope_table(const RowMeta* meta, int M, int d, float theta, float2* table, cudaStream_t st) {
   if (M <= 0) return;
-  k_rope_table<<<M, d / 2, 0, st>>>(meta, d, theta, table);
+  launch_k(k_rope_table, M, d / 2, 0, st, meta, d, theta, table);
 }
 
 void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
@@ -652,11 +707,11 @@ void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, 
   const int heads = Hq + Hkv;
   dim3 grid(M, cdiv(heads, 4));
   if (d == 64) {
-    DFL_DISPATCH(dt, k_qkv_post<T, 2><<<grid, 128, 0, st>>>(qkv, ldq, meta, rope, (const T*)q_norm,
+    DFL_DISPATCH(dt, launch_k(k_qkv_post<T, 2>, grid, 128, 0, st, qkv, ldq, meta, rope, (const T*)q_norm,
                                                               (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
                                                               (T*)Q, G));
   } else {
-    DFL_DISPATCH(dt, k_qkv_post<T, 4><<<grid, 128, 0, st>>>(qkv, ldq, meta, rope, (const T*)q_norm,
+    DFL_DISPATCH(dt, launch_k(k_qkv_post<T, 4>, grid, 128, 0, st, qkv, ldq, meta, rope, (const T*)q_norm,
                                                               (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
                                                               (T*)Q, G));
   }
@@ -669,57 +724,57 @@ void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_it
   const size_t smem = sizeof(float) * ((size_t)R * p.d * 2 + 32 * (p.d + 1) + 32 * p.d + 2 * R);
   DFL_DISPATCH(dt, {
     cudaFuncSetAttribute(k_attn_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_attn_simt<T><<<n_items, 256, smem, st>>>((const T*)Q, items, tabs, p, part);
+    launch_k(k_attn_simt<T>, n_items, 256, smem, st, (const T*)Q, items, tabs, p, part);
   });
 }
 
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count, int B,
                               AttnParams p, const float* G, void* O, cudaStream_t st) {
   const int total = B * p.nrows * p.Hq;
-  DFL_DISPATCH(dt, k_attn_combine<T><<<cdiv(total, 4), 128, 0, st>>>(part, item_first, item_count, p, total, G,
+  DFL_DISPATCH(dt, launch_k(k_attn_combine<T>, cdiv(total, 4), 128, 0, st, part, item_first, item_count, p, total, G,
                                                                       (T*)O));
 }
 
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld, int rows, int H, cudaStream_t st) {
   if (rows <= 0) return;
-  DFL_DISPATCH(dt, k_residual<T><<<rows, 256, 0, st>>>((T*)h, delta, ld, H));
+  DFL_DISPATCH(dt, launch_k(k_residual<T>, rows, 256, 0, st, (T*)h, delta, ld, H));
 }
 
 void launch_swiglu(DT dt, const float* gu, int64_t ld, int rows, int I, int up_off, void* a, cudaStream_t st) {
   if (rows <= 0) return;
-  DFL_DISPATCH(dt, k_swiglu<T><<<rows, 256, 0, st>>>(gu, ld, I, up_off, (T*)a));
+  DFL_DISPATCH(dt, launch_k(k_swiglu<T>, rows, 256, 0, st, gu, ld, I, up_off, (T*)a));
 }
 
 void launch_gemm_simt(DT dt, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy, int M,
                       int N, int K, cudaStream_t st) {
   if (M <= 0 || N <= 0) return;
   dim3 grid(cdiv(N, 64), cdiv(M, 64));
-  DFL_DISPATCH(dt, k_gemm_simt<T><<<grid, 256, 0, st>>>((const T*)X, ldx, (const T*)W, ldw, Y, ldy, M, N, K));
+  DFL_DISPATCH(dt, launch_k(k_gemm_simt<T>, grid, 256, 0, st, (const T*)X, ldx, (const T*)W, ldw, Y, ldy, M, N, K));
 }
 
-void launch_kv_copy(DT dt, void* dst, int64_t dcap, int64_t dfirst, const void* src, int64_t scap, int64_t sfirst,
-                    int n, int Hkv, int d, cudaStream_t st) {
+void launch_kv_copy(DT dt, void* cache, int64_t cap, int64_t first, void* flat, int n, int Hkv, int d, bool to_cache,
+                    bool transposed, cudaStream_t st) {
   if (n <= 0) return;
-  DFL_DISPATCH(dt, k_kv_copy<T><<<dim3(n, Hkv), 128, 0, st>>>((T*)dst, dcap, dfirst, (const T*)src, scap, sfirst,
-                                                               n, d));
+  DFL_DISPATCH(dt, launch_k(k_kv_copy<T>, dim3(n, Hkv), 128, 0, st, (T*)cache, cap, first, (T*)flat, n, d,
+                            (int)to_cache, (int)transposed));
 }
 
 void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st) {
   if (a.rows <= 0) return;
-  k_sample_partials<<<dim3(a.rows, cdiv(a.V, chunk)), 256, 0, st>>>(a, chunk, part);
+  launch_k(k_sample_partials, dim3(a.rows, cdiv(a.V, chunk)), 256, 0, st, a, chunk, part);
 }
 
 void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, int32_t* tok, float* qtok, float* lse,
                            cudaStream_t st) {
   if (a.rows <= 0) return;
-  k_sample_combine<<<cdiv(a.rows, 128), 128, 0, st>>>(a, chunks, part, tok, qtok, lse);
+  launch_k(k_sample_combine, cdiv(a.rows, 128), 128, 0, st, a, chunks, part, tok, qtok, lse);
 }
 
 void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st) {
   if (a.B <= 0) return;
-  const int chunk = 4096, chunks = (int)cdiv(a.V, chunk);
-  if (a.temperature > 0.f) k_verify_bonus<<<dim3(a.B, chunks), 256, 0, st>>>(a, chunk, part);
-  k_verify_finish<<<cdiv(a.B, 64), 64, 0, st>>>(a, chunks, part);
+  const int chunk = kVerifyBonusChunk, chunks = verify_bonus_chunks(a.V);
+  if (a.temperature > 0.f) launch_k(k_verify_bonus, dim3(a.B, chunks), 256, 0, st, a, chunk, part);
+  launch_k(k_verify_finish, cdiv(a.B, 64), 64, 0, st, a, chunks, part);
 }
 
 }  // namespace dfl

@@ -145,7 +145,7 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   const size_t o_lse = off;
   off = up16(off + (size_t)rows * sizeof(float));
   const size_t o_bonus = off;
-  off = up16(off + (size_t)batch * chunks * sizeof(VerifyPart));
+  off = up16(off + (size_t)batch * verify_bonus_chunks(V) * sizeof(VerifyPart));
   const size_t o_rej = off;
   off = up16(off + (size_t)batch * sizeof(int32_t));
   if (off > kScratchBytes) {
