@@ -283,9 +283,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       m_used = m_new;
       uint32_t hi2[16], lo2[16];
       float ls = 0.f;
+      // while a row has seen no visible key its max is -inf and every score
+      // is -inf too: exponentiate against 0 so that P = exp2(-inf) = 0
+      const float mref = m_used == -INFINITY ? 0.f : m_used;
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float p0 = exp2f(s[j] - m_used), p1 = exp2f(s[j + 1] - m_used);  // exp2(-inf) = 0
+        const float p0 = exp2f(s[j] - mref), p1 = exp2f(s[j + 1] - mref);
         ls += p0 + p1;
         split_pack(p0, p1, hi2[j / 2], lo2[j / 2]);
       }

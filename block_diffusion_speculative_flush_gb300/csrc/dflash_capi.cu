@@ -513,6 +513,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   sa.rows_per_seq = n;
   sa.row_offset = 1;
   sa.seq_ids = tabs.seq;
+  sa.err = m->d_err;
   int32_t* tok = m->vstat.as<int32_t>();
   float* lse = (float*)(tok + Rz);
   {
@@ -709,6 +710,7 @@ int dflash_device_status(dflash_model* m) {
     if (e & 2) why += "draft token id outside the vocabulary; ";
     if (e & 4) why += "tensor-core GEMM pipeline wait expired; ";
     if (e & 8) why += "tensor-core attention pipeline wait expired; ";
+    if (e & 16) why += "a logits row had no comparable score (non-finite values); ";
     return fail(DFLASH_ERR_DEVICE, "device reported: %s", why.c_str());
   }
   return DFLASH_OK;
@@ -945,6 +947,7 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   sa.gumbel = 0;
   sa.rows_per_seq = n + 1;
   sa.row_offset = 0;
+  sa.err = m->d_err;
   const double tbytes = (double)rows * V * (sa.in_bf16 ? 2 : 4) + (double)batch * V * 4;
   Timed tm(m, kVerify, tbytes, 4.0 * rows * V, st);
   launch_sample_partials(sa, chunk, m->vpart.as<float4>(), st);

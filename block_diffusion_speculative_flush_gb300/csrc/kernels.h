@@ -95,6 +95,7 @@ struct SampleArgs {
   int row_offset;          // Philox row of a session's first row
   const int32_t* seq_ids;  // [B] seq id per session
   const int32_t* out_map;  // [B] output row block of each session (NULL: identity)
+  int32_t* err;            // bit 16: a row had no comparable score (non-finite logits)
 };
 void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st);
 // Writes tok[row], q[row] (probability of the token at T), lse[row] (log-sum-exp of logits/T).

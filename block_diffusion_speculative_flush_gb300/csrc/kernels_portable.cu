@@ -505,6 +505,12 @@ __global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restr
     if (pc.x != -INFINITY) L += pc.y * expf(pc.x - M);
     bb = better(bb, ArgMax{pc.z, __float_as_int(pc.w)});
   }
+  // a row whose scores were all NaN has no argmax: record it and answer 0
+  // rather than reading a logit at an undefined index
+  if (bb.i < 0 || bb.i >= a.V) {
+    if (a.err) atomicOr(a.err, 16);
+    bb.i = 0;
+  }
   const float ls = M + logf(L);
   int orow = row;
   if (a.out_map) orow = a.out_map[row / a.rows_per_seq] * a.rows_per_seq + row % a.rows_per_seq;
@@ -631,7 +637,7 @@ __global__ void k_verify_finish(VerifyArgs a, int chunks, const VerifyPart* __re
   if (a.temperature <= 0.f) {
     accn = 0;
     while (accn < n && a.amax_t[b * (n + 1) + accn] == a.draft[b * n + accn]) ++accn;
-    bonus = a.amax_t[b * (n + 1) + accn];
+    bonus = a.amax_t[b * (n + 1) + accn];      // in range: the row statistics clamp it
   } else {
     const int rej = a.rej[b];
     float S = 0.f;
@@ -644,6 +650,10 @@ __global__ void k_verify_finish(VerifyArgs a, int chunks, const VerifyPart* __re
     }
     accn = rej ? rej - 1 : n;
     bonus = (rej && S > 0.f) ? R.i : P.i;
+    if (bonus < 0 || bonus >= a.V) {  // no comparable score (non-finite logits)
+      atomicOr(a.err, 16);
+      bonus = 0;
+    }
   }
   a.accept[b] = accn;
   a.bonus[b] = bonus;

@@ -186,6 +186,7 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   sa.gumbel = 0;
   sa.rows_per_seq = n + 1;
   sa.row_offset = 0;
+  sa.err = err;
   float4* part = (float4*)(base + o_part);
   int32_t* amax = (int32_t*)(base + o_amax);
   float* lse = (float*)(base + o_lse);
