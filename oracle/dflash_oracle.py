@@ -27,7 +27,7 @@ call):
     probabilities (dflash.go propose comment; DFlash2 commit note), as in
     Leviathan, Kalman & Matias (2023) and Chen et al. (2023).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   R1 norm gains are inputs (random 1 + N(0, 0.02) in tests);
   R3 eps = 1e-6;  R4 one RMSNorm per tap over that tap's slice;
   R5 per-head RMSNorm on q and k;  R6 rotate-half RoPE on pairs (j, j+d/2);

@@ -17,8 +17,8 @@ from tests.gpu_util import (TOL_Q, assert_cache_close, assert_logits_full, check
 
 pytestmark = pytest.mark.gpu
 
-C1 = S.CONFIGS["qwen3_8b_bf16"]
-C3 = S.CONFIGS["laguna_bf16"]
+QWEN = S.CONFIGS["qwen3_8b_bf16"]
+LAGUNA = S.CONFIGS["laguna_bf16"]
 
 
 class Full:
@@ -36,13 +36,13 @@ class Full:
 
 
 @pytest.fixture(scope="module")
-def c1():
-    return Full(C1)
+def qwen():
+    return Full(QWEN)
 
 
 @pytest.fixture(scope="module")
-def c3():
-    return Full(C3)
+def laguna():
+    return Full(LAGUNA)
 
 
 def _seeded_context(D, cfg, sess, first, n, seed, name):
@@ -89,13 +89,13 @@ def _round(D, full, cfg, model, odraft, ctx_first, ctx_n, F0, T, seed, tag):
     return s, o, g_lg, err
 
 
-def test_c1_round_at_ctx_4096(c1):
+def test_qwen3_8b_round_at_ctx_4096(qwen):
     """Qwen3-8B-shaped draft, bs1: 4092 restored context rows + 4 committed
     rows, block 16 at T = 1.0, then the verify of the oracle's tokens."""
     D = lib()
-    cfg = c1.cfg
+    cfg = qwen.cfg
     n = cfg.block_size - 1
-    s, o, g_lg, err = _round(D, c1, cfg, c1.model, c1.oracle, 0, 4092, 4092, 1.0, 21, "c1")
+    s, o, g_lg, err = _round(D, qwen, cfg, qwen.model, qwen.oracle, 0, 4092, 4092, 1.0, 21, "qwen")
     d = o.last["tokens"][None].astype(np.int32)
     tl = S.make_target_logits(1, n + 1, cfg.vocab, d, seed=5, std=3.0)
     acc = torch.empty(1, dtype=torch.int32, device="cuda")
@@ -108,16 +108,16 @@ def test_c1_round_at_ctx_4096(c1):
             assert (int(acc[0]), int(bon[0])) == (a_ref, b_ref)
         else:
             assert 0 <= int(acc[0]) <= n
-    D.dflash_device_status(c1.model)
+    D.dflash_device_status(qwen.model)
     D.dflash_close(s)
 
 
-def test_c2_flush_8_x_256_rows(c1):
+def test_flush_8_x_256_rows(qwen):
     """8 sequences at context offsets 0, 1k, ..., 7k each commit 256 rows,
     which flush in one context-only forward after a block rewind; the cursors
     stay consistent and sampled cache rows equal the oracle's."""
     D = lib()
-    cfg = c1.cfg
+    cfg = qwen.cfg
     n = cfg.block_size - 1
     feats = S.make_features(cfg, 256, seed=33)
     fd = torch.from_numpy(feats).cuda().to(torch.bfloat16)
@@ -126,7 +126,7 @@ def test_c2_flush_8_x_256_rows(c1):
     q = torch.empty((1, n), dtype=torch.float32, device="cuda")
     sess = []
     for j in range(8):
-        s = D.dflash_open(c1.model, restored_offset=1024 * j, max_ctx=1024 * j + 512)
+        s = D.dflash_open(qwen.model, restored_offset=1024 * j, max_ctx=1024 * j + 512)
         if j:
             assert D.dflash_propose([s], cur, n, 0.0, 0, 0, tok, q) == [n]
             assert D.dflash_session_state(s) == (1024 * j, 0, True)
@@ -134,8 +134,8 @@ def test_c2_flush_8_x_256_rows(c1):
         assert D.dflash_session_state(s) == (1024 * j + 256, 0, False)
         sess.append(s)
     picks = [0, 1, 128, 255]
-    Ks, Vs = c1.oracle.context_kv(feats[picks], [1024 * 7 + p for p in picks])
-    Ks0, _ = c1.oracle.context_kv(feats[picks], picks)
+    Ks, Vs = qwen.oracle.context_kv(feats[picks], [1024 * 7 + p for p in picks])
+    Ks0, _ = qwen.oracle.context_kv(feats[picks], picks)
     for l in range(cfg.n_layers):
         k7, v7 = export_kv(D, sess[7], cfg, l, 1024 * 7, 256)
         k0, _ = export_kv(D, sess[0], cfg, l, 0, 256)
@@ -144,8 +144,8 @@ def test_c2_flush_8_x_256_rows(c1):
             assert_cache_close(v7[:, p], Vs[l][i])
             assert_cache_close(k0[:, p], Ks0[l][i])
     # pieces against one flush, bit for bit, at full width
-    a = D.dflash_open(c1.model, max_ctx=512)
-    b = D.dflash_open(c1.model, max_ctx=512)
+    a = D.dflash_open(qwen.model, max_ctx=512)
+    b = D.dflash_open(qwen.model, max_ctx=512)
     D.dflash_committed(a, fd, 0)
     D.dflash_committed(b, fd[:100], 0)
     D.dflash_committed(b, fd[100:], 100)
@@ -159,32 +159,32 @@ def test_c2_flush_8_x_256_rows(c1):
 
 
 @pytest.mark.parametrize("block", [16, 8])
-def test_c3_laguna_round_with_window(c3, block):
+def test_laguna_round_with_window(laguna, block):
     """Laguna-style draft (fused QKV + per-head gate, window 512): a frontier
     of 32768 with the 507 newest restored rows + 4 committed rows visible;
     blocks of 16 and 8 at T = 1.0."""
     D = lib()
-    cfg, model, odraft = c3.model_with(block_size=block)
+    cfg, model, odraft = laguna.model_with(block_size=block)
     F0 = 32768 - 4
     first = 32768 - 511
-    s, o, g_lg, err = _round(D, c3, cfg, model, odraft, first, F0 - first, F0, 1.0, 44 + block, f"c3.{block}")
+    s, o, g_lg, err = _round(D, laguna, cfg, model, odraft, first, F0 - first, F0, 1.0, 44 + block, f"laguna.{block}")
     D.dflash_device_status(model)
     D.dflash_close(s)
 
 
-def test_c3_window_drop_before_fc(c3):
+def test_laguna_window_drop_before_fc(laguna):
     """Context rows older than the window are never computed: a 1100-row
     flush writes only the 511 newest rows, which equal the oracle's."""
     D = lib()
-    cfg = c3.cfg
+    cfg = laguna.cfg
     feats = S.make_features(cfg, 1100, seed=55)
-    s = D.dflash_open(c3.model, max_ctx=2048)
+    s = D.dflash_open(laguna.model, max_ctx=2048)
     D.dflash_committed(s, torch.from_numpy(feats).cuda().to(torch.bfloat16), 0)
     assert D.dflash_session_state(s) == (1100, 0, False)
     st = D.dflash_stats(s)
     assert st["flushed_rows"] == 1100
     picks = [589, 800, 1099]
-    Ks, Vs = c3.oracle.context_kv(feats[picks], picks)
+    Ks, Vs = laguna.oracle.context_kv(feats[picks], picks)
     for l in range(cfg.n_layers):
         k, v = export_kv(D, s, cfg, l, 589, 511)
         for i, p in enumerate(picks):
@@ -193,13 +193,13 @@ def test_c3_window_drop_before_fc(c3):
     D.dflash_close(s)
 
 
-def test_c4_serving_mix_64_sequences(c1):
+def test_serving_mix_64_sequences(qwen):
     """64 sequences, contexts uniform in 1k..16k, one batched propose at
     T = 0.7: the sessions with the shortest and the longest context against
     the oracle (seq id = batch index), and greedy verify of seeded draft
     tokens for all 64 against the oracle's rule."""
     D = lib()
-    cfg = c1.cfg
+    cfg = qwen.cfg
     n = cfg.block_size - 1
     V = cfg.vocab
     B = 64
@@ -210,10 +210,10 @@ def test_c4_serving_mix_64_sequences(c1):
     sess, oss = [], {}
     for b in range(B):
         c = int(ctxs[b])
-        s = D.dflash_open(c1.model, restored_offset=c, max_ctx=c + 64)
+        s = D.dflash_open(qwen.model, restored_offset=c, max_ctx=c + 64)
         if b in check:
-            cache = _seeded_context(D, cfg, s, 0, c, 60 + b, f"c4.{b}")
-            oss[b] = O.OracleSession(c1.oracle, restored_offset=c, restored_cache=cache, seq=b)
+            cache = _seeded_context(D, cfg, s, 0, c, 60 + b, f"mix.{b}")
+            oss[b] = O.OracleSession(qwen.oracle, restored_offset=c, restored_cache=cache, seq=b)
         else:
             for l in range(cfg.n_layers):
                 kk = torch.randn((cfg.n_kv_heads, c, cfg.head_dim), generator=g, device="cuda").to(torch.bfloat16)
@@ -242,6 +242,6 @@ def test_c4_serving_mix_64_sequences(c1):
         a_ref, b_ref = O.verify(tl[b].astype(np.float64), d[b], None, d[b], 0.0, 0.0, 1, 2, b)
         assert (int(a_gpu[b]), int(b_gpu[b])) == (a_ref, b_ref)
     assert a_gpu.max() > 0        # the boost makes some prefixes accepted
-    D.dflash_device_status(c1.model)
+    D.dflash_device_status(qwen.model)
     for s in sess:
         D.dflash_close(s)
