@@ -3,22 +3,37 @@
 // TMA (cp.async.bulk.tensor) with 128-byte swizzle.
 //
 // Shape of the work.  The draft's products are skinny: a few to a few
-// hundred activation rows (16 block rows per sequence, plus the pending
-// context rows) against weight matrices of 10^7..10^9 elements, so the
-// weight stream from HBM is the cost.  The MMA's 128-row side therefore
-// takes 128 weight rows (output features) and its N side takes the
-// activation rows ("swap AB"): D[feature][row] = W[feature][:] . X[row][:].
-// One CTA owns one 128-feature tile, one token tile of BN rows and one
-// contiguous range of K; when K is split, the CTA that finishes a tile last
-// sums the partials in split order (no spin, no atomics on data), so results
-// are deterministic and a row's value never depends on how many rows share
-// the call.
+// thousand activation rows (16 block rows per sequence, plus the pending
+// context rows) against weight matrices of 10^7..10^9 elements.  The MMA's
+// 128-row side therefore takes 128 weight rows (output features) and its N
+// side takes the activation rows ("swap AB"):
+//     D[feature][row] = W[feature][:] . X[row][:].
 //
-// Roles in a 128-thread CTA: thread 0 issues TMA loads into a STAGES-deep
-// ring, thread 32 issues the MMAs (4 x K=16 per 64-wide stage) and commits
-// each stage back to the producer, then all four warps read TMEM (warp w owns
-// lanes 32w..32w+31) and store.  Every wait is bounded: a wait that runs past
-// its limit sets an error bit and the CTA drains and exits.
+// Summation order.  K is cut into S splits, S a function of N, K and the SM
+// count only.  Each split is accumulated from zero in TMEM, and the splits
+// are added in split order: y = ((0 + P_0) + P_1) + ... + P_{S-1}.  Because
+// S never depends on M, a row's result is bit-identical whatever other rows
+// share the call.  Two schedules produce exactly that sum:
+//
+//  * split clusters (up to a few hundred rows): the S split CTAs of one tile
+//    form a thread-block cluster; each stages its partial tile in its own
+//    shared memory, and after a cluster barrier CTA r sums slice r of the
+//    tile over the S partials through distributed shared memory.  No
+//    partial touches global memory.
+//  * persistent tiles (many rows): one CTA per SM walks tiles and, within a
+//    tile, the S splits in order, with two TMEM accumulators so that the
+//    tensor core fills one while the epilogue warps drain the other into a
+//    running sum kept in a third TMEM region.  Consecutive tiles share a
+//    weight tile, so the CTAs running at one time read each weight tile from
+//    HBM once and find it in L2 after that.
+//
+// Roles in a 192-thread CTA: warp 0 lane 0 issues TMA loads into a
+// STAGES-deep ring, warp 1 lane 0 issues the MMAs (4 x K=16 per 64-wide
+// stage) and owns the TMEM allocation, warps 2..5 drain TMEM (warp w reads
+// lanes 32*(w%4)..+31).  Every wait is bounded: a wait that runs past its
+// limit sets bit 4 of the error word, and the CTA drains its own copies and
+// MMAs, frees its TMEM and exits through the same barriers as a good run.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -30,386 +45,459 @@
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace dfl {
 
 namespace {
 
+namespace cg = cooperative_groups;
+using namespace tc;
 using bf16 = __nv_bfloat16;
 
 thread_local std::string g_tc_err;
 
-constexpr int BM = 128;  // weight rows per tile (MMA M)
-constexpr int BK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int BM = 128;        // weight rows per tile (MMA M)
+constexpr int BK = 64;         // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kMaxSplits = 8;  // the largest portable cluster
+constexpr int kPersistBN = 128;
+constexpr int kErrBit = 4;
 
 struct TcParams {
   void* Y;         // fp32 output, bf16 residual stream, or bf16 SwiGLU product
   int64_t ldy;
   int M, N;        // activation rows; output features
   int mode;        // TcMode
-  int n_tiles, splits, kb_total;
-  float* ws;       // split partials [tile][split][BN][BM]
-  int* counters;   // [tile] arrivals, returned to zero by the last CTA
+  int m_tiles, n_tiles, splits, kb_total;
+  int vec;         // rows of Y start on 16-byte boundaries (ldy % 4 == 0, Y aligned)
   int* err;
 };
 
-constexpr int kMaxSplits = 16;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+template <int BN, bool PERSIST>
+__host__ __device__ constexpr int stages_for() {
+  return PERSIST ? 4 : BN <= 16 ? 6 : BN <= 32 ? 5 : BN <= 64 ? 4 : 3;
 }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+template <int BN, bool PERSIST>
+__host__ __device__ constexpr int tmem_cols() {
+  return PERSIST ? 512 : BN < 32 ? 32 : BN;
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
+// fp32 tile staged for the store: aliases the idle pipeline in the cluster
+// schedule, a region of its own in the persistent one (the pipeline is busy
+// with the next tile while the epilogue stores).
+template <int BN, bool PERSIST>
+__host__ __device__ constexpr size_t staging_bytes() {
+  return PERSIST ? (size_t)BN * BM * 4 : 0;
+}
+template <int BN, bool PERSIST>
+__host__ __device__ constexpr size_t smem_bytes() {
+  return (size_t)stages_for<BN, PERSIST>() * (BM * BK * 2 + BN * BK * 2) + staging_bytes<BN, PERSIST>() + 1024 + 256;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier of the four epilogue warps that also ORs a flag across them, so
+// that all four take the same branch after it.
+__device__ __forceinline__ bool epi_bar_or(bool v) {
+  uint32_t out;
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)v)
       : "memory");
-  return ok != 0;
+  return out != 0;
 }
-// Wait for the phase of `parity` to complete; false if the CTA was told to
-// abort or the wait ran past its limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+
+// Split s of the tile's K range, in 64-wide blocks.
+__device__ __forceinline__ void split_range(const TcParams& p, int s, int& kb0, int& kb1) {
+  kb0 = (int)((int64_t)s * p.kb_total / p.splits);
+  kb1 = (int)((int64_t)(s + 1) * p.kb_total / p.splits);
+}
+
+// Walks this CTA's (tile, split) units in order, calling f(tile, split) for
+// each; f returns false to stop.
+template <bool PERSIST, typename F>
+__device__ __forceinline__ void for_each_unit(const TcParams& p, F f) {
+  const int tiles = p.m_tiles * p.n_tiles;
+  if (PERSIST) {
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x)
+      for (int s = 0; s < p.splits; ++s)
+        if (!f(t, s)) return;
+  } else {
+    f((int)blockIdx.x / p.splits, (int)blockIdx.x % p.splits);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
+  if constexpr (N == 32) tmem_ld32(taddr, v);
+  else tmem_ld16(taddr, v);
+}
+
+// Writes the tile's 4-feature groups [lo, hi) (group e = column c * rows/4
+// + f/4, so consecutive threads write consecutive features) through the
+// output mode.  get4(c, f) returns the fp32 sums of weight rows f..f+3 for
+// token column c.  Loads are issued for U groups before any store depends on
+// them; a group that crosses N, or an output without 16-byte rows, is
+// written element by element.
+template <bool SWI, typename Get4>
+__device__ __forceinline__ void store_tile(const TcParams& p, int m_tile, int tok0, int lo, int hi, int tid, int nthr,
+                                           Get4 get4) {
+  constexpr int U = 2;
+  constexpr int ROWS = SWI ? BM / 2 : BM;
+  constexpr int G = ROWS / 4;
+  for (int e0 = lo + tid; e0 < hi; e0 += U * nthr) {
+    float4 v[U], w[U];
+    int64_t off[U];
+    int nv[U];  // valid features of the group (0..4)
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * nthr;
+      const int c = e / G, f = (e % G) * 4;
+      const int t = tok0 + c, feat = m_tile * ROWS + f;
+      nv[u] = (e < hi && t < p.M) ? max(0, min(4, p.N - feat)) : 0;
+      off[u] = (int64_t)t * p.ldy + feat;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      w[u] = v[u];
+      if (nv[u]) {
+        v[u] = get4(c, f);
+        if (SWI) {
+          w[u] = get4(c, f + BM / 2);
+        } else if (p.mode == kResidBf16) {
+          const bf16* h = reinterpret_cast<const bf16*>(p.Y) + off[u];
+          if (nv[u] == 4 && p.vec) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(h);
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+            w[u] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+          } else {
+            float* wf = reinterpret_cast<float*>(&w[u]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (i < nv[u]) wf[i] = __bfloat162float(h[i]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!nv[u]) continue;
+      float4 o;
+      const bool bf = SWI || p.mode == kResidBf16;
+      if (SWI) {
+        const float* g = reinterpret_cast<const float*>(&v[u]);
+        const float* up = reinterpret_cast<const float*>(&w[u]);
+        float* of = reinterpret_cast<float*>(&o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) of[i] = g[i] / (1.f + expf(-g[i])) * up[i];
+      } else if (p.mode == kResidBf16) {
+        o = make_float4(w[u].x + v[u].x, w[u].y + v[u].y, w[u].z + v[u].z, w[u].w + v[u].w);
+      } else {
+        o = v[u];
+      }
+      if (bf) {
+        bf16* y = reinterpret_cast<bf16*>(p.Y) + off[u];
+        if (nv[u] == 4 && p.vec) {
+          const __nv_bfloat162 a = __floats2bfloat162_rn(o.x, o.y), b = __floats2bfloat162_rn(o.z, o.w);
+          uint2 raw;
+          raw.x = *reinterpret_cast<const uint32_t*>(&a);
+          raw.y = *reinterpret_cast<const uint32_t*>(&b);
+          *reinterpret_cast<uint2*>(y) = raw;
+        } else {
+          const float* of = reinterpret_cast<const float*>(&o);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < nv[u]) y[i] = __float2bfloat16_rn(of[i]);
+        }
+      } else {
+        float* y = reinterpret_cast<float*>(p.Y) + off[u];
+        if (nv[u] == 4 && p.vec) {
+          *reinterpret_cast<float4*>(y) = o;
+        } else {
+          const float* of = reinterpret_cast<const float*>(&o);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < nv[u]) y[i] = of[i];
+        }
+      }
     }
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte
-// swizzle layout: rows of 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address (16-byte units)
-  d |= (uint64_t)1 << 16;                    // leading byte offset (unused when swizzled)
-  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: next 8-row group
-  d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
-template <int BN>
-__host__ __device__ constexpr uint32_t idesc_bf16() {
-  return (1u << 4)                          // D format fp32
-         | (1u << 7)                        // A format bf16
-         | (1u << 10)                       // B format bf16
-         | ((uint32_t)(BN >> 3) << 17)      // N
-         | ((uint32_t)(BM >> 4) << 24);     // M
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v);
-
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-template <>
-__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-template <int BN>
-__host__ __device__ constexpr int stages_for() {
-  return BN <= 16 ? 6 : BN <= 32 ? 5 : BN <= 64 ? 4 : BN <= 128 ? 3 : 4;
-}
-template <int BN>
-__host__ __device__ constexpr int tmem_cols() {
-  return BN < 32 ? 32 : BN;
-}
-template <int BN>
-__host__ __device__ constexpr size_t smem_bytes() {
-  return (size_t)stages_for<BN>() * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
-}
-
 // SWI: the 128-row weight tile is 64 gate rows then the 64 matching up rows
 // (two TMA boxes from two matrices), and the epilogue writes silu(g) * u.
-template <int BN, bool SWI>
-__global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmW,
-                                                    const __grid_constant__ CUtensorMap tmW2,
-                                                    const __grid_constant__ CUtensorMap tmX, TcParams p) {
-  constexpr int STAGES = stages_for<BN>();
+template <int BN, bool SWI, bool PERSIST>
+__global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __grid_constant__ CUtensorMap tmW,
+                                                                       const __grid_constant__ CUtensorMap tmW2,
+                                                                       const __grid_constant__ CUtensorMap tmX,
+                                                                       TcParams p) {
+  constexpr int STAGES = stages_for<BN, PERSIST>();
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr uint32_t TX = A_BYTES + B_BYTES;
   constexpr int CH = BN < 32 ? BN : 32;
-  static_assert((size_t)BN * BM * 4 <= (size_t)STAGES * (A_BYTES + B_BYTES), "epilogue tile must fit the pipeline");
+  constexpr int ROWS = SWI ? BM / 2 : BM;
+  static_assert(PERSIST || (size_t)BN * BM * 4 <= (size_t)STAGES * (A_BYTES + B_BYTES),
+                "the staged tile must fit the idle pipeline");
+  static_assert(!PERSIST || BN == kPersistBN, "persistent tiles are 128 rows wide");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = (uint64_t*)(sB + STAGES * B_BYTES);
+  float* stg = PERSIST ? reinterpret_cast<float*>(sB + STAGES * B_BYTES) : reinterpret_cast<float*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES + staging_bytes<BN, PERSIST>());
   uint64_t* empty = full + STAGES;
-  uint64_t* done = empty + STAGES;
-  uint32_t* tmem_slot = (uint32_t*)(done + 1);
-  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  int* last_flag = (int*)(tmem_slot + 2);
+  uint64_t* accf = empty + STAGES;  // [2] accumulator b holds a finished split
+  uint64_t* acce = accf + 2;        // [2] accumulator b has been drained
+  uint64_t* drain = acce + 2;       // MMAs still in flight when a CTA aborts
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int w = blockIdx.x;
-  const int split = w % p.splits;
-  w /= p.splits;
-  const int n_tile = w % p.n_tiles;
-  const int m_tile = w / p.n_tiles;
-  const int kb0 = (int)((int64_t)split * p.kb_total / p.splits);
-  const int kb1 = (int)((int64_t)(split + 1) * p.kb_total / p.splits);
-  const int nkb = kb1 - kb0;
-
   pdl_trigger();  // the next kernel may be scheduled as this one's CTAs retire
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmW) : "memory");
     if (SWI) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmW2) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmX) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"((uint32_t)tmem_cols<BN>())
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    tc_fence_before();
+    tmem_alloc(tmem_slot, (uint32_t)tmem_cols<BN, PERSIST>());
+    fence_before();
   }
   __syncthreads();
-  tc_fence_after();
+  fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (threadIdx.x == 0) {
+  if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
     uint64_t pol_w, pol_x;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+    if (PERSIST) {
+      // a weight tile is read by the CTAs of neighbouring tiles at about the same time
+      asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol_w));
+    } else {
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+    }
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
-    auto load_w = [&](int i, int s) {
+    auto load_w = [&](int st, int m_tile, int kb) {
       if (SWI) {
-        tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, m_tile * (BM / 2), pol_w);
-        tma_load_2d(sA + s * A_BYTES + A_BYTES / 2, &tmW2, &full[s], (kb0 + i) * BK, m_tile * (BM / 2), pol_w);
+        tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], kb * BK, m_tile * (BM / 2), pol_w);
+        tma_load_2d(sA + st * A_BYTES + A_BYTES / 2, &tmW2, &full[st], kb * BK, m_tile * (BM / 2), pol_w);
       } else {
-        tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM, pol_w);
+        tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], kb * BK, m_tile * BM, pol_w);
       }
     };
     // Weights do not depend on the previous kernel: the first stages of them
     // are requested before waiting for it, so the weight stream starts while
     // the previous kernel drains.
-    const int pre = nkb < STAGES ? nkb : STAGES;
-    for (int i = 0; i < pre; ++i) {
-      mbar_expect_tx(&full[i], TX);
-      load_w(i, i);
-    }
-    pdl_wait();
-    for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * B_BYTES, &tmX, &full[i], (kb0 + i) * BK, n_tile * BN, pol_x);
-    int issued = pre;
-    for (int i = pre; i < nkb; ++i) {
-      const int s = i % STAGES;
-      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-      if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
-        atomicOr(p.err, 4);
-        *abort_flag = 1;
-        break;
+    int it = 0;
+    for_each_unit<PERSIST>(p, [&](int t, int s) {
+      int kb0, kb1;
+      split_range(p, s, kb0, kb1);
+      for (int kb = kb0; kb < kb1 && it < STAGES; ++kb, ++it) {
+        mbar_expect_tx(&full[it], TX);
+        load_w(it, t / p.n_tiles, kb);
       }
-      mbar_expect_tx(&full[s], TX);
-      load_w(i, s);
-      tma_load_2d(sB + s * B_BYTES, &tmX, &full[s], (kb0 + i) * BK, n_tile * BN, pol_x);
-      ++issued;
-    }
-    if (*abort_flag) {
+      return it < STAGES;
+    });
+    const int pre = it;
+    pdl_wait();
+    it = 0;
+    bool ok = true;
+    for_each_unit<PERSIST>(p, [&](int t, int s) {
+      int kb0, kb1;
+      split_range(p, s, kb0, kb1);
+      const int m_tile = t / p.n_tiles, n_tile = t % p.n_tiles;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int st = it % STAGES;
+        if (it >= pre) {
+          if (!mbar_wait(&empty[st], ((uint32_t)(it / STAGES) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            return false;
+          }
+          mbar_expect_tx(&full[st], TX);
+          load_w(st, m_tile, kb);
+        }
+        tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], kb * BK, n_tile * BN, pol_x);
+      }
+      return true;
+    });
+    if (!ok) {
+      atomicOr(p.err, kErrBit);
+      *abort_flag = 1;
       // let this CTA's own copies land before its shared memory is released
-      for (int i = max(0, issued - STAGES); i < issued; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      for (int i = max(0, it - STAGES); i < it; ++i) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&full[s], ph) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u) &&
+               globaltimer_ns() - t0 < kWaitLimitNs) {
         }
       }
     }
-  } else if (threadIdx.x == 32) {
+  } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
-    constexpr uint32_t idesc = idesc_bf16<BN>();
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % STAGES;
-      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-      if (!mbar_wait(&full[s], ph, abort_flag)) {
-        atomicOr(p.err, 4);
-        *abort_flag = 1;
-        break;
+    constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    int it = 0, j = 0;
+    bool ok = true;
+    for_each_unit<PERSIST>(p, [&](int, int s) {
+      const int b = PERSIST ? (j & 1) : 0;
+      if (PERSIST && j >= 2 && !mbar_wait(&acce[b], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+        ok = false;
+        return false;
       }
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(sA + s * A_BYTES), b0 = smem_u32(sB + s * B_BYTES);
+      fence_after();
+      const uint32_t d = tmem + (uint32_t)(b * BN);
+      int kb0, kb1;
+      split_range(p, s, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int st = it % STAGES;
+        if (!mbar_wait(&full[st], (uint32_t)(it / STAGES) & 1u, abort_flag)) {
+          ok = false;
+          return false;
+        }
+        fence_after();
+        const uint32_t a0 = smem_u32(sA + st * A_BYTES), b0 = smem_u32(sB + st * B_BYTES);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k)
-        umma_bf16(tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc, (i | k) != 0);
-      umma_commit(&empty[s]);
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16(d, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty[st]);
+      }
+      umma_commit(&accf[b]);  // arrives once every MMA of this split has completed
+      ++j;
+      return true;
+    });
+    if (!ok) {
+      atomicOr(p.err, kErrBit);
+      *abort_flag = 1;
+      umma_commit(drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
     }
-    umma_commit(done);  // arrives once every MMA issued above has completed
+  } else if (warp >= 2) {
+    // ---- epilogue: TMEM -> sums -> staged tile ----
+    const int q = warp & 3;  // the TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;
+    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+    pdl_wait();  // the stores below read (residual) and write memory of earlier kernels
+    int j = 0;
+    for_each_unit<PERSIST>(p, [&](int t, int s) {
+      const int b = PERSIST ? (j & 1) : 0;
+      bool bad = !mbar_wait(&accf[b], PERSIST ? (uint32_t)(j >> 1) & 1u : 0u, abort_flag);
+      if (PERSIST) bad = epi_bar_or(bad);
+      if (bad) {
+        if (lane == 0) atomicOr(p.err, kErrBit);
+        *abort_flag = 1;
+        return false;
+      }
+      fence_after();
+      const uint32_t acc = lanes + (uint32_t)(b * BN);
+      const uint32_t run = lanes + (uint32_t)(2 * BN);  // running sum (persistent, split > 0)
+      const bool last = s == p.splits - 1;
+      if (!PERSIST || last) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += CH) {
+          float v[CH];
+          tmem_ld<CH>(acc + c0, v);
+          if (PERSIST && p.splits > 1) {
+            float r[CH];
+            tmem_ld<CH>(run + c0, r);
+#pragma unroll
+            for (int i = 0; i < CH; ++i) v[i] = r[i] + v[i];
+          }
+#pragma unroll
+          for (int i = 0; i < CH; ++i) stg[(c0 + i) * BM + row] = v[i];
+        }
+      } else {
+        // running sum of the splits so far: (0 + P_0) + P_1 + ...
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32], r[32];
+          tmem_ld32(acc + c0, v);
+          if (s == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0.f + v[i];
+          } else {
+            tmem_ld32(run + c0, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = r[i] + v[i];
+          }
+          tmem_st32(run + c0, r);
+        }
+      }
+      // accumulator b may be refilled
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[b]);
+      if (PERSIST && last) {
+        epi_bar();  // the staged tile is complete
+        store_tile<SWI>(p, t / p.n_tiles, (t % p.n_tiles) * BN, 0, BN * ROWS / 4, (int)threadIdx.x - 64, kEpiThreads,
+                        [&](int c, int f) { return *reinterpret_cast<const float4*>(&stg[c * BM + f]); });
+        epi_bar();  // staging is free for the next tile
+      }
+      ++j;
+      return true;
+    });
   }
   __syncwarp();
-  pdl_wait();  // the epilogue reads (residual) and writes memory the previous kernels use
 
-  // ---- epilogue: TMEM -> registers -> global ----
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(done, 0)) {
-    if (globaltimer_ns() - t0 > 2 * kWaitLimitNs) {
-      atomicOr(p.err, 4);
-      break;
-    }
-  }
-  tc_fence_after();
-  const int row = warp * 32 + lane;   // TMEM lane = weight row within the tile
-  const int tok0 = n_tile * BN;
-  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-  // The pipeline buffers are idle once every MMA has completed: the final
-  // tile is staged there as S[col][row] (fp32) for a coalesced store.
-  float* S = reinterpret_cast<float*>(smem);
-  bool store = true;
-  if (p.splits == 1) {
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += CH) {
-      float v[CH];
-      tmem_ld<CH>(taddr + c0, v);
-#pragma unroll
-      for (int j = 0; j < CH; ++j) S[(c0 + j) * BM + row] = v[j];
-    }
-  } else {
-    const int tile = m_tile * p.n_tiles + n_tile;
-    float* mine = p.ws + ((int64_t)(tile * p.splits + split) * BN) * BM;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += CH) {
-      float v[CH];
-      tmem_ld<CH>(taddr + c0, v);
-#pragma unroll
-      for (int j = 0; j < CH; ++j) __stcg(mine + (int64_t)(c0 + j) * BM + row, v[j]);
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *last_flag = atomicAdd(&p.counters[tile], 1) == p.splits - 1;
-    __syncthreads();
-    store = *last_flag != 0;
-    if (store) {
-      // the last CTA of the tile sums the partials in split order; all loads
-      // of a column group are issued before the adds
-      __threadfence();
-      const float* base = p.ws + (int64_t)tile * p.splits * BN * BM + row;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 4) {
-        float v[kMaxSplits][4];
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplits; ++sp)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            v[sp][j] = sp < p.splits ? __ldcg(base + ((int64_t)sp * BN + c0 + j) * BM) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float acc = 0.f;
-#pragma unroll
-          for (int sp = 0; sp < kMaxSplits; ++sp)
-            if (sp < p.splits) acc += v[sp][j];
-          S[(c0 + j) * BM + row] = acc;
-        }
-      }
-      if (threadIdx.x == 0) p.counters[tile] = 0;
-    }
-  }
-  __syncthreads();
-  if (store) {
-    if (SWI) {
-      // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
-      bf16* out = reinterpret_cast<bf16*>(p.Y);
-      for (int e = threadIdx.x; e < BN * (BM / 2); e += blockDim.x) {
-        const int c = e / (BM / 2), f = e % (BM / 2);
-        const int t = tok0 + c, feat = m_tile * (BM / 2) + f;
-        if (t < p.M && feat < p.N) {
-          const float g = S[c * BM + f], u = S[c * BM + BM / 2 + f];
-          out[(int64_t)t * p.ldy + feat] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
-        }
-      }
-    } else if (p.mode == kResidBf16) {
-      bf16* h = reinterpret_cast<bf16*>(p.Y);
-      for (int e = threadIdx.x; e < BN * BM; e += blockDim.x) {
-        const int c = e / BM, f = e % BM;
-        const int t = tok0 + c, feat = m_tile * BM + f;
-        if (t < p.M && feat < p.N) {
-          bf16* hp = h + (int64_t)t * p.ldy + feat;
-          *hp = __float2bfloat16_rn(__bfloat162float(*hp) + S[c * BM + f]);
-        }
-      }
+  if (!PERSIST) {
+    // ---- split clusters: sum the partials in split order, then store ----
+    pdl_wait();
+    const int t = (int)blockIdx.x / p.splits;
+    const int m_tile = t / p.n_tiles, tok0 = (t % p.n_tiles) * BN;
+    const int E = BN * ROWS / 4;  // 4-feature groups of the tile
+    if (p.splits == 1) {
+      __syncthreads();
+      if (!*abort_flag)
+        store_tile<SWI>(p, m_tile, tok0, 0, E, threadIdx.x, kThreads,
+                        [&](int c, int f) { return *reinterpret_cast<const float4*>(&stg[c * BM + f]); });
     } else {
-      float* Y = reinterpret_cast<float*>(p.Y);
-      for (int e = threadIdx.x; e < BN * BM; e += blockDim.x) {
-        const int c = e / BM, f = e % BM;
-        const int t = tok0 + c, feat = m_tile * BM + f;
-        if (t < p.M && feat < p.N) Y[(int64_t)t * p.ldy + feat] = S[c * BM + f];
-      }
+      cg::cluster_group cl = cg::this_cluster();
+      cl.sync();  // every partial of the tile is staged
+      const int r = (int)cl.block_rank();
+      const float4* peer[kMaxSplits];
+#pragma unroll
+      for (int i = 0; i < kMaxSplits; ++i)
+        peer[i] = reinterpret_cast<const float4*>(i < p.splits ? cl.map_shared_rank(stg, i) : stg);
+      const int lo = (int)((int64_t)r * E / p.splits), hi = (int)((int64_t)(r + 1) * E / p.splits);
+      if (!*abort_flag)
+        store_tile<SWI>(p, m_tile, tok0, lo, hi, threadIdx.x, kThreads, [&](int c, int f) {
+          const int idx = (c * BM + f) / 4;
+          float4 v[kMaxSplits];
+#pragma unroll
+          for (int i = 0; i < kMaxSplits; ++i) v[i] = i < p.splits ? peer[i][idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < kMaxSplits; ++i)
+            if (i < p.splits) {
+              acc.x += v[i].x;
+              acc.y += v[i].y;
+              acc.z += v[i].z;
+              acc.w += v[i].w;
+            }
+          return acc;
+        });
+      cl.sync();  // no CTA leaves while a peer still reads its partial
     }
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)tmem_cols<BN>())
-                 : "memory");
+    fence_after();
+    tmem_dealloc(tmem, (uint32_t)tmem_cols<BN, PERSIST>());
   }
 }
 
@@ -418,12 +506,8 @@ __global__ void __launch_bounds__(128, 1) k_gemm_tc(const __grid_constant__ CUte
 struct TcContext {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   int num_sms = 0;
-  float* ws = nullptr;
-  size_t ws_cap = 0;
-  int* counters = nullptr;
-  size_t cnt_cap = 0;
   int* err = nullptr;
-  bool attr_set[10] = {};
+  bool attr_set[12] = {};
 };
 
 const char* tc_last_error() { return g_tc_err.c_str(); }
@@ -450,12 +534,7 @@ int tc_create(TcContext** out, int num_sms, int* err) {
   return 0;
 }
 
-void tc_destroy(TcContext* c) {
-  if (!c) return;
-  cudaFree(c->ws);
-  cudaFree(c->counters);
-  delete c;
-}
+void tc_destroy(TcContext* c) { delete c; }
 
 static int encode_2d(TcContext* c, CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, int64_t ld_elems,
                      uint32_t box_rows) {
@@ -501,18 +580,32 @@ int tc_encode_kv_maps(TcContext* c, const void* kv, int64_t cap, int d, int plan
   return 0;
 }
 
-template <int BN, bool SWI>
+template <int BN, bool SWI, bool PERSIST>
 static int launch_bn(TcContext* c, const CUtensorMap& mw, const CUtensorMap& mw2, const CUtensorMap& mx,
-                     const TcParams& p, int grid, cudaStream_t st, int slot) {
-  const size_t smem = smem_bytes<BN>();
+                     const TcParams& p, int grid, int cluster, cudaStream_t st, int slot) {
+  const size_t smem = smem_bytes<BN, PERSIST>();
   if (!c->attr_set[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, SWI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_gemm_tc<BN, SWI, PERSIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return tc_fail("smem attribute", e);
     c->attr_set[slot] = true;
   }
-  const cudaError_t e = launch_k(k_gemm_tc<BN, SWI>, grid, 128, smem, st, mw, mw2, mx, p);
+  const cudaError_t e = launch_kc(k_gemm_tc<BN, SWI, PERSIST>, grid, kThreads, smem, st, cluster, mw, mw2, mx, p);
   if (e != cudaSuccess) return tc_fail("k_gemm_tc launch", e);
   return 0;
+}
+
+template <bool SWI>
+static int launch_mode(TcContext* c, int BN, bool persist, const CUtensorMap& mw, const CUtensorMap& mw2,
+                       const CUtensorMap& mx, const TcParams& p, int grid, int cluster, cudaStream_t st) {
+  const int base = SWI ? 6 : 0;
+  if (persist) return launch_bn<kPersistBN, SWI, true>(c, mw, mw2, mx, p, grid, cluster, st, base + 5);
+  switch (BN) {
+    case 16: return launch_bn<16, SWI, false>(c, mw, mw2, mx, p, grid, cluster, st, base + 0);
+    case 32: return launch_bn<32, SWI, false>(c, mw, mw2, mx, p, grid, cluster, st, base + 1);
+    case 64: return launch_bn<64, SWI, false>(c, mw, mw2, mx, p, grid, cluster, st, base + 2);
+    default: return launch_bn<128, SWI, false>(c, mw, mw2, mx, p, grid, cluster, st, base + 3);
+  }
 }
 
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y,
@@ -522,38 +615,19 @@ int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void*
   if (K % BK || ldx % 8 || ldw % 8 || ((uintptr_t)X & 15) || ((uintptr_t)W & 15) || (swi && ((uintptr_t)W2 & 15)))
     return tc_fail("tc_gemm: K must be a multiple of 64, strides multiples of 8, operands 16-byte aligned");
   if (mode < kF32 || mode > kSwigluBf16) return tc_fail("tc_gemm: unknown mode");
-  const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   const int rows_per_tile = swi ? BM / 2 : BM;
-  const int m_tiles = (N + rows_per_tile - 1) / rows_per_tile, n_tiles = (M + BN - 1) / BN, kb_total = K / BK;
-  // Split K so that the weight tiles fill one wave of resident CTAs (two per
-  // SM up to BN = 128, one at 256); the split depends on N and K only.
-  const int slots = c->num_sms * (BN <= 128 ? 2 : 1);
-  int splits = slots / m_tiles;
+  const int m_tiles = (N + rows_per_tile - 1) / rows_per_tile, kb_total = K / BK;
+  // The split of K fills about one wave of two CTAs per SM with the weight
+  // tiles of a small call; it depends on N, K and the SM count only.
+  int splits = 2 * c->num_sms / m_tiles;
   splits = std::max(1, std::min({splits, kMaxSplits, std::max(1, kb_total / 2)}));
+  // Many rows: persistent 128-row tiles once they cover half of the SMs;
+  // otherwise one CTA per (tile, split), the splits of a tile in a cluster.
+  const int tiles128 = m_tiles * ((M + kPersistBN - 1) / kPersistBN);
+  const bool persist = M > 128 && 2 * tiles128 >= c->num_sms;
+  const int BN = persist ? kPersistBN : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  const int n_tiles = (M + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
-  if (splits > 1) {
-    const size_t need = (size_t)tiles * splits * BN * BM * sizeof(float);
-    if (need > c->ws_cap) {
-      cudaError_t e = cudaStreamSynchronize(st);
-      if (e == cudaSuccess) e = cudaFree(c->ws);
-      c->ws = nullptr;
-      c->ws_cap = 0;
-      if (e == cudaSuccess) e = cudaMalloc(&c->ws, need + need / 4);
-      if (e != cudaSuccess) return tc_fail("split workspace", e);
-      c->ws_cap = need + need / 4;
-    }
-    if ((size_t)tiles > c->cnt_cap) {
-      cudaError_t e = cudaStreamSynchronize(st);
-      if (e == cudaSuccess) e = cudaFree(c->counters);
-      c->counters = nullptr;
-      c->cnt_cap = 0;
-      const size_t want = (size_t)tiles * 2;
-      if (e == cudaSuccess) e = cudaMalloc(&c->counters, want * sizeof(int));
-      if (e == cudaSuccess) e = cudaMemsetAsync(c->counters, 0, want * sizeof(int), st);
-      if (e != cudaSuccess) return tc_fail("split counters", e);
-      c->cnt_cap = want;
-    }
-  }
   CUtensorMap mw, mw2, mx;
   if (encode_2d(c, &mw, W, (uint64_t)K, (uint64_t)N, ldw, (uint32_t)rows_per_tile)) return -1;
   if (swi) {
@@ -562,24 +636,12 @@ int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void*
     mw2 = mw;
   }
   if (encode_2d(c, &mx, X, (uint64_t)K, (uint64_t)M, ldx, (uint32_t)BN)) return -1;
-  TcParams p{Y, ldy, M, N, mode, n_tiles, splits, kb_total, c->ws, c->counters, c->err};
-  const int grid = tiles * splits;
-  if (swi) {
-    switch (BN) {
-      case 16: return launch_bn<16, true>(c, mw, mw2, mx, p, grid, st, 5);
-      case 32: return launch_bn<32, true>(c, mw, mw2, mx, p, grid, st, 6);
-      case 64: return launch_bn<64, true>(c, mw, mw2, mx, p, grid, st, 7);
-      case 128: return launch_bn<128, true>(c, mw, mw2, mx, p, grid, st, 8);
-      default: return launch_bn<256, true>(c, mw, mw2, mx, p, grid, st, 9);
-    }
-  }
-  switch (BN) {
-    case 16: return launch_bn<16, false>(c, mw, mw2, mx, p, grid, st, 0);
-    case 32: return launch_bn<32, false>(c, mw, mw2, mx, p, grid, st, 1);
-    case 64: return launch_bn<64, false>(c, mw, mw2, mx, p, grid, st, 2);
-    case 128: return launch_bn<128, false>(c, mw, mw2, mx, p, grid, st, 3);
-    default: return launch_bn<256, false>(c, mw, mw2, mx, p, grid, st, 4);
-  }
+  const int vec = ldy % 4 == 0 && ((uintptr_t)Y & 15) == 0;
+  TcParams p{Y, ldy, M, N, mode, m_tiles, n_tiles, splits, kb_total, vec, c->err};
+  const int grid = persist ? std::min(tiles, c->num_sms) : tiles * splits;
+  const int cluster = persist ? 1 : splits;
+  return swi ? launch_mode<true>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st)
+             : launch_mode<false>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st);
 }
 
 }  // namespace dfl
