@@ -88,13 +88,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
 
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const AttnItem it = items[blockIdx.x];
-  const int G = p.Hq / p.Hkv, R = p.nrows * G;
-  const int64_t F = tabs.frontier[it.sess], cap = tabs.cap[it.sess];
-  const CUtensorMap* kmap = tabs.kvmaps[it.sess];
-  const CUtensorMap* vmap = kmap + 1;
-  const int planeK = 2 * p.layer * p.Hkv + it.kvh, planeV = (2 * p.layer + 1) * p.Hkv + it.kvh;
-  const int T = (int)((it.k1 - it.k0 + KT - 1) / KT);
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -110,8 +103,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     mbar_init(o_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)kmap) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)vmap) : "memory");
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -120,7 +111,20 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // Q and the block's K/V come from the previous kernel
+  // The work item and the session tables belong to this call: they are
+  // written by an earlier kernel of the chain, like Q and the block's K/V.
+  pdl_wait();
+  const AttnItem it = items[blockIdx.x];
+  const int G = p.Hq / p.Hkv, R = p.nrows * G;
+  const int64_t F = tabs.frontier[it.sess], cap = tabs.cap[it.sess];
+  const CUtensorMap* kmap = tabs.kvmaps[it.sess];
+  const CUtensorMap* vmap = kmap + 1;
+  const int planeK = 2 * p.layer * p.Hkv + it.kvh, planeV = (2 * p.layer + 1) * p.Hkv + it.kvh;
+  const int T = (int)((it.k1 - it.k0 + KT - 1) / KT);
+  if (tid == 256) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)kmap) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)vmap) : "memory");
+  }
 
   // ---- Q rows of this KV head, zero padded to 128, as the MMA's A tile
   if (warp < 8) {

@@ -81,9 +81,11 @@ struct Buf {
   template <typename T> T* as() const { return (T*)p; }
 };
 
-// Packs the small per-call tables into one host block, uploaded with a single
-// copy.  The host side is a ring of pinned slots guarded by events so that a
-// slot is never rewritten while its copy is still queued.
+// Packs the small per-call tables into one host block.  Up to
+// kTableParamMax bytes it travels as the parameter of a one-CTA kernel in the
+// launch chain (launch_table_write); a larger block is copied from a ring of
+// pinned host slots guarded by events, so that a slot is never rewritten
+// while its copy is still queued.
 struct TablePack {
   std::vector<char> host;
   size_t add(const void* src, size_t bytes) {
@@ -104,6 +106,11 @@ struct HostRing {
   int upload(const TablePack& t, Buf& dev, cudaStream_t st) {
     const size_t bytes = std::max<size_t>(t.host.size(), 16);
     ST_TRY(dev.ensure(bytes, st));
+    if (t.host.size() <= (size_t)kTableParamMax) {
+      // small tables go through the launch chain as a kernel parameter
+      if (launch_table_write(dev.p, t.host.data(), t.host.size(), st)) return fail(DFLASH_ERR_CUDA, "table write launch");
+      return DFLASH_OK;
+    }
     const int i = next;
     next = (next + 1) % kSlots;
     if (!ev[i]) CU_TRY(cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming));
@@ -258,6 +265,18 @@ int gemm(dflash_model* m, const void* X, int64_t ldx, const void* W, int64_t ldw
   return DFLASH_OK;
 }
 
+// Y rows [j*seg_rows, (j+1)*seg_rows) into yseg[j] (device table); tensor-core path only.
+int gemm_rows(dflash_model* m, const void* X, int64_t ldx, const void* W, int64_t ldw, void* const* yseg, int seg_rows,
+              int64_t ldy, int M, int N, int K, cudaStream_t st) {
+  if (M <= 0) return DFLASH_OK;
+  const double bytes = (double)N * K * m->esz + (double)M * K * m->esz + (double)M * N * 4;
+  Timed tm(m, kGemmTc, bytes, 2.0 * M * N * K, st);
+  m->launches++;
+  if (tc_gemm(m->tc, X, ldx, W, nullptr, ldw, nullptr, ldy, M, N, K, kF32, st, yseg, seg_rows))
+    return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
+  return DFLASH_OK;
+}
+
 // h[M][N] = storage(h + X W^T): the residual add after the attention output
 // and after the MLP down projection.
 int gemm_resid(dflash_model* m, const void* X, int64_t ldx, const void* W, void* h, float* tmp, int M, int N, int K,
@@ -389,6 +408,15 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
           items.push_back(AttnItem{j, h, k0v[j] + s * chunk, std::min(k1v[j], k0v[j] + (s + 1) * chunk)});
     }
   }
+  // each session's proposal state, written in place by the unembedding and the draw
+  std::vector<float*> plog(Bc), plse(Bc);
+  std::vector<int32_t*> ptok(Bc);
+  for (int j = 0; j < Bc; ++j) {
+    plog[j] = fw.sess[j]->plogits;
+    plse[j] = fw.sess[j]->plse;
+    ptok[j] = fw.sess[j]->ptok;
+  }
+  const size_t o_plog = tp.add(plog), o_plse = tp.add(plse), o_ptok = tp.add(ptok);
   const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
                o_front = tp.add(front), o_seq = tp.add(seqv), o_items = tp.add(items), o_ifirst = tp.add(ifirst),
                o_icount = tp.add(icount), o_map = tp.add(fw.sess_map), o_maps = tp.add(mapv);
@@ -489,19 +517,29 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   const int n = fw.n, Rz = Bc * n;
   launch_rmsnorm(m->dt, false, m->h.p, Mb, nullptr, H, m->final_norm, m->z.p, H, Rz, H, n, nrows, 1, c.rms_eps, st);
   m->launches++;
-  float* lg;
+  // The tensor-core unembedding writes each session's rows straight into its
+  // proposal buffer; the CUDA-core path writes one block that is copied out.
+  float* lg = nullptr;
+  const bool seg = m->use_tc && Bc > 1;
   if (Bc == 1) {
     lg = fw.sess[0]->plogits;
-  } else {
+  } else if (!seg) {
     ST_TRY(m->logits.ensure((size_t)Rz * V * 4, st));
     lg = m->logits.as<float>();
   }
-  ST_TRY(gemm(m, m->z.p, H, m->unembed, H, lg, V, Rz, V, H, st));
+  if (seg) {
+    ST_TRY(gemm_rows(m, m->z.p, H, m->unembed, H, (void* const*)(tb + o_plog), n, V, Rz, V, H, st));
+  } else {
+    ST_TRY(gemm(m, m->z.p, H, m->unembed, H, lg, V, Rz, V, H, st));
+  }
   const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
   ST_TRY(m->spart.ensure((size_t)Rz * chunks * sizeof(float4), st));
   ST_TRY(m->vstat.ensure((size_t)Rz * 8, st));
   SampleArgs sa{};
   sa.logits = lg;
+  sa.seq_logits = seg ? (const float* const*)(tb + o_plog) : nullptr;
+  sa.sess_tok = (int32_t* const*)(tb + o_ptok);
+  sa.sess_lse = (float* const*)(tb + o_plse);
   sa.ld = V;
   sa.rows = Rz;
   sa.V = V;
@@ -514,23 +552,19 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   sa.row_offset = 1;
   sa.seq_ids = tabs.seq;
   sa.err = m->d_err;
-  int32_t* tok = m->vstat.as<int32_t>();
-  float* lse = (float*)(tok + Rz);
   {
     Timed tm(m, kSample, (double)Rz * V * 4, 6.0 * Rz * V, st);
     launch_sample_partials(sa, chunk, m->spart.as<float4>(), st);
-    launch_sample_combine(sa, chunks, m->spart.as<float4>(), tok, nullptr, lse, st);
-    // outputs in caller order
+    // tokens and log-sum-exp into the sessions, tokens and q(token) in caller order
     sa.out_map = (const int32_t*)(tb + o_map);
     launch_sample_combine(sa, chunks, m->spart.as<float4>(), fw.out_tokens, fw.out_q, nullptr, st);
-    m->launches += 3;
+    m->launches += 2;
   }
   ST_TRY(launch_check("sample"));
   for (int j = 0; j < Bc; ++j) {
     dflash_session* s = fw.sess[j];
-    if (Bc > 1) CU_TRY(cudaMemcpyAsync(s->plogits, lg + (size_t)j * n * V, (size_t)n * V * 4, cudaMemcpyDeviceToDevice, st));
-    CU_TRY(cudaMemcpyAsync(s->plse, lse + j * n, n * 4, cudaMemcpyDeviceToDevice, st));
-    CU_TRY(cudaMemcpyAsync(s->ptok, tok + j * n, n * 4, cudaMemcpyDeviceToDevice, st));
+    if (Bc > 1 && !seg)
+      CU_TRY(cudaMemcpyAsync(s->plogits, lg + (size_t)j * n * V, (size_t)n * V * 4, cudaMemcpyDeviceToDevice, st));
     if (fw.out_logits)
       CU_TRY(cudaMemcpyAsync(fw.out_logits + (size_t)fw.sess_map[j] * n * V, s->plogits, (size_t)n * V * 4,
                              cudaMemcpyDeviceToDevice, st));
@@ -783,8 +817,9 @@ int dflash_committed(dflash_session* s, const void* features, int64_t row_stride
   const size_t es = s->m->esz;
   const char* src = (const char*)features + (size_t)start * row_stride * es;
   if (s->P + add < DFLASH_PENDING_FLUSH_TOKENS) {
-    CU_TRY(cudaMemcpy2DAsync((char*)s->pending + (size_t)s->P * width * es, width * es, src, row_stride * es, width * es,
-                             add, cudaMemcpyDeviceToDevice, s->stream));
+    launch_copy_rows((char*)s->pending + (size_t)s->P * width * es, (int64_t)(width * es), src,
+                     (int64_t)(row_stride * es), (int64_t)(width * es), add, s->stream);
+    ST_TRY(launch_check("pending rows"));
     s->P += add;
     return DFLASH_OK;
   }

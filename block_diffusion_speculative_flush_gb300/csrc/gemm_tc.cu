@@ -61,7 +61,12 @@ constexpr int BM = 128;        // weight rows per tile (MMA M)
 constexpr int BK = 64;         // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kMaxSplits = 8;  // the largest portable cluster
+// Splits are clusters of at most 4 CTAs: with 8, only about half of the
+// clusters of a one-wave grid were resident at once on GB300 and the rest ran
+// as a second wave.
+constexpr int kMaxSplits = 4;
+constexpr int kMaxStages = 16;
+constexpr size_t kBarrierBytes = 512;
 constexpr int kPersistBN = 128;
 constexpr int kErrBit = 4;
 
@@ -72,27 +77,22 @@ struct TcParams {
   int mode;        // TcMode
   int m_tiles, n_tiles, splits, kb_total;
   int vec;         // rows of Y start on 16-byte boundaries (ldy % 4 == 0, Y aligned)
+  int stages;      // depth of the TMA ring (2..kMaxStages), from the shared memory budget
+  void* const* yseg;  // fp32 output only: rows [j*seg_rows, (j+1)*seg_rows) go to yseg[j] (NULL: Y)
+  int seg_rows;
   int* err;
 };
 
-template <int BN, bool PERSIST>
-__host__ __device__ constexpr int stages_for() {
-  return PERSIST ? 4 : BN <= 16 ? 6 : BN <= 32 ? 5 : BN <= 64 ? 4 : 3;
-}
+constexpr int stage_bytes(int BN) { return BM * BK * 2 + BN * BK * 2; }
 template <int BN, bool PERSIST>
 __host__ __device__ constexpr int tmem_cols() {
   return PERSIST ? 512 : BN < 32 ? 32 : BN;
 }
-// fp32 tile staged for the store: aliases the idle pipeline in the cluster
-// schedule, a region of its own in the persistent one (the pipeline is busy
-// with the next tile while the epilogue stores).
-template <int BN, bool PERSIST>
-__host__ __device__ constexpr size_t staging_bytes() {
-  return PERSIST ? (size_t)BN * BM * 4 : 0;
-}
-template <int BN, bool PERSIST>
-__host__ __device__ constexpr size_t smem_bytes() {
-  return (size_t)stages_for<BN, PERSIST>() * (BM * BK * 2 + BN * BK * 2) + staging_bytes<BN, PERSIST>() + 1024 + 256;
+// Dynamic shared memory: the TMA ring, then (persistent schedule only) the
+// fp32 tile staged for the store, which in the cluster schedule aliases the
+// idle ring instead; then the barriers.
+size_t smem_bytes(int BN, bool persist, int stages) {
+  return (size_t)stages * stage_bytes(BN) + (persist ? (size_t)BN * BM * 4 : 0) + 1024 + kBarrierBytes;
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -149,36 +149,42 @@ __device__ __forceinline__ void store_tile(const TcParams& p, int m_tile, int to
   constexpr int U = 2;
   constexpr int ROWS = SWI ? BM / 2 : BM;
   constexpr int G = ROWS / 4;
+  const bool bf = SWI || p.mode == kResidBf16;
   for (int e0 = lo + tid; e0 < hi; e0 += U * nthr) {
     float4 v[U], w[U];
-    int64_t off[U];
-    int nv[U];  // valid features of the group (0..4)
+    void* yp[U];  // first output element of the group
+    int nv[U];    // valid features of the group (0..4)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int e = e0 + u * nthr;
       const int c = e / G, f = (e % G) * 4;
       const int t = tok0 + c, feat = m_tile * ROWS + f;
       nv[u] = (e < hi && t < p.M) ? max(0, min(4, p.N - feat)) : 0;
-      off[u] = (int64_t)t * p.ldy + feat;
       v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       w[u] = v[u];
-      if (nv[u]) {
-        v[u] = get4(c, f);
-        if (SWI) {
-          w[u] = get4(c, f + BM / 2);
-        } else if (p.mode == kResidBf16) {
-          const bf16* h = reinterpret_cast<const bf16*>(p.Y) + off[u];
-          if (nv[u] == 4 && p.vec) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(h);
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-            w[u] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
-          } else {
-            float* wf = reinterpret_cast<float*>(&w[u]);
+      yp[u] = nullptr;
+      if (!nv[u]) continue;
+      if (p.yseg)
+        yp[u] = reinterpret_cast<float*>(p.yseg[t / p.seg_rows]) + (int64_t)(t % p.seg_rows) * p.ldy + feat;
+      else if (bf)
+        yp[u] = reinterpret_cast<bf16*>(p.Y) + (int64_t)t * p.ldy + feat;
+      else
+        yp[u] = reinterpret_cast<float*>(p.Y) + (int64_t)t * p.ldy + feat;
+      v[u] = get4(c, f);
+      if (SWI) {
+        w[u] = get4(c, f + BM / 2);
+      } else if (p.mode == kResidBf16) {
+        const bf16* h = reinterpret_cast<const bf16*>(yp[u]);
+        if (nv[u] == 4 && p.vec) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(h);
+          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+          w[u] = make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+        } else {
+          float* wf = reinterpret_cast<float*>(&w[u]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (i < nv[u]) wf[i] = __bfloat162float(h[i]);
-          }
+          for (int i = 0; i < 4; ++i)
+            if (i < nv[u]) wf[i] = __bfloat162float(h[i]);
         }
       }
     }
@@ -186,7 +192,6 @@ __device__ __forceinline__ void store_tile(const TcParams& p, int m_tile, int to
     for (int u = 0; u < U; ++u) {
       if (!nv[u]) continue;
       float4 o;
-      const bool bf = SWI || p.mode == kResidBf16;
       if (SWI) {
         const float* g = reinterpret_cast<const float*>(&v[u]);
         const float* up = reinterpret_cast<const float*>(&w[u]);
@@ -199,7 +204,7 @@ __device__ __forceinline__ void store_tile(const TcParams& p, int m_tile, int to
         o = v[u];
       }
       if (bf) {
-        bf16* y = reinterpret_cast<bf16*>(p.Y) + off[u];
+        bf16* y = reinterpret_cast<bf16*>(yp[u]);
         if (nv[u] == 4 && p.vec) {
           const __nv_bfloat162 a = __floats2bfloat162_rn(o.x, o.y), b = __floats2bfloat162_rn(o.z, o.w);
           uint2 raw;
@@ -213,7 +218,7 @@ __device__ __forceinline__ void store_tile(const TcParams& p, int m_tile, int to
             if (i < nv[u]) y[i] = __float2bfloat16_rn(of[i]);
         }
       } else {
-        float* y = reinterpret_cast<float*>(p.Y) + off[u];
+        float* y = reinterpret_cast<float*>(yp[u]);
         if (nv[u] == 4 && p.vec) {
           *reinterpret_cast<float4*>(y) = o;
         } else {
@@ -234,21 +239,19 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
                                                                        const __grid_constant__ CUtensorMap tmW2,
                                                                        const __grid_constant__ CUtensorMap tmX,
                                                                        TcParams p) {
-  constexpr int STAGES = stages_for<BN, PERSIST>();
+  const int STAGES = p.stages;
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr uint32_t TX = A_BYTES + B_BYTES;
   constexpr int CH = BN < 32 ? BN : 32;
   constexpr int ROWS = SWI ? BM / 2 : BM;
-  static_assert(PERSIST || (size_t)BN * BM * 4 <= (size_t)STAGES * (A_BYTES + B_BYTES),
-                "the staged tile must fit the idle pipeline");
   static_assert(!PERSIST || BN == kPersistBN, "persistent tiles are 128 rows wide");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   float* stg = PERSIST ? reinterpret_cast<float*>(sB + STAGES * B_BYTES) : reinterpret_cast<float*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES + staging_bytes<BN, PERSIST>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES + (PERSIST ? (size_t)BN * BM * 4 : 0));
   uint64_t* empty = full + STAGES;
   uint64_t* accf = empty + STAGES;  // [2] accumulator b holds a finished split
   uint64_t* acce = accf + 2;        // [2] accumulator b has been drained
@@ -580,13 +583,18 @@ int tc_encode_kv_maps(TcContext* c, const void* kv, int64_t cap, int d, int plan
   return 0;
 }
 
+// Largest dynamic shared memory a k_gemm_tc launch asks for.
+constexpr size_t kSmemMax = 227 * 1024;
+
 template <int BN, bool SWI, bool PERSIST>
 static int launch_bn(TcContext* c, const CUtensorMap& mw, const CUtensorMap& mw2, const CUtensorMap& mx,
                      const TcParams& p, int grid, int cluster, cudaStream_t st, int slot) {
-  const size_t smem = smem_bytes<BN, PERSIST>();
+  const size_t smem = smem_bytes(BN, PERSIST, p.stages);
+  if (smem > kSmemMax || p.stages < 2 || p.stages > kMaxStages || (size_t)BN * BM * 4 > (size_t)p.stages * stage_bytes(BN))
+    return tc_fail("tc_gemm: pipeline does not fit shared memory");
   if (!c->attr_set[slot]) {
     cudaError_t e =
-        cudaFuncSetAttribute(k_gemm_tc<BN, SWI, PERSIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_gemm_tc<BN, SWI, PERSIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
     if (e != cudaSuccess) return tc_fail("smem attribute", e);
     c->attr_set[slot] = true;
   }
@@ -609,18 +617,22 @@ static int launch_mode(TcContext* c, int BN, bool persist, const CUtensorMap& mw
 }
 
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y,
-            int64_t ldy, int M, int N, int K, int mode, cudaStream_t st) {
+            int64_t ldy, int M, int N, int K, int mode, cudaStream_t st, void* const* yseg, int seg_rows) {
   if (M <= 0 || N <= 0) return 0;
   const bool swi = mode == kSwigluBf16;
+  if (yseg && (mode != kF32 || seg_rows <= 0)) return tc_fail("tc_gemm: row segments need fp32 output");
   if (K % BK || ldx % 8 || ldw % 8 || ((uintptr_t)X & 15) || ((uintptr_t)W & 15) || (swi && ((uintptr_t)W2 & 15)))
     return tc_fail("tc_gemm: K must be a multiple of 64, strides multiples of 8, operands 16-byte aligned");
   if (mode < kF32 || mode > kSwigluBf16) return tc_fail("tc_gemm: unknown mode");
   const int rows_per_tile = swi ? BM / 2 : BM;
   const int m_tiles = (N + rows_per_tile - 1) / rows_per_tile, kb_total = K / BK;
   // The split of K fills about one wave of two CTAs per SM with the weight
-  // tiles of a small call; it depends on N, K and the SM count only.
-  int splits = 2 * c->num_sms / m_tiles;
-  splits = std::max(1, std::min({splits, kMaxSplits, std::max(1, kb_total / 2)}));
+  // tiles of a small call; it depends on N, K and the SM count only.  It is
+  // a power of two: clusters of 3, 5, 6 or 7 CTAs pack the GPCs badly (a
+  // 6-way split of a 48-tile product ran 1.5x slower than a 4-way one).
+  int cap = std::max(1, std::min({2 * c->num_sms / m_tiles, kMaxSplits, std::max(1, kb_total / 2)}));
+  int splits = 1;
+  while (splits * 2 <= cap) splits *= 2;
   // Many rows: persistent 128-row tiles once they cover half of the SMs;
   // otherwise one CTA per (tile, split), the splits of a tile in a cluster.
   const int tiles128 = m_tiles * ((M + kPersistBN - 1) / kPersistBN);
@@ -637,8 +649,14 @@ int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void*
   }
   if (encode_2d(c, &mx, X, (uint64_t)K, (uint64_t)M, ldx, (uint32_t)BN)) return -1;
   const int vec = ldy % 4 == 0 && ((uintptr_t)Y & 15) == 0;
-  TcParams p{Y, ldy, M, N, mode, m_tiles, n_tiles, splits, kb_total, vec, c->err};
   const int grid = persist ? std::min(tiles, c->num_sms) : tiles * splits;
+  // Pipeline depth from the shared memory of one CTA per SM when the grid
+  // fits one per SM, else of two: each CTA's stream is latency-bound, so the
+  // bytes in flight per SM set its bandwidth.
+  const size_t fixed = (persist ? (size_t)BN * BM * 4 : 0) + 1024 + kBarrierBytes;
+  const size_t budget = (persist || grid <= c->num_sms) ? kSmemMax : 112 * 1024;
+  const int stages = (int)std::min<size_t>(kMaxStages, (budget - fixed) / stage_bytes(BN));
+  TcParams p{Y, ldy, M, N, mode, m_tiles, n_tiles, splits, kb_total, vec, stages, yseg, seg_rows, c->err};
   const int cluster = persist ? 1 : splits;
   return swi ? launch_mode<true>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st)
              : launch_mode<false>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st);

@@ -26,8 +26,11 @@ enum TcMode {
 // multiples of 8 elements and 16-byte aligned operands; any M, N >= 1.  The
 // k order of every output element depends on N and K only (never on M), so
 // a row's result does not change with the number of rows in the call.
+// With yseg (device table, kF32 only) output rows [j*seg_rows, (j+1)*seg_rows)
+// go to the buffer yseg[j] (row stride ldy, 16-byte aligned) instead of
+// Y + row * ldy; Y is then unused.
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y, int64_t ldy,
-            int M, int N, int K, int mode, cudaStream_t st);
+            int M, int N, int K, int mode, cudaStream_t st, void* const* yseg = nullptr, int seg_rows = 0);
 
 // TMA maps of a session's K/V cache for the attention kernel: out[0] views
 // the K planes ([planes][cap][d], 64 x 64 boxes), out[1] the V^T planes

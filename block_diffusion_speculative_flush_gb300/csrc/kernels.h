@@ -96,6 +96,10 @@ struct SampleArgs {
   const int32_t* seq_ids;  // [B] seq id per session
   const int32_t* out_map;  // [B] output row block of each session (NULL: identity)
   int32_t* err;            // bit 16: a row had no comparable score (non-finite logits)
+  // optional per-session rows (fp32 logits only): row r of session b = r / rows_per_seq
+  const float* const* seq_logits;  // [B] logits of the session's rows (NULL: logits + row * ld)
+  int32_t* const* sess_tok;        // [B] also write the token of each row here
+  float* const* sess_lse;          // [B] also write the log-sum-exp of each row here
 };
 void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st);
 // Writes tok[row], q[row] (probability of the token at T), lse[row] (log-sum-exp of logits/T).
@@ -140,5 +144,15 @@ void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st
 
 // --- tensor-core path (bf16, sm_103a) --------------------------------------
 struct TcGemmPlan;  // opaque, defined in gemm_tc.cu
+
+// Largest per-call table that travels as a kernel parameter.
+constexpr int kTableParamMax = 31744;
+// Writes bytes (<= kTableParamMax) of host data to dst with a one-CTA kernel
+// in the launch chain; returns -1 if the table is too large.
+int launch_table_write(void* dst, const void* src, size_t bytes, cudaStream_t st);
+
+// rows x row_bytes from src (row stride src_ld bytes) to dst (dst_ld bytes), as a kernel.
+void launch_copy_rows(void* dst, int64_t dst_ld, const void* src, int64_t src_ld, int64_t row_bytes, int rows,
+                      cudaStream_t st);
 
 }  // namespace dfl

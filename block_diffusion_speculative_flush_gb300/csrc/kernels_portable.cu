@@ -18,6 +18,9 @@
 #include <float.h>
 #include <math.h>
 
+#include <cstring>
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.h"
@@ -435,6 +438,13 @@ __device__ __forceinline__ float load_logit(const void* p, int in_bf16, int64_t 
 
 // part[row][chunk] = (max of l/T, sum exp(l/T - max), best score, best index)
 // where the score is l/T + Gumbel (draft draw) or l/T (argmax / row stats).
+// Logit v of sampled row `row`, from the session's own rows when given.
+__device__ __forceinline__ float sample_logit(const SampleArgs& a, int row, int v) {
+  if (a.seq_logits)
+    return a.seq_logits[row / a.rows_per_seq][(int64_t)(row % a.rows_per_seq) * a.ld + v];
+  return load_logit(a.logits, a.in_bf16, (int64_t)row * a.ld + v);
+}
+
 __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
   pdl_trigger();
   pdl_wait();
@@ -449,7 +459,7 @@ __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ 
   float m = -INFINITY, l = 0.f;
   ArgMax best{-INFINITY, INT32_MAX};
   for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-    const float s = load_logit(a.logits, a.in_bf16, (int64_t)row * a.ld + v) * invT;
+    const float s = sample_logit(a, row, v) * invT;
     if (s > m) {
       l = l * expf(m - s) + 1.f;
       m = s;
@@ -516,9 +526,11 @@ __global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restr
   if (a.out_map) orow = a.out_map[row / a.rows_per_seq] * a.rows_per_seq + row % a.rows_per_seq;
   if (tok) tok[orow] = bb.i;
   if (lse) lse[orow] = ls;
+  if (a.sess_tok) a.sess_tok[row / a.rows_per_seq][row % a.rows_per_seq] = bb.i;
+  if (a.sess_lse) a.sess_lse[row / a.rows_per_seq][row % a.rows_per_seq] = ls;
   if (qtok) {
     if (a.temperature > 0.f) {
-      const float x = load_logit(a.logits, a.in_bf16, (int64_t)row * a.ld + bb.i) / a.temperature;
+      const float x = sample_logit(a, row, bb.i) / a.temperature;
       qtok[orow] = expf(x - ls);
     } else {
       qtok[orow] = 1.f;
@@ -662,6 +674,42 @@ __global__ void k_verify_finish(VerifyArgs a, int chunks, const VerifyPart* __re
 
 inline unsigned cdiv(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
 
+
+// Row copy inside the launch chain (a stream copy would stop programmatic
+// launch): grid (rows, pieces of 4096 bytes); 16-byte moves when both sides
+// allow them.
+__global__ void k_copy_rows(char* __restrict__ dst, int64_t dst_ld, const char* __restrict__ src, int64_t src_ld,
+                            int64_t row_bytes, int vec) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t r = blockIdx.x;
+  const int64_t b0 = (int64_t)blockIdx.y * 4096, b1 = min(row_bytes, b0 + 4096);
+  char* d = dst + r * dst_ld;
+  const char* s = src + r * src_ld;
+  if (vec) {
+    for (int64_t b = b0 + (int64_t)threadIdx.x * 16; b < b1; b += (int64_t)blockDim.x * 16)
+      *reinterpret_cast<uint4*>(d + b) = *reinterpret_cast<const uint4*>(s + b);
+  } else {
+    for (int64_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) d[b] = s[b];
+  }
+}
+
+// Per-call tables as a kernel parameter, written to device memory once the
+// previous kernel has completed (every kernel completes only after its own
+// predecessor, so no earlier launch still reads the buffer).  Keeps the
+// launch chain programmatic, where a host-to-device copy in the stream would
+// wait for the previous kernel to drain and start the next one cold.
+template <int N>
+struct TableBytes {
+  uint4 d[N / 16];
+};
+template <int N>
+__global__ void k_table_write(uint4* __restrict__ dst, int n16, const __grid_constant__ TableBytes<N> src) {
+  pdl_trigger();
+  pdl_wait();
+  for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src.d[i];
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -785,6 +833,28 @@ void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st
   const int chunk = kVerifyBonusChunk, chunks = verify_bonus_chunks(a.V);
   if (a.temperature > 0.f) launch_k(k_verify_bonus, dim3(a.B, chunks), 256, 0, st, a, chunk, part);
   launch_k(k_verify_finish, cdiv(a.B, 64), 64, 0, st, a, chunks, part);
+}
+
+int launch_table_write(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  const int n16 = (int)((bytes + 15) / 16);
+  auto go = [&](auto tag) -> int {
+    constexpr int N = decltype(tag)::value;
+    TableBytes<N> t;
+    memcpy(t.d, src, bytes);
+    return launch_k(k_table_write<N>, 1, 256, 0, st, (uint4*)dst, n16, t) == cudaSuccess ? 0 : -1;
+  };
+  if (bytes <= 4096) return go(std::integral_constant<int, 4096>());
+  if (bytes <= 16384) return go(std::integral_constant<int, 16384>());
+  if (bytes <= kTableParamMax) return go(std::integral_constant<int, kTableParamMax>());
+  return -1;
+}
+
+void launch_copy_rows(void* dst, int64_t dst_ld, const void* src, int64_t src_ld, int64_t row_bytes, int rows,
+                      cudaStream_t st) {
+  if (rows <= 0 || row_bytes <= 0) return;
+  const int vec = ((uintptr_t)dst | (uintptr_t)src | (uintptr_t)dst_ld | (uintptr_t)src_ld | (uintptr_t)row_bytes) % 16 == 0;
+  launch_k(k_copy_rows, dim3(rows, (unsigned)cdiv(row_bytes, 4096)), 256, 0, st, (char*)dst, dst_ld, (const char*)src,
+           src_ld, row_bytes, vec);
 }
 
 }  // namespace dfl

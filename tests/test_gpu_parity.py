@@ -421,3 +421,38 @@ def test_rows_do_not_depend_on_the_batch(D):
     D.dflash_device_status(p.model)
     for s in sess:
         D.dflash_close(s)
+
+
+def test_sessions_called_back_to_back_keep_their_own_tables(D):
+    """Six sessions with different context lengths propose one after another
+    on one stream, twice round: each call's kernels must read that call's
+    tables (work items, frontiers, cache maps), never the previous call's, so
+    every proposal equals its own session's oracle."""
+    p = Pair(S.CONFIGS["small_bf16"])
+    cfg = p.cfg
+    n = cfg.block_size - 1
+    lens = [12, 300, 40, 190, 75, 260]
+    sess, oss = [], []
+    for b, L in enumerate(lens):
+        f_np, f = p.feats(L, seed=40 + b)
+        s = D.dflash_open(p.model, max_ctx=512)
+        D.dflash_committed(s, f, 0)
+        o = O.OracleSession(p.oracle)
+        o.committed(f_np, 0)
+        sess.append(s)
+        oss.append(o)
+    tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+    lgs = [torch.empty((1, n, cfg.vocab), dtype=torch.float32, device="cuda") for _ in lens]
+    for rnd in range(2):
+        for b in range(len(lens)):
+            cur = torch.tensor([(5 * b + rnd) % cfg.vocab], dtype=torch.int32, device="cuda")
+            assert D.dflash_propose([sess[b]], cur, n, 0.0, 0, rnd, tok, q, lgs[b]) == [n]
+        torch.cuda.synchronize()
+        for b in range(len(lens)):
+            ref = oss[b].propose((5 * b + rnd) % cfg.vocab, n, 0.0, 0, rnd)
+            assert np.max(np.abs(lgs[b][0].double().cpu().numpy() - ref["logits"])) <= TOL_LOGITS["bf16"]
+            oss[b].commit_block()
+    D.dflash_device_status(p.model)
+    for s in sess:
+        D.dflash_close(s)
