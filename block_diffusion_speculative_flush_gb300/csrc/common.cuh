@@ -93,12 +93,20 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
 
 enum : uint32_t { kStreamDraft = 0, kStreamAccept = 1, kStreamBonus = 2 };
 
-// Word 0 of Philox at counter (v, row | stream << 16, seq, round), key = seed.
+// The random word for index v (a vocabulary entry, or 0 for a row's single
+// draw): word v & 3 of Philox at counter (v >> 2, row | stream << 16, seq,
+// round), key = seed.  One evaluation serves four consecutive indices.
+__device__ __forceinline__ uint4 rand_block(uint64_t seed, uint32_t rnd, uint32_t stream, uint32_t seq, uint32_t row,
+                                           uint32_t blk) {
+  const uint4 c = make_uint4(blk, (row & 0xFFFFu) | (stream << 16), seq, rnd);
+  const uint2 k = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+  return philox4x32_10(c, k);
+}
 __device__ __forceinline__ uint32_t rand_u32(uint64_t seed, uint32_t rnd, uint32_t stream,
                                              uint32_t seq, uint32_t row, uint32_t v) {
-  const uint4 c = make_uint4(v, (row & 0xFFFFu) | (stream << 16), seq, rnd);
-  const uint2 k = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
-  return philox4x32_10(c, k).x;
+  const uint4 r = rand_block(seed, rnd, stream, seq, row, v >> 2);
+  const uint32_t w = v & 3u;
+  return w == 0 ? r.x : w == 1 ? r.y : w == 2 ? r.z : r.w;
 }
 
 // u = ((x >> 9) + 0.5) * 2^-23: strictly inside (0, 1) and exact in fp32.
@@ -106,10 +114,14 @@ __device__ __forceinline__ float uniform_open(uint32_t x) {
   return ((float)(x >> 9) + 0.5f) * 1.1920928955078125e-07f;
 }
 
+__device__ __forceinline__ float gumbel_of(uint32_t x) { return -logf(-logf(uniform_open(x))); }
+
 __device__ __forceinline__ float gumbel(uint64_t seed, uint32_t rnd, uint32_t stream, uint32_t seq,
                                         uint32_t row, uint32_t v) {
-  const float u = uniform_open(rand_u32(seed, rnd, stream, seq, row, v));
-  return -logf(-logf(u));
+  return gumbel_of(rand_u32(seed, rnd, stream, seq, row, v));
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& r, int w) {
+  return w == 0 ? r.x : w == 1 ? r.y : w == 2 ? r.z : r.w;
 }
 
 // ---------------------------------------------------------------------------

@@ -458,17 +458,26 @@ __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ 
   const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
   float m = -INFINITY, l = 0.f;
   ArgMax best{-INFINITY, INT32_MAX};
-  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-    const float s = sample_logit(a, row, v) * invT;
-    if (s > m) {
-      l = l * expf(m - s) + 1.f;
-      m = s;
-    } else {
-      l += expf(s - m);
+  // four consecutive entries per thread: one Philox evaluation gives their
+  // four random words (chunks start on multiples of 4)
+  for (int v4 = v0 + 4 * threadIdx.x; v4 < v1; v4 += 4 * blockDim.x) {
+    uint4 r = make_uint4(0, 0, 0, 0);
+    if (a.gumbel) r = rand_block(a.seed, a.rnd, kStreamDraft, seq, prow, (uint32_t)v4 >> 2);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int v = v4 + w;
+      if (v >= v1) break;
+      const float s = sample_logit(a, row, v) * invT;
+      if (s > m) {
+        l = l * expf(m - s) + 1.f;
+        m = s;
+      } else {
+        l += expf(s - m);
+      }
+      float score = s;
+      if (a.gumbel) score += gumbel_of(word_of(r, w));
+      best = better(best, ArgMax{score, v});
     }
-    float score = s;
-    if (a.gumbel) score += gumbel(a.seed, a.rnd, kStreamDraft, seq, prow, (uint32_t)v);
-    best = better(best, ArgMax{score, v});
   }
   // warp merge
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -596,17 +605,23 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   float rsum = 0.f;
   ArgMax bres{-INFINITY, INT32_MAX}, bp{-INFINITY, INT32_MAX};
-  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-    const float lp = load_logit(a.target, a.in_bf16, tbase + (int64_t)trow * V + v) * invT - lse;
-    const float g = gumbel(a.seed, a.rnd, kStreamBonus, seq, prow, (uint32_t)v);
-    bp = better(bp, ArgMax{lp + g, v});
-    if (rej) {
-      const float p = expf(lp);
-      const float q = Tq > 0.f ? expf(dl[(int64_t)(rej - 1) * V + v] / Tq - dlse[rej - 1])
-                               : (v == dtok[rej - 1] ? 1.f : 0.f);
-      const float res = fmaxf(p - q, 0.f);
-      rsum += res;
-      if (res > 0.f) bres = better(bres, ArgMax{logf(res) + g, v});
+  for (int v4 = v0 + 4 * threadIdx.x; v4 < v1; v4 += 4 * blockDim.x) {
+    const uint4 rw = rand_block(a.seed, a.rnd, kStreamBonus, seq, prow, (uint32_t)v4 >> 2);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int v = v4 + w;
+      if (v >= v1) break;
+      const float lp = load_logit(a.target, a.in_bf16, tbase + (int64_t)trow * V + v) * invT - lse;
+      const float g = gumbel_of(word_of(rw, w));
+      bp = better(bp, ArgMax{lp + g, v});
+      if (rej) {
+        const float p = expf(lp);
+        const float q = Tq > 0.f ? expf(dl[(int64_t)(rej - 1) * V + v] / Tq - dlse[rej - 1])
+                                 : (v == dtok[rej - 1] ? 1.f : 0.f);
+        const float res = fmaxf(p - q, 0.f);
+        rsum += res;
+        if (res > 0.f) bres = better(bres, ArgMax{logf(res) + g, v});
+      }
     }
   }
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;

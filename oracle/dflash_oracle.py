@@ -119,13 +119,17 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def random_u32(seed: int, rnd: int, stream: int, seq: int, row: int, v):
-    """Word 0 of Philox4x32-10 at counter (v, row | stream<<16, seq, round),
-    key (low 32 bits of seed, high 32 bits of seed)."""
+    """The random word for index v: word v mod 4 of Philox4x32-10 at counter
+    (floor(v / 4), row | stream<<16, seq, round), key (low 32 bits of seed,
+    high 32 bits of seed).  Each Philox output block of four words thus
+    covers four consecutive indices."""
     seed = int(seed) & (2**64 - 1)
     u64 = lambda a: np.asarray(a, dtype=np.uint64)
+    v = u64(v)
     ctr1 = (u64(row) & np.uint64(0xFFFF)) | ((u64(stream) & np.uint64(0xFFFF)) << np.uint64(16))
-    x, _, _, _ = philox4x32_10(v, ctr1, u64(seq), u64(rnd), seed & 0xFFFFFFFF, seed >> 32)
-    return x
+    words = philox4x32_10(v >> np.uint64(2), ctr1, u64(seq), u64(rnd), seed & 0xFFFFFFFF, seed >> 32)
+    w = np.broadcast_to((v & np.uint64(3)).astype(np.int64), np.broadcast(*words).shape)
+    return np.choose(w, words)
 
 
 def uniform_open(x_u32) -> np.ndarray:
