@@ -296,11 +296,22 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
   const int S = item_count[b];
   const float* base = part + ((int64_t)(item_first[b] + kvh * S) * R + rr) * PD;
   const int64_t sstride = (int64_t)R * PD;
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, base[s * sstride]);
-  M = warp_max(M);
+  // (m, l) of up to 32 splits in one pass, one split per lane
+  float M = -INFINITY, mv = -INFINITY, lv = 0.f;
+  if (lane < S) {
+    const float2 ml = *reinterpret_cast<const float2*>(base + lane * sstride);
+    mv = ml.x;
+    lv = ml.y;
+  }
+  for (int s = lane + 32; s < S; s += 32) M = fmaxf(M, base[s * sstride]);
+  M = warp_max(fmaxf(M, mv));
   float L = 0.f;
-  for (int s = lane; s < S; s += 32) {
+  if (lane < S) {
+    const float w = mv == -INFINITY ? 0.f : expf(mv - M);
+    L = lv * w;
+    wsm[wl][lane] = w;
+  }
+  for (int s = lane + 32; s < S; s += 32) {
     const float m = base[s * sstride];
     const float w = m == -INFINITY ? 0.f : expf(m - M);
     L += base[s * sstride + 1] * w;
@@ -313,15 +324,15 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
   T* out = O + ((int64_t)bi * p.Hq + hq) * d;
   for (int t4 = lane * 4; t4 < d; t4 += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // eight splits' loads in flight at a time; the sum keeps split order
-    for (int s0 = 0; s0 < S; s0 += 8) {
-      float4 v[8];
+    // sixteen splits' loads in flight at a time; the sum keeps split order
+    for (int s0 = 0; s0 < S; s0 += 16) {
+      float4 v[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < 16; ++k)
         v[k] = s0 + k < S ? __ldg(reinterpret_cast<const float4*>(base + (s0 + k) * sstride + 4 + t4))
                           : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 16; ++k) {
         const int s = s0 + k;
         if (s >= S) break;
         float w;
