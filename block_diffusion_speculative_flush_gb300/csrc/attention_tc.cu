@@ -22,6 +22,7 @@
 //                 memory as the next MMA's A operand; finally O and
 //                 (max, sum) go out as this key range's partial.
 // Every wait is bounded; an expired wait sets bit 8 of the error word.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -34,6 +35,7 @@ namespace dfl {
 namespace {
 
 using namespace tc;
+namespace cg = cooperative_groups;
 
 constexpr int D = 128;                       // head dim
 constexpr int KT = 64;                       // keys per tile (MMA N of S)
@@ -324,7 +326,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     float* xl = xch + 2 * 256;
     xl[half * 128 + r] = l;
     asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
-    float* pr = part + ((int64_t)blockIdx.x * R + (rv ? r : 0)) * (D + 4);
+    // the partial goes to global memory, or (clustered) to this CTA's idle K/V stages
+    float* pr = p.cluster > 1 ? reinterpret_cast<float*>(sK) + (rv ? r : 0) * (D + 4)
+                              : part + ((int64_t)blockIdx.x * R + (rv ? r : 0)) * (D + 4);
     if (rv && half == 0) {
       *reinterpret_cast<float4*>(pr) = make_float4(m_used == -INFINITY ? -INFINITY : m_used * 0.6931471805599453f,
                                                    xl[r] + xl[128 + r], 0.f, 0.f);
@@ -340,6 +344,47 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       }
     }
   }
+  if (p.cluster > 1) {
+    // ---- merge of the cluster's key ranges, in range order: rank q owns rows
+    // [q R / S, (q+1) R / S); 32 threads per row, 4 output columns each
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();  // every range's partial is staged
+    const int S = p.cluster, q = (int)cl.block_rank();
+    const int r0 = q * R / S, r1 = (q + 1) * R / S;
+    const int ln = lane;
+    float* mine = reinterpret_cast<float*>(sK);
+    for (int rr = r0 + warp; rr < r1; rr += THREADS / 32) {
+      float mi = -INFINITY, li = 0.f;
+      if (ln < S) {
+        const float* pp = cl.map_shared_rank(mine, ln) + rr * (D + 4);
+        mi = pp[0];
+        li = pp[1];
+      }
+      const float M = warp_max(mi);
+      const float wi = (ln < S && mi != -INFINITY) ? expf(mi - M) : 0.f;
+      const float L = warp_sum(li * wi);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sidx = 0; sidx < S; ++sidx) {
+        const float ws = __shfl_sync(0xffffffffu, wi, sidx);
+        if (ws == 0.f) continue;  // a range with no visible key holds no O
+        const float4 v = *reinterpret_cast<const float4*>(cl.map_shared_rank(mine, sidx) + rr * (D + 4) + 4 + 4 * ln);
+        acc.x += ws * v.x;
+        acc.y += ws * v.y;
+        acc.z += ws * v.z;
+        acc.w += ws * v.w;
+      }
+      const int i = rr / G, g = rr % G, hq = it.kvh * G + g;
+      const int64_t orow = (int64_t)it.sess * p.nrows + i;
+      const float sc = (p.gates ? p.gates[orow * p.Hq + hq] : 1.f) / L;
+      const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * sc, acc.y * sc);
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc.z * sc, acc.w * sc);
+      uint2 raw;
+      raw.x = *reinterpret_cast<const uint32_t*>(&a);
+      raw.y = *reinterpret_cast<const uint32_t*>(&b2);
+      *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.out) + (orow * p.Hq + hq) * D + 4 * ln) = raw;
+    }
+    cl.sync();  // no CTA leaves while a peer still reads its partial
+  }
   fence_before();
   __syncthreads();
   if (warp == 9) {
@@ -350,15 +395,27 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
 
 }  // namespace
 
-bool launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
-                         int* err, cudaStream_t st) {
+int launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
+                        int* err, cudaStream_t st) {
   const int R = p.nrows * (p.Hq / p.Hkv);
-  if (p.d != D || R > 128 || !tabs.kvmaps) return false;
-  if (n_items <= 0) return true;
+  if (p.d != D || R > 128 || !tabs.kvmaps) return 0;
+  if (n_items <= 0) return 1;
   const size_t smem = (size_t)DATA_BYTES + 1024 + 256 + 3 * 1024;
-  cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attrs = false;
+  if (!attrs) {
+    cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    attrs = true;
+  }
+  if (p.cluster > 1 && p.cluster <= kAttnMaxCluster && n_items % p.cluster == 0 && p.out) {
+    if (launch_kc(k_attn_tc, n_items, THREADS, smem, st, p.cluster, (const bf16*)Q, items, tabs, p, part, err) ==
+        cudaSuccess)
+      return 2;
+    cudaGetLastError();  // the cluster did not fit: the same ranges, merged by k_attn_combine
+  }
+  p.cluster = 1;
   launch_k(k_attn_tc, n_items, THREADS, smem, st, (const bf16*)Q, items, tabs, p, part, err);
-  return true;
+  return 1;
 }
 
 }  // namespace dfl

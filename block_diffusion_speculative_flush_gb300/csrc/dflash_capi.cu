@@ -384,6 +384,9 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   // attention work items: split every (session, KV head) key range in chunks
   std::vector<AttnItem> items;
   std::vector<int32_t> ifirst(Bc), icount(Bc);
+  // in-kernel merge of the key ranges: one session on the tensor-core path
+  const bool attn_cluster_ok = block && Bc == 1 && m->dt == DT::BF16 && d == 128 && nrows * (Hq / Hkv) <= 128;
+  int attn_cluster = 1;
   if (block) {
     int64_t total = 0;
     std::vector<int64_t> k0v(Bc), k1v(Bc);
@@ -399,6 +402,15 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     // partials (R x (d + 4) floats per item) small next to the K/V bytes
     int64_t chunk = align_up(std::max<int64_t>(1, total / std::max(1, m->num_sms)), 64);
     chunk = std::min<int64_t>(std::max<int64_t>(chunk, 128), 8192);
+    const int64_t tiles0 = (k1v[0] - k0v[0] + 63) / 64;
+    if (attn_cluster_ok && tiles0 > 1 && tiles0 <= kAttnMaxCluster) {
+      // one session with a short key range per KV head (a window): one
+      // 64-key tile per CTA, the head's tiles one cluster merged in-kernel.
+      // Longer ranges keep partials + k_attn_combine: on GB300 clusters of
+      // CTAs that stream several tiles each did not beat it.
+      chunk = 64;
+      attn_cluster = (int)tiles0;
+    }
     for (int j = 0; j < Bc; ++j) {
       const int S = (int)((k1v[j] - k0v[j] + chunk - 1) / chunk);
       ifirst[j] = (int32_t)items.size();
@@ -495,12 +507,18 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     {
       Timed tm(m, kAttention, attn_bytes, attn_flops, st);
       const AttnItem* ditems = (const AttnItem*)(tb + o_items);
-      if (m->dt != DT::BF16 ||
-          !launch_attention_tc(m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), m->d_err, st))
+      ap.cluster = attn_cluster;
+      ap.out = m->O.p;
+      ap.gates = c.gated_attention ? m->G.as<float>() : nullptr;
+      int how = 0;
+      if (m->dt == DT::BF16)
+        how = launch_attention_tc(m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), m->d_err, st);
+      if (how == 0)
         launch_attention_simt(m->dt, m->Q.p, ditems, (int)items.size(), tabs, ap, m->apart.as<float>(), st);
-      launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
-                               (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
-                               m->O.p, st);
+      if (how != 2)
+        launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
+                                 (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
+                                 m->O.p, st);
       m->launches += 2;
     }
     ST_TRY(launch_check("attention"));

@@ -44,6 +44,14 @@ struct AttnParams {
   int window, causal;
   int L, layer;
   float scale;
+  // Split-key merge inside the attention kernel (tensor-core path): the
+  // `cluster` key ranges of one (session, KV head) form a thread-block
+  // cluster and merge their partials through distributed shared memory into
+  // out (bf16 [rows][Hq][d], times gates [rows][Hq] when given).  1: partials
+  // go to global memory for k_attn_combine.
+  int cluster;
+  void* out;
+  const float* gates;
 };
 
 // --- portable kernels (any storage type) ----------------------------------
@@ -67,8 +75,12 @@ void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_it
 // bf16 block attention on tcgen05 tensor cores (key ranges must start on a
 // multiple of 64); false if the shape is not supported (head_dim other than
 // 128, more than 128 query rows per KV head, no tensor maps).
-bool launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
-                         int* err, cudaStream_t st);
+// Largest cluster of key ranges merged in-kernel (non-portable size).
+constexpr int kAttnMaxCluster = 16;
+// Returns 0 if the shapes need the CUDA-core path, 1 if partials were written
+// for k_attn_combine, 2 if the output was merged in-kernel (p.cluster > 1).
+int launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
+                        int* err, cudaStream_t st);
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count,
                               int B, AttnParams p, const float* G, void* O, cudaStream_t st);
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld_delta, int rows, int H, cudaStream_t st);
