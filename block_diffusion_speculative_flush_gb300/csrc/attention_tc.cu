@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       raw.y = *reinterpret_cast<const uint32_t*>(&b2);
       *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.out) + (orow * p.Hq + hq) * D + 4 * ln) = raw;
     }
-    cl.sync();  // no CTA leaves while a peer still reads its partial
+    cluster_sync_relaxed();  // no CTA leaves while a peer still reads its partial
   }
   fence_before();
   __syncthreads();

@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
             }
           return acc;
         });
-      cl.sync();  // no CTA leaves while a peer still reads its partial
+      cluster_sync_relaxed();  // no CTA leaves while a peer still reads its partial
     }
   }
   fence_before();

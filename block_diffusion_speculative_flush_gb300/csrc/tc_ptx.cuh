@@ -155,5 +155,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Cluster barrier without release semantics.  Enough where it only has to
+// keep a CTA's shared memory alive until its peers' DSMEM loads (whose values
+// they have consumed) are done: unlike the default release arrive, it does
+// not wait for this thread's global stores to become visible.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+  asm volatile("barrier.cluster.wait;" ::: "memory");
+}
+
 }  // namespace tc
 }  // namespace dfl
