@@ -432,6 +432,20 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
                o_front = tp.add(front), o_seq = tp.add(seqv), o_items = tp.add(items), o_ifirst = tp.add(ifirst),
                o_icount = tp.add(icount), o_map = tp.add(fw.sess_map), o_maps = tp.add(mapv);
+  // RoPE cos/sin per row: formed here in double (angle pos * theta^(-2j/d))
+  // when the rows fit the parameter table, else by k_rope_table on the device
+  const size_t rope_bytes = (size_t)M * (d / 2) * sizeof(float2);
+  const bool host_rope = tp.host.size() + rope_bytes + 64 <= (size_t)kTableParamMax;
+  size_t o_rope = 0;
+  if (host_rope) {
+    std::vector<float2> rt((size_t)M * (d / 2));
+    for (int r = 0; r < M; ++r)
+      for (int j = 0; j < d / 2; ++j) {
+        const double ang = (double)meta[r].pos * std::pow((double)c.rope_theta, -2.0 * j / (double)d);
+        rt[(size_t)r * (d / 2) + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    o_rope = tp.add(rt);
+  }
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
   SessTables tabs{(void* const*)(tb + o_kv), (const int64_t*)(tb + o_cap), (const int64_t*)(tb + o_front),
@@ -473,8 +487,11 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
                  m->d_err, st);
     m->launches++;
   }
-  launch_rope_table(dmeta, M, d, c.rope_theta, m->rope.as<float2>(), st);
-  m->launches++;
+  const float2* rope = host_rope ? (const float2*)(tb + o_rope) : m->rope.as<float2>();
+  if (!host_rope) {
+    launch_rope_table(dmeta, M, d, c.rope_theta, m->rope.as<float2>(), st);
+    m->launches++;
+  }
   ST_TRY(launch_check("context path"));
 
   AttnParams ap{Hq, Hkv, d, nrows, c.window, c.causal_block, c.n_layers, 0, 1.f / std::sqrt((float)d)};
@@ -498,7 +515,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       const char* wkv = (const char*)w.w_qkv + (size_t)qd * H * es;
       ST_TRY(gemm(m, m->x.p, H, wkv, H, m->qkv.as<float>() + qd, m->qkv_cols, M, 2 * kd, H, st));
     }
-    launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, m->rope.as<float2>(), w.q_norm, w.k_norm, Hq,
+    launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, rope, w.q_norm, w.k_norm, Hq,
                     Hkv, d, c.gated_attention, c.rms_eps, tabs, c.n_layers, l, m->Q.p, m->G.as<float>(), st);
     m->launches++;
     ST_TRY(launch_check("qkv"));
