@@ -58,10 +58,11 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["round", "flush", "laguna", "batched"], default="round",
+    ap.add_argument("--workload", choices=["round", "flush", "laguna", "batched", "spec"], default="round",
                     help="round: the bs1 Qwen3-8B-shaped round (the default line); flush: 8 sequences x 256-row "
                          "context flushes; laguna: window-512 gated draft, bs1, blocks 16 and 8; batched: 64 "
-                         "sequences, contexts 1k-16k, propose + rejection-sampling verify at T=0.7")
+                         "sequences, contexts 1k-16k, propose + rejection-sampling verify at T=0.7; spec: greedy "
+                         "speculative decoding with the tiny fp32 draft and the synthetic target, both on the GPU")
     return ap.parse_args(argv)
 
 
@@ -205,7 +206,7 @@ def gpu_weights(cfg, seed, device):
         x = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 0.02
         if name.endswith("norm") or name == "aux_norms":
             x += 1.0
-        out[name] = x.to(torch.bfloat16)
+        out[name] = x.to(torch.bfloat16 if cfg.dtype == "bf16" else torch.float32)
     return out
 
 
@@ -526,6 +527,9 @@ def run_workload(args, rank, world, local_rank):
                       "block8_round_roofline_frac": round(res[8][3] / (res[8][1] / K * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                                           4)}, clk16)
 
+    if args.workload == "spec":
+        return _spec_decode(args, world, local_rank, dev, stream, K, W)
+
     # batched serving mix
     cfg = S.CONFIGS[CFG_NAME]
     B, n, Tb = 64, cfg.block_size - 1, 0.7
@@ -579,6 +583,101 @@ def run_workload(args, rank, world, local_rank):
                                "ideal_ms_per_step": round(ideal * 1e3, 3), "frac": round(ideal / t_step, 4),
                                "gemm_tflop_per_step": round(gemm_flops / 1e12, 3),
                                "kv_gb_per_step": round(kv_bytes / 1e9, 2)}}, clk)
+
+
+def _spec_decode(args, world, local_rank, dev, stream, K, W):
+    """Whole greedy speculative rounds on the GPU: the tiny fp32 draft proposes
+    7 tokens, the synthetic 2-layer target runs its 8-row verify forward (logits
+    and the 5 hidden taps), verify takes the accepted prefix and the bonus
+    token, the target cache is trimmed to the accepted rows and their taps are
+    committed to the draft.  The accept length is read on the host every round
+    (trim and commit take host integers), so a step ends in one device sync."""
+    import numpy as np
+    import torch
+
+    import block_diffusion_speculative_flush_gb300 as D
+    import synthetic as S
+    from synthetic.target import SyntheticTarget
+
+    cfg = S.CONFIGS["tiny_fp32"]
+    n = cfg.block_size - 1
+    ht = SyntheticTarget(seed=1)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    tcfg = dict(hidden=ht.H, n_heads=ht.nh, head_dim=ht.d, intermediate=ht.I, vocab=ht.V, n_layers=ht.L,
+                rope_theta=ht.theta, rms_eps=ht.eps)
+    tw = dict(embed=f32(ht.E), unembed=f32(ht.U), final_norm=f32(ht.nf),
+              layers=[{k: f32(v) for k, v in lw.items()} for lw in ht.layers])
+    model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED, dev))
+    max_ctx = 16 + (n + 1) * (W + K + 2)
+    V, NT = ht.V, ht.n_taps * ht.H
+    prompt = [int(x) for x in S.rng_for(0, "prompt").integers(0, V, size=8)]
+    with torch.cuda.stream(stream):
+        tgt = D.dflash_target_create(tcfg, tw, max_ctx=max_ctx, stream=stream)
+        sess = D.dflash_open(model, max_ctx=max_ctx, stream=stream)
+        lg_p = torch.empty((len(prompt), V), dtype=torch.float32, device=dev)
+        tp_p = torch.empty((len(prompt), NT), dtype=torch.float32, device=dev)
+        D.dflash_target_forward(tgt, torch.tensor(prompt, dtype=torch.int32, device=dev), 0, lg_p, tp_p)
+        cur = torch.empty(1, dtype=torch.int32, device=dev)
+        D.dflash_target_argmax(tgt, lg_p[-1:], cur)
+        D.dflash_committed(sess, tp_p, 0)
+        blk = torch.empty(n + 1, dtype=torch.int32, device=dev)
+        lg = torch.empty((n + 1, V), dtype=torch.float32, device=dev)
+        tp = torch.empty((n + 1, NT), dtype=torch.float32, device=dev)
+        tok = blk[1:].view(1, n)
+        q = torch.empty((1, n), dtype=torch.float32, device=dev)
+        acc = torch.empty(1, dtype=torch.int32, device=dev)
+        bon = torch.empty(1, dtype=torch.int32, device=dev)
+        host = torch.empty(2, dtype=torch.int32, pin_memory=True)
+    st = {"pos": len(prompt), "tokens": 0, "accepted": 0}
+
+    def step(i):
+        if i == W:          # first timed step: count tokens from here
+            st["mark_tokens"], st["mark_accepted"] = st["tokens"], st["accepted"]
+        blk[:1].copy_(cur)
+        D.dflash_propose([sess], cur, n, 0.0, 0, i, tok, q)
+        D.dflash_target_forward(tgt, blk, st["pos"], lg, tp)
+        D.dflash_verify([sess], lg[None], tok, n, 0.0, 0, i, acc, bon)
+        host[:1].copy_(acc, non_blocking=True)
+        stream.synchronize()
+        a = int(host[0])
+        D.dflash_target_trim(tgt, st["pos"] + a + 1)
+        D.dflash_committed(sess, tp[:a + 1], st["pos"])
+        cur.copy_(bon)
+        st["pos"] += a + 1
+        st["tokens"] += a + 1
+        st["accepted"] += a
+
+    ms, clk = _timed(torch, stream, step, K, W, local_rank, world, dev)
+    timed_tokens = st["tokens"] - st["mark_tokens"]
+    timed_accepted = st["accepted"] - st["mark_accepted"]
+    # the target's verify forward alone (8 rows at the cached frontier, trimmed back each time)
+    fw = torch.cuda.Event(enable_timing=True)
+    fe = torch.cuda.Event(enable_timing=True)
+    base = st["pos"]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            D.dflash_target_forward(tgt, blk, base, lg, tp)
+            D.dflash_target_trim(tgt, base)
+        fw.record(stream)
+        for _ in range(50):
+            D.dflash_target_forward(tgt, blk, base, lg, tp)
+            D.dflash_target_trim(tgt, base)
+        fe.record(stream)
+    torch.cuda.synchronize()
+    fwd_us = fw.elapsed_time(fe) / 50 * 1e3
+    D.dflash_target_device_status(tgt)
+    D.dflash_device_status(model)
+    D.dflash_close(sess)
+    launches_fwd = 2 + 14 * ht.L + 2 + 1
+    return _line("generated tok/s (greedy speculative decoding, tiny fp32 draft + synthetic target, on GPU)",
+                 "generated tok/s", world * timed_tokens / (ms * 1e-3), world, K, W, ms, "f32",
+                 {"workload": "tiny_fp32 draft (2 layers, H 256, block 8, n=7) + a 2-layer H-256 fp32 target, "
+                              "8-token prompt, greedy rounds: propose, 8-row target verify forward with 5 taps, "
+                              "verify, trim, commit", "l2": "all weights (6 MB) L2-resident: latency-bound"},
+                 {"rounds_s": round(world * K / (ms * 1e-3), 2),
+                  "mean_accepted": round(timed_accepted / K, 3),
+                  "target_forward_us": round(fwd_us, 2), "target_forward_launches": launches_fwd,
+                  "total_tokens": timed_tokens}, clk)
 
 
 # ---------------------------------------------------------------------------

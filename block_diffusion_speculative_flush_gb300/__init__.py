@@ -26,6 +26,8 @@ __all__ = [
     "dflash_committed", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
     "dflash_close", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
     "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read", "dflash_verify_noalloc",
+    "Target", "dflash_target_create", "dflash_target_destroy", "dflash_target_forward", "dflash_target_trim",
+    "dflash_target_length", "dflash_target_argmax", "dflash_target_device_status",
 ]
 
 
@@ -229,3 +231,100 @@ def dflash_timing_read(model: Model) -> dict:
     _check(lib.dflash_timing_read(model.handle, arr, 16, C.byref(n)))
     return {arr[i].name.decode(): dict(launches=arr[i].launches, total_ms=arr[i].total_ms, bytes=arr[i].bytes,
                                        flops=arr[i].flops) for i in range(n.value)}
+
+
+# ---------------------------------------------------------------------------
+# synthetic target (fp32)
+# ---------------------------------------------------------------------------
+class Target:
+    """Handle of a dflash_target; keeps the weight tensors alive."""
+
+    def __init__(self, handle: int, cfg: dict, tensors: list, layer_structs):
+        self.handle = handle
+        self.cfg = cfg
+        self._tensors = tensors
+        self._layers = layer_structs
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            lib.dflash_target_destroy(self.handle)
+            self.handle = None
+
+
+def dflash_target_create(cfg: dict, weights: dict, max_ctx: int = 4096, stream=None) -> Target:
+    """cfg: hidden, n_heads, head_dim, intermediate, vocab, n_layers, rope_theta, rms_eps;
+    weights: fp32 CUDA tensors embed, unembed, final_norm and layers = [dict n1, wq, wk,
+    wv, wo, n2, wg, wu, wd]."""
+    c = _abi.dflash_target_config(hidden=cfg["hidden"], n_heads=cfg["n_heads"], head_dim=cfg["head_dim"],
+                                  intermediate=cfg["intermediate"], vocab=cfg["vocab"], n_layers=cfg["n_layers"],
+                                  rope_theta=cfg["rope_theta"], rms_eps=cfg["rms_eps"])
+    keep = []
+    H, qd, I, V = cfg["hidden"], cfg["n_heads"] * cfg["head_dim"], cfg["intermediate"], cfg["vocab"]
+    shapes = dict(n1=(H,), wq=(qd, H), wk=(qd, H), wv=(qd, H), wo=(H, qd), n2=(H,), wg=(I, H), wu=(I, H),
+                  wd=(H, I))
+
+    def dev(t, shape, name):
+        t = t.contiguous()
+        if not t.is_cuda or t.dtype != torch.float32:
+            raise ValueError("target weights are fp32 CUDA tensors")
+        if tuple(t.shape) != shape:
+            raise ValueError(f"target weight {name}: shape {tuple(t.shape)}, expected {shape}")
+        keep.append(t)
+        return t.data_ptr()
+
+    if len(weights["layers"]) != cfg["n_layers"]:
+        raise ValueError("target weights: one dict per layer")
+    layers = (_abi.dflash_target_layer * cfg["n_layers"])()
+    for l, lw in enumerate(weights["layers"]):
+        for name, shape in shapes.items():
+            setattr(layers[l], name, dev(lw[name], shape, name))
+    w = _abi.dflash_target_weights(embed=dev(weights["embed"], (V, H), "embed"),
+                                   unembed=dev(weights["unembed"], (V, H), "unembed"),
+                                   final_norm=dev(weights["final_norm"], (H,), "final_norm"), layers=layers)
+    stream = stream if stream is not None else torch.cuda.current_stream()
+    out = C.c_void_p()
+    _check(lib.dflash_target_create(C.byref(c), C.byref(w), max_ctx, C.c_void_p(stream.cuda_stream), C.byref(out)))
+    return Target(out.value, dict(cfg), keep, layers)
+
+
+def dflash_target_destroy(target: Target) -> None:
+    if target.handle:
+        _check(lib.dflash_target_destroy(target.handle))
+        target.handle = None
+
+
+def dflash_target_forward(target: Target, tokens: torch.Tensor, start: int, logits: torch.Tensor,
+                          taps: torch.Tensor | None = None) -> None:
+    """tokens: int32 CUDA [rows]; logits: fp32 CUDA [rows][vocab]; taps: fp32 CUDA [rows][(2L+1)*hidden]."""
+    c = target.cfg
+    rows = tokens.numel()
+    if tokens.dtype != torch.int32 or not tokens.is_contiguous():
+        raise ValueError("tokens must be contiguous int32")
+    if logits.dtype != torch.float32 or not logits.is_contiguous() or tuple(logits.shape) != (rows, c["vocab"]):
+        raise ValueError("logits must be contiguous fp32 [rows, vocab]")
+    if taps is not None and (taps.dtype != torch.float32 or not taps.is_contiguous() or
+                             tuple(taps.shape) != (rows, (2 * c["n_layers"] + 1) * c["hidden"])):
+        raise ValueError("taps must be contiguous fp32 [rows, (2 * n_layers + 1) * hidden]")
+    _check(lib.dflash_target_forward(target.handle, _ptr(tokens), tokens.numel(), start, _ptr(logits), _ptr(taps)))
+
+
+def dflash_target_trim(target: Target, length: int) -> None:
+    _check(lib.dflash_target_trim(target.handle, length))
+
+
+def dflash_target_length(target: Target) -> int:
+    v = C.c_int64()
+    _check(lib.dflash_target_length(target.handle, C.byref(v)))
+    return v.value
+
+
+def dflash_target_argmax(target: Target, logits: torch.Tensor, out: torch.Tensor) -> None:
+    """logits: fp32 CUDA [rows][vocab]; out: int32 CUDA [rows], the greedy token of each row."""
+    if logits.dtype != torch.float32 or not logits.is_contiguous() or logits.dim() != 2 or \
+            logits.shape[1] != target.cfg["vocab"] or out.dtype != torch.int32 or out.numel() < logits.shape[0]:
+        raise ValueError("logits must be contiguous fp32 [rows, vocab] and out int32 [rows]")
+    _check(lib.dflash_target_argmax(target.handle, _ptr(logits), logits.shape[0], _ptr(out)))
+
+
+def dflash_target_device_status(target: Target) -> None:
+    _check(lib.dflash_target_device_status(target.handle))

@@ -54,6 +54,20 @@ class dflash_kernel_time(C.Structure):
                 ("bytes", C.c_double), ("flops", C.c_double)]
 
 
+class dflash_target_config(C.Structure):
+    _fields_ = [("hidden", C.c_int32), ("n_heads", C.c_int32), ("head_dim", C.c_int32), ("intermediate", C.c_int32),
+                ("vocab", C.c_int32), ("n_layers", C.c_int32), ("rope_theta", C.c_float), ("rms_eps", C.c_float)]
+
+
+class dflash_target_layer(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("n1", "wq", "wk", "wv", "wo", "n2", "wg", "wu", "wd")]
+
+
+class dflash_target_weights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("unembed", C.c_void_p), ("final_norm", C.c_void_p),
+                ("layers", C.POINTER(dflash_target_layer))]
+
+
 P = C.c_void_p
 SessArr = C.POINTER(C.c_void_p)
 
@@ -83,6 +97,14 @@ SIGNATURES = {
     "dflash_kv_import": (C.c_int, [P, C.c_int32, C.c_int64, C.c_int32, P, P]),
     "dflash_timing_enable": (C.c_int, [P, C.c_int32]),
     "dflash_timing_read": (C.c_int, [P, C.POINTER(dflash_kernel_time), C.c_int32, C.POINTER(C.c_int32)]),
+    "dflash_target_create": (C.c_int, [C.POINTER(dflash_target_config), C.POINTER(dflash_target_weights), C.c_int64,
+                                       P, C.POINTER(C.c_void_p)]),
+    "dflash_target_destroy": (C.c_int, [P]),
+    "dflash_target_forward": (C.c_int, [P, P, C.c_int32, C.c_int64, P, P]),
+    "dflash_target_trim": (C.c_int, [P, C.c_int64]),
+    "dflash_target_length": (C.c_int, [P, C.POINTER(C.c_int64)]),
+    "dflash_target_argmax": (C.c_int, [P, P, C.c_int32, P]),
+    "dflash_target_device_status": (C.c_int, [P]),
 }
 
 

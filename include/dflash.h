@@ -280,6 +280,61 @@ DFLASH_API int dflash_timing_enable(dflash_model* m, int32_t on);
  * (host) and their number to *n_entries (host). */
 DFLASH_API int dflash_timing_read(dflash_model* m, dflash_kernel_time* out, int32_t max_entries, int32_t* n_entries);
 
+/* ---------------------------------------------------------------------------
+ * Synthetic target (the model the draft speculates for).
+ *
+ * ollama mlxrunner/dflash.go and the mlxcel PR #1771 ("add the Laguna DFlash
+ * drafter": the verify forward with its 5-tap capture and rollback trim) run
+ * the draft against a real target.  No target checkpoint exists here: a small
+ * fp32 dense decoder stands in (RMSNorm, rotate-half RoPE, causal multi-head
+ * attention over its own cache, SwiGLU MLP).  Per position it gives what
+ * dflash_committed consumes, the taps (the embedding output and the residual
+ * stream after each attention and each MLP, [rows][(2 * n_layers + 1) *
+ * hidden]), and what dflash_verify consumes, raw next-token logits
+ * [rows][vocab].  Every row is computed against the cache and the earlier
+ * rows of the call, so a multi-row verify forward equals token-by-token
+ * decoding.
+ * ------------------------------------------------------------------------- */
+typedef struct dflash_target dflash_target;
+
+typedef struct dflash_target_config {
+  int32_t hidden, n_heads, head_dim, intermediate, vocab, n_layers;
+  float rope_theta, rms_eps;
+} dflash_target_config;
+
+/* fp32 device matrices, row-major [out][in]; borrowed (must outlive the target) */
+typedef struct dflash_target_layer {
+  const void *n1, *wq, *wk, *wv, *wo, *n2, *wg, *wu, *wd;
+} dflash_target_layer;
+
+typedef struct dflash_target_weights {
+  const void* embed;         /* [vocab][hidden] */
+  const void* unembed;       /* [vocab][hidden] */
+  const void* final_norm;    /* [hidden] */
+  const dflash_target_layer* layers;  /* host array of n_layers */
+} dflash_target_weights;
+
+/* Validates the shapes (hidden and n_heads * head_dim at most 4096, head_dim a
+ * multiple of 4 and at most 128, else DFLASH_ERR_SHAPE), allocates
+ * a cache of max_ctx positions; every call enqueues on `stream`. */
+DFLASH_API int dflash_target_create(const dflash_target_config* cfg, const dflash_target_weights* w, int64_t max_ctx,
+                                    void* stream, dflash_target** out);
+DFLASH_API int dflash_target_destroy(dflash_target* t);
+/* Forward of `rows` tokens (device int32) at positions start.. , which must
+ * equal the cached length (else DFLASH_ERR_CONTEXT_GAP); writes logits (device
+ * fp32 [rows][vocab]) and, when taps is not NULL, the taps (device fp32).  The
+ * rows join the cache. */
+DFLASH_API int dflash_target_forward(dflash_target* t, const int32_t* tokens, int32_t rows, int64_t start,
+                                     float* logits, float* taps);
+/* Rolls the cache back to `length` rows (a rejected verify tail). */
+DFLASH_API int dflash_target_trim(dflash_target* t, int64_t length);
+DFLASH_API int dflash_target_length(const dflash_target* t, int64_t* length);
+/* Greedy token of each logits row (device int32 [rows]), lowest id on a tie. */
+DFLASH_API int dflash_target_argmax(dflash_target* t, const float* logits, int32_t rows, int32_t* out);
+/* Synchronises the target's stream and reports a device-side error (a token
+ * id outside [0, vocab)) as DFLASH_ERR_DEVICE. */
+DFLASH_API int dflash_target_device_status(dflash_target* t);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,139 @@
+"""The synthetic target on the GPU (dflash_target_*): its logits and hidden
+taps against the CPU target, the rollback trim, and a whole greedy
+speculative decode (draft and target both on the GPU) against plain greedy
+decoding of the CPU target."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+from synthetic.target import SyntheticTarget
+from tests.gpu_util import Pair, lib
+
+pytestmark = pytest.mark.gpu
+
+
+def upload_target(D, tgt: SyntheticTarget, max_ctx: int = 512):
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    cfg = dict(hidden=tgt.H, n_heads=tgt.nh, head_dim=tgt.d, intermediate=tgt.I, vocab=tgt.V, n_layers=tgt.L,
+               rope_theta=tgt.theta, rms_eps=tgt.eps)
+    w = dict(embed=f32(tgt.E), unembed=f32(tgt.U), final_norm=f32(tgt.nf),
+             layers=[{k: f32(v) for k, v in lw.items()} for lw in tgt.layers])
+    return D.dflash_target_create(cfg, w, max_ctx=max_ctx)
+
+
+def _fwd(D, t, tokens, start, V, NT):
+    tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+    lg = torch.empty((len(tokens), V), dtype=torch.float32, device="cuda")
+    tp = torch.empty((len(tokens), NT), dtype=torch.float32, device="cuda")
+    D.dflash_target_forward(t, tok, start, lg, tp)
+    torch.cuda.synchronize()
+    return lg.cpu().numpy(), tp.cpu().numpy()
+
+
+def _close(g, r, tol):
+    assert np.all(np.abs(g - r) <= tol * np.maximum(1.0, np.abs(r))), float(np.max(np.abs(g - r)))
+
+
+def test_target_forward_and_trim_match_the_cpu_target():
+    """Prompt rows, a 5-row verify chunk, a trim to 10 rows and 3 more rows:
+    logits and taps equal the CPU target's (fp32 against float64 arithmetic)."""
+    D = lib()
+    ref = SyntheticTarget(seed=1)
+    t = upload_target(D, ref)
+    V, NT = ref.V, ref.n_taps * ref.H
+    prompt = list(S.rng_for(0, "prompt").integers(0, V, size=8))
+    for tokens, start, trim in ((prompt, 0, None), ([3, 7, 1, 30, 12], 8, 10), ([5, 9, 2], 10, None)):
+        lg, tp = _fwd(D, t, tokens, start, V, NT)
+        rl, rt = ref.forward(tokens, start)
+        _close(lg, rl, 1e-3)
+        _close(tp, rt, 1e-4)
+        if trim is not None:
+            D.dflash_target_trim(t, trim)
+            ref.trim(trim)
+        assert D.dflash_target_length(t) == ref.length
+    D.dflash_target_device_status(t)
+
+
+def test_target_refuses_a_gap_and_a_bad_trim():
+    D = lib()
+    ref = SyntheticTarget(seed=1)
+    t = upload_target(D, ref)
+    _fwd(D, t, [1, 2, 3], 0, ref.V, ref.n_taps * ref.H)
+    with pytest.raises(D.DFlashError) as e:
+        _fwd(D, t, [4], 5, ref.V, ref.n_taps * ref.H)
+    assert e.value.status == D.DFLASH_ERR_CONTEXT_GAP
+    with pytest.raises(D.DFlashError):
+        D.dflash_target_trim(t, 4)
+    assert D.dflash_target_length(t) == 3
+
+
+def test_gpu_speculative_decode_equals_greedy_decode():
+    """Draft and target both on the GPU: 128 tokens of greedy speculative
+    decoding (propose, a multi-row target forward, verify, trim, commit the
+    accepted taps) equal plain greedy decoding of the CPU target."""
+    D = lib()
+    p = Pair(S.CONFIGS["tiny_fp32"])
+    cfg = p.cfg
+    n = cfg.block_size - 1
+    cpu = SyntheticTarget(seed=1)
+    prompt = list(S.rng_for(0, "prompt").integers(0, 32, size=8))
+    ref = cpu.greedy_decode(prompt, 200)
+    t = upload_target(D, cpu)
+    V, NT = cpu.V, cpu.n_taps * cpu.H
+    lg = torch.empty((n + 1, V), dtype=torch.float32, device="cuda")
+    tp = torch.empty((n + 1, NT), dtype=torch.float32, device="cuda")
+    first = torch.empty(1, dtype=torch.int32, device="cuda")
+    lg_p = torch.empty((len(prompt), V), dtype=torch.float32, device="cuda")
+    tp_p = torch.empty((len(prompt), NT), dtype=torch.float32, device="cuda")
+    D.dflash_target_forward(t, torch.tensor(prompt, dtype=torch.int32, device="cuda"), 0, lg_p, tp_p)
+    D.dflash_target_argmax(t, lg_p[-1:], first)
+    s = D.dflash_open(p.model, max_ctx=512)
+    D.dflash_committed(s, tp_p, 0)
+    out = [int(first.item())]
+    pos = len(prompt)
+    tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    bon = torch.empty(1, dtype=torch.int32, device="cuda")
+    cur = torch.empty(1, dtype=torch.int32, device="cuda")
+    rnd, accepted = 0, 0
+    while len(out) < 128:
+        cur.fill_(out[-1])
+        assert D.dflash_propose([s], cur, n, 0.0, 0, rnd, tok, q) == [n]
+        D.dflash_target_forward(t, torch.cat([cur, tok[0]]), pos, lg, tp)
+        D.dflash_verify([s], lg[None], tok, n, 0.0, 0, rnd, acc, bon)
+        a, b = int(acc.item()), int(bon.item())
+        D.dflash_target_trim(t, pos + a + 1)
+        D.dflash_committed(s, tp[:a + 1], pos)
+        out += tok[0, :a].cpu().tolist() + [b]
+        pos += a + 1
+        accepted += a
+        rnd += 1
+    assert out[:128] == ref[:128]
+    assert D.dflash_target_length(t) == pos
+    st = D.dflash_stats(s)
+    assert st["rounds"] == rnd and st["accepted"] == accepted
+    D.dflash_target_device_status(t)
+    D.dflash_device_status(p.model)
+    D.dflash_close(s)
+
+
+def test_target_block_forward_equals_chain_forward_bitwise():
+    """Every row of the target is computed on its own (GEMMs with a fixed k
+    order, attention splits fixed by absolute position): an 8-row verify
+    forward and 8 one-row forwards give bit-identical logits and taps, so
+    greedy speculative output cannot diverge from greedy decoding."""
+    D = lib()
+    ref = SyntheticTarget(seed=1)
+    V, NT = ref.V, ref.n_taps * ref.H
+    prompt = [int(x) for x in S.rng_for(0, "prompt").integers(0, V, size=250)]
+    block = [4, 17, 9, 9, 30, 1, 0, 22]   # rows 250..257 cross the 256-key split boundary
+    ta = upload_target(D, ref)
+    tb = upload_target(D, ref)
+    _fwd(D, ta, prompt, 0, V, NT)
+    _fwd(D, tb, prompt, 0, V, NT)
+    lg_b, tp_b = _fwd(D, ta, block, len(prompt), V, NT)
+    rows = [_fwd(D, tb, [x], len(prompt) + i, V, NT) for i, x in enumerate(block)]
+    assert np.array_equal(lg_b, np.concatenate([r[0] for r in rows]))
+    assert np.array_equal(tp_b, np.concatenate([r[1] for r in rows]))
