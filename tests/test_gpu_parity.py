@@ -8,7 +8,8 @@ import torch
 
 import synthetic as S
 from oracle import dflash_oracle as O
-from synthetic.target import SyntheticTarget
+from oracle.target_oracle import OracleTarget
+from synthetic.target import TARGET_TINY, make_target_weights
 from tests.gpu_util import MARGIN, TOL_LOGITS, TOL_Q, Pair, assert_cache_close, check_tokens, export_kv, lib
 
 pytestmark = pytest.mark.gpu
@@ -313,7 +314,7 @@ def test_greedy_speculative_output_equals_greedy_decode(D):
     p = Pair(S.CONFIGS["tiny_fp32"])
     cfg = p.cfg
     n = cfg.block_size - 1
-    tgt = SyntheticTarget(seed=1)
+    tgt = OracleTarget(make_target_weights(1), TARGET_TINY)
     prompt = list(S.rng_for(0, "prompt").integers(0, 32, size=8))
     ref = tgt.greedy_decode(prompt, 200)
     plan = [0, 1, 2, n]

@@ -5,7 +5,8 @@ import pytest
 
 import synthetic as S
 from oracle import dflash_oracle as O
-from synthetic.target import SyntheticTarget
+from oracle.target_oracle import OracleTarget
+from synthetic.target import TARGET_TINY, make_target_weights
 
 TINY = S.CONFIGS["tiny_fp32"]
 
@@ -286,7 +287,7 @@ def _speculative_run(draft, target, prompt, n_new, forced=None, check=None):
 def test_greedy_speculative_equals_greedy_decode(tiny):
     """Speculative output with the real draft equals plain greedy decoding of
     the target, token for token, over 128 tokens."""
-    tgt = SyntheticTarget(seed=1)
+    tgt = OracleTarget(make_target_weights(1), TARGET_TINY)
     prompt = list(S.rng_for(0, "prompt").integers(0, 32, size=8))
     ref = tgt.greedy_decode(prompt, 128)
     out, sess = _speculative_run(tiny, tgt, prompt, 128)
@@ -298,7 +299,7 @@ def test_forced_accept_lengths_keep_greedy_output(tiny):
     """Laguna PR greedy_invariant_with_forced_rejections: a drafter that forces
     accept lengths 0, 1, 2 and full; each round must accept exactly the forced
     length with the bonus sitting at the reference index."""
-    tgt = SyntheticTarget(seed=1)
+    tgt = OracleTarget(make_target_weights(1), TARGET_TINY)
     prompt = list(S.rng_for(0, "prompt").integers(0, 32, size=8))
     ref = tgt.greedy_decode(prompt, 200)
     plan = [0, 1, 2, 7]
