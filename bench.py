@@ -597,22 +597,21 @@ def _spec_decode(args, world, local_rank, dev, stream, K, W):
 
     import block_diffusion_speculative_flush_gb300 as D
     import synthetic as S
-    from synthetic.target import SyntheticTarget
+    from synthetic.target import TARGET_TINY, make_target_weights
 
     cfg = S.CONFIGS["tiny_fp32"]
     n = cfg.block_size - 1
-    ht = SyntheticTarget(seed=1)
+    ts = TARGET_TINY
+    hw = make_target_weights(1, ts)
     f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
-    tcfg = dict(hidden=ht.H, n_heads=ht.nh, head_dim=ht.d, intermediate=ht.I, vocab=ht.V, n_layers=ht.L,
-                rope_theta=ht.theta, rms_eps=ht.eps)
-    tw = dict(embed=f32(ht.E), unembed=f32(ht.U), final_norm=f32(ht.nf),
-              layers=[{k: f32(v) for k, v in lw.items()} for lw in ht.layers])
+    tw = dict(embed=f32(hw["embed"]), unembed=f32(hw["unembed"]), final_norm=f32(hw["final_norm"]),
+              layers=[{k: f32(v) for k, v in lw.items()} for lw in hw["layers"]])
     model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED, dev))
     max_ctx = 16 + (n + 1) * (W + K + 2)
-    V, NT = ht.V, ht.n_taps * ht.H
+    V, NT = ts.vocab, ts.n_taps * ts.hidden
     prompt = [int(x) for x in S.rng_for(0, "prompt").integers(0, V, size=8)]
     with torch.cuda.stream(stream):
-        tgt = D.dflash_target_create(tcfg, tw, max_ctx=max_ctx, stream=stream)
+        tgt = D.dflash_target_create(ts.as_dict(), tw, max_ctx=max_ctx, stream=stream)
         sess = D.dflash_open(model, max_ctx=max_ctx, stream=stream)
         lg_p = torch.empty((len(prompt), V), dtype=torch.float32, device=dev)
         tp_p = torch.empty((len(prompt), NT), dtype=torch.float32, device=dev)
@@ -668,7 +667,7 @@ def _spec_decode(args, world, local_rank, dev, stream, K, W):
     D.dflash_target_device_status(tgt)
     D.dflash_device_status(model)
     D.dflash_close(sess)
-    launches_fwd = 2 + 14 * ht.L + 2 + 1
+    launches_fwd = 2 + 14 * ts.n_layers + 2 + 1
     return _line("generated tok/s (greedy speculative decoding, tiny fp32 draft + synthetic target, on GPU)",
                  "generated tok/s", world * timed_tokens / (ms * 1e-3), world, K, W, ms, "f32",
                  {"workload": "tiny_fp32 draft (2 layers, H 256, block 8, n=7) + a 2-layer H-256 fp32 target, "

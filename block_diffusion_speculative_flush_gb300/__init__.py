@@ -28,6 +28,7 @@ __all__ = [
     "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read", "dflash_verify_noalloc",
     "Target", "dflash_target_create", "dflash_target_destroy", "dflash_target_forward", "dflash_target_trim",
     "dflash_target_length", "dflash_target_argmax", "dflash_target_device_status",
+    "dflash_logits_compare", "dflash_exactness_summarize", "dflash_target_exactness_probe", "exactness_rows",
 ]
 
 
@@ -328,3 +329,60 @@ def dflash_target_argmax(target: Target, logits: torch.Tensor, out: torch.Tensor
 
 def dflash_target_device_status(target: Target) -> None:
     _check(lib.dflash_target_device_status(target.handle))
+
+
+EXACTNESS_ROW_BYTES = C.sizeof(_abi.dflash_exactness_row)
+
+
+def _rows_buffer(out: torch.Tensor, rows: int) -> None:
+    if out.dtype != torch.uint8 or not out.is_contiguous() or out.numel() < rows * EXACTNESS_ROW_BYTES:
+        raise ValueError(f"out must be a contiguous uint8 CUDA buffer of rows * {EXACTNESS_ROW_BYTES} bytes")
+
+
+def _logits_pair(a: torch.Tensor, b: torch.Tensor) -> tuple:
+    if a.dtype != torch.float32 or b.dtype != torch.float32 or a.dim() != 2 or a.shape != b.shape or \
+            not a.is_contiguous() or not b.is_contiguous():
+        raise ValueError("block and chain logits must be contiguous fp32 [rows, vocab] of one shape")
+    return a.shape[0], a.shape[1]
+
+
+def dflash_logits_compare(block: torch.Tensor, chain: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """block, chain: fp32 CUDA [rows][vocab]; out: uint8 CUDA buffer of rows dflash_exactness_row records."""
+    rows, V = _logits_pair(block, chain)
+    _rows_buffer(out, rows)
+    stream = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.dflash_logits_compare(_ptr(block), _ptr(chain), rows, V, _ptr(out), C.c_void_p(stream.cuda_stream)))
+
+
+def _records(buf):
+    raw = bytes(buf.cpu().numpy().tobytes()) if isinstance(buf, torch.Tensor) else bytes(buf)
+    n = len(raw) // EXACTNESS_ROW_BYTES
+    return (_abi.dflash_exactness_row * n).from_buffer_copy(raw[:n * EXACTNESS_ROW_BYTES])
+
+
+def exactness_rows(buf) -> list:
+    """Decodes row records (the uint8 buffer, copied to the host) into dicts."""
+    return [dict(differing_bytes=r.differing_bytes, block_top=list(r.block_top), chain_top=list(r.chain_top),
+                 block_val=list(r.block_val), chain_val=list(r.chain_val)) for r in _records(buf)]
+
+
+def dflash_exactness_summarize(buf) -> dict:
+    arr = _records(buf)
+    s = _abi.dflash_exactness_summary()
+    _check(lib.dflash_exactness_summarize(arr, len(arr), C.byref(s)))
+    return {k: getattr(s, k) for k, _ in s._fields_}
+
+
+def dflash_target_exactness_probe(target: Target, tokens: torch.Tensor, start: int, block_logits: torch.Tensor,
+                                  chain_logits: torch.Tensor, out: torch.Tensor) -> dict:
+    """Block forward and one-token forwards of `tokens` at start, compared; the
+    cache is left at `start`.  Returns the summary (the call synchronises)."""
+    rows, V = _logits_pair(block_logits, chain_logits)
+    if tokens.dtype != torch.int32 or not tokens.is_contiguous() or tokens.numel() != rows or \
+            V != target.cfg["vocab"]:
+        raise ValueError("tokens must be contiguous int32 [rows] and logits [rows, vocab]")
+    _rows_buffer(out, rows)
+    s = _abi.dflash_exactness_summary()
+    _check(lib.dflash_target_exactness_probe(target.handle, _ptr(tokens), rows, start, _ptr(block_logits),
+                                             _ptr(chain_logits), _ptr(out), C.byref(s)))
+    return {k: getattr(s, k) for k, _ in s._fields_}

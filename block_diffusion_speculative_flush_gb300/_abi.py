@@ -68,6 +68,16 @@ class dflash_target_weights(C.Structure):
                 ("layers", C.POINTER(dflash_target_layer))]
 
 
+class dflash_exactness_row(C.Structure):
+    _fields_ = [("differing_bytes", C.c_int32), ("block_top", C.c_int32 * 2), ("chain_top", C.c_int32 * 2),
+                ("block_val", C.c_float * 2), ("chain_val", C.c_float * 2)]
+
+
+class dflash_exactness_summary(C.Structure):
+    _fields_ = [("rows", C.c_int64), ("differing_bytes", C.c_int64), ("first_row_differing_bytes", C.c_int64),
+                ("disagreements", C.c_int32), ("allows", C.c_int32)]
+
+
 P = C.c_void_p
 SessArr = C.POINTER(C.c_void_p)
 
@@ -105,6 +115,11 @@ SIGNATURES = {
     "dflash_target_length": (C.c_int, [P, C.POINTER(C.c_int64)]),
     "dflash_target_argmax": (C.c_int, [P, P, C.c_int32, P]),
     "dflash_target_device_status": (C.c_int, [P]),
+    "dflash_logits_compare": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P]),
+    "dflash_exactness_summarize": (C.c_int, [C.POINTER(dflash_exactness_row), C.c_int32,
+                                             C.POINTER(dflash_exactness_summary)]),
+    "dflash_target_exactness_probe": (C.c_int, [P, P, C.c_int32, C.c_int64, P, P, P,
+                                                C.POINTER(dflash_exactness_summary)]),
 }
 
 

@@ -12,9 +12,10 @@
 // to the cache and to the earlier rows of the call, so a multi-row verify
 // forward and token-by-token decoding compute the same rows.
 //
-// It reuses the draft's CUDA-core kernels: the RMSNorm, the GEMM, the split-
-// key attention and its merge (the new rows are the "block" rows, causal
-// among themselves), the residual add, SwiGLU and the row copy for the taps.
+// It reuses the draft's CUDA-core kernels: the RMSNorm, the split-key
+// attention and its merge (the new rows are the "block" rows, causal among
+// themselves), the residual add, SwiGLU and the row copy for the taps; its
+// matrix products are a skinny warp-per-column kernel (k_gemm_rows).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -76,6 +77,55 @@ __global__ void k_target_qkv(const float* __restrict__ qkv, const float2* __rest
   for (int j = threadIdx.x; j < d; j += blockDim.x) vp[(int64_t)j * cap] = row[2 * qd + h * d + j];
 }
 
+// Y[M][N] = X[M][K] . W[N][K]^T for few rows: one warp per output column n,
+// lanes striding K by float4 (lane l takes k = 4l + 128j), eight rows per
+// pass, then a butterfly sum.  A row's arithmetic (its lane partition and the
+// reduction tree) does not depend on M or on which pass holds it, so a
+// multi-row forward and one-row forwards give bit-identical rows.  Rows are
+// 16-byte aligned (K, ldx, ldw multiples of 4).
+__global__ void __launch_bounds__(256) k_gemm_rows(const float* __restrict__ X, int64_t ldx,
+                                                   const float* __restrict__ W, int64_t ldw, float* __restrict__ Y,
+                                                   int64_t ldy, int M, int N, int K) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (n >= N) return;
+  const float4* w4 = reinterpret_cast<const float4*>(W + (int64_t)n * ldw);
+  const int K4 = K >> 2;
+  for (int m0 = 0; m0 < M; m0 += 8) {
+    float acc[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) acc[r] = 0.f;
+    for (int k = lane; k < K4; k += 32) {
+      const float4 w = __ldg(w4 + k);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (m0 + r < M) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(X + (int64_t)(m0 + r) * ldx) + k);
+          float a = acc[r];
+          a = fmaf(x.x, w.x, a);
+          a = fmaf(x.y, w.y, a);
+          a = fmaf(x.z, w.z, a);
+          a = fmaf(x.w, w.w, a);
+          acc[r] = a;
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float v = warp_sum(acc[r]);
+      if (lane == 0 && m0 + r < M) Y[(int64_t)(m0 + r) * ldy + n] = v;
+    }
+  }
+}
+
+void launch_gemm_rows(const float* X, int64_t ldx, const float* W, int64_t ldw, float* Y, int64_t ldy, int M, int N,
+                      int K, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return;
+  launch_k(k_gemm_rows, (unsigned)((N + 7) / 8), 256, 0, st, X, ldx, W, ldw, Y, ldy, M, N, K);
+}
+
 // Greedy choice of each row (lowest index on a tie), for the speculative loop.
 __global__ void k_row_argmax(const float* __restrict__ logits, int V, int32_t* __restrict__ out) {
   pdl_trigger();
@@ -91,6 +141,88 @@ __global__ void k_row_argmax(const float* __restrict__ logits, int V, int32_t* _
     ArgMax b = sm[0];
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) b = better(b, sm[w]);
     out[r] = b.i < 0 || b.i >= V ? 0 : b.i;
+  }
+}
+
+// Best two entries of a row by (value descending, id ascending); NaN never
+// enters (both comparisons are false for it).
+struct Top2 {
+  ArgMax a, b;
+};
+__device__ __forceinline__ bool beats(ArgMax x, ArgMax y) { return x.v > y.v || (x.v == y.v && x.i < y.i); }
+__device__ __forceinline__ void top2_insert(Top2& t, ArgMax x) {
+  if (beats(x, t.a)) {
+    t.b = t.a;
+    t.a = x;
+  } else if (beats(x, t.b)) {
+    t.b = x;
+  }
+}
+__device__ __forceinline__ Top2 top2_merge(Top2 p, Top2 q) {
+  Top2 r = p;
+  top2_insert(r, q.a);
+  top2_insert(r, q.b);
+  return r;
+}
+__device__ __forceinline__ Top2 shfl_top2(Top2 t, int o) {
+  Top2 u;
+  u.a.v = __shfl_xor_sync(0xffffffffu, t.a.v, o);
+  u.a.i = __shfl_xor_sync(0xffffffffu, t.a.i, o);
+  u.b.v = __shfl_xor_sync(0xffffffffu, t.b.v, o);
+  u.b.i = __shfl_xor_sync(0xffffffffu, t.b.i, o);
+  return u;
+}
+
+// One CTA per row: the count of differing bytes of the two fp32 encodings
+// and the top two of each arm.
+__global__ void __launch_bounds__(256) k_logits_compare(const float* __restrict__ block,
+                                                        const float* __restrict__ chain, int V,
+                                                        dflash_exactness_row* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x;
+  const ArgMax none{-INFINITY, INT32_MAX};
+  Top2 tb{none, none}, tc{none, none};
+  int diff = 0;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = block[(int64_t)r * V + v], y = chain[(int64_t)r * V + v];
+    const uint32_t d = __float_as_uint(x) ^ __float_as_uint(y);
+    diff += ((d & 0xffu) != 0) + ((d & 0xff00u) != 0) + ((d & 0xff0000u) != 0) + ((d & 0xff000000u) != 0);
+    top2_insert(tb, ArgMax{x, v});
+    top2_insert(tc, ArgMax{y, v});
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tb = top2_merge(tb, shfl_top2(tb, o));
+    tc = top2_merge(tc, shfl_top2(tc, o));
+    diff += __shfl_xor_sync(0xffffffffu, diff, o);
+  }
+  __shared__ Top2 sb[8], sc[8];
+  __shared__ int sd[8];
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sb[w] = tb;
+    sc[w] = tc;
+    sd[w] = diff;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < (int)(blockDim.x >> 5); ++k) {
+      tb = top2_merge(tb, sb[k]);
+      tc = top2_merge(tc, sc[k]);
+      diff += sd[k];
+    }
+    dflash_exactness_row o;
+    o.differing_bytes = diff;
+    o.block_top[0] = tb.a.i;
+    o.block_top[1] = tb.b.i;
+    o.chain_top[0] = tc.a.i;
+    o.chain_top[1] = tc.b.i;
+    o.block_val[0] = tb.a.v;
+    o.block_val[1] = tb.b.v;
+    o.chain_val[0] = tc.a.v;
+    o.chain_val[1] = tc.b.v;
+    out[r] = o;
   }
 }
 
@@ -160,9 +292,17 @@ DFLASH_API int dflash_target_create(const dflash_target_config* cfg, const dflas
   if (!cfg || !w || !out || !w->embed || !w->unembed || !w->final_norm || !w->layers)
     return tfail(DFLASH_ERR_INVALID_ARG, "dflash_target_create: null argument");
   const dflash_target_config& c = *cfg;
-  if (c.hidden <= 0 || c.n_heads <= 0 || c.head_dim <= 0 || c.head_dim % 4 || c.head_dim > 128 || c.intermediate <= 0 || c.vocab <= 0 ||
+  if (c.hidden <= 0 || c.n_heads <= 0 || c.head_dim <= 0 || c.head_dim % 4 || c.head_dim > 128 || c.intermediate <= 0 || c.hidden % 4 || c.intermediate % 4 || c.vocab <= 0 ||
       c.n_layers <= 0 || c.n_layers > 64 || c.hidden > 4096 || c.n_heads * c.head_dim > 4096 || max_ctx <= 0)
     return tfail(DFLASH_ERR_SHAPE, "dflash_target_create: unsupported shape");
+  if ((uintptr_t)w->unembed % 16) return tfail(DFLASH_ERR_INVALID_ARG, "dflash_target_create: unembed not 16-byte aligned");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_target_layer& L = w->layers[l];
+    if (!L.n1 || !L.wq || !L.wk || !L.wv || !L.wo || !L.n2 || !L.wg || !L.wu || !L.wd)
+      return tfail(DFLASH_ERR_INVALID_ARG, "dflash_target_create: null layer weight");
+    if (((uintptr_t)L.wo | (uintptr_t)L.wd) % 16)
+      return tfail(DFLASH_ERR_INVALID_ARG, "dflash_target_create: wo or wd not 16-byte aligned");
+  }
   dflash_target* t = new dflash_target();
   t->cfg = c;
   t->E = (const float*)w->embed;
@@ -177,10 +317,6 @@ DFLASH_API int dflash_target_create(const dflash_target_config* cfg, const dflas
   if (e == cudaSuccess) e = cudaMalloc(&t->kv, (size_t)2 * c.n_layers * c.n_heads * max_ctx * c.head_dim * 4);
   for (int l = 0; l < c.n_layers && e == cudaSuccess; ++l) {
     const dflash_target_layer& L = w->layers[l];
-    if (!L.n1 || !L.wq || !L.wk || !L.wv || !L.wo || !L.n2 || !L.wg || !L.wu || !L.wd) {
-      e = cudaErrorInvalidValue;
-      break;
-    }
     dflash_target::Layer Lw{(const float*)L.n1, (const float*)L.wo, (const float*)L.n2, (const float*)L.wd, nullptr,
                             nullptr};
     const size_t qb = (size_t)qd * H * 4, gb = (size_t)I * H * 4;
@@ -196,7 +332,7 @@ DFLASH_API int dflash_target_create(const dflash_target_config* cfg, const dflas
   if (e != cudaSuccess) {
     const int rc = tcheck(e, "dflash_target_create");
     dflash_target_destroy(t);
-    return rc == DFLASH_OK ? tfail(DFLASH_ERR_INVALID_ARG, "dflash_target_create: null layer weight") : rc;
+    return rc;
   }
   *out = t;
   return DFLASH_OK;
@@ -309,7 +445,7 @@ DFLASH_API int dflash_target_forward(dflash_target* t, const int32_t* tokens, in
     for (int l = 0; l < c.n_layers; ++l) {
       const dflash_target::Layer& L = t->layers[l];
       launch_rmsnorm(DT::F32, true, X, R, nullptr, H, L.n1, Y, H, R, H, R, 0, 0, c.rms_eps, st);
-      launch_gemm_simt(DT::F32, Y, H, L.wqkv, H, t->qkv.as<float>(), 3 * qd, R, 3 * qd, H, st);
+      launch_gemm_rows(Y, H, L.wqkv, H, t->qkv.as<float>(), 3 * qd, R, 3 * qd, H, st);
       launch_k(k_target_qkv, dim3(R, nh), 64, 0, st, (const float*)t->qkv.as<float>(),
                (const float2*)(tb + o_rope), nh, d, F, t->cap, l, t->Q.as<float>(), t->kv);
       ap.layer = l;
@@ -317,22 +453,68 @@ DFLASH_API int dflash_target_forward(dflash_target* t, const int32_t* tokens, in
                             t->part.as<float>(), st);
       launch_attention_combine(DT::F32, t->part.as<float>(), (const int32_t*)(tb + o_first),
                                (const int32_t*)(tb + o_cnt), 1, ap, nullptr, t->O.p, st);
-      launch_gemm_simt(DT::F32, t->O.p, qd, L.wo, qd, t->tmp.as<float>(), H, R, H, qd, st);
+      launch_gemm_rows(t->O.as<float>(), qd, L.wo, qd, t->tmp.as<float>(), H, R, H, qd, st);
       launch_residual(DT::F32, X, t->tmp.as<float>(), H, R, H, st);
       tap(1 + 2 * l);
       launch_rmsnorm(DT::F32, true, X, R, nullptr, H, L.n2, Y, H, R, H, R, 0, 0, c.rms_eps, st);
-      launch_gemm_simt(DT::F32, Y, H, L.wgu, H, t->gu.as<float>(), 2 * I, R, 2 * I, H, st);
+      launch_gemm_rows(Y, H, L.wgu, H, t->gu.as<float>(), 2 * I, R, 2 * I, H, st);
       launch_swiglu(DT::F32, t->gu.as<float>(), 2 * I, R, I, I, t->a.p, st);
-      launch_gemm_simt(DT::F32, t->a.p, I, L.wd, I, t->tmp.as<float>(), H, R, H, I, st);
+      launch_gemm_rows(t->a.as<float>(), I, L.wd, I, t->tmp.as<float>(), H, R, H, I, st);
       launch_residual(DT::F32, X, t->tmp.as<float>(), H, R, H, st);
       tap(2 + 2 * l);
     }
     launch_rmsnorm(DT::F32, true, X, R, nullptr, H, t->nf, Y, H, R, H, R, 0, 0, c.rms_eps, st);
-    launch_gemm_simt(DT::F32, Y, H, t->U, H, logits + (size_t)r0 * V, V, R, V, H, st);
+    launch_gemm_rows(Y, H, t->U, H, logits + (size_t)r0 * V, V, R, V, H, st);
     if ((rc = tcheck(cudaGetLastError(), "target forward")) != DFLASH_OK) return rc;
     t->len = F + R;
   }
   return DFLASH_OK;
+}
+
+DFLASH_API int dflash_logits_compare(const float* block, const float* chain, int32_t rows, int32_t vocab,
+                                     dflash_exactness_row* out, void* stream) {
+  if (!block || !chain || !out || rows <= 0 || vocab <= 0)
+    return tfail(DFLASH_ERR_INVALID_ARG, "dflash_logits_compare: bad argument");
+  launch_k(k_logits_compare, rows, 256, 0, (cudaStream_t)stream, block, chain, (int)vocab, out);
+  return tcheck(cudaGetLastError(), "dflash_logits_compare");
+}
+
+DFLASH_API int dflash_exactness_summarize(const dflash_exactness_row* rows_host, int32_t rows,
+                                          dflash_exactness_summary* out) {
+  if (!rows_host || !out || rows <= 0) return tfail(DFLASH_ERR_INVALID_ARG, "dflash_exactness_summarize: bad argument");
+  dflash_exactness_summary s{};
+  s.rows = rows;
+  for (int r = 0; r < rows; ++r) {
+    s.differing_bytes += rows_host[r].differing_bytes;
+    s.disagreements += rows_host[r].block_top[0] != rows_host[r].chain_top[0];
+  }
+  s.first_row_differing_bytes = rows_host[0].differing_bytes;
+  s.allows = s.first_row_differing_bytes == 0;
+  *out = s;
+  return DFLASH_OK;
+}
+
+DFLASH_API int dflash_target_exactness_probe(dflash_target* t, const int32_t* tokens, int32_t rows, int64_t start,
+                                             float* block_logits, float* chain_logits,
+                                             dflash_exactness_row* out_rows, dflash_exactness_summary* summary) {
+  if (!t || !tokens || !block_logits || !chain_logits || !out_rows || rows <= 0)
+    return tfail(DFLASH_ERR_INVALID_ARG, "dflash_target_exactness_probe: bad argument");
+  if (start != t->len) return tfail(DFLASH_ERR_CONTEXT_GAP, "dflash_target_exactness_probe: start is not the cached length");
+  const int64_t V = t->cfg.vocab;
+  int rc = dflash_target_forward(t, tokens, rows, start, block_logits, nullptr);
+  if (rc == DFLASH_OK) t->len = start;
+  for (int i = 0; i < rows && rc == DFLASH_OK; ++i)
+    rc = dflash_target_forward(t, tokens + i, 1, start + i, chain_logits + i * V, nullptr);
+  t->len = std::min(t->len, start);
+  if (rc != DFLASH_OK) return rc;
+  if ((rc = dflash_logits_compare(block_logits, chain_logits, rows, (int32_t)V, out_rows, t->st)) != DFLASH_OK) return rc;
+  if (!summary) return DFLASH_OK;
+  std::vector<dflash_exactness_row> h(rows);
+  rc = tcheck(cudaMemcpyAsync(h.data(), out_rows, rows * sizeof(dflash_exactness_row), cudaMemcpyDeviceToHost, t->st),
+              "exactness rows");
+  if (rc == DFLASH_OK) rc = tcheck(cudaStreamSynchronize(t->st), "exactness rows");
+  if (rc != DFLASH_OK) return rc;
+  return dflash_exactness_summarize(h.data(), rows, summary);
 }
 
 DFLASH_API int dflash_target_device_status(dflash_target* t) {

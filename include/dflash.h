@@ -314,8 +314,10 @@ typedef struct dflash_target_weights {
   const dflash_target_layer* layers;  /* host array of n_layers */
 } dflash_target_weights;
 
-/* Validates the shapes (hidden and n_heads * head_dim at most 4096, head_dim a
- * multiple of 4 and at most 128, else DFLASH_ERR_SHAPE), allocates
+/* Validates the shapes (hidden and n_heads * head_dim at most 4096, hidden and
+ * intermediate multiples of 4, head_dim a multiple of 4 and at most 128, else
+ * DFLASH_ERR_SHAPE) and the weights (non-NULL; wo, wd and unembed 16-byte
+ * aligned, else DFLASH_ERR_INVALID_ARG); allocates
  * a cache of max_ctx positions; every call enqueues on `stream`. */
 DFLASH_API int dflash_target_create(const dflash_target_config* cfg, const dflash_target_weights* w, int64_t max_ctx,
                                     void* stream, dflash_target** out);
@@ -334,6 +336,53 @@ DFLASH_API int dflash_target_argmax(dflash_target* t, const float* logits, int32
 /* Synchronises the target's stream and reports a device-side error (a token
  * id outside [0, vocab)) as DFLASH_ERR_DEVICE. */
 DFLASH_API int dflash_target_device_status(dflash_target* t);
+
+/* ---- block-versus-chain exactness ----------------------------------------
+ * Greedy speculative output equals plain greedy decoding only if the target's
+ * multi-row verify forward gives the same logits as one-token decoding.  The
+ * mlxcel Laguna PR (the real-checkpoint probe commit and the report commits)
+ * compares a block_size-wide verify block with single-token decode on the
+ * target alone, counts the logit bytes that differ at the first verify
+ * position (its gate declines the pairing when any do) and reports the top-2
+ * logits of both arms at every argmax disagreement, whose chain-arm margin
+ * (0.0 or 0.125 there) shows a bf16 tie.  Logits here are fp32; bytes are
+ * counted over their fp32 encodings. */
+typedef struct {
+  int32_t differing_bytes; /* bytes of the row's fp32 logits that differ between the arms */
+  int32_t block_top[2];    /* the block arm's best and second token (value desc, then id asc) */
+  int32_t chain_top[2];    /* the chain arm's */
+  float block_val[2];      /* their logits */
+  float chain_val[2];
+} dflash_exactness_row;
+
+typedef struct {
+  int64_t rows;
+  int64_t differing_bytes;           /* over all rows */
+  int64_t first_row_differing_bytes; /* at the first verify position */
+  int32_t disagreements;             /* rows whose block and chain argmax differ */
+  int32_t allows;                    /* 1 when no logit byte differs at the first position */
+} dflash_exactness_summary;
+
+/* Row records of two device fp32 logit arrays [rows][vocab] (block arm,
+ * chain arm) into device out[rows], on `stream`.  NaN entries are never
+ * chosen as a top token.  Any [rows][vocab] pair can be compared, e.g. the
+ * logits of an external target.  Bad sizes or null pointers:
+ * DFLASH_ERR_INVALID_ARG. */
+DFLASH_API int dflash_logits_compare(const float* block, const float* chain, int32_t rows, int32_t vocab,
+                                     dflash_exactness_row* out, void* stream);
+/* Host reduction of `rows` row records (host memory) into *out. */
+DFLASH_API int dflash_exactness_summarize(const dflash_exactness_row* rows_host, int32_t rows,
+                                          dflash_exactness_summary* out);
+/* The probe on a dflash_target: `rows` tokens at start (= the cached length,
+ * else DFLASH_ERR_CONTEXT_GAP) as one block forward into block_logits, then
+ * as `rows` one-token forwards into chain_logits (both device fp32
+ * [rows][vocab], caller-owned), then the comparison into device out_rows.
+ * The cache is trimmed back to `start`, so the probe leaves the target as it
+ * found it.  When summary is not NULL the call synchronises the stream and
+ * fills it. */
+DFLASH_API int dflash_target_exactness_probe(dflash_target* t, const int32_t* tokens, int32_t rows, int64_t start,
+                                             float* block_logits, float* chain_logits,
+                                             dflash_exactness_row* out_rows, dflash_exactness_summary* summary);
 
 #ifdef __cplusplus
 }

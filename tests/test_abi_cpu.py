@@ -82,3 +82,53 @@ def test_null_arguments_are_refused(lib):
     assert lib.dflash_model_create(C.byref(c), None, C.byref(out)) == _abi.DFLASH_ERR_INVALID_ARG
     w = _abi.dflash_weights()   # all weights null
     assert lib.dflash_model_create(C.byref(c), C.byref(w), C.byref(out)) == _abi.DFLASH_ERR_INVALID_ARG
+
+
+def test_exactness_summary_is_host_code_that_agrees_with_the_oracle(lib):
+    """dflash_exactness_summarize reduces row records on the host (no GPU):
+    the same gate and counts as the probe oracle on the same records."""
+    import numpy as np
+
+    from oracle.target_oracle import exactness_rows, exactness_summary
+    rng = np.random.default_rng(4)
+    block = rng.standard_normal((5, 40)).astype(np.float32)
+    chain = block.copy()
+    chain[1, 3] += 1.0
+    chain[3] = block[3, ::-1]
+    for first_differs in (False, True):
+        if first_differs:
+            chain[0, 0] = -chain[0, 0]
+        rows = exactness_rows(block, chain)
+        recs = (_abi.dflash_exactness_row * 5)()
+        for rec, r in zip(recs, rows):
+            rec.differing_bytes = r["differing_bytes"]
+            rec.block_top[:] = r["block_top"]
+            rec.chain_top[:] = r["chain_top"]
+            rec.block_val[:] = r["block_val"]
+            rec.chain_val[:] = r["chain_val"]
+        s = _abi.dflash_exactness_summary()
+        assert lib.dflash_exactness_summarize(recs, 5, C.byref(s)) == 0
+        assert {k: getattr(s, k) for k, _ in s._fields_} == exactness_summary(rows)
+    assert lib.dflash_exactness_summarize(None, 5, C.byref(s)) == _abi.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_logits_compare(None, None, 1, 1, None, None) == _abi.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_target_exactness_probe(None, None, 1, 0, None, None, None, None) == _abi.DFLASH_ERR_INVALID_ARG
+
+
+def test_target_create_refuses_bad_shapes_and_weights_on_the_host(lib):
+    cfg = _abi.dflash_target_config(hidden=256, n_heads=4, head_dim=64, intermediate=512, vocab=32, n_layers=1,
+                                    rope_theta=1e6, rms_eps=1e-6)
+    out = C.c_void_p()
+    layers = (_abi.dflash_target_layer * 1)()
+    w = _abi.dflash_target_weights(embed=16, unembed=16, final_norm=16, layers=layers)
+    # a null layer weight and a misaligned one are refused before anything is allocated
+    assert lib.dflash_target_create(C.byref(cfg), C.byref(w), 64, None, C.byref(out)) == _abi.DFLASH_ERR_INVALID_ARG
+    for name in ("n1", "wq", "wk", "wv", "wo", "n2", "wg", "wu", "wd"):
+        setattr(layers[0], name, 4096)
+    layers[0].wo = 4100
+    assert lib.dflash_target_create(C.byref(cfg), C.byref(w), 64, None, C.byref(out)) == _abi.DFLASH_ERR_INVALID_ARG
+    w.unembed = 20
+    assert lib.dflash_target_create(C.byref(cfg), C.byref(w), 64, None, C.byref(out)) == _abi.DFLASH_ERR_INVALID_ARG
+    for field, bad in (("head_dim", 66), ("head_dim", 256), ("hidden", 258), ("n_layers", 0)):
+        c2 = _abi.dflash_target_config.from_buffer_copy(cfg)
+        setattr(c2, field, bad)
+        assert lib.dflash_target_create(C.byref(c2), C.byref(w), 64, None, C.byref(out)) == _abi.DFLASH_ERR_SHAPE
