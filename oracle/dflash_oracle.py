@@ -35,7 +35,9 @@ Readings where the pages are silent:
   R8 fused qkv rows are ordered q | k | v;  R9 one sigmoid gate per query
   head from g_proj;  R10 bidirectional attention inside the block unless the
   config says causal;  R11 block K/V never persist (rewound before any write);
-  R13 full-vocabulary distributions (no top-k / top-p);  R15 if the
+  R13 full-vocabulary distributions unless the session sets a truncation;
+  R24 truncation = top-k, softmax, top-p, min-p, each keeping a prefix of
+  the (value desc, id asc) order, for draft and target rows alike;  R15 if the
   residual max(0, p - q) sums to zero, the bonus is drawn from p.
 
 Storage rounding: for bf16 configs the values that the CUDA path stores in
@@ -357,12 +359,48 @@ class OracleDraft:
 # Sampling and verification
 # ---------------------------------------------------------------------------
 
-def sample_rows(logits, temperature, seed, rnd, seq):
+def truncated_support(s, top_k=0, top_p=1.0, min_p=0.0):
+    """The ids a truncating sampler keeps for one row of scaled scores s = l/T.
+
+    dflash.go selectBlock draws from the sampler's Distribution, whose IDs
+    are the kept tokens.  The truncation (reading R24): order the row by
+    value, descending, then by id; keep the first top_k (0: all); take the
+    softmax over what is kept; keep an entry while the probability mass
+    strictly before it is below top_p; keep entries whose probability is at
+    least min_p times the largest.  Every step keeps a prefix of the order,
+    so the result is a prefix too.  NaN scores are never kept.
+    Returns the kept ids in that order.
+    """
+    s = np.asarray(s, dtype=np.float64)
+    ids = np.arange(len(s))
+    ok = ~np.isnan(s)
+    order = ids[ok][np.lexsort((ids[ok], -s[ok]))]
+    if top_k:
+        order = order[:top_k]
+    e = np.exp(s[order] - s[order[0]])
+    p = e / e.sum()
+    keep = len(order)
+    if top_p < 1.0:
+        before = np.cumsum(p) - p
+        keep = min(keep, int(np.count_nonzero(before < top_p)))
+    if min_p > 0.0:
+        keep = min(keep, int(np.count_nonzero(p >= min_p * p[0])))
+    return order[:keep]
+
+
+def truncation_active(trunc) -> bool:
+    return trunc is not None and (trunc[0] > 0 or trunc[1] < 1.0 or trunc[2] > 0.0)
+
+
+def sample_rows(logits, temperature, seed, rnd, seq, trunc=None):
     """One batched draw for rows 1..n of a block (dflash.go selectBlock).
 
     T == 0: argmax (lowest index on ties), q(token) = 1.
     T > 0: token = argmax_v(l_v/T + Gumbel_v), which is an exact draw from
     softmax(l/T); q(token) = exp(l_token/T - logsumexp(l/T)).
+    trunc = (top_k, top_p, min_p) at T > 0: the same draw over the kept ids
+    only (truncated_support), with the log-sum-exp over them; T == 0 is
+    unchanged (the best id is always kept).
     Returns tokens [n], q(token) [n], lse [n] (nan when T == 0).
     """
     logits = np.atleast_2d(np.asarray(logits, dtype=np.float64))
@@ -375,24 +413,42 @@ def sample_rows(logits, temperature, seed, rnd, seq):
             toks[i] = int(np.argmax(logits[i]))
             continue
         s = logits[i] / temperature
-        lse[i] = logsumexp(s)
         g = gumbel(seed, rnd, STREAM_DRAFT, seq, i + 1, np.arange(V))
-        toks[i] = int(np.argmax(s + g))
+        if truncation_active(trunc):
+            kept = truncated_support(s, *trunc)
+            lse[i] = logsumexp(s[kept])
+            score = np.full(V, -np.inf)
+            score[kept] = s[kept] + g[kept]
+        else:
+            lse[i] = logsumexp(s)
+            score = s + g
+        toks[i] = int(np.argmax(score))
         qtok[i] = np.exp(s[toks[i]] - lse[i])
     return toks, qtok, lse
 
 
-def proposal_distribution(draft_logits_row, draft_temperature, proposed_token):
-    """q of one block row: softmax(l/T) at T > 0, one-hot of the proposal at T == 0."""
+def sampler_distribution(logits_row, temperature, trunc=None):
+    """softmax(l/T), restricted to the kept ids and renormalised when trunc is active."""
+    s = np.asarray(logits_row, dtype=np.float64) / temperature
+    if not truncation_active(trunc):
+        return softmax(s)
+    kept = truncated_support(s, *trunc)
+    p = np.zeros(len(s))
+    p[kept] = softmax(s[kept])
+    return p
+
+
+def proposal_distribution(draft_logits_row, draft_temperature, proposed_token, trunc=None):
+    """q of one block row: the sampler's distribution at T > 0, one-hot of the proposal at T == 0."""
     if draft_temperature == 0:
         q = np.zeros(len(draft_logits_row))
         q[int(proposed_token)] = 1.0
         return q
-    return softmax(np.asarray(draft_logits_row, dtype=np.float64) / draft_temperature)
+    return sampler_distribution(draft_logits_row, draft_temperature, trunc)
 
 
 def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_temperature,
-           temperature, seed, rnd, seq):
+           temperature, seed, rnd, seq, trunc=None, draft_trunc=None):
     """Accepted prefix length a and bonus token b.
 
     target_logits [n+1, V]: row r scores the token after [current, d_1..d_r].
@@ -405,6 +461,10 @@ def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_tem
     p_i = softmax(target row i-1 / T); at the first rejection draw b from
     max(0, p_i - q_i) (from p_i if that is all zero, R15); if all n pass,
     draw b from p of row n.
+    trunc: the sampler's truncation of the target rows (p is the truncated,
+    renormalised distribution); draft_trunc: the one the proposal was drawn
+    with (q likewise).  The rule is unchanged, so the emitted tokens follow
+    the truncated target distribution.
     """
     tl = np.atleast_2d(np.asarray(target_logits, dtype=np.float64))
     n = len(draft_tokens)
@@ -415,8 +475,8 @@ def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_tem
             a += 1
         return a, int(np.argmax(tl[a]))
     for i in range(1, n + 1):
-        p = softmax(tl[i - 1] / temperature)
-        q = proposal_distribution(draft_logits[i - 1], draft_temperature, proposed_tokens[i - 1])
+        p = sampler_distribution(tl[i - 1], temperature, trunc)
+        q = proposal_distribution(draft_logits[i - 1], draft_temperature, proposed_tokens[i - 1], draft_trunc)
         d = int(draft_tokens[i - 1])
         r = uniform_open(random_u32(seed, rnd, STREAM_ACCEPT, seq, i, 0))
         if r * q[d] < p[d]:
@@ -427,7 +487,7 @@ def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_tem
         with np.errstate(divide="ignore"):
             score = np.log(res) + gumbel(seed, rnd, STREAM_BONUS, seq, i, np.arange(V))
         return i - 1, int(np.argmax(score))
-    p = softmax(tl[n] / temperature)
+    p = sampler_distribution(tl[n], temperature, trunc)
     with np.errstate(divide="ignore"):
         score = np.log(p) + gumbel(seed, rnd, STREAM_BONUS, seq, n + 1, np.arange(V))
     return n, int(np.argmax(score))
@@ -458,7 +518,12 @@ class OracleSession:
         self.cache = dict(restored_cache or {})
         self.seq = seq
         self.last = None               # what the last propose drew from
+        self.sampler = None            # (top_k, top_p, min_p) truncation, None: full distributions
         self.stats = dict(rounds=0, proposed=0, accepted=0)
+
+    def set_sampler(self, top_k: int = 0, top_p: float = 1.0, min_p: float = 0.0):
+        """The session's truncation, used for its draft rows and its target rows."""
+        self.sampler = (int(top_k), float(top_p), float(min_p))
 
     # dflash.go draftLimit
     @property
@@ -550,8 +615,8 @@ class OracleSession:
         tokens = [int(current)] + [c.mask_token] * n
         h = self.draft.block_forward(tokens, self.F, self.context())
         logits = self.draft.unembed(h[1:])          # the anchor row is unused
-        toks, q, lse = sample_rows(logits, temperature, seed, rnd, self.seq)
-        self.last = dict(tokens=toks, logits=logits, temperature=temperature)
+        toks, q, lse = sample_rows(logits, temperature, seed, rnd, self.seq, self.sampler)
+        self.last = dict(tokens=toks, logits=logits, temperature=temperature, trunc=self.sampler)
         self.stats["rounds"] += 1
         self.stats["proposed"] += n
         return dict(tokens=toks, q=q, logits=logits, lse=lse, hidden=h, n=n)
@@ -560,7 +625,8 @@ class OracleSession:
         if self.last is None:
             raise RuntimeError("verify without a proposal")
         a, b = verify(target_logits, draft_tokens, self.last["logits"], self.last["tokens"],
-                      self.last["temperature"], temperature, seed, rnd, self.seq)
+                      self.last["temperature"], temperature, seed, rnd, self.seq, self.sampler,
+                      self.last["trunc"])
         self.stats["accepted"] += a
         return a, b
 
