@@ -24,7 +24,7 @@ __all__ = [
     "DFlashError", "Model", "Session", "lib", "torch_dtype",
     "dflash_model_create", "dflash_model_destroy", "dflash_draft_limit", "dflash_device_status", "dflash_open",
     "dflash_committed", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
-    "dflash_close", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
+    "dflash_close", "dflash_set_sampler", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
     "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read", "dflash_verify_noalloc",
     "Target", "dflash_target_create", "dflash_target_destroy", "dflash_target_forward", "dflash_target_trim",
     "dflash_target_length", "dflash_target_argmax", "dflash_target_device_status",
@@ -197,6 +197,10 @@ def dflash_close(session: Session) -> None:
     if session.handle:
         _check(lib.dflash_close(session.handle))
         session.handle = None
+
+
+def dflash_set_sampler(session: Session, top_k: int = 0, top_p: float = 1.0, min_p: float = 0.0) -> None:
+    _check(lib.dflash_set_sampler(session.handle, top_k, top_p, min_p))
 
 
 def dflash_stats(session: Session) -> dict:

@@ -107,6 +107,7 @@ SIGNATURES = {
     "dflash_kv_import": (C.c_int, [P, C.c_int32, C.c_int64, C.c_int32, P, P]),
     "dflash_timing_enable": (C.c_int, [P, C.c_int32]),
     "dflash_timing_read": (C.c_int, [P, C.POINTER(dflash_kernel_time), C.c_int32, C.POINTER(C.c_int32)]),
+    "dflash_set_sampler": (C.c_int, [P, C.c_int32, C.c_float, C.c_float]),
     "dflash_target_create": (C.c_int, [C.POINTER(dflash_target_config), C.POINTER(dflash_target_weights), C.c_int64,
                                        P, C.POINTER(C.c_void_p)]),
     "dflash_target_destroy": (C.c_int, [P]),

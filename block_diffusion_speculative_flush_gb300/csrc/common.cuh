@@ -59,6 +59,27 @@ __device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
   if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
   return a;
 }
+// ---------------------------------------------------------------------------
+// the sampler's order: value descending, then id ascending
+// ---------------------------------------------------------------------------
+// Monotone map of a float to uint32 (a larger float gives a larger word;
+// -0 is taken as +0); NaN maps to 0.
+__device__ __forceinline__ uint32_t float_order(float s) {
+  if (s != s) return 0u;
+  uint32_t u = s == 0.f ? 0u : __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float float_of_order(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+// Key of entry v with scaled score s: a larger key comes first in the order;
+// NaN keys are 0.  A truncated distribution keeps the entries whose key is at
+// least its cut (cut 0: all entries).
+__device__ __forceinline__ uint64_t order_key(float s, int v) {
+  const uint32_t o = float_order(s);
+  return o ? ((uint64_t)o << 32) | (uint64_t)(0xffffffffu - (uint32_t)v) : 0ull;
+}
+
 __device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

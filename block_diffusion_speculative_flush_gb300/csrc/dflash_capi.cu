@@ -167,7 +167,7 @@ struct dflash_model {
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_pool;
   size_t ev_used = 0;
   // workspace
-  Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart, vbonus;
+  Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart, vbonus, cutbuf;
   HostRing ring;
 };
 
@@ -183,11 +183,14 @@ struct dflash_session {
   float* plogits = nullptr; // [B_s-1][V] logits of the last proposal
   float* plse = nullptr;    // [B_s-1]
   int32_t* ptok = nullptr;  // [B_s-1]
+  uint64_t* pcut = nullptr; // [B_s-1] truncation cut of each proposal row (when last_trunc)
   long long* d_accepted = nullptr;
   CUtensorMap* d_maps = nullptr;  // {K planes, V^T planes} for the tensor-core attention, or NULL
   bool has_prop = false;
   int last_n = 0;
   float last_T = 0.f;
+  Trunc trunc{0, 1.f, 0.f, 0};  // the sampler's truncation (top_k 0: full distributions)
+  bool last_trunc = false;      // the last proposal was drawn from a truncated distribution
   int64_t rounds = 0, proposed = 0, flushes = 0, flushed_rows = 0;
 };
 
@@ -429,6 +432,22 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     ptok[j] = fw.sess[j]->ptok;
   }
   const size_t o_plog = tp.add(plog), o_plse = tp.add(plse), o_ptok = tp.add(ptok);
+  // truncated draws (T > 0 and a session with a top_k): per-session settings and cut rows
+  bool any_trunc = false;
+  size_t o_trunc = 0, o_pcut = 0;
+  if (block && fw.temperature > 0.f) {
+    std::vector<Trunc> trv(Bc);
+    std::vector<uint64_t*> pcv(Bc);
+    for (int j = 0; j < Bc; ++j) {
+      trv[j] = fw.sess[j]->trunc;
+      pcv[j] = fw.sess[j]->pcut;
+      any_trunc = any_trunc || trv[j].top_k > 0;
+    }
+    if (any_trunc) {
+      o_trunc = tp.add(trv);
+      o_pcut = tp.add(pcv);
+    }
+  }
   const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
                o_front = tp.add(front), o_seq = tp.add(seqv), o_items = tp.add(items), o_ifirst = tp.add(ifirst),
                o_icount = tp.add(icount), o_map = tp.add(fw.sess_map), o_maps = tp.add(mapv);
@@ -573,6 +592,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   SampleArgs sa{};
   sa.logits = lg;
   sa.seq_logits = seg ? (const float* const*)(tb + o_plog) : nullptr;
+  if (any_trunc) ST_TRY(m->cutbuf.ensure((size_t)Rz * 8, st));
   sa.sess_tok = (int32_t* const*)(tb + o_ptok);
   sa.sess_lse = (float* const*)(tb + o_plse);
   sa.ld = V;
@@ -589,6 +609,12 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   sa.err = m->d_err;
   {
     Timed tm(m, kSample, (double)Rz * V * 4, 6.0 * Rz * V, st);
+    if (any_trunc) {
+      uint64_t* cut = m->cutbuf.as<uint64_t>();
+      launch_trunc_cut(sa, (const Trunc*)(tb + o_trunc), cut, (uint64_t* const*)(tb + o_pcut), st);
+      sa.cut = cut;
+      m->launches++;
+    }
     launch_sample_partials(sa, chunk, m->spart.as<float4>(), st);
     // tokens and log-sum-exp into the sessions, tokens and q(token) in caller order
     sa.out_map = (const int32_t*)(tb + o_map);
@@ -655,6 +681,12 @@ extern "C" {
 // Internal accessors for the allocation-free verify (verify_noalloc.cu);
 // hidden symbols, not part of the ABI.
 int dflash__set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+int dflash__session_truncation(const dflash_session* s, Trunc* trunc, const uint64_t** proposal_cut) {
+  *trunc = s->trunc;
+  *proposal_cut = s->last_trunc ? s->pcut : nullptr;
+  return DFLASH_OK;
+}
 
 int dflash__session_proposal(const dflash_session* s, const float** logits, const float** lse,
                              const int32_t** tokens, float* temperature, int32_t* n, long long** accepted,
@@ -748,7 +780,7 @@ int dflash_model_destroy(dflash_model* m) {
   for (auto& L : m->layers)
     if (L.w_qkvg) cudaFree(L.w_qkvg);
   Buf* bufs[] = {&m->tables, &m->u, &m->fcout, &m->c, &m->h, &m->x, &m->qkv, &m->rope, &m->Q, &m->G,
-                 &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart,
+                 &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart, &m->cutbuf,
                  &m->vbonus};
   for (Buf* b : bufs) b->release();
   m->ring.release();
@@ -806,6 +838,7 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->plogits, nb * c.vocab * 4);
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->plse, nb * 4);
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->ptok, nb * 4);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&s->pcut, nb * 8);
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->d_accepted, 8);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->d_accepted, 0, 8, s->stream);
   if (e == cudaSuccess && m->use_tc && c.head_dim == 128) {
@@ -823,6 +856,7 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
     cudaFree(s->plogits);
     cudaFree(s->plse);
     cudaFree(s->ptok);
+    cudaFree(s->pcut);
     cudaFree(s->d_accepted);
     cudaFree(s->d_maps);
     delete s;
@@ -962,6 +996,7 @@ int dflash_propose(dflash_session* const* s, int32_t batch, const int32_t* curre
     x->has_prop = true;
     x->last_n = n;
     x->last_T = temperature;
+    x->last_trunc = temperature > 0.f && x->trunc.top_k > 0;  // the forward drew it truncated
     x->rounds++;
     x->proposed += n;
     out_n[fw.sess_map[j]] = n;
@@ -990,6 +1025,9 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   std::vector<float> dT(batch);
   std::vector<long long*> acc(batch);
   std::vector<int32_t> seqv(batch);
+  std::vector<Trunc> trv(batch);
+  std::vector<const uint64_t*> dcut(batch);
+  bool any_trunc = false, any_dcut = false;
   for (int b = 0; b < batch; ++b) {
     dl[b] = s[b]->plogits;
     dlse[b] = s[b]->plse;
@@ -997,9 +1035,14 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
     dT[b] = s[b]->last_T;
     acc[b] = s[b]->d_accepted;
     seqv[b] = b;
+    trv[b] = s[b]->trunc;
+    dcut[b] = s[b]->last_trunc ? s[b]->pcut : nullptr;
+    any_trunc = any_trunc || (temperature > 0.f && trv[b].top_k > 0);
+    any_dcut = any_dcut || (temperature > 0.f && dcut[b]);
   }
   const size_t o_dl = tp.add(dl), o_dlse = tp.add(dlse), o_dtok = tp.add(dtok), o_dT = tp.add(dT), o_acc = tp.add(acc),
                o_seq = tp.add(seqv);
+  const size_t o_trunc = any_trunc ? tp.add(trv) : 0, o_dcut = any_dcut ? tp.add(dcut) : 0;
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
   const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
@@ -1020,6 +1063,12 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   sa.err = m->d_err;
   const double tbytes = (double)rows * V * (sa.in_bf16 ? 2 : 4) + (double)batch * V * 4;
   Timed tm(m, kVerify, tbytes, 4.0 * rows * V, st);
+  if (any_trunc) {
+    ST_TRY(m->cutbuf.ensure((size_t)rows * 8, st));
+    launch_trunc_cut(sa, (const Trunc*)(tb + o_trunc), m->cutbuf.as<uint64_t>(), nullptr, st);
+    sa.cut = m->cutbuf.as<uint64_t>();
+    m->launches++;
+  }
   launch_sample_partials(sa, chunk, m->vpart.as<float4>(), st);
   launch_sample_combine(sa, chunks, m->vpart.as<float4>(), amax, nullptr, lse, st);
   m->launches += 3;
@@ -1044,12 +1093,25 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   va.bonus = out_bonus;
   va.accepted_total = (long long* const*)(tb + o_acc);
   va.err = m->d_err;
+  va.cut_t = sa.cut;
+  va.dcut = any_dcut ? (const uint64_t* const*)(tb + o_dcut) : nullptr;
   const int bchunks = verify_bonus_chunks(V);
   ST_TRY(m->vbonus.ensure((size_t)batch * bchunks * sizeof(VerifyPart) + (size_t)batch * 4, st));
   va.rej = (int32_t*)(m->vbonus.as<char>() + (size_t)batch * bchunks * sizeof(VerifyPart));
   launch_verify_accept(va, m->vbonus.as<VerifyPart>(), st);
   m->launches += temperature > 0.f ? 1 : 0;
   return launch_check("verify");
+}
+
+int dflash_set_sampler(dflash_session* s, int32_t top_k, float top_p, float min_p) {
+  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+  if (top_k < 0 || top_k > kTruncMaxK) return fail(DFLASH_ERR_INVALID_ARG, "top_k %d outside [0, %d]", top_k, kTruncMaxK);
+  if (!(top_p > 0.f && top_p <= 1.f)) return fail(DFLASH_ERR_INVALID_ARG, "top_p outside (0, 1]");
+  if (!(min_p >= 0.f && min_p <= 1.f)) return fail(DFLASH_ERR_INVALID_ARG, "min_p outside [0, 1]");
+  if (top_k == 0 && (top_p < 1.f || min_p > 0.f))
+    return fail(DFLASH_ERR_INVALID_ARG, "top_p and min_p act inside a top_k of 1..%d", kTruncMaxK);
+  s->trunc = Trunc{top_k, top_p, min_p, 0};
+  return DFLASH_OK;
 }
 
 int dflash_close(dflash_session* s) {
@@ -1061,6 +1123,7 @@ int dflash_close(dflash_session* s) {
   cudaFree(s->plogits);
   cudaFree(s->plse);
   cudaFree(s->ptok);
+  cudaFree(s->pcut);
   cudaFree(s->d_accepted);
   cudaFree(s->d_maps);
   delete s;

@@ -112,7 +112,24 @@ struct SampleArgs {
   const float* const* seq_logits;  // [B] logits of the session's rows (NULL: logits + row * ld)
   int32_t* const* sess_tok;        // [B] also write the token of each row here
   float* const* sess_lse;          // [B] also write the log-sum-exp of each row here
+  // truncated distributions: row r keeps entry v iff order_key(l_v / T, v) >= cut[r]
+  // (NULL: every entry); the statistics and the draw then run over the kept entries
+  const uint64_t* cut;
 };
+
+// The sampler's truncation of one session's distributions: top_k (0: none,
+// else at most kTruncMaxK), then top_p and min_p inside the top_k.
+struct Trunc {
+  int32_t top_k;
+  float top_p, min_p;
+  int32_t pad;
+};
+constexpr int kTruncMaxK = 1024;
+// cut[row] for the rows of a.rows (session of a row: row / a.rows_per_seq,
+// with its Trunc in tr[]); sessions with top_k == 0 get cut 0.  Also into
+// sess_cut[b][row % rows_per_seq] when given.
+void launch_trunc_cut(const SampleArgs& a, const Trunc* tr, uint64_t* cut, uint64_t* const* sess_cut,
+                      cudaStream_t st);
 void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st);
 // Writes tok[row], q[row] (probability of the token at T), lse[row] (log-sum-exp of logits/T).
 void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, int32_t* tok, float* qtok,
@@ -138,6 +155,10 @@ struct VerifyArgs {
   long long* const* accepted_total;  // [B] -> running counter of each session
   int32_t* err;                 // bit 2: a draft token id outside [0, V)
   int32_t* rej;                 // [B] scratch: first rejected position (0: none)
+  // truncated distributions (NULL: full): the cut of each target row, and of
+  // each session's proposal rows (dcut[b] NULL: that proposal was not truncated)
+  const uint64_t* cut_t;        // [B][n+1]
+  const uint64_t* const* dcut;  // [B] -> [n]
 };
 // Bonus-draw partial of one vocabulary chunk of one session.
 struct VerifyPart {

@@ -467,6 +467,7 @@ __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ 
   const int b = row / a.rows_per_seq;
   const uint32_t prow = (uint32_t)(row % a.rows_per_seq + a.row_offset);
   const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
+  const uint64_t cutv = a.cut ? a.cut[row] : 0ull;
   float m = -INFINITY, l = 0.f;
   ArgMax best{-INFINITY, INT32_MAX};
   // four consecutive entries per thread: one Philox evaluation gives their
@@ -479,6 +480,7 @@ __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ 
       const int v = v4 + w;
       if (v >= v1) break;
       const float s = sample_logit(a, row, v) * invT;
+      if (cutv && order_key(s, v) < cutv) continue;  // outside the truncated support
       if (s > m) {
         l = l * expf(m - s) + 1.f;
         m = s;
@@ -558,6 +560,179 @@ __global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restr
   }
 }
 
+// ---------------------------------------------------------------------------
+// truncated distributions: the cut of each row
+// ---------------------------------------------------------------------------
+constexpr int kCutThreads = 1024;
+
+// Exclusive prefix sum over the CTA's threads in thread order; total gets the
+// sum.  sm holds 33 entries; every thread of the CTA must call it.
+template <typename T>
+__device__ __forceinline__ T block_scan_excl(T x, T* sm, T& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  T incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const T t = lane < nw ? sm[lane] : T(0);
+    T ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const T y = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += y;
+    }
+    if (lane < nw) sm[lane] = ti - t;
+    if (lane == 31) sm[32] = ti;
+  }
+  __syncthreads();
+  const T r = sm[w] + (incl - x);
+  total = sm[32];
+  __syncthreads();
+  return r;
+}
+
+// One CTA per row.  The k-th entry of the sampler's order (value descending,
+// then id) by radix select over the 32-bit value words: four 8-bit digits,
+// warp-private histograms with equal digits of a warp aggregated.  Then the
+// k candidates are gathered (ties at the k-th value by id, in id order),
+// sorted by key (bitonic), and top-p (the mass strictly before an entry
+// below top_p) and min-p (probability at least min_p times the largest) cut
+// the sorted list.  The cut is the key of the last entry kept; rows of a
+// session without truncation get 0, rows with no comparable entry ~0.
+__global__ void __launch_bounds__(kCutThreads) k_trunc_cut(SampleArgs a, const Trunc* __restrict__ tr,
+                                                            uint64_t* __restrict__ cut,
+                                                            uint64_t* const* __restrict__ sess_cut) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int hist[32][256];
+  __shared__ uint64_t cand[kTruncMaxK];
+  __shared__ int scan_i[33];
+  __shared__ float scan_f[33];
+  __shared__ int s_bin, s_above, s_eq, s_ncand;
+  const int row = blockIdx.x, b = row / a.rows_per_seq;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const Trunc t = tr[b];
+  const int V = a.V;
+  uint64_t result = 0ull;
+  if (t.top_k > 0) {
+    const float invT = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
+    uint32_t prefix = 0u, pmask = 0u;
+    int need = min(t.top_k, kTruncMaxK), kc = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = tid; i < 32 * 256; i += kCutThreads) (&hist[0][0])[i] = 0;
+      __syncthreads();
+      for (int v0 = 0; v0 < V; v0 += kCutThreads) {
+        const int v = v0 + tid;
+        const uint32_t o = v < V ? float_order(sample_logit(a, row, v) * invT) : 0u;
+        const bool act = o != 0u && (o & pmask) == prefix;
+        const unsigned am = __ballot_sync(0xffffffffu, act);
+        if (act) {
+          const uint32_t dg = (o >> shift) & 255u;
+          const unsigned peers = __match_any_sync(am, dg);
+          if (lane == __ffs(peers) - 1) atomicAdd(&hist[w][dg], __popc(peers));
+        }
+      }
+      __syncthreads();
+      // digit totals in descending digit order: thread j < 256 holds digit 255 - j
+      int c = 0;
+      if (tid < 256)
+        for (int q = 0; q < 32; ++q) c += hist[q][255 - tid];
+      int total = 0;
+      const int before = block_scan_excl(c, scan_i, total);
+      if (pass == 0) {
+        need = min(need, total);            // fewer comparable entries than k
+        kc = need;
+      }
+      if (need == 0) break;                 // uniform: nothing comparable in the row
+      if (tid < 256 && c > 0 && before < need && need <= before + c) {
+        s_bin = 255 - tid;
+        s_above = before;
+        s_eq = c;
+      }
+      __syncthreads();
+      need -= s_above;
+      prefix |= (uint32_t)s_bin << shift;
+      pmask |= 255u << shift;
+      __syncthreads();
+    }
+    if (kc == 0) {
+      result = ~0ull;
+    } else {
+      // gather: every entry above the k-th value, and the first `need` entries
+      // (by id) equal to it
+      const uint32_t tau = prefix;
+      const bool all_eq = need == s_eq;
+      if (tid == 0) s_ncand = 0;
+      __syncthreads();
+      int eq_base = 0;
+      for (int v0 = 0; v0 < V; v0 += kCutThreads) {
+        const int v = v0 + tid;
+        float sv = 0.f;
+        uint32_t o = 0u;
+        if (v < V) {
+          sv = sample_logit(a, row, v) * invT;
+          o = float_order(sv);
+        }
+        bool take = o > tau;
+        bool eq = o == tau;
+        if (!all_eq) {
+          int tot = 0;
+          const int r = block_scan_excl(eq ? 1 : 0, scan_i, tot);
+          eq = eq && eq_base + r < need;
+          eq_base += tot;
+        }
+        if (take || eq) {
+          const int at = atomicAdd(&s_ncand, 1);
+          if (at < kTruncMaxK) cand[at] = order_key(sv, v);
+        }
+      }
+      __syncthreads();
+      int P = 1;
+      while (P < kc) P <<= 1;
+      for (int i = kc + tid; i < P; i += kCutThreads) cand[i] = 0ull;
+      __syncthreads();
+      for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int i = tid; i < P; i += kCutThreads) {
+            const int j = i ^ stride;
+            if (j > i) {
+              const uint64_t x = cand[i], y = cand[j];
+              const bool desc = (i & size) == 0;
+              if (desc ? x < y : x > y) {
+                cand[i] = y;
+                cand[j] = x;
+              }
+            }
+          }
+          __syncthreads();
+        }
+      }
+      int J = kc;
+      if (t.top_p < 1.f || t.min_p > 0.f) {
+        const float m = float_of_order((uint32_t)(cand[0] >> 32));
+        const float e = tid < kc ? expf(float_of_order((uint32_t)(cand[tid] >> 32)) - m) : 0.f;
+        float Z = 0.f;
+        const float before = block_scan_excl(e, scan_f, Z);
+        bool keep = tid < kc;
+        if (t.top_p < 1.f) keep = keep && before < t.top_p * Z;
+        if (t.min_p > 0.f) keep = keep && e >= t.min_p;
+        J = __syncthreads_count(keep);
+      }
+      result = cand[max(J, 1) - 1];
+    }
+  }
+  if (tid == 0) {
+    cut[row] = result;
+    if (sess_cut) sess_cut[b][row % a.rows_per_seq] = result;
+  }
+}
+
 // Acceptance scan of one session (T > 0): the first i in 1..n whose draft
 // token fails u_i * q_i(d_i) < p_i(d_i), or 0 if all n pass.
 __device__ int verify_scan(const VerifyArgs& a, int b) {
@@ -569,16 +744,19 @@ __device__ int verify_scan(const VerifyArgs& a, int b) {
   const float* dl = a.dlogits[b];
   const float* dlse = a.dlse[b];
   const int32_t* dtok = a.dtok[b];
+  const uint64_t* dc = a.dcut ? a.dcut[b] : nullptr;
   for (int i = 1; i <= n; ++i) {
     int dtk = a.draft[b * n + i - 1];
     if (dtk < 0 || dtk >= V) {
       atomicOr(a.err, 2);
       dtk = 0;
     }
-    const float p = expf(load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT -
-                         a.lse_t[b * (n + 1) + i - 1]);
-    const float q = Tq > 0.f ? expf(dl[(int64_t)(i - 1) * V + dtk] / Tq - dlse[i - 1])
-                             : (dtk == dtok[i - 1] ? 1.f : 0.f);
+    const float st = load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT;
+    float p = expf(st - a.lse_t[b * (n + 1) + i - 1]);
+    if (a.cut_t && order_key(st, dtk) < a.cut_t[b * (n + 1) + i - 1]) p = 0.f;
+    const float dv = dl[(int64_t)(i - 1) * V + dtk];
+    float q = Tq > 0.f ? expf(dv / Tq - dlse[i - 1]) : (dtk == dtok[i - 1] ? 1.f : 0.f);
+    if (Tq > 0.f && dc && order_key(dv * (1.f / Tq), dtk) < dc[i - 1]) q = 0.f;
     const float r = uniform_open(rand_u32(a.seed, a.rnd, kStreamAccept, seq, (uint32_t)i, 0u));
     if (!(r * q < p)) return i;
   }
@@ -613,6 +791,9 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
   const int trow = rej ? rej - 1 : n;                 // target row of the bonus draw
   const uint32_t prow = rej ? (uint32_t)rej : (uint32_t)(n + 1);
   const float lse = a.lse_t[b * (n + 1) + trow];
+  const uint64_t cutt = a.cut_t ? a.cut_t[b * (n + 1) + trow] : 0ull;
+  const uint64_t* dc = a.dcut ? a.dcut[b] : nullptr;
+  const float invTq = Tq > 0.f ? 1.f / Tq : 1.f;
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   float rsum = 0.f;
   ArgMax bres{-INFINITY, INT32_MAX}, bp{-INFINITY, INT32_MAX};
@@ -622,13 +803,16 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
     for (int w = 0; w < 4; ++w) {
       const int v = v4 + w;
       if (v >= v1) break;
-      const float lp = load_logit(a.target, a.in_bf16, tbase + (int64_t)trow * V + v) * invT - lse;
+      const float st = load_logit(a.target, a.in_bf16, tbase + (int64_t)trow * V + v) * invT;
+      const float lp = st - lse;
+      const bool kept = !cutt || order_key(st, v) >= cutt;
       const float g = gumbel_of(word_of(rw, w));
-      bp = better(bp, ArgMax{lp + g, v});
+      if (kept) bp = better(bp, ArgMax{lp + g, v});
       if (rej) {
-        const float p = expf(lp);
-        const float q = Tq > 0.f ? expf(dl[(int64_t)(rej - 1) * V + v] / Tq - dlse[rej - 1])
-                                 : (v == dtok[rej - 1] ? 1.f : 0.f);
+        const float p = kept ? expf(lp) : 0.f;
+        const float dv = dl[(int64_t)(rej - 1) * V + v];
+        float q = Tq > 0.f ? expf(dv / Tq - dlse[rej - 1]) : (v == dtok[rej - 1] ? 1.f : 0.f);
+        if (Tq > 0.f && dc && order_key(dv * invTq, v) < dc[rej - 1]) q = 0.f;
         const float res = fmaxf(p - q, 0.f);
         rsum += res;
         if (res > 0.f) bres = better(bres, ArgMax{logf(res) + g, v});
@@ -817,6 +1001,12 @@ void launch_attention_combine(DT dt, const float* part, const int32_t* item_firs
   const int total = B * p.nrows * p.Hq;
   DFL_DISPATCH(dt, launch_k(k_attn_combine<T>, cdiv(total, 4), 128, 0, st, part, item_first, item_count, p, total, G,
                                                                       (T*)O));
+}
+
+void launch_trunc_cut(const SampleArgs& a, const Trunc* tr, uint64_t* cut, uint64_t* const* sess_cut,
+                      cudaStream_t st) {
+  if (a.rows <= 0) return;
+  launch_k(k_trunc_cut, a.rows, kCutThreads, 0, st, a, tr, cut, sess_cut);
 }
 
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld, int rows, int H, cudaStream_t st) {

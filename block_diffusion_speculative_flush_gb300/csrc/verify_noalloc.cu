@@ -28,6 +28,7 @@ extern "C" int dflash__session_proposal(const dflash_session* s, const float** l
                                         const int32_t** tokens, float* temperature, int32_t* n,
                                         long long** accepted, void** stream, int32_t* vocab, int32_t* draft_limit,
                                         int32_t** err, const void** model);
+extern "C" int dflash__session_truncation(const dflash_session* s, Trunc* trunc, const uint64_t** proposal_cut);
 extern "C" int dflash__set_error(int code, const char* msg);
 
 namespace {
@@ -91,6 +92,9 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   float dT[kMaxBatch];
   long long* acc[kMaxBatch];
   int32_t seq[kMaxBatch];
+  Trunc trv[kMaxBatch];
+  const uint64_t* dcut[kMaxBatch];
+  bool any_trunc = false, any_dcut = false;
   void* stream = nullptr;
   int32_t V = 0, limit = 0;
   int32_t* err = nullptr;
@@ -118,6 +122,9 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
       return dflash__set_error(DFLASH_ERR_STATE, msg);
     }
     seq[b] = b;
+    dflash__session_truncation(s[b], &trv[b], &dcut[b]);
+    any_trunc = any_trunc || (temperature > 0.f && trv[b].top_k > 0);
+    any_dcut = any_dcut || (temperature > 0.f && dcut[b]);
   }
   if (n < 1 || n > limit) return dflash__set_error(DFLASH_ERR_INVALID_ARG, "n out of range");
 
@@ -137,7 +144,13 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   off = up16(off + batch * sizeof(void*));
   const size_t o_seq = off;
   off = up16(off + batch * sizeof(int32_t));
+  const size_t o_trunc = off;
+  off = up16(off + batch * sizeof(Trunc));
+  const size_t o_dcut = off;
+  off = up16(off + batch * sizeof(void*));
   const size_t tables_end = off;
+  const size_t o_cut = off;
+  off = up16(off + (any_trunc ? (size_t)rows * sizeof(uint64_t) : 0));
   const size_t o_part = off;
   off = up16(off + (size_t)rows * chunks * sizeof(float4));
   const size_t o_amax = off;
@@ -162,14 +175,16 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   cudaStream_t st = (cudaStream_t)stream;
 
   // tables: one copy from a host staging block on the stack
-  alignas(16) char host[up16(kMaxBatch * sizeof(void*)) * 4 + up16(kMaxBatch * sizeof(float)) +
-                        up16(kMaxBatch * sizeof(int32_t))];
+  alignas(16) char host[up16(kMaxBatch * sizeof(void*)) * 5 + up16(kMaxBatch * sizeof(float)) +
+                        up16(kMaxBatch * sizeof(int32_t)) + up16(kMaxBatch * sizeof(Trunc))];
   memcpy(host + o_dl, dl, batch * sizeof(void*));
   memcpy(host + o_dlse, dlse, batch * sizeof(void*));
   memcpy(host + o_dtok, dtok, batch * sizeof(void*));
   memcpy(host + o_dT, dT, batch * sizeof(float));
   memcpy(host + o_acc, acc, batch * sizeof(void*));
   memcpy(host + o_seq, seq, batch * sizeof(int32_t));
+  memcpy(host + o_trunc, trv, batch * sizeof(Trunc));
+  memcpy(host + o_dcut, dcut, batch * sizeof(void*));
   // a copy from pageable memory returns only once the source has been read
   cudaError_t e = cudaMemcpyAsync(base, host, tables_end, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return dflash__set_error(DFLASH_ERR_CUDA, cudaGetErrorString(e));
@@ -190,6 +205,10 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   float4* part = (float4*)(base + o_part);
   int32_t* amax = (int32_t*)(base + o_amax);
   float* lse = (float*)(base + o_lse);
+  if (any_trunc) {
+    launch_trunc_cut(sa, (const Trunc*)(base + o_trunc), (uint64_t*)(base + o_cut), nullptr, st);
+    sa.cut = (const uint64_t*)(base + o_cut);
+  }
   launch_sample_partials(sa, kChunk, part, st);
   launch_sample_combine(sa, chunks, part, amax, nullptr, lse, st);
   VerifyArgs va{};
@@ -214,6 +233,8 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   va.accepted_total = (long long* const*)(base + o_acc);
   va.err = err;
   va.rej = (int32_t*)(base + o_rej);
+  va.cut_t = sa.cut;
+  va.dcut = any_dcut ? (const uint64_t* const*)(base + o_dcut) : nullptr;
   launch_verify_accept(va, (VerifyPart*)(base + o_bonus), st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return dflash__set_error(DFLASH_ERR_CUDA, cudaGetErrorString(e));

@@ -204,6 +204,18 @@ DFLASH_API int dflash_propose(dflash_session* const* s /*host [batch]*/, int32_t
                    int32_t max_tokens, float temperature, uint64_t seed, uint64_t round, int32_t* out_tokens,
                    float* out_q, float* out_logits, int32_t* out_n /*host*/);
 
+/* The session's sampler truncation (dflash.go selectBlock draws from the
+ * sampler's Distribution, whose IDs are the kept tokens).  At T > 0 the
+ * draft's draw and q, and verify's target p, use the truncated distribution:
+ * order a row of l/T by value (descending), then id; keep the first top_k;
+ * over those, keep an entry while the probability mass strictly before it is
+ * below top_p, and while its probability is at least min_p times the largest;
+ * renormalise over what is kept.  top_k in [0, 1024] (0: no truncation),
+ * top_p in (0, 1], min_p in [0, 1]; top_p < 1 or min_p > 0 need top_k >= 1.
+ * Else DFLASH_ERR_INVALID_ARG and nothing changes.  Takes effect at the next
+ * propose and verify; verify's q stays the one the proposal was drawn with. */
+DFLASH_API int dflash_set_sampler(dflash_session* s, int32_t top_k, float top_p, float min_p);
+
 /* Speculative verification of each session's last proposal.
  * target_logits [batch, n+1, V] (fp32 or bf16 per logits_dtype): row r
  * scores the token after [current, d_1..d_r].  draft_tokens [batch, n]: the
@@ -213,7 +225,8 @@ DFLASH_API int dflash_propose(dflash_session* const* s /*host [batch]*/, int32_t
  * at the first rejection the bonus is drawn from max(0, p_i - q_i) (from p_i
  * if that is all zero), after n acceptances from p of row n (stream 2).
  * q_i is the proposal's distribution softmax(l_i / T_propose) (one-hot of
- * the proposed token if that proposal was greedy).
+ * the proposed token if that proposal was greedy); with a truncating sampler
+ * (dflash_set_sampler) p and q are the truncated distributions.
  * Outputs: out_accept [batch] int32 in 0..n, out_bonus [batch] int32.
  * Errors: STATE if a session has no proposal with this n. */
 DFLASH_API int dflash_verify(dflash_session* const* s /*host [batch]*/, int32_t batch, const void* target_logits,
