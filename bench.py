@@ -58,11 +58,14 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["round", "flush", "laguna", "batched", "spec"], default="round",
+    ap.add_argument("--workload", choices=["round", "flush", "laguna", "batched", "spec", "truncated"],
+                    default="round",
                     help="round: the bs1 Qwen3-8B-shaped round (the default line); flush: 8 sequences x 256-row "
                          "context flushes; laguna: window-512 gated draft, bs1, blocks 16 and 8; batched: 64 "
                          "sequences, contexts 1k-16k, propose + rejection-sampling verify at T=0.7; spec: greedy "
-                         "speculative decoding with the tiny fp32 draft and the synthetic target, both on the GPU")
+                         "speculative decoding with the tiny fp32 draft and the synthetic target, both on the GPU; "
+                         "truncated: the bs1 round with a top-k 40 / top-p 0.9 sampler against the same round "
+                         "with full distributions")
     return ap.parse_args(argv)
 
 
@@ -529,6 +532,8 @@ def run_workload(args, rank, world, local_rank):
 
     if args.workload == "spec":
         return _spec_decode(args, world, local_rank, dev, stream, K, W)
+    if args.workload == "truncated":
+        return _truncated_round(args, world, local_rank, dev, stream, K, W, peaks, peak_kind)
 
     # batched serving mix
     cfg = S.CONFIGS[CFG_NAME]
@@ -583,6 +588,75 @@ def run_workload(args, rank, world, local_rank):
                                "ideal_ms_per_step": round(ideal * 1e3, 3), "frac": round(ideal / t_step, 4),
                                "gemm_tflop_per_step": round(gemm_flops / 1e12, 3),
                                "kv_gb_per_step": round(kv_bytes / 1e9, 2)}}, clk)
+
+
+def _truncated_round(args, world, local_rank, dev, stream, K, W, peaks, peak_kind):
+    """The bs1 Qwen3-8B-shaped round at T = 1 with the session's sampler
+    truncating to top-k 40 / top-p 0.9 (draft rows and target rows), timed
+    against the same round with full distributions, alternating on one box.
+    The truncation's own cost is the cut kernel (k_trunc_cut): one CTA per row
+    reads the row of logits five times (four radix passes and the gather),
+    from L2."""
+    import torch
+
+    import block_diffusion_speculative_flush_gb300 as D
+    import synthetic as S
+
+    cfg = S.CONFIGS[CFG_NAME]
+    n, V = cfg.block_size - 1, cfg.vocab
+    model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED, dev))
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 11)
+    start = CTX - P_ROWS * (W + K)
+    sess = {}
+    with torch.cuda.stream(stream):
+        for name in ("full", "trunc"):
+            s_ = D.dflash_open(model, max_ctx=start + P_ROWS * (2 * (W + K) + 8), stream=stream)
+            for lo in range(0, start, 1024):
+                f = torch.randn((min(start, lo + 1024) - lo, cfg.feature_width), generator=g,
+                                device=dev).to(torch.bfloat16)
+                D.dflash_committed(s_, f, lo)
+                del f
+            D.dflash_flush([s_])
+            sess[name] = s_
+        D.dflash_set_sampler(sess["trunc"], 40, 0.9, 0.0)
+        feats = torch.randn((W + K, P_ROWS, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+        tl = (torch.randn((1, n + 1, V), generator=g, device=dev) * 3.0).contiguous()
+        cur = torch.full((1,), 17, dtype=torch.int32, device=dev)
+        tok = torch.empty((1, n), dtype=torch.int32, device=dev)
+        q = torch.empty((1, n), dtype=torch.float32, device=dev)
+        acc = torch.empty(1, dtype=torch.int32, device=dev)
+        bon = torch.empty(1, dtype=torch.int32, device=dev)
+    res = {}
+    for name in ("full", "trunc", "full", "trunc"):          # alternate: two timed runs each
+        s_ = sess[name]
+        base = D.dflash_session_state(s_)[0] + D.dflash_session_state(s_)[1]
+
+        def step(i, s_=s_, base=base):
+            D.dflash_committed(s_, feats[i % (W + K)], base + P_ROWS * i)
+            D.dflash_propose([s_], cur, n, TEMP, SEED, i, tok, q)
+            D.dflash_verify([s_], tl, tok, n, TEMP, SEED, i, acc, bon)
+
+        ms, clk = _timed(torch, stream, step, K // 2, W, local_rank, world, dev)
+        # the W warm-up steps advanced the cursor too: base moves on for the next run
+        prev = res.get(name, (0.0, 0, None))
+        res[name] = (prev[0] + ms, prev[1] + K // 2, clk)
+    D.dflash_device_status(model)
+    for s_ in sess.values():
+        D.dflash_close(s_)
+    ms_t, k_t, clk = res["trunc"]
+    ms_f, k_f, _ = res["full"]
+    v_t, v_f = world * k_t / (ms_t * 1e-3), world * k_f / (ms_f * 1e-3)
+    rows = 2 * n + 1                                            # n proposal rows + n + 1 target rows
+    return _line("draft rounds/s (bs1 Qwen3-8B-shaped round, top-k 40 / top-p 0.9 sampler)", "draft rounds/s", v_t,
+                 world, k_t, W, ms_t, "bf16",
+                 {"workload": "qwen3_8b_bf16 draft round, bs1, block 16 (n=15), ctx ~4096, 4 committed rows per "
+                              "round, T=1.0, session sampler top_k 40, top_p 0.9 on the 15 draft rows and the 16 "
+                              "target rows [1,16,151936]", "l2": "no flush: 3.4 GB of weights streamed per step"},
+                 {"full_distribution_rounds_s": round(v_f, 2),
+                  "truncation_cost_us_per_round": round((ms_t / k_t - ms_f / k_f) * 1e3, 2),
+                  "cut_rows_per_round": rows,
+                  "cut_algorithmic_bytes_per_round": rows * V * 4}, clk)
 
 
 def _spec_decode(args, world, local_rank, dev, stream, K, W):

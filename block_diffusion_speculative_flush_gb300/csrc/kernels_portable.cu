@@ -21,6 +21,8 @@
 #include <cstring>
 #include <type_traits>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.h"
@@ -563,7 +565,56 @@ __global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restr
 // ---------------------------------------------------------------------------
 // truncated distributions: the cut of each row
 // ---------------------------------------------------------------------------
-constexpr int kCutThreads = 1024;
+constexpr int kCutThreads = 512;
+constexpr int kCutWarps = kCutThreads / 32;
+constexpr int kCutPer = kTruncMaxK / kCutThreads;  // sorted candidates per thread in the top-p scan
+constexpr int kCutQuads = 4;    // quads of entries in flight per thread in each pass over a row
+constexpr int kCutCluster = 8;  // CTAs per row
+
+// One row of logits for the cut kernel, read four entries at a time (one
+// 16-byte fp32 or 8-byte bf16 load when the row is aligned and V % 4 == 0).
+struct RowRef {
+  const void* p;
+  int bf;
+  bool vec;
+};
+__device__ __forceinline__ RowRef row_ref(const SampleArgs& a, int row) {
+  RowRef r{nullptr, 0, false};
+  if (a.seq_logits) {
+    r.p = a.seq_logits[row / a.rows_per_seq] + (int64_t)(row % a.rows_per_seq) * a.ld;
+  } else {
+    r.bf = a.in_bf16;
+    r.p = r.bf ? (const void*)((const bf16*)a.logits + (int64_t)row * a.ld)
+               : (const void*)((const float*)a.logits + (int64_t)row * a.ld);
+  }
+  r.vec = (a.V & 3) == 0 && ((uintptr_t)r.p & (r.bf ? 7u : 15u)) == 0;
+  return r;
+}
+// Entries 4g..4g+3 scaled by invT (the same product as the draw's); entries
+// at or past V read as NaN, which is never comparable.
+__device__ __forceinline__ void load_quad(const RowRef& r, int g, int V, float invT, float x[4]) {
+  const int v = 4 * g;
+  if (r.vec && v < V) {
+    if (r.bf) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(r.p) + g);
+      x[0] = __uint_as_float(w.x << 16) * invT;
+      x[1] = __uint_as_float(w.x & 0xffff0000u) * invT;
+      x[2] = __uint_as_float(w.y << 16) * invT;
+      x[3] = __uint_as_float(w.y & 0xffff0000u) * invT;
+    } else {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(r.p) + g);
+      x[0] = f.x * invT;
+      x[1] = f.y * invT;
+      x[2] = f.z * invT;
+      x[3] = f.w * invT;
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    x[k] = v + k < V ? (r.bf ? __bfloat162float(((const bf16*)r.p)[v + k]) : ((const float*)r.p)[v + k]) * invT
+                     : __int_as_float(0x7fc00000);
+}
 
 // Exclusive prefix sum over the CTA's threads in thread order; total gets the
 // sum.  sm holds 33 entries; every thread of the CTA must call it.
@@ -596,138 +647,224 @@ __device__ __forceinline__ T block_scan_excl(T x, T* sm, T& total) {
   return r;
 }
 
-// One CTA per row.  The k-th entry of the sampler's order (value descending,
-// then id) by radix select over the 32-bit value words: four 8-bit digits,
-// warp-private histograms with equal digits of a warp aggregated.  Then the
-// k candidates are gathered (ties at the k-th value by id, in id order),
-// sorted by key (bitonic), and top-p (the mass strictly before an entry
-// below top_p) and min-p (probability at least min_p times the largest) cut
-// the sorted list.  The cut is the key of the last entry kept; rows of a
-// session without truncation get 0, rows with no comparable entry ~0.
-__global__ void __launch_bounds__(kCutThreads) k_trunc_cut(SampleArgs a, const Trunc* __restrict__ tr,
+// A cluster of kCutCluster CTAs per row, each over a contiguous slice.  The
+// k-th entry of the sampler's order (value descending, then id) is found by
+// radix select over the 32-bit value words: four 8-bit digits, each CTA
+// counting its slice in warp-private histograms (equal digits of a warp
+// aggregated), every CTA summing the cluster's counts through distributed
+// shared memory and taking the same digit.  The k candidates are then
+// gathered into the first CTA (ties at the k-th value by id, in id order
+// across the slices), sorted by key (bitonic), and top-p (the mass strictly
+// before an entry below top_p) and min-p (probability at least min_p times
+// the largest) cut the sorted list.  The cut is the key of the last entry
+// kept; rows of a session without truncation get 0, rows with no comparable
+// entry ~0.  Every CTA of a cluster takes the same branches.
+__global__ void __launch_bounds__(kCutThreads, 2) k_trunc_cut(SampleArgs a, const Trunc* __restrict__ tr,
                                                             uint64_t* __restrict__ cut,
                                                             uint64_t* const* __restrict__ sess_cut) {
   pdl_trigger();
   pdl_wait();
-  __shared__ int hist[32][256];
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  __shared__ int hist[kCutWarps][256];
+  __shared__ int tot[2][256];  // this CTA's digit counts, double-buffered by pass
   __shared__ uint64_t cand[kTruncMaxK];
   __shared__ int scan_i[33];
   __shared__ float scan_f[33];
-  __shared__ int s_bin, s_above, s_eq, s_ncand;
-  const int row = blockIdx.x, b = row / a.rows_per_seq;
+  __shared__ int s_bin, s_above, s_eq, s_ncand, s_eqbase;
+  const int C = (int)cl.num_blocks(), cr = (int)cl.block_rank();
+  const int row = blockIdx.x / C, b = row / a.rows_per_seq;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const Trunc t = tr[b];
   const int V = a.V;
-  uint64_t result = 0ull;
-  if (t.top_k > 0) {
-    const float invT = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
-    uint32_t prefix = 0u, pmask = 0u;
-    int need = min(t.top_k, kTruncMaxK), kc = 0;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      for (int i = tid; i < 32 * 256; i += kCutThreads) (&hist[0][0])[i] = 0;
-      __syncthreads();
-      for (int v0 = 0; v0 < V; v0 += kCutThreads) {
-        const int v = v0 + tid;
-        const uint32_t o = v < V ? float_order(sample_logit(a, row, v) * invT) : 0u;
-        const bool act = o != 0u && (o & pmask) == prefix;
-        const unsigned am = __ballot_sync(0xffffffffu, act);
-        if (act) {
-          const uint32_t dg = (o >> shift) & 255u;
-          const unsigned peers = __match_any_sync(am, dg);
-          if (lane == __ffs(peers) - 1) atomicAdd(&hist[w][dg], __popc(peers));
-        }
-      }
-      __syncthreads();
-      // digit totals in descending digit order: thread j < 256 holds digit 255 - j
-      int c = 0;
-      if (tid < 256)
-        for (int q = 0; q < 32; ++q) c += hist[q][255 - tid];
-      int total = 0;
-      const int before = block_scan_excl(c, scan_i, total);
-      if (pass == 0) {
-        need = min(need, total);            // fewer comparable entries than k
-        kc = need;
-      }
-      if (need == 0) break;                 // uniform: nothing comparable in the row
-      if (tid < 256 && c > 0 && before < need && need <= before + c) {
-        s_bin = 255 - tid;
-        s_above = before;
-        s_eq = c;
-      }
-      __syncthreads();
-      need -= s_above;
-      prefix |= (uint32_t)s_bin << shift;
-      pmask |= 255u << shift;
-      __syncthreads();
+  if (t.top_k <= 0) {
+    if (cr == 0 && tid == 0) {
+      cut[row] = 0ull;
+      if (sess_cut) sess_cut[b][row % a.rows_per_seq] = 0ull;
     }
-    if (kc == 0) {
-      result = ~0ull;
-    } else {
-      // gather: every entry above the k-th value, and the first `need` entries
-      // (by id) equal to it
-      const uint32_t tau = prefix;
-      const bool all_eq = need == s_eq;
-      if (tid == 0) s_ncand = 0;
-      __syncthreads();
-      int eq_base = 0;
-      for (int v0 = 0; v0 < V; v0 += kCutThreads) {
-        const int v = v0 + tid;
-        float sv = 0.f;
-        uint32_t o = 0u;
-        if (v < V) {
-          sv = sample_logit(a, row, v) * invT;
-          o = float_order(sv);
-        }
-        bool take = o > tau;
-        bool eq = o == tau;
-        if (!all_eq) {
-          int tot = 0;
-          const int r = block_scan_excl(eq ? 1 : 0, scan_i, tot);
-          eq = eq && eq_base + r < need;
-          eq_base += tot;
-        }
-        if (take || eq) {
-          const int at = atomicAdd(&s_ncand, 1);
-          if (at < kTruncMaxK) cand[at] = order_key(sv, v);
+    return;
+  }
+  if (tid == 0) s_ncand = 0;
+  const float invT = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
+  const RowRef rr = row_ref(a, row);
+  const int G = (V + 3) >> 2;
+  const int glo = (int)((int64_t)G * cr / C), ghi = (int)((int64_t)G * (cr + 1) / C);
+  uint32_t prefix = 0u, pmask = 0u;
+  int need = min(t.top_k, kTruncMaxK), kc = 0;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass, buf = pass & 1;
+    for (int i = tid; i < kCutWarps * 256; i += kCutThreads) (&hist[0][0])[i] = 0;
+    __syncthreads();
+    for (int g0 = glo; g0 < ghi; g0 += kCutThreads * kCutQuads) {
+      float x[kCutQuads][4];
+#pragma unroll
+      for (int u = 0; u < kCutQuads; ++u) {
+        const int g = g0 + u * kCutThreads + tid;
+        if (g < ghi) {
+          load_quad(rr, g, V, invT, x[u]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) x[u][k] = __int_as_float(0x7fc00000);
         }
       }
-      __syncthreads();
-      int P = 1;
-      while (P < kc) P <<= 1;
-      for (int i = kc + tid; i < P; i += kCutThreads) cand[i] = 0ull;
-      __syncthreads();
-      for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int i = tid; i < P; i += kCutThreads) {
-            const int j = i ^ stride;
-            if (j > i) {
-              const uint64_t x = cand[i], y = cand[j];
-              const bool desc = (i & size) == 0;
-              if (desc ? x < y : x > y) {
-                cand[i] = y;
-                cand[j] = x;
-              }
-            }
+#pragma unroll
+      for (int u = 0; u < kCutQuads; ++u)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t o = float_order(x[u][k]);
+          const bool act = o != 0u && (o & pmask) == prefix;
+          const unsigned am = __ballot_sync(0xffffffffu, act);
+          if (act) {
+            const uint32_t dg = (o >> shift) & 255u;
+            const unsigned peers = __match_any_sync(am, dg);
+            if (lane == __ffs(peers) - 1) atomicAdd(&hist[w][dg], __popc(peers));
           }
-          __syncthreads();
+        }
+    }
+    __syncthreads();
+    if (tid < 256) {
+      int c = 0;
+      for (int q = 0; q < kCutWarps; ++q) c += hist[q][tid];
+      tot[buf][tid] = c;
+    }
+    cl.sync();  // every CTA's counts of this pass are visible
+    // the cluster's counts in descending digit order: thread j < 256 holds digit 255 - j
+    int c = 0;
+    if (tid < 256)
+      for (int r = 0; r < C; ++r) c += cl.map_shared_rank(&tot[buf][0], r)[255 - tid];
+    int total = 0;
+    const int before = block_scan_excl(c, scan_i, total);
+    if (pass == 0) {
+      need = min(need, total);  // fewer comparable entries than k
+      kc = need;
+    }
+    if (need == 0) break;       // the same in every CTA: nothing comparable in the row
+    if (tid < 256 && c > 0 && before < need && need <= before + c) {
+      s_bin = 255 - tid;
+      s_above = before;
+      s_eq = c;
+    }
+    __syncthreads();
+    need -= s_above;
+    prefix |= (uint32_t)s_bin << shift;
+    pmask |= 255u << shift;
+    if (pass == 3 && tid == 0) {
+      // entries equal to the k-th value in the slices before this one
+      int eb = 0;
+      for (int r = 0; r < cr; ++r) eb += cl.map_shared_rank(&tot[buf][0], r)[s_bin];
+      s_eqbase = eb;
+    }
+    __syncthreads();
+  }
+  cl.sync();  // no CTA reads another's counts after this
+  if (kc == 0) {
+    if (cr == 0 && tid == 0) {
+      cut[row] = ~0ull;
+      if (sess_cut) sess_cut[b][row % a.rows_per_seq] = ~0ull;
+    }
+    return;
+  }
+  {
+    // gather into the first CTA: every entry above the k-th value, and the
+    // first `need` entries (by id) equal to it
+    const uint32_t tau = prefix;
+    const bool all_eq = need == s_eq;
+    int* ncand0 = cl.map_shared_rank(&s_ncand, 0);
+    uint64_t* cand0 = cl.map_shared_rank(&cand[0], 0);
+    int eq_base = s_eqbase;
+    for (int g0 = glo; g0 < ghi; g0 += kCutThreads * kCutQuads) {
+      float x[kCutQuads][4];
+#pragma unroll
+      for (int u = 0; u < kCutQuads; ++u) {
+        const int g = g0 + u * kCutThreads + tid;
+        if (g < ghi) {
+          load_quad(rr, g, V, invT, x[u]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) x[u][k] = __int_as_float(0x7fc00000);
         }
       }
-      int J = kc;
-      if (t.top_p < 1.f || t.min_p > 0.f) {
-        const float m = float_of_order((uint32_t)(cand[0] >> 32));
-        const float e = tid < kc ? expf(float_of_order((uint32_t)(cand[tid] >> 32)) - m) : 0.f;
-        float Z = 0.f;
-        const float before = block_scan_excl(e, scan_f, Z);
-        bool keep = tid < kc;
-        if (t.top_p < 1.f) keep = keep && before < t.top_p * Z;
-        if (t.min_p > 0.f) keep = keep && e >= t.min_p;
-        J = __syncthreads_count(keep);
+      // each u covers 4 * kCutThreads consecutive ids, thread by thread, in
+      // increasing id order
+#pragma unroll
+      for (int u = 0; u < kCutQuads; ++u) {
+        const int g = g0 + u * kCutThreads + tid;
+        int rank = 0;
+        if (!all_eq) {
+          int neq = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) neq += float_order(x[u][k]) == tau;
+          int tot_eq = 0;
+          rank = eq_base + block_scan_excl(neq, scan_i, tot_eq);
+          eq_base += tot_eq;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t o = float_order(x[u][k]);
+          bool take = o > tau;
+          if (o == tau) take = all_eq || rank++ < need;
+          if (take) {
+            const int at = atomicAdd(ncand0, 1);
+            if (at < kTruncMaxK) cand0[at] = order_key(x[u][k], 4 * g + k);
+          }
+        }
       }
-      result = cand[max(J, 1) - 1];
     }
   }
+  cl.sync();  // the candidates are in the first CTA
+  if (cr != 0) return;
+  int P = 1;
+  while (P < kc) P <<= 1;
+  for (int i = kc + tid; i < P; i += kCutThreads) cand[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += kCutThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const uint64_t x = cand[i], y = cand[j];
+          const bool desc = (i & size) == 0;
+          if (desc ? x < y : x > y) {
+            cand[i] = y;
+            cand[j] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  int J = kc;
+  if (t.top_p < 1.f || t.min_p > 0.f) {
+    // thread i holds sorted entries kCutPer*i .. kCutPer*i + kCutPer-1
+    const float m = float_of_order((uint32_t)(cand[0] >> 32));
+    float e[kCutPer];
+    float local = 0.f;
+#pragma unroll
+    for (int k = 0; k < kCutPer; ++k) {
+      const int j = kCutPer * tid + k;
+      e[k] = j < kc ? expf(float_of_order((uint32_t)(cand[j] >> 32)) - m) : 0.f;
+    }
+    // the in-thread sum in entry order, then the scan across threads
+#pragma unroll
+    for (int k = 0; k < kCutPer; ++k) local += e[k];
+    float Z = 0.f;
+    float before = block_scan_excl(local, scan_f, Z);
+    int kept = 0;
+#pragma unroll
+    for (int k = 0; k < kCutPer; ++k) {
+      const int j = kCutPer * tid + k;
+      bool keep = j < kc;
+      if (t.top_p < 1.f) keep = keep && before < t.top_p * Z;
+      if (t.min_p > 0.f) keep = keep && e[k] >= t.min_p;
+      kept += keep;
+      before += e[k];
+    }
+    int total = 0;
+    (void)block_scan_excl(kept, scan_i, total);
+    J = total;
+  }
   if (tid == 0) {
+    const uint64_t result = cand[max(J, 1) - 1];
     cut[row] = result;
     if (sess_cut) sess_cut[b][row % a.rows_per_seq] = result;
   }
@@ -1006,7 +1143,12 @@ void launch_attention_combine(DT dt, const float* part, const int32_t* item_firs
 void launch_trunc_cut(const SampleArgs& a, const Trunc* tr, uint64_t* cut, uint64_t* const* sess_cut,
                       cudaStream_t st) {
   if (a.rows <= 0) return;
-  launch_k(k_trunc_cut, a.rows, kCutThreads, 0, st, a, tr, cut, sess_cut);
+  // a cluster of kCutCluster CTAs per row; one CTA per row if that launch is refused
+  if (launch_kc(k_trunc_cut, dim3(a.rows * kCutCluster), dim3(kCutThreads), 0, st, kCutCluster, a, tr, cut,
+                sess_cut) != cudaSuccess) {
+    (void)cudaGetLastError();
+    launch_k(k_trunc_cut, a.rows, kCutThreads, 0, st, a, tr, cut, sess_cut);
+  }
 }
 
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld, int rows, int H, cudaStream_t st) {
