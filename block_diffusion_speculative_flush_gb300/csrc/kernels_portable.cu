@@ -565,11 +565,16 @@ __global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restr
 // ---------------------------------------------------------------------------
 // truncated distributions: the cut of each row
 // ---------------------------------------------------------------------------
-constexpr int kCutThreads = 512;
-constexpr int kCutWarps = kCutThreads / 32;
-constexpr int kCutPer = kTruncMaxK / kCutThreads;  // sorted candidates per thread in the top-p scan
-constexpr int kCutQuads = 4;    // quads of entries in flight per thread in each pass over a row
-constexpr int kCutCluster = 8;  // CTAs per row
+// The cut kernel runs a cluster of CTAs per row.  Rows up to
+// kCutRegQuads * 4 * kCutThreads * kCutMaxCluster entries are read once into
+// registers (kCutRegQuads quads per thread) and every pass runs on them; longer
+// rows are streamed from memory in every pass by a cluster of kCutCluster CTAs.
+constexpr int kCutThreads = 1024;
+constexpr int kCutRegQuads = 5;
+constexpr int kCutMaxCluster = 8;
+constexpr int kCutStreamThreads = 512;
+constexpr int kCutQuads = 4;    // quads in flight per thread in each streamed pass
+constexpr int kCutCluster = 8;  // CTAs per row when streaming
 
 // One row of logits for the cut kernel, read four entries at a time (one
 // 16-byte fp32 or 8-byte bf16 load when the row is aligned and V % 4 == 0).
@@ -647,26 +652,49 @@ __device__ __forceinline__ T block_scan_excl(T x, T* sm, T& total) {
   return r;
 }
 
-// A cluster of kCutCluster CTAs per row, each over a contiguous slice.  The
+// Histogram update of one entry's order word: digit (o >> shift) & 255 of
+// the entries that match the prefix so far, equal digits of a warp
+// aggregated into one atomic on the warp's private histogram.
+__device__ __forceinline__ void hist_add(int (*hist)[256], int w, int lane, uint32_t o, uint32_t pmask,
+                                         uint32_t prefix, int shift) {
+  const bool act = o != 0u && (o & pmask) == prefix;
+  const unsigned am = __ballot_sync(0xffffffffu, act);
+  if (act) {
+    const uint32_t dg = (o >> shift) & 255u;
+    const unsigned peers = __match_any_sync(am, dg);
+    if (lane == __ffs(peers) - 1) atomicAdd(&hist[w][dg], __popc(peers));
+  }
+}
+
+__device__ __forceinline__ uint64_t key_of_order(uint32_t o, int v) {
+  return ((uint64_t)o << 32) | (uint64_t)(0xffffffffu - (uint32_t)v);
+}
+
+// A cluster of CTAs per row, each over a contiguous slice of the row.  The
 // k-th entry of the sampler's order (value descending, then id) is found by
-// radix select over the 32-bit value words: four 8-bit digits, each CTA
-// counting its slice in warp-private histograms (equal digits of a warp
-// aggregated), every CTA summing the cluster's counts through distributed
-// shared memory and taking the same digit.  The k candidates are then
-// gathered into the first CTA (ties at the k-th value by id, in id order
-// across the slices), sorted by key (bitonic), and top-p (the mass strictly
-// before an entry below top_p) and min-p (probability at least min_p times
-// the largest) cut the sorted list.  The cut is the key of the last entry
-// kept; rows of a session without truncation get 0, rows with no comparable
-// entry ~0.  Every CTA of a cluster takes the same branches.
-__global__ void __launch_bounds__(kCutThreads, 2) k_trunc_cut(SampleArgs a, const Trunc* __restrict__ tr,
-                                                            uint64_t* __restrict__ cut,
-                                                            uint64_t* const* __restrict__ sess_cut) {
+// radix select over the 32-bit order words: four 8-bit digits, each CTA
+// counting its slice in warp-private histograms, every CTA summing the
+// cluster's counts through distributed shared memory (double-buffered by
+// pass, one cluster barrier per pass) and taking the same digit.  The k
+// candidates are gathered into the first CTA (ties at the k-th value by id,
+// in id order across the slices), sorted by key (bitonic), and top-p (the
+// mass strictly before an entry below top_p) and min-p (probability at least
+// min_p times the largest) cut the sorted list.  The cut is the key of the
+// last entry kept; rows of a session without truncation get 0, rows with no
+// comparable entry ~0.  Every CTA of a cluster takes the same branches.
+// RQ > 0: the slice is RQ quads per thread, read once into registers;
+// RQ == 0: the slice is streamed from memory in every pass.
+template <int THREADS, int RQ>
+__global__ void __launch_bounds__(THREADS, 1) k_trunc_cut(SampleArgs a, const Trunc* __restrict__ tr,
+                                                         uint64_t* __restrict__ cut,
+                                                         uint64_t* const* __restrict__ sess_cut) {
+  constexpr int NW = THREADS / 32;
+  constexpr int PER = kTruncMaxK / THREADS;  // sorted candidates per thread in the top-p scan
   pdl_trigger();
   pdl_wait();
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
-  __shared__ int hist[kCutWarps][256];
+  __shared__ int hist[NW][256];
   __shared__ int tot[2][256];  // this CTA's digit counts, double-buffered by pass
   __shared__ uint64_t cand[kTruncMaxK];
   __shared__ int scan_i[33];
@@ -688,43 +716,74 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_trunc_cut(SampleArgs a, cons
   const float invT = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
   const RowRef rr = row_ref(a, row);
   const int G = (V + 3) >> 2;
-  const int glo = (int)((int64_t)G * cr / C), ghi = (int)((int64_t)G * (cr + 1) / C);
+  int glo, ghi;
+  if constexpr (RQ > 0) {
+    glo = cr * THREADS * RQ;
+    ghi = min(G, glo + THREADS * RQ);
+  } else {
+    glo = (int)((int64_t)G * cr / C);
+    ghi = (int)((int64_t)G * (cr + 1) / C);
+  }
+  uint32_t ro[RQ > 0 ? RQ : 1][4];
+  if constexpr (RQ > 0) {
+#pragma unroll
+    for (int u = 0; u < RQ; ++u) {
+      const int g = glo + u * THREADS + tid;
+      float x[4];
+      if (g < ghi) {
+        load_quad(rr, g, V, invT, x);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = __int_as_float(0x7fc00000);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ro[u][k] = float_order(x[k]);
+    }
+  }
+  // the order words of streamed quads g0 + u * THREADS + tid, u < kCutQuads
+  auto stream_in = [&](int g0, uint32_t (&o)[kCutQuads][4]) {
+    float x[kCutQuads][4];
+#pragma unroll
+    for (int u = 0; u < kCutQuads; ++u) {
+      const int g = g0 + u * THREADS + tid;
+      if (g < ghi) {
+        load_quad(rr, g, V, invT, x[u]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[u][k] = __int_as_float(0x7fc00000);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCutQuads; ++u)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[u][k] = float_order(x[u][k]);
+  };
+
   uint32_t prefix = 0u, pmask = 0u;
   int need = min(t.top_k, kTruncMaxK), kc = 0;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass, buf = pass & 1;
-    for (int i = tid; i < kCutWarps * 256; i += kCutThreads) (&hist[0][0])[i] = 0;
+    for (int i = tid; i < NW * 256; i += THREADS) (&hist[0][0])[i] = 0;
     __syncthreads();
-    for (int g0 = glo; g0 < ghi; g0 += kCutThreads * kCutQuads) {
-      float x[kCutQuads][4];
+    if constexpr (RQ > 0) {
 #pragma unroll
-      for (int u = 0; u < kCutQuads; ++u) {
-        const int g = g0 + u * kCutThreads + tid;
-        if (g < ghi) {
-          load_quad(rr, g, V, invT, x[u]);
-        } else {
+      for (int u = 0; u < RQ; ++u)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) x[u][k] = __int_as_float(0x7fc00000);
-        }
+        for (int k = 0; k < 4; ++k) hist_add(hist, w, lane, ro[u][k], pmask, prefix, shift);
+    } else {
+      for (int g0 = glo; g0 < ghi; g0 += THREADS * kCutQuads) {
+        uint32_t o[kCutQuads][4];
+        stream_in(g0, o);
+#pragma unroll
+        for (int u = 0; u < kCutQuads; ++u)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) hist_add(hist, w, lane, o[u][k], pmask, prefix, shift);
       }
-#pragma unroll
-      for (int u = 0; u < kCutQuads; ++u)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t o = float_order(x[u][k]);
-          const bool act = o != 0u && (o & pmask) == prefix;
-          const unsigned am = __ballot_sync(0xffffffffu, act);
-          if (act) {
-            const uint32_t dg = (o >> shift) & 255u;
-            const unsigned peers = __match_any_sync(am, dg);
-            if (lane == __ffs(peers) - 1) atomicAdd(&hist[w][dg], __popc(peers));
-          }
-        }
     }
     __syncthreads();
     if (tid < 256) {
       int c = 0;
-      for (int q = 0; q < kCutWarps; ++q) c += hist[q][tid];
+      for (int q = 0; q < NW; ++q) c += hist[q][tid];
       tot[buf][tid] = c;
     }
     cl.sync();  // every CTA's counts of this pass are visible
@@ -766,48 +825,42 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_trunc_cut(SampleArgs a, cons
   }
   {
     // gather into the first CTA: every entry above the k-th value, and the
-    // first `need` entries (by id) equal to it
+    // first `need` entries (by id) equal to it.  Each group of THREADS quads
+    // holds 4 * THREADS consecutive ids, thread by thread.
     const uint32_t tau = prefix;
     const bool all_eq = need == s_eq;
     int* ncand0 = cl.map_shared_rank(&s_ncand, 0);
     uint64_t* cand0 = cl.map_shared_rank(&cand[0], 0);
     int eq_base = s_eqbase;
-    for (int g0 = glo; g0 < ghi; g0 += kCutThreads * kCutQuads) {
-      float x[kCutQuads][4];
+    auto take_quad = [&](const uint32_t (&o)[4], int g) {
+      int rank = 0;
+      if (!all_eq) {
+        int neq = 0;
 #pragma unroll
-      for (int u = 0; u < kCutQuads; ++u) {
-        const int g = g0 + u * kCutThreads + tid;
-        if (g < ghi) {
-          load_quad(rr, g, V, invT, x[u]);
-        } else {
+        for (int k = 0; k < 4; ++k) neq += o[k] == tau;
+        int tot_eq = 0;
+        rank = eq_base + block_scan_excl(neq, scan_i, tot_eq);
+        eq_base += tot_eq;
+      }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) x[u][k] = __int_as_float(0x7fc00000);
+      for (int k = 0; k < 4; ++k) {
+        bool take = o[k] > tau;
+        if (o[k] == tau) take = all_eq || rank++ < need;
+        if (take) {
+          const int at = atomicAdd(ncand0, 1);
+          if (at < kTruncMaxK) cand0[at] = key_of_order(o[k], 4 * g + k);
         }
       }
-      // each u covers 4 * kCutThreads consecutive ids, thread by thread, in
-      // increasing id order
+    };
+    if constexpr (RQ > 0) {
 #pragma unroll
-      for (int u = 0; u < kCutQuads; ++u) {
-        const int g = g0 + u * kCutThreads + tid;
-        int rank = 0;
-        if (!all_eq) {
-          int neq = 0;
+      for (int u = 0; u < RQ; ++u) take_quad(ro[u], glo + u * THREADS + tid);
+    } else {
+      for (int g0 = glo; g0 < ghi; g0 += THREADS * kCutQuads) {
+        uint32_t o[kCutQuads][4];
+        stream_in(g0, o);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) neq += float_order(x[u][k]) == tau;
-          int tot_eq = 0;
-          rank = eq_base + block_scan_excl(neq, scan_i, tot_eq);
-          eq_base += tot_eq;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t o = float_order(x[u][k]);
-          bool take = o > tau;
-          if (o == tau) take = all_eq || rank++ < need;
-          if (take) {
-            const int at = atomicAdd(ncand0, 1);
-            if (at < kTruncMaxK) cand0[at] = order_key(x[u][k], 4 * g + k);
-          }
-        }
+        for (int u = 0; u < kCutQuads; ++u) take_quad(o[u], g0 + u * THREADS + tid);
       }
     }
   }
@@ -815,11 +868,11 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_trunc_cut(SampleArgs a, cons
   if (cr != 0) return;
   int P = 1;
   while (P < kc) P <<= 1;
-  for (int i = kc + tid; i < P; i += kCutThreads) cand[i] = 0ull;
+  for (int i = kc + tid; i < P; i += THREADS) cand[i] = 0ull;
   __syncthreads();
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P; i += kCutThreads) {
+      for (int i = tid; i < P; i += THREADS) {
         const int j = i ^ stride;
         if (j > i) {
           const uint64_t x = cand[i], y = cand[j];
@@ -835,24 +888,22 @@ __global__ void __launch_bounds__(kCutThreads, 2) k_trunc_cut(SampleArgs a, cons
   }
   int J = kc;
   if (t.top_p < 1.f || t.min_p > 0.f) {
-    // thread i holds sorted entries kCutPer*i .. kCutPer*i + kCutPer-1
+    // thread i holds sorted entries PER*i .. PER*i + PER-1
     const float m = float_of_order((uint32_t)(cand[0] >> 32));
-    float e[kCutPer];
+    float e[PER];
     float local = 0.f;
 #pragma unroll
-    for (int k = 0; k < kCutPer; ++k) {
-      const int j = kCutPer * tid + k;
+    for (int k = 0; k < PER; ++k) {
+      const int j = PER * tid + k;
       e[k] = j < kc ? expf(float_of_order((uint32_t)(cand[j] >> 32)) - m) : 0.f;
+      local += e[k];
     }
-    // the in-thread sum in entry order, then the scan across threads
-#pragma unroll
-    for (int k = 0; k < kCutPer; ++k) local += e[k];
     float Z = 0.f;
     float before = block_scan_excl(local, scan_f, Z);
     int kept = 0;
 #pragma unroll
-    for (int k = 0; k < kCutPer; ++k) {
-      const int j = kCutPer * tid + k;
+    for (int k = 0; k < PER; ++k) {
+      const int j = PER * tid + k;
       bool keep = j < kc;
       if (t.top_p < 1.f) keep = keep && before < t.top_p * Z;
       if (t.min_p > 0.f) keep = keep && e[k] >= t.min_p;
@@ -1143,11 +1194,25 @@ void launch_attention_combine(DT dt, const float* part, const int32_t* item_firs
 void launch_trunc_cut(const SampleArgs& a, const Trunc* tr, uint64_t* cut, uint64_t* const* sess_cut,
                       cudaStream_t st) {
   if (a.rows <= 0) return;
-  // a cluster of kCutCluster CTAs per row; one CTA per row if that launch is refused
-  if (launch_kc(k_trunc_cut, dim3(a.rows * kCutCluster), dim3(kCutThreads), 0, st, kCutCluster, a, tr, cut,
-                sess_cut) != cudaSuccess) {
+  const int64_t G = (a.V + 3) / 4, per_cta = (int64_t)kCutThreads * kCutRegQuads;
+  const int creg = (int)((G + per_cta - 1) / per_cta);
+  if (creg <= kCutMaxCluster) {
+    // the row in registers: creg CTAs per row; one CTA per row cannot hold
+    // it, so a refused cluster launch is an error here
+    if (creg == 1) {
+      launch_k(k_trunc_cut<kCutThreads, kCutRegQuads>, a.rows, kCutThreads, 0, st, a, tr, cut, sess_cut);
+    } else {
+      launch_kc(k_trunc_cut<kCutThreads, kCutRegQuads>, dim3(a.rows * creg), dim3(kCutThreads), 0, st, creg, a,
+                tr, cut, sess_cut);
+    }
+    return;
+  }
+  // long rows streamed: a cluster of kCutCluster CTAs per row; one CTA per row
+  // if that launch is refused
+  if (launch_kc(k_trunc_cut<kCutStreamThreads, 0>, dim3(a.rows * kCutCluster), dim3(kCutStreamThreads), 0, st,
+                kCutCluster, a, tr, cut, sess_cut) != cudaSuccess) {
     (void)cudaGetLastError();
-    launch_k(k_trunc_cut, a.rows, kCutThreads, 0, st, a, tr, cut, sess_cut);
+    launch_k(k_trunc_cut<kCutStreamThreads, 0>, a.rows, kCutStreamThreads, 0, st, a, tr, cut, sess_cut);
   }
 }
 
