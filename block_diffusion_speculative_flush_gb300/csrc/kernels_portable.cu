@@ -449,135 +449,8 @@ __device__ __forceinline__ float load_logit(const void* p, int in_bf16, int64_t 
   return in_bf16 ? __bfloat162float(((const bf16*)p)[idx]) : ((const float*)p)[idx];
 }
 
-// part[row][chunk] = (max of l/T, sum exp(l/T - max), best score, best index)
-// where the score is l/T + Gumbel (draft draw) or l/T (argmax / row stats).
-// Logit v of sampled row `row`, from the session's own rows when given.
-__device__ __forceinline__ float sample_logit(const SampleArgs& a, int row, int v) {
-  if (a.seq_logits)
-    return a.seq_logits[row / a.rows_per_seq][(int64_t)(row % a.rows_per_seq) * a.ld + v];
-  return load_logit(a.logits, a.in_bf16, (int64_t)row * a.ld + v);
-}
-
-__global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float sm_m[32], sm_l[32], sm_s[32];
-  __shared__ int32_t sm_i[32];
-  const int row = blockIdx.x, c = blockIdx.y, nch = gridDim.y;
-  const int v0 = c * chunk, v1 = min(a.V, v0 + chunk);
-  const float invT = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
-  const int b = row / a.rows_per_seq;
-  const uint32_t prow = (uint32_t)(row % a.rows_per_seq + a.row_offset);
-  const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
-  const uint64_t cutv = a.cut ? a.cut[row] : 0ull;
-  float m = -INFINITY, l = 0.f;
-  ArgMax best{-INFINITY, INT32_MAX};
-  // four consecutive entries per thread: one Philox evaluation gives their
-  // four random words (chunks start on multiples of 4)
-  for (int v4 = v0 + 4 * threadIdx.x; v4 < v1; v4 += 4 * blockDim.x) {
-    uint4 r = make_uint4(0, 0, 0, 0);
-    if (a.gumbel) r = rand_block(a.seed, a.rnd, kStreamDraft, seq, prow, (uint32_t)v4 >> 2);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const int v = v4 + w;
-      if (v >= v1) break;
-      const float s = sample_logit(a, row, v) * invT;
-      if (cutv && order_key(s, v) < cutv) continue;  // outside the truncated support
-      if (s > m) {
-        l = l * expf(m - s) + 1.f;
-        m = s;
-      } else {
-        l += expf(s - m);
-      }
-      float score = s;
-      if (a.gumbel) score += gumbel_of(word_of(r, w));
-      best = better(best, ArgMax{score, v});
-    }
-  }
-  // warp merge
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    const float M = fmaxf(m, m2);
-    l = (m == -INFINITY ? 0.f : l * expf(m - M)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - M));
-    m = M;
-  }
-  best = warp_argmax(best);
-  if (lane == 0) {
-    sm_m[w] = m;
-    sm_l[w] = l;
-    sm_s[w] = best.v;
-    sm_i[w] = best.i;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int i = 0; i < nw; ++i) M = fmaxf(M, sm_m[i]);
-    float L = 0.f;
-    ArgMax bb{-INFINITY, INT32_MAX};
-    for (int i = 0; i < nw; ++i) {
-      if (sm_m[i] != -INFINITY) L += sm_l[i] * expf(sm_m[i] - M);
-      bb = better(bb, ArgMax{sm_s[i], sm_i[i]});
-    }
-    part[(int64_t)row * nch + c] = make_float4(M, L, bb.v, __int_as_float(bb.i));
-  }
-}
-
-__global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restrict__ part, int32_t* __restrict__ tok,
-                                 float* __restrict__ qtok, float* __restrict__ lse) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= a.rows) return;
-  float M = -INFINITY;
-  for (int c = 0; c < chunks; ++c) M = fmaxf(M, part[(int64_t)row * chunks + c].x);
-  float L = 0.f;
-  ArgMax bb{-INFINITY, INT32_MAX};
-  for (int c = 0; c < chunks; ++c) {
-    const float4 pc = part[(int64_t)row * chunks + c];
-    if (pc.x != -INFINITY) L += pc.y * expf(pc.x - M);
-    bb = better(bb, ArgMax{pc.z, __float_as_int(pc.w)});
-  }
-  // a row whose scores were all NaN has no argmax: record it and answer 0
-  // rather than reading a logit at an undefined index
-  if (bb.i < 0 || bb.i >= a.V) {
-    if (a.err) atomicOr(a.err, 16);
-    bb.i = 0;
-  }
-  const float ls = M + logf(L);
-  int orow = row;
-  if (a.out_map) orow = a.out_map[row / a.rows_per_seq] * a.rows_per_seq + row % a.rows_per_seq;
-  if (tok) tok[orow] = bb.i;
-  if (lse) lse[orow] = ls;
-  if (a.sess_tok) a.sess_tok[row / a.rows_per_seq][row % a.rows_per_seq] = bb.i;
-  if (a.sess_lse) a.sess_lse[row / a.rows_per_seq][row % a.rows_per_seq] = ls;
-  if (qtok) {
-    if (a.temperature > 0.f) {
-      const float x = sample_logit(a, row, bb.i) / a.temperature;
-      qtok[orow] = expf(x - ls);
-    } else {
-      qtok[orow] = 1.f;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// truncated distributions: the cut of each row
-// ---------------------------------------------------------------------------
-// The cut kernel runs a cluster of CTAs per row.  Rows up to
-// kCutRegQuads * 4 * kCutThreads * kCutMaxCluster entries are read once into
-// registers (kCutRegQuads quads per thread) and every pass runs on them; longer
-// rows are streamed from memory in every pass by a cluster of kCutCluster CTAs.
-constexpr int kCutThreads = 1024;
-constexpr int kCutRegQuads = 5;
-constexpr int kCutMaxCluster = 8;
-constexpr int kCutStreamThreads = 512;
-constexpr int kCutQuads = 4;    // quads in flight per thread in each streamed pass
-constexpr int kCutCluster = 8;  // CTAs per row when streaming
-
-// One row of logits for the cut kernel, read four entries at a time (one
-// 16-byte fp32 or 8-byte bf16 load when the row is aligned and V % 4 == 0).
+// One row of logits, read four entries at a time (one 16-byte fp32 or
+// 8-byte bf16 load when the row is aligned and V % 4 == 0).
 struct RowRef {
   const void* p;
   int bf;
@@ -651,6 +524,159 @@ __device__ __forceinline__ T block_scan_excl(T x, T* sm, T& total) {
   __syncthreads();
   return r;
 }
+
+// part[row][chunk] = (max of l/T, sum exp(l/T - max), best score, best index)
+// where the score is l/T + Gumbel (draft draw) or l/T (argmax / row stats).
+// Logit v of sampled row `row`, from the session's own rows when given.
+__device__ __forceinline__ float sample_logit(const SampleArgs& a, int row, int v) {
+  if (a.seq_logits)
+    return a.seq_logits[row / a.rows_per_seq][(int64_t)(row % a.rows_per_seq) * a.ld + v];
+  return load_logit(a.logits, a.in_bf16, (int64_t)row * a.ld + v);
+}
+
+constexpr int kSampleSteps = 4;
+
+__global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sm_m[32], sm_l[32], sm_s[32];
+  __shared__ int32_t sm_i[32];
+  const int row = blockIdx.x, c = blockIdx.y, nch = gridDim.y;
+  const int v0 = c * chunk, v1 = min(a.V, v0 + chunk);
+  const float invT = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
+  const int b = row / a.rows_per_seq;
+  const uint32_t prow = (uint32_t)(row % a.rows_per_seq + a.row_offset);
+  const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
+  const uint64_t cutv = a.cut ? a.cut[row] : 0ull;
+  float m = -INFINITY, l = 0.f;
+  ArgMax best{-INFINITY, INT32_MAX};
+  const RowRef rr = row_ref(a, row);
+  // four consecutive entries per thread and step: one Philox evaluation gives
+  // their four random words (chunks start on multiples of 4); kSampleSteps
+  // steps' loads are issued before any is used
+  for (int base = v0 + 4 * threadIdx.x; base < v1; base += 4 * blockDim.x * kSampleSteps) {
+    float x[kSampleSteps][4];
+#pragma unroll
+    for (int it = 0; it < kSampleSteps; ++it) {
+      const int v4 = base + it * 4 * blockDim.x;
+      if (v4 < v1) {
+        load_quad(rr, v4 >> 2, a.V, invT, x[it]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[it][k] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kSampleSteps; ++it) {
+      const int v4 = base + it * 4 * blockDim.x;
+      if (v4 >= v1) break;
+      uint4 r = make_uint4(0, 0, 0, 0);
+      if (a.gumbel) r = rand_block(a.seed, a.rnd, kStreamDraft, seq, prow, (uint32_t)v4 >> 2);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int v = v4 + w;
+        if (v >= v1) break;
+        const float s = x[it][w];
+        if (cutv && order_key(s, v) < cutv) continue;  // outside the truncated support
+        if (s > m) {
+          l = l * expf(m - s) + 1.f;
+          m = s;
+        } else {
+          l += expf(s - m);
+        }
+        float score = s;
+        if (a.gumbel) score += gumbel_of(word_of(r, w));
+        best = better(best, ArgMax{score, v});
+      }
+    }
+  }
+  // warp merge
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    const float M = fmaxf(m, m2);
+    l = (m == -INFINITY ? 0.f : l * expf(m - M)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - M));
+    m = M;
+  }
+  best = warp_argmax(best);
+  if (lane == 0) {
+    sm_m[w] = m;
+    sm_l[w] = l;
+    sm_s[w] = best.v;
+    sm_i[w] = best.i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int i = 0; i < nw; ++i) M = fmaxf(M, sm_m[i]);
+    float L = 0.f;
+    ArgMax bb{-INFINITY, INT32_MAX};
+    for (int i = 0; i < nw; ++i) {
+      if (sm_m[i] != -INFINITY) L += sm_l[i] * expf(sm_m[i] - M);
+      bb = better(bb, ArgMax{sm_s[i], sm_i[i]});
+    }
+    part[(int64_t)row * nch + c] = make_float4(M, L, bb.v, __int_as_float(bb.i));
+  }
+}
+
+__global__ void k_sample_combine(SampleArgs a, int chunks, const float4* __restrict__ part, int32_t* __restrict__ tok,
+                                 float* __restrict__ qtok, float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
+  // one warp per row, lane c over chunks c, c + 32, ...
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= a.rows) return;
+  float M = -INFINITY;
+  for (int c = lane; c < chunks; c += 32) M = fmaxf(M, part[(int64_t)row * chunks + c].x);
+  M = warp_max(M);
+  float L = 0.f;
+  ArgMax bb{-INFINITY, INT32_MAX};
+  for (int c = lane; c < chunks; c += 32) {
+    const float4 pc = part[(int64_t)row * chunks + c];
+    if (pc.x != -INFINITY) L += pc.y * expf(pc.x - M);
+    bb = better(bb, ArgMax{pc.z, __float_as_int(pc.w)});
+  }
+  L = warp_sum(L);
+  bb = warp_argmax(bb);
+  if (lane != 0) return;
+  // a row whose scores were all NaN has no argmax: record it and answer 0
+  // rather than reading a logit at an undefined index
+  if (bb.i < 0 || bb.i >= a.V) {
+    if (a.err) atomicOr(a.err, 16);
+    bb.i = 0;
+  }
+  const float ls = M + logf(L);
+  int orow = row;
+  if (a.out_map) orow = a.out_map[row / a.rows_per_seq] * a.rows_per_seq + row % a.rows_per_seq;
+  if (tok) tok[orow] = bb.i;
+  if (lse) lse[orow] = ls;
+  if (a.sess_tok) a.sess_tok[row / a.rows_per_seq][row % a.rows_per_seq] = bb.i;
+  if (a.sess_lse) a.sess_lse[row / a.rows_per_seq][row % a.rows_per_seq] = ls;
+  if (qtok) {
+    if (a.temperature > 0.f) {
+      const float x = sample_logit(a, row, bb.i) / a.temperature;
+      qtok[orow] = expf(x - ls);
+    } else {
+      qtok[orow] = 1.f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// truncated distributions: the cut of each row
+// ---------------------------------------------------------------------------
+// The cut kernel runs a cluster of CTAs per row.  Rows up to
+// kCutRegQuads * 4 * kCutThreads * kCutMaxCluster entries are read once into
+// registers (kCutRegQuads quads per thread) and every pass runs on them; longer
+// rows are streamed from memory in every pass by a cluster of kCutCluster CTAs.
+constexpr int kCutThreads = 1024;
+constexpr int kCutRegQuads = 5;
+constexpr int kCutMaxCluster = 8;
+constexpr int kCutStreamThreads = 512;
+constexpr int kCutQuads = 4;    // quads in flight per thread in each streamed pass
+constexpr int kCutCluster = 8;  // CTAs per row when streaming
 
 // Histogram update of one entry's order word: digit (o >> shift) & 255 of
 // the entries that match the prefix so far, equal digits of a warp
@@ -922,8 +948,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_trunc_cut(SampleArgs a, const Tr
 }
 
 // Acceptance scan of one session (T > 0): the first i in 1..n whose draft
-// token fails u_i * q_i(d_i) < p_i(d_i), or 0 if all n pass.
+// token fails u_i * q_i(d_i) < p_i(d_i), or 0 if all n pass.  A warp tests
+// 32 positions at once and every lane returns the answer; a draft id outside
+// [0, V) at or before the first failure sets bit 2 of the error word.
 __device__ int verify_scan(const VerifyArgs& a, int b) {
+  const int lane = threadIdx.x & 31;
   const int n = a.n, V = a.V;
   const int64_t tbase = (int64_t)b * (n + 1) * V;
   const uint32_t seq = a.seq_ids ? (uint32_t)a.seq_ids[b] : (uint32_t)b;
@@ -933,20 +962,29 @@ __device__ int verify_scan(const VerifyArgs& a, int b) {
   const float* dlse = a.dlse[b];
   const int32_t* dtok = a.dtok[b];
   const uint64_t* dc = a.dcut ? a.dcut[b] : nullptr;
-  for (int i = 1; i <= n; ++i) {
-    int dtk = a.draft[b * n + i - 1];
-    if (dtk < 0 || dtk >= V) {
-      atomicOr(a.err, 2);
-      dtk = 0;
+  for (int i0 = 1; i0 <= n; i0 += 32) {
+    const int i = i0 + lane;
+    bool fail = false, bad = false;
+    if (i <= n) {
+      int dtk = a.draft[b * n + i - 1];
+      if (dtk < 0 || dtk >= V) {
+        bad = true;
+        dtk = 0;
+      }
+      const float st = load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT;
+      float p = expf(st - a.lse_t[b * (n + 1) + i - 1]);
+      if (a.cut_t && order_key(st, dtk) < a.cut_t[b * (n + 1) + i - 1]) p = 0.f;
+      const float dv = dl[(int64_t)(i - 1) * V + dtk];
+      float q = Tq > 0.f ? expf(dv / Tq - dlse[i - 1]) : (dtk == dtok[i - 1] ? 1.f : 0.f);
+      if (Tq > 0.f && dc && order_key(dv * (1.f / Tq), dtk) < dc[i - 1]) q = 0.f;
+      const float r = uniform_open(rand_u32(a.seed, a.rnd, kStreamAccept, seq, (uint32_t)i, 0u));
+      fail = !(r * q < p);
     }
-    const float st = load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT;
-    float p = expf(st - a.lse_t[b * (n + 1) + i - 1]);
-    if (a.cut_t && order_key(st, dtk) < a.cut_t[b * (n + 1) + i - 1]) p = 0.f;
-    const float dv = dl[(int64_t)(i - 1) * V + dtk];
-    float q = Tq > 0.f ? expf(dv / Tq - dlse[i - 1]) : (dtk == dtok[i - 1] ? 1.f : 0.f);
-    if (Tq > 0.f && dc && order_key(dv * (1.f / Tq), dtk) < dc[i - 1]) q = 0.f;
-    const float r = uniform_open(rand_u32(a.seed, a.rnd, kStreamAccept, seq, (uint32_t)i, 0u));
-    if (!(r * q < p)) return i;
+    const unsigned fm = __ballot_sync(0xffffffffu, fail);
+    const int first = fm ? i0 + __ffs(fm) - 1 : 0;
+    const unsigned bm = __ballot_sync(0xffffffffu, bad && (first == 0 || i <= first));
+    if (bm && lane == 0) atomicOr(a.err, 2);
+    if (first) return first;
   }
   return 0;
 }
@@ -963,9 +1001,12 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
   __shared__ int32_t sm_ri[32], sm_pi[32];
   const int b = blockIdx.x, c = blockIdx.y, nch = gridDim.y;
   const int n = a.n, V = a.V;
-  if (threadIdx.x == 0) {
-    s_rej = verify_scan(a, b);
-    if (c == 0) a.rej[b] = s_rej;
+  if (threadIdx.x < 32) {
+    const int rj = verify_scan(a, b);
+    if (threadIdx.x == 0) {
+      s_rej = rj;
+      if (c == 0) a.rej[b] = rj;
+    }
   }
   __syncthreads();
   const int rej = s_rej;
@@ -1040,11 +1081,14 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
 __global__ void k_verify_finish(VerifyArgs a, int chunks, const VerifyPart* __restrict__ part) {
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  // one warp per session, lane c over chunks c, c + 32, ...
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= a.B) return;
   const int n = a.n;
   int accn, bonus;
   if (a.temperature <= 0.f) {
+    if (lane != 0) return;
     accn = 0;
     while (accn < n && a.amax_t[b * (n + 1) + accn] == a.draft[b * n + accn]) ++accn;
     bonus = a.amax_t[b * (n + 1) + accn];      // in range: the row statistics clamp it
@@ -1052,12 +1096,16 @@ __global__ void k_verify_finish(VerifyArgs a, int chunks, const VerifyPart* __re
     const int rej = a.rej[b];
     float S = 0.f;
     ArgMax R{-INFINITY, INT32_MAX}, P{-INFINITY, INT32_MAX};
-    for (int c = 0; c < chunks; ++c) {
+    for (int c = lane; c < chunks; c += 32) {
       const VerifyPart o = part[(int64_t)b * chunks + c];
       S += o.rsum;
       R = better(R, ArgMax{o.rv, o.ri});
       P = better(P, ArgMax{o.pv, o.pi});
     }
+    S = warp_sum(S);
+    R = warp_argmax(R);
+    P = warp_argmax(P);
+    if (lane != 0) return;
     accn = rej ? rej - 1 : n;
     bonus = (rej && S > 0.f) ? R.i : P.i;
     if (bonus < 0 || bonus >= a.V) {  // no comparable score (non-finite logits)
@@ -1248,14 +1296,14 @@ void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaSt
 void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, int32_t* tok, float* qtok, float* lse,
                            cudaStream_t st) {
   if (a.rows <= 0) return;
-  launch_k(k_sample_combine, cdiv(a.rows, 128), 128, 0, st, a, chunks, part, tok, qtok, lse);
+  launch_k(k_sample_combine, cdiv(a.rows, 4), 128, 0, st, a, chunks, part, tok, qtok, lse);
 }
 
 void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st) {
   if (a.B <= 0) return;
   const int chunk = kVerifyBonusChunk, chunks = verify_bonus_chunks(a.V);
   if (a.temperature > 0.f) launch_k(k_verify_bonus, dim3(a.B, chunks), 256, 0, st, a, chunk, part);
-  launch_k(k_verify_finish, cdiv(a.B, 64), 64, 0, st, a, chunks, part);
+  launch_k(k_verify_finish, cdiv(a.B, 4), 128, 0, st, a, chunks, part);
 }
 
 int launch_table_write(void* dst, const void* src, size_t bytes, cudaStream_t st) {
