@@ -171,7 +171,7 @@ struct VerifyPart {
 // T > 0: one grid of (session, vocabulary chunk) CTAs for the bonus draw,
 // then the per-session finish; T == 0: the finish alone.  part holds
 // B * verify_bonus_chunks(V) entries.
-constexpr int kVerifyBonusChunk = 2048;
+constexpr int kVerifyBonusChunk = 1024;
 inline int verify_bonus_chunks(int V) { return (V + kVerifyBonusChunk - 1) / kVerifyBonusChunk; }
 void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st);
 

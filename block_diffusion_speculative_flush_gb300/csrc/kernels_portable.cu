@@ -536,7 +536,7 @@ __device__ __forceinline__ float sample_logit(const SampleArgs& a, int row, int 
 
 constexpr int kSampleSteps = 4;
 
-__global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
+__global__ void __launch_bounds__(256, 4) k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
   pdl_trigger();
   pdl_wait();
   __shared__ float sm_m[32], sm_l[32], sm_s[32];
@@ -566,6 +566,36 @@ __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ 
         for (int k = 0; k < 4; ++k) x[it][k] = 0.f;
       }
     }
+    // entries outside the chunk or the truncated support become -inf: they
+    // add nothing to the sum and never win the draw
+#pragma unroll
+    for (int it = 0; it < kSampleSteps; ++it) {
+      const int v4 = base + it * 4 * blockDim.x;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int v = v4 + w;
+        if (v >= v1 || (cutv && order_key(x[it][w], v) < cutv)) x[it][w] = -INFINITY;
+      }
+    }
+    // the step's max, then one exponential per entry
+    float ms = -INFINITY;
+#pragma unroll
+    for (int it = 0; it < kSampleSteps; ++it)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) ms = fmaxf(ms, x[it][w]);
+    if (ms != -INFINITY) {
+      float ls = 0.f;
+#pragma unroll
+      for (int it = 0; it < kSampleSteps; ++it)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) ls += expf(x[it][w] - ms);
+      if (ms > m) {
+        l = (m == -INFINITY ? 0.f : l * expf(m - ms)) + ls;
+        m = ms;
+      } else {
+        l += ls * expf(ms - m);
+      }
+    }
 #pragma unroll
     for (int it = 0; it < kSampleSteps; ++it) {
       const int v4 = base + it * 4 * blockDim.x;
@@ -577,13 +607,7 @@ __global__ void k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ 
         const int v = v4 + w;
         if (v >= v1) break;
         const float s = x[it][w];
-        if (cutv && order_key(s, v) < cutv) continue;  // outside the truncated support
-        if (s > m) {
-          l = l * expf(m - s) + 1.f;
-          m = s;
-        } else {
-          l += expf(s - m);
-        }
+        if (s == -INFINITY && cutv) continue;  // outside the truncated support
         float score = s;
         if (a.gumbel) score += gumbel_of(word_of(r, w));
         best = better(best, ArgMax{score, v});
