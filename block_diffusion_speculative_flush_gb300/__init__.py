@@ -84,6 +84,23 @@ def _sessions(sessions):
     return arr, len(sessions)
 
 
+def _need(t, dtypes, numel: int, what: str) -> None:
+    """The library reads or writes numel elements of t from its data pointer:
+    t must be a contiguous CUDA tensor of one of dtypes with at least that many."""
+    if t is None:
+        return
+    if not isinstance(dtypes, tuple):
+        dtypes = (dtypes,)
+    if not t.is_cuda or t.dtype not in dtypes or not t.is_contiguous() or t.numel() < numel:
+        raise ValueError(f"{what}: a contiguous CUDA tensor of {'/'.join(str(d) for d in dtypes)} with at least "
+                         f"{numel} elements")
+
+
+def _model_of(sessions):
+    first = sessions if isinstance(sessions, Session) else sessions[0]
+    return first.model
+
+
 def dflash_version() -> int:
     return lib.dflash_version()
 
@@ -144,6 +161,9 @@ def dflash_committed(session: Session, features: torch.Tensor, position: int) ->
     """features: CUDA tensor [n_rows, K*H_t] (row stride from the tensor)."""
     if features.dim() != 2 or features.stride(1) != 1:
         raise ValueError("features must be 2-D with unit column stride")
+    cfg = session.model.cfg
+    if not features.is_cuda or features.dtype != torch_dtype(cfg) or features.shape[1] != cfg.feature_width:
+        raise ValueError(f"features: CUDA {torch_dtype(cfg)} rows of width {cfg.feature_width}")
     _check(lib.dflash_committed(session.handle, _ptr(features), features.stride(0), features.shape[0], position))
 
 
@@ -165,18 +185,32 @@ def dflash_propose(sessions, current: torch.Tensor, max_tokens: int, temperature
                    out_tokens: torch.Tensor, out_q: torch.Tensor, out_logits: torch.Tensor | None = None) -> list:
     """Returns out_n per session (0 where the pages return nil)."""
     arr, n = _sessions(sessions)
+    cfg = _model_of(sessions).cfg
+    rows = n * max(0, min(int(max_tokens), cfg.block_size - 1))
+    _need(current, torch.int32, n, "current")
+    _need(out_tokens, torch.int32, rows, "out_tokens")
+    _need(out_q, torch.float32, rows, "out_q")
+    _need(out_logits, torch.float32, rows * cfg.vocab, "out_logits")
     out_n = (C.c_int32 * n)()
     _check(lib.dflash_propose(arr, n, _ptr(current), max_tokens, float(temperature), seed, rnd, _ptr(out_tokens),
                               _ptr(out_q), _ptr(out_logits), out_n))
     return list(out_n)
 
 
+def _verify_args(sessions, b, target_logits, draft_tokens, n, out_accept, out_bonus) -> None:
+    V = _model_of(sessions).cfg.vocab
+    n = max(0, int(n))
+    _need(target_logits, (torch.float32, torch.bfloat16), b * (n + 1) * V, "target_logits [batch, n+1, V]")
+    _need(draft_tokens, torch.int32, b * n, "draft_tokens [batch, n]")
+    _need(out_accept, torch.int32, b, "out_accept")
+    _need(out_bonus, torch.int32, b, "out_bonus")
+
+
 def dflash_verify(sessions, target_logits: torch.Tensor, draft_tokens: torch.Tensor, n: int, temperature: float,
                   seed: int, rnd: int, out_accept: torch.Tensor, out_bonus: torch.Tensor) -> None:
     arr, b = _sessions(sessions)
+    _verify_args(sessions, b, target_logits, draft_tokens, n, out_accept, out_bonus)
     dt = DFLASH_DTYPE_BF16 if target_logits.dtype == torch.bfloat16 else DFLASH_DTYPE_F32
-    if target_logits.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("target logits must be fp32 or bf16")
     _check(lib.dflash_verify(arr, b, _ptr(target_logits), dt, _ptr(draft_tokens), n, float(temperature), seed, rnd,
                              _ptr(out_accept), _ptr(out_bonus)))
 
@@ -186,8 +220,7 @@ def dflash_verify_noalloc(sessions, target_logits: torch.Tensor, draft_tokens: t
                           out_bonus: torch.Tensor) -> None:
     """dflash_verify on the library's static scratch (no device allocation)."""
     arr, b = _sessions(sessions)
-    if target_logits.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("target logits must be fp32 or bf16")
+    _verify_args(sessions, b, target_logits, draft_tokens, n, out_accept, out_bonus)
     dt = DFLASH_DTYPE_BF16 if target_logits.dtype == torch.bfloat16 else DFLASH_DTYPE_F32
     _check(lib.dflash_verify_noalloc(arr, b, _ptr(target_logits), dt, _ptr(draft_tokens), n, float(temperature), seed,
                                      rnd, _ptr(out_accept), _ptr(out_bonus)))

@@ -132,3 +132,24 @@ def test_target_create_refuses_bad_shapes_and_weights_on_the_host(lib):
         c2 = _abi.dflash_target_config.from_buffer_copy(cfg)
         setattr(c2, field, bad)
         assert lib.dflash_target_create(C.byref(c2), C.byref(w), 64, None, C.byref(out)) == _abi.DFLASH_ERR_SHAPE
+
+
+def test_binding_refuses_buffers_the_library_would_overrun(lib):
+    """The Python binding checks dtype, contiguity, device and size of every
+    tensor it hands to the library before the call (host-side; no GPU)."""
+    import torch
+
+    import block_diffusion_speculative_flush_gb300 as D
+    import synthetic as S
+    cfg = S.CONFIGS["tiny_fp32"]
+    sess = D.Session(0, D.Model(0, cfg, {}, None))
+    n = cfg.block_size - 1
+    cur = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError):   # host tensors
+        D.dflash_propose([sess], cur, n, 0.0, 0, 0, torch.zeros((1, n), dtype=torch.int32),
+                         torch.zeros((1, n)))
+    with pytest.raises(ValueError):
+        D.dflash_verify([sess], torch.zeros((1, n + 1, cfg.vocab)), torch.zeros((1, n), dtype=torch.int32), n,
+                        0.0, 0, 0, torch.zeros(1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        D.dflash_committed(sess, torch.zeros((2, cfg.feature_width + 1)), 0)
