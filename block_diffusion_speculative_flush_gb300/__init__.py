@@ -23,7 +23,7 @@ lib = _abi.load()
 __all__ = [
     "DFlashError", "Model", "Session", "lib", "torch_dtype",
     "dflash_model_create", "dflash_model_destroy", "dflash_draft_limit", "dflash_device_status", "dflash_open",
-    "dflash_committed", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
+    "dflash_committed", "dflash_committed_taps", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
     "dflash_close", "dflash_set_sampler", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
     "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read", "dflash_verify_noalloc",
     "Target", "dflash_target_create", "dflash_target_destroy", "dflash_target_forward", "dflash_target_trim",
@@ -165,6 +165,21 @@ def dflash_committed(session: Session, features: torch.Tensor, position: int) ->
     if not features.is_cuda or features.dtype != torch_dtype(cfg) or features.shape[1] != cfg.feature_width:
         raise ValueError(f"features: CUDA {torch_dtype(cfg)} rows of width {cfg.feature_width}")
     _check(lib.dflash_committed(session.handle, _ptr(features), features.stride(0), features.shape[0], position))
+
+
+def dflash_committed_taps(session: Session, taps, position: int) -> None:
+    """taps: n_taps CUDA tensors [n_rows, H_t] (unit column stride, one row stride for all)."""
+    cfg = session.model.cfg
+    taps = list(taps)
+    if len(taps) != cfg.n_taps:
+        raise ValueError(f"{cfg.n_taps} taps expected")
+    rows, stride = taps[0].shape[0], taps[0].stride(0)
+    for t in taps:
+        if t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda or t.dtype != torch_dtype(cfg) or \
+                t.shape != (rows, cfg.target_hidden) or t.stride(0) != stride:
+            raise ValueError(f"taps: CUDA {torch_dtype(cfg)} [{rows}, {cfg.target_hidden}] with one row stride")
+    arr = (C.c_void_p * len(taps))(*[t.data_ptr() for t in taps])
+    _check(lib.dflash_committed_taps(session.handle, arr, stride, rows, position))
 
 
 def dflash_flush(sessions) -> None:

@@ -91,6 +91,7 @@ SIGNATURES = {
     "dflash_device_status": (C.c_int, [P]),
     "dflash_open": (C.c_int, [P, C.c_int64, C.c_int64, P, C.POINTER(C.c_void_p)]),
     "dflash_committed": (C.c_int, [P, P, C.c_int64, C.c_int32, C.c_int64]),
+    "dflash_committed_taps": (C.c_int, [P, C.POINTER(C.c_void_p), C.c_int64, C.c_int32, C.c_int64]),
     "dflash_flush": (C.c_int, [SessArr, C.c_int32]),
     "dflash_settle": (C.c_int, [P]),
     "dflash_commit_block": (C.c_int, [SessArr, C.c_int32]),

@@ -232,6 +232,7 @@ int check_config(const dflash_config& c) {
       c.intermediate < 1 || c.vocab < 2)
     return fail(DFLASH_ERR_SHAPE, "non-positive dimension in config");
   if (c.block_size < 2 || c.block_size > 512) return fail(DFLASH_ERR_SHAPE, "block_size %d outside 2..512", c.block_size);
+  if (c.n_taps > kMaxTaps) return fail(DFLASH_ERR_SHAPE, "n_taps %d above %d", c.n_taps, kMaxTaps);
   if (c.window != 0 && (c.window < 2 || c.window > (1 << 20)))
     return fail(DFLASH_ERR_SHAPE, "window %d outside 2..2^20", c.window);
   if (c.head_dim != 64 && c.head_dim != 128) return fail(DFLASH_ERR_SHAPE, "head_dim %d (64 or 128 supported)", c.head_dim);
@@ -328,9 +329,9 @@ int launch_check(const char* what) {
 // one batched forward: context rows (flush) and optionally block rows
 // ---------------------------------------------------------------------------
 struct CtxRow {
-  const void* src;  // feature row
-  int32_t sess;     // compact session index
-  int64_t pos;      // slot
+  const void* tap[kMaxTaps];  // the row's n_taps target hidden states
+  int32_t sess;               // compact session index
+  int64_t pos;                // slot
 };
 
 struct Forward {
@@ -363,10 +364,10 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
 
   // ---- per-call tables ---------------------------------------------------
   TablePack tp;
-  std::vector<const void*> rowsrc(Mc);
+  std::vector<const void*> rowsrc((size_t)Mc * c.n_taps);  // [Mc][K]: tap k of context row r
   std::vector<RowMeta> meta(M);
   for (int r = 0; r < Mc; ++r) {
-    rowsrc[r] = fw.ctx[r].src;
+    for (int k = 0; k < c.n_taps; ++k) rowsrc[(size_t)r * c.n_taps + k] = fw.ctx[r].tap[k];
     meta[r] = RowMeta{fw.ctx[r].sess, -1, fw.ctx[r].pos};
   }
   std::vector<void*> kvb(Bc);
@@ -636,19 +637,25 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
 // Context rows of one session's held features (and optionally extra rows
 // straight from the caller), with the window drop applied.  F advances
 // past every row; P returns to zero.
-void take_pending(dflash_session* s, int32_t sess_idx, const void* extra, int64_t extra_stride, int extra_rows,
+// The held rows (staged, concatenated taps) and then extra_rows new rows read
+// in place: tap k of new row j at extra[k] + j * extra_stride bytes.
+void take_pending(dflash_session* s, int32_t sess_idx, const char* const* extra, int64_t extra_stride, int extra_rows,
                   std::vector<CtxRow>& out) {
   const dflash_config& c = s->m->cfg;
-  const size_t rowb = (size_t)c.n_taps * c.target_hidden * s->m->esz;
+  const size_t tapb = (size_t)c.target_hidden * s->m->esz, rowb = (size_t)c.n_taps * tapb;
   const int64_t first = s->F;
   const int total = s->P + extra_rows;
   const int64_t Fnew = first + total;
   for (int r = 0; r < total; ++r) {
     const int64_t slot = first + r;
     if (c.window && slot <= Fnew - c.window) continue;  // no later query can see it
-    const void* src = r < s->P ? (const char*)s->pending + (size_t)r * rowb
-                               : (const char*)extra + (size_t)(r - s->P) * extra_stride * s->m->esz;
-    out.push_back(CtxRow{src, sess_idx, slot});
+    CtxRow row{};
+    row.sess = sess_idx;
+    row.pos = slot;
+    for (int k = 0; k < c.n_taps; ++k)
+      row.tap[k] = r < s->P ? (const char*)s->pending + (size_t)r * rowb + k * tapb
+                            : extra[k] + (size_t)(r - s->P) * extra_stride;
+    out.push_back(row);
   }
   s->flushed_rows += total;
   s->F = Fnew;
@@ -867,13 +874,12 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
   return DFLASH_OK;
 }
 
-int dflash_committed(dflash_session* s, const void* features, int64_t row_stride, int32_t n_rows, int64_t position) {
-  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+// committed for a run whose tap k of row j is at taps[k] + j * row_bytes;
+// concat: the taps are the consecutive slices of one feature row.
+static int committed_impl(dflash_session* s, const char* const* taps, int64_t row_bytes, bool concat, int32_t n_rows,
+                   int64_t position) {
   const dflash_config& c = s->m->cfg;
   const int64_t width = (int64_t)c.n_taps * c.target_hidden;
-  if (n_rows < 0 || position < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_rows %d / position %lld", n_rows, (long long)position);
-  if (n_rows > 0 && (!features || row_stride < width))
-    return fail(DFLASH_ERR_INVALID_ARG, "features null or row_stride %lld < %lld", (long long)row_stride, (long long)width);
   const int64_t start = s->F + s->P - position;
   if (start < 0)
     return fail(DFLASH_ERR_CONTEXT_GAP, "committed run at %lld leaves a context gap at %lld", (long long)position,
@@ -884,10 +890,18 @@ int dflash_committed(dflash_session* s, const void* features, int64_t row_stride
     return fail(DFLASH_ERR_CAPACITY, "context would reach %lld rows, max_ctx %lld", (long long)(s->F + s->P + add),
                 (long long)s->max_ctx);
   const size_t es = s->m->esz;
-  const char* src = (const char*)features + (size_t)start * row_stride * es;
+  const char* src[kMaxTaps];
+  for (int k = 0; k < c.n_taps; ++k) src[k] = taps[k] + (size_t)start * row_bytes;
   if (s->P + add < DFLASH_PENDING_FLUSH_TOKENS) {
-    launch_copy_rows((char*)s->pending + (size_t)s->P * width * es, (int64_t)(width * es), src,
-                     (int64_t)(row_stride * es), (int64_t)(width * es), add, s->stream);
+    char* dst = (char*)s->pending + (size_t)s->P * width * es;
+    if (concat) {
+      launch_copy_rows(dst, (int64_t)(width * es), src[0], row_bytes, (int64_t)(width * es), add, s->stream);
+    } else {
+      TapSrc ts{};
+      for (int k = 0; k < c.n_taps; ++k) ts.p[k] = src[k];
+      launch_copy_taps(dst, (int64_t)(width * es), ts, c.n_taps, row_bytes, (int64_t)c.target_hidden * es, add,
+                       s->stream);
+    }
     ST_TRY(launch_check("pending rows"));
     s->P += add;
     return DFLASH_OK;
@@ -899,7 +913,7 @@ int dflash_committed(dflash_session* s, const void* features, int64_t row_stride
   fw.sess = {s};
   const int64_t F0 = s->F;
   const int32_t P0 = s->P;
-  take_pending(s, 0, src, row_stride, add, fw.ctx);
+  take_pending(s, 0, src, row_bytes, add, fw.ctx);
   const int rc = run_forward(s->m, fw, s->stream);
   if (rc != DFLASH_OK) {
     s->F = F0;
@@ -908,6 +922,33 @@ int dflash_committed(dflash_session* s, const void* features, int64_t row_stride
   }
   s->flushes++;
   return DFLASH_OK;
+}
+
+int dflash_committed(dflash_session* s, const void* features, int64_t row_stride, int32_t n_rows, int64_t position) {
+  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+  const dflash_config& c = s->m->cfg;
+  const int64_t width = (int64_t)c.n_taps * c.target_hidden;
+  if (n_rows < 0 || position < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_rows %d / position %lld", n_rows, (long long)position);
+  if (n_rows > 0 && (!features || row_stride < width))
+    return fail(DFLASH_ERR_INVALID_ARG, "features null or row_stride %lld < %lld", (long long)row_stride, (long long)width);
+  const char* taps[kMaxTaps];
+  for (int k = 0; k < c.n_taps; ++k) taps[k] = (const char*)features + (size_t)k * c.target_hidden * s->m->esz;
+  return committed_impl(s, taps, row_stride * (int64_t)s->m->esz, true, n_rows, position);
+}
+
+int dflash_committed_taps(dflash_session* s, const void* const* taps, int64_t row_stride, int32_t n_rows,
+                          int64_t position) {
+  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+  const dflash_config& c = s->m->cfg;
+  if (n_rows < 0 || position < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_rows %d / position %lld", n_rows, (long long)position);
+  if (n_rows > 0 && (!taps || row_stride < c.target_hidden))
+    return fail(DFLASH_ERR_INVALID_ARG, "taps null or row_stride %lld < %d", (long long)row_stride, c.target_hidden);
+  const char* tp[kMaxTaps];
+  for (int k = 0; k < c.n_taps; ++k) {
+    if (n_rows > 0 && !taps[k]) return fail(DFLASH_ERR_INVALID_ARG, "tap %d is null", k);
+    tp[k] = (const char*)taps[k];
+  }
+  return committed_impl(s, tp, row_stride * (int64_t)s->m->esz, false, n_rows, position);
 }
 
 int dflash_commit_block(dflash_session* const* s, int32_t batch) {

@@ -55,6 +55,7 @@ struct AttnParams {
 };
 
 // --- portable kernels (any storage type) ----------------------------------
+// src: [rows][K] device table, src[r * K + k] = tap k of context row r.
 void launch_tap_norm(DT dt, const void* const* src, int rows, const void* aux, void* u, int K, int Ht,
                      float eps, cudaStream_t st);
 // out[j] = rmsnorm(in[map(j)]) * g, in rows taken from in0 for map < rows0 else in1.
@@ -184,6 +185,14 @@ constexpr int kTableParamMax = 31744;
 // in the launch chain; returns -1 if the table is too large.
 int launch_table_write(void* dst, const void* src, size_t bytes, cudaStream_t st);
 
+// The target's taps of one committed run: K separate buffers (passed by value).
+constexpr int kMaxTaps = 8;
+struct TapSrc {
+  const char* p[kMaxTaps];
+};
+// Row r of tap k (src.p[k] + r * src_ld bytes, tap_bytes long) to dst + r * dst_ld + k * tap_bytes.
+void launch_copy_taps(void* dst, int64_t dst_ld, const TapSrc& src, int K, int64_t src_ld, int64_t tap_bytes, int rows,
+                      cudaStream_t st);
 // rows x row_bytes from src (row stride src_ld bytes) to dst (dst_ld bytes), as a kernel.
 void launch_copy_rows(void* dst, int64_t dst_ld, const void* src, int64_t src_ld, int64_t row_bytes, int rows,
                       cudaStream_t st);

@@ -38,7 +38,7 @@ __global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict
   pdl_wait();
   __shared__ float red[32];
   const int r = blockIdx.x, k = blockIdx.y;
-  const T* f = src[r] + (size_t)k * Ht;
+  const T* f = src[(size_t)r * K + k];  // tap k of row r
   float ss = 0.f;
   for (int j = threadIdx.x; j < Ht; j += blockDim.x) {
     const float x = to_f(f[j]);
@@ -1164,6 +1164,24 @@ __global__ void k_copy_rows(char* __restrict__ dst, int64_t dst_ld, const char* 
   }
 }
 
+// Row r of tap k (rows src_ld bytes apart from src.p[k]) to dst + r * dst_ld
+// + k * tap_bytes: K separate tap buffers into concatenated feature rows.
+__global__ void k_copy_taps(char* __restrict__ dst, int64_t dst_ld, TapSrc src, int64_t src_ld, int64_t tap_bytes,
+                            int vec) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t r = blockIdx.x;
+  const int k = blockIdx.y;
+  char* d = dst + r * dst_ld + (int64_t)k * tap_bytes;
+  const char* s = src.p[k] + r * src_ld;
+  if (vec) {
+    for (int64_t b = (int64_t)threadIdx.x * 16; b < tap_bytes; b += (int64_t)blockDim.x * 16)
+      *reinterpret_cast<uint4*>(d + b) = *reinterpret_cast<const uint4*>(s + b);
+  } else {
+    for (int64_t b = threadIdx.x; b < tap_bytes; b += blockDim.x) d[b] = s[b];
+  }
+}
+
 // Per-call tables as a kernel parameter, written to device memory once the
 // previous kernel has completed (every kernel completes only after its own
 // predecessor, so no earlier launch still reads the buffer).  Keeps the
@@ -1350,6 +1368,14 @@ void launch_copy_rows(void* dst, int64_t dst_ld, const void* src, int64_t src_ld
   const int vec = ((uintptr_t)dst | (uintptr_t)src | (uintptr_t)dst_ld | (uintptr_t)src_ld | (uintptr_t)row_bytes) % 16 == 0;
   launch_k(k_copy_rows, dim3(rows, (unsigned)cdiv(row_bytes, 4096)), 256, 0, st, (char*)dst, dst_ld, (const char*)src,
            src_ld, row_bytes, vec);
+}
+
+void launch_copy_taps(void* dst, int64_t dst_ld, const TapSrc& src, int K, int64_t src_ld, int64_t tap_bytes, int rows,
+                      cudaStream_t st) {
+  if (rows <= 0 || K <= 0) return;
+  int vec = ((uintptr_t)dst | (uint64_t)dst_ld | (uint64_t)src_ld | (uint64_t)tap_bytes) % 16 == 0;
+  for (int k = 0; k < K; ++k) vec = vec && (uintptr_t)src.p[k] % 16 == 0;
+  launch_k(k_copy_taps, dim3(rows, K), 256, 0, st, (char*)dst, dst_ld, src, src_ld, tap_bytes, vec);
 }
 
 }  // namespace dfl

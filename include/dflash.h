@@ -77,7 +77,8 @@ typedef struct dflash_session dflash_session;
 /* Draft geometry and block parameters.  Bounds checked by dflash_model_create
  * (the Laguna PR treats the drafter config as untrusted): block_size in
  * 2..512, window 0 (full attention) or 2..2^20, head_dim 64 or 128,
- * n_q_heads a multiple of n_kv_heads, bf16 widths multiples of 64. */
+ * n_q_heads a multiple of n_kv_heads, bf16 widths multiples of 64, n_taps
+ * at most 8. */
 typedef struct dflash_config {
   int32_t dtype;           /* DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16 */
   int32_t n_taps;          /* K: tapped target layers */
@@ -173,6 +174,16 @@ DFLASH_API int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max
  * Errors: INVALID_ARG, CONTEXT_GAP, CAPACITY (F + P + new rows > max_ctx). */
 DFLASH_API int dflash_committed(dflash_session* s, const void* features, int64_t row_stride, int32_t n_rows,
                      int64_t position);
+/* The same run given as the target's n_taps hidden states in separate
+ * buffers: taps is a host array of n_taps device pointers, tap k being
+ * [n_rows, H_t] with rows row_stride elements apart.  The rows are read where
+ * they are (a flush reads them in place; staged rows are copied once, tap by
+ * tap), so a target that keeps its captured hidden states apart needs no
+ * concatenation (the Laguna PR paid a copy of [1, T, 5 * hidden] per round).
+ * Same state changes and errors as dflash_committed; a null tap pointer is
+ * INVALID_ARG. */
+DFLASH_API int dflash_committed_taps(dflash_session* s, const void* const* taps /*host [n_taps]*/, int64_t row_stride,
+                                     int32_t n_rows, int64_t position);
 
 /* dflash.go flush: rewinds each session's outstanding block, then writes all
  * held rows in one batched context-only forward.  When the draft has a

@@ -457,3 +457,39 @@ def test_sessions_called_back_to_back_keep_their_own_tables(D):
     D.dflash_device_status(p.model)
     for s in sess:
         D.dflash_close(s)
+
+
+@pytest.mark.parametrize("rows", [37, 300])
+def test_committed_taps_equals_concatenated_features(D, rows):
+    """dflash_committed_taps (the target's taps in separate buffers, read in
+    place) leaves the same cache and the same next proposal as
+    dflash_committed with the concatenated rows: staged (37 rows) and
+    flushed at the threshold (300 rows)."""
+    p = Pair(S.CONFIGS["small_bf16"])
+    cfg = p.cfg
+    n, Ht, K = cfg.block_size - 1, cfg.target_hidden, cfg.n_taps
+    _, f = p.feats(rows, seed=41)
+    a = D.dflash_open(p.model, max_ctx=512)
+    b = D.dflash_open(p.model, max_ctx=512)
+    c = D.dflash_open(p.model, max_ctx=512)
+    D.dflash_committed(a, f, 0)
+    D.dflash_committed_taps(b, [f[:, k * Ht:(k + 1) * Ht] for k in range(K)], 0)          # one strided buffer
+    D.dflash_committed_taps(c, [f[:, k * Ht:(k + 1) * Ht].contiguous() for k in range(K)], 0)  # K buffers
+    assert D.dflash_session_state(b) == D.dflash_session_state(c) == D.dflash_session_state(a)
+    outs = []
+    for s in (a, b, c):
+        tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+        q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+        lg = torch.empty((1, n, cfg.vocab), dtype=torch.float32, device="cuda")
+        D.dflash_propose([s], torch.tensor([9], dtype=torch.int32, device="cuda"), n, 0.8, 3, 2, tok, q, lg)
+        torch.cuda.synchronize()
+        outs.append((tok.clone(), lg.clone(), [export_kv(D, s, cfg, l, 0, rows) for l in range(cfg.n_layers)]))
+    for o in outs[1:]:
+        assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1])
+        for (k0, v0), (k1, v1) in zip(outs[0][2], o[2]):
+            assert np.array_equal(k0, k1) and np.array_equal(v0, v1)
+    with pytest.raises(ValueError):
+        D.dflash_committed_taps(a, [f[:, :Ht]] * (K - 1), rows)
+    D.dflash_device_status(p.model)
+    for s in (a, b, c):
+        D.dflash_close(s)
