@@ -931,8 +931,9 @@ int dflash_committed(dflash_session* s, const void* features, int64_t row_stride
   if (n_rows < 0 || position < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_rows %d / position %lld", n_rows, (long long)position);
   if (n_rows > 0 && (!features || row_stride < width))
     return fail(DFLASH_ERR_INVALID_ARG, "features null or row_stride %lld < %lld", (long long)row_stride, (long long)width);
-  const char* taps[kMaxTaps];
-  for (int k = 0; k < c.n_taps; ++k) taps[k] = (const char*)features + (size_t)k * c.target_hidden * s->m->esz;
+  const char* taps[kMaxTaps] = {};
+  if (features)
+    for (int k = 0; k < c.n_taps; ++k) taps[k] = (const char*)features + (size_t)k * c.target_hidden * s->m->esz;
   return committed_impl(s, taps, row_stride * (int64_t)s->m->esz, true, n_rows, position);
 }
 
@@ -943,9 +944,9 @@ int dflash_committed_taps(dflash_session* s, const void* const* taps, int64_t ro
   if (n_rows < 0 || position < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_rows %d / position %lld", n_rows, (long long)position);
   if (n_rows > 0 && (!taps || row_stride < c.target_hidden))
     return fail(DFLASH_ERR_INVALID_ARG, "taps null or row_stride %lld < %d", (long long)row_stride, c.target_hidden);
-  const char* tp[kMaxTaps];
-  for (int k = 0; k < c.n_taps; ++k) {
-    if (n_rows > 0 && !taps[k]) return fail(DFLASH_ERR_INVALID_ARG, "tap %d is null", k);
+  const char* tp[kMaxTaps] = {};
+  for (int k = 0; k < c.n_taps && n_rows > 0; ++k) {
+    if (!taps[k]) return fail(DFLASH_ERR_INVALID_ARG, "tap %d is null", k);
     tp[k] = (const char*)taps[k];
   }
   return committed_impl(s, tp, row_stride * (int64_t)s->m->esz, false, n_rows, position);

@@ -75,6 +75,7 @@ def test_config_bounds_are_refused(lib, bad, code):
 def test_null_arguments_are_refused(lib):
     assert lib.dflash_draft_limit(None) == _abi.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_committed(None, None, 0, 0, 0) == _abi.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_committed_taps(None, None, 0, 0, 0) == _abi.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_flush(None, 1) == _abi.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_close(None) == _abi.DFLASH_ERR_INVALID_ARG
     c = _cfg()
