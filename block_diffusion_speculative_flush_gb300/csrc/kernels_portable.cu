@@ -31,6 +31,60 @@ namespace dfl {
 
 namespace {
 
+// 8 bf16 of a 16-byte word as floats, and back.
+__device__ __forceinline__ void unpack8(const uint4& w, float* v) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    u[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+// bf16 rows held in registers as 16-byte words (up to kNormVec per thread):
+// one load of each input word, one store of each output word.
+constexpr int kNormVec = 4;
+__device__ __forceinline__ bool norm_vec_ok(const void* x, const void* g, const void* o, int H) {
+  return H % 8 == 0 && H / 8 <= kNormVec * (int)blockDim.x && (((uintptr_t)x | (uintptr_t)g | (uintptr_t)o) & 15) == 0;
+}
+__device__ __forceinline__ void norm_row_vec(const bf16* x, const bf16* g, bf16* o, int H, float eps, float* red) {
+  const int nv = H / 8;
+  uint4 w[kNormVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    w[i] = c < nv ? __ldg(reinterpret_cast<const uint4*>(x) + c) : make_uint4(0, 0, 0, 0);
+    float v[8];
+    unpack8(w[i], v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)H + eps);
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    if (c >= nv) continue;
+    float v[8], gv[8];
+    unpack8(w[i], v);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(g) + c), gv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = v[e] * inv * gv[e];
+    reinterpret_cast<uint4*>(o)[c] = pack8(v);
+  }
+}
+
 template <typename T>
 __global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict__ aux, T* __restrict__ u,
                            int K, int Ht, float eps) {
@@ -39,6 +93,13 @@ __global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict
   __shared__ float red[32];
   const int r = blockIdx.x, k = blockIdx.y;
   const T* f = src[(size_t)r * K + k];  // tap k of row r
+  if constexpr (std::is_same<T, bf16>::value) {
+    T* o = u + (size_t)r * K * Ht + (size_t)k * Ht;
+    if (norm_vec_ok(f, aux + (size_t)k * Ht, o, Ht)) {
+      norm_row_vec(f, aux + (size_t)k * Ht, o, Ht, eps, red);
+      return;
+    }
+  }
   float ss = 0.f;
   for (int j = threadIdx.x; j < Ht; j += blockDim.x) {
     const float x = to_f(f[j]);
@@ -63,6 +124,13 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, in
   const int j = blockIdx.x;
   const int src = (j / a) * b + (j % a) + c;
   const TIn* x = src < rows0 ? in0 + (int64_t)src * ld_in : in1 + (int64_t)(src - rows0) * ld_in;
+  if constexpr (std::is_same<TIn, bf16>::value && std::is_same<T, bf16>::value) {
+    T* o = out + (int64_t)j * ld_out;
+    if (norm_vec_ok(x, g, o, H)) {
+      norm_row_vec(x, g, o, H, eps, red);
+      return;
+    }
+  }
   constexpr int MAXV = 8;
   float v[MAXV];
   float ss = 0.f;
