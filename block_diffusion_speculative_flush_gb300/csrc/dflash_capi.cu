@@ -535,9 +535,9 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       const char* wkv = (const char*)w.w_qkv + (size_t)qd * H * es;
       ST_TRY(gemm(m, m->x.p, H, wkv, H, m->qkv.as<float>() + qd, m->qkv_cols, M, 2 * kd, H, st));
     }
-    launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, rope, w.q_norm, w.k_norm, Hq,
-                    Hkv, d, c.gated_attention, c.rms_eps, tabs, c.n_layers, l, m->Q.p, m->G.as<float>(), st);
-    m->launches++;
+    m->launches += launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, rope, w.q_norm, w.k_norm, Hq,
+                                   Hkv, d, c.gated_attention, c.rms_eps, tabs, c.n_layers, l, m->Q.p,
+                                   m->G.as<float>(), st);
     ST_TRY(launch_check("qkv"));
     if (!block) continue;
     ap.layer = l;

@@ -68,9 +68,12 @@ void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* 
 void launch_embed(DT dt, const void* E, const int32_t* current, const int32_t* sess_map, int mask_token, int V,
                   int B, int nrows, int H, void* h, int32_t* err, cudaStream_t st);
 void launch_rope_table(const RowMeta* meta, int M, int d, float theta, float2* table, cudaStream_t st);
-void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
-                     const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
-                     SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st);
+// Returns the number of kernels launched (2 from kVApartRows rows on: the V
+// rows go to the transposed cache planes 32 rows at a time).
+constexpr int kVApartRows = 64;
+int launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
+                    const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
+                    SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st);
 void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_items, SessTables tabs,
                            AttnParams p, float* part, cudaStream_t st);
 // bf16 block attention on tcgen05 tensor cores (key ranges must start on a

@@ -195,7 +195,7 @@ template <typename T, int DU>  // DU = d / 32
 __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const RowMeta* __restrict__ meta,
                            const float2* __restrict__ rope, const T* __restrict__ q_norm,
                            const T* __restrict__ k_norm, int Hq, int Hkv, int gated, float eps, SessTables tabs,
-                           int layer, T* __restrict__ Q, float* __restrict__ G) {
+                           int layer, T* __restrict__ Q, float* __restrict__ G, int v_apart) {
   pdl_trigger();
   pdl_wait();
   constexpr int d = DU * 32;
@@ -250,8 +250,36 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
 #pragma unroll
   for (int u = 0; u < DU; ++u) {
     kd[lane + 32 * u] = from_f<T>(y[u]);
-    vd[(int64_t)(lane + 32 * u) * cap] = from_f<T>(xv[lane + 32 * u]);
+    if (!v_apart) vd[(int64_t)(lane + 32 * u) * cap] = from_f<T>(xv[lane + 32 * u]);
   }
+}
+
+// V of one KV head for 32 consecutive rows into the transposed V planes
+// ([d][cap]): the rows go through shared memory, and lane r writes row r's
+// entry of each plane row, so 32 consecutive slots of one session land as one
+// contiguous run (k_qkv_post writes them one plane row per lane otherwise).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_v_cache_t(const float* __restrict__ qkv, int64_t ldq,
+                                                   const RowMeta* __restrict__ meta, int M, int Hq, int Hkv,
+                                                   SessTables tabs, int layer) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float tile[32][D + 1];
+  const int kh = blockIdx.y, m0 = blockIdx.x * 32;
+  const int64_t col = (int64_t)(Hq + Hkv + kh) * D;
+  for (int e = threadIdx.x; e < 32 * D; e += blockDim.x) {
+    const int r = e / D, j = e % D;
+    tile[r][j] = m0 + r < M ? qkv[(int64_t)(m0 + r) * ldq + col + j] : 0.f;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int m = m0 + lane;
+  if (m >= M) return;
+  const RowMeta rm = meta[m];
+  const int64_t cap = tabs.cap[rm.sess];
+  const int64_t slot = rm.pos % cap;
+  T* vd = (T*)tabs.kv[rm.sess] + ((int64_t)(2 * layer + 1) * Hkv + kh) * cap * D + slot;
+  for (int j = w; j < D; j += nw) vd[(int64_t)j * cap] = from_f<T>(tile[lane][j]);
 }
 
 // Key visibility for block row i (position F + i) and key position r.
@@ -1313,22 +1341,31 @@ void launch_rope_table(const RowMeta* meta, int M, int d, float theta, float2* t
   launch_k(k_rope_table, M, d / 2, 0, st, meta, d, theta, table);
 }
 
-void launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
-                     const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
-                     SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st) {
+int launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
+                    const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
+                    SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st) {
   (void)L;
-  if (M <= 0) return;
+  if (M <= 0) return 0;
   const int heads = Hq + Hkv;
   dim3 grid(M, cdiv(heads, 4));
+  // many rows: V goes to the cache in a second kernel, 32 rows at a time
+  const int v_apart = M >= kVApartRows;
   if (d == 64) {
     DFL_DISPATCH(dt, launch_k(k_qkv_post<T, 2>, grid, 128, 0, st, qkv, ldq, meta, rope, (const T*)q_norm,
                                                               (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
-                                                              (T*)Q, G));
+                                                              (T*)Q, G, v_apart));
+    if (v_apart)
+      DFL_DISPATCH(dt, launch_k(k_v_cache_t<T, 64>, dim3(cdiv(M, 32), Hkv), 256, 0, st, qkv, ldq, meta, M, Hq, Hkv,
+                                tabs, layer));
   } else {
     DFL_DISPATCH(dt, launch_k(k_qkv_post<T, 4>, grid, 128, 0, st, qkv, ldq, meta, rope, (const T*)q_norm,
                                                               (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
-                                                              (T*)Q, G));
+                                                              (T*)Q, G, v_apart));
+    if (v_apart)
+      DFL_DISPATCH(dt, launch_k(k_v_cache_t<T, 128>, dim3(cdiv(M, 32), Hkv), 256, 0, st, qkv, ldq, meta, M, Hq, Hkv,
+                                tabs, layer));
   }
+  return 1 + v_apart;
 }
 
 void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p,
