@@ -1,5 +1,28 @@
 """Shared helpers of the GPU parity tests: one seeded input set handed to both
-the CUDA library (through the C ABI binding) and the CPU oracle."""
+the CUDA library (through the C ABI binding) and the CPU oracle.
+
+The parity bar.
+  * Token ids, accept lengths and bonus tokens are bit-exact with the
+    oracle's, except in a row whose oracle top-2 score margin (of the logits
+    at T = 0, of the Gumbel-perturbed scores at T > 0) is below 1e-3.  Every
+    check returns how many rows it exempted and the callers cap that count.
+  * Logits: max-abs 1e-4 (fp32 configs) and 2e-2 (bf16 configs); q: 1e-3.
+
+The full-size bf16 drafts (hidden 3072 / 4096, 4-5 layers) do not meet the
+logit bar or the token rule as written, and the tests there assert a stated
+departure instead (assert_logits_full, check_tokens_full).  Both sides round
+to bf16 at the same storage points, but a value that lands within the fp32
+/ fp64 difference of a rounding boundary flips by one ulp on one side; the
+next product spreads the flip over every output, where it seeds more flips,
+so the difference settles near one bf16 ulp per stored element.  Measured on
+a GB300: max-abs 0.064-0.075 (RMS 0.0123) on the Qwen3-8B-shaped draft's
+logits, 0.047-0.051 on the Laguna-style draft's, with 2-11% of the logits
+above 2e-2; the small test drafts stay below 0.012.  At full size the token
+rule is therefore checked in two parts: the GPU's draw must equal the
+oracle's decision on the GPU's own logits (bit-exact, 1e-3 margin), and a
+row that differs from the oracle's own draw must have an oracle margin
+within what the measured logit difference can move (2 * max-abs / T).
+"""
 from __future__ import annotations
 
 import numpy as np
@@ -12,21 +35,22 @@ from oracle import dflash_oracle as O
 TOL_LOGITS = {"f32": 1e-4, "bf16": 2e-2}
 TOL_Q = 1e-3
 MARGIN = 1e-3
-# Full-size bf16 drafts: both sides round to bf16 at the same points, but a
-# 1-ulp flip seeded by fp32-vs-fp64 accumulation spreads through every later
-# product, so the difference grows with depth x width (sigma ~ 0.012 on
-# logits of std ~1.3 at 5 layers x 4096).  The 2e-2 bar is then met as the
-# RMS difference; the maximum over millions of logits (~5 sigma) is bounded
-# at 0.1.
-TOL_LOGITS_RMS_FULL = 2e-2
+# the stated full-size departure (see the module docstring): max-abs bound and
+# the RMS, which stays within the 2e-2 bar
 TOL_LOGITS_MAX_FULL = 0.1
+TOL_LOGITS_RMS_FULL = 2e-2
+# an acceptance test r * q(d) < p(d) within this relative distance of its
+# threshold is decided by fp32 rounding on the GPU (fp64 in the oracle)
+ACCEPT_RTOL = 1e-5
 
 
 def assert_logits_full(g, ref):
-    d = np.asarray(g, dtype=np.float64) - np.asarray(ref, dtype=np.float64)
-    rms, mx = float(np.sqrt(np.mean(d * d))), float(np.max(np.abs(d)))
-    assert rms <= TOL_LOGITS_RMS_FULL and mx <= TOL_LOGITS_MAX_FULL, (rms, mx)
-    return rms, mx
+    """Full-size bf16 logits: max-abs within the stated departure bound and the
+    RMS within 2e-2.  Returns (rms, max-abs, count above 2e-2, count)."""
+    d = np.abs(np.asarray(g, dtype=np.float64) - np.asarray(ref, dtype=np.float64))
+    rms, mx = float(np.sqrt(np.mean(d * d))), float(np.max(d))
+    assert mx <= TOL_LOGITS_MAX_FULL and rms <= TOL_LOGITS_RMS_FULL, (rms, mx)
+    return rms, mx, int(np.count_nonzero(d > TOL_LOGITS["bf16"])), int(d.size)
 
 
 def assert_cache_close(g, ref, tol=2e-2):
@@ -83,27 +107,104 @@ def oracle_scores(logits, T, seed, rnd, seq):
     return np.array(out)
 
 
-def check_tokens(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq):
-    """Token ids must equal the oracle's.  The one exemption is a row where the
-    two sides' logits differ by delta and the oracle's score of the GPU's
-    token is within max(1e-3, 2 delta / T) of the oracle's top score: there
-    the choice is decided by rounding, not by the method (bf16 storage at the
-    same points on both sides still leaves logits up to ~1e-2 apart).
-    Returns the number of exempted rows."""
+def top2_margin(scores) -> float:
+    s = np.sort(np.asarray(scores, dtype=np.float64))
+    return float(s[-1] - s[-2])
+
+
+def check_tokens(gpu_tok, ora_logits, T, seed, rnd, seq, cap=1):
+    """The stated rule: each GPU token equals the oracle's, except in a row
+    whose oracle top-2 score margin is below 1e-3.  Asserts that at most `cap`
+    rows were exempted and returns their number."""
     gpu_tok = np.asarray(gpu_tok).reshape(-1)
-    gl = np.atleast_2d(np.asarray(gpu_logits, dtype=np.float64))
-    ol = np.atleast_2d(np.asarray(ora_logits, dtype=np.float64))
-    sc = oracle_scores(ol, T, seed, rnd, seq)
-    teff = T if T > 0 else 1.0
+    sc = oracle_scores(ora_logits, T, seed, rnd, seq)
     exempt = 0
     for i in range(len(gpu_tok)):
         top = int(np.argmax(sc[i]))
         g = int(gpu_tok[i])
         if g == top:
             continue
-        delta = float(np.max(np.abs(gl[i] - ol[i])))
-        bound = max(MARGIN, 2.0 * delta / teff)
-        gap = sc[i][top] - sc[i][g]
-        assert gap <= bound, f"row {i}: gpu token {g}, oracle {top}, score gap {gap:.3g} > bound {bound:.3g}"
+        m = top2_margin(sc[i])
+        assert m < MARGIN, f"row {i}: gpu token {g}, oracle {top}, oracle top-2 margin {m:.3g}"
         exempt += 1
+    assert exempt <= cap, f"{exempt} rows exempted (cap {cap})"
     return exempt
+
+
+def check_tokens_full(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq, cap=2):
+    """Full-size token check (the stated departure of the module docstring).
+
+    1. The GPU's draw equals the oracle's decision on the GPU's own logits,
+       except where that decision's top-2 margin is below 1e-3.
+    2. A row that differs from the oracle's draw on the oracle's logits has
+       an oracle margin of at most 2 * (that row's max-abs logit difference) / T
+       (T = 1 for greedy), and at most `cap` rows differ that way.
+    Returns (rows differing from the oracle's own draw, rows exempted in 1)."""
+    gpu_tok = np.asarray(gpu_tok).reshape(-1)
+    gl = np.atleast_2d(np.asarray(gpu_logits, dtype=np.float64))
+    ol = np.atleast_2d(np.asarray(ora_logits, dtype=np.float64))
+    own = oracle_scores(gl, T, seed, rnd, seq)
+    sc = oracle_scores(ol, T, seed, rnd, seq)
+    teff = T if T > 0 else 1.0
+    own_exempt = differ = 0
+    for i in range(len(gpu_tok)):
+        g = int(gpu_tok[i])
+        if g != int(np.argmax(own[i])):
+            assert top2_margin(own[i]) < MARGIN, f"row {i}: draw {g} is not the oracle's choice on the same logits"
+            own_exempt += 1
+        top = int(np.argmax(sc[i]))
+        if g == top:
+            continue
+        m = top2_margin(sc[i])
+        if m < MARGIN:
+            continue
+        bound = 2.0 * float(np.max(np.abs(gl[i] - ol[i]))) / teff
+        assert sc[i][top] - sc[i][g] <= bound, f"row {i}: oracle margin {m:.3g} above the logit-difference bound"
+        differ += 1
+    assert differ <= cap and own_exempt <= 1, (differ, own_exempt)
+    return differ, own_exempt
+
+
+def verify_parity(gpu_ab, target_logits, draft_tokens, draft_logits, proposed, draft_T, T, seed, rnd, seq,
+                  trunc=None, draft_trunc=None):
+    """dflash_verify's (accept, bonus) against the oracle's verify on the same
+    inputs: the target logits and the draft logits that the GPU session keeps
+    from its proposal (copied back).  A result may differ only where the
+    decision lies within rounding of its threshold: an acceptance test
+    r q(d) < p(d) within ACCEPT_RTOL, or a bonus draw whose top-2 score margin
+    is below 1e-3.  Returns True when the pair was compared, False when
+    exempted."""
+    tl = np.asarray(target_logits, dtype=np.float64)
+    dl = np.asarray(draft_logits, dtype=np.float64)
+    a_ref, b_ref = O.verify(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc)
+    if tuple(int(x) for x in gpu_ab) == (a_ref, b_ref):
+        return True
+    assert _verify_near(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc), \
+        (tuple(int(x) for x in gpu_ab), (a_ref, b_ref))
+    return False
+
+
+def _verify_near(tl, d, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc):
+    """True when some decision of this verify lies within rounding of its threshold."""
+    n, V = len(d), tl.shape[1]
+    if T == 0:
+        for i in range(n + 1):
+            if top2_margin(tl[i]) < MARGIN:
+                return True
+        return False
+    for i in range(1, n + 1):
+        p = O.sampler_distribution(tl[i - 1], T, trunc)
+        q = O.proposal_distribution(dl[i - 1], draft_T, proposed[i - 1], draft_trunc)
+        r = O.uniform_open(O.random_u32(seed, rnd, O.STREAM_ACCEPT, seq, i, 0))
+        x, y = r * q[int(d[i - 1])], p[int(d[i - 1])]
+        if abs(x - y) <= ACCEPT_RTOL * max(abs(y), 1e-300):
+            return True
+        if not x < y:
+            res = np.maximum(p - q, 0.0)
+            w, row = (res if res.sum() > 0 else p), i
+            break
+    else:
+        w, row = O.sampler_distribution(tl[n], T, trunc), n + 1
+    with np.errstate(divide="ignore"):
+        sc = np.log(w) + O.gumbel(seed, rnd, O.STREAM_BONUS, seq, row, np.arange(V))
+    return top2_margin(sc) < MARGIN

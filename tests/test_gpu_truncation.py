@@ -124,17 +124,20 @@ def test_truncated_batched_propose_and_verify(D, cfg_name):
     bon = torch.empty(3, dtype=torch.int32, device="cuda")
     D.dflash_verify(sess, torch.from_numpy(tl_np).cuda(), torch.from_numpy(d_np).cuda(), n, T, 17, 4, acc, bon)
     torch.cuda.synchronize()
+    compared = 0
     for b in range(3):
         tr = samplers[b]
-        # the oracle on the GPU's draft logits (q) and the same target logits (p)
-        if not all(_clear(tl_np[b][i].astype(np.float64) / T, tr, 1e-5) for i in range(n + 1)):
-            continue
-        if not all(_clear(g_lg[b][i] / T, tr, 1e-5) for i in range(n)):
+        # the oracle on the GPU's draft logits (q) and the same target logits
+        # (p); a support or a decision within rounding of its boundary is
+        # exempt, and the test counts the sessions actually compared
+        clear = all(_clear(tl_np[b][i].astype(np.float64) / T, tr, 1e-5) for i in range(n + 1)) and \
+            all(_clear(g_lg[b][i] / T, tr, 1e-5) for i in range(n))
+        if not clear or _near(tl_np[b], d_np[b], g_lg[b], T, tr, 17, 4, b):
             continue
         a_ref, b_ref = O.verify(tl_np[b].astype(np.float64), d_np[b], g_lg[b], d_np[b], T, T, 17, 4, b, tr, tr)
-        if _near(tl_np[b], d_np[b], g_lg[b], T, tr, 17, 4, b):
-            continue
         assert (int(acc[b]), int(bon[b])) == (a_ref, b_ref), (b, int(acc[b]), int(bon[b]), a_ref, b_ref)
+        compared += 1
+    assert compared >= 2, compared
     D.dflash_device_status(p.model)
     for s in sess:
         D.dflash_close(s)
@@ -240,18 +243,22 @@ def test_truncated_draw_at_full_vocabulary(D):
     tl_np = S.make_target_logits(1, n + 1, V, d_np, seed=9, std=3.0, boost=6.0)
     acc = torch.empty(1, dtype=torch.int32, device="cuda")
     bon = torch.empty(1, dtype=torch.int32, device="cuda")
-    D.dflash_verify([s], torch.from_numpy(tl_np).cuda(), torch.from_numpy(d_np).cuda(), n, T, 31, 1, acc, bon)
-    torch.cuda.synchronize()
-    a_ref, b_ref = O.verify(tl_np[0].astype(np.float64), d_np[0], g_lg, d_np[0], T, T, 31, 1, 0, tr, tr)
-    clear = all(_clear(tl_np[0][i].astype(np.float64) / T, tr, 1e-5) for i in range(n + 1)) and \
-        all(_clear(g_lg[i] / T, tr, 1e-5) for i in range(n))
-    if clear and not _near(tl_np[0], d_np[0], g_lg, T, tr, 31, 1, 0):
-        assert (int(acc[0]), int(bon[0])) == (a_ref, b_ref)
-    # the bonus comes from the residual or from p of the row after the prefix:
-    # either way from that row's truncated support
-    row = tl_np[0][int(acc[0])].astype(np.float64) / T
-    if _clear(row, tr, 1e-5):
-        assert int(bon[0]) in set(O.truncated_support(row, *tr).tolist())
+    clear_q = all(_clear(g_lg[i] / T, tr, 1e-5) for i in range(n))
+    compared = 0
+    for rnd in range(1, 7):
+        D.dflash_verify([s], torch.from_numpy(tl_np).cuda(), torch.from_numpy(d_np).cuda(), n, T, 31, rnd, acc, bon)
+        torch.cuda.synchronize()
+        a_ref, b_ref = O.verify(tl_np[0].astype(np.float64), d_np[0], g_lg, d_np[0], T, T, 31, rnd, 0, tr, tr)
+        clear = clear_q and all(_clear(tl_np[0][i].astype(np.float64) / T, tr, 1e-5) for i in range(n + 1))
+        if clear and not _near(tl_np[0], d_np[0], g_lg, T, tr, 31, rnd, 0):
+            assert (int(acc[0]), int(bon[0])) == (a_ref, b_ref), rnd
+            compared += 1
+        # the bonus comes from the residual or from p of the row after the
+        # prefix: either way from that row's truncated support
+        row = tl_np[0][int(acc[0])].astype(np.float64) / T
+        if _clear(row, tr, 1e-5):
+            assert int(bon[0]) in set(O.truncated_support(row, *tr).tolist())
+    assert compared >= 3, compared
     D.dflash_device_status(p.model)
     D.dflash_close(s)
 
