@@ -192,6 +192,7 @@ struct dflash_session {
   Trunc trunc{0, 1.f, 0.f, 0};  // the sampler's truncation (top_k 0: full distributions)
   bool last_trunc = false;      // the last proposal was drawn from a truncated distribution
   int64_t rounds = 0, proposed = 0, flushes = 0, flushed_rows = 0;
+  int device = 0;               // the CUDA device that was current at dflash_open
 };
 
 namespace {
@@ -712,6 +713,26 @@ int dflash__session_proposal(const dflash_session* s, const float** logits, cons
   return DFLASH_OK;
 }
 
+int dflash__session_device(const dflash_session* s) { return s->device; }
+
+// A Timed bracket that the allocation-free verify can open and close across
+// its launches (the class is kVerify); the handle is an index into the
+// model's records, or -1 while timing is off.
+long long dflash__verify_timing_begin(const void* model, double bytes, double flops, void* stream) {
+  dflash_model* m = (dflash_model*)model;
+  Timed t(m, kVerify, bytes, flops, (cudaStream_t)stream);
+  const long long idx = t.idx == (size_t)-1 ? -1 : (long long)t.idx;
+  t.idx = (size_t)-1;  // closed by dflash__verify_timing_end
+  return idx;
+}
+
+void dflash__verify_timing_end(const void* model, long long idx, void* stream) {
+  dflash_model* m = (dflash_model*)model;
+  if (idx >= 0 && (size_t)idx < m->recs.size()) cudaEventRecord(m->recs[(size_t)idx].e1, (cudaStream_t)stream);
+}
+
+void dflash__count_launches(const void* model, int n) { ((dflash_model*)model)->launches += n; }
+
 const char* dflash_last_error(void) { return g_err.c_str(); }
 int dflash_version(void) { return 100; }
 
@@ -833,6 +854,7 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
   dflash_session* s = new dflash_session();
   s->m = m;
   s->stream = (cudaStream_t)stream;
+  if (cudaGetDevice(&s->device) != cudaSuccess) s->device = 0;
   s->F = restored_offset;
   s->max_ctx = max_ctx;
   s->cap = c.window ? align_up((int64_t)c.window + c.block_size, 64) : align_up(max_ctx + c.block_size, 64);
@@ -1141,7 +1163,7 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   ST_TRY(m->vbonus.ensure((size_t)batch * bchunks * sizeof(VerifyPart) + (size_t)batch * 4, st));
   va.rej = (int32_t*)(m->vbonus.as<char>() + (size_t)batch * bchunks * sizeof(VerifyPart));
   launch_verify_accept(va, m->vbonus.as<VerifyPart>(), st);
-  m->launches += temperature > 0.f ? 1 : 0;
+  m->launches += temperature > 0.f ? 2 : 1;  // bonus draw (T > 0) and finish
   return launch_check("verify");
 }
 

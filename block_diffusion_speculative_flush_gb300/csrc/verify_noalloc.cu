@@ -23,12 +23,17 @@
 
 using namespace dfl;
 
-// Accessors into the session and the error string (dflash_capi.cu; not exported).
+// Accessors into the session, the model's measurement state and the error
+// string (dflash_capi.cu; not exported).
 extern "C" int dflash__session_proposal(const dflash_session* s, const float** logits, const float** lse,
                                         const int32_t** tokens, float* temperature, int32_t* n,
                                         long long** accepted, void** stream, int32_t* vocab, int32_t* draft_limit,
                                         int32_t** err, const void** model);
 extern "C" int dflash__session_truncation(const dflash_session* s, Trunc* trunc, const uint64_t** proposal_cut);
+extern "C" int dflash__session_device(const dflash_session* s);
+extern "C" long long dflash__verify_timing_begin(const void* model, double bytes, double flops, void* stream);
+extern "C" void dflash__verify_timing_end(const void* model, long long idx, void* stream);
+extern "C" void dflash__count_launches(const void* model, int n);
 extern "C" int dflash__set_error(int code, const char* msg);
 
 namespace {
@@ -47,23 +52,35 @@ static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 std::mutex g_mu;
 void* g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per
-// device (the host-side symbol is only a stand-in, not a device address).
-int scratch_on_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return dflash__set_error(DFLASH_ERR_CUDA, cudaGetErrorString(e));
+// Device address of the scratch on device `dev`, looked up once per device
+// with that device current (the host-side symbol is only a stand-in, not a
+// device address).  The caller has made `dev` current.
+int scratch_on_device(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return dflash__set_error(DFLASH_ERR_CUDA, "device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_verify_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_verify_scratch);
     if (e != cudaSuccess) return dflash__set_error(DFLASH_ERR_CUDA, cudaGetErrorString(e));
     g_scratch[dev] = p;
   }
   *out = g_scratch[dev];
   return DFLASH_OK;
 }
+
+// Makes the sessions' device current for the life of the object and puts
+// the caller's device back afterwards.
+struct DeviceScope {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceScope(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = prev == dev || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceScope() {
+    if (ok && prev >= 0) cudaSetDevice(prev);
+  }
+};
 
 constexpr size_t up16(size_t x) { return (x + 15) & ~(size_t)15; }
 
@@ -168,15 +185,23 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
              batch, n + 1, chunks, off, kScratchBytes);
     return dflash__set_error(DFLASH_ERR_CAPACITY, msg);
   }
+  // the scratch and the launches belong to the sessions' device, whatever
+  // device the caller has current
+  const int dev = dflash__session_device(s[0]);
+  DeviceScope scope(dev);
+  if (!scope.ok) return dflash__set_error(DFLASH_ERR_CUDA, "cannot make the sessions' device current");
   void* scratch = nullptr;
-  int rc = scratch_on_current_device(&scratch);
+  int rc = scratch_on_device(dev, &scratch);
   if (rc != DFLASH_OK) return rc;
   char* base = (char*)scratch;
   cudaStream_t st = (cudaStream_t)stream;
 
-  // tables: one copy from a host staging block on the stack
+  // tables: staged on the stack, then written by a one-CTA kernel that takes
+  // them as its parameter, in stream order (no host-to-device copy, so the
+  // call never waits for the stream; the block is at most ~8 KB)
   alignas(16) char host[up16(kMaxBatch * sizeof(void*)) * 5 + up16(kMaxBatch * sizeof(float)) +
                         up16(kMaxBatch * sizeof(int32_t)) + up16(kMaxBatch * sizeof(Trunc))];
+  static_assert(sizeof(host) <= (size_t)kTableParamMax, "verify tables exceed a kernel parameter block");
   memcpy(host + o_dl, dl, batch * sizeof(void*));
   memcpy(host + o_dlse, dlse, batch * sizeof(void*));
   memcpy(host + o_dtok, dtok, batch * sizeof(void*));
@@ -185,9 +210,13 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   memcpy(host + o_seq, seq, batch * sizeof(int32_t));
   memcpy(host + o_trunc, trv, batch * sizeof(Trunc));
   memcpy(host + o_dcut, dcut, batch * sizeof(void*));
-  // a copy from pageable memory returns only once the source has been read
-  cudaError_t e = cudaMemcpyAsync(base, host, tables_end, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return dflash__set_error(DFLASH_ERR_CUDA, cudaGetErrorString(e));
+  const double tbytes = (double)rows * V * (logits_dtype == DFLASH_DTYPE_BF16 ? 2 : 4) + (double)batch * V * 4;
+  const long long timed = dflash__verify_timing_begin(model, tbytes, 4.0 * rows * V, stream);
+  if (launch_table_write(base, host, tables_end, st)) {
+    dflash__verify_timing_end(model, timed, stream);
+    return dflash__set_error(DFLASH_ERR_CUDA, "verify table write launch");
+  }
+  cudaError_t e = cudaSuccess;
   // nothing in the scratch has to start at zero: every partial, statistic and
   // the rejection index are written before they are read
 
@@ -236,6 +265,8 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   va.cut_t = sa.cut;
   va.dcut = any_dcut ? (const uint64_t* const*)(base + o_dcut) : nullptr;
   launch_verify_accept(va, (VerifyPart*)(base + o_bonus), st);
+  dflash__verify_timing_end(model, timed, stream);
+  dflash__count_launches(model, 3 + (any_trunc ? 1 : 0) + (temperature > 0.f ? 2 : 1));
   e = cudaGetLastError();
   if (e != cudaSuccess) return dflash__set_error(DFLASH_ERR_CUDA, cudaGetErrorString(e));
   return DFLASH_OK;

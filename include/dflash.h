@@ -255,11 +255,16 @@ DFLASH_API int dflash_verify(dflash_session* const* s /*host [batch]*/, int32_t 
  * process exits.  Limits: at most 128 sessions per call, and
  * batch * (n + 1) * ceil(V / 4096) 16-byte row partials plus the bonus
  * partials must fit the 4 MiB (about 200k partials); larger calls return
- * DFLASH_ERR_CAPACITY and change nothing.  The first call on a device looks
- * up the scratch's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Every call
- * shares the one scratch area, so calls that overlap on the GPU (different
- * streams, no ordering between them) race; issue them in stream order.
+ * DFLASH_ERR_CAPACITY and change nothing.  The call runs on the device the
+ * sessions were opened on: it makes that device current for its duration and
+ * restores the caller's afterwards.  The first call on a device looks up the
+ * scratch's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  The per-session tables
+ * travel as a kernel parameter, so the call does not wait for the stream.
+ * Every call shares the one scratch area and leaves its contents there, so
+ * calls that overlap on the GPU (different streams, no ordering between
+ * them) race; issue them in stream order.  With timing on
+ * (dflash_timing_enable) the call is timed and counted as dflash_verify is.
  * Arguments, outputs and errors otherwise as dflash_verify. */
 DFLASH_API int dflash_verify_noalloc(dflash_session* const* s /*host [batch]*/, int32_t batch,
                                      const void* target_logits, int32_t logits_dtype, const int32_t* draft_tokens,

@@ -8,20 +8,22 @@ The parity bar.
     check returns how many rows it exempted and the callers cap that count.
   * Logits: max-abs 1e-4 (fp32 configs) and 2e-2 (bf16 configs); q: 1e-3.
 
-The full-size bf16 drafts (hidden 3072 / 4096, 4-5 layers) do not meet the
-logit bar or the token rule as written, and the tests there assert a stated
-departure instead (assert_logits_full, check_tokens_full).  Both sides round
-to bf16 at the same storage points, but a value that lands within the fp32
-/ fp64 difference of a rounding boundary flips by one ulp on one side; the
-next product spreads the flip over every output, where it seeds more flips,
-so the difference settles near one bf16 ulp per stored element.  Measured on
-a GB300: max-abs 0.064-0.075 (RMS 0.0123) on the Qwen3-8B-shaped draft's
-logits, 0.047-0.051 on the Laguna-style draft's, with 2-11% of the logits
-above 2e-2; the small test drafts stay below 0.012.  At full size the token
-rule is therefore checked in two parts: the GPU's draw must equal the
-oracle's decision on the GPU's own logits (bit-exact, 1e-3 margin), and a
-row that differs from the oracle's own draw must have an oracle margin
-within what the measured logit difference can move (2 * max-abs / T).
+The bf16 drafts do not meet the token rule as written, and the full-size
+ones (hidden 3072 / 4096, 4-5 layers) not the logit bar either; the tests
+assert a stated departure instead (check_tokens_bf16, assert_logits_full).
+Both sides round to bf16 at the same storage points, but a value that lands
+within the fp32 / fp64 difference of a rounding boundary flips by one ulp on
+one side; the next product spreads the flip over every output, where it
+seeds more flips, so the difference settles near one bf16 ulp per stored
+element.  Measured on a GB300: max-abs 0.007-0.011 on the small bf16 drafts'
+logits, 0.064-0.075 (RMS 0.0123) on the Qwen3-8B-shaped draft's and
+0.047-0.051 on the Laguna-style draft's, with 2-11% of the full-size logits
+above 2e-2.  A draw then follows the logits it is given: on a bf16 draft the
+token rule is checked in two parts.  The GPU's draw must equal the oracle's
+decision on the GPU's own logits (bit-exact, 1e-3 margin), and a row that
+differs from the oracle's draw on the oracle's logits must have an oracle
+margin within what the logit difference can move (2 * max-abs / T); such
+rows are counted and capped.  The fp32 draft meets the rule as written.
 """
 from __future__ import annotations
 
@@ -113,9 +115,9 @@ def top2_margin(scores) -> float:
 
 
 def check_tokens(gpu_tok, ora_logits, T, seed, rnd, seq, cap=1):
-    """The stated rule: each GPU token equals the oracle's, except in a row
-    whose oracle top-2 score margin is below 1e-3.  Asserts that at most `cap`
-    rows were exempted and returns their number."""
+    """The stated rule (fp32 drafts): each GPU token equals the oracle's,
+    except in a row whose oracle top-2 score margin is below 1e-3.  Asserts
+    that at most `cap` rows were exempted and returns their number."""
     gpu_tok = np.asarray(gpu_tok).reshape(-1)
     sc = oracle_scores(ora_logits, T, seed, rnd, seq)
     exempt = 0
@@ -131,14 +133,15 @@ def check_tokens(gpu_tok, ora_logits, T, seed, rnd, seq, cap=1):
     return exempt
 
 
-def check_tokens_full(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq, cap=2):
-    """Full-size token check (the stated departure of the module docstring).
+def check_tokens_bf16(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq, cap=None):
+    """Token check of a bf16 draft (the stated departure of the module docstring).
 
     1. The GPU's draw equals the oracle's decision on the GPU's own logits,
-       except where that decision's top-2 margin is below 1e-3.
-    2. A row that differs from the oracle's draw on the oracle's logits has
-       an oracle margin of at most 2 * (that row's max-abs logit difference) / T
-       (T = 1 for greedy), and at most `cap` rows differ that way.
+       except where that decision's top-2 margin is below 1e-3 (at most one row).
+    2. A row that differs from the oracle's draw on the oracle's logits, with
+       an oracle margin of 1e-3 or more, has an oracle score gap of at most
+       2 * (that row's max-abs logit difference) / T (T = 1 for greedy); at
+       most `cap` rows (default: a fifth of the rows, at least 2) differ so.
     Returns (rows differing from the oracle's own draw, rows exempted in 1)."""
     gpu_tok = np.asarray(gpu_tok).reshape(-1)
     gl = np.atleast_2d(np.asarray(gpu_logits, dtype=np.float64))
@@ -146,6 +149,7 @@ def check_tokens_full(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq, cap=2)
     own = oracle_scores(gl, T, seed, rnd, seq)
     sc = oracle_scores(ol, T, seed, rnd, seq)
     teff = T if T > 0 else 1.0
+    cap = max(2, len(gpu_tok) // 5) if cap is None else cap
     own_exempt = differ = 0
     for i in range(len(gpu_tok)):
         g = int(gpu_tok[i])
@@ -153,16 +157,21 @@ def check_tokens_full(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq, cap=2)
             assert top2_margin(own[i]) < MARGIN, f"row {i}: draw {g} is not the oracle's choice on the same logits"
             own_exempt += 1
         top = int(np.argmax(sc[i]))
-        if g == top:
-            continue
-        m = top2_margin(sc[i])
-        if m < MARGIN:
+        if g == top or top2_margin(sc[i]) < MARGIN:
             continue
         bound = 2.0 * float(np.max(np.abs(gl[i] - ol[i]))) / teff
-        assert sc[i][top] - sc[i][g] <= bound, f"row {i}: oracle margin {m:.3g} above the logit-difference bound"
+        gap = sc[i][top] - sc[i][g]
+        assert gap <= bound, f"row {i}: oracle score gap {gap:.3g} above the logit-difference bound {bound:.3g}"
         differ += 1
     assert differ <= cap and own_exempt <= 1, (differ, own_exempt)
     return differ, own_exempt
+
+
+def check_tokens_for(cfg, gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq):
+    """The token rule of the draft's storage type."""
+    if cfg.dtype == "f32":
+        return check_tokens(gpu_tok, ora_logits, T, seed, rnd, seq)
+    return check_tokens_bf16(gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq)
 
 
 def verify_parity(gpu_ab, target_logits, draft_tokens, draft_logits, proposed, draft_T, T, seed, rnd, seq,

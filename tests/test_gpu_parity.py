@@ -10,7 +10,7 @@ import synthetic as S
 from oracle import dflash_oracle as O
 from oracle.target_oracle import OracleTarget
 from synthetic.target import TARGET_TINY, make_target_weights
-from tests.gpu_util import (TOL_LOGITS, TOL_Q, Pair, assert_cache_close, check_tokens, export_kv, lib,
+from tests.gpu_util import (TOL_LOGITS, TOL_Q, Pair, assert_cache_close, check_tokens_for, export_kv, lib,
                             verify_parity)
 
 pytestmark = pytest.mark.gpu
@@ -89,7 +89,7 @@ def test_propose_matches_oracle(D, pair, T):
         err = np.max(np.abs(g_lg - ref["logits"]))
         assert err <= TOL_LOGITS[cfg.dtype], err
         g_tok = tok[0].cpu().numpy()
-        check_tokens(g_tok, ref["logits"], T, 1234, rnd, 0)
+        check_tokens_for(cfg, g_tok, g_lg, ref["logits"], T, 1234, rnd, 0)
         same = g_tok == ref["tokens"]
         assert np.max(np.abs(q[0].cpu().numpy()[same] - ref["q"][same])) <= TOL_Q
         assert D.dflash_session_state(s) == (os_.F, 0, True)
@@ -251,7 +251,7 @@ def test_batched_propose_and_verify(D, cfg_name, T):
     g_tok = tok.cpu().numpy()
     for b in range(3):
         assert np.max(np.abs(g_lg[b] - refs[b]["logits"])) <= TOL_LOGITS[cfg.dtype]
-        check_tokens(g_tok[b], refs[b]["logits"], T, 77, 5, b)
+        check_tokens_for(cfg, g_tok[b], g_lg[b], refs[b]["logits"], T, 77, 5, b)
     # verify on both sides: the oracle reads the draft logits that the GPU
     # session keeps from its proposal and the same target logits
     d_np = np.stack([r["tokens"] for r in refs]).astype(np.int32)
@@ -348,7 +348,7 @@ def test_windowed_rounds_follow_the_oracle(D, block):
         g_lg = lg[0].double().cpu().numpy()
         assert np.all(np.isfinite(g_lg)), f"round {r}: non-finite logits"
         assert np.max(np.abs(g_lg - ref["logits"])) <= TOL_LOGITS["bf16"], r
-        check_tokens(tok[0].cpu().numpy(), ref["logits"], 1.0, 3, r, 0)
+        check_tokens_for(cfg, tok[0].cpu().numpy(), g_lg, ref["logits"], 1.0, 3, r, 0)
     D.dflash_device_status(p.model)
     D.dflash_close(s)
 
