@@ -38,7 +38,15 @@ Readings where the pages are silent:
   R13 full-vocabulary distributions unless the session sets a truncation;
   R24 truncation = top-k, softmax, top-p, min-p, each keeping a prefix of
   the (value desc, id asc) order, for draft and target rows alike;  R15 if the
-  residual max(0, p - q) sums to zero, the bonus is drawn from p.
+  residual max(0, p - q) sums to zero, the bonus is drawn from p;
+  R25 penalties are the sampler's repetition, presence and frequency
+  penalties over a token history the caller supplies: an id seen c > 0
+  times has a positive logit divided by the repetition penalty and a
+  non-positive one multiplied by it, then loses the presence penalty once
+  and the frequency penalty c times;  R26 every draft row sees the same
+  committed history (no row of the block counts toward another's
+  penalties), while target row r of verify sees that history plus the draft
+  tokens d_1..d_r before it, the history classic decoding would have had.
 
 Storage rounding: for bf16 configs the values that the CUDA path stores in
 bf16 are rounded to the nearest bf16 here too (u, c, the layer inputs fed to
@@ -392,6 +400,38 @@ def truncation_active(trunc) -> bool:
     return trunc is not None and (trunc[0] > 0 or trunc[1] < 1.0 or trunc[2] > 0.0)
 
 
+def apply_penalties(logits_row, history, repeat=1.0, presence=0.0, frequency=0.0):
+    """One row of logits after the sampler's penalties over `history` (R25).
+
+    For every id that occurs c > 0 times in the history: a positive logit is
+    divided by `repeat` and a non-positive one multiplied by it; then
+    `presence` is subtracted once and `frequency` c times.  Ids that do not
+    occur are unchanged.  ("Ollama DFlash block-diffusion draft model in
+    mlxrunner", Facts: penalties see only committed history, not other rows
+    of the block; dflash.go selectBlock.)
+    """
+    out = np.array(logits_row, dtype=np.float64)
+    ids, counts = np.unique(np.asarray(history, dtype=np.int64), return_counts=True)
+    for v, c in zip(ids, counts):
+        x = out[v]
+        x = x / repeat if x > 0 else x * repeat
+        out[v] = x - presence - frequency * float(c)
+    return out
+
+
+def penalties_active(pen) -> bool:
+    return pen is not None and (pen[0] != 1.0 or pen[1] != 0.0 or pen[2] != 0.0)
+
+
+def penalized(logits_row, pen, extra=()):
+    """The row after the penalties `pen` = (repeat, presence, frequency,
+    history), with `extra` tokens appended to the history; unchanged when no
+    penalty is active."""
+    if not penalties_active(pen):
+        return np.asarray(logits_row, dtype=np.float64)
+    return apply_penalties(logits_row, list(pen[3]) + [int(t) for t in extra], *pen[:3])
+
+
 def sample_rows(logits, temperature, seed, rnd, seq, trunc=None):
     """One batched draw for rows 1..n of a block (dflash.go selectBlock).
 
@@ -448,7 +488,7 @@ def proposal_distribution(draft_logits_row, draft_temperature, proposed_token, t
 
 
 def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_temperature,
-           temperature, seed, rnd, seq, trunc=None, draft_trunc=None):
+           temperature, seed, rnd, seq, trunc=None, draft_trunc=None, penalties=None):
     """Accepted prefix length a and bonus token b.
 
     target_logits [n+1, V]: row r scores the token after [current, d_1..d_r].
@@ -465,8 +505,13 @@ def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_tem
     renormalised distribution); draft_trunc: the one the proposal was drawn
     with (q likewise).  The rule is unchanged, so the emitted tokens follow
     the truncated target distribution.
+    penalties = (repeat, presence, frequency, history): target row r is
+    penalised over the history plus d_1..d_r (R26); draft_logits are the
+    logits the proposal was drawn from, its penalties already applied.
     """
     tl = np.atleast_2d(np.asarray(target_logits, dtype=np.float64))
+    if penalties_active(penalties):
+        tl = np.stack([penalized(tl[r], penalties, draft_tokens[:r]) for r in range(len(tl))])
     n = len(draft_tokens)
     V = tl.shape[1]
     if temperature == 0:
@@ -519,7 +564,12 @@ class OracleSession:
         self.seq = seq
         self.last = None               # what the last propose drew from
         self.sampler = None            # (top_k, top_p, min_p) truncation, None: full distributions
+        self.penalties = None          # (repeat, presence, frequency, history), None: no penalties
         self.stats = dict(rounds=0, proposed=0, accepted=0)
+
+    def set_penalties(self, repeat: float = 1.0, presence: float = 0.0, frequency: float = 0.0, history=()):
+        """The sampler's penalties and the committed token history they count."""
+        self.penalties = (float(repeat), float(presence), float(frequency), tuple(int(t) for t in history))
 
     def set_sampler(self, top_k: int = 0, top_p: float = 1.0, min_p: float = 0.0):
         """The session's truncation, used for its draft rows and its target rows."""
@@ -615,6 +665,8 @@ class OracleSession:
         tokens = [int(current)] + [c.mask_token] * n
         h = self.draft.block_forward(tokens, self.F, self.context())
         logits = self.draft.unembed(h[1:])          # the anchor row is unused
+        # every row sees the same committed history (R26)
+        logits = np.stack([penalized(row, self.penalties) for row in logits])
         toks, q, lse = sample_rows(logits, temperature, seed, rnd, self.seq, self.sampler)
         self.last = dict(tokens=toks, logits=logits, temperature=temperature, trunc=self.sampler)
         self.stats["rounds"] += 1
@@ -626,7 +678,7 @@ class OracleSession:
             raise RuntimeError("verify without a proposal")
         a, b = verify(target_logits, draft_tokens, self.last["logits"], self.last["tokens"],
                       self.last["temperature"], temperature, seed, rnd, self.seq, self.sampler,
-                      self.last["trunc"])
+                      self.last["trunc"], self.penalties)
         self.stats["accepted"] += a
         return a, b
 
