@@ -182,6 +182,26 @@ def dflash_committed_taps(session: Session, taps, position: int) -> None:
     _check(lib.dflash_committed_taps(session.handle, arr, stride, rows, position))
 
 
+def dflash_committed_batch(sessions, features, positions) -> None:
+    """features: one CUDA tensor [n_rows_b, K*H_t] per session (one row stride
+    for all); positions: the committed run's position per session.  Sessions
+    that reach the flush threshold flush in one batched forward."""
+    arr, b = _sessions(sessions)
+    features, positions = list(features), [int(x) for x in positions]
+    if len(features) != b or len(positions) != b:
+        raise ValueError("one features tensor and one position per session")
+    cfg = _model_of(sessions).cfg
+    stride = features[0].stride(0)
+    for f in features:
+        if f.dim() != 2 or f.stride(1) != 1 or not f.is_cuda or f.dtype != torch_dtype(cfg) or \
+                f.shape[1] != cfg.feature_width or (f.shape[0] > 1 and f.stride(0) != stride):
+            raise ValueError(f"features: CUDA {torch_dtype(cfg)} rows of width {cfg.feature_width}, one row stride")
+    ptrs = (C.c_void_p * b)(*[f.data_ptr() for f in features])
+    rows = (C.c_int32 * b)(*[f.shape[0] for f in features])
+    pos = (C.c_int64 * b)(*positions)
+    _check(lib.dflash_committed_batch(arr, b, ptrs, stride, rows, pos))
+
+
 def dflash_flush(sessions) -> None:
     arr, n = _sessions(sessions)
     _check(lib.dflash_flush(arr, n))
@@ -245,6 +265,16 @@ def dflash_close(session: Session) -> None:
     if session.handle:
         _check(lib.dflash_close(session.handle))
         session.handle = None
+
+
+def dflash_set_penalties(session: Session, repeat: float = 1.0, presence: float = 0.0, frequency: float = 0.0,
+                         history: torch.Tensor | None = None) -> None:
+    """The sampler's penalties over a committed history (CUDA int32 [n] token ids)."""
+    n = 0 if history is None else int(history.numel())
+    if n and (not history.is_cuda or history.dtype != torch.int32 or not history.is_contiguous()):
+        raise ValueError("history: contiguous CUDA int32 token ids")
+    _check(lib.dflash_set_penalties(session.handle, float(repeat), float(presence), float(frequency),
+                                    _ptr(history) if n else None, n))
 
 
 def dflash_set_sampler(session: Session, top_k: int = 0, top_p: float = 1.0, min_p: float = 0.0) -> None:

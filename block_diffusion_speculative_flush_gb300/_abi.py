@@ -92,6 +92,8 @@ SIGNATURES = {
     "dflash_open": (C.c_int, [P, C.c_int64, C.c_int64, P, C.POINTER(C.c_void_p)]),
     "dflash_committed": (C.c_int, [P, P, C.c_int64, C.c_int32, C.c_int64]),
     "dflash_committed_taps": (C.c_int, [P, C.POINTER(C.c_void_p), C.c_int64, C.c_int32, C.c_int64]),
+    "dflash_committed_batch": (C.c_int, [P, C.c_int32, C.POINTER(C.c_void_p), C.c_int64, C.POINTER(C.c_int32),
+                                         C.POINTER(C.c_int64)]),
     "dflash_flush": (C.c_int, [SessArr, C.c_int32]),
     "dflash_settle": (C.c_int, [P]),
     "dflash_commit_block": (C.c_int, [SessArr, C.c_int32]),
@@ -109,6 +111,7 @@ SIGNATURES = {
     "dflash_timing_enable": (C.c_int, [P, C.c_int32]),
     "dflash_timing_read": (C.c_int, [P, C.POINTER(dflash_kernel_time), C.c_int32, C.POINTER(C.c_int32)]),
     "dflash_set_sampler": (C.c_int, [P, C.c_int32, C.c_float, C.c_float]),
+    "dflash_set_penalties": (C.c_int, [P, C.c_float, C.c_float, C.c_float, P, C.c_int32]),
     "dflash_target_create": (C.c_int, [C.POINTER(dflash_target_config), C.POINTER(dflash_target_weights), C.c_int64,
                                        P, C.POINTER(C.c_void_p)]),
     "dflash_target_destroy": (C.c_int, [P]),

@@ -7,9 +7,13 @@
 //
 // One CTA per work item (session, KV head, key range starting on a multiple
 // of 64).  Query rows (at most 128, zero padded) form the MMA's M = 128 side.
-//   warp 8        TMA: a 64-key K tile [64 keys][128 d] and the matching
-//                 V^T tile [128 d][64 keys] per stage (3 stages); the cache
-//                 keeps V transposed so that both are K-major operand tiles.
+//   warp 8        TMA: 64-key K tiles [64 keys][128 d] into a 2-stage ring and
+//                 the matching V^T tiles [128 d][64 keys] into a 5-stage
+//                 ring; the cache keeps V transposed so that both are K-major
+//                 operand tiles.  A K stage is free once S = Q K^T is done, a
+//                 V stage only once P V is done, one to two tiles later, so V
+//                 gets the deeper ring: it keeps two to three tiles of loads
+//                 in flight past the ones being computed.
 //   warp 9        MMA: S = Q K^T into one of two TMEM buffers, then
 //                 O += P V^T (P as a bf16 hi + lo pair, ~16 bits of the
 //                 probabilities) into the TMEM accumulator.
@@ -39,12 +43,13 @@ namespace cg = cooperative_groups;
 
 constexpr int D = 128;                       // head dim
 constexpr int KT = 64;                       // keys per tile (MMA N of S)
-constexpr int ST = 3;                        // K/V stages in flight
+constexpr int KST = 2;                       // K stages
+constexpr int VST = 5;                       // V^T stages
 constexpr int QBYTES = 128 * D * 2;          // Q: two [128 rows][64 d] swizzled blocks
 constexpr int KBYTES = KT * D * 2;           // K tile: two [64 keys][64 d] blocks
 constexpr int VBYTES = D * KT * 2;           // V^T tile: one [128 d][64 keys] block
 constexpr int PBYTES = 128 * KT * 2;         // P tile: one [128 rows][64 keys] block
-constexpr int DATA_BYTES = QBYTES + ST * (KBYTES + VBYTES) + 4 * PBYTES;  // + barriers and 1 KB exchange
+constexpr int DATA_BYTES = QBYTES + KST * KBYTES + VST * VBYTES + 4 * PBYTES;  // + barriers and exchange
 constexpr int THREADS = 320;
 constexpr int SOFTMAX_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 256;          // O [0,128), S0 [128,192), S1 [192,256)
@@ -73,11 +78,13 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + QBYTES;
-  uint8_t* sV = sK + ST * KBYTES;
-  uint8_t* sP = sV + ST * VBYTES;  // [2 buffers][hi, lo]
-  uint64_t* kv_full = (uint64_t*)(sP + 4 * PBYTES);
-  uint64_t* kv_empty = kv_full + ST;
-  uint64_t* s_full = kv_empty + ST;
+  uint8_t* sV = sK + KST * KBYTES;
+  uint8_t* sP = sV + VST * VBYTES;  // [2 buffers][hi, lo]
+  uint64_t* k_full = (uint64_t*)(sP + 4 * PBYTES);
+  uint64_t* k_empty = k_full + KST;
+  uint64_t* v_full = k_empty + KST;
+  uint64_t* v_empty = v_full + VST;
+  uint64_t* s_full = v_empty + VST;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* pv_done = p_full + 2;
@@ -92,9 +99,13 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -153,26 +164,38 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
 
   if (warp == 8) {
     if (lane == 0) {
-      // ---- TMA producer
-      int issued = 0;
+      // ---- TMA producer: K(t) then V^T(t), each into its own ring
+      int issued_k = 0, issued_v = 0;
       for (int t = 0; t < T; ++t) {
-        const int s = t % ST;
-        if (t >= ST && !mbar_wait(&kv_empty[s], (uint32_t)((t / ST) - 1) & 1u, abort_flag)) {
+        const int ks = t % KST, vs = t % VST;
+        const int slot0 = (int)((it.k0 + (int64_t)t * KT) % cap);
+        if (t >= KST && !mbar_wait(&k_empty[ks], (uint32_t)((t / KST) - 1) & 1u, abort_flag)) {
           atomicOr(err, 8);
           *abort_flag = 1;
           break;
         }
-        mbar_expect_tx(&kv_full[s], KBYTES + VBYTES);
-        const int slot0 = (int)((it.k0 + (int64_t)t * KT) % cap);
-        tma_load_3d(sK + s * KBYTES, kmap, &kv_full[s], 0, slot0, planeK);
-        tma_load_3d(sK + s * KBYTES + KBYTES / 2, kmap, &kv_full[s], 64, slot0, planeK);
-        tma_load_3d(sV + s * VBYTES, vmap, &kv_full[s], slot0, 0, planeV);
-        ++issued;
+        mbar_expect_tx(&k_full[ks], KBYTES);
+        tma_load_3d(sK + ks * KBYTES, kmap, &k_full[ks], 0, slot0, planeK);
+        tma_load_3d(sK + ks * KBYTES + KBYTES / 2, kmap, &k_full[ks], 64, slot0, planeK);
+        ++issued_k;
+        if (t >= VST && !mbar_wait(&v_empty[vs], (uint32_t)((t / VST) - 1) & 1u, abort_flag)) {
+          atomicOr(err, 8);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_expect_tx(&v_full[vs], VBYTES);
+        tma_load_3d(sV + vs * VBYTES, vmap, &v_full[vs], slot0, 0, planeV);
+        ++issued_v;
       }
       if (*abort_flag) {  // let this CTA's own copies land before leaving
-        for (int t = issued - ST > 0 ? issued - ST : 0; t < issued; ++t) {
+        for (int t = issued_k - KST > 0 ? issued_k - KST : 0; t < issued_k; ++t) {
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&kv_full[t % ST], (uint32_t)(t / ST) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          while (!mbar_try_wait(&k_full[t % KST], (uint32_t)(t / KST) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+        for (int t = issued_v - VST > 0 ? issued_v - VST : 0; t < issued_v; ++t) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&v_full[t % VST], (uint32_t)(t / VST) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
@@ -183,23 +206,24 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       constexpr uint32_t idS = idesc_bf16(128, KT), idPV = idesc_bf16(128, D);
       const uint32_t tO = tmem;
       auto issue_pv = [&](int u) -> bool {
-        const int pb = u & 1, s = u % ST;
+        const int pb = u & 1, vs = u % VST;
         if (!mbar_wait(&p_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag)) return false;
+        if (!mbar_wait(&v_full[vs], (uint32_t)(u / VST) & 1u, abort_flag)) return false;
         fence_after();
-        const uint32_t ph = smem_u32(sP + pb * 2 * PBYTES), pl = ph + PBYTES, v0 = smem_u32(sV + s * VBYTES);
+        const uint32_t ph = smem_u32(sP + pb * 2 * PBYTES), pl = ph + PBYTES, v0 = smem_u32(sV + vs * VBYTES);
 #pragma unroll
         for (int ks = 0; ks < KT / 16; ++ks)
           umma_bf16(tO, sdesc_sw128(ph + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, (u > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
         for (int ks = 0; ks < KT / 16; ++ks) umma_bf16(tO, sdesc_sw128(pl + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, 1u);
         umma_commit(&pv_done[pb]);
-        umma_commit(&kv_empty[s]);
+        umma_commit(&v_empty[vs]);
         return true;
       };
       bool ok = true;
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t % ST, sb = t & 1;
-        if (!mbar_wait(&kv_full[s], (uint32_t)(t / ST) & 1u, abort_flag)) {
+        const int s = t % KST, sb = t & 1;
+        if (!mbar_wait(&k_full[s], (uint32_t)(t / KST) & 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -215,6 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
           umma_bf16(tS, sdesc_sw128(q0 + (ks >> 2) * (QBYTES / 2) + (ks & 3) * 32),
                     sdesc_sw128(k0 + (ks >> 2) * (KBYTES / 2) + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
         umma_commit(&s_full[sb]);
+        umma_commit(&k_empty[s]);  // the K stage is free once S(t) is done
         if (t >= 1) ok = issue_pv(t - 1);
       }
       if (ok && T > 0) ok = issue_pv(T - 1);
@@ -229,6 +254,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     const int r = (warp & 3) * 32 + lane;
     const int half = warp >> 2;                // keys [32 half, +32) of a tile, O columns [64 half, +64)
     const bool rv = r < R;
+    // a warp whose 32 rows are all padding (r >= R) computes nothing: the
+    // P rows it would write only meet O rows that are never read.  It keeps
+    // the barrier protocol (one arrival per tile on s_free and p_full, the
+    // per-tile exchange barrier), so no phase runs ahead of the others.
+    const bool live = (warp & 3) * 32 < R;
     const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale * 1.4426950408889634f;
     // the row's visible key positions form one interval [vlo, vhi]
@@ -247,6 +277,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       const int sb = t & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, abort_flag));
       if (!ok) break;
+      if (!live) {
+        mbar_arrive(&s_free[sb]);
+        asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
+        mbar_arrive(&p_full[t & 1]);
+        continue;
+      }
       fence_after();
       float s[32];
       tmem_ld32(tmem + lrow + 128 + sb * KT + 32 * half, s);
@@ -334,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
                                                    xl[r] + xl[128 + r], 0.f, 0.f);
     }
 #pragma unroll 1
-    for (int c = 64 * half; c < 64 * half + 64; c += 32) {
+    for (int c = 64 * half; c < 64 * half + 64 && live; c += 32) {
       float o[32];
       tmem_ld32(tmem + lrow + c, o);
       if (rv) {

@@ -167,7 +167,8 @@ struct dflash_model {
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_pool;
   size_t ev_used = 0;
   // workspace
-  Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart, vbonus, cutbuf;
+  Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart, vbonus, cutbuf,
+      vpen, vpen_tab;
   HostRing ring;
 };
 
@@ -193,7 +194,13 @@ struct dflash_session {
   bool last_trunc = false;      // the last proposal was drawn from a truncated distribution
   int64_t rounds = 0, proposed = 0, flushes = 0, flushed_rows = 0;
   int device = 0;               // the CUDA device that was current at dflash_open
+  Penalty pen{1.f, 0.f, 0.f, 0, nullptr};  // the sampler's penalties (hist: the session's copy)
+  int32_t* d_hist = nullptr;    // [kMaxPenaltyHistory] committed history for the penalties
 };
+
+namespace {
+bool penalties_on(const Penalty& p) { return p.repeat != 1.f || p.presence != 0.f || p.frequency != 0.f; }
+}  // namespace
 
 namespace {
 
@@ -403,10 +410,28 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       k1v[j] = F + nrows;
       total += (k1v[j] - k0v[j]) * Hkv;
     }
-    // about one work item per SM: fewer, longer key ranges keep the split
-    // partials (R x (d + 4) floats per item) small next to the K/V bytes
-    int64_t chunk = align_up(std::max<int64_t>(1, total / std::max(1, m->num_sms)), 64);
-    chunk = std::min<int64_t>(std::max<int64_t>(chunk, 128), 8192);
+    // The key range length of the work items: one CTA runs per SM, so the
+    // items run in waves of num_sms, and a wave lasts as long as its longest
+    // item.  Among lengths that are multiples of 64 (at least 128), take the
+    // one that minimises waves x (length + a fixed cost per item, about four
+    // tiles of keys).  Fewer, longer ranges also keep the split partials
+    // (R x (d + 4) floats per item) small next to the K/V bytes.
+    int64_t maxlen = 1;
+    for (int j = 0; j < Bc; ++j) maxlen = std::max<int64_t>(maxlen, k1v[j] - k0v[j]);
+    const int64_t top = std::max<int64_t>(128, align_up(maxlen, 64));
+    int64_t chunk = top;
+    double best = 1e300;
+    for (int64_t ch = 128; ch <= top; ch += ch < 1024 ? 64 : 256) {
+      int64_t n_items = 0;
+      for (int j = 0; j < Bc; ++j) n_items += (int64_t)Hkv * ((k1v[j] - k0v[j] + ch - 1) / ch);
+      const int64_t waves = (n_items + m->num_sms - 1) / std::max(1, m->num_sms);
+      const double cost = (double)waves * (double)(std::min(ch, maxlen) + 256);
+      if (cost < best) {
+        best = cost;
+        chunk = ch;
+      }
+    }
+    (void)total;
     const int64_t tiles0 = (k1v[0] - k0v[0] + 63) / 64;
     if (attn_cluster_ok && tiles0 > 1 && tiles0 <= kAttnMaxCluster) {
       // one session with a short key range per KV head (a window): one
@@ -448,6 +473,18 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     if (any_trunc) {
       o_trunc = tp.add(trv);
       o_pcut = tp.add(pcv);
+    }
+  }
+  // the sessions' penalties (propose only; none active: no launch)
+  std::vector<Penalty> pen_tab;
+  bool o_pen = false;
+  for (int j = 0; j < Bc && block; ++j)
+    if (penalties_on(fw.sess[j]->pen) && fw.sess[j]->pen.n_hist > 0) o_pen = true;
+  if (o_pen) {
+    pen_tab.resize(Bc);
+    for (int j = 0; j < Bc; ++j) {
+      pen_tab[j] = fw.sess[j]->pen;
+      if (!penalties_on(pen_tab[j])) pen_tab[j].n_hist = 0;
     }
   }
   const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
@@ -588,6 +625,18 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   } else {
     ST_TRY(gemm(m, m->z.p, H, m->unembed, H, lg, V, Rz, V, H, st));
   }
+  if (o_pen) {
+    // every row of a session's block gets the same committed-history penalties
+    std::vector<float*> rows(Bc);
+    for (int j = 0; j < Bc; ++j) rows[j] = (seg || Bc == 1) ? fw.sess[j]->plogits : lg + (size_t)j * n * V;
+    TablePack pk;
+    const size_t o_p = pk.add(pen_tab), o_r = pk.add(rows);
+    ST_TRY(m->ring.upload(pk, m->vpen_tab, st));
+    char* pb = m->vpen_tab.as<char>();
+    launch_penalize_rows((const Penalty*)(pb + o_p), (float* const*)(pb + o_r), n, V, V, Bc, st);
+    m->launches += 2;
+    ST_TRY(launch_check("penalties"));
+  }
   const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
   ST_TRY(m->spart.ensure((size_t)Rz * chunks * sizeof(float4), st));
   ST_TRY(m->vstat.ensure((size_t)Rz * 8, st));
@@ -714,6 +763,7 @@ int dflash__session_proposal(const dflash_session* s, const float** logits, cons
 }
 
 int dflash__session_device(const dflash_session* s) { return s->device; }
+int dflash__session_penalties(const dflash_session* s) { return penalties_on(s->pen) ? 1 : 0; }
 
 // A Timed bracket that the allocation-free verify can open and close across
 // its launches (the class is kVerify); the handle is an index into the
@@ -809,7 +859,7 @@ int dflash_model_destroy(dflash_model* m) {
     if (L.w_qkvg) cudaFree(L.w_qkvg);
   Buf* bufs[] = {&m->tables, &m->u, &m->fcout, &m->c, &m->h, &m->x, &m->qkv, &m->rope, &m->Q, &m->G,
                  &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart, &m->cutbuf,
-                 &m->vbonus};
+                 &m->vbonus, &m->vpen, &m->vpen_tab};
   for (Buf* b : bufs) b->release();
   m->ring.release();
   for (auto& e : m->ev_pool) {
@@ -974,6 +1024,69 @@ int dflash_committed_taps(dflash_session* s, const void* const* taps, int64_t ro
   return committed_impl(s, tp, row_stride * (int64_t)s->m->esz, false, n_rows, position);
 }
 
+int dflash_committed_batch(dflash_session* const* s, int32_t batch, const void* const* features, int64_t row_stride,
+                           const int32_t* n_rows, const int64_t* position) {
+  ST_TRY(check_sessions(s, batch));
+  if (!features || !n_rows || !position) return fail(DFLASH_ERR_INVALID_ARG, "null features / n_rows / position");
+  dflash_model* m = s[0]->m;
+  const dflash_config& c = m->cfg;
+  const int64_t width = (int64_t)c.n_taps * c.target_hidden;
+  const size_t es = m->esz;
+  // every check first, so that an error changes no session
+  for (int b = 0; b < batch; ++b) {
+    if (n_rows[b] < 0 || position[b] < 0)
+      return fail(DFLASH_ERR_INVALID_ARG, "session %d: n_rows %d / position %lld", b, n_rows[b], (long long)position[b]);
+    if (n_rows[b] > 0 && (!features[b] || row_stride < width))
+      return fail(DFLASH_ERR_INVALID_ARG, "session %d: features null or row_stride %lld < %lld", b,
+                  (long long)row_stride, (long long)width);
+    const int64_t start = s[b]->F + s[b]->P - position[b];
+    if (start < 0)
+      return fail(DFLASH_ERR_CONTEXT_GAP, "session %d: committed run at %lld leaves a context gap at %lld", b,
+                  (long long)position[b], (long long)(s[b]->F + s[b]->P));
+    const int64_t add = std::max<int64_t>(0, n_rows[b] - start);
+    if (s[b]->F + s[b]->P + add > s[b]->max_ctx)
+      return fail(DFLASH_ERR_CAPACITY, "session %d: context would reach %lld rows, max_ctx %lld", b,
+                  (long long)(s[b]->F + s[b]->P + add), (long long)s[b]->max_ctx);
+  }
+  Forward fw;
+  std::vector<int64_t> F0(batch);
+  std::vector<int32_t> P0(batch);
+  for (int b = 0; b < batch; ++b) {
+    dflash_session* x = s[b];
+    F0[b] = x->F;
+    P0[b] = x->P;
+    const int64_t start = x->F + x->P - position[b];
+    if (start >= n_rows[b]) continue;  // restored prefix: nothing new
+    const int add = (int)(n_rows[b] - start);
+    const char* src[kMaxTaps];
+    for (int k = 0; k < c.n_taps; ++k)
+      src[k] = (const char*)features[b] + ((size_t)start * row_stride + (size_t)k * c.target_hidden) * es;
+    if (x->P + add < DFLASH_PENDING_FLUSH_TOKENS) {
+      launch_copy_rows((char*)x->pending + (size_t)x->P * width * es, (int64_t)(width * es), src[0],
+                       row_stride * (int64_t)es, (int64_t)(width * es), add, s[0]->stream);
+      x->P += add;
+      continue;
+    }
+    // this session reaches the threshold: its held rows and the new rows
+    // (read in place) join the one context-only forward of the call
+    commit_block(x);
+    const int32_t j = (int32_t)fw.sess.size();
+    fw.sess.push_back(x);
+    take_pending(x, j, src, row_stride * (int64_t)es, add, fw.ctx);
+  }
+  int rc = launch_check("pending rows");
+  if (rc == DFLASH_OK && !fw.sess.empty()) rc = run_forward(m, fw, s[0]->stream);
+  if (rc != DFLASH_OK) {
+    for (int b = 0; b < batch; ++b) {
+      s[b]->F = F0[b];
+      s[b]->P = P0[b];
+    }
+    return rc;
+  }
+  for (auto* x : fw.sess) x->flushes++;
+  return DFLASH_OK;
+}
+
 int dflash_commit_block(dflash_session* const* s, int32_t batch) {
   ST_TRY(check_sessions(s, batch));
   for (int b = 0; b < batch; ++b) commit_block(s[b]);
@@ -1104,9 +1217,17 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
     any_trunc = any_trunc || (temperature > 0.f && trv[b].top_k > 0);
     any_dcut = any_dcut || (temperature > 0.f && dcut[b]);
   }
+  // penalties: target row r of session b counts b's history plus d_1..d_r
+  std::vector<Penalty> penv(batch);
+  bool any_pen = false;
+  for (int b = 0; b < batch; ++b) {
+    penv[b] = s[b]->pen;
+    any_pen = any_pen || penalties_on(penv[b]);
+  }
   const size_t o_dl = tp.add(dl), o_dlse = tp.add(dlse), o_dtok = tp.add(dtok), o_dT = tp.add(dT), o_acc = tp.add(acc),
                o_seq = tp.add(seqv);
   const size_t o_trunc = any_trunc ? tp.add(trv) : 0, o_dcut = any_dcut ? tp.add(dcut) : 0;
+  const size_t o_pen = any_pen ? tp.add(penv) : 0;
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
   const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
@@ -1127,6 +1248,16 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   sa.err = m->d_err;
   const double tbytes = (double)rows * V * (sa.in_bf16 ? 2 : 4) + (double)batch * V * 4;
   Timed tm(m, kVerify, tbytes, 4.0 * rows * V, st);
+  if (any_pen) {
+    // the penalised target rows go to a workspace copy (fp32); the caller's
+    // logits are never written
+    ST_TRY(m->vpen.ensure((size_t)rows * V * 4, st));
+    launch_penalize_target((const Penalty*)(tb + o_pen), target_logits, sa.in_bf16, m->vpen.as<float>(),
+                           draft_tokens, batch, n, V, st);
+    m->launches++;
+    sa.logits = m->vpen.p;
+    sa.in_bf16 = 0;
+  }
   if (any_trunc) {
     ST_TRY(m->cutbuf.ensure((size_t)rows * 8, st));
     launch_trunc_cut(sa, (const Trunc*)(tb + o_trunc), m->cutbuf.as<uint64_t>(), nullptr, st);
@@ -1137,7 +1268,7 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   launch_sample_combine(sa, chunks, m->vpart.as<float4>(), amax, nullptr, lse, st);
   m->launches += 3;
   VerifyArgs va{};
-  va.target = target_logits;
+  va.target = sa.logits;
   va.in_bf16 = sa.in_bf16;
   va.B = batch;
   va.n = n;
@@ -1167,6 +1298,22 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   return launch_check("verify");
 }
 
+int dflash_set_penalties(dflash_session* s, float repeat_penalty, float presence_penalty, float frequency_penalty,
+                         const int32_t* history, int32_t n_history) {
+  if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
+  if (!(repeat_penalty > 0.f) || std::isinf(repeat_penalty) || !std::isfinite(presence_penalty) ||
+      !std::isfinite(frequency_penalty))
+    return fail(DFLASH_ERR_INVALID_ARG, "repeat_penalty must be positive and finite; the others finite");
+  if (n_history < 0 || n_history > kMaxPenaltyHistory)
+    return fail(DFLASH_ERR_INVALID_ARG, "n_history %d outside [0, %d]", n_history, kMaxPenaltyHistory);
+  if (n_history > 0 && !history) return fail(DFLASH_ERR_INVALID_ARG, "null history");
+  if (n_history > 0 && !s->d_hist) CU_TRY(cudaMalloc((void**)&s->d_hist, (size_t)kMaxPenaltyHistory * 4));
+  if (n_history > 0)
+    CU_TRY(cudaMemcpyAsync(s->d_hist, history, (size_t)n_history * 4, cudaMemcpyDeviceToDevice, s->stream));
+  s->pen = Penalty{repeat_penalty, presence_penalty, frequency_penalty, n_history, s->d_hist};
+  return DFLASH_OK;
+}
+
 int dflash_set_sampler(dflash_session* s, int32_t top_k, float top_p, float min_p) {
   if (!s) return fail(DFLASH_ERR_INVALID_ARG, "null session");
   if (top_k < 0 || top_k > kTruncMaxK) return fail(DFLASH_ERR_INVALID_ARG, "top_k %d outside [0, %d]", top_k, kTruncMaxK);
@@ -1190,6 +1337,7 @@ int dflash_close(dflash_session* s) {
   cudaFree(s->pcut);
   cudaFree(s->d_accepted);
   cudaFree(s->d_maps);
+  cudaFree(s->d_hist);
   delete s;
   return rc;
 }

@@ -179,6 +179,27 @@ constexpr int kVerifyBonusChunk = 1024;
 inline int verify_bonus_chunks(int V) { return (V + kVerifyBonusChunk - 1) / kVerifyBonusChunk; }
 void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st);
 
+// The sampler's penalties of one session over a committed token history:
+// an id seen c > 0 times has a positive logit divided by `repeat` and a
+// non-positive one multiplied by it, then loses `presence` once and
+// `frequency` c times.  n_hist == 0: no penalties for this session.
+struct Penalty {
+  float repeat, presence, frequency;
+  int32_t n_hist;
+  const int32_t* hist;  // device [n_hist] token ids
+};
+constexpr int kMaxPenaltyHistory = 4096;
+// Draft rows, in place: rows_per_seq rows of session b (rows[b] + i * ld)
+// get b's penalties; every row of a block sees the same history.  One CTA per
+// session.  Ids outside [0, V) are ignored.
+void launch_penalize_rows(const Penalty* pen, float* const* rows, int rows_per_seq, int64_t ld, int V, int B,
+                          cudaStream_t st);
+// Target rows of verify: out [B][n+1][V] fp32 = target (fp32, or bf16 when
+// in_bf16) with row r of session b penalised over b's history plus the draft
+// tokens draft[b][0..r).  One CTA per row.
+void launch_penalize_target(const Penalty* pen, const void* target, int in_bf16, float* out, const int32_t* draft,
+                            int B, int n, int V, cudaStream_t st);
+
 // --- tensor-core path (bf16, sm_103a) --------------------------------------
 struct TcGemmPlan;  // opaque, defined in gemm_tc.cu
 

@@ -1294,6 +1294,90 @@ __global__ void k_table_write(uint4* __restrict__ dst, int n16, const __grid_con
   for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src.d[i];
 }
 
+// ---------------------------------------------------------------------------
+// penalties over a token history
+// ---------------------------------------------------------------------------
+constexpr int kPenThreads = 1024;
+
+// Sorts ids[0..n) in shared memory (n <= kMaxPenaltyHistory + a block of
+// draft tokens, padded with INT32_MAX to a power of two), then calls
+// f(id, count) once per distinct id, from the thread holding its first copy.
+template <typename F>
+__device__ __forceinline__ void for_each_distinct(int32_t* ids, int n, F f) {
+  int N = 1;
+  while (N < n) N <<= 1;
+  for (int i = n + (int)threadIdx.x; i < N; i += blockDim.x) ids[i] = INT32_MAX;
+  __syncthreads();
+  for (int k = 2; k <= N; k <<= 1) {        // bitonic sort, ascending
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const int32_t a = ids[i], b = ids[l];
+          if ((a > b) == ((i & k) == 0)) {
+            ids[i] = b;
+            ids[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int32_t v = ids[i];
+    if (i > 0 && ids[i - 1] == v) continue;
+    int c = 1;
+    while (i + c < n && ids[i + c] == v) ++c;
+    f(v, c);
+  }
+}
+
+__device__ __forceinline__ float penalize(float x, int c, const Penalty& p) {
+  x = x > 0.f ? x / p.repeat : x * p.repeat;
+  return x - p.presence - p.frequency * (float)c;
+}
+
+__global__ void __launch_bounds__(kPenThreads) k_penalize_rows(const Penalty* __restrict__ pens,
+                                                              float* const* __restrict__ rows, int rows_per_seq,
+                                                              int64_t ld, int V) {
+  __shared__ int32_t ids[kMaxPenaltyHistory];
+  pdl_trigger();
+  pdl_wait();
+  const Penalty p = pens[blockIdx.x];
+  if (p.n_hist <= 0) return;
+  const int n = min(p.n_hist, kMaxPenaltyHistory);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) ids[i] = p.hist[i];
+  __syncthreads();
+  float* base = rows[blockIdx.x];
+  for_each_distinct(ids, n, [&](int32_t v, int c) {
+    if (v < 0 || v >= V) return;
+    for (int r = 0; r < rows_per_seq; ++r) base[r * ld + v] = penalize(base[r * ld + v], c, p);
+  });
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPenThreads) k_penalize_target(const Penalty* __restrict__ pens,
+                                                                const T* __restrict__ target, float* __restrict__ out,
+                                                                const int32_t* __restrict__ draft, int n, int V) {
+  // the history plus at most 511 draft tokens, padded to a power of two
+  __shared__ int32_t ids[2 * kMaxPenaltyHistory];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x / (n + 1), r = blockIdx.x % (n + 1);
+  const T* src = target + (int64_t)blockIdx.x * V;
+  float* dst = out + (int64_t)blockIdx.x * V;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) dst[v] = to_f(src[v]);
+  const Penalty p = pens[b];
+  if (!(p.repeat != 1.f || p.presence != 0.f || p.frequency != 0.f)) return;  // no penalties: a plain copy
+  const int nh = min(p.n_hist, kMaxPenaltyHistory);
+  for (int i = threadIdx.x; i < nh; i += blockDim.x) ids[i] = p.hist[i];
+  for (int i = threadIdx.x; i < r; i += blockDim.x) ids[nh + i] = draft[(int64_t)b * n + i];
+  __syncthreads();  // the copied row is visible to every thread of the block too
+  for_each_distinct(ids, nh + r, [&](int32_t v, int c) {
+    if (v >= 0 && v < V) dst[v] = penalize(dst[v], c, p);
+  });
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -1451,6 +1535,21 @@ void launch_verify_accept(const VerifyArgs& a, VerifyPart* part, cudaStream_t st
   const int chunk = kVerifyBonusChunk, chunks = verify_bonus_chunks(a.V);
   if (a.temperature > 0.f) launch_k(k_verify_bonus, dim3(a.B, chunks), 256, 0, st, a, chunk, part);
   launch_k(k_verify_finish, cdiv(a.B, 4), 128, 0, st, a, chunks, part);
+}
+
+void launch_penalize_rows(const Penalty* pen, float* const* rows, int rows_per_seq, int64_t ld, int V, int B,
+                          cudaStream_t st) {
+  if (B <= 0 || rows_per_seq <= 0) return;
+  launch_k(k_penalize_rows, B, kPenThreads, 0, st, pen, rows, rows_per_seq, ld, V);
+}
+
+void launch_penalize_target(const Penalty* pen, const void* target, int in_bf16, float* out, const int32_t* draft,
+                            int B, int n, int V, cudaStream_t st) {
+  if (B <= 0) return;
+  if (in_bf16)
+    launch_k(k_penalize_target<bf16>, B * (n + 1), kPenThreads, 0, st, pen, (const bf16*)target, out, draft, n, V);
+  else
+    launch_k(k_penalize_target<float>, B * (n + 1), kPenThreads, 0, st, pen, (const float*)target, out, draft, n, V);
 }
 
 int launch_table_write(void* dst, const void* src, size_t bytes, cudaStream_t st) {

@@ -31,6 +31,7 @@ extern "C" int dflash__session_proposal(const dflash_session* s, const float** l
                                         int32_t** err, const void** model);
 extern "C" int dflash__session_truncation(const dflash_session* s, Trunc* trunc, const uint64_t** proposal_cut);
 extern "C" int dflash__session_device(const dflash_session* s);
+extern "C" int dflash__session_penalties(const dflash_session* s);
 extern "C" long long dflash__verify_timing_begin(const void* model, double bytes, double flops, void* stream);
 extern "C" void dflash__verify_timing_end(const void* model, long long idx, void* stream);
 extern "C" void dflash__count_launches(const void* model, int n);
@@ -138,6 +139,9 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
       snprintf(msg, sizeof msg, "session %d has no proposal of %d tokens to verify against", b, n);
       return dflash__set_error(DFLASH_ERR_STATE, msg);
     }
+    if (dflash__session_penalties(s[b]))
+      return dflash__set_error(DFLASH_ERR_INVALID_ARG,
+                               "a session has penalties set: their penalised target rows need dflash_verify's workspace");
     seq[b] = b;
     dflash__session_truncation(s[b], &trv[b], &dcut[b]);
     any_trunc = any_trunc || (temperature > 0.f && trv[b].top_k > 0);

@@ -185,6 +185,21 @@ DFLASH_API int dflash_committed(dflash_session* s, const void* features, int64_t
 DFLASH_API int dflash_committed_taps(dflash_session* s, const void* const* taps /*host [n_taps]*/, int64_t row_stride,
                                      int32_t n_rows, int64_t position);
 
+/* dflash_committed for a batch of sessions of one model in one call: session
+ * b receives n_rows[b] rows at features[b] (a device pointer; rows
+ * row_stride elements apart, the same stride for all) for the committed run
+ * at position[b].  Each session's run is taken as dflash_committed takes it
+ * (gap check, a restored prefix skipped, rows held below the threshold);
+ * every session whose held rows reach DFLASH_PENDING_FLUSH_TOKENS flushes,
+ * and those flushes run together as one batched context-only forward (dflash.go
+ * committed and flush: the held rows flush in one context-only forward).  The
+ * work runs on the first session's stream.  Every check runs before any state
+ * changes, so an error leaves every session as it was.  Errors: INVALID_ARG,
+ * CONTEXT_GAP, CAPACITY, with the session's index in the message. */
+DFLASH_API int dflash_committed_batch(dflash_session* const* s /*host [batch]*/, int32_t batch,
+                                      const void* const* features /*host [batch]*/, int64_t row_stride,
+                                      const int32_t* n_rows /*host [batch]*/, const int64_t* position /*host [batch]*/);
+
 /* dflash.go flush: rewinds each session's outstanding block, then writes all
  * held rows in one batched context-only forward.  When the draft has a
  * window, rows that no later query can see (slot <= F_new - W) are dropped
@@ -226,6 +241,35 @@ DFLASH_API int dflash_propose(dflash_session* const* s /*host [batch]*/, int32_t
  * Else DFLASH_ERR_INVALID_ARG and nothing changes.  Takes effect at the next
  * propose and verify; verify's q stays the one the proposal was drawn with. */
 DFLASH_API int dflash_set_sampler(dflash_session* s, int32_t top_k, float top_p, float min_p);
+
+/* The session's sampler penalties over the committed token history
+ * ("Ollama DFlash block-diffusion draft model in mlxrunner", Facts: penalties
+ * see only committed history, not other rows of the block; dflash.go
+ * selectBlock).  The form is the sampler's repetition, presence and frequency
+ * penalties (the pages do not state it): an id that occurs c > 0 times in the
+ * history has a positive logit divided by repeat_penalty and a non-positive
+ * one multiplied by it, then loses presence_penalty once and
+ * frequency_penalty c times; penalties act on the raw logits, before the
+ * temperature and any truncation.
+ *   propose: every row of the block is penalised over the same history, so
+ *   no row of the block counts toward another's penalties; out_logits and the
+ *   logits the session keeps for verify are the penalised ones (the
+ *   distribution the proposal was drawn from).
+ *   verify: target row r is penalised over the history plus the draft tokens
+ *   d_1..d_r in front of it, the history classic decoding would have had, so
+ *   the output keeps the target sampler's law.  The penalised rows go to a
+ *   workspace copy; the caller's target logits are never written.
+ * history: device [n_history] token ids, n_history <= 4096 (the caller's
+ * window, oldest first); copied in stream order into the session, so the
+ * buffer must stay valid until the stream reaches this call.  Call again with
+ * the new window as tokens are committed.  repeat 1, presence 0 and frequency
+ * 0 turn the penalties off.  Errors: INVALID_ARG (repeat <= 0 or not finite,
+ * a non-finite penalty, n_history outside [0, 4096], a null history).
+ * Sessions with penalties on are verified by dflash_verify only:
+ * dflash_verify_noalloc refuses them (INVALID_ARG). */
+DFLASH_API int dflash_set_penalties(dflash_session* s, float repeat_penalty, float presence_penalty,
+                                    float frequency_penalty, const int32_t* history /*device [n_history]*/,
+                                    int32_t n_history);
 
 /* Speculative verification of each session's last proposal.
  * target_logits [batch, n+1, V] (fp32 or bf16 per logits_dtype): row r

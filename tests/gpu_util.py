@@ -175,17 +175,20 @@ def check_tokens_for(cfg, gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq):
 
 
 def verify_parity(gpu_ab, target_logits, draft_tokens, draft_logits, proposed, draft_T, T, seed, rnd, seq,
-                  trunc=None, draft_trunc=None):
+                  trunc=None, draft_trunc=None, penalties=None):
     """dflash_verify's (accept, bonus) against the oracle's verify on the same
     inputs: the target logits and the draft logits that the GPU session keeps
     from its proposal (copied back).  A result may differ only where the
     decision lies within rounding of its threshold: an acceptance test
     r q(d) < p(d) within ACCEPT_RTOL, or a bonus draw whose top-2 score margin
-    is below 1e-3.  Returns True when the pair was compared, False when
-    exempted."""
+    is below 1e-3.  penalties: the session's (repeat, presence, frequency,
+    history); draft_logits are then the penalised logits the proposal used.
+    Returns True when the pair was compared, False when exempted."""
     tl = np.asarray(target_logits, dtype=np.float64)
     dl = np.asarray(draft_logits, dtype=np.float64)
-    a_ref, b_ref = O.verify(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc)
+    a_ref, b_ref = O.verify(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc, penalties)
+    if O.penalties_active(penalties):
+        tl = np.stack([O.penalized(tl[r], penalties, draft_tokens[:r]) for r in range(len(tl))])
     if tuple(int(x) for x in gpu_ab) == (a_ref, b_ref):
         return True
     assert _verify_near(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc), \

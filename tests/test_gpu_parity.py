@@ -547,3 +547,60 @@ def test_rows_older_than_the_window_do_not_change_the_block_on_gpu(D):
     mixed[F - cfg.window + 1] = g_np[F - cfg.window + 1]      # the oldest visible row does matter
     c = _propose_logits(D, p.model, cfg, torch.from_numpy(mixed).cuda().to(torch.bfloat16), 0, 7)
     assert not np.array_equal(a, c)
+
+
+def test_committed_batch_flushes_together_and_equals_single_commits(D):
+    """dflash_committed_batch: sessions that reach 256 held rows flush in one
+    batched forward, sessions below it stage their rows, a restored prefix is
+    skipped, and the caches and cursors equal those of one dflash_committed
+    per session, bit for bit.  A gap in any session changes no session."""
+    p = Pair(S.CONFIGS["small_bf16"])
+    cfg = p.cfg
+    n = cfg.block_size - 1
+    f_np, f = p.feats(300, seed=80)
+    offs = [0, 64, 128, 192, 256, 320]
+    rows = [256, 100, 256, 300, 30, 256]
+    held = [0, 0, 20, 0, 0, 5]
+    single, batch = [], []
+    for j in range(len(offs)):
+        for group in (single, batch):
+            s = D.dflash_open(p.model, restored_offset=offs[j], max_ctx=offs[j] + 600)
+            if held[j]:
+                D.dflash_committed(s, f[:held[j]], offs[j])
+            if j % 2:   # an outstanding block that the flush must rewind
+                D.dflash_propose([s], torch.tensor([3], dtype=torch.int32, device="cuda"), n, 0.0, 0, 0,
+                                 torch.empty((1, n), dtype=torch.int32, device="cuda"),
+                                 torch.empty((1, n), dtype=torch.float32, device="cuda"))
+            group.append(s)
+    # the batch call: each session's run starts where its held rows start
+    feats = [f[:held[j] + rows[j]] for j in range(len(offs))]
+    before = [D.dflash_session_state(s) for s in batch]
+    bad_pos = [offs[j] for j in range(len(offs))]
+    bad_pos[3] += 1 + held[3]                                   # session 3: a gap
+    with pytest.raises(D.DFlashError) as e:
+        D.dflash_committed_batch(batch, feats, bad_pos)
+    assert e.value.status == D.DFLASH_ERR_CONTEXT_GAP
+    assert [D.dflash_session_state(s) for s in batch] == before
+    D.dflash_committed_batch(batch, feats, offs)
+    for j, s in enumerate(single):
+        D.dflash_committed(s, feats[j], offs[j])
+    for a, b in zip(single, batch):
+        assert D.dflash_session_state(a) == D.dflash_session_state(b)
+    for j, (a, b) in enumerate(zip(single, batch)):
+        F_, P_, _ = D.dflash_session_state(a)
+        assert (P_ == 0) == (held[j] + rows[j] >= 256)
+        if F_ == offs[j]:
+            continue                # staged only: nothing in the cache yet
+        for l in (0, cfg.n_layers - 1):
+            ka, va = export_kv(D, a, cfg, l, offs[j], F_ - offs[j])
+            kb, vb = export_kv(D, b, cfg, l, offs[j], F_ - offs[j])
+            assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    # the flushed rows equal the oracle's
+    o = O.OracleSession(p.oracle, restored_offset=offs[0])
+    o.committed(f_np[:256], offs[0])
+    k, v = export_kv(D, batch[0], cfg, 1, 0, 256)
+    assert_cache_close(k, np.stack([o.cache[s][0][1] for s in range(256)], axis=1))
+    assert_cache_close(v, np.stack([o.cache[s][1][1] for s in range(256)], axis=1))
+    D.dflash_device_status(p.model)
+    for s in single + batch:
+        D.dflash_close(s)
