@@ -378,6 +378,17 @@ def run_ours(args, rank, world, local_rank):
         D.dflash_close(s)
     del model, weights
     torch.cuda.empty_cache()
+    # the metric's other two configurations, each timed the same way (own
+    # warm-up, CUDA events, clocks sampled during its own timed region)
+    for key, wl in (("bs64", "batched"), ("flush", "flush")):
+        sub = run_workload(argparse.Namespace(**dict(vars(args), workload=wl)), rank, world, local_rank)
+        torch.cuda.empty_cache()
+        if result is not None:
+            result[key] = {k: sub[k] for k in ("metric", "value", "unit", "ms_per_step", "roofline", "clocks",
+                                               "gpu_launches", "config") if k in sub}
+            for extra in ("rounds_s", "per_sequence_flush_rows_s"):
+                if extra in sub:
+                    result[key][extra] = sub[extra]
     if result is not None and host_w is not None:
         result["cpu_baseline"] = cpu_baseline(cfg, host_w)
     return result
@@ -408,6 +419,27 @@ def _timed(torch, stream, fn, K, W, local_rank, world, dev):
     return max_over_ranks(e0.elapsed_time(e1), world, dev), clk
 
 
+def _instrumented_step(D, model, stream, step, torch, i=0):
+    """One more step with the library's per-class CUDA events: returns its
+    kernel launches and, per kernel class, launches, milliseconds and GB/s.
+    (The events break the launch overlap, so this step is not a timed one.)"""
+    D.dflash_timing_enable(model, True)
+    with torch.cuda.stream(stream):
+        step(i)
+    t = D.dflash_timing_read(model)
+    D.dflash_timing_enable(model, False)
+    classes = {k: {"launches": v["launches"], "ms": round(v["total_ms"], 4),
+                   "gbs": round(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 1) if v["total_ms"] else None,
+                   "tflops": round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1) if v["total_ms"] else None}
+               for k, v in t.items() if k != "all"}
+    return int(t.get("all", {}).get("launches", 0)), classes
+
+
+def _launches_per_step(D, model, stream, step, torch, i=0):
+    """Kernel launches of one more step, counted by the library."""
+    return _instrumented_step(D, model, stream, step, torch, i)[0]
+
+
 def _line(metric, unit, value, world, K, W, ms, dtype, config, extra, clk):
     out = {"metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K, "warmup": W,
            "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -435,37 +467,42 @@ def run_workload(args, rank, world, local_rank):
 
     if args.workload == "flush":
         # 8 sequences at context offsets 0, 1k, ..., 7k; each step every
-        # sequence commits 256 new feature rows, which reach the pending
-        # threshold and flush in one context-only forward (M = 256)
+        # sequence commits 256 new feature rows in one dflash_committed_batch
+        # call: all 8 reach the pending threshold and flush together as one
+        # context-only forward of 2048 rows (the first step also rewinds the
+        # outstanding blocks)
         cfg = S.CONFIGS[CFG_NAME]
         rows, nseq = 256, 8
         model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED + rank, dev))
         with torch.cuda.stream(stream):
-            sess = [D.dflash_open(model, restored_offset=1024 * j, max_ctx=1024 * j + rows * (2 * K + W + 8),
+            sess = [D.dflash_open(model, restored_offset=1024 * j, max_ctx=1024 * j + rows * (2 * K + 2 * W + 8),
                                   stream=stream) for j in range(nseq)]
             feats = torch.randn((rows, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
             n = cfg.block_size - 1
             cur = torch.full((1,), 3, dtype=torch.int32, device=dev)
             tok = torch.empty((1, n), dtype=torch.int32, device=dev)
             q = torch.empty((1, n), dtype=torch.float32, device=dev)
-            for s_ in sess[1:]:      # an outstanding block that the first flush rewinds
+            for s_ in sess:      # an outstanding block that the first flush rewinds
                 D.dflash_propose([s_], cur, n, 0.0, 0, 0, tok, q)
+        pos = [1024 * j for j in range(nseq)]
 
         def step(i):
-            for j, s_ in enumerate(sess):
-                D.dflash_committed(s_, feats, 1024 * j + rows * i)
+            D.dflash_committed_batch(sess, [feats] * nseq, pos)
+            for j in range(nseq):
+                pos[j] += rows
 
         ms, clk = _timed(torch, stream, step, K, W, local_rank, world, dev)
         for j, s_ in enumerate(sess):       # cursor consistency after every rewind + flush
             assert D.dflash_session_state(s_) == (1024 * j + rows * (K + W), 0, False)
-        # the same rows as one batched flush: 255 staged rows per sequence, one forward of 2040 rows
-        def step_b(i):
+        launches, classes = _instrumented_step(D, model, stream, step, torch)
+        # the same rows flushed one sequence at a time (dflash_committed per
+        # sequence: eight forwards of 256 rows)
+        def step_1(i):
             for j, s_ in enumerate(sess):
-                D.dflash_committed(s_, feats[:rows - 1], 1024 * j + rows * (K + W) + (rows - 1) * i)
-            D.dflash_flush(sess)
+                D.dflash_committed(s_, feats, pos[j])
+                pos[j] += rows
 
-        Kb = max(1, K // 2)
-        ms_b, _ = _timed(torch, stream, step_b, Kb, 1, local_rank, world, dev)
+        ms_1, _ = _timed(torch, stream, step_1, max(1, K // 2), 1, local_rank, world, dev)
         kv_params = 2 * cfg.n_kv_heads * cfg.head_dim * cfg.hidden * cfg.n_layers
         fc_params = cfg.hidden * cfg.feature_width
         flops = 2.0 * rows * nseq * (fc_params + kv_params)
@@ -475,14 +512,17 @@ def run_workload(args, rank, world, local_rank):
             D.dflash_close(s_)
         return _line("flush rows/s (8 sequences x 256 pending rows, Qwen3-8B-shaped draft)", "rows/s",
                      world * rows * nseq / (ms / K * 1e-3), world, K, W, ms, "bf16",
-                     {"workload": "8 x committed(256 rows [256, 20480]) at context offsets 0..7k, each a "
-                                  "context-only forward after a block rewind", "l2": "252 MB of fc/K/V weights "
-                                  "per flush; features 10.5 MB resident"},
+                     {"workload": "8 sequences at context offsets 0..7k commit 256 rows [256, 20480] each per step "
+                                  "(dflash_committed_batch): one batched context-only forward of 2048 rows, the "
+                                  "first after a block rewind", "l2": "252 MB of fc/K/V weights per flush; "
+                                  "features 10.5 MB resident"},
                      {"roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak_t,
                                    "unit": "TFLOP/s", "frac": round(tflops / peak_t, 4),
-                                   "peak_kind": f"{peak_kind} bf16 (sustained)"},
-                      "batched_flush_rows_s": round(world * (rows - 1) * nseq / (ms_b / Kb * 1e-3), 1),
-                      "gpu_launches": None}, clk)
+                                   "peak_kind": f"{peak_kind} bf16 (sustained)",
+                                   "algorithmic_flops_per_step": flops},
+                      "per_sequence_flush_rows_s": round(world * rows * nseq / (ms_1 / max(1, K // 2) * 1e-3), 1),
+                      "kernel_classes_instrumented_one_step": classes,
+                      "gpu_launches": launches * K}, clk)
 
     if args.workload == "laguna":
         res = {}
@@ -498,7 +538,8 @@ def run_workload(args, rank, world, local_rank):
                     D.dflash_committed(s_, f, lo)
                     del f
                 D.dflash_flush([s_])
-                feats = torch.randn((W + K, P_ROWS, cfg.feature_width), generator=g, device=dev).to(torch.bfloat16)
+                feats = torch.randn((W + K + 1, P_ROWS, cfg.feature_width), generator=g,
+                                    device=dev).to(torch.bfloat16)
                 tl = (torch.randn((1, n + 1, cfg.vocab), generator=g, device=dev) * 3.0).contiguous()
                 cur = torch.full((1,), 17, dtype=torch.int32, device=dev)
                 tok = torch.empty((1, n), dtype=torch.int32, device=dev)
@@ -513,19 +554,23 @@ def run_workload(args, rank, world, local_rank):
 
             ms, clk = _timed(torch, stream, step, K, W, local_rank, world, dev)
             rb = round_bytes(cfg, T, P_ROWS)
-            res[bs] = (world * K / (ms * 1e-3), ms, clk, rb)
+            res[bs] = (world * K / (ms * 1e-3), ms, clk, rb, _launches_per_step(D, model, stream, step, torch, K + W))
             D.dflash_close(s_)
             del model
             torch.cuda.empty_cache()
-        v16, ms16, clk16, rb16 = res[16]
+        v16, ms16, clk16, rb16, launches16 = res[16]
         gbs = rb16 / (ms16 / K * 1e-3) / 1e9
         return _line("draft rounds/s (Laguna-style gated window-512 draft, bs1, block 16)", "draft rounds/s", v16,
                      world, K, W, ms16, "bf16",
                      {"workload": "laguna_bf16: 4 layers, H 3072, 24/8 heads x 128, I 8192 (assumed), V 100352, "
                                   "window 512 over a 32768-row temporal context, 4 committed rows per round, T=1.0",
-                      "l2": "no flush: 2.1 GB of weights streamed per round"},
-                     {"round_roofline": {"bound": "hbm", "algorithmic_bytes": rb16, "achieved_gbs": round(gbs, 1),
-                                         "peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)},
+                      "l2": f"no flush: {rb16 / 1e9:.2f} GB of weights, K/V and logits per round"},
+                     {"roofline": {"kernel": "whole round (weight-streaming GEMMs dominate)", "bound": "hbm",
+                                   "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                   "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                                   "algorithmic_bytes_per_step": rb16, "traffic": None},
+                      "gpu_launches": launches16 * K,
                       "block8_rounds_s": round(res[8][0], 2),
                       "block8_round_roofline_frac": round(res[8][3] / (res[8][1] / K * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                                           4)}, clk16)
@@ -566,6 +611,7 @@ def run_workload(args, rank, world, local_rank):
         D.dflash_verify(sess, tl, tok, n, Tb, SEED, i, acc, bon)
 
     ms, clk = _timed(torch, stream, step, K, W, local_rank, world, dev)
+    launches, classes = _instrumented_step(D, model, stream, step, torch, K + W)
     H, I, V = cfg.hidden, cfg.intermediate, cfg.vocab
     per_layer = cfg.qkv_rows * H + H * cfg.n_q_heads * cfg.head_dim + 3 * H * I
     gemm_flops = 2.0 * (B * (n + 1) * (cfg.n_layers * per_layer) + B * n * V * H +
@@ -583,7 +629,8 @@ def run_workload(args, rank, world, local_rank):
                  {"workload": "64 sequences, contexts uniform 1k-16k (seeded K/V), 4 committed rows each per round, "
                               "batched propose + rejection-sampling verify at T=0.7 on N(0,3) target logits "
                               "[64,16,151936]", "l2": "no flush: 11+ GB of K/V and 3.4 GB of weights per round"},
-                 {"rounds_s": round(world / t_step, 2),
+                 {"rounds_s": round(world / t_step, 2), "gpu_launches": launches * K,
+                  "kernel_classes_instrumented_one_step": classes,
                   "roofline": {"bound": "mixed (GEMMs tensor, attention and verify HBM)",
                                "ideal_ms_per_step": round(ideal * 1e3, 3), "frac": round(ideal / t_step, 4),
                                "gemm_tflop_per_step": round(gemm_flops / 1e12, 3),
@@ -779,10 +826,99 @@ def _threads():
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu on Arm hosts, /proc/cpuinfo elsewhere)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_sample_child():
+    """One bounded sample of the round on the oracle, in a fresh process whose
+    BLAS runs one thread: the context path of the 4 held rows, one draft layer
+    (its K/V of the new rows and the 16-row block layer at ctx 4096), 1/16 of
+    the unembedding, and the draw + verify over the whole vocabulary.  Prints
+    the times as JSON, with the round time extrapolated as
+    start + L * layer + 16 * unembed slice + finish."""
+    import numpy as np
+
+    import synthetic as S
+    from oracle import dflash_oracle as O
+    cfg = S.CONFIGS[CFG_NAME]
+    L, n, V, H = cfg.n_layers, cfg.block_size - 1, cfg.vocab, cfg.hidden
+    J = 16
+    names = ["aux_norms", "w_fc", "hidden_norm", "final_norm"] + \
+        [k for k in S.weight_shapes(cfg) if k.startswith("layers.0.")]
+    w = S.make_weights(cfg, seed=SEED, names=names)
+    # the embedding is only gathered (two rows) and 1/16 of the unembedding is
+    # read: untouched zero pages stand for the rest
+    w["embed"] = np.zeros((V, H), dtype=np.float32)
+    w["unembed"] = np.zeros((V, H), dtype=np.float32)
+    w["unembed"][: V // J] = S.normal(SEED, "unembed", (V // J, H), std=0.02, dtype="bf16")
+    d = O.OracleDraft(cfg, w)
+    feats = S.make_features(cfg, P_ROWS, seed=SEED)
+    Kc = S.make_kv(cfg, CTX - P_ROWS, SEED, "ctx_k")[0].transpose(1, 0, 2).astype(np.float64)
+    Vc = S.make_kv(cfg, CTX - P_ROWS, SEED, "ctx_v")[0].transpose(1, 0, 2).astype(np.float64)
+    tl = np.random.default_rng(SEED).standard_normal((n + 1, V)) * 3.0
+    t = {}
+    t0 = time.perf_counter()
+    hid = d.context_hidden(feats)
+    h = d.w.rows("embed", [17] + [cfg.mask_token] * n)
+    t["start"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    ck, cv = d.context_layer_kv(0, hid, np.arange(CTX - P_ROWS, CTX))
+    h = d.block_layer(0, h, CTX + np.arange(n + 1, dtype=np.float64), np.concatenate([Kc, ck]),
+                      np.concatenate([Vc, cv]), np.arange(CTX, dtype=np.float64))
+    t["layer"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    lg = np.zeros((n, V))
+    lg[:, : V // J] = d.unembed(h[1:], 0, V // J)
+    t["unembed_slice"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    toks, _, _ = O.sample_rows(lg, TEMP, SEED, 0, 0)
+    O.verify(tl, toks, lg, toks, TEMP, TEMP, SEED, 0, 0)
+    t["finish"] = time.perf_counter() - t0
+    t["round_s"] = t["start"] + L * t["layer"] + J * t["unembed_slice"] + t["finish"]
+    print(json.dumps(t), flush=True)
+
+
+def _oracle_samples(nproc: int):
+    """Runs _oracle_sample_child in nproc fresh single-threaded processes at
+    once; returns their results and the wall time."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    cmd = [sys.executable, "-c", "import bench; bench._oracle_sample_child()"]
+    t0 = time.perf_counter()
+    procs = [subprocess.Popen(cmd, cwd=ROOT, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+             for _ in range(nproc)]
+    outs = []
+    for pr in procs:
+        out, _ = pr.communicate(timeout=600)
+        if pr.returncode == 0 and out.strip():
+            outs.append(json.loads(out.strip().splitlines()[-1]))
+    return outs, time.perf_counter() - t0
+
+
 def cpu_baseline(cfg, host_w):
-    """One whole round of the oracle on the host: 4 held rows through the
-    context path, the 16-row block at ctx 4096 (context K/V seeded directly),
-    the unembedding, the draw, and the verify."""
+    """One whole round of the oracle on the host with every BLAS thread: 4
+    held rows through the context path, the 16-row block at ctx 4096 (context
+    K/V seeded directly), the unembedding, the draw, and the verify.  Then a
+    bounded single-thread sample of the round (extrapolated to a round), and
+    the same sample in one single-threaded process per host core at once
+    (independent sequences)."""
     O, d, cache, feats, tl = _oracle_setup(cfg, host_w)
     n = cfg.block_size - 1
     s = O.OracleSession(d, restored_offset=CTX - P_ROWS, restored_cache={k: v for k, v in cache.items()
@@ -792,9 +928,24 @@ def cpu_baseline(cfg, host_w):
     out = s.propose(17, n, TEMP, SEED, 0)
     s.verify(tl, out["tokens"], TEMP, SEED, 0)
     dt = time.perf_counter() - t0
-    return {"value": round(1.0 / dt, 5), "unit": UNIT, "cores": _threads(), "kind": "oracle",
-            "sample": f"one whole round on the host ({dt:.1f} s): 4 held rows, 16-row block at ctx 4096 "
-                      "(context K/V seeded directly), unembedding, draw and verify; float64 numpy"}
+    del d, cache, s
+    res = {"value": round(1.0 / dt, 5), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+           "sample": f"one whole round on the host ({dt:.1f} s): 4 held rows, 16-row block at ctx 4096 "
+                     "(context K/V seeded directly), unembedding, draw and verify; float64 numpy",
+           "cpu_model": cpu_model(), "nproc": os.cpu_count()}
+    one, _ = _oracle_samples(1)
+    if one:
+        res["single_thread"] = {"rounds_s": round(1.0 / one[0]["round_s"], 5), "round_s": round(one[0]["round_s"], 2),
+                                "sample": "context path + 1 of 5 layers + 1/16 of the unembedding + draw and "
+                                          "verify, one BLAS thread, extrapolated to a round", "times_s": one[0]}
+    N = os.cpu_count() or 1
+    many, wall = _oracle_samples(N)
+    if many:
+        res["n_process"] = {"processes": len(many),
+                            "rounds_s": round(sum(1.0 / m["round_s"] for m in many), 5),
+                            "sample": "the single-thread sample in one process per core at once, one sequence "
+                                      "each; rounds/s summed over the processes", "wall_s": round(wall, 1)}
+    return res
 
 
 def run_reference(args, rank, world):
