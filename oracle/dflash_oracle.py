@@ -46,7 +46,18 @@ Readings where the pages are silent:
   and the frequency penalty c times;  R26 every draft row sees the same
   committed history (no row of the block counts toward another's
   penalties), while target row r of verify sees that history plus the draft
-  tokens d_1..d_r before it, the history classic decoding would have had.
+  tokens d_1..d_r before it, the history classic decoding would have had;
+  R27 (DFlash2) each layer's block-local dynamic convolution follows the
+  attention residual: x = RMSNorm(h; conv_norm), per row i and channel group
+  g (one group per query head) kernel weights softmax_j((W_dc x_i)[g, j])
+  over conv_taps taps, and h_i += sum_j w_ij * x_{i-j} over the block's own
+  rows (rows before the anchor count as zero);  R28 (DFlash2) the selector's
+  candidates at position i are the sel_candidates largest logits of row i
+  (value desc, id asc), scored l_i(c) + <A[prev], B[c]> with prev the token
+  chosen at i - 1 (the anchor for i = 1) and A, B the [V, sel_rank] selector
+  tables; the draw is Gumbel-max over the candidates at the request
+  temperature only, and q_i = softmax(score / T) over them;  R29 (DFlash2)
+  a proposal always drafts min(7, B_s - 1) tokens (dflash2Depth).
 
 Storage rounding: for bf16 configs the values that the CUDA path stores in
 bf16 are rounded to the nearest bf16 here too (u, c, the layer inputs fed to
@@ -63,6 +74,7 @@ from __future__ import annotations
 import numpy as np
 
 PENDING_FLUSH_TOKENS = 256   # dflash.go: dflashPendingFlushTokens
+DFLASH2_DEPTH = 7            # dflash.go: dflash2Depth, a DFlash2 session's fixed draft length
 
 
 class ContextGap(Exception):
@@ -316,6 +328,23 @@ class OracleDraft:
                 o[i, hq] = softmax((keys @ q[i, hq]) * scale) @ vals
         return o
 
+    def dynamic_conv(self, l, h):
+        """DFlash2's block-local dynamic convolution of layer l over the block
+        rows h [nb, H] (R27); returns h plus the convolution."""
+        c, st = self.cfg, self.st
+        nb, H = h.shape
+        G, kap = c.n_q_heads, c.conv_taps
+        x = st(rmsnorm(h, self.w[f"layers.{l}.conv_norm"], c.rms_eps))
+        a = linear(self.w[f"layers.{l}.w_dc"], x).reshape(nb, G, kap)
+        wk = np.exp(a - a.max(axis=-1, keepdims=True))
+        wk /= wk.sum(axis=-1, keepdims=True)
+        gw = H // G
+        out = np.zeros_like(h)
+        for i in range(nb):
+            for j in range(min(kap, i + 1)):
+                out[i] += np.repeat(wk[i, :, j], gw) * x[i - j]
+        return st(h + out)
+
     def block_layer(self, l, h, pos, ck, cv, cpos):
         """One draft layer over the block rows h [nb, H] at positions pos,
         against context K/V ck, cv [N, Hkv, d] at positions cpos."""
@@ -338,6 +367,8 @@ class OracleDraft:
             o = o * gate[:, :, None]
         o = st(o.reshape(nb, qd))
         h = st(h + linear(w[p + "w_o"], o))
+        if c.variant == "dflash2":
+            h = self.dynamic_conv(l, h)
         y = st(rmsnorm(h, w[p + "post_norm"], c.rms_eps))
         a = st(silu(linear(w[p + "w_gate"], y)) * linear(w[p + "w_up"], y))
         return st(h + linear(w[p + "w_down"], a))
@@ -354,6 +385,36 @@ class OracleDraft:
         for l in range(self.cfg.n_layers):
             h = self.block_layer(l, h, pos, ctx["k"][l], ctx["v"][l], cpos)
         return h
+
+    def select_block(self, logits, current, temperature, seed, rnd, seq):
+        """DFlash2's candidate selector over rows 1..n (R28; dflash.go
+        selectBlock, the BlockSelector branch): each position's token is
+        drawn from its candidates conditioned on its predecessor.  Returns
+        tokens [n], candidate ids [n, k], their probabilities [n, k] (one-hot
+        on the token at T = 0) and q(token) [n]."""
+        c = self.cfg
+        logits = np.atleast_2d(np.asarray(logits, dtype=np.float64))
+        n, V = logits.shape
+        k = min(c.sel_candidates, V)
+        A, B = self.w["sel_prev"], self.w["sel_next"]
+        toks = np.zeros(n, dtype=np.int64)
+        ids = np.zeros((n, k), dtype=np.int64)
+        probs = np.zeros((n, k))
+        prev = int(current)
+        for i in range(n):
+            row = logits[i]
+            cand = np.lexsort((np.arange(V), -row))[:k]
+            score = row[cand] + B[cand] @ A[prev]
+            if temperature == 0:
+                j = int(np.argmax(score))
+                probs[i, j] = 1.0
+            else:
+                z = score / temperature + gumbel(seed, rnd, STREAM_DRAFT, seq, i + 1, cand)
+                j = int(np.argmax(z))
+                probs[i] = softmax(score / temperature)
+            ids[i] = cand
+            toks[i] = prev = int(cand[j])
+        return toks, ids, probs, probs[np.arange(n), np.argmax(ids == toks[:, None], axis=1)]
 
     def unembed(self, h_rows, lo=0, hi=None):
         """Raw draft logits of block rows (final norm, then the unembedding);
@@ -478,8 +539,13 @@ def sampler_distribution(logits_row, temperature, trunc=None):
     return p
 
 
-def proposal_distribution(draft_logits_row, draft_temperature, proposed_token, trunc=None):
-    """q of one block row: the sampler's distribution at T > 0, one-hot of the proposal at T == 0."""
+def proposal_distribution(draft_logits_row, draft_temperature, proposed_token, trunc=None, cands=None):
+    """q of one block row: the sampler's distribution at T > 0, one-hot of the
+    proposal at T == 0; cands = (ids, probs): a DFlash2 candidate distribution."""
+    if cands is not None and draft_temperature > 0:
+        q = np.zeros(len(draft_logits_row))
+        q[np.asarray(cands[0], dtype=np.int64)] = cands[1]
+        return q
     if draft_temperature == 0:
         q = np.zeros(len(draft_logits_row))
         q[int(proposed_token)] = 1.0
@@ -488,7 +554,7 @@ def proposal_distribution(draft_logits_row, draft_temperature, proposed_token, t
 
 
 def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_temperature,
-           temperature, seed, rnd, seq, trunc=None, draft_trunc=None, penalties=None):
+           temperature, seed, rnd, seq, trunc=None, draft_trunc=None, penalties=None, draft_cands=None):
     """Accepted prefix length a and bonus token b.
 
     target_logits [n+1, V]: row r scores the token after [current, d_1..d_r].
@@ -508,6 +574,9 @@ def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_tem
     penalties = (repeat, presence, frequency, history): target row r is
     penalised over the history plus d_1..d_r (R26); draft_logits are the
     logits the proposal was drawn from, its penalties already applied.
+    draft_cands = (ids [n, k], probs [n, k]): DFlash2's per-position candidate
+    distributions, which are q (the DFlash2 commit note: verification uses
+    each position's candidate distribution to keep the output exact).
     """
     tl = np.atleast_2d(np.asarray(target_logits, dtype=np.float64))
     if penalties_active(penalties):
@@ -521,7 +590,8 @@ def verify(target_logits, draft_tokens, draft_logits, proposed_tokens, draft_tem
         return a, int(np.argmax(tl[a]))
     for i in range(1, n + 1):
         p = sampler_distribution(tl[i - 1], temperature, trunc)
-        q = proposal_distribution(draft_logits[i - 1], draft_temperature, proposed_tokens[i - 1], draft_trunc)
+        q = proposal_distribution(draft_logits[i - 1], draft_temperature, proposed_tokens[i - 1], draft_trunc,
+                                  None if draft_cands is None else (draft_cands[0][i - 1], draft_cands[1][i - 1]))
         d = int(draft_tokens[i - 1])
         r = uniform_open(random_u32(seed, rnd, STREAM_ACCEPT, seq, i, 0))
         if r * q[d] < p[d]:
@@ -658,6 +728,8 @@ class OracleSession:
         n = min(int(max_tokens), c.block_size - 1)
         if n <= 0 or self.F + self.P == 0:
             return None
+        if c.variant == "dflash2":
+            n = min(DFLASH2_DEPTH, c.block_size - 1)      # the fixed depth overrides max_tokens (R29)
         self.commit_block()
         rows, first = self.take_pending()
         self._write_context(rows, first)
@@ -665,10 +737,18 @@ class OracleSession:
         tokens = [int(current)] + [c.mask_token] * n
         h = self.draft.block_forward(tokens, self.F, self.context())
         logits = self.draft.unembed(h[1:])          # the anchor row is unused
+        if c.variant == "dflash2":
+            # the selector draws at the request temperature only (DFlash2 note)
+            toks, ids, probs, q = self.draft.select_block(logits, current, temperature, seed, rnd, self.seq)
+            lse = np.full(n, np.nan)
+            self.last = dict(tokens=toks, logits=logits, temperature=temperature, trunc=None, cands=(ids, probs))
+            self.stats["rounds"] += 1
+            self.stats["proposed"] += n
+            return dict(tokens=toks, q=q, logits=logits, lse=lse, hidden=h, n=n, cand_ids=ids, cand_probs=probs)
         # every row sees the same committed history (R26)
         logits = np.stack([penalized(row, self.penalties) for row in logits])
         toks, q, lse = sample_rows(logits, temperature, seed, rnd, self.seq, self.sampler)
-        self.last = dict(tokens=toks, logits=logits, temperature=temperature, trunc=self.sampler)
+        self.last = dict(tokens=toks, logits=logits, temperature=temperature, trunc=self.sampler, cands=None)
         self.stats["rounds"] += 1
         self.stats["proposed"] += n
         return dict(tokens=toks, q=q, logits=logits, lse=lse, hidden=h, n=n)
@@ -678,7 +758,7 @@ class OracleSession:
             raise RuntimeError("verify without a proposal")
         a, b = verify(target_logits, draft_tokens, self.last["logits"], self.last["tokens"],
                       self.last["temperature"], temperature, seed, rnd, self.seq, self.sampler,
-                      self.last["trunc"], self.penalties)
+                      self.last["trunc"], self.penalties, self.last["cands"])
         self.stats["accepted"] += a
         return a, b
 

@@ -53,6 +53,13 @@ class DraftConfig:
     gated_attention: bool = False  # per-head sigmoid gate (g_proj) on the attention output
     rope_theta: float = 1e6
     rms_eps: float = 1e-6
+    # DFlash2 (block-local dynamic convolutions and a candidate selector):
+    # "dflash" or "dflash2"; the convolution's width, the selector tables'
+    # rank and the number of candidates per position are not on the pages
+    variant: str = "dflash"
+    conv_taps: int = 4
+    sel_rank: int = 64
+    sel_candidates: int = 8
 
     @property
     def feature_width(self) -> int:
@@ -102,6 +109,16 @@ CONFIGS: dict[str, DraftConfig] = {
         hidden=384, n_layers=2, n_q_heads=6, n_kv_heads=2, head_dim=128,
         intermediate=768, vocab=1000, block_size=8, mask_token=999, window=64,
         gated_attention=True),
+    # DFlash2 drafts: the tiny fp32 and small bf16 shapes with the dynamic
+    # convolutions and the candidate selector
+    "tiny_dflash2_fp32": DraftConfig(
+        name="tiny_dflash2_fp32", dtype="f32", n_taps=5, target_hidden=256, hidden=256,
+        n_layers=2, n_q_heads=4, n_kv_heads=4, head_dim=64, intermediate=512,
+        vocab=32, block_size=8, mask_token=31, causal_block=True, variant="dflash2"),
+    "small_dflash2_bf16": DraftConfig(
+        name="small_dflash2_bf16", dtype="bf16", n_taps=3, target_hidden=512, hidden=512,
+        n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128, intermediate=1024,
+        vocab=1000, block_size=16, mask_token=999, variant="dflash2"),
 }
 
 
@@ -158,6 +175,12 @@ def weight_shapes(cfg: DraftConfig) -> dict[str, tuple]:
         s[p + "w_gate"] = (cfg.intermediate, H)
         s[p + "w_up"] = (cfg.intermediate, H)
         s[p + "w_down"] = (H, cfg.intermediate)
+        if cfg.variant == "dflash2":
+            s[p + "conv_norm"] = (H,)
+            s[p + "w_dc"] = (cfg.n_q_heads * cfg.conv_taps, H)
+    if cfg.variant == "dflash2":
+        s["sel_prev"] = (cfg.vocab, cfg.sel_rank)
+        s["sel_next"] = (cfg.vocab, cfg.sel_rank)
     return s
 
 
@@ -169,6 +192,9 @@ def make_weights(cfg: DraftConfig, seed: int = 0, names=None) -> dict[str, np.nd
             continue
         if name.endswith("norm") or name == "aux_norms":
             out[name] = normal(seed, name, shape, std=0.02, mean=1.0, dtype=cfg.dtype)
+        elif name in ("sel_prev", "sel_next"):
+            # selector tables: a transition term of std ~0.125 next to the logits
+            out[name] = normal(seed, name, shape, std=0.125, dtype=cfg.dtype)
         else:
             out[name] = normal(seed, name, shape, std=0.02, dtype=cfg.dtype)
     return out
