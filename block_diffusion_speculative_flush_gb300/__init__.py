@@ -16,7 +16,8 @@ import torch
 from . import _abi
 from ._abi import (DFLASH_DTYPE_BF16, DFLASH_DTYPE_F32, DFLASH_ERR_CAPACITY, DFLASH_ERR_CONTEXT_GAP,
                    DFLASH_ERR_CUDA, DFLASH_ERR_DEVICE, DFLASH_ERR_INVALID_ARG, DFLASH_ERR_OOM, DFLASH_ERR_SHAPE,
-                   DFLASH_ERR_STATE, DFLASH_FLAG_SIMT_GEMM, DFLASH_OK, DFLASH_PENDING_FLUSH_TOKENS)
+                   DFLASH_ERR_STATE, DFLASH_FLAG_SIMT_GEMM, DFLASH_OK, DFLASH_PENDING_FLUSH_TOKENS,
+                   DFLASH_VARIANT_DFLASH, DFLASH_VARIANT_DFLASH2, DFLASH2_DEPTH)
 
 lib = _abi.load()
 
@@ -24,7 +25,7 @@ __all__ = [
     "DFlashError", "Model", "Session", "lib", "torch_dtype",
     "dflash_model_create", "dflash_model_destroy", "dflash_draft_limit", "dflash_device_status", "dflash_open",
     "dflash_committed", "dflash_committed_taps", "dflash_flush", "dflash_settle", "dflash_commit_block", "dflash_propose", "dflash_verify",
-    "dflash_close", "dflash_set_sampler", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
+    "dflash_close", "dflash_set_sampler", "dflash_set_penalties", "dflash_candidates", "dflash_committed_batch", "dflash_stats", "dflash_session_state", "dflash_kv_export", "dflash_kv_import",
     "dflash_version", "dflash_last_error", "dflash_timing_enable", "dflash_timing_read", "dflash_verify_noalloc",
     "Target", "dflash_target_create", "dflash_target_destroy", "dflash_target_forward", "dflash_target_trim",
     "dflash_target_length", "dflash_target_argmax", "dflash_target_device_status",
@@ -118,7 +119,10 @@ def dflash_model_create(cfg, weights: dict, flags: int = 0) -> Model:
         n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, intermediate=cfg.intermediate, vocab=cfg.vocab,
         block_size=cfg.block_size, mask_token=cfg.mask_token, window=cfg.window,
         causal_block=int(cfg.causal_block), gated_attention=int(cfg.gated_attention), flags=flags,
-        rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps)
+        rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps,
+        variant=DFLASH_VARIANT_DFLASH2 if getattr(cfg, "variant", "dflash") == "dflash2" else DFLASH_VARIANT_DFLASH,
+        conv_taps=getattr(cfg, "conv_taps", 0), sel_rank=getattr(cfg, "sel_rank", 0),
+        sel_candidates=getattr(cfg, "sel_candidates", 0))
     t = {k: v.contiguous() for k, v in weights.items()}
     layers = (_abi.dflash_layer_weights * cfg.n_layers)()
     for l in range(cfg.n_layers):
@@ -127,9 +131,10 @@ def dflash_model_create(cfg, weights: dict, flags: int = 0) -> Model:
         layers[l] = _abi.dflash_layer_weights(
             _ptr(t[p + "in_norm"]), _ptr(t[p + "w_qkv"]), _ptr(t[p + "q_norm"]), _ptr(t[p + "k_norm"]), _ptr(g),
             _ptr(t[p + "w_o"]), _ptr(t[p + "post_norm"]), _ptr(t[p + "w_gate"]), _ptr(t[p + "w_up"]),
-            _ptr(t[p + "w_down"]))
+            _ptr(t[p + "w_down"]), _ptr(t.get(p + "conv_norm")), _ptr(t.get(p + "w_dc")))
     w = _abi.dflash_weights(_ptr(t["aux_norms"]), _ptr(t["w_fc"]), _ptr(t["hidden_norm"]), _ptr(t["final_norm"]),
-                            _ptr(t["embed"]), _ptr(t["unembed"]), layers)
+                            _ptr(t["embed"]), _ptr(t["unembed"]), layers, _ptr(t.get("sel_prev")),
+                            _ptr(t.get("sel_next")))
     out = C.c_void_p()
     _check(lib.dflash_model_create(C.byref(c), C.byref(w), C.byref(out)))
     return Model(out.value, cfg, t, layers)
@@ -221,7 +226,10 @@ def dflash_propose(sessions, current: torch.Tensor, max_tokens: int, temperature
     """Returns out_n per session (0 where the pages return nil)."""
     arr, n = _sessions(sessions)
     cfg = _model_of(sessions).cfg
-    rows = n * max(0, min(int(max_tokens), cfg.block_size - 1))
+    per = max(0, min(int(max_tokens), cfg.block_size - 1))
+    if per and getattr(cfg, "variant", "dflash") == "dflash2":
+        per = min(DFLASH2_DEPTH, cfg.block_size - 1)      # a DFlash2 proposal's fixed length
+    rows = n * per
     _need(current, torch.int32, n, "current")
     _need(out_tokens, torch.int32, rows, "out_tokens")
     _need(out_q, torch.float32, rows, "out_q")
@@ -265,6 +273,16 @@ def dflash_close(session: Session) -> None:
     if session.handle:
         _check(lib.dflash_close(session.handle))
         session.handle = None
+
+
+def dflash_candidates(session: Session, out_ids: torch.Tensor, out_probs: torch.Tensor) -> None:
+    """A DFlash2 session's last candidate distributions: ids int32 and
+    probabilities fp32, each [n, sel_candidates] on the device."""
+    cfg = session.model.cfg
+    k, n = cfg.sel_candidates, min(DFLASH2_DEPTH, cfg.block_size - 1)
+    _need(out_ids, torch.int32, n * k, "out_ids [n, sel_candidates]")
+    _need(out_probs, torch.float32, n * k, "out_probs [n, sel_candidates]")
+    _check(lib.dflash_candidates(session.handle, _ptr(out_ids), _ptr(out_probs)))
 
 
 def dflash_set_penalties(session: Session, repeat: float = 1.0, presence: float = 0.0, frequency: float = 0.0,

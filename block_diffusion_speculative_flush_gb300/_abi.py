@@ -21,6 +21,9 @@ DFLASH_DTYPE_F32 = 0
 DFLASH_DTYPE_BF16 = 1
 DFLASH_PENDING_FLUSH_TOKENS = 256
 DFLASH_FLAG_SIMT_GEMM = 1
+DFLASH_VARIANT_DFLASH = 0
+DFLASH_VARIANT_DFLASH2 = 1
+DFLASH2_DEPTH = 7
 
 
 class dflash_config(C.Structure):
@@ -30,18 +33,20 @@ class dflash_config(C.Structure):
         ("intermediate", C.c_int32), ("vocab", C.c_int32), ("block_size", C.c_int32), ("mask_token", C.c_int32),
         ("window", C.c_int32), ("causal_block", C.c_int32), ("gated_attention", C.c_int32), ("flags", C.c_uint32),
         ("rope_theta", C.c_float), ("rms_eps", C.c_float),
+        ("variant", C.c_int32), ("conv_taps", C.c_int32), ("sel_rank", C.c_int32), ("sel_candidates", C.c_int32),
     ]
 
 
 class dflash_layer_weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in
-                ("in_norm", "w_qkv", "q_norm", "k_norm", "w_g", "w_o", "post_norm", "w_gate", "w_up", "w_down")]
+                ("in_norm", "w_qkv", "q_norm", "k_norm", "w_g", "w_o", "post_norm", "w_gate", "w_up", "w_down",
+                 "conv_norm", "w_dc")]
 
 
 class dflash_weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in
                 ("aux_norms", "w_fc", "hidden_norm", "final_norm", "embed", "unembed")] + \
-               [("layers", C.POINTER(dflash_layer_weights))]
+               [("layers", C.POINTER(dflash_layer_weights)), ("sel_prev", C.c_void_p), ("sel_next", C.c_void_p)]
 
 
 class dflash_counters(C.Structure):
@@ -112,6 +117,7 @@ SIGNATURES = {
     "dflash_timing_read": (C.c_int, [P, C.POINTER(dflash_kernel_time), C.c_int32, C.POINTER(C.c_int32)]),
     "dflash_set_sampler": (C.c_int, [P, C.c_int32, C.c_float, C.c_float]),
     "dflash_set_penalties": (C.c_int, [P, C.c_float, C.c_float, C.c_float, P, C.c_int32]),
+    "dflash_candidates": (C.c_int, [P, P, P]),
     "dflash_target_create": (C.c_int, [C.POINTER(dflash_target_config), C.POINTER(dflash_target_weights), C.c_int64,
                                        P, C.POINTER(C.c_void_p)]),
     "dflash_target_destroy": (C.c_int, [P]),

@@ -143,6 +143,7 @@ struct HostRing {
 struct LayerW {
   const void *in_norm, *w_qkv, *q_norm, *k_norm, *w_g, *w_o, *post_norm, *w_gate, *w_up, *w_down;
   void* w_qkvg = nullptr;  // owned: [w_qkv ; w_g] rows, one product for q, k, v and the gate
+  const void *conv_norm = nullptr, *w_dc = nullptr;  // DFlash2's dynamic convolution
 };
 
 }  // namespace
@@ -152,6 +153,8 @@ struct dflash_model {
   DT dt = DT::F32;
   size_t esz = 4;
   const void *aux_norms, *w_fc, *hidden_norm, *final_norm, *embed, *unembed;
+  const void *sel_prev = nullptr, *sel_next = nullptr;  // DFlash2's selector tables
+  bool dflash2 = false;
   std::vector<LayerW> layers;
   int qkv_rows = 0;   // (Hq + 2 Hkv) d
   int qkv_cols = 0;   // qkv_rows (+ Hq for the gate)
@@ -168,7 +171,7 @@ struct dflash_model {
   size_t ev_used = 0;
   // workspace
   Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart, vbonus, cutbuf,
-      vpen, vpen_tab;
+      vpen, vpen_tab, d2part, d2cand;
   HostRing ring;
 };
 
@@ -196,6 +199,8 @@ struct dflash_session {
   int device = 0;               // the CUDA device that was current at dflash_open
   Penalty pen{1.f, 0.f, 0.f, 0, nullptr};  // the sampler's penalties (hist: the session's copy)
   int32_t* d_hist = nullptr;    // [kMaxPenaltyHistory] committed history for the penalties
+  int32_t* pcand_ids = nullptr;  // DFlash2: [n][sel_candidates] candidates of the last proposal
+  float* pcand_probs = nullptr;  // DFlash2: their probabilities (one-hot on the token at T = 0)
 };
 
 namespace {
@@ -251,6 +256,15 @@ int check_config(const dflash_config& c) {
   if (c.causal_block != 0 && c.causal_block != 1) return fail(DFLASH_ERR_INVALID_ARG, "causal_block must be 0 or 1");
   if (c.gated_attention != 0 && c.gated_attention != 1) return fail(DFLASH_ERR_INVALID_ARG, "gated_attention must be 0 or 1");
   if (!(c.rope_theta > 1.f) || !(c.rms_eps >= 0.f)) return fail(DFLASH_ERR_INVALID_ARG, "rope_theta / rms_eps");
+  if (c.variant != DFLASH_VARIANT_DFLASH && c.variant != DFLASH_VARIANT_DFLASH2)
+    return fail(DFLASH_ERR_INVALID_ARG, "variant %d", c.variant);
+  if (c.variant == DFLASH_VARIANT_DFLASH2) {
+    if (c.conv_taps < 1 || c.conv_taps > kMaxConvTaps) return fail(DFLASH_ERR_SHAPE, "conv_taps %d outside 1..%d", c.conv_taps, kMaxConvTaps);
+    if (c.sel_rank < 1 || c.sel_rank > 256) return fail(DFLASH_ERR_SHAPE, "sel_rank %d outside 1..256", c.sel_rank);
+    if (c.sel_candidates < 1 || c.sel_candidates > kMaxCandidates || c.sel_candidates > c.vocab)
+      return fail(DFLASH_ERR_SHAPE, "sel_candidates %d outside 1..%d (and at most vocab)", c.sel_candidates, kMaxCandidates);
+    if (c.hidden % c.n_q_heads) return fail(DFLASH_ERR_SHAPE, "hidden %d not a multiple of n_q_heads", c.hidden);
+  }
   if (c.dtype == DFLASH_DTYPE_BF16) {
     const int w[] = {c.target_hidden, c.hidden, c.intermediate, c.n_q_heads * c.head_dim};
     for (int x : w)
@@ -598,6 +612,17 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     }
     ST_TRY(launch_check("attention"));
     ST_TRY(gemm_resid(m, m->O.p, qd, w.w_o, m->h.p, m->tmp.as<float>(), Mb, H, qd, st));
+    if (m->dflash2) {
+      // DFlash2's block-local dynamic convolution: x = RMSNorm(h; conv_norm)
+      // (into y, free until the post-norm below), the kernel logits W_dc x
+      // (into tmp), then h_i += sum_j softmax(...)_j x_{i-j} within the block
+      const int GK = Hq * c.conv_taps;
+      launch_rmsnorm(m->dt, false, m->h.p, Mb, nullptr, H, w.conv_norm, m->y.p, H, Mb, H, Mb, 0, 0, c.rms_eps, st);
+      ST_TRY(gemm(m, m->y.p, H, w.w_dc, H, m->tmp.as<float>(), GK, Mb, GK, H, st));
+      launch_dynconv(m->dt, m->h.p, m->y.p, m->tmp.as<float>(), Mb, nrows, H, Hq, c.conv_taps, st);
+      m->launches += 2;
+      ST_TRY(launch_check("dynamic convolution"));
+    }
     launch_rmsnorm(m->dt, false, m->h.p, Mb, nullptr, H, w.post_norm, m->y.p, H, Mb, H, Mb, 0, 0, c.rms_eps, st);
     m->launches++;
     ST_TRY(gemm_swiglu(m, m->y.p, w.w_gate, w.w_up, m->a.p, m->tmp.as<float>(), Mb, I, H, st));
@@ -625,12 +650,78 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   } else {
     ST_TRY(gemm(m, m->z.p, H, m->unembed, H, lg, V, Rz, V, H, st));
   }
-  if (o_pen) {
-    // every row of a session's block gets the same committed-history penalties
+  // the sessions' rows of logits, and the copies that finish a draw: the
+  // logits block of a CUDA-core batch into each session, and out_logits
+  auto session_rows = [&]() {
     std::vector<float*> rows(Bc);
     for (int j = 0; j < Bc; ++j) rows[j] = (seg || Bc == 1) ? fw.sess[j]->plogits : lg + (size_t)j * n * V;
+    return rows;
+  };
+  auto finish_copies = [&]() -> int {
+    for (int j = 0; j < Bc; ++j) {
+      dflash_session* s = fw.sess[j];
+      if (Bc > 1 && !seg)
+        CU_TRY(cudaMemcpyAsync(s->plogits, lg + (size_t)j * n * V, (size_t)n * V * 4, cudaMemcpyDeviceToDevice, st));
+      if (fw.out_logits)
+        CU_TRY(cudaMemcpyAsync(fw.out_logits + (size_t)fw.sess_map[j] * n * V, s->plogits, (size_t)n * V * 4,
+                               cudaMemcpyDeviceToDevice, st));
+    }
+    return DFLASH_OK;
+  };
+  if (m->dflash2) {
+    // DFlash2's selector (dflash.go selectBlock, the BlockSelector branch):
+    // the candidates of every row, then each session's positions in order,
+    // at the request temperature only (no truncation, no penalties)
+    const int kc = c.sel_candidates, nch = topk_chunks(V);
+    std::vector<int32_t*> sid(Bc);
+    std::vector<float*> spr(Bc);
+    for (int j = 0; j < Bc; ++j) {
+      sid[j] = fw.sess[j]->pcand_ids;
+      spr[j] = fw.sess[j]->pcand_probs;
+    }
     TablePack pk;
-    const size_t o_p = pk.add(pen_tab), o_r = pk.add(rows);
+    const size_t o_r = pk.add(session_rows()), o_i = pk.add(sid), o_p = pk.add(spr);
+    ST_TRY(m->ring.upload(pk, m->vpen_tab, st));
+    char* pb = m->vpen_tab.as<char>();
+    ST_TRY(m->d2part.ensure((size_t)Rz * nch * kc * sizeof(uint64_t), st));
+    ST_TRY(m->d2cand.ensure((size_t)Rz * kc * 8, st));
+    int32_t* cid = m->d2cand.as<int32_t>();
+    float* clg = reinterpret_cast<float*>(cid + (size_t)Rz * kc);
+    {
+      Timed tm(m, kSample, (double)Rz * V * 4, 2.0 * Rz * V, st);
+      launch_topk_candidates((const float* const*)(pb + o_r), n, V, V, kc, Rz, m->d2part.as<uint64_t>(), cid, clg, st);
+      SelectArgs sel{};
+      sel.B = Bc;
+      sel.n = n;
+      sel.kc = kc;
+      sel.rank = c.sel_rank;
+      sel.V = V;
+      sel.temperature = fw.temperature;
+      sel.seed = fw.seed;
+      sel.rnd = (uint32_t)fw.rnd;
+      sel.current = fw.current;
+      sel.sess_map = (const int32_t*)(tb + o_map);
+      sel.seq_ids = tabs.seq;
+      sel.sel_prev = m->sel_prev;
+      sel.sel_next = m->sel_next;
+      sel.cand_ids = cid;
+      sel.cand_logit = clg;
+      sel.sess_tok = (int32_t* const*)(tb + o_ptok);
+      sel.sess_ids = (int32_t* const*)(pb + o_i);
+      sel.sess_probs = (float* const*)(pb + o_p);
+      sel.out_tokens = fw.out_tokens;
+      sel.out_q = fw.out_q;
+      sel.err = m->d_err;
+      launch_select(m->dt, sel, st);
+      m->launches += 4;
+    }
+    ST_TRY(launch_check("selector"));
+    return finish_copies();
+  }
+  if (o_pen) {
+    // every row of a session's block gets the same committed-history penalties
+    TablePack pk;
+    const size_t o_p = pk.add(pen_tab), o_r = pk.add(session_rows());
     ST_TRY(m->ring.upload(pk, m->vpen_tab, st));
     char* pb = m->vpen_tab.as<char>();
     launch_penalize_rows((const Penalty*)(pb + o_p), (float* const*)(pb + o_r), n, V, V, Bc, st);
@@ -673,15 +764,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     m->launches += 2;
   }
   ST_TRY(launch_check("sample"));
-  for (int j = 0; j < Bc; ++j) {
-    dflash_session* s = fw.sess[j];
-    if (Bc > 1 && !seg)
-      CU_TRY(cudaMemcpyAsync(s->plogits, lg + (size_t)j * n * V, (size_t)n * V * 4, cudaMemcpyDeviceToDevice, st));
-    if (fw.out_logits)
-      CU_TRY(cudaMemcpyAsync(fw.out_logits + (size_t)fw.sess_map[j] * n * V, s->plogits, (size_t)n * V * 4,
-                             cudaMemcpyDeviceToDevice, st));
-  }
-  return DFLASH_OK;
+  return finish_copies();
 }
 
 // Context rows of one session's held features (and optionally extra rows
@@ -784,7 +867,7 @@ void dflash__verify_timing_end(const void* model, long long idx, void* stream) {
 void dflash__count_launches(const void* model, int n) { ((dflash_model*)model)->launches += n; }
 
 const char* dflash_last_error(void) { return g_err.c_str(); }
-int dflash_version(void) { return 100; }
+int dflash_version(void) { return 200; }
 
 int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflash_model** out) {
   if (!cfg || !w || !out) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
@@ -798,10 +881,19 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
         !lw.w_down)
       return fail(DFLASH_ERR_INVALID_ARG, "null weight in layer %d", l);
     if (c.gated_attention && !lw.w_g) return fail(DFLASH_ERR_SHAPE, "layer %d: gated attention without g_proj", l);
+    if (c.variant == DFLASH_VARIANT_DFLASH2 && (!lw.conv_norm || !lw.w_dc))
+      return fail(DFLASH_ERR_INVALID_ARG, "layer %d: DFlash2 without conv_norm / w_dc", l);
     if (!c.gated_attention && lw.w_g) return fail(DFLASH_ERR_SHAPE, "layer %d: g_proj given but gating is off", l);
   }
+  if (c.variant == DFLASH_VARIANT_DFLASH2 && (!w->sel_prev || !w->sel_next))
+    return fail(DFLASH_ERR_INVALID_ARG, "DFlash2 without the selector tables");
   dflash_model* m = new dflash_model();
   m->cfg = c;
+  m->dflash2 = c.variant == DFLASH_VARIANT_DFLASH2;
+  if (m->dflash2) {
+    m->sel_prev = w->sel_prev;
+    m->sel_next = w->sel_next;
+  }
   m->dt = c.dtype == DFLASH_DTYPE_BF16 ? DT::BF16 : DT::F32;
   m->esz = dt_size(m->dt);
   m->aux_norms = w->aux_norms;
@@ -826,7 +918,7 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
     const dflash_layer_weights& lw = w->layers[l];
     LayerW& L = m->layers[l];
     L = LayerW{lw.in_norm, lw.w_qkv, lw.q_norm, lw.k_norm, lw.w_g, lw.w_o, lw.post_norm, lw.w_gate, lw.w_up, lw.w_down,
-               nullptr};
+               nullptr, m->dflash2 ? lw.conv_norm : nullptr, m->dflash2 ? lw.w_dc : nullptr};
     if (c.gated_attention) {
       // one product for q | k | v | gate: a packed copy of the two matrices
       const size_t a = (size_t)m->qkv_rows * c.hidden * m->esz, g = (size_t)c.n_q_heads * c.hidden * m->esz;
@@ -859,7 +951,7 @@ int dflash_model_destroy(dflash_model* m) {
     if (L.w_qkvg) cudaFree(L.w_qkvg);
   Buf* bufs[] = {&m->tables, &m->u, &m->fcout, &m->c, &m->h, &m->x, &m->qkv, &m->rope, &m->Q, &m->G,
                  &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart, &m->cutbuf,
-                 &m->vbonus, &m->vpen, &m->vpen_tab};
+                 &m->vbonus, &m->vpen, &m->vpen_tab, &m->d2part, &m->d2cand};
   for (Buf* b : bufs) b->release();
   m->ring.release();
   for (auto& e : m->ev_pool) {
@@ -919,6 +1011,8 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->ptok, nb * 4);
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->pcut, nb * 8);
   if (e == cudaSuccess) e = cudaMalloc((void**)&s->d_accepted, 8);
+  if (e == cudaSuccess && m->dflash2) e = cudaMalloc((void**)&s->pcand_ids, nb * c.sel_candidates * 4);
+  if (e == cudaSuccess && m->dflash2) e = cudaMalloc((void**)&s->pcand_probs, nb * c.sel_candidates * 4);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->d_accepted, 0, 8, s->stream);
   if (e == cudaSuccess && m->use_tc && c.head_dim == 128) {
     CUtensorMap maps[2];
@@ -938,6 +1032,8 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
     cudaFree(s->pcut);
     cudaFree(s->d_accepted);
     cudaFree(s->d_maps);
+    cudaFree(s->pcand_ids);
+    cudaFree(s->pcand_probs);
     delete s;
     return fail(e == cudaErrorMemoryAllocation ? DFLASH_ERR_OOM : DFLASH_ERR_CUDA, "session buffers: %s",
                 cudaGetErrorString(e));
@@ -1129,9 +1225,11 @@ int dflash_propose(dflash_session* const* s, int32_t batch, const int32_t* curre
   if (!out_n) return fail(DFLASH_ERR_INVALID_ARG, "out_n is null");
   if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(DFLASH_ERR_INVALID_ARG, "temperature");
   dflash_model* m = s[0]->m;
-  const int n = std::min<int>(max_tokens, m->cfg.block_size - 1);
+  int n = std::min<int>(max_tokens, m->cfg.block_size - 1);
   for (int b = 0; b < batch; ++b) out_n[b] = 0;
   if (n <= 0) return DFLASH_OK;
+  // dflash.go dflash2Depth: a DFlash2 session drafts seven tokens every round
+  if (m->dflash2) n = std::min<int>(kDflash2Depth, m->cfg.block_size - 1);
   if (!current || !out_tokens || !out_q) return fail(DFLASH_ERR_INVALID_ARG, "null current / out_tokens / out_q");
   Forward fw;
   fw.n = n;
@@ -1228,6 +1326,18 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
                o_seq = tp.add(seqv);
   const size_t o_trunc = any_trunc ? tp.add(trv) : 0, o_dcut = any_dcut ? tp.add(dcut) : 0;
   const size_t o_pen = any_pen ? tp.add(penv) : 0;
+  // DFlash2: q of each position is its candidate distribution
+  size_t o_cid = 0, o_cpr = 0;
+  if (m->dflash2) {
+    std::vector<const int32_t*> cid(batch);
+    std::vector<const float*> cpr(batch);
+    for (int b = 0; b < batch; ++b) {
+      cid[b] = s[b]->pcand_ids;
+      cpr[b] = s[b]->pcand_probs;
+    }
+    o_cid = tp.add(cid);
+    o_cpr = tp.add(cpr);
+  }
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
   const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
@@ -1290,12 +1400,34 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   va.err = m->d_err;
   va.cut_t = sa.cut;
   va.dcut = any_dcut ? (const uint64_t* const*)(tb + o_dcut) : nullptr;
+  if (m->dflash2) {
+    va.cand_ids = (const int32_t* const*)(tb + o_cid);
+    va.cand_probs = (const float* const*)(tb + o_cpr);
+    va.ncand = m->cfg.sel_candidates;
+  }
   const int bchunks = verify_bonus_chunks(V);
   ST_TRY(m->vbonus.ensure((size_t)batch * bchunks * sizeof(VerifyPart) + (size_t)batch * 4, st));
   va.rej = (int32_t*)(m->vbonus.as<char>() + (size_t)batch * bchunks * sizeof(VerifyPart));
   launch_verify_accept(va, m->vbonus.as<VerifyPart>(), st);
   m->launches += temperature > 0.f ? 2 : 1;  // bonus draw (T > 0) and finish
   return launch_check("verify");
+}
+
+int dflash_candidates(const dflash_session* s, int32_t* out_ids, float* out_probs) {
+  if (!s || !out_ids || !out_probs) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  if (!s->m->dflash2) return fail(DFLASH_ERR_STATE, "the model is not a DFlash2 draft");
+  if (!s->has_prop) return fail(DFLASH_ERR_STATE, "no proposal yet");
+  const size_t bytes = (size_t)s->last_n * s->m->cfg.sel_candidates * 4;
+  CU_TRY(cudaMemcpyAsync(out_ids, s->pcand_ids, bytes, cudaMemcpyDeviceToDevice, s->stream));
+  CU_TRY(cudaMemcpyAsync(out_probs, s->pcand_probs, bytes, cudaMemcpyDeviceToDevice, s->stream));
+  return DFLASH_OK;
+}
+
+int dflash__session_candidates(const dflash_session* s, const int32_t** ids, const float** probs, int32_t* kc) {
+  *ids = s->m->dflash2 ? s->pcand_ids : nullptr;
+  *probs = s->m->dflash2 ? s->pcand_probs : nullptr;
+  *kc = s->m->dflash2 ? s->m->cfg.sel_candidates : 0;
+  return DFLASH_OK;
 }
 
 int dflash_set_penalties(dflash_session* s, float repeat_penalty, float presence_penalty, float frequency_penalty,
@@ -1338,6 +1470,8 @@ int dflash_close(dflash_session* s) {
   cudaFree(s->d_accepted);
   cudaFree(s->d_maps);
   cudaFree(s->d_hist);
+  cudaFree(s->pcand_ids);
+  cudaFree(s->pcand_probs);
   delete s;
   return rc;
 }

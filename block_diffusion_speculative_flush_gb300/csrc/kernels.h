@@ -163,6 +163,11 @@ struct VerifyArgs {
   // each session's proposal rows (dcut[b] NULL: that proposal was not truncated)
   const uint64_t* cut_t;        // [B][n+1]
   const uint64_t* const* dcut;  // [B] -> [n]
+  // DFlash2 proposals (NULL, or cand_ids[b] NULL: q from the draft logits):
+  // q_i is the candidate distribution of position i, ncand ids and probabilities
+  const int32_t* const* cand_ids;   // [B] -> [n][ncand]
+  const float* const* cand_probs;   // [B] -> [n][ncand]
+  int ncand;
 };
 // Bonus-draw partial of one vocabulary chunk of one session.
 struct VerifyPart {
@@ -199,6 +204,42 @@ void launch_penalize_rows(const Penalty* pen, float* const* rows, int rows_per_s
 // tokens draft[b][0..r).  One CTA per row.
 void launch_penalize_target(const Penalty* pen, const void* target, int in_bf16, float* out, const int32_t* draft,
                             int B, int n, int V, cudaStream_t st);
+
+// --- DFlash2 ---------------------------------------------------------------
+constexpr int kMaxConvTaps = 8;
+constexpr int kMaxCandidates = 32;
+constexpr int kDflash2Depth = 7;  // dflash.go dflash2Depth: a DFlash2 session's fixed draft length
+// h[row] += sum over taps j <= row % nrows of softmax_j(a[row][g][.]) * x[row - j],
+// channel c in group g = c / (H / G); a: [rows][G * taps] fp32, x: the
+// normalised rows in the storage type.  One CTA per row.
+void launch_dynconv(DT dt, void* h, const void* x, const float* a, int rows, int nrows, int H, int G, int taps,
+                    cudaStream_t st);
+// The kc largest logits of each of n_rows rows (row r: rows[r / rows_per_seq]
+// + (r % rows_per_seq) * ld) in the sampler's order: ids and logits
+// [n_rows][kc]; part holds n_rows * topk_chunks(V) * kc keys.
+int topk_chunks(int V);
+void launch_topk_candidates(const float* const* rows, int rows_per_seq, int64_t ld, int V, int kc, int n_rows,
+                            uint64_t* part, int32_t* ids, float* logit, cudaStream_t st);
+struct SelectArgs {
+  int B, n, kc, rank, V;
+  float temperature;
+  uint64_t seed;
+  uint32_t rnd;
+  const int32_t* current;    // [caller batch] anchors
+  const int32_t* sess_map;   // [B] caller index of each session
+  const int32_t* seq_ids;    // [B]
+  const void* sel_prev;      // [V][rank] A, storage type
+  const void* sel_next;      // [V][rank] B
+  const int32_t* cand_ids;   // [B * n][kc]
+  const float* cand_logit;   // [B * n][kc]
+  int32_t* const* sess_tok;  // [B] -> [n]
+  int32_t* const* sess_ids;  // [B] -> [n][kc]
+  float* const* sess_probs;  // [B] -> [n][kc]
+  int32_t* out_tokens;       // [caller batch][n]
+  float* out_q;              // [caller batch][n]
+  int32_t* err;              // bit 1: an anchor outside [0, V)
+};
+void launch_select(DT dt, const SelectArgs& a, cudaStream_t st);
 
 // --- tensor-core path (bf16, sm_103a) --------------------------------------
 struct TcGemmPlan;  // opaque, defined in gemm_tc.cu

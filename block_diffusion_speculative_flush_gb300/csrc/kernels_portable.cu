@@ -1067,6 +1067,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_trunc_cut(SampleArgs a, const Tr
   }
 }
 
+// q of a DFlash2 proposal at position i: the candidate distribution's
+// probability of v, 0 for an id outside the candidates.
+__device__ __forceinline__ float candidate_q(const int32_t* ids, const float* probs, int kc, int i, int v) {
+  for (int c = 0; c < kc; ++c)
+    if (ids[i * kc + c] == v) return probs[i * kc + c];
+  return 0.f;
+}
+
 // Acceptance scan of one session (T > 0): the first i in 1..n whose draft
 // token fails u_i * q_i(d_i) < p_i(d_i), or 0 if all n pass.  A warp tests
 // 32 positions at once and every lane returns the answer; a draft id outside
@@ -1082,6 +1090,8 @@ __device__ int verify_scan(const VerifyArgs& a, int b) {
   const float* dlse = a.dlse[b];
   const int32_t* dtok = a.dtok[b];
   const uint64_t* dc = a.dcut ? a.dcut[b] : nullptr;
+  const int32_t* cid = a.cand_ids ? a.cand_ids[b] : nullptr;
+  const float* cpr = a.cand_probs ? a.cand_probs[b] : nullptr;
   for (int i0 = 1; i0 <= n; i0 += 32) {
     const int i = i0 + lane;
     bool fail = false, bad = false;
@@ -1094,9 +1104,14 @@ __device__ int verify_scan(const VerifyArgs& a, int b) {
       const float st = load_logit(a.target, a.in_bf16, tbase + (int64_t)(i - 1) * V + dtk) * invT;
       float p = expf(st - a.lse_t[b * (n + 1) + i - 1]);
       if (a.cut_t && order_key(st, dtk) < a.cut_t[b * (n + 1) + i - 1]) p = 0.f;
-      const float dv = dl[(int64_t)(i - 1) * V + dtk];
-      float q = Tq > 0.f ? expf(dv / Tq - dlse[i - 1]) : (dtk == dtok[i - 1] ? 1.f : 0.f);
-      if (Tq > 0.f && dc && order_key(dv * (1.f / Tq), dtk) < dc[i - 1]) q = 0.f;
+      float q;
+      if (cid && Tq > 0.f) {
+        q = candidate_q(cid, cpr, a.ncand, i - 1, dtk);
+      } else {
+        const float dv = dl[(int64_t)(i - 1) * V + dtk];
+        q = Tq > 0.f ? expf(dv / Tq - dlse[i - 1]) : (dtk == dtok[i - 1] ? 1.f : 0.f);
+        if (Tq > 0.f && dc && order_key(dv * (1.f / Tq), dtk) < dc[i - 1]) q = 0.f;
+      }
       const float r = uniform_open(rand_u32(a.seed, a.rnd, kStreamAccept, seq, (uint32_t)i, 0u));
       fail = !(r * q < p);
     }
@@ -1142,6 +1157,8 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
   const float lse = a.lse_t[b * (n + 1) + trow];
   const uint64_t cutt = a.cut_t ? a.cut_t[b * (n + 1) + trow] : 0ull;
   const uint64_t* dc = a.dcut ? a.dcut[b] : nullptr;
+  const int32_t* cid = (a.cand_ids && Tq > 0.f) ? a.cand_ids[b] : nullptr;
+  const float* cpr = a.cand_probs ? a.cand_probs[b] : nullptr;
   const float invTq = Tq > 0.f ? 1.f / Tq : 1.f;
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   float rsum = 0.f;
@@ -1159,9 +1176,14 @@ __global__ void k_verify_bonus(VerifyArgs a, int chunk, VerifyPart* __restrict__
       if (kept) bp = better(bp, ArgMax{lp + g, v});
       if (rej) {
         const float p = kept ? expf(lp) : 0.f;
-        const float dv = dl[(int64_t)(rej - 1) * V + v];
-        float q = Tq > 0.f ? expf(dv / Tq - dlse[rej - 1]) : (v == dtok[rej - 1] ? 1.f : 0.f);
-        if (Tq > 0.f && dc && order_key(dv * invTq, v) < dc[rej - 1]) q = 0.f;
+        float q;
+        if (cid) {
+          q = candidate_q(cid, cpr, a.ncand, rej - 1, v);
+        } else {
+          const float dv = dl[(int64_t)(rej - 1) * V + v];
+          q = Tq > 0.f ? expf(dv / Tq - dlse[rej - 1]) : (v == dtok[rej - 1] ? 1.f : 0.f);
+          if (Tq > 0.f && dc && order_key(dv * invTq, v) < dc[rej - 1]) q = 0.f;
+        }
         const float res = fmaxf(p - q, 0.f);
         rsum += res;
         if (res > 0.f) bres = better(bres, ArgMax{logf(res) + g, v});

@@ -32,6 +32,8 @@ extern "C" int dflash__session_proposal(const dflash_session* s, const float** l
 extern "C" int dflash__session_truncation(const dflash_session* s, Trunc* trunc, const uint64_t** proposal_cut);
 extern "C" int dflash__session_device(const dflash_session* s);
 extern "C" int dflash__session_penalties(const dflash_session* s);
+extern "C" int dflash__session_candidates(const dflash_session* s, const int32_t** ids, const float** probs,
+                                          int32_t* kc);
 extern "C" long long dflash__verify_timing_begin(const void* model, double bytes, double flops, void* stream);
 extern "C" void dflash__verify_timing_end(const void* model, long long idx, void* stream);
 extern "C" void dflash__count_launches(const void* model, int n);
@@ -112,6 +114,9 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   int32_t seq[kMaxBatch];
   Trunc trv[kMaxBatch];
   const uint64_t* dcut[kMaxBatch];
+  const int32_t* cid[kMaxBatch];
+  const float* cpr[kMaxBatch];
+  int32_t kc = 0;
   bool any_trunc = false, any_dcut = false;
   void* stream = nullptr;
   int32_t V = 0, limit = 0;
@@ -143,6 +148,7 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
       return dflash__set_error(DFLASH_ERR_INVALID_ARG,
                                "a session has penalties set: their penalised target rows need dflash_verify's workspace");
     seq[b] = b;
+    dflash__session_candidates(s[b], &cid[b], &cpr[b], &kc);
     dflash__session_truncation(s[b], &trv[b], &dcut[b]);
     any_trunc = any_trunc || (temperature > 0.f && trv[b].top_k > 0);
     any_dcut = any_dcut || (temperature > 0.f && dcut[b]);
@@ -168,6 +174,10 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   const size_t o_trunc = off;
   off = up16(off + batch * sizeof(Trunc));
   const size_t o_dcut = off;
+  off = up16(off + batch * sizeof(void*));
+  const size_t o_cid = off;
+  off = up16(off + batch * sizeof(void*));
+  const size_t o_cpr = off;
   off = up16(off + batch * sizeof(void*));
   const size_t tables_end = off;
   const size_t o_cut = off;
@@ -203,7 +213,7 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   // tables: staged on the stack, then written by a one-CTA kernel that takes
   // them as its parameter, in stream order (no host-to-device copy, so the
   // call never waits for the stream; the block is at most ~8 KB)
-  alignas(16) char host[up16(kMaxBatch * sizeof(void*)) * 5 + up16(kMaxBatch * sizeof(float)) +
+  alignas(16) char host[up16(kMaxBatch * sizeof(void*)) * 7 + up16(kMaxBatch * sizeof(float)) +
                         up16(kMaxBatch * sizeof(int32_t)) + up16(kMaxBatch * sizeof(Trunc))];
   static_assert(sizeof(host) <= (size_t)kTableParamMax, "verify tables exceed a kernel parameter block");
   memcpy(host + o_dl, dl, batch * sizeof(void*));
@@ -214,6 +224,8 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   memcpy(host + o_seq, seq, batch * sizeof(int32_t));
   memcpy(host + o_trunc, trv, batch * sizeof(Trunc));
   memcpy(host + o_dcut, dcut, batch * sizeof(void*));
+  memcpy(host + o_cid, cid, batch * sizeof(void*));
+  memcpy(host + o_cpr, cpr, batch * sizeof(void*));
   const double tbytes = (double)rows * V * (logits_dtype == DFLASH_DTYPE_BF16 ? 2 : 4) + (double)batch * V * 4;
   const long long timed = dflash__verify_timing_begin(model, tbytes, 4.0 * rows * V, stream);
   if (launch_table_write(base, host, tables_end, st)) {
@@ -268,6 +280,11 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
   va.rej = (int32_t*)(base + o_rej);
   va.cut_t = sa.cut;
   va.dcut = any_dcut ? (const uint64_t* const*)(base + o_dcut) : nullptr;
+  if (kc > 0) {
+    va.cand_ids = (const int32_t* const*)(base + o_cid);
+    va.cand_probs = (const float* const*)(base + o_cpr);
+    va.ncand = kc;
+  }
   launch_verify_accept(va, (VerifyPart*)(base + o_bonus), st);
   dflash__verify_timing_end(model, timed, stream);
   dflash__count_launches(model, 3 + (any_trunc ? 1 : 0) + (temperature > 0.f ? 2 : 1));

@@ -98,7 +98,21 @@ typedef struct dflash_config {
   uint32_t flags;          /* DFLASH_FLAG_* */
   float rope_theta;        /* RoPE base (rotate-half pairs j, j + d/2) */
   float rms_eps;           /* RMSNorm epsilon */
+  /* DFlash2 (ollama dflash.go, the DFlash2 commit note): block-local dynamic
+   * convolutions and a candidate selector.  variant DFLASH_VARIANT_DFLASH (0)
+   * ignores the three fields after it.  For DFLASH_VARIANT_DFLASH2:
+   * conv_taps in 1..8 (the convolution's width), sel_rank in 1..256 (the
+   * selector tables' rank), sel_candidates in 1..32 (candidates per
+   * position, at most vocab); the pages give none of the three. */
+  int32_t variant;
+  int32_t conv_taps;
+  int32_t sel_rank;
+  int32_t sel_candidates;
 } dflash_config;
+
+#define DFLASH_VARIANT_DFLASH 0
+#define DFLASH_VARIANT_DFLASH2 1
+#define DFLASH2_DEPTH 7 /* dflash.go dflash2Depth: a DFlash2 proposal's fixed length */
 
 /* Per-layer weights, device pointers in the storage type.  Borrowed: they
  * must stay valid until dflash_model_destroy. */
@@ -113,6 +127,13 @@ typedef struct dflash_layer_weights {
   const void* w_gate;    /* [I, H] */
   const void* w_up;      /* [I, H] */
   const void* w_down;    /* [H, I] */
+  /* DFlash2 only (NULL otherwise): the layer's dynamic convolution, after the
+   * attention residual.  x = RMSNorm(h; conv_norm); row i of the block adds
+   * sum_j w_ij * x_{i-j} over j < conv_taps (rows before the anchor's count
+   * as zero), w_i = softmax over the taps of (w_dc x_i) taken per channel
+   * group, one group of H / Hq channels per query head. */
+  const void* conv_norm; /* [H] */
+  const void* w_dc;      /* [Hq conv_taps, H]: row g * conv_taps + j is tap j of group g */
 } dflash_layer_weights;
 
 typedef struct dflash_weights {
@@ -123,6 +144,12 @@ typedef struct dflash_weights {
   const void* embed;       /* [V, H] token embeddings of the block */
   const void* unembed;     /* [V, H] */
   const dflash_layer_weights* layers; /* (host) array of n_layers */
+  /* DFlash2 only (NULL otherwise): the selector's tables.  The candidates of
+   * position i are the sel_candidates largest logits of block row i (value
+   * descending, then id), scored logit + <sel_prev[prev], sel_next[c]> with
+   * prev the token chosen at position i - 1 (the anchor for the first). */
+  const void* sel_prev;  /* [V, sel_rank] */
+  const void* sel_next;  /* [V, sel_rank] */
 } dflash_weights;
 
 typedef struct dflash_counters {
@@ -214,7 +241,16 @@ DFLASH_API int dflash_settle(dflash_session* s);
  * path (committed, flush, propose) runs this first. */
 DFLASH_API int dflash_commit_block(dflash_session* const* s /*host [batch]*/, int32_t batch);
 
-/* dflash.go propose + selectBlock, batched.  n = min(max_tokens, B_s - 1).
+/* dflash.go propose + selectBlock, batched.  n = min(max_tokens, B_s - 1);
+ * a DFlash2 model drafts n = min(DFLASH2_DEPTH, B_s - 1) whenever
+ * max_tokens > 0 (dflash2Depth replaces the depth controller's pick), so the
+ * outputs must hold that many rows, and draws them with its candidate
+ * selector at the request temperature only (no truncation, no penalties):
+ * position i's token comes from the sel_candidates largest logits of row i,
+ * scored logit + <sel_prev[prev], sel_next[c]>, by Gumbel-max at T > 0
+ * (stream 0, keyed by the candidate's id) or argmax at T = 0, and the
+ * position's candidate distribution softmax(score / T) is kept for verify
+ * (dflash_candidates reads it).
  * A session gets out_n[b] = 0 (the pages' nil) when n <= 0 or it has no
  * context yet (F + P == 0); the others draft n tokens:
  *   commitBlock; the held rows become context (written first, at slots
@@ -267,6 +303,15 @@ DFLASH_API int dflash_set_sampler(dflash_session* s, int32_t top_k, float top_p,
  * a non-finite penalty, n_history outside [0, 4096], a null history).
  * Sessions with penalties on are verified by dflash_verify only:
  * dflash_verify_noalloc refuses them (INVALID_ARG). */
+/* A DFlash2 session's candidate distributions from its last proposal (the
+ * DFlash2 commit note: the selector returns each position's candidate
+ * distribution, which verification uses): out_ids [n, sel_candidates] int32
+ * and out_probs [n, sel_candidates] fp32, device, in candidate order (logit
+ * descending, then id); at T = 0 the probabilities are one-hot on the token.
+ * Copied in stream order.  Errors: STATE if the model is not DFlash2 or the
+ * session has no proposal. */
+DFLASH_API int dflash_candidates(const dflash_session* s, int32_t* out_ids, float* out_probs);
+
 DFLASH_API int dflash_set_penalties(dflash_session* s, float repeat_penalty, float presence_penalty,
                                     float frequency_penalty, const int32_t* history /*device [n_history]*/,
                                     int32_t n_history);
@@ -281,7 +326,9 @@ DFLASH_API int dflash_set_penalties(dflash_session* s, float repeat_penalty, flo
  * if that is all zero), after n acceptances from p of row n (stream 2).
  * q_i is the proposal's distribution softmax(l_i / T_propose) (one-hot of
  * the proposed token if that proposal was greedy); with a truncating sampler
- * (dflash_set_sampler) p and q are the truncated distributions.
+ * (dflash_set_sampler) p and q are the truncated distributions; for a
+ * DFlash2 proposal q_i is position i's candidate distribution (zero outside
+ * the candidates).
  * Outputs: out_accept [batch] int32 in 0..n, out_bonus [batch] int32.
  * Errors: STATE if a session has no proposal with this n. */
 DFLASH_API int dflash_verify(dflash_session* const* s /*host [batch]*/, int32_t batch, const void* target_logits,

@@ -175,7 +175,7 @@ def check_tokens_for(cfg, gpu_tok, gpu_logits, ora_logits, T, seed, rnd, seq):
 
 
 def verify_parity(gpu_ab, target_logits, draft_tokens, draft_logits, proposed, draft_T, T, seed, rnd, seq,
-                  trunc=None, draft_trunc=None, penalties=None):
+                  trunc=None, draft_trunc=None, penalties=None, draft_cands=None):
     """dflash_verify's (accept, bonus) against the oracle's verify on the same
     inputs: the target logits and the draft logits that the GPU session keeps
     from its proposal (copied back).  A result may differ only where the
@@ -186,17 +186,18 @@ def verify_parity(gpu_ab, target_logits, draft_tokens, draft_logits, proposed, d
     Returns True when the pair was compared, False when exempted."""
     tl = np.asarray(target_logits, dtype=np.float64)
     dl = np.asarray(draft_logits, dtype=np.float64)
-    a_ref, b_ref = O.verify(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc, penalties)
+    a_ref, b_ref = O.verify(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc, penalties,
+                            draft_cands)
     if O.penalties_active(penalties):
         tl = np.stack([O.penalized(tl[r], penalties, draft_tokens[:r]) for r in range(len(tl))])
     if tuple(int(x) for x in gpu_ab) == (a_ref, b_ref):
         return True
-    assert _verify_near(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc), \
+    assert _verify_near(tl, draft_tokens, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc, draft_cands), \
         (tuple(int(x) for x in gpu_ab), (a_ref, b_ref))
     return False
 
 
-def _verify_near(tl, d, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc):
+def _verify_near(tl, d, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_trunc, draft_cands=None):
     """True when some decision of this verify lies within rounding of its threshold."""
     n, V = len(d), tl.shape[1]
     if T == 0:
@@ -206,7 +207,8 @@ def _verify_near(tl, d, dl, proposed, draft_T, T, seed, rnd, seq, trunc, draft_t
         return False
     for i in range(1, n + 1):
         p = O.sampler_distribution(tl[i - 1], T, trunc)
-        q = O.proposal_distribution(dl[i - 1], draft_T, proposed[i - 1], draft_trunc)
+        q = O.proposal_distribution(dl[i - 1], draft_T, proposed[i - 1], draft_trunc,
+                                    None if draft_cands is None else (draft_cands[0][i - 1], draft_cands[1][i - 1]))
         r = O.uniform_open(O.random_u32(seed, rnd, O.STREAM_ACCEPT, seq, i, 0))
         x, y = r * q[int(d[i - 1])], p[int(d[i - 1])]
         if abs(x - y) <= ACCEPT_RTOL * max(abs(y), 1e-300):

@@ -37,7 +37,7 @@ def test_every_header_symbol_is_exported(lib):
 
 
 def test_version_and_error_string(lib):
-    assert lib.dflash_version() == 100
+    assert lib.dflash_version() == 200
     assert isinstance(lib.dflash_last_error(), bytes)
 
 
