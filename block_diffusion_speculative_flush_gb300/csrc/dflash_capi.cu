@@ -155,10 +155,16 @@ struct dflash_model {
   const void *aux_norms, *w_fc, *hidden_norm, *final_norm, *embed, *unembed;
   const void *sel_prev = nullptr, *sel_next = nullptr;  // DFlash2's selector tables
   bool dflash2 = false;
+  // context-only forwards of many rows: every layer's K/V rows of the fused
+  // projection packed into one matrix [L][2 Hkv d][H] (owned), and device
+  // tables of the layers' input-norm and k-norm gains [2][L]
+  void* w_kv = nullptr;
+  const void** d_gains = nullptr;
   std::vector<LayerW> layers;
   int qkv_rows = 0;   // (Hq + 2 Hkv) d
   int qkv_cols = 0;   // qkv_rows (+ Hq for the gate)
   int num_sms = 0;
+  int64_t rope_len = 0;  // positions the RoPE table (rope) holds
   bool use_tc = false;
   int32_t* d_err = nullptr;
   TcContext* tc = nullptr;
@@ -171,7 +177,7 @@ struct dflash_model {
   size_t ev_used = 0;
   // workspace
   Buf tables, u, fcout, c, h, x, qkv, rope, Q, G, O, tmp, y, a, z, logits, spart, apart, vstat, vpart, vbonus, cutbuf,
-      vpen, vpen_tab, d2part, d2cand;
+      vpen, vpen_tab, d2part, d2cand, xall, kvall;
   HostRing ring;
 };
 
@@ -317,7 +323,8 @@ int gemm_resid(dflash_model* m, const void* X, int64_t ldx, const void* W, void*
   const double bytes = (double)N * K * 2 + (double)M * K * 2 + (double)M * N * 4;
   Timed tm(m, kGemmTc, bytes, 2.0 * M * N * K, st);
   m->launches++;
-  if (tc_gemm(m->tc, X, ldx, W, nullptr, K, h, N, M, N, K, kResidBf16, st))
+  // tmp ([M][N] fp32, idle on this path) carries the split sums of many-row calls
+  if (tc_gemm(m->tc, X, ldx, W, nullptr, K, h, N, M, N, K, kResidBf16, st, nullptr, 0, tmp))
     return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
   return DFLASH_OK;
 }
@@ -504,19 +511,17 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
                o_front = tp.add(front), o_seq = tp.add(seqv), o_items = tp.add(items), o_ifirst = tp.add(ifirst),
                o_icount = tp.add(icount), o_map = tp.add(fw.sess_map), o_maps = tp.add(mapv);
-  // RoPE cos/sin per row: formed here in double (angle pos * theta^(-2j/d))
-  // when the rows fit the parameter table, else by k_rope_table on the device
-  const size_t rope_bytes = (size_t)M * (d / 2) * sizeof(float2);
-  const bool host_rope = tp.host.size() + rope_bytes + 64 <= (size_t)kTableParamMax;
-  size_t o_rope = 0;
-  if (host_rope) {
-    std::vector<float2> rt((size_t)M * (d / 2));
-    for (int r = 0; r < M; ++r)
-      for (int j = 0; j < d / 2; ++j) {
-        const double ang = (double)meta[r].pos * std::pow((double)c.rope_theta, -2.0 * j / (double)d);
-        rt[(size_t)r * (d / 2) + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
-      }
-    o_rope = tp.add(rt);
+  // RoPE cos/sin: the model's table indexed by position (angle pos *
+  // theta^(-2j/d) in double), extended when a call reaches past it; it grows
+  // geometrically, so a steady stream of rounds computes no trigonometry
+  int64_t maxpos = 0;
+  for (int r = 0; r < M; ++r) maxpos = std::max<int64_t>(maxpos, meta[r].pos + 1);
+  if (maxpos > m->rope_len) {
+    const int64_t want = std::max<int64_t>({maxpos, 2 * m->rope_len, 4096});
+    ST_TRY(m->rope.ensure((size_t)want * (d / 2) * sizeof(float2), st));
+    launch_rope_table(nullptr, 0, (int)want, d, c.rope_theta, m->rope.as<float2>(), st);
+    m->launches++;
+    m->rope_len = want;
   }
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
@@ -527,7 +532,6 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   // ---- buffers -----------------------------------------------------------
   ST_TRY(m->x.ensure((size_t)M * H * es, st));
   ST_TRY(m->qkv.ensure((size_t)M * m->qkv_cols * 4, st));
-  ST_TRY(m->rope.ensure((size_t)M * (d / 2) * sizeof(float2), st));
   if (Mc) {
     ST_TRY(m->u.ensure((size_t)Mc * KHt * es, st));
     ST_TRY(m->fcout.ensure((size_t)Mc * H * 4, st));
@@ -559,12 +563,31 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
                  m->d_err, st);
     m->launches++;
   }
-  const float2* rope = host_rope ? (const float2*)(tb + o_rope) : m->rope.as<float2>();
-  if (!host_rope) {
-    launch_rope_table(dmeta, M, d, c.rope_theta, m->rope.as<float2>(), st);
-    m->launches++;
-  }
+  const float2* rope = m->rope.as<float2>();
   ST_TRY(launch_check("context path"));
+  const int qd = Hq * d, kd = Hkv * d;
+  const void* const* d_in_gains = m->d_gains;
+  const void* const* d_k_gains = m->d_gains + c.n_layers;
+  if (!block && m->use_tc && M > 128) {
+    // many context rows: every layer's input norm in one launch, every
+    // layer's K/V product as one grouped product (each layer's sums as its
+    // own call would make them), every layer's cache write in one launch
+    const int L = c.n_layers;
+    ST_TRY(m->xall.ensure((size_t)L * M * H * es, st));
+    ST_TRY(m->kvall.ensure((size_t)L * M * 2 * kd * 4, st));
+    launch_rmsnorm_layers(m->dt, m->c.p, H, d_in_gains, m->xall.p, H, (int64_t)M * H, M, L, H, c.rms_eps, st);
+    {
+      const double bytes = (double)L * (2.0 * kd * H * es + (double)M * H * es + (double)M * 2 * kd * 4);
+      Timed tm(m, kGemmTc, bytes, 2.0 * L * M * 2 * kd * H, st);
+      if (tc_gemm_grouped(m->tc, m->xall.p, H, m->w_kv, H, m->kvall.as<float>(), 2 * kd, (int64_t)M * 2 * kd, M,
+                          2 * kd, H, L, st))
+        return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
+    }
+    launch_kv_ctx(m->dt, m->kvall.as<float>(), 2 * kd, 0, kd, (int64_t)M * 2 * kd, dmeta, M, rope, d_k_gains, Hkv, d,
+                  c.rms_eps, tabs, 0, L, st);
+    m->launches += 3;
+    return launch_check("grouped context forward");
+  }
 
   AttnParams ap{Hq, Hkv, d, nrows, c.window, c.causal_block, c.n_layers, 0, 1.f / std::sqrt((float)d)};
   double attn_bytes = 0, attn_flops = 0;  // per layer: K/V read once, Q read, O written
@@ -573,7 +596,6 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     attn_flops += 4.0 * (it.k1 - it.k0) * d * nrows * (Hq / Hkv);
   }
   attn_bytes += 2.0 * Mb * Hq * d * es;
-  const int qd = Hq * d, kd = Hkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& w = m->layers[l];
     // input_layernorm over [context rows ; block rows]
@@ -587,11 +609,18 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       const char* wkv = (const char*)w.w_qkv + (size_t)qd * H * es;
       ST_TRY(gemm(m, m->x.p, H, wkv, H, m->qkv.as<float>() + qd, m->qkv_cols, M, 2 * kd, H, st));
     }
+    if (!block) {
+      // context rows only: K and V straight into the caches, 32 rows per CTA
+      launch_kv_ctx(m->dt, m->qkv.as<float>(), m->qkv_cols, qd, qd + kd, 0, dmeta, M, rope, d_k_gains + l, Hkv, d,
+                    c.rms_eps, tabs, l, 1, st);
+      m->launches++;
+      ST_TRY(launch_check("kv"));
+      continue;
+    }
     m->launches += launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, rope, w.q_norm, w.k_norm, Hq,
                                    Hkv, d, c.gated_attention, c.rms_eps, tabs, c.n_layers, l, m->Q.p,
                                    m->G.as<float>(), st);
     ST_TRY(launch_check("qkv"));
-    if (!block) continue;
     ap.layer = l;
     {
       Timed tm(m, kAttention, attn_bytes, attn_flops, st);
@@ -940,6 +969,26 @@ int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflas
       return fail(DFLASH_ERR_CUDA, "tcgen05 setup: %s", msg.c_str());
     }
   }
+  {
+    // the gain tables, and (tensor-core path) the packed K/V weight rows
+    std::vector<const void*> gains(2 * (size_t)c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+      gains[l] = m->layers[l].in_norm;
+      gains[c.n_layers + l] = m->layers[l].k_norm;
+    }
+    e = cudaMalloc((void**)&m->d_gains, gains.size() * sizeof(void*));
+    if (e == cudaSuccess) e = cudaMemcpy(m->d_gains, gains.data(), gains.size() * sizeof(void*), cudaMemcpyHostToDevice);
+    const size_t kvb = (size_t)2 * c.n_kv_heads * c.head_dim * c.hidden * m->esz;
+    const size_t qb = (size_t)c.n_q_heads * c.head_dim * c.hidden * m->esz;
+    if (e == cudaSuccess && m->use_tc) e = cudaMalloc(&m->w_kv, kvb * c.n_layers);
+    for (int l = 0; l < c.n_layers && e == cudaSuccess && m->use_tc; ++l)
+      e = cudaMemcpy((char*)m->w_kv + kvb * l, (const char*)m->layers[l].w_qkv + qb, kvb, cudaMemcpyDeviceToDevice);
+    if (e != cudaSuccess) {
+      dflash_model_destroy(m);
+      return fail(e == cudaErrorMemoryAllocation ? DFLASH_ERR_OOM : DFLASH_ERR_CUDA, "gain tables / packed K/V: %s",
+                  cudaGetErrorString(e));
+    }
+  }
   *out = m;
   return DFLASH_OK;
 }
@@ -951,7 +1000,7 @@ int dflash_model_destroy(dflash_model* m) {
     if (L.w_qkvg) cudaFree(L.w_qkvg);
   Buf* bufs[] = {&m->tables, &m->u, &m->fcout, &m->c, &m->h, &m->x, &m->qkv, &m->rope, &m->Q, &m->G,
                  &m->O, &m->tmp, &m->y, &m->a, &m->z, &m->logits, &m->spart, &m->apart, &m->vstat, &m->vpart, &m->cutbuf,
-                 &m->vbonus, &m->vpen, &m->vpen_tab, &m->d2part, &m->d2cand};
+                 &m->vbonus, &m->vpen, &m->vpen_tab, &m->d2part, &m->d2cand, &m->xall, &m->kvall};
   for (Buf* b : bufs) b->release();
   m->ring.release();
   for (auto& e : m->ev_pool) {
@@ -959,6 +1008,8 @@ int dflash_model_destroy(dflash_model* m) {
     cudaEventDestroy(e.second);
   }
   if (m->d_err) cudaFree(m->d_err);
+  if (m->w_kv) cudaFree(m->w_kv);
+  if (m->d_gains) cudaFree(m->d_gains);
   if (m->tc) tc_destroy(m->tc);
   delete m;
   return DFLASH_OK;
@@ -1014,6 +1065,20 @@ int dflash_open(dflash_model* m, int64_t restored_offset, int64_t max_ctx, void*
   if (e == cudaSuccess && m->dflash2) e = cudaMalloc((void**)&s->pcand_ids, nb * c.sel_candidates * 4);
   if (e == cudaSuccess && m->dflash2) e = cudaMalloc((void**)&s->pcand_probs, nb * c.sel_candidates * 4);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->d_accepted, 0, 8, s->stream);
+  // the model's RoPE table covers every position this session can reach
+  // (committed rows stop at max_ctx; a block adds block_size), so no call of
+  // the session has to grow it
+  const int64_t positions = max_ctx + c.block_size;
+  if (e == cudaSuccess && positions > m->rope_len) {
+    e = cudaDeviceSynchronize();  // no call of any stream may still read the old table
+    if (e == cudaSuccess && m->rope.ensure((size_t)positions * (c.head_dim / 2) * sizeof(float2), s->stream) != DFLASH_OK)
+      e = cudaErrorMemoryAllocation;
+    if (e == cudaSuccess) {
+      launch_rope_table(nullptr, 0, (int)positions, c.head_dim, c.rope_theta, m->rope.as<float2>(), s->stream);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) m->rope_len = positions;
+  }
   if (e == cudaSuccess && m->use_tc && c.head_dim == 128) {
     CUtensorMap maps[2];
     if (tc_encode_kv_maps(m->tc, s->kv, s->cap, c.head_dim, 2 * c.n_layers * c.n_kv_heads, maps) != 0) {

@@ -25,7 +25,11 @@
 //    tensor core fills one while the epilogue warps drain the other into a
 //    running sum kept in a third TMEM region.  Consecutive tiles share a
 //    weight tile, so the CTAs running at one time read each weight tile from
-//    HBM once and find it in L2 after that.
+//    HBM once and find it in L2 after that.  Products with an fp32 output
+//    use tiles 256 activation rows wide instead (MMA N = 256): per FLOP a
+//    stage then moves a quarter fewer bytes from L2 into shared memory, and
+//    the two 256-column accumulators fill TMEM, so the running sum of the
+//    splits lives in the fp32 output itself, added in the same order.
 //
 // Roles in a 192-thread CTA: warp 0 lane 0 issues TMA loads into a
 // STAGES-deep ring, warp 1 lane 0 issues the MMAs (4 x K=16 per 64-wide
@@ -41,6 +45,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <string>
+#include <type_traits>
 
 #include "common.cuh"
 #include "gemm_tc.h"
@@ -68,6 +73,7 @@ constexpr int kMaxSplits = 4;
 constexpr int kMaxStages = 16;
 constexpr size_t kBarrierBytes = 512;
 constexpr int kPersistBN = 128;
+constexpr int kWideBN = 256;   // persistent tiles of fp32-output products
 constexpr int kErrBit = 4;
 
 struct TcParams {
@@ -81,18 +87,40 @@ struct TcParams {
   void* const* yseg;  // fp32 output only: rows [j*seg_rows, (j+1)*seg_rows) go to yseg[j] (NULL: Y)
   int seg_rows;
   int* err;
+  float* ws;          // 256-wide persistent tiles of the residual mode: [M][N] fp32 running sum of the splits
+  // grouped products (256-wide fp32 tiles only): `groups` independent
+  // products of the same shape, X stacked [groups * M][K], W stacked
+  // [groups * N][K], product g written at Y + g * y_group
+  int groups;
+  int64_t y_group;
 };
+
+// The tile a unit index names: product g, weight-row tile, activation-row tile.
+struct TileIdx {
+  int g, m_tile, n_tile;
+};
+__device__ __forceinline__ TileIdx tile_of(const TcParams& p, int t) {
+  const int per = p.m_tiles * p.n_tiles;
+  return TileIdx{t / per, (t % per) / p.n_tiles, (t % per) % p.n_tiles};
+}
 
 constexpr int stage_bytes(int BN) { return BM * BK * 2 + BN * BK * 2; }
 template <int BN, bool PERSIST>
 __host__ __device__ constexpr int tmem_cols() {
   return PERSIST ? 512 : BN < 32 ? 32 : BN;
 }
-// Dynamic shared memory: the TMA ring, then (persistent schedule only) the
-// fp32 tile staged for the store, which in the cluster schedule aliases the
-// idle ring instead; then the barriers.
-size_t smem_bytes(int BN, bool persist, int stages) {
-  return (size_t)stages * stage_bytes(BN) + (persist ? (size_t)BN * BM * 4 : 0) + 1024 + kBarrierBytes;
+// Dynamic shared memory: the TMA ring, then (128-row persistent tiles only)
+// the fp32 tile staged for the store, which in the cluster schedule aliases
+// the idle ring instead; then the barriers.
+// (256-wide SwiGLU tiles: the up half of one 32-column chunk, 64 rows with a
+// padded stride of 33 floats, for the exchange between the epilogue warps.)
+constexpr bool stages_tile(int BN, bool persist) { return persist && BN == kPersistBN; }
+constexpr size_t kSwiXchBytes = 64 * 33 * 4;
+constexpr size_t extra_bytes(int BN, bool persist, bool swi) {
+  return stages_tile(BN, persist) ? (size_t)BN * BM * 4 : (persist && swi ? kSwiXchBytes : 0);
+}
+size_t smem_bytes(int BN, bool persist, bool swi, int stages) {
+  return (size_t)stages * stage_bytes(BN) + extra_bytes(BN, persist, swi) + 1024 + kBarrierBytes;
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -121,7 +149,7 @@ __device__ __forceinline__ void split_range(const TcParams& p, int s, int& kb0, 
 // each; f returns false to stop.
 template <bool PERSIST, typename F>
 __device__ __forceinline__ void for_each_unit(const TcParams& p, F f) {
-  const int tiles = p.m_tiles * p.n_tiles;
+  const int tiles = p.m_tiles * p.n_tiles * p.groups;
   if (PERSIST) {
     for (int t = blockIdx.x; t < tiles; t += gridDim.x)
       for (int s = 0; s < p.splits; ++s)
@@ -245,13 +273,16 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
   constexpr uint32_t TX = A_BYTES + B_BYTES;
   constexpr int CH = BN < 32 ? BN : 32;
   constexpr int ROWS = SWI ? BM / 2 : BM;
-  static_assert(!PERSIST || BN == kPersistBN, "persistent tiles are 128 rows wide");
+  static_assert(!PERSIST || BN == kPersistBN || BN == kWideBN, "persistent tile widths");
+  // 256-wide persistent tiles: the running sum of the splits lives in the fp32
+  // output (kF32) or in p.ws (residual); SwiGLU tiles come with one split only
+  constexpr bool WIDE = PERSIST && BN == kWideBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   float* stg = PERSIST ? reinterpret_cast<float*>(sB + STAGES * B_BYTES) : reinterpret_cast<float*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES + (PERSIST ? (size_t)BN * BM * 4 : 0));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES + extra_bytes(BN, PERSIST, SWI));
   uint64_t* empty = full + STAGES;
   uint64_t* accf = empty + STAGES;  // [2] accumulator b holds a finished split
   uint64_t* acce = accf + 2;        // [2] accumulator b has been drained
@@ -295,12 +326,13 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
     }
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
-    auto load_w = [&](int st, int m_tile, int kb) {
+    auto load_w = [&](int st, int t, int kb) {
+      const TileIdx ti = tile_of(p, t);
       if (SWI) {
-        tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], kb * BK, m_tile * (BM / 2), pol_w);
-        tma_load_2d(sA + st * A_BYTES + A_BYTES / 2, &tmW2, &full[st], kb * BK, m_tile * (BM / 2), pol_w);
+        tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], kb * BK, ti.m_tile * (BM / 2), pol_w);
+        tma_load_2d(sA + st * A_BYTES + A_BYTES / 2, &tmW2, &full[st], kb * BK, ti.m_tile * (BM / 2), pol_w);
       } else {
-        tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], kb * BK, m_tile * BM, pol_w);
+        tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], kb * BK, ti.g * p.N + ti.m_tile * BM, pol_w);
       }
     };
     // Weights do not depend on the previous kernel: the first stages of them
@@ -312,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
       split_range(p, s, kb0, kb1);
       for (int kb = kb0; kb < kb1 && it < STAGES; ++kb, ++it) {
         mbar_expect_tx(&full[it], TX);
-        load_w(it, t / p.n_tiles, kb);
+        load_w(it, t, kb);
       }
       return it < STAGES;
     });
@@ -323,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
     for_each_unit<PERSIST>(p, [&](int t, int s) {
       int kb0, kb1;
       split_range(p, s, kb0, kb1);
-      const int m_tile = t / p.n_tiles, n_tile = t % p.n_tiles;
+      const TileIdx ti = tile_of(p, t);
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         const int st = it % STAGES;
         if (it >= pre) {
@@ -332,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
             return false;
           }
           mbar_expect_tx(&full[st], TX);
-          load_w(st, m_tile, kb);
+          load_w(st, t, kb);
         }
-        tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], kb * BK, n_tile * BN, pol_x);
+        tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], kb * BK, ti.g * p.M + ti.n_tile * BN, pol_x);
       }
       return true;
     });
@@ -407,6 +439,89 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
       }
       fence_after();
       const uint32_t acc = lanes + (uint32_t)(b * BN);
+      if constexpr (WIDE) {
+        const TileIdx ti = tile_of(p, t);
+        const int tok0 = ti.n_tile * BN, m_tile = ti.m_tile;
+        const bool last = s == p.splits - 1;
+        if constexpr (SWI) {
+          // one split: gate rows 0..63 take the matching up row (64 + r) of
+          // each 32-column chunk through shared memory
+          const int r64 = row & 63, feat = m_tile * (BM / 2) + r64;
+          bf16* y = reinterpret_cast<bf16*>(p.Y) + feat;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            float v[32];
+            tmem_ld32(acc + c0, v);
+            if (row >= 64) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) stg[r64 * 33 + i] = v[i];
+            }
+            epi_bar();
+            const int nt = (row < 64 && feat < p.N) ? min(32, p.M - (tok0 + c0)) : 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nt) {
+                const float g = v[i], u = stg[r64 * 33 + i];
+                y[(int64_t)(tok0 + c0 + i) * p.ldy] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+              }
+            epi_bar();
+          }
+        } else {
+          // Y (fp32 output) or p.ws (residual) holds the running sum of the
+          // splits so far, ((0 + P_0) + P_1) + ...; a thread only rereads what
+          // it wrote for the split before (a tile's splits run in order here)
+          const int feat = m_tile * BM + row;
+          const bool resid = p.mode == kResidBf16;
+          auto run_ptr = [&](int tok) -> float* {
+            if (resid) return p.ws + (int64_t)tok * p.N + feat;
+            if (p.yseg) return reinterpret_cast<float*>(p.yseg[tok / p.seg_rows]) + (int64_t)(tok % p.seg_rows) * p.ldy + feat;
+            return reinterpret_cast<float*>(p.Y) + ti.g * p.y_group + (int64_t)tok * p.ldy + feat;
+          };
+          // 32 columns at a time for an fp32 output, 16 for the residual
+          // stream (which also holds h in registers)
+          auto chunk = [&](auto cw_tag, int c0) {
+            constexpr int CW = decltype(cw_tag)::value;
+            float v[CW];
+            tmem_ld<CW>(acc + c0, v);
+            const int nt = feat < p.N ? min(CW, p.M - (tok0 + c0)) : 0;
+            if (s > 0) {
+              float pr[CW];
+#pragma unroll
+              for (int i = 0; i < CW; ++i) pr[i] = i < nt ? *run_ptr(tok0 + c0 + i) : 0.f;
+#pragma unroll
+              for (int i = 0; i < CW; ++i) v[i] = pr[i] + v[i];
+            } else {
+#pragma unroll
+              for (int i = 0; i < CW; ++i) v[i] = 0.f + v[i];
+            }
+            if (resid && last) {
+              bf16* h = reinterpret_cast<bf16*>(p.Y) + feat;
+              float hv[CW];
+#pragma unroll
+              for (int i = 0; i < CW; ++i) hv[i] = i < nt ? __bfloat162float(h[(int64_t)(tok0 + c0 + i) * p.ldy]) : 0.f;
+#pragma unroll
+              for (int i = 0; i < CW; ++i)
+                if (i < nt) h[(int64_t)(tok0 + c0 + i) * p.ldy] = __float2bfloat16_rn(hv[i] + v[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < CW; ++i)
+                if (i < nt) *run_ptr(tok0 + c0 + i) = v[i];
+            }
+          };
+          if (resid) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) chunk(std::integral_constant<int, 16>(), c0);
+          } else {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) chunk(std::integral_constant<int, 32>(), c0);
+          }
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce[b]);
+        ++j;
+        return true;
+      }
       const uint32_t run = lanes + (uint32_t)(2 * BN);  // running sum (persistent, split > 0)
       const bool last = s == p.splits - 1;
       if (!PERSIST || last) {
@@ -510,7 +625,7 @@ struct TcContext {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   int num_sms = 0;
   int* err = nullptr;
-  bool attr_set[12] = {};
+  bool attr_set[16] = {};
 };
 
 const char* tc_last_error() { return g_tc_err.c_str(); }
@@ -589,7 +704,7 @@ constexpr size_t kSmemMax = 227 * 1024;
 template <int BN, bool SWI, bool PERSIST>
 static int launch_bn(TcContext* c, const CUtensorMap& mw, const CUtensorMap& mw2, const CUtensorMap& mx,
                      const TcParams& p, int grid, int cluster, cudaStream_t st, int slot) {
-  const size_t smem = smem_bytes(BN, PERSIST, p.stages);
+  const size_t smem = smem_bytes(BN, PERSIST, SWI, p.stages);
   if (smem > kSmemMax || p.stages < 2 || p.stages > kMaxStages || (size_t)BN * BM * 4 > (size_t)p.stages * stage_bytes(BN))
     return tc_fail("tc_gemm: pipeline does not fit shared memory");
   if (!c->attr_set[slot]) {
@@ -607,6 +722,7 @@ template <bool SWI>
 static int launch_mode(TcContext* c, int BN, bool persist, const CUtensorMap& mw, const CUtensorMap& mw2,
                        const CUtensorMap& mx, const TcParams& p, int grid, int cluster, cudaStream_t st) {
   const int base = SWI ? 6 : 0;
+  if (persist && BN == kWideBN) return launch_bn<kWideBN, SWI, true>(c, mw, mw2, mx, p, grid, cluster, st, SWI ? 13 : 12);
   if (persist) return launch_bn<kPersistBN, SWI, true>(c, mw, mw2, mx, p, grid, cluster, st, base + 5);
   switch (BN) {
     case 16: return launch_bn<16, SWI, false>(c, mw, mw2, mx, p, grid, cluster, st, base + 0);
@@ -616,8 +732,30 @@ static int launch_mode(TcContext* c, int BN, bool persist, const CUtensorMap& mw
   }
 }
 
+int tc_gemm_grouped(TcContext* c, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy,
+                    int64_t y_group, int M, int N, int K, int groups, cudaStream_t st) {
+  if (M <= 0 || N <= 0 || groups <= 0) return 0;
+  if (K % BK || ldx % 8 || ldw % 8 || ((uintptr_t)X & 15) || ((uintptr_t)W & 15))
+    return tc_fail("tc_gemm_grouped: K must be a multiple of 64, strides multiples of 8, operands 16-byte aligned");
+  const int m_tiles = (N + BM - 1) / BM, kb_total = K / BK;
+  // the splits of one product of this shape, as tc_gemm chooses them
+  int cap = std::max(1, std::min({2 * c->num_sms / m_tiles, kMaxSplits, std::max(1, kb_total / 2)}));
+  int splits = 1;
+  while (splits * 2 <= cap) splits *= 2;
+  const int n_tiles = (M + kWideBN - 1) / kWideBN;
+  const int tiles = m_tiles * n_tiles * groups;
+  CUtensorMap mw, mx;
+  if (encode_2d(c, &mw, W, (uint64_t)K, (uint64_t)N * groups, ldw, (uint32_t)BM)) return -1;
+  if (encode_2d(c, &mx, X, (uint64_t)K, (uint64_t)M * groups, ldx, (uint32_t)kWideBN)) return -1;
+  const size_t fixed = extra_bytes(kWideBN, true, false) + 1024 + kBarrierBytes;
+  const int stages = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed) / stage_bytes(kWideBN));
+  TcParams p{Y, ldy, M, N, kF32, m_tiles, n_tiles, splits, kb_total, 0, stages, nullptr, 0, c->err, nullptr, groups,
+             y_group};
+  return launch_bn<kWideBN, false, true>(c, mw, mw, mx, p, std::min(tiles, c->num_sms), 1, st, 12);
+}
+
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y,
-            int64_t ldy, int M, int N, int K, int mode, cudaStream_t st, void* const* yseg, int seg_rows) {
+            int64_t ldy, int M, int N, int K, int mode, cudaStream_t st, void* const* yseg, int seg_rows, float* ws) {
   if (M <= 0 || N <= 0) return 0;
   const bool swi = mode == kSwigluBf16;
   if (yseg && (mode != kF32 || seg_rows <= 0)) return tc_fail("tc_gemm: row segments need fp32 output");
@@ -637,7 +775,8 @@ int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void*
   // otherwise one CTA per (tile, split), the splits of a tile in a cluster.
   const int tiles128 = m_tiles * ((M + kPersistBN - 1) / kPersistBN);
   const bool persist = M > 128 && 2 * tiles128 >= c->num_sms;
-  const int BN = persist ? kPersistBN : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  const bool wide = persist && (mode == kF32 || (mode == kResidBf16 && ws) || (swi && splits == 1));
+  const int BN = wide ? kWideBN : persist ? kPersistBN : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
   const int n_tiles = (M + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
   CUtensorMap mw, mw2, mx;
@@ -653,10 +792,10 @@ int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void*
   // Pipeline depth from the shared memory of one CTA per SM when the grid
   // fits one per SM, else of two: each CTA's stream is latency-bound, so the
   // bytes in flight per SM set its bandwidth.
-  const size_t fixed = (persist ? (size_t)BN * BM * 4 : 0) + 1024 + kBarrierBytes;
+  const size_t fixed = extra_bytes(BN, persist, swi) + 1024 + kBarrierBytes;
   const size_t budget = (persist || grid <= c->num_sms) ? kSmemMax : 112 * 1024;
   const int stages = (int)std::min<size_t>(kMaxStages, (budget - fixed) / stage_bytes(BN));
-  TcParams p{Y, ldy, M, N, mode, m_tiles, n_tiles, splits, kb_total, vec, stages, yseg, seg_rows, c->err};
+  TcParams p{Y, ldy, M, N, mode, m_tiles, n_tiles, splits, kb_total, vec, stages, yseg, seg_rows, c->err, ws, 1, 0};
   const int cluster = persist ? 1 : splits;
   return swi ? launch_mode<true>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st)
              : launch_mode<false>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st);

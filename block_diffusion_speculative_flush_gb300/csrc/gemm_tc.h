@@ -28,9 +28,20 @@ enum TcMode {
 // a row's result does not change with the number of rows in the call.
 // With yseg (device table, kF32 only) output rows [j*seg_rows, (j+1)*seg_rows)
 // go to the buffer yseg[j] (row stride ldy, 16-byte aligned) instead of
-// Y + row * ldy; Y is then unused.
+// Y + row * ldy; Y is then unused.  ws (kResidBf16 only, may be NULL): an
+// fp32 [M][N] scratch that lets many-row calls use 256-wide tiles, holding
+// the running sum of the K splits; its contents are overwritten.
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y, int64_t ldy,
-            int M, int N, int K, int mode, cudaStream_t st, void* const* yseg = nullptr, int seg_rows = 0);
+            int M, int N, int K, int mode, cudaStream_t st, void* const* yseg = nullptr, int seg_rows = 0,
+            float* ws = nullptr);
+
+// `groups` independent fp32 products of one shape in one persistent launch of
+// 256-wide tiles: X stacked [groups * M][ldx], W stacked [groups * N][ldw],
+// product g into Y + g * y_group (rows ldy apart).  Each product sums its K
+// splits exactly as tc_gemm does for that shape, so its results are the same
+// bits as a separate call's.
+int tc_gemm_grouped(TcContext* c, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy,
+                    int64_t y_group, int M, int N, int K, int groups, cudaStream_t st);
 
 // TMA maps of a session's K/V cache for the attention kernel: out[0] views
 // the K planes ([planes][cap][d], 64 x 64 boxes), out[1] the V^T planes

@@ -67,10 +67,26 @@ void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* 
 // [0, V) set bit 1 of *err and read row 0.
 void launch_embed(DT dt, const void* E, const int32_t* current, const int32_t* sess_map, int mask_token, int V,
                   int B, int nrows, int H, void* h, int32_t* err, cudaStream_t st);
-void launch_rope_table(const RowMeta* meta, int M, int d, float theta, float2* table, cudaStream_t st);
+// table[m] = cos / sin of pos(m) * theta^(-2j/d), j < d/2: pos(m) = meta[m].pos,
+// or first + m when meta is NULL (the model's table indexed by position).
+void launch_rope_table(const RowMeta* meta, int64_t first, int M, int d, float theta, float2* table,
+                       cudaStream_t st);
+// Context-only forward: K (k norm, RoPE from the position table) and V of
+// every row into the session caches, 32 rows of one KV head of one layer per
+// CTA; the same bits as k_qkv_post writes for a context row.  Layer layer0 + z
+// (z < layers) reads qkv + z * layer_stride, rows ldq apart, K of head h at
+// column kcol0 + h d and V at vcol0 + h d, with gain k_norms[z] (a device table).
+void launch_kv_ctx(DT dt, const float* qkv, int64_t ldq, int64_t kcol0, int64_t vcol0, int64_t layer_stride,
+                   const RowMeta* meta, int M, const float2* rope, const void* const* k_norms, int Hkv, int d,
+                   float eps, SessTables tabs, int layer0, int layers, cudaStream_t st);
+// Every layer's norm of the same rows: out + l * out_layer = rmsnorm(in; gains[l])
+// (gains: a device table), the sums in launch_rmsnorm's order.
+void launch_rmsnorm_layers(DT dt, const void* in, int64_t ld_in, const void* const* gains, void* out, int64_t ld_out,
+                           int64_t out_layer, int rows, int layers, int H, float eps, cudaStream_t st);
 // Returns the number of kernels launched (2 from kVApartRows rows on: the V
 // rows go to the transposed cache planes 32 rows at a time).
 constexpr int kVApartRows = 64;
+// rope: the model's table indexed by position ([pos][d/2]).
 int launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
                     const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
                     SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st);

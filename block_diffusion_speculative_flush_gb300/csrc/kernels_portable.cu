@@ -85,6 +85,48 @@ __device__ __forceinline__ void norm_row_vec(const bf16* x, const bf16* g, bf16*
   }
 }
 
+// fp32 rows of up to 4096 into bf16 (the fc output's hidden_norm): 128
+// threads, each holding its eight float4 words in registers; one load of each
+// input word and of each gain word, one 8-byte store per output word.
+constexpr int kNormF32Vec = 8;
+__global__ void __launch_bounds__(128) k_rmsnorm_f32v(const float* __restrict__ in, int64_t ld_in,
+                                                      const bf16* __restrict__ g, bf16* __restrict__ out,
+                                                      int64_t ld_out, int H, float eps) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int j = blockIdx.x, nv = H / 4;
+  const float4* x = reinterpret_cast<const float4*>(in + (int64_t)j * ld_in);
+  float4 w[kNormF32Vec];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormF32Vec; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    w[i] = c < nv ? __ldg(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += w[i].x * w[i].x;
+    ss += w[i].y * w[i].y;
+    ss += w[i].z * w[i].z;
+    ss += w[i].w * w[i].w;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)H + eps);
+  bf16* o = out + (int64_t)j * ld_out;
+#pragma unroll
+  for (int i = 0; i < kNormF32Vec; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    if (c >= nv) continue;
+    const uint2 gw = __ldg(reinterpret_cast<const uint2*>(g) + c);
+    const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.x));
+    const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.y));
+    const __nv_bfloat162 a = __floats2bfloat162_rn(w[i].x * inv * g01.x, w[i].y * inv * g01.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(w[i].z * inv * g23.x, w[i].w * inv * g23.y);
+    uint2 raw;
+    raw.x = *reinterpret_cast<const uint32_t*>(&a);
+    raw.y = *reinterpret_cast<const uint32_t*>(&b);
+    reinterpret_cast<uint2*>(o)[c] = raw;
+  }
+}
+
 template <typename T>
 __global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict__ aux, T* __restrict__ u,
                            int K, int Ht, float eps) {
@@ -112,20 +154,12 @@ __global__ void k_tap_norm(const T* const* __restrict__ src, const T* __restrict
   for (int j = threadIdx.x; j < Ht; j += blockDim.x) o[j] = from_f<T>(to_f(f[j]) * inv * to_f(g[j]));
 }
 
-// One CTA per output row; the row stays in registers between the sum of
-// squares and the scaled write (up to 8 x blockDim.x elements per row).
+// One row of RMSNorm by the whole CTA; the row stays in registers between
+// the sum of squares and the scaled write (up to 8 x blockDim.x elements).
 template <typename TIn, typename T>
-__global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, int rows0, const TIn* __restrict__ in1,
-                                                 int64_t ld_in, const T* __restrict__ g, T* __restrict__ out,
-                                                 int64_t ld_out, int H, int a, int b, int c, float eps) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float red[32];
-  const int j = blockIdx.x;
-  const int src = (j / a) * b + (j % a) + c;
-  const TIn* x = src < rows0 ? in0 + (int64_t)src * ld_in : in1 + (int64_t)(src - rows0) * ld_in;
+__device__ __forceinline__ void rmsnorm_row(const TIn* __restrict__ x, const T* __restrict__ g, T* __restrict__ o,
+                                            int H, float eps, float* red) {
   if constexpr (std::is_same<TIn, bf16>::value && std::is_same<T, bf16>::value) {
-    T* o = out + (int64_t)j * ld_out;
     if (norm_vec_ok(x, g, o, H)) {
       norm_row_vec(x, g, o, H, eps, red);
       return;
@@ -146,13 +180,40 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, in
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)H + eps);
-  T* o = out + (int64_t)j * ld_out;
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
     const int t = threadIdx.x + k * blockDim.x;
     if (t < H) o[t] = from_f<T>(v[k] * inv * to_f(g[t]));
   }
   for (int t = threadIdx.x + MAXV * blockDim.x; t < H; t += blockDim.x) o[t] = from_f<T>(to_f(x[t]) * inv * to_f(g[t]));
+}
+
+// One CTA per output row.
+template <typename TIn, typename T>
+__global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, int rows0, const TIn* __restrict__ in1,
+                                                 int64_t ld_in, const T* __restrict__ g, T* __restrict__ out,
+                                                 int64_t ld_out, int H, int a, int b, int c, float eps) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int j = blockIdx.x;
+  const int src = (j / a) * b + (j % a) + c;
+  const TIn* x = src < rows0 ? in0 + (int64_t)src * ld_in : in1 + (int64_t)(src - rows0) * ld_in;
+  rmsnorm_row(x, g, out + (int64_t)j * ld_out, H, eps, red);
+}
+
+// Every layer's input norm of the same rows at once (a context-only
+// forward): CTA (j, l) writes row j of out + l * out_layer with the gain of
+// layer l, by the arithmetic of k_rmsnorm.
+template <typename T>
+__global__ void __launch_bounds__(512) k_rmsnorm_layers(const T* __restrict__ in, int64_t ld_in,
+                                                        const T* const* __restrict__ gains, T* __restrict__ out,
+                                                        int64_t ld_out, int64_t out_layer, int H, float eps) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int j = blockIdx.x, l = blockIdx.y;
+  rmsnorm_row(in + (int64_t)j * ld_in, gains[l], out + l * out_layer + (int64_t)j * ld_out, H, eps, red);
 }
 
 // Block rows [anchor, mask x n]: rows of E copied 16 bytes at a time.
@@ -176,14 +237,16 @@ __global__ void k_embed(const T* __restrict__ E, const int32_t* __restrict__ cur
 }
 
 // cos / sin of pos * theta^(-2j/d), the angle formed and reduced in double so
-// that large positions keep full fp32 accuracy.
-__global__ void k_rope_table(const RowMeta* __restrict__ meta, int d, float theta, float2* __restrict__ table) {
+// that large positions keep full fp32 accuracy; row m of the table is position
+// meta[m].pos, or first + m without a row table.
+__global__ void k_rope_table(const RowMeta* __restrict__ meta, int64_t first, int d, float theta,
+                             float2* __restrict__ table) {
   pdl_trigger();
   pdl_wait();
   const int m = blockIdx.x, j = threadIdx.x;
   if (j >= d / 2) return;
   const double inv = pow((double)theta, -2.0 * (double)j / (double)d);
-  const double ang = (double)meta[m].pos * inv;
+  const double ang = (double)(meta ? meta[m].pos : first + m) * inv;
   double s, c;
   sincos(ang, &s, &c);
   table[(int64_t)m * (d / 2) + j] = make_float2((float)c, (float)s);
@@ -227,7 +290,7 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
   const T* gn = is_q ? q_norm : k_norm;
 #pragma unroll
   for (int u = 0; u < DU; ++u) y[u] = y[u] * inv * to_f(gn[lane + 32 * u]);
-  const float2* rt = rope + (int64_t)m * (d / 2);
+  const float2* rt = rope + rm.pos * (d / 2);  // the table is indexed by position
 #pragma unroll
   for (int u = 0; u < DU / 2; ++u) {
     const float2 cs = rt[lane + 32 * u];
@@ -279,6 +342,92 @@ __global__ void __launch_bounds__(256) k_v_cache_t(const float* __restrict__ qkv
   const int64_t cap = tabs.cap[rm.sess];
   const int64_t slot = rm.pos % cap;
   T* vd = (T*)tabs.kv[rm.sess] + ((int64_t)(2 * layer + 1) * Hkv + kh) * cap * D + slot;
+  for (int j = w; j < D; j += nw) vd[(int64_t)j * cap] = from_f<T>(tile[lane][j]);
+}
+
+// Context-only forward: K and V of 32 consecutive rows of one KV head into
+// the cache.  Each warp takes four rows of K with the arithmetic of
+// k_qkv_post (lane l holds elements l + 32u; the same sum order, norm, gain
+// and rotation), so a context row's cache entry is the same bits whichever
+// kernel wrote it; V goes through shared memory into the transposed planes as
+// in k_v_cache_t.  One CTA replaces a grid of M x (Hq + Hkv) / 4 head warps.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_kv_ctx(const float* __restrict__ qkv_all, int64_t ldq, int64_t kcol0,
+                                                int64_t vcol0, int64_t layer_stride, const RowMeta* __restrict__ meta,
+                                                int M, const float2* __restrict__ rope,
+                                                const T* const* __restrict__ k_norms, int Hkv, float eps,
+                                                SessTables tabs, int layer0) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int DU = D / 32;
+  __shared__ float tile[32][D + 1];
+  const int kh = blockIdx.y, m0 = blockIdx.x * 32, layer = layer0 + (int)blockIdx.z;
+  const float* qkv = qkv_all + (int64_t)blockIdx.z * layer_stride;
+  const T* k_norm = k_norms[blockIdx.z];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t vcol = vcol0 + (int64_t)kh * D;
+  for (int e = threadIdx.x; e < 32 * D; e += blockDim.x) {
+    const int r = e / D, j = e % D;
+    tile[r][j] = m0 + r < M ? qkv[(int64_t)(m0 + r) * ldq + vcol + j] : 0.f;
+  }
+  // K: warp w takes rows w, w + 8, w + 16, w + 24; every load of its four
+  // rows (meta, K, gains, then the rotation of each row's position) is issued
+  // before the arithmetic that needs it
+  constexpr int RPW = 4;
+  float y[RPW][DU], gn[DU];
+  int64_t pos[RPW];
+  int sess[RPW];
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = w + k * 8;
+    pos[k] = -1;
+    sess[k] = 0;
+    if (m0 + r < M) {
+      const RowMeta rm = meta[m0 + r];
+      pos[k] = rm.pos;
+      sess[k] = rm.sess;
+      const float* x = qkv + (int64_t)(m0 + r) * ldq + kcol0 + (int64_t)kh * D;
+#pragma unroll
+      for (int u = 0; u < DU; ++u) y[k][u] = x[lane + 32 * u];
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < DU; ++u) gn[u] = to_f(k_norm[lane + 32 * u]);
+  float2 cs[RPW][DU / 2];
+#pragma unroll
+  for (int k = 0; k < RPW; ++k)
+    if (pos[k] >= 0) {
+      const float2* rt = rope + pos[k] * (D / 2);
+#pragma unroll
+      for (int u = 0; u < DU / 2; ++u) cs[k][u] = rt[lane + 32 * u];
+    }
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    if (pos[k] < 0) continue;  // the same for the whole warp
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < DU; ++u) ss += y[k][u] * y[k][u];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / (float)D + eps);
+#pragma unroll
+    for (int u = 0; u < DU; ++u) y[k][u] = y[k][u] * inv * gn[u];
+#pragma unroll
+    for (int u = 0; u < DU / 2; ++u) {
+      const float a = y[k][u], b = y[k][u + DU / 2];
+      y[k][u] = a * cs[k][u].x - b * cs[k][u].y;
+      y[k][u + DU / 2] = b * cs[k][u].x + a * cs[k][u].y;
+    }
+    const int64_t cap = tabs.cap[sess[k]];
+    T* kd = (T*)tabs.kv[sess[k]] + (((int64_t)(2 * layer) * Hkv + kh) * cap + pos[k] % cap) * D;
+#pragma unroll
+    for (int u = 0; u < DU; ++u) kd[lane + 32 * u] = from_f<T>(y[k][u]);
+  }
+  __syncthreads();
+  const int m = m0 + lane;
+  if (m >= M) return;
+  const RowMeta rm = meta[m];
+  const int64_t cap = tabs.cap[rm.sess];
+  T* vd = (T*)tabs.kv[rm.sess] + ((int64_t)(2 * layer + 1) * Hkv + kh) * cap * D + rm.pos % cap;
   for (int j = w; j < D; j += nw) vd[(int64_t)j * cap] = from_f<T>(tile[lane][j]);
 }
 
@@ -1427,10 +1576,25 @@ void launch_rmsnorm(DT dt, bool in_f32, const void* in0, int rows0, const void* 
                     void* out, int64_t ld_out, int rows, int H, int a, int b, int c, float eps, cudaStream_t st) {
   if (rows <= 0) return;
   if (in_f32) {
+    // fp32 rows into bf16 (one input, the identity row map): the vector
+    // kernel whenever the width allows it; the choice depends on H only, so a
+    // row's sum order never depends on how many rows share a call
+    // (row map j -> (j / a) * b + j % a + c is the identity when a >= rows and c == 0)
+    const bool vec = dt == DT::BF16 && H % 4 == 0 && H <= 4 * kNormF32Vec * 128 && rows0 >= rows && a >= rows &&
+                     c == 0 && ld_in % 4 == 0 && ld_out % 4 == 0 && (((uintptr_t)in0 | (uintptr_t)g |
+                     (uintptr_t)out) & 15) == 0;
+    if (vec) {
+      launch_k(k_rmsnorm_f32v, rows, 128, 0, st, (const float*)in0, ld_in, (const bf16*)g, (bf16*)out, ld_out, H, eps);
+      return;
+    }
     DFL_DISPATCH(dt, launch_k(k_rmsnorm<float, T>, rows, 512, 0, st, (const float*)in0, rows0, (const float*)in1, ld_in,
                                                                 (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
   } else {
-    DFL_DISPATCH(dt, launch_k(k_rmsnorm<T, T>, rows, 512, 0, st, (const T*)in0, rows0, (const T*)in1, ld_in,
+    // bf16 rows of up to 4096 fit 128 threads of four 16-byte words each, so
+    // sixteen rows per SM are in flight at once; the block shape depends on H
+    // only, so a row's sum order never depends on how many rows share a call
+    const int threads = (dt == DT::BF16 && H % 8 == 0 && H <= 8 * kNormVec * 128) ? 128 : 512;
+    DFL_DISPATCH(dt, launch_k(k_rmsnorm<T, T>, rows, threads, 0, st, (const T*)in0, rows0, (const T*)in1, ld_in,
                                                             (const T*)g, (T*)out, ld_out, H, a, b, c, eps));
   }
 }
@@ -1442,9 +1606,33 @@ void launch_embed(DT dt, const void* E, const int32_t* current, const int32_t* s
                                                           (T*)h, err));
 }
 
-void launch_rope_table(const RowMeta* meta, int M, int d, float theta, float2* table, cudaStream_t st) {
+void launch_rope_table(const RowMeta* meta, int64_t first, int M, int d, float theta, float2* table,
+                       cudaStream_t st) {
   if (M <= 0) return;
-  launch_k(k_rope_table, M, d / 2, 0, st, meta, d, theta, table);
+  launch_k(k_rope_table, M, 64, 0, st, meta, first, d, theta, table);
+}
+
+void launch_kv_ctx(DT dt, const float* qkv, int64_t ldq, int64_t kcol0, int64_t vcol0, int64_t layer_stride,
+                   const RowMeta* meta, int M, const float2* rope, const void* const* k_norms, int Hkv, int d,
+                   float eps, SessTables tabs, int layer0, int layers, cudaStream_t st) {
+  if (M <= 0 || layers <= 0) return;
+  const dim3 grid(cdiv(M, 32), Hkv, layers);
+  if (d == 64) {
+    DFL_DISPATCH(dt, launch_k(k_kv_ctx<T, 64>, grid, 256, 0, st, qkv, ldq, kcol0, vcol0, layer_stride, meta, M, rope,
+                              (const T* const*)k_norms, Hkv, eps, tabs, layer0));
+  } else {
+    DFL_DISPATCH(dt, launch_k(k_kv_ctx<T, 128>, grid, 256, 0, st, qkv, ldq, kcol0, vcol0, layer_stride, meta, M, rope,
+                              (const T* const*)k_norms, Hkv, eps, tabs, layer0));
+  }
+}
+
+void launch_rmsnorm_layers(DT dt, const void* in, int64_t ld_in, const void* const* gains, void* out, int64_t ld_out,
+                           int64_t out_layer, int rows, int layers, int H, float eps, cudaStream_t st) {
+  if (rows <= 0 || layers <= 0) return;
+  // the block shape of launch_rmsnorm's storage-type rows, so the sums agree
+  const int threads = (dt == DT::BF16 && H % 8 == 0 && H <= 8 * kNormVec * 128) ? 128 : 512;
+  DFL_DISPATCH(dt, launch_k(k_rmsnorm_layers<T>, dim3(rows, layers), threads, 0, st, (const T*)in, ld_in,
+                            (const T* const*)gains, (T*)out, ld_out, out_layer, H, eps));
 }
 
 int launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,

@@ -145,20 +145,22 @@ def test_pending_rows_flush_at_256(D):
 @pytest.mark.parametrize("cfg_name", ["tiny_fp32", "small_bf16"])
 def test_incremental_flush_is_bit_identical(D, cfg_name):
     """A context entry depends only on its own features: flushing in pieces
-    gives the same cache bytes as one flush."""
+    gives the same cache bytes as one flush.  One flush of 300 rows takes the
+    grouped many-row path (every layer's norm, K/V product and cache write in
+    one launch each); pieces of up to 120 rows take the per-layer path."""
     p = Pair(S.CONFIGS[cfg_name])
     cfg = p.cfg
-    _, f = p.feats(120, seed=4)
+    _, f = p.feats(300, seed=4)
     a = D.dflash_open(p.model, max_ctx=512)
     D.dflash_committed(a, f, 0)
     D.dflash_flush([a])
     b = D.dflash_open(p.model, max_ctx=512)
-    for lo, hi in [(0, 1), (1, 9), (9, 70), (70, 120)]:
+    for lo, hi in [(0, 1), (1, 9), (9, 70), (70, 190), (190, 300)]:
         D.dflash_committed(b, f[lo:hi], lo)
         D.dflash_flush([b])
     for l in range(cfg.n_layers):
-        ka, va = export_kv(D, a, cfg, l, 0, 120)
-        kb, vb = export_kv(D, b, cfg, l, 0, 120)
+        ka, va = export_kv(D, a, cfg, l, 0, 300)
+        kb, vb = export_kv(D, b, cfg, l, 0, 300)
         assert np.array_equal(ka, kb) and np.array_equal(va, vb)
     D.dflash_close(a)
     D.dflash_close(b)
@@ -353,12 +355,14 @@ def test_windowed_rounds_follow_the_oracle(D, block):
     D.dflash_close(s)
 
 
-def test_rows_do_not_depend_on_the_batch(D):
+@pytest.mark.parametrize("intermediate", [1024, 12288])
+def test_rows_do_not_depend_on_the_batch(D, intermediate):
     """A session's block logits are bit-identical whether it proposes alone
     or among 127 other sessions: the K order of every product depends on the
     weight shape only, so the 16-row and the 2048-row schedules (split
-    clusters, persistent tiles with several K splits) sum alike."""
-    p = Pair(S.CONFIGS["small_bf16"])
+    clusters; persistent tiles 128 or 256 rows wide, with several K splits,
+    and the one-split SwiGLU of a wide MLP) sum alike."""
+    p = Pair(S.CONFIGS["small_bf16"].replace(intermediate=intermediate))
     cfg = p.cfg
     n = cfg.block_size - 1
     B = 128
