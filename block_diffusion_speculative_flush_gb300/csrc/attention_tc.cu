@@ -15,15 +15,16 @@
 //                 gets the deeper ring: it keeps two to three tiles of loads
 //                 in flight past the ones being computed.
 //   warp 9        MMA: S = Q K^T into one of two TMEM buffers, then
-//                 O += P V^T (P as a bf16 hi + lo pair, ~16 bits of the
-//                 probabilities) into the TMEM accumulator.
+//                 O += P V^T (P rounded to bf16) into the TMEM accumulator.
 //   warps 0..7    softmax, two threads per query row (warps w and w + 4 read
 //                 the same TMEM lanes; each takes 32 keys of a tile and 64
 //                 columns of O): S from TMEM, mask against the row's visible
 //                 key range, online max in the exp2 domain with lazy
 //                 rescaling (O and the sum are rescaled only when the row max
-//                 grows by more than 2^8, so P <= 256), P written to shared
-//                 memory as the next MMA's A operand; finally O and
+//                 grows by more than 2^8, so P <= 256), P rounded to bf16 and
+//                 written to shared memory as the next MMA's A operand (the
+//                 row sum adds the rounded values, so the weights P V uses
+//                 are exactly normalised); finally O and
 //                 (max, sum) go out as this key range's partial.
 // Every wait is bounded; an expired wait sets bit 8 of the error word.
 #include <cooperative_groups.h>
@@ -44,12 +45,12 @@ namespace cg = cooperative_groups;
 constexpr int D = 128;                       // head dim
 constexpr int KT = 64;                       // keys per tile (MMA N of S)
 constexpr int KST = 2;                       // K stages
-constexpr int VST = 5;                       // V^T stages
+constexpr int VST = 7;                       // V^T stages
 constexpr int QBYTES = 128 * D * 2;          // Q: two [128 rows][64 d] swizzled blocks
 constexpr int KBYTES = KT * D * 2;           // K tile: two [64 keys][64 d] blocks
 constexpr int VBYTES = D * KT * 2;           // V^T tile: one [128 d][64 keys] block
 constexpr int PBYTES = 128 * KT * 2;         // P tile: one [128 rows][64 keys] block
-constexpr int DATA_BYTES = QBYTES + KST * KBYTES + VST * VBYTES + 4 * PBYTES;  // + barriers and exchange
+constexpr int DATA_BYTES = QBYTES + KST * KBYTES + VST * VBYTES + 2 * PBYTES;  // + barriers and exchange
 constexpr int THREADS = 320;
 constexpr int SOFTMAX_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 256;          // O [0,128), S0 [128,192), S1 [192,256)
@@ -60,12 +61,12 @@ __device__ __forceinline__ bool visible(int64_t F, int i, int64_t r, int window,
   return true;
 }
 
-__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+// Two probabilities rounded to bf16 (packed), and the rounded values' sum.
+__device__ __forceinline__ uint32_t pack_p(float x0, float x1, float& sum) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
   const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
+  sum += hf.x + hf.y;
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // byte offset of 16-byte chunk c of row r inside a [rows][128 B] swizzled block
@@ -79,8 +80,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + QBYTES;
   uint8_t* sV = sK + KST * KBYTES;
-  uint8_t* sP = sV + VST * VBYTES;  // [2 buffers][hi, lo]
-  uint64_t* k_full = (uint64_t*)(sP + 4 * PBYTES);
+  uint8_t* sP = sV + VST * VBYTES;  // [2 buffers]
+  uint64_t* k_full = (uint64_t*)(sP + 2 * PBYTES);
   uint64_t* k_empty = k_full + KST;
   uint64_t* v_full = k_empty + KST;
   uint64_t* v_empty = v_full + VST;
@@ -210,12 +211,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
         if (!mbar_wait(&p_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag)) return false;
         if (!mbar_wait(&v_full[vs], (uint32_t)(u / VST) & 1u, abort_flag)) return false;
         fence_after();
-        const uint32_t ph = smem_u32(sP + pb * 2 * PBYTES), pl = ph + PBYTES, v0 = smem_u32(sV + vs * VBYTES);
+        const uint32_t ph = smem_u32(sP + pb * PBYTES), v0 = smem_u32(sV + vs * VBYTES);
 #pragma unroll
         for (int ks = 0; ks < KT / 16; ++ks)
           umma_bf16(tO, sdesc_sw128(ph + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, (u > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < KT / 16; ++ks) umma_bf16(tO, sdesc_sw128(pl + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, 1u);
         umma_commit(&pv_done[pb]);
         umma_commit(&v_empty[vs]);
         return true;
@@ -293,10 +292,20 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       const int lo = lo64 < 0 ? 0 : (lo64 > 32 ? 32 : (int)lo64);
       const int hi = hi64 < -1 ? -1 : (hi64 > 31 ? 31 : (int)hi64);
       float mt = -INFINITY;
+      if (__all_sync(0xffffffffu, lo == 0 && hi == 31)) {
+        // every key of this half-tile is visible to every row of the warp
+        // (the common case without a window): no mask to apply
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        s[j] = (j >= lo && j <= hi) ? s[j] * sl2 : -INFINITY;
-        mt = fmaxf(mt, s[j]);
+        for (int j = 0; j < 32; ++j) {
+          s[j] *= sl2;
+          mt = fmaxf(mt, s[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          s[j] = (j >= lo && j <= hi) ? s[j] * sl2 : -INFINITY;
+          mt = fmaxf(mt, s[j]);
+        }
       }
       // both threads of a row agree on the tile max
       float* xt = xch + (t & 1) * 256;
@@ -323,30 +332,24 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       }
       l *= f;
       m_used = m_new;
-      uint32_t hi2[16], lo2[16];
+      uint32_t hi2[16];
       float ls = 0.f;
       // while a row has seen no visible key its max is -inf and every score
       // is -inf too: exponentiate against 0 so that P = exp2(-inf) = 0
       const float mref = m_used == -INFINITY ? 0.f : m_used;
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float p0 = exp2f(s[j] - mref), p1 = exp2f(s[j + 1] - mref);
-        ls += p0 + p1;
-        split_pack(p0, p1, hi2[j / 2], lo2[j / 2]);
-      }
+      for (int j = 0; j < 32; j += 2) hi2[j / 2] = pack_p(exp2f(s[j] - mref), exp2f(s[j + 1] - mref), ls);
       l += ls;
       const int pb = t & 1;
       if (t >= 2) {  // the P buffer is free once the product of tile t-2 is done
         ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[pb], (uint32_t)((t >> 1) - 1) & 1u, abort_flag));
         if (!ok) break;
       }
-      uint8_t* ph = sP + pb * 2 * PBYTES;
+      uint8_t* ph = sP + pb * PBYTES;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int cc = 4 * half + c;
         *reinterpret_cast<uint4*>(ph + swz(r, cc)) = make_uint4(hi2[4 * c], hi2[4 * c + 1], hi2[4 * c + 2], hi2[4 * c + 3]);
-        *reinterpret_cast<uint4*>(ph + PBYTES + swz(r, cc)) =
-            make_uint4(lo2[4 * c], lo2[4 * c + 1], lo2[4 * c + 2], lo2[4 * c + 3]);
       }
       fence_proxy_async();
       fence_before();
