@@ -12,20 +12,32 @@
 //                 ring; the cache keeps V transposed so that both are K-major
 //                 operand tiles.  A K stage is free once S = Q K^T is done, a
 //                 V stage only once P V is done, one to two tiles later, so V
-//                 gets the deeper ring: it keeps two to three tiles of loads
-//                 in flight past the ones being computed.
-//   warp 9        MMA: S = Q K^T into one of two TMEM buffers, then
-//                 O += P V^T (P rounded to bf16) into the TMEM accumulator.
+//                 gets the deeper ring.
+//   warp 9        MMA, the whole warp running one loop and one elected lane
+//                 issuing (queued MMAs do not hold the warp up): S(t) = Q K^T
+//                 into one of two TMEM buffers as soon as K(t) has landed and
+//                 the softmax has read S(t-2) out of that buffer; O += P V^T
+//                 in tile order as soon as P(u) and V(u) are in shared memory.
+//                 P is a bf16 pair hi + lo (~16 bits of the probabilities):
+//                 two MMAs per 16 keys.
 //   warps 0..7    softmax, two threads per query row (warps w and w + 4 read
 //                 the same TMEM lanes; each takes 32 keys of a tile and 64
 //                 columns of O): S from TMEM, mask against the row's visible
 //                 key range, online max in the exp2 domain with lazy
 //                 rescaling (O and the sum are rescaled only when the row max
-//                 grows by more than 2^8, so P <= 256), P rounded to bf16 and
-//                 written to shared memory as the next MMA's A operand (the
-//                 row sum adds the rounded values, so the weights P V uses
-//                 are exactly normalised); finally O and
+//                 grows by more than 2^8, so P <= 256), P = 2^(s k - m) with
+//                 the scale k folded into one packed two-lane FMA, written to
+//                 shared memory as the next MMA's A operand; finally O and
 //                 (max, sum) go out as this key range's partial.
+// Two streams when the query rows fit in 64 (R <= 64): TMEM lanes are tied to
+// warp quarters, so 64 rows would leave the softmax to warps 0, 1, 4, 5 (two
+// of the four SM sub-partitions).  Instead Q is stored twice (rows 64..127
+// repeat rows 0..63); warps of quarters 0-1 take the even key tiles (S buffer
+// 0, P buffer 0, O rows 0..63) and warps of quarters 2-3 the odd ones (S
+// buffer 1, P buffer 1, O rows 64..127), each with its own online softmax.
+// P buffer 0 keeps rows 64..127 at zero and buffer 1 rows 0..63, so the one
+// accumulator takes P V of each tile into its own stream's rows only.  The
+// two streams' (max, sum, O) merge in shared memory at the end.
 // Every wait is bounded; an expired wait sets bit 8 of the error word.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -45,32 +57,75 @@ namespace cg = cooperative_groups;
 constexpr int D = 128;                       // head dim
 constexpr int KT = 64;                       // keys per tile (MMA N of S)
 constexpr int KST = 2;                       // K stages
-constexpr int VST = 7;                       // V^T stages
+constexpr int VST = 5;                       // V^T stages
 constexpr int QBYTES = 128 * D * 2;          // Q: two [128 rows][64 d] swizzled blocks
 constexpr int KBYTES = KT * D * 2;           // K tile: two [64 keys][64 d] blocks
 constexpr int VBYTES = D * KT * 2;           // V^T tile: one [128 d][64 keys] block
 constexpr int PBYTES = 128 * KT * 2;         // P tile: one [128 rows][64 keys] block
-constexpr int DATA_BYTES = QBYTES + KST * KBYTES + VST * VBYTES + 2 * PBYTES;  // + barriers and exchange
+constexpr int DATA_BYTES = QBYTES + KST * KBYTES + VST * VBYTES + 4 * PBYTES;  // + barriers and exchange
 constexpr int THREADS = 320;
 constexpr int SOFTMAX_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 256;          // O [0,128), S0 [128,192), S1 [192,256)
 
-__device__ __forceinline__ bool visible(int64_t F, int i, int64_t r, int window, int causal) {
-  if (window && (F + i) - r >= window) return false;
-  if (causal && r >= F && (r - F) > i) return false;
-  return true;
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
 }
-
-// Two probabilities rounded to bf16 (packed), and the rounded values' sum.
-__device__ __forceinline__ uint32_t pack_p(float x0, float x1, float& sum) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  sum += hf.x + hf.y;
-  return *reinterpret_cast<const uint32_t*>(&h);
+// 2^x on the special-function unit (results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+// Two probabilities P = 2^(s k + c) of two scores s as bf16 pairs hi + lo
+// (hi the rounded P, lo the rounded remainder; returns hi, lo through `lo`);
+// P is added to the pair of partial sums.  The affine step, the remainder
+// and the sum run as packed two-lane fp32 instructions.
+__device__ __forceinline__ uint32_t p_pair(float s0, float s1, uint64_t k2, uint64_t c2, uint64_t& sum2, uint32_t& lo) {
+  uint64_t x;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(f2pack(s0, s1)), "l"(k2), "l"(c2));
+  const float2 e = f2unpack(x);
+  const float p0 = ex2(e.x), p1 = ex2(e.y);
+  const uint64_t pp = f2pack(p0, p1);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+  const uint32_t b = *reinterpret_cast<const uint32_t*>(&h);
+  uint64_t rr;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(rr) : "l"(pp), "l"(f2pack(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u))));
+  const float2 r = f2unpack(rr);
+  const __nv_bfloat162 l2 = __floats2bfloat162_rn(r.x, r.y);
+  lo = *reinterpret_cast<const uint32_t*>(&l2);
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(sum2) : "l"(pp));
+  return b;
 }
 
 // byte offset of 16-byte chunk c of row r inside a [rows][128 B] swizzled block
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Named barrier `id` over `count` threads that also ANDs a predicate over them.
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__ Q, const AttnItem* __restrict__ items,
                                                         SessTables tabs, AttnParams p, float* __restrict__ part,
@@ -80,8 +135,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + QBYTES;
   uint8_t* sV = sK + KST * KBYTES;
-  uint8_t* sP = sV + VST * VBYTES;  // [2 buffers]
-  uint64_t* k_full = (uint64_t*)(sP + 2 * PBYTES);
+  uint8_t* sP = sV + VST * VBYTES;  // [2 buffers][hi, lo]
+  uint64_t* k_full = (uint64_t*)(sP + 4 * PBYTES);
   uint64_t* k_empty = k_full + KST;
   uint64_t* v_full = k_empty + KST;
   uint64_t* v_empty = v_full + VST;
@@ -98,6 +153,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
 
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool dual = p.nrows * (p.Hq / p.Hkv) <= 64;
+  const int tile_threads = dual ? SOFTMAX_THREADS / 2 : SOFTMAX_THREADS;  // softmax threads per key tile
 
   if (tid == 0) {
     for (int s = 0; s < KST; ++s) {
@@ -110,8 +167,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], SOFTMAX_THREADS);
-      mbar_init(&p_full[b], SOFTMAX_THREADS);
+      mbar_init(&s_free[b], tile_threads);
+      mbar_init(&p_full[b], tile_threads);
       mbar_init(&pv_done[b], 1);
     }
     mbar_init(o_done, 1);
@@ -140,13 +197,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)vmap) : "memory");
   }
 
-  // ---- Q rows of this KV head, zero padded to 128, as the MMA's A tile
+  // ---- Q rows of this KV head, zero padded to 128 (two streams: rows 0..63
+  // twice), as the MMA's A tile
   if (warp < 8) {
     // all 8 loads of a thread are issued before the first store
     uint4 v[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int e = tid + SOFTMAX_THREADS * k, r = e >> 4, c = e & 15;
+      const int e = tid + SOFTMAX_THREADS * k, r = dual ? (e >> 4) & 63 : e >> 4, c = e & 15;
       v[k] = make_uint4(0, 0, 0, 0);
       if (r < R) {
         const int i = r / G, g = r % G;
@@ -158,6 +216,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     for (int k = 0; k < 8; ++k) {
       const int e = tid + SOFTMAX_THREADS * k, r = e >> 4, c = e & 15;
       *reinterpret_cast<uint4*>(sQ + (c >> 3) * (QBYTES / 2) + swz(r, c & 7)) = v[k];
+    }
+    if (dual) {  // the rows of each P buffer that belong to the other stream stay zero
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = tid + SOFTMAX_THREADS * k;  // 16-byte chunk, 0..1023
+        uint8_t* z = e < 512 ? sP + PBYTES / 2 + e * 16 : sP + 2 * PBYTES + (e - 512) * 16;
+        *reinterpret_cast<uint4*>(z) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(z + PBYTES) = make_uint4(0, 0, 0, 0);
+      }
     }
     fence_proxy_async();
   }
@@ -202,68 +269,87 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       }
     }
   } else if (warp == 9) {
-    if (lane == 0) {
-      // ---- MMA issuer
-      constexpr uint32_t idS = idesc_bf16(128, KT), idPV = idesc_bf16(128, D);
-      const uint32_t tO = tmem;
-      auto issue_pv = [&](int u) -> bool {
-        const int pb = u & 1, vs = u % VST;
-        if (!mbar_wait(&p_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag)) return false;
-        if (!mbar_wait(&v_full[vs], (uint32_t)(u / VST) & 1u, abort_flag)) return false;
-        fence_after();
-        const uint32_t ph = smem_u32(sP + pb * PBYTES), v0 = smem_u32(sV + vs * VBYTES);
+    // ---- MMA issuer: the whole warp runs the loop and takes every decision
+    // together (each lane waits on the barrier itself); one elected lane
+    // issues each MMA and commit, which queue without holding up the warp
+    constexpr uint32_t idS = idesc_bf16(128, KT), idPV = idesc_bf16(128, D);
+    const uint32_t tO = tmem;
+    auto issue_s = [&](int t) {
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + (t % KST) * KBYTES);
+      const uint32_t tS = tmem + 128 + (t & 1) * KT;
 #pragma unroll
-        for (int ks = 0; ks < KT / 16; ++ks)
-          umma_bf16(tO, sdesc_sw128(ph + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, (u > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&pv_done[pb]);
-        umma_commit(&v_empty[vs]);
-        return true;
-      };
-      bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
-        const int s = t % KST, sb = t & 1;
-        if (!mbar_wait(&k_full[s], (uint32_t)(t / KST) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (t >= 2 && !mbar_wait(&s_free[sb], (uint32_t)((t >> 1) - 1) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        fence_after();
-        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + s * KBYTES);
-        const uint32_t tS = tmem + 128 + sb * KT;
+      for (int ks = 0; ks < D / 16; ++ks)
+        umma_bf16_warp(tS, sdesc_sw128(q0 + (ks >> 2) * (QBYTES / 2) + (ks & 3) * 32),
+                       sdesc_sw128(k0 + (ks >> 2) * (KBYTES / 2) + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
+      umma_commit_warp(&s_full[t & 1]);
+      umma_commit_warp(&k_empty[t % KST]);  // the K stage is free once S(t) is done
+    };
+    auto issue_pv = [&](int u) {
+      const uint32_t ph = smem_u32(sP + (u & 1) * 2 * PBYTES), pl = ph + PBYTES, v0 = smem_u32(sV + (u % VST) * VBYTES);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma_bf16(tS, sdesc_sw128(q0 + (ks >> 2) * (QBYTES / 2) + (ks & 3) * 32),
-                    sdesc_sw128(k0 + (ks >> 2) * (KBYTES / 2) + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
-        umma_commit(&s_full[sb]);
-        umma_commit(&k_empty[s]);  // the K stage is free once S(t) is done
-        if (t >= 1) ok = issue_pv(t - 1);
+      for (int ks = 0; ks < KT / 16; ++ks)
+        umma_bf16_warp(tO, sdesc_sw128(ph + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, (u > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < KT / 16; ++ks) umma_bf16_warp(tO, sdesc_sw128(pl + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, 1u);
+      umma_commit_warp(&pv_done[u & 1]);
+      umma_commit_warp(&v_empty[u % VST]);
+    };
+    // S(t) as soon as K(t) has landed and the softmax has read S(t-2) out of
+    // the same TMEM buffer, P V(u) (in tile order) as soon as P(u) and V(u)
+    // are in place: S of a stream's next tile is computed while the stream
+    // still works on its current one.  A test counts only once every lane
+    // has seen the phase complete.
+    int ns = 0, np = 0;  // next S, next P V
+    bool ok = true;
+    uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 1; np < T; ++spin) {
+      if (ns < T && __all_sync(0xffffffffu, mbar_test_wait(&k_full[ns % KST], (uint32_t)(ns / KST) & 1u) &&
+                                                (ns < 2 || mbar_test_wait(&s_free[ns & 1], (uint32_t)((ns >> 1) - 1) & 1u)))) {
+        fence_after();
+        issue_s(ns++);
+        t0 = globaltimer_ns();
+        continue;
       }
-      if (ok && T > 0) ok = issue_pv(T - 1);
-      if (!ok) {
-        atomicOr(err, 8);
-        *abort_flag = 1;
+      if (np < ns && __all_sync(0xffffffffu, mbar_test_wait(&p_full[np & 1], (uint32_t)(np >> 1) & 1u) &&
+                                                 mbar_test_wait(&v_full[np % VST], (uint32_t)(np / VST) & 1u))) {
+        fence_after();
+        issue_pv(np++);
+        t0 = globaltimer_ns();
+        continue;
       }
-      umma_commit(o_done);  // arrives once every MMA issued above has completed
+      if ((spin & 63u) == 0 && __any_sync(0xffffffffu, *abort_flag != 0 || globaltimer_ns() - t0 > kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
     }
+    if (!ok) {
+      if (lane == 0) atomicOr(err, 8);
+      *abort_flag = 1;
+    }
+    umma_commit_warp(o_done);  // arrives once every MMA issued above has completed
   } else {
-    // ---- softmax: two threads per query row (row = TMEM lane)
+    // ---- softmax: two threads per TMEM row (row = TMEM lane)
     const int r = (warp & 3) * 32 + lane;
     const int half = warp >> 2;                // keys [32 half, +32) of a tile, O columns [64 half, +64)
-    const bool rv = r < R;
-    // a warp whose 32 rows are all padding (r >= R) computes nothing: the
+    const int stream = dual ? (warp & 3) >> 1 : 0;  // key tiles stream, stream + tstep, ...
+    const int tstep = dual ? 2 : 1;
+    const int qr = r - 64 * stream;            // the query row this TMEM row holds
+    const bool rv = qr < R;
+    // warps w and w + 4 share their rows: the per-tile exchange is a barrier
+    // of the pair alone, and it also makes the pair's decision to stop on an
+    // expired wait a common one, so the two always meet the same barriers
+    const int pair_bar = 1 + (warp & 3);
+    // a warp whose 32 rows are all padding (qr >= R) computes nothing: the
     // P rows it would write only meet O rows that are never read.  It keeps
     // the barrier protocol (one arrival per tile on s_free and p_full, the
-    // per-tile exchange barrier), so no phase runs ahead of the others.
-    const bool live = (warp & 3) * 32 < R;
+    // pair barrier), so no phase runs ahead of the others.
+    const bool live = (warp & 3) * 32 - 64 * stream < R;
     const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale * 1.4426950408889634f;
     // the row's visible key positions form one interval [vlo, vhi]
     int64_t vlo = it.k0, vhi = it.k1 - 1;
     if (rv) {
-      const int64_t qpos = F + r / G;
+      const int64_t qpos = F + qr / G;
       if (p.window) vlo = vlo > qpos - p.window + 1 ? vlo : qpos - p.window + 1;
       if (p.causal) vhi = vhi < qpos ? vhi : qpos;
     } else {
@@ -272,54 +358,65 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     }
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
+    for (int t = stream; t < T; t += tstep) {
       const int sb = t & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, abort_flag));
-      if (!ok) break;
-      if (!live) {
+      bool w = ok && __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)(t >> 1) & 1u, abort_flag));
+      float s[32], mt = -INFINITY;
+      if (w) {
+        if (live) {
+          fence_after();
+          tmem_ld32(tmem + lrow + 128 + sb * KT + 32 * half, s);
+          fence_before();
+        }
         mbar_arrive(&s_free[sb]);
-        asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
-        mbar_arrive(&p_full[t & 1]);
+      }
+      if (w && live) {
+        const int64_t kt = it.k0 + (int64_t)t * KT + 32 * half;
+        const int64_t lo64 = vlo - kt, hi64 = vhi - kt;
+        const int lo = lo64 < 0 ? 0 : (lo64 > 32 ? 32 : (int)lo64);
+        const int hi = hi64 < -1 ? -1 : (hi64 > 31 ? 31 : (int)hi64);
+        // the max of the raw scores (the scale is positive): the scale
+        // folds into the exponent below
+        if (!__all_sync(0xffffffffu, lo == 0 && hi == 31)) {
+          // keys outside the row's visible range (a window, the causal
+          // block, the end of the range); without them (the common case)
+          // the half-tile needs no mask
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] = (j >= lo && j <= hi) ? s[j] : -INFINITY;
+        }
+        float m0 = fmaxf(s[0], s[1]), m1 = fmaxf(s[2], s[3]);
+#pragma unroll
+        for (int j = 4; j < 32; j += 4) {
+          m0 = max3(m0, s[j], s[j + 1]);
+          m1 = max3(m1, s[j + 2], s[j + 3]);
+        }
+        mt = fmaxf(m0, m1);
+      }
+      // both threads of a row agree on the tile max (a buffer per parity of
+      // the stream's own tile count: a value is read before it is rewritten)
+      float* xt = xch + ((dual ? t >> 1 : t) & 1) * 256;
+      xt[half * 128 + r] = mt;
+      if (!bar_and(pair_bar, 64, w)) {
+        ok = false;
+        break;
+      }
+      if (!live) {
+        mbar_arrive(&p_full[sb]);
         continue;
       }
-      fence_after();
-      float s[32];
-      tmem_ld32(tmem + lrow + 128 + sb * KT + 32 * half, s);
-      fence_before();
-      mbar_arrive(&s_free[sb]);
-      const int64_t kt = it.k0 + (int64_t)t * KT + 32 * half;
-      const int64_t lo64 = vlo - kt, hi64 = vhi - kt;
-      const int lo = lo64 < 0 ? 0 : (lo64 > 32 ? 32 : (int)lo64);
-      const int hi = hi64 < -1 ? -1 : (hi64 > 31 ? 31 : (int)hi64);
-      float mt = -INFINITY;
-      if (__all_sync(0xffffffffu, lo == 0 && hi == 31)) {
-        // every key of this half-tile is visible to every row of the warp
-        // (the common case without a window): no mask to apply
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          s[j] *= sl2;
-          mt = fmaxf(mt, s[j]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          s[j] = (j >= lo && j <= hi) ? s[j] * sl2 : -INFINITY;
-          mt = fmaxf(mt, s[j]);
-        }
-      }
-      // both threads of a row agree on the tile max
-      float* xt = xch + (t & 1) * 256;
-      xt[half * 128 + r] = mt;
-      asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
-      mt = fmaxf(mt, xt[(half ^ 1) * 128 + r]);
+      mt = fmaxf(mt, xt[(half ^ 1) * 128 + r]) * sl2;  // the exp2 domain
       // lazy rescale: move the reference max only when it grows past 2^8
       const bool grow = mt > m_used + 8.f;
       const float m_new = grow ? mt : m_used;
       const float f = (grow && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
       if (__any_sync(0xffffffffu, f != 1.f)) {
-        // O must hold every earlier tile's product before it is scaled
-        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag));
-        if (!ok) break;
+        // O must hold every earlier tile's product before it is scaled (with
+        // two streams the later products cannot be in flight either: P V of
+        // tile t + 1 is issued only after P of tile t, which waits on this)
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
+          ok = false;  // the pair stops together at the next tile's barrier
+          continue;
+        }
         fence_after();
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
@@ -332,28 +429,32 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       }
       l *= f;
       m_used = m_new;
-      uint32_t hi2[16];
-      float ls = 0.f;
+      uint32_t hi2[16], lo2[16];
       // while a row has seen no visible key its max is -inf and every score
       // is -inf too: exponentiate against 0 so that P = exp2(-inf) = 0
       const float mref = m_used == -INFINITY ? 0.f : m_used;
+      const uint64_t k2 = f2pack(sl2, sl2), c2 = f2pack(-mref, -mref);
+      uint64_t ls2 = f2pack(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) hi2[j / 2] = pack_p(exp2f(s[j] - mref), exp2f(s[j + 1] - mref), ls);
-      l += ls;
-      const int pb = t & 1;
+      for (int j = 0; j < 32; j += 2) hi2[j / 2] = p_pair(s[j], s[j + 1], k2, c2, ls2, lo2[j / 2]);
+      const float2 ls = f2unpack(ls2);
+      l += ls.x + ls.y;
       if (t >= 2) {  // the P buffer is free once the product of tile t-2 is done
-        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[pb], (uint32_t)((t >> 1) - 1) & 1u, abort_flag));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[sb], (uint32_t)((t >> 1) - 1) & 1u, abort_flag))) {
+          ok = false;
+          continue;
+        }
       }
-      uint8_t* ph = sP + pb * PBYTES;
+      uint8_t* ph = sP + sb * 2 * PBYTES;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int cc = 4 * half + c;
         *reinterpret_cast<uint4*>(ph + swz(r, cc)) = make_uint4(hi2[4 * c], hi2[4 * c + 1], hi2[4 * c + 2], hi2[4 * c + 3]);
+        *reinterpret_cast<uint4*>(ph + PBYTES + swz(r, cc)) = make_uint4(lo2[4 * c], lo2[4 * c + 1], lo2[4 * c + 2], lo2[4 * c + 3]);
       }
       fence_proxy_async();
       fence_before();
-      mbar_arrive(&p_full[pb]);
+      mbar_arrive(&p_full[sb]);
     }
     if (!ok) {
       atomicOr(err, 8);
@@ -364,19 +465,52 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     fence_after();
     float* xl = xch + 2 * 256;
     xl[half * 128 + r] = l;
-    asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
+    bar_and(pair_bar, 64, true);
+    float lsum = xl[r] + xl[128 + r], we = 1.f, wo = 0.f;
+    // two streams: the odd stream's rows go through idle V stages (every
+    // copy has landed and every MMA has completed) to the even stream's
+    float* xo = reinterpret_cast<float*>(sV + 3 * VBYTES) + (rv ? qr : 0) * (D + 4);
+    if (dual) {
+      if (stream == 1 && live) {
+        if (rv && half == 0) *reinterpret_cast<float2*>(xo) = make_float2(m_used, lsum);
+#pragma unroll 1
+        for (int c = 64 * half; c < 64 * half + 64; c += 32) {
+          float o[32];
+          tmem_ld32(tmem + lrow + c, o);
+          if (rv) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(xo + 4 + c + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+          }
+        }
+      }
+      // warps of quarters q and q + 2 (and their partners) hold the same query rows
+      bar_and(5 + (warp & 1), 128, true);
+      if (stream == 0 && rv) {
+        const float2 mo = *reinterpret_cast<const float2*>(xo);
+        const float M = fmaxf(m_used, mo.x);
+        we = m_used == -INFINITY ? 0.f : exp2f(m_used - M);
+        wo = mo.x == -INFINITY ? 0.f : exp2f(mo.x - M);
+        lsum = lsum * we + mo.y * wo;
+        m_used = M;
+      }
+    }
     // the partial goes to global memory, or (clustered) to this CTA's idle K/V stages
-    float* pr = p.cluster > 1 ? reinterpret_cast<float*>(sK) + (rv ? r : 0) * (D + 4)
-                              : part + ((int64_t)blockIdx.x * R + (rv ? r : 0)) * (D + 4);
-    if (rv && half == 0) {
-      *reinterpret_cast<float4*>(pr) = make_float4(m_used == -INFINITY ? -INFINITY : m_used * 0.6931471805599453f,
-                                                   xl[r] + xl[128 + r], 0.f, 0.f);
+    float* pr = p.cluster > 1 ? reinterpret_cast<float*>(sK) + (rv ? qr : 0) * (D + 4)
+                              : part + ((int64_t)blockIdx.x * R + (rv ? qr : 0)) * (D + 4);
+    if (stream == 0 && rv && half == 0) {
+      *reinterpret_cast<float4*>(pr) =
+          make_float4(m_used == -INFINITY ? -INFINITY : m_used * 0.6931471805599453f, lsum, 0.f, 0.f);
     }
 #pragma unroll 1
-    for (int c = 64 * half; c < 64 * half + 64 && live; c += 32) {
+    for (int c = 64 * half; c < 64 * half + 64 && live && stream == 0; c += 32) {
       float o[32];
       tmem_ld32(tmem + lrow + c, o);
       if (rv) {
+        if (dual) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = o[j] * we + xo[4 + c + j] * wo;
+        }
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           *reinterpret_cast<float4*>(pr + 4 + c + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);

@@ -355,6 +355,48 @@ def test_windowed_rounds_follow_the_oracle(D, block):
     D.dflash_close(s)
 
 
+@pytest.mark.parametrize("block", [12, 16, 24, 32])
+def test_query_row_counts_and_key_tile_counts(D, block):
+    """The tensor-core attention runs one softmax stream over 128 TMEM rows
+    when a KV head's query rows (block x group) exceed 64, and two streams
+    (even and odd key tiles) when they fit in 64.  Blocks of 12, 16, 24 and
+    32 rows with groups of 4 give 48, 64, 96 and 128 query rows.  76
+    sessions x 2 KV heads fill one wave of work items, so each item takes a
+    session's whole key range: contexts of 20, 40, 663 and 700 rows give one
+    key tile (the odd stream idle), two, an odd count and an even count."""
+    cfg = S.CONFIGS["small_bf16"].replace(block_size=block)
+    p = Pair(cfg)
+    n, V = block - 1, cfg.vocab
+    ctxs = [20, 40, 663, 700]
+    B = 76
+    feats = [p.feats(L, seed=31 + i) for i, L in enumerate(ctxs)]
+    sess = []
+    for b in range(B):
+        f_np, f = feats[b % 4]
+        s = D.dflash_open(p.model, max_ctx=1024)
+        D.dflash_committed(s, f, 0)
+        sess.append(s)
+    cur_np = np.array([9 + b % 4 for b in range(B)], dtype=np.int32)
+    refs = [_oracle_session(p, f_np).propose(int(cur_np[i]), n, 1.0, 8, 0)["logits"]
+            for i, (f_np, _) in enumerate(feats)]
+    tok = torch.empty((B, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((B, n), dtype=torch.float32, device="cuda")
+    lg = torch.empty((B, n, V), dtype=torch.float32, device="cuda")
+    assert D.dflash_propose(sess, torch.from_numpy(cur_np).cuda(), n, 1.0, 8, 0, tok, q, lg) == [n] * B
+    torch.cuda.synchronize()
+    g_lg = lg.double().cpu().numpy()
+    g_tok = tok.cpu().numpy()
+    assert np.all(np.isfinite(g_lg))
+    for b in range(B):
+        ref = refs[b % 4]
+        err = np.max(np.abs(g_lg[b] - ref))
+        assert err <= TOL_LOGITS["bf16"], (b, err)
+        check_tokens_for(cfg, g_tok[b], g_lg[b], ref, 1.0, 8, 0, b)
+    D.dflash_device_status(p.model)
+    for s in sess:
+        D.dflash_close(s)
+
+
 @pytest.mark.parametrize("intermediate", [1024, 12288])
 def test_rows_do_not_depend_on_the_batch(D, intermediate):
     """A session's block logits are bit-identical whether it proposes alone
