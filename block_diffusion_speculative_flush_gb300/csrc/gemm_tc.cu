@@ -381,14 +381,17 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer ----
+  } else if (warp == 1) {
+    // ---- MMA issuer: the whole warp runs the loop (every lane waits on the
+    // barriers itself, decisions are taken together) and one elected lane
+    // issues, so the MMAs queue without holding the warp up ----
     constexpr uint32_t idesc = idesc_bf16(BM, BN);
     int it = 0, j = 0;
     bool ok = true;
     for_each_unit<PERSIST>(p, [&](int, int s) {
       const int b = PERSIST ? (j & 1) : 0;
-      if (PERSIST && j >= 2 && !mbar_wait(&acce[b], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+      if (PERSIST && j >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&acce[b], (uint32_t)((j >> 1) - 1) & 1u, abort_flag))) {
         ok = false;
         return false;
       }
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
       split_range(p, s, kb0, kb1);
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         const int st = it % STAGES;
-        if (!mbar_wait(&full[st], (uint32_t)(it / STAGES) & 1u, abort_flag)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (uint32_t)(it / STAGES) & 1u, abort_flag))) {
           ok = false;
           return false;
         }
@@ -406,17 +409,17 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
         const uint32_t a0 = smem_u32(sA + st * A_BYTES), b0 = smem_u32(sB + st * B_BYTES);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
-          umma_bf16(d, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-        umma_commit(&empty[st]);
+          umma_bf16_warp(d, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        umma_commit_warp(&empty[st]);
       }
-      umma_commit(&accf[b]);  // arrives once every MMA of this split has completed
+      umma_commit_warp(&accf[b]);  // arrives once every MMA of this split has completed
       ++j;
       return true;
     });
     if (!ok) {
-      atomicOr(p.err, kErrBit);
+      if (lane == 0) atomicOr(p.err, kErrBit);
       *abort_flag = 1;
-      umma_commit(drain);
+      umma_commit_warp(drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
