@@ -757,7 +757,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     m->launches += 2;
     ST_TRY(launch_check("penalties"));
   }
-  const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
+  const int chunk = sample_chunk(Rz, V, m->num_sms), chunks = (V + chunk - 1) / chunk;
   ST_TRY(m->spart.ensure((size_t)Rz * chunks * sizeof(float4), st));
   ST_TRY(m->vstat.ensure((size_t)Rz * 8, st));
   SampleArgs sa{};
@@ -1405,7 +1405,7 @@ int dflash_verify(dflash_session* const* s, int32_t batch, const void* target_lo
   }
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
-  const int chunk = 4096, chunks = (V + chunk - 1) / chunk;
+  const int chunk = sample_chunk(rows, V, m->num_sms), chunks = (V + chunk - 1) / chunk;
   ST_TRY(m->vpart.ensure((size_t)rows * chunks * sizeof(float4), st));
   ST_TRY(m->vstat.ensure((size_t)rows * 8, st));
   int32_t* amax = m->vstat.as<int32_t>();

@@ -150,6 +150,15 @@ constexpr int kTruncMaxK = 1024;
 // sess_cut[b][row % rows_per_seq] when given.
 void launch_trunc_cut(const SampleArgs& a, const Trunc* tr, uint64_t* cut, uint64_t* const* sess_cut,
                       cudaStream_t st);
+// Vocabulary entries per CTA of the sampling partials: 16384 when the rows
+// give every SM at least eight such CTAs (the per-CTA merge then costs less
+// next to the entries), else 4096 so that a few rows still spread over the
+// SMs.  Both are multiples of 1024.
+constexpr int kSampleChunkSmall = 4096, kSampleChunkLarge = 16384;
+inline int sample_chunk(int64_t rows, int V, int num_sms) {
+  const int64_t big = rows * ((V + kSampleChunkLarge - 1) / kSampleChunkLarge);
+  return big >= 8 * (int64_t)num_sms ? kSampleChunkLarge : kSampleChunkSmall;
+}
 void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st);
 // Writes tok[row], q[row] (probability of the token at T), lse[row] (log-sum-exp of logits/T).
 void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, int32_t* tok, float* qtok,

@@ -833,12 +833,12 @@ __global__ void __launch_bounds__(256, 4) k_sample_partials(SampleArgs a, int ch
 #pragma unroll
       for (int it = 0; it < kSampleSteps; ++it)
 #pragma unroll
-        for (int w = 0; w < 4; ++w) ls += expf(x[it][w] - ms);
+        for (int w = 0; w < 4; ++w) ls += __expf(x[it][w] - ms);
       if (ms > m) {
-        l = (m == -INFINITY ? 0.f : l * expf(m - ms)) + ls;
+        l = (m == -INFINITY ? 0.f : l * __expf(m - ms)) + ls;
         m = ms;
       } else {
-        l += ls * expf(ms - m);
+        l += ls * __expf(ms - m);
       }
     }
 #pragma unroll
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(256, 4) k_sample_partials(SampleArgs a, int ch
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
     const float M = fmaxf(m, m2);
-    l = (m == -INFINITY ? 0.f : l * expf(m - M)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - M));
+    l = (m == -INFINITY ? 0.f : l * __expf(m - M)) + (m2 == -INFINITY ? 0.f : l2 * __expf(m2 - M));
     m = M;
   }
   best = warp_argmax(best);
@@ -882,7 +882,7 @@ __global__ void __launch_bounds__(256, 4) k_sample_partials(SampleArgs a, int ch
     float L = 0.f;
     ArgMax bb{-INFINITY, INT32_MAX};
     for (int i = 0; i < nw; ++i) {
-      if (sm_m[i] != -INFINITY) L += sm_l[i] * expf(sm_m[i] - M);
+      if (sm_m[i] != -INFINITY) L += sm_l[i] * __expf(sm_m[i] - M);
       bb = better(bb, ArgMax{sm_s[i], sm_i[i]});
     }
     part[(int64_t)row * nch + c] = make_float4(M, L, bb.v, __int_as_float(bb.i));

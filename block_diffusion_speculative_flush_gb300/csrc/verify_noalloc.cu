@@ -43,12 +43,12 @@ namespace {
 
 // Size of the static scratch: 4 MiB.  It holds, per call, the per-session
 // pointer tables (at most kMaxBatch sessions), the row statistics of the
-// batch * (n + 1) target rows (one float4 partial per 4096-entry vocabulary
-// chunk, then log-sum-exp and argmax) and the bonus-draw partials.
+// batch * (n + 1) target rows (one float4 partial per vocabulary chunk of
+// the sampling partials, then log-sum-exp and argmax) and the bonus-draw
+// partials.
 constexpr size_t kScratchBytes = 4u << 20;
 constexpr int kMaxBatch = 128;
 constexpr int kMaxDevices = 64;
-constexpr int kChunk = 4096;
 
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
@@ -157,7 +157,10 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
 
   // scratch layout
   const int rows = batch * (n + 1);
-  const int chunks = (V + kChunk - 1) / kChunk;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dflash__session_device(s[0])) != cudaSuccess)
+    return dflash__set_error(DFLASH_ERR_CUDA, "cannot read the sessions' device");
+  const int chunk = sample_chunk(rows, V, sms), chunks = (V + chunk - 1) / chunk;
   size_t off = 0;
   const size_t o_dl = off;
   off = up16(off + batch * sizeof(void*));
@@ -254,7 +257,7 @@ extern "C" DFLASH_API int dflash_verify_noalloc(dflash_session* const* s, int32_
     launch_trunc_cut(sa, (const Trunc*)(base + o_trunc), (uint64_t*)(base + o_cut), nullptr, st);
     sa.cut = (const uint64_t*)(base + o_cut);
   }
-  launch_sample_partials(sa, kChunk, part, st);
+  launch_sample_partials(sa, chunk, part, st);
   launch_sample_combine(sa, chunks, part, amax, nullptr, lse, st);
   VerifyArgs va{};
   va.target = target_logits;
