@@ -604,9 +604,10 @@ def run_workload(args, rank, world, local_rank):
         acc = torch.empty(B, dtype=torch.int32, device=dev)
         bon = torch.empty(B, dtype=torch.int32, device=dev)
 
+    feat_list = [feats[b] for b in range(B)]
+
     def step(i):
-        for b, s_ in enumerate(sess):
-            D.dflash_committed(s_, feats[b], int(ctxs[b]) + P_ROWS * i)
+        D.dflash_committed_batch(sess, feat_list, [int(c) + P_ROWS * i for c in ctxs])
         D.dflash_propose(sess, cur, n, Tb, SEED, i, tok, q)
         D.dflash_verify(sess, tl, tok, n, Tb, SEED, i, acc, bon)
 

@@ -1212,6 +1212,10 @@ int dflash_committed_batch(dflash_session* const* s, int32_t batch, const void* 
   Forward fw;
   std::vector<int64_t> F0(batch);
   std::vector<int32_t> P0(batch);
+  // the staged rows of every session go in one launch per kMaxRowCopies sessions
+  RowCopies cp;
+  cp.n = 0;
+  cp.row_bytes = width * (int64_t)es;
   for (int b = 0; b < batch; ++b) {
     dflash_session* x = s[b];
     F0[b] = x->F;
@@ -1223,8 +1227,15 @@ int dflash_committed_batch(dflash_session* const* s, int32_t batch, const void* 
     for (int k = 0; k < c.n_taps; ++k)
       src[k] = (const char*)features[b] + ((size_t)start * row_stride + (size_t)k * c.target_hidden) * es;
     if (x->P + add < DFLASH_PENDING_FLUSH_TOKENS) {
-      launch_copy_rows((char*)x->pending + (size_t)x->P * width * es, (int64_t)(width * es), src[0],
-                       row_stride * (int64_t)es, (int64_t)(width * es), add, s[0]->stream);
+      if (cp.n == kMaxRowCopies) {
+        launch_copy_rows_batch(cp, s[0]->stream);
+        cp.n = 0;
+      }
+      cp.dst[cp.n] = (char*)x->pending + (size_t)x->P * width * es;
+      cp.src[cp.n] = src[0];
+      cp.src_ld[cp.n] = row_stride * (int64_t)es;
+      cp.rows[cp.n] = add;
+      ++cp.n;
       x->P += add;
       continue;
     }
@@ -1235,6 +1246,7 @@ int dflash_committed_batch(dflash_session* const* s, int32_t batch, const void* 
     fw.sess.push_back(x);
     take_pending(x, j, src, row_stride * (int64_t)es, add, fw.ctx);
   }
+  launch_copy_rows_batch(cp, s[0]->stream);
   int rc = launch_check("pending rows");
   if (rc == DFLASH_OK && !fw.sess.empty()) rc = run_forward(m, fw, s[0]->stream);
   if (rc != DFLASH_OK) {

@@ -284,6 +284,19 @@ struct TapSrc {
 void launch_copy_taps(void* dst, int64_t dst_ld, const TapSrc& src, int K, int64_t src_ld, int64_t tap_bytes, int rows,
                       cudaStream_t st);
 // rows x row_bytes from src (row stride src_ld bytes) to dst (dst_ld bytes), as a kernel.
+// Several row copies in one launch: copy i moves rows[i] rows of row_bytes
+// bytes from src[i] (rows src_ld[i] bytes apart) to dst[i] (rows packed).
+// The table travels as the kernel's parameter.
+constexpr int kMaxRowCopies = 128;
+struct RowCopies {
+  char* dst[kMaxRowCopies];
+  const char* src[kMaxRowCopies];
+  int64_t src_ld[kMaxRowCopies];
+  int32_t rows[kMaxRowCopies];
+  int32_t n;
+  int64_t row_bytes;
+};
+void launch_copy_rows_batch(const RowCopies& t, cudaStream_t st);
 void launch_copy_rows(void* dst, int64_t dst_ld, const void* src, int64_t src_ld, int64_t row_bytes, int rows,
                       cudaStream_t st);
 

@@ -1431,6 +1431,30 @@ __global__ void k_copy_rows(char* __restrict__ dst, int64_t dst_ld, const char* 
   }
 }
 
+// Copy blockIdx.y of the table; its rows split over blockIdx.x, 16 bytes a
+// thread when every address and length allows it.
+__global__ void k_copy_rows_batch(RowCopies t, int vec) {
+  pdl_trigger();
+  pdl_wait();
+  const int i = blockIdx.y;
+  const int64_t total = (int64_t)t.rows[i] * t.row_bytes;
+  char* d = t.dst[i];
+  const char* s = t.src[i];
+  const int64_t ld = t.src_ld[i];
+  if (vec) {
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 16; b < total;
+         b += (int64_t)gridDim.x * blockDim.x * 16) {
+      const int64_t r = b / t.row_bytes, c = b - r * t.row_bytes;
+      *reinterpret_cast<uint4*>(d + b) = *reinterpret_cast<const uint4*>(s + r * ld + c);
+    }
+  } else {
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total; b += (int64_t)gridDim.x * blockDim.x) {
+      const int64_t r = b / t.row_bytes, c = b - r * t.row_bytes;
+      d[b] = s[r * ld + c];
+    }
+  }
+}
+
 // Row r of tap k (rows src_ld bytes apart from src.p[k]) to dst + r * dst_ld
 // + k * tap_bytes: K separate tap buffers into concatenated feature rows.
 __global__ void k_copy_taps(char* __restrict__ dst, int64_t dst_ld, TapSrc src, int64_t src_ld, int64_t tap_bytes,
@@ -1782,6 +1806,18 @@ void launch_copy_rows(void* dst, int64_t dst_ld, const void* src, int64_t src_ld
   const int vec = ((uintptr_t)dst | (uintptr_t)src | (uintptr_t)dst_ld | (uintptr_t)src_ld | (uintptr_t)row_bytes) % 16 == 0;
   launch_k(k_copy_rows, dim3(rows, (unsigned)cdiv(row_bytes, 4096)), 256, 0, st, (char*)dst, dst_ld, (const char*)src,
            src_ld, row_bytes, vec);
+}
+
+void launch_copy_rows_batch(const RowCopies& t, cudaStream_t st) {
+  if (t.n <= 0) return;
+  int vec = t.row_bytes % 16 == 0;
+  int64_t most = 0;
+  for (int i = 0; i < t.n; ++i) {
+    vec = vec && ((uintptr_t)t.dst[i] | (uintptr_t)t.src[i] | (uint64_t)t.src_ld[i]) % 16 == 0;
+    most = std::max<int64_t>(most, (int64_t)t.rows[i] * t.row_bytes);
+  }
+  const unsigned bx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, cdiv(most, 256 * 16 * 4)));
+  launch_k(k_copy_rows_batch, dim3(bx, (unsigned)t.n), 256, 0, st, t, vec);
 }
 
 void launch_copy_taps(void* dst, int64_t dst_ld, const TapSrc& src, int K, int64_t src_ld, int64_t tap_bytes, int rows,

@@ -641,6 +641,17 @@ def test_committed_batch_flushes_together_and_equals_single_commits(D):
             ka, va = export_kv(D, a, cfg, l, offs[j], F_ - offs[j])
             kb, vb = export_kv(D, b, cfg, l, offs[j], F_ - offs[j])
             assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    # the staged rows (one batched copy for all staged sessions) flush to the
+    # same caches as the rows each dflash_committed staged
+    D.dflash_flush(single)
+    D.dflash_flush(batch)
+    for j, (a, b) in enumerate(zip(single, batch)):
+        F_, P_, _ = D.dflash_session_state(a)
+        assert D.dflash_session_state(b) == (F_, P_, _) and P_ == 0
+        for l in (0, cfg.n_layers - 1):
+            ka, va = export_kv(D, a, cfg, l, offs[j], F_ - offs[j])
+            kb, vb = export_kv(D, b, cfg, l, offs[j], F_ - offs[j])
+            assert np.array_equal(ka, kb) and np.array_equal(va, vb)
     # the flushed rows equal the oracle's
     o = O.OracleSession(p.oracle, restored_offset=offs[0])
     o.committed(f_np[:256], offs[0])
