@@ -49,6 +49,7 @@ CTX = 4096
 P_ROWS = 4
 TEMP = 1.0
 SEED = 20260201
+PROFILE_RANGE = False   # --profile-range
 
 
 def parse_args(argv=None):
@@ -58,6 +59,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="batched only: the same serving mix with one draft layer and a 32000-entry "
+                         "vocabulary (about 3 GB on the device), a case small enough for a full ncu capture")
+    ap.add_argument("--profile-range", action="store_true",
+                    help="bracket every timed region with cudaProfilerStart/Stop, so that "
+                         "`ncu --profile-from-start off` captures the timed steps only")
     ap.add_argument("--workload", choices=["round", "flush", "laguna", "batched", "spec", "truncated"],
                     default="round",
                     help="round: the bs1 Qwen3-8B-shaped round (the default line); flush: 8 sequences x 256-row "
@@ -272,12 +279,14 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    _profile_range(torch, True)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(W, W + K):
             step(sa, i, feats[i], tl)
         e1.record(stream)
     torch.cuda.synchronize()
+    _profile_range(torch, False)
     barrier(world)
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
@@ -397,6 +406,11 @@ def run_ours(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 # further workloads (one JSON line each; the default line is the round above)
 # ---------------------------------------------------------------------------
+def _profile_range(torch, on):
+    if PROFILE_RANGE:
+        (torch.cuda.profiler.start if on else torch.cuda.profiler.stop)()
+
+
 def _timed(torch, stream, fn, K, W, local_rank, world, dev):
     with torch.cuda.stream(stream):
         for i in range(W):
@@ -408,12 +422,14 @@ def _timed(torch, stream, fn, K, W, local_rank, world, dev):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    _profile_range(torch, True)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(W, W + K):
             fn(i)
         e1.record(stream)
     torch.cuda.synchronize()
+    _profile_range(torch, False)
     barrier(world)
     clk = clocks.stop()
     return max_over_ranks(e0.elapsed_time(e1), world, dev), clk
@@ -582,6 +598,8 @@ def run_workload(args, rank, world, local_rank):
 
     # batched serving mix
     cfg = S.CONFIGS[CFG_NAME]
+    if args.small:
+        cfg = cfg.replace(n_layers=1, vocab=32000, mask_token=31999)
     B, n, Tb = 64, cfg.block_size - 1, 0.7
     ctxs = np.random.default_rng(0).integers(1024, 16385, size=B)
     model = D.dflash_model_create(cfg, gpu_weights(cfg, SEED + rank, dev))
@@ -625,7 +643,8 @@ def run_workload(args, rank, world, local_rank):
     D.dflash_device_status(model)
     for s_ in sess:
         D.dflash_close(s_)
-    return _line("proposed tok/s (bs64 serving mix, Qwen3-8B-shaped draft, block 16, ctx 1k-16k)", "proposed tok/s",
+    shape = "Qwen3-8B-shaped draft" if not args.small else "Qwen3-8B-shaped draft cut to 1 layer and V 32000 (--small)"
+    return _line(f"proposed tok/s (bs64 serving mix, {shape}, block 16, ctx 1k-16k)", "proposed tok/s",
                  world * B * n / t_step, world, K, W, ms, "bf16",
                  {"workload": "64 sequences, contexts uniform 1k-16k (seeded K/V), 4 committed rows each per round, "
                               "batched propose + rejection-sampling verify at T=0.7 on N(0,3) target logits "
@@ -1041,7 +1060,9 @@ def run_reference(args, rank, world):
 
 
 def main(argv=None):
+    global PROFILE_RANGE
     args = parse_args(argv)
+    PROFILE_RANGE = args.profile_range
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
