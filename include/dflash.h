@@ -344,13 +344,14 @@ DFLASH_API int dflash_verify(dflash_session* const* s /*host [batch]*/, int32_t 
  * cudaFree or an allocating routine.  Its scratch is a 4 MiB array inside the
  * library image, present on every GPU that loads the library until the
  * process exits.  Limits: at most 128 sessions per call, and
- * batch * (n + 1) * ceil(V / 4096) 16-byte row partials plus the bonus
- * partials must fit the 4 MiB (about 200k partials); larger calls return
- * DFLASH_ERR_CAPACITY and change nothing.  The call runs on the device the
- * sessions were opened on: it makes that device current for its duration and
- * restores the caller's afterwards.  The first call on a device looks up the
- * scratch's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  The per-session tables
+ * batch * (n + 1) * ceil(V / chunk) 16-byte row partials (chunk = 16384 when
+ * the call's target rows give every SM of the device eight such chunks, else
+ * 4096) plus the bonus partials must fit the 4 MiB (about 200k partials);
+ * larger calls return DFLASH_ERR_CAPACITY and change nothing.  The call runs
+ * on the device the sessions were opened on: it makes that device current for
+ * its duration and restores the caller's afterwards.  The first call on a
+ * device looks up the scratch's device address (cudaGetSymbolAddress) with
+ * that device current.  The per-session tables
  * travel as a kernel parameter, so the call does not wait for the stream.
  * Every call shares the one scratch area and leaves its contents there, so
  * calls that overlap on the GPU (different streams, no ordering between
