@@ -10,8 +10,8 @@ import synthetic as S
 from oracle import dflash_oracle as O
 from oracle.target_oracle import OracleTarget
 from synthetic.target import TARGET_TINY, make_target_weights
-from tests.gpu_util import (TOL_LOGITS, TOL_Q, Pair, assert_cache_close, check_tokens_for, export_kv, lib,
-                            verify_parity)
+from tests.gpu_util import (TOL_LOGITS, TOL_Q, Pair, assert_cache_close, check_tokens, check_tokens_for, export_kv,
+                            lib, verify_parity)
 
 pytestmark = pytest.mark.gpu
 
@@ -395,6 +395,61 @@ def test_query_row_counts_and_key_tile_counts(D, block):
     D.dflash_device_status(p.model)
     for s in sess:
         D.dflash_close(s)
+
+
+@pytest.mark.parametrize("T", [0.0, 0.8])
+def test_batched_draw_on_a_32000_entry_vocabulary(D, T):
+    """A batch of many rows over a 32000-entry vocabulary: the unembedding
+    runs on 256-wide persistent tiles and the draw on 4096-entry chunks.  On
+    the GPU's own logits every token is the oracle's Gumbel-max (or argmax)
+    decision, q(token) is the oracle's softmax at the token, and verify
+    against the kept log-sum-exp follows the oracle's verify; the block
+    logits also follow the oracle's."""
+    cfg = S.CONFIGS["small_bf16"].replace(vocab=32000, mask_token=31999)
+    p = Pair(cfg)
+    n, V, B = cfg.block_size - 1, cfg.vocab, 12
+    sess, refs = [], []
+    for b in range(B):
+        f_np, f = p.feats(30 + 7 * b, seed=60 + b)
+        s = D.dflash_open(p.model, max_ctx=512)
+        D.dflash_committed(s, f, 0)
+        sess.append(s)
+        if b < 2:
+            o = O.OracleSession(p.oracle, seq=b)
+            o.committed(f_np, 0)
+            refs.append(o)
+    cur_np = (np.arange(B, dtype=np.int32) * 131) % V
+    tok = torch.empty((B, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((B, n), dtype=torch.float32, device="cuda")
+    lg = torch.empty((B, n, V), dtype=torch.float32, device="cuda")
+    assert D.dflash_propose(sess, torch.from_numpy(cur_np).cuda(), n, T, 41, 3, tok, q, lg) == [n] * B
+    torch.cuda.synchronize()
+    g_lg, g_tok, g_q = lg.double().cpu().numpy(), tok.cpu().numpy(), q.double().cpu().numpy()
+    for b in range(B):
+        check_tokens(g_tok[b], g_lg[b], T, 41, 3, b)
+        if T > 0:
+            for i in range(n):
+                want = O.softmax(g_lg[b, i] / T)[g_tok[b, i]]
+                assert abs(g_q[b, i] - want) <= 1e-5 * want + 1e-9, (b, i, g_q[b, i], want)
+        else:
+            assert np.all(g_q[b] == 1.0)
+    for b, o in enumerate(refs):
+        ref = o.propose(int(cur_np[b]), n, T, 41, 3)
+        assert np.max(np.abs(g_lg[b] - ref["logits"])) <= TOL_LOGITS["bf16"]
+        check_tokens_for(cfg, g_tok[b], g_lg[b], ref["logits"], T, 41, 3, b)
+    # verify reads each session's kept log-sum-exp of the fused draw
+    tl_np = S.make_target_logits(B, n + 1, V, g_tok.astype(np.int32), seed=9, std=2.0, boost=5.0)
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    bon = torch.empty(B, dtype=torch.int32, device="cuda")
+    D.dflash_verify(sess, torch.from_numpy(tl_np).cuda(), tok, n, T, 17, 3, acc, bon)
+    torch.cuda.synchronize()
+    a_g, b_g = acc.cpu().numpy(), bon.cpu().numpy()
+    compared = sum(verify_parity((a_g[b], b_g[b]), tl_np[b], g_tok[b], g_lg[b], g_tok[b], T, T, 17, 3, b)
+                   for b in range(B))
+    assert compared >= B - 1, compared
+    D.dflash_device_status(p.model)
+    for s_ in sess:
+        D.dflash_close(s_)
 
 
 @pytest.mark.parametrize("intermediate", [1024, 12288])
