@@ -7,19 +7,19 @@
 //
 // One CTA per work item (session, KV head, key range starting on a multiple
 // of 64).  Query rows (at most 128, zero padded) form the MMA's M = 128 side.
-//   warp 8        TMA: 64-key K tiles [64 keys][128 d] into a 2-stage ring and
-//                 the matching V^T tiles [128 d][64 keys] into a 5-stage
-//                 ring; the cache keeps V transposed so that both are K-major
-//                 operand tiles.  A K stage is free once S = Q K^T is done, a
-//                 V stage only once P V is done, one to two tiles later, so V
-//                 gets the deeper ring.
+//   warps 8, 10   TMA, one producer per ring: 64-key K tiles [64 keys][128 d]
+//                 into a 4-stage ring (warp 8) and the matching V^T tiles
+//                 [128 d][64 keys] into a 5-stage ring (warp 10); the cache
+//                 keeps V transposed so that both are K-major operand tiles.
+//                 A K stage is free once S = Q K^T is done, a V stage once
+//                 P V is done.
 //   warp 9        MMA, the whole warp running one loop and one elected lane
 //                 issuing (queued MMAs do not hold the warp up): S(t) = Q K^T
 //                 into one of two TMEM buffers as soon as K(t) has landed and
-//                 the softmax has read S(t-2) out of that buffer; O += P V^T
-//                 in tile order as soon as P(u) and V(u) are in shared memory.
-//                 P is a bf16 pair hi + lo (~16 bits of the probabilities):
-//                 two MMAs per 16 keys.
+//                 the softmax has read S(t-2) out of that buffer; O += P V^T,
+//                 each stream's tiles in order, as soon as P(u) and V(u) are
+//                 in shared memory.  P is a bf16 pair hi + lo (~16 bits of the
+//                 probabilities): two MMAs per 16 keys.
 //   warps 0..7    softmax, two threads per query row (warps w and w + 4 read
 //                 the same TMEM lanes; each takes 32 keys of a tile and 64
 //                 columns of O): S from TMEM, mask against the row's visible
@@ -33,11 +33,13 @@
 // warp quarters, so 64 rows would leave the softmax to warps 0, 1, 4, 5 (two
 // of the four SM sub-partitions).  Instead Q is stored twice (rows 64..127
 // repeat rows 0..63); warps of quarters 0-1 take the even key tiles (S buffer
-// 0, P buffer 0, O rows 0..63) and warps of quarters 2-3 the odd ones (S
-// buffer 1, P buffer 1, O rows 64..127), each with its own online softmax.
-// P buffer 0 keeps rows 64..127 at zero and buffer 1 rows 0..63, so the one
-// accumulator takes P V of each tile into its own stream's rows only.  The
-// two streams' (max, sum, O) merge in shared memory at the end.
+// 0, O region 0, rows 0..63) and warps of quarters 2-3 the odd ones (S buffer
+// 1, O region 1, rows 64..127), each with its own online softmax.  Each
+// stream has its own O accumulator in TMEM, so the streams' products never
+// wait on each other; both write their 64 rows of the one P tile, and a
+// product's rows of the other stream land in O rows of its region that are
+// never read.  The two streams' (max, sum, O) merge in shared memory at the
+// end.  TMEM: O0 [0,128), O1 [128,256), S0 [256,320), S1 [320,384).
 // Every wait is bounded; an expired wait sets bit 8 of the error word.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -56,16 +58,17 @@ namespace cg = cooperative_groups;
 
 constexpr int D = 128;                       // head dim
 constexpr int KT = 64;                       // keys per tile (MMA N of S)
-constexpr int KST = 2;                       // K stages
+constexpr int KST = 4;                       // K stages
 constexpr int VST = 5;                       // V^T stages
 constexpr int QBYTES = 128 * D * 2;          // Q: two [128 rows][64 d] swizzled blocks
 constexpr int KBYTES = KT * D * 2;           // K tile: two [64 keys][64 d] blocks
 constexpr int VBYTES = D * KT * 2;           // V^T tile: one [128 d][64 keys] block
 constexpr int PBYTES = 128 * KT * 2;         // P tile: one [128 rows][64 keys] block
-constexpr int DATA_BYTES = QBYTES + KST * KBYTES + VST * VBYTES + 4 * PBYTES;  // + barriers and exchange
-constexpr int THREADS = 320;
+constexpr int DATA_BYTES = QBYTES + KST * KBYTES + VST * VBYTES + 2 * PBYTES;  // + barriers and exchange
+constexpr int THREADS = 352;
 constexpr int SOFTMAX_THREADS = 256;
-constexpr uint32_t TMEM_COLS = 256;          // O [0,128), S0 [128,192), S1 [192,256)
+constexpr uint32_t TMEM_COLS = 512;          // O0 [0,128), O1 [128,256) (two streams), S0 [256,320), S1 [320,384)
+constexpr uint32_t S_COL = 256;
 
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -135,8 +138,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + QBYTES;
   uint8_t* sV = sK + KST * KBYTES;
-  uint8_t* sP = sV + VST * VBYTES;  // [2 buffers][hi, lo]
-  uint64_t* k_full = (uint64_t*)(sP + 4 * PBYTES);
+  uint8_t* sP = sV + VST * VBYTES;  // [hi, lo]
+  uint64_t* k_full = (uint64_t*)(sP + 2 * PBYTES);
   uint64_t* k_empty = k_full + KST;
   uint64_t* v_full = k_empty + KST;
   uint64_t* v_empty = v_full + VST;
@@ -217,53 +220,41 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       const int e = tid + SOFTMAX_THREADS * k, r = e >> 4, c = e & 15;
       *reinterpret_cast<uint4*>(sQ + (c >> 3) * (QBYTES / 2) + swz(r, c & 7)) = v[k];
     }
-    if (dual) {  // the rows of each P buffer that belong to the other stream stay zero
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int e = tid + SOFTMAX_THREADS * k;  // 16-byte chunk, 0..1023
-        uint8_t* z = e < 512 ? sP + PBYTES / 2 + e * 16 : sP + 2 * PBYTES + (e - 512) * 16;
-        *reinterpret_cast<uint4*>(z) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(z + PBYTES) = make_uint4(0, 0, 0, 0);
-      }
-    }
     fence_proxy_async();
   }
   __syncthreads();
 
-  if (warp == 8) {
+  if (warp == 8 || warp == 10) {
     if (lane == 0) {
-      // ---- TMA producer: K(t) then V^T(t), each into its own ring
-      int issued_k = 0, issued_v = 0;
+      // ---- TMA producers, one per ring: warp 8 the K tiles, warp 10 the V^T
+      // tiles, so that neither ring waits for the other's free stage
+      const bool isK = warp == 8;
+      const int NS = isK ? KST : VST;
+      uint64_t* full = isK ? k_full : v_full;
+      uint64_t* empty = isK ? k_empty : v_empty;
+      int issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int ks = t % KST, vs = t % VST;
+        const int st = t % NS;
         const int slot0 = (int)((it.k0 + (int64_t)t * KT) % cap);
-        if (t >= KST && !mbar_wait(&k_empty[ks], (uint32_t)((t / KST) - 1) & 1u, abort_flag)) {
+        if (t >= NS && !mbar_wait(&empty[st], (uint32_t)((t / NS) - 1) & 1u, abort_flag)) {
           atomicOr(err, 8);
           *abort_flag = 1;
           break;
         }
-        mbar_expect_tx(&k_full[ks], KBYTES);
-        tma_load_3d(sK + ks * KBYTES, kmap, &k_full[ks], 0, slot0, planeK);
-        tma_load_3d(sK + ks * KBYTES + KBYTES / 2, kmap, &k_full[ks], 64, slot0, planeK);
-        ++issued_k;
-        if (t >= VST && !mbar_wait(&v_empty[vs], (uint32_t)((t / VST) - 1) & 1u, abort_flag)) {
-          atomicOr(err, 8);
-          *abort_flag = 1;
-          break;
+        if (isK) {
+          mbar_expect_tx(&full[st], KBYTES);
+          tma_load_3d(sK + st * KBYTES, kmap, &full[st], 0, slot0, planeK);
+          tma_load_3d(sK + st * KBYTES + KBYTES / 2, kmap, &full[st], 64, slot0, planeK);
+        } else {
+          mbar_expect_tx(&full[st], VBYTES);
+          tma_load_3d(sV + st * VBYTES, vmap, &full[st], slot0, 0, planeV);
         }
-        mbar_expect_tx(&v_full[vs], VBYTES);
-        tma_load_3d(sV + vs * VBYTES, vmap, &v_full[vs], slot0, 0, planeV);
-        ++issued_v;
+        ++issued;
       }
       if (*abort_flag) {  // let this CTA's own copies land before leaving
-        for (int t = issued_k - KST > 0 ? issued_k - KST : 0; t < issued_k; ++t) {
+        for (int t = issued - NS > 0 ? issued - NS : 0; t < issued; ++t) {
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&k_full[t % KST], (uint32_t)(t / KST) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-        for (int t = issued_v - VST > 0 ? issued_v - VST : 0; t < issued_v; ++t) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&v_full[t % VST], (uint32_t)(t / VST) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          while (!mbar_try_wait(&full[t % NS], (uint32_t)(t / NS) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
@@ -276,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     const uint32_t tO = tmem;
     auto issue_s = [&](int t) {
       const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + (t % KST) * KBYTES);
-      const uint32_t tS = tmem + 128 + (t & 1) * KT;
+      const uint32_t tS = tmem + S_COL + (t & 1) * KT;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         umma_bf16_warp(tS, sdesc_sw128(q0 + (ks >> 2) * (QBYTES / 2) + (ks & 3) * 32),
@@ -284,25 +275,30 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       umma_commit_warp(&s_full[t & 1]);
       umma_commit_warp(&k_empty[t % KST]);  // the K stage is free once S(t) is done
     };
+    // two streams: stream u & 1 accumulates into its own O region, so the
+    // streams' products never wait on each other
+    const int nst = dual ? 2 : 1;
     auto issue_pv = [&](int u) {
-      const uint32_t ph = smem_u32(sP + (u & 1) * 2 * PBYTES), pl = ph + PBYTES, v0 = smem_u32(sV + (u % VST) * VBYTES);
+      const uint32_t ph = smem_u32(sP), pl = ph + PBYTES, v0 = smem_u32(sV + (u % VST) * VBYTES);
+      const uint32_t tOu = tO + (dual ? (uint32_t)((u & 1) * D) : 0u);
 #pragma unroll
       for (int ks = 0; ks < KT / 16; ++ks)
-        umma_bf16_warp(tO, sdesc_sw128(ph + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, (u > 0 || ks > 0) ? 1u : 0u);
+        umma_bf16_warp(tOu, sdesc_sw128(ph + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, (u >= nst || ks > 0) ? 1u : 0u);
 #pragma unroll
-      for (int ks = 0; ks < KT / 16; ++ks) umma_bf16_warp(tO, sdesc_sw128(pl + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, 1u);
+      for (int ks = 0; ks < KT / 16; ++ks) umma_bf16_warp(tOu, sdesc_sw128(pl + ks * 32), sdesc_sw128(v0 + ks * 32), idPV, 1u);
       umma_commit_warp(&pv_done[u & 1]);
       umma_commit_warp(&v_empty[u % VST]);
     };
     // S(t) as soon as K(t) has landed and the softmax has read S(t-2) out of
-    // the same TMEM buffer, P V(u) (in tile order) as soon as P(u) and V(u)
-    // are in place: S of a stream's next tile is computed while the stream
-    // still works on its current one.  A test counts only once every lane
-    // has seen the phase complete.
-    int ns = 0, np = 0;  // next S, next P V
+    // the same TMEM buffer, P V(u) (each stream's in tile order) as soon as
+    // P(u) and V(u) are in place: S of a stream's next tile is computed while
+    // the stream still works on its current one.  A test counts only once
+    // every lane has seen the phase complete.
+    int ns = 0, npv[2] = {0, 1};  // next S; next P V of each stream
+    if (!dual) npv[1] = T;
     bool ok = true;
     uint64_t t0 = globaltimer_ns();
-    for (uint32_t spin = 1; np < T; ++spin) {
+    for (uint32_t spin = 1; npv[0] < T || npv[1] < T; ++spin) {
       if (ns < T && __all_sync(0xffffffffu, mbar_test_wait(&k_full[ns % KST], (uint32_t)(ns / KST) & 1u) &&
                                                 (ns < 2 || mbar_test_wait(&s_free[ns & 1], (uint32_t)((ns >> 1) - 1) & 1u)))) {
         fence_after();
@@ -310,10 +306,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
         t0 = globaltimer_ns();
         continue;
       }
-      if (np < ns && __all_sync(0xffffffffu, mbar_test_wait(&p_full[np & 1], (uint32_t)(np >> 1) & 1u) &&
-                                                 mbar_test_wait(&v_full[np % VST], (uint32_t)(np / VST) & 1u))) {
-        fence_after();
-        issue_pv(np++);
+      bool issued = false;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int u = npv[x];
+        if (u < ns && __all_sync(0xffffffffu, mbar_test_wait(&p_full[u & 1], (uint32_t)(u >> 1) & 1u) &&
+                                                  mbar_test_wait(&v_full[u % VST], (uint32_t)(u / VST) & 1u))) {
+          fence_after();
+          issue_pv(u);
+          npv[x] = u + nst;
+          issued = true;
+        }
+      }
+      if (issued) {
         t0 = globaltimer_ns();
         continue;
       }
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       *abort_flag = 1;
     }
     umma_commit_warp(o_done);  // arrives once every MMA issued above has completed
-  } else {
+  } else if (warp < 8) {
     // ---- softmax: two threads per TMEM row (row = TMEM lane)
     const int r = (warp & 3) * 32 + lane;
     const int half = warp >> 2;                // keys [32 half, +32) of a tile, O columns [64 half, +64)
@@ -345,6 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     // pair barrier), so no phase runs ahead of the others.
     const bool live = (warp & 3) * 32 - 64 * stream < R;
     const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t ocol = (uint32_t)(stream * D);  // this stream's O region (O1 only with two streams)
     const float sl2 = p.scale * 1.4426950408889634f;
     // the row's visible key positions form one interval [vlo, vhi]
     int64_t vlo = it.k0, vhi = it.k1 - 1;
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       if (w) {
         if (live) {
           fence_after();
-          tmem_ld32(tmem + lrow + 128 + sb * KT + 32 * half, s);
+          tmem_ld32(tmem + lrow + S_COL + sb * KT + 32 * half, s);
           fence_before();
         }
         mbar_arrive(&s_free[sb]);
@@ -410,10 +416,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       const float m_new = grow ? mt : m_used;
       const float f = (grow && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.f;
       if (__any_sync(0xffffffffu, f != 1.f)) {
-        // O must hold every earlier tile's product before it is scaled (with
-        // two streams the later products cannot be in flight either: P V of
-        // tile t + 1 is issued only after P of tile t, which waits on this)
-        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
+        // O must hold every earlier tile's product before it is scaled; the
+        // later ones wait for this tile's P.  (Two streams: only the stream's
+        // own products write its O region.)
+        const int tp = t - tstep;
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[tp & 1], (uint32_t)(tp >> 1) & 1u, abort_flag))) {
           ok = false;  // the pair stops together at the next tile's barrier
           continue;
         }
@@ -421,10 +428,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
           float o[32];
-          tmem_ld32(tmem + lrow + c, o);
+          tmem_ld32(tmem + lrow + ocol + c, o);
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] *= f;
-          tmem_st32(tmem + lrow + c, o);
+          tmem_st32(tmem + lrow + ocol + c, o);
         }
       }
       l *= f;
@@ -439,13 +446,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       for (int j = 0; j < 32; j += 2) hi2[j / 2] = p_pair(s[j], s[j + 1], k2, c2, ls2, lo2[j / 2]);
       const float2 ls = f2unpack(ls2);
       l += ls.x + ls.y;
-      if (t >= 2) {  // the P buffer is free once the product of tile t-2 is done
-        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[sb], (uint32_t)((t >> 1) - 1) & 1u, abort_flag))) {
+      // One P tile (hi, lo) serves every tile: this thread's rows are free
+      // once the product of its stream's previous tile is done.  (With two
+      // streams each writes its own 64 rows; each product reads all 128, but
+      // the other stream's rows only reach O rows of that product's region
+      // that are never read.)
+      if (t >= tstep) {
+        const int tw = t - tstep;
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[tw & 1], (uint32_t)(tw >> 1) & 1u, abort_flag))) {
           ok = false;
           continue;
         }
       }
-      uint8_t* ph = sP + sb * 2 * PBYTES;
+      uint8_t* ph = sP;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int cc = 4 * half + c;
@@ -469,14 +482,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     float lsum = xl[r] + xl[128 + r], we = 1.f, wo = 0.f;
     // two streams: the odd stream's rows go through idle V stages (every
     // copy has landed and every MMA has completed) to the even stream's
-    float* xo = reinterpret_cast<float*>(sV + 3 * VBYTES) + (rv ? qr : 0) * (D + 4);
+    float* xo = reinterpret_cast<float*>(sV + 2 * VBYTES) + (rv ? qr : 0) * (D + 4);
     if (dual) {
       if (stream == 1 && live) {
         if (rv && half == 0) *reinterpret_cast<float2*>(xo) = make_float2(m_used, lsum);
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
           float o[32];
-          tmem_ld32(tmem + lrow + c, o);
+          tmem_ld32(tmem + lrow + ocol + c, o);
           if (rv) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
@@ -505,7 +518,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
 #pragma unroll 1
     for (int c = 64 * half; c < 64 * half + 64 && live && stream == 0; c += 32) {
       float o[32];
-      tmem_ld32(tmem + lrow + c, o);
+      tmem_ld32(tmem + lrow + ocol + c, o);
       if (rv) {
         if (dual) {
 #pragma unroll
