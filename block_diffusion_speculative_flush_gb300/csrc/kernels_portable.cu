@@ -780,6 +780,7 @@ __device__ __forceinline__ float sample_logit(const SampleArgs& a, int row, int 
 }
 
 constexpr int kSampleSteps = 4;
+constexpr int kSampleThreads = 256;
 
 __global__ void __launch_bounds__(256, 4) k_sample_partials(SampleArgs a, int chunk, float4* __restrict__ part) {
   pdl_trigger();
@@ -798,7 +799,67 @@ __global__ void __launch_bounds__(256, 4) k_sample_partials(SampleArgs a, int ch
   const RowRef rr = row_ref(a, row);
   // four consecutive entries per thread and step: one Philox evaluation gives
   // their four random words (chunks start on multiples of 4); kSampleSteps
-  // steps' loads are issued before any is used
+  // steps' loads are issued before any is used.
+  // The common case (fp32 rows on 16-byte boundaries, no truncation) first:
+  // the same steps and the same arithmetic in the same order, with the
+  // per-entry range tests only on a quad that crosses the chunk's end.
+  if (!cutv && rr.vec && !rr.bf && blockDim.x == kSampleThreads) {
+    const float* rowp = static_cast<const float*>(rr.p);
+    float bv = -INFINITY;  // this thread's best score; entries come in index order
+    int bi = INT32_MAX;
+    for (int base = v0 + 4 * threadIdx.x; base < v1; base += 4 * kSampleThreads * kSampleSteps) {
+      float x[kSampleSteps][4];
+#pragma unroll
+      for (int it = 0; it < kSampleSteps; ++it) {
+        const int v4 = base + it * 4 * kSampleThreads;
+        if (v4 + 3 < v1) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(rowp + v4));
+          x[it][0] = f.x * invT;
+          x[it][1] = f.y * invT;
+          x[it][2] = f.z * invT;
+          x[it][3] = f.w * invT;
+        } else {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) x[it][w] = v4 + w < v1 ? rowp[v4 + w] * invT : -INFINITY;
+        }
+      }
+      float ms = -INFINITY;
+#pragma unroll
+      for (int it = 0; it < kSampleSteps; ++it)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) ms = fmaxf(ms, x[it][w]);
+      if (ms != -INFINITY) {
+        float ls = 0.f;
+#pragma unroll
+        for (int it = 0; it < kSampleSteps; ++it)
+#pragma unroll
+          for (int w = 0; w < 4; ++w) ls += __expf(x[it][w] - ms);
+        if (ms > m) {
+          l = (m == -INFINITY ? 0.f : l * __expf(m - ms)) + ls;
+          m = ms;
+        } else {
+          l += ls * __expf(ms - m);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < kSampleSteps; ++it) {
+        const int v4 = base + it * 4 * kSampleThreads;
+        uint4 r = make_uint4(0, 0, 0, 0);
+        if (a.gumbel && v4 < v1) r = rand_block(a.seed, a.rnd, kStreamDraft, seq, prow, (uint32_t)v4 >> 2);
+        const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          // an entry past the chunk is -inf and never beats a score
+          const float sc = a.gumbel ? x[it][w] + gumbel_of(wd[w]) : x[it][w];
+          if (sc > bv) {
+            bv = sc;
+            bi = v4 + w;
+          }
+        }
+      }
+    }
+    best = ArgMax{bv, bi};
+  } else
   for (int base = v0 + 4 * threadIdx.x; base < v1; base += 4 * blockDim.x * kSampleSteps) {
     float x[kSampleSteps][4];
 #pragma unroll
@@ -1755,7 +1816,7 @@ void launch_kv_copy(DT dt, void* cache, int64_t cap, int64_t first, void* flat, 
 
 void launch_sample_partials(const SampleArgs& a, int chunk, float4* part, cudaStream_t st) {
   if (a.rows <= 0) return;
-  launch_k(k_sample_partials, dim3(a.rows, cdiv(a.V, chunk)), 256, 0, st, a, chunk, part);
+  launch_k(k_sample_partials, dim3(a.rows, cdiv(a.V, chunk)), kSampleThreads, 0, st, a, chunk, part);
 }
 
 void launch_sample_combine(const SampleArgs& a, int chunks, const float4* part, int32_t* tok, float* qtok, float* lse,
