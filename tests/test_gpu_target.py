@@ -41,7 +41,8 @@ def _close(g, r, tol):
 
 def test_target_forward_and_trim_match_the_cpu_target():
     """Prompt rows, a 5-row verify chunk, a trim to 10 rows and 3 more rows:
-    logits and taps equal the CPU target's (fp32 against float64 arithmetic)."""
+    logits and taps equal the CPU target's within the fp32 bar, 1e-4
+    (relative above 1; fp32 against float64 arithmetic)."""
     D = lib()
     ref = oracle_target()
     t = upload_target(D)
@@ -50,7 +51,7 @@ def test_target_forward_and_trim_match_the_cpu_target():
     for tokens, start, trim in ((prompt, 0, None), ([3, 7, 1, 30, 12], 8, 10), ([5, 9, 2], 10, None)):
         lg, tp = _fwd(D, t, tokens, start, V, NT)
         rl, rt = ref.forward(tokens, start)
-        _close(lg, rl, 1e-3)
+        _close(lg, rl, 1e-4)
         _close(tp, rt, 1e-4)
         if trim is not None:
             D.dflash_target_trim(t, trim)
@@ -192,7 +193,7 @@ def test_exactness_probe_allows_the_synthetic_target_and_leaves_its_cache():
     ref = oracle_target()
     ref.forward(prompt, 0)
     rl, _ = ref.forward(block.cpu().tolist(), len(prompt))
-    _close(bl.cpu().numpy(), rl, 1e-3)
+    _close(bl.cpu().numpy(), rl, 1e-4)
     rows = D.exactness_rows(out)
     assert [r["block_top"][0] for r in rows] == list(np.argmax(bl.cpu().numpy(), axis=1))
     D.dflash_target_device_status(t)
