@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     }
     fence_proxy_async();
   }
-  __syncthreads();
+  // Q staged: the MMA warp needs it (and the softmax warps wrote it); the
+  // producers do not, and start their loads at once
+  if (warp < 8 || warp == 9) asm volatile("bar.sync 7, %0;" ::"r"(SOFTMAX_THREADS + 32) : "memory");
 
   if (warp == 8 || warp == 10) {
     if (lane == 0) {
