@@ -543,6 +543,45 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
   const int S = item_count[b];
   const float* base = part + ((int64_t)(item_first[b] + kvh * S) * R + rr) * PD;
   const int64_t sstride = (int64_t)R * PD;
+  if (S <= 16 && d == 128) {
+    // every lane loads every split's (m, l) and its four output columns of
+    // every split at once: one round trip to memory, then the merge in split
+    // order as below
+    const float gate = Gt ? Gt[(int64_t)bi * p.Hq + hq] : 1.f;
+    float2 ml[16];
+    float4 v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (k < S) {
+        ml[k] = __ldg(reinterpret_cast<const float2*>(base + k * sstride));
+        v[k] = __ldg(reinterpret_cast<const float4*>(base + k * sstride + 4 + lane * 4));
+      } else {
+        ml[k] = make_float2(-INFINITY, 0.f);
+        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) M = fmaxf(M, ml[k].x);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float w = ml[k].x == -INFINITY ? 0.f : expf(ml[k].x - M);
+      L += ml[k].y * w;
+      acc.x += w * v[k].x;
+      acc.y += w * v[k].y;
+      acc.z += w * v[k].z;
+      acc.w += w * v[k].w;
+    }
+    const float scale = gate / L;
+    T* out = O + ((int64_t)bi * p.Hq + hq) * d + lane * 4;
+    out[0] = from_f<T>(acc.x * scale);
+    out[1] = from_f<T>(acc.y * scale);
+    out[2] = from_f<T>(acc.z * scale);
+    out[3] = from_f<T>(acc.w * scale);
+    return;
+  }
   // (m, l) of up to 32 splits in one pass, one split per lane
   float M = -INFINITY, mv = -INFINITY, lv = 0.f;
   if (lane < S) {
