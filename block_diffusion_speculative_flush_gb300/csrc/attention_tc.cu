@@ -185,9 +185,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  // The work item and the session tables belong to this call: they are
-  // written by an earlier kernel of the chain, like Q and the block's K/V.
-  pdl_wait();
+  // The work item, the session tables and every cache row older than this
+  // forward were written before the kernel that precedes this one (k_qkv_post,
+  // or the V^T writer after it) finished its own wait, and that kernel lets
+  // this one start only then: they are read before this kernel's wait.  Q and
+  // the rows this forward writes come from that kernel and are read after it.
   const AttnItem it = items[blockIdx.x];
   const int G = p.Hq / p.Hkv, R = p.nrows * G;
   const int64_t F = tabs.frontier[it.sess], cap = tabs.cap[it.sess];
@@ -195,11 +197,20 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   const CUtensorMap* vmap = kmap + 1;
   const int planeK = 2 * p.layer * p.Hkv + it.kvh, planeV = (2 * p.layer + 1) * p.Hkv + it.kvh;
   const int T = (int)((it.k1 - it.k0 + KT - 1) / KT);
+  // key tiles [0, T_old) hold no row that this forward writes
+  int T_old = 0;
+  if (tabs.fresh) {
+    const int64_t fresh = tabs.fresh[it.sess];
+    T_old = fresh <= it.k0 ? 0 : (int)min((int64_t)T, (fresh - it.k0) / KT);
+  }
   if (tid == 256) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)kmap) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)vmap) : "memory");
   }
 
+  // everyone but the producers waits here; they first request the tiles of
+  // older rows
+  if (warp != 8 && warp != 10) pdl_wait();
   // ---- Q rows of this KV head, zero padded to 128 (two streams: rows 0..63
   // twice), as the MMA's A tile
   if (warp < 8) {
@@ -227,30 +238,41 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   if (warp < 8 || warp == 9) asm volatile("bar.sync 7, %0;" ::"r"(SOFTMAX_THREADS + 32) : "memory");
 
   if (warp == 8 || warp == 10) {
+    // ---- TMA producers, one per ring: warp 8 the K tiles, warp 10 the V^T
+    // tiles, so that neither ring waits for the other's free stage
+    const bool isK = warp == 8;
+    const int NS = isK ? KST : VST;
+    uint64_t* full = isK ? k_full : v_full;
+    uint64_t* empty = isK ? k_empty : v_empty;
+    auto load = [&](int t) {
+      const int st = t % NS;
+      const int slot0 = (int)((it.k0 + (int64_t)t * KT) % cap);
+      if (isK) {
+        mbar_expect_tx(&full[st], KBYTES);
+        tma_load_3d(sK + st * KBYTES, kmap, &full[st], 0, slot0, planeK);
+        tma_load_3d(sK + st * KBYTES + KBYTES / 2, kmap, &full[st], 64, slot0, planeK);
+      } else {
+        mbar_expect_tx(&full[st], VBYTES);
+        tma_load_3d(sV + st * VBYTES, vmap, &full[st], slot0, 0, planeV);
+      }
+    };
+    // the first stages, where they hold older rows only, while the previous
+    // kernel drains; then the whole warp waits (its other lanes write the
+    // clustered merge's output at the end); then the rest in order
+    const int early = min(T_old, NS);
+    if (lane == 0)
+      for (int t = 0; t < early; ++t) load(t);
+    __syncwarp();
+    pdl_wait();
     if (lane == 0) {
-      // ---- TMA producers, one per ring: warp 8 the K tiles, warp 10 the V^T
-      // tiles, so that neither ring waits for the other's free stage
-      const bool isK = warp == 8;
-      const int NS = isK ? KST : VST;
-      uint64_t* full = isK ? k_full : v_full;
-      uint64_t* empty = isK ? k_empty : v_empty;
-      int issued = 0;
-      for (int t = 0; t < T; ++t) {
-        const int st = t % NS;
-        const int slot0 = (int)((it.k0 + (int64_t)t * KT) % cap);
-        if (t >= NS && !mbar_wait(&empty[st], (uint32_t)((t / NS) - 1) & 1u, abort_flag)) {
+      int issued = early;
+      for (int t = early; t < T; ++t) {
+        if (t >= NS && !mbar_wait(&empty[t % NS], (uint32_t)((t / NS) - 1) & 1u, abort_flag)) {
           atomicOr(err, 8);
           *abort_flag = 1;
           break;
         }
-        if (isK) {
-          mbar_expect_tx(&full[st], KBYTES);
-          tma_load_3d(sK + st * KBYTES, kmap, &full[st], 0, slot0, planeK);
-          tma_load_3d(sK + st * KBYTES + KBYTES / 2, kmap, &full[st], 64, slot0, planeK);
-        } else {
-          mbar_expect_tx(&full[st], VBYTES);
-          tma_load_3d(sV + st * VBYTES, vmap, &full[st], slot0, 0, planeV);
-        }
+        load(t);
         ++issued;
       }
       if (*abort_flag) {  // let this CTA's own copies land before leaving

@@ -401,7 +401,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   }
   std::vector<void*> kvb(Bc);
   std::vector<const CUtensorMap*> mapv(Bc);
-  std::vector<int64_t> capv(Bc), front(Bc);
+  std::vector<int64_t> capv(Bc), front(Bc), fresh(Bc);
   std::vector<int32_t> seqv(Bc);
   bool have_maps = true;
   for (int j = 0; j < Bc; ++j) {
@@ -410,13 +410,16 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     kvb[j] = fw.sess[j]->kv;
     capv[j] = fw.sess[j]->cap;
     front[j] = fw.sess[j]->F;
+    fresh[j] = fw.sess[j]->F;  // the block's rows start at F
     seqv[j] = block ? fw.sess_map[j] : j;
   }
+  for (int r = 0; r < Mc; ++r) fresh[fw.ctx[r].sess] = std::min(fresh[fw.ctx[r].sess], fw.ctx[r].pos);
   for (int j = 0; j < Bc && block; ++j)
     for (int i = 0; i < nrows; ++i) meta[Mc + j * nrows + i] = RowMeta{j, j * nrows + i, fw.sess[j]->F + i};
   // attention work items: split every (session, KV head) key range in chunks
   std::vector<AttnItem> items;
   std::vector<int32_t> ifirst(Bc), icount(Bc);
+  int max_splits = 0;
   // in-kernel merge of the key ranges: one session on the tensor-core path
   const bool attn_cluster_ok = block && Bc == 1 && m->dt == DT::BF16 && d == 128 && nrows * (Hq / Hkv) <= 128;
   int attn_cluster = 1;
@@ -466,6 +469,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       const int S = (int)((k1v[j] - k0v[j] + chunk - 1) / chunk);
       ifirst[j] = (int32_t)items.size();
       icount[j] = S;
+      max_splits = std::max(max_splits, S);
       for (int h = 0; h < Hkv; ++h)
         for (int s = 0; s < S; ++s)
           items.push_back(AttnItem{j, h, k0v[j] + s * chunk, std::min(k1v[j], k0v[j] + (s + 1) * chunk)});
@@ -510,7 +514,8 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   }
   const size_t o_rowsrc = tp.add(rowsrc), o_meta = tp.add(meta), o_kv = tp.add(kvb), o_cap = tp.add(capv),
                o_front = tp.add(front), o_seq = tp.add(seqv), o_items = tp.add(items), o_ifirst = tp.add(ifirst),
-               o_icount = tp.add(icount), o_map = tp.add(fw.sess_map), o_maps = tp.add(mapv);
+               o_icount = tp.add(icount), o_map = tp.add(fw.sess_map), o_maps = tp.add(mapv),
+               o_fresh = tp.add(fresh);
   // RoPE cos/sin: the model's table indexed by position (angle pos *
   // theta^(-2j/d) in double), extended when a call reaches past it; it grows
   // geometrically, so a steady stream of rounds computes no trigonometry
@@ -526,7 +531,8 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
   ST_TRY(m->ring.upload(tp, m->tables, st));
   char* tb = m->tables.as<char>();
   SessTables tabs{(void* const*)(tb + o_kv), (const int64_t*)(tb + o_cap), (const int64_t*)(tb + o_front),
-                  (const int32_t*)(tb + o_seq), have_maps ? (const CUtensorMap* const*)(tb + o_maps) : nullptr};
+                  (const int32_t*)(tb + o_seq), have_maps ? (const CUtensorMap* const*)(tb + o_maps) : nullptr,
+                  (const int64_t*)(tb + o_fresh)};
   const RowMeta* dmeta = (const RowMeta*)(tb + o_meta);
 
   // ---- buffers -----------------------------------------------------------
@@ -636,7 +642,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       if (how != 2)
         launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
                                  (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
-                                 m->O.p, st);
+                                 m->O.p, st, max_splits);
       m->launches += 2;
     }
     ST_TRY(launch_check("attention"));

@@ -31,6 +31,9 @@ struct SessTables {
   const int64_t* frontier; // [B] F: position of the block's anchor row
   const int32_t* seq;      // [B] seq id used by the random streams
   const CUtensorMap* const* kvmaps;  // [B] -> {K planes, V^T planes} TMA maps (bf16, d = 128), or NULL
+  // [B] lowest position whose K/V this forward writes (its context rows,
+  // then the block), or NULL: every older row of the cache is left as it was
+  const int64_t* fresh;
 };
 
 // One attention work item: keys [k0, k1) (positions) of one session / KV head.
@@ -101,8 +104,10 @@ constexpr int kAttnMaxCluster = 16;
 // for k_attn_combine, 2 if the output was merged in-kernel (p.cluster > 1).
 int launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
                         int* err, cudaStream_t st);
+// max_splits: the largest item count of a session (0: not known); up to 32
+// the merge runs in one pass for d = 128
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count,
-                              int B, AttnParams p, const float* G, void* O, cudaStream_t st);
+                              int B, AttnParams p, const float* G, void* O, cudaStream_t st, int max_splits = 0);
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld_delta, int rows, int H, cudaStream_t st);
 void launch_swiglu(DT dt, const float* gu, int64_t ld, int rows, int I, int up_offset, void* a,
                    cudaStream_t st);

@@ -57,7 +57,17 @@ constexpr int kNormVec = 4;
 __device__ __forceinline__ bool norm_vec_ok(const void* x, const void* g, const void* o, int H) {
   return H % 8 == 0 && H / 8 <= kNormVec * (int)blockDim.x && (((uintptr_t)x | (uintptr_t)g | (uintptr_t)o) & 15) == 0;
 }
-__device__ __forceinline__ void norm_row_vec(const bf16* x, const bf16* g, bf16* o, int H, float eps, float* red) {
+// The gain words of this thread (loaded ahead: the gain is a weight).
+__device__ __forceinline__ void norm_gain_vec(const bf16* g, int H, uint4 (&gw)[kNormVec]) {
+  const int nv = H / 8;
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    gw[i] = c < nv ? __ldg(reinterpret_cast<const uint4*>(g) + c) : make_uint4(0, 0, 0, 0);
+  }
+}
+__device__ __forceinline__ void norm_row_vec(const bf16* x, const uint4 (&gw)[kNormVec], bf16* o, int H, float eps,
+                                             float* red) {
   const int nv = H / 8;
   uint4 w[kNormVec];
   float ss = 0.f;
@@ -78,11 +88,16 @@ __device__ __forceinline__ void norm_row_vec(const bf16* x, const bf16* g, bf16*
     if (c >= nv) continue;
     float v[8], gv[8];
     unpack8(w[i], v);
-    unpack8(__ldg(reinterpret_cast<const uint4*>(g) + c), gv);
+    unpack8(gw[i], gv);
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = v[e] * inv * gv[e];
     reinterpret_cast<uint4*>(o)[c] = pack8(v);
   }
+}
+__device__ __forceinline__ void norm_row_vec(const bf16* x, const bf16* g, bf16* o, int H, float eps, float* red) {
+  uint4 gw[kNormVec];
+  norm_gain_vec(g, H, gw);
+  norm_row_vec(x, gw, o, H, eps, red);
 }
 
 // fp32 rows of up to 4096 into bf16 (the fc output's hidden_norm): 128
@@ -93,9 +108,15 @@ __global__ void __launch_bounds__(128) k_rmsnorm_f32v(const float* __restrict__ 
                                                       const bf16* __restrict__ g, bf16* __restrict__ out,
                                                       int64_t ld_out, int H, float eps) {
   pdl_trigger();
+  const int j = blockIdx.x, nv = H / 4;
+  uint2 gw[kNormF32Vec];  // the gain is a weight: read before the wait
+#pragma unroll
+  for (int i = 0; i < kNormF32Vec; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    gw[i] = c < nv ? __ldg(reinterpret_cast<const uint2*>(g) + c) : make_uint2(0u, 0u);
+  }
   pdl_wait();
   __shared__ float red[32];
-  const int j = blockIdx.x, nv = H / 4;
   const float4* x = reinterpret_cast<const float4*>(in + (int64_t)j * ld_in);
   float4 w[kNormF32Vec];
   float ss = 0.f;
@@ -115,9 +136,8 @@ __global__ void __launch_bounds__(128) k_rmsnorm_f32v(const float* __restrict__ 
   for (int i = 0; i < kNormF32Vec; ++i) {
     const int c = threadIdx.x + i * blockDim.x;
     if (c >= nv) continue;
-    const uint2 gw = __ldg(reinterpret_cast<const uint2*>(g) + c);
-    const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.x));
-    const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw.y));
+    const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i].x));
+    const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i].y));
     const __nv_bfloat162 a = __floats2bfloat162_rn(w[i].x * inv * g01.x, w[i].y * inv * g01.y);
     const __nv_bfloat162 b = __floats2bfloat162_rn(w[i].z * inv * g23.x, w[i].w * inv * g23.y);
     uint2 raw;
@@ -194,12 +214,23 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, in
                                                  int64_t ld_in, const T* __restrict__ g, T* __restrict__ out,
                                                  int64_t ld_out, int H, int a, int b, int c, float eps) {
   pdl_trigger();
-  pdl_wait();
   __shared__ float red[32];
   const int j = blockIdx.x;
   const int src = (j / a) * b + (j % a) + c;
   const TIn* x = src < rows0 ? in0 + (int64_t)src * ld_in : in1 + (int64_t)(src - rows0) * ld_in;
-  rmsnorm_row(x, g, out + (int64_t)j * ld_out, H, eps, red);
+  T* o = out + (int64_t)j * ld_out;
+  if constexpr (std::is_same<TIn, bf16>::value && std::is_same<T, bf16>::value) {
+    if (norm_vec_ok(x, g, o, H)) {
+      // the gain is a weight: its words are read before the wait, the row after
+      uint4 gw[kNormVec];
+      norm_gain_vec(g, H, gw);
+      pdl_wait();
+      norm_row_vec(x, gw, o, H, eps, red);
+      return;
+    }
+  }
+  pdl_wait();
+  rmsnorm_row(x, g, o, H, eps, red);
 }
 
 // Every layer's input norm of the same rows at once (a context-only
@@ -259,37 +290,44 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
                            const float2* __restrict__ rope, const T* __restrict__ q_norm,
                            const T* __restrict__ k_norm, int Hq, int Hkv, int gated, float eps, SessTables tabs,
                            int layer, T* __restrict__ Q, float* __restrict__ G, int v_apart) {
-  pdl_trigger();
-  pdl_wait();
   constexpr int d = DU * 32;
   const int m = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const int hh = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const RowMeta rm = meta[m];
+  const bool is_q = hh < Hq, head = hh < Hq + Hkv;
+  // the head-norm gain is a weight: read before the wait
+  float gv[DU];
+  const T* gn = is_q ? q_norm : k_norm;
+#pragma unroll
+  for (int u = 0; u < DU; ++u) gv[u] = head ? to_f(gn[lane + 32 * u]) : 0.f;
+  // The attention kernel that follows reads the session tables and the
+  // cache rows older than this forward before its own wait: it may start
+  // only once every kernel before this one has finished, so the trigger
+  // comes after the wait.
+  pdl_wait();
+  pdl_trigger();
   const float* row = qkv + (int64_t)m * ldq;
+  // the head's values are read together with the row's table entry
+  float y[DU];
+#pragma unroll
+  for (int u = 0; u < DU; ++u) y[u] = head ? row[(int64_t)hh * d + lane + 32 * u] : 0.f;
+  const RowMeta rm = meta[m];
   if (gated && rm.blk >= 0 && blockIdx.y == 0) {
     for (int hq = threadIdx.x; hq < Hq; hq += blockDim.x) {
       const float x = row[(Hq + 2 * Hkv) * d + hq];
       G[(int64_t)rm.blk * Hq + hq] = 1.f / (1.f + expf(-x));
     }
   }
-  if (hh >= Hq + Hkv) return;
-  const bool is_q = hh < Hq;
+  if (!head) return;
   if (is_q && rm.blk < 0) return;  // context rows need only K and V
   const int kh = hh - Hq;
-  const float* x = row + (int64_t)hh * d;
-  float y[DU];
   float ss = 0.f;
 #pragma unroll
-  for (int u = 0; u < DU; ++u) {
-    y[u] = x[lane + 32 * u];
-    ss += y[u] * y[u];
-  }
+  for (int u = 0; u < DU; ++u) ss += y[u] * y[u];
   ss = warp_sum(ss);
   const float inv = rsqrtf(ss / (float)d + eps);
-  const T* gn = is_q ? q_norm : k_norm;
 #pragma unroll
-  for (int u = 0; u < DU; ++u) y[u] = y[u] * inv * to_f(gn[lane + 32 * u]);
+  for (int u = 0; u < DU; ++u) y[u] = y[u] * inv * gv[u];
   const float2* rt = rope + rm.pos * (d / 2);  // the table is indexed by position
 #pragma unroll
   for (int u = 0; u < DU / 2; ++u) {
@@ -325,8 +363,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) k_v_cache_t(const float* __restrict__ qkv, int64_t ldq,
                                                    const RowMeta* __restrict__ meta, int M, int Hq, int Hkv,
                                                    SessTables tabs, int layer) {
+  pdl_wait();  // as in k_qkv_post: the attention that follows relies on it
   pdl_trigger();
-  pdl_wait();
   __shared__ float tile[32][D + 1];
   const int kh = blockIdx.y, m0 = blockIdx.x * 32;
   const int64_t col = (int64_t)(Hq + Hkv + kh) * D;
@@ -522,10 +560,53 @@ __global__ void k_attn_simt(const T* __restrict__ Q, const AttnItem* __restrict_
   }
 }
 
+// The merge below for d = 128 and at most NS splits: every lane loads every
+// split's (m, l) and its four output columns of every split at once (one
+// round trip to memory), then merges them in split order.  Splits past S
+// weigh zero and add exact zeros, so NS does not change the result.
+template <int NS, typename T>
+__device__ __forceinline__ void combine_d128(const float* __restrict__ base, int64_t sstride, int S, int lane,
+                                             float gate, T* __restrict__ out) {
+  float2 ml[NS];
+  float4 v[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    if (k < S) {
+      ml[k] = __ldg(reinterpret_cast<const float2*>(base + k * sstride));
+      v[k] = __ldg(reinterpret_cast<const float4*>(base + k * sstride + 4 + lane * 4));
+    } else {
+      ml[k] = make_float2(-INFINITY, 0.f);
+      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NS; ++k) M = fmaxf(M, ml[k].x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const float w = ml[k].x == -INFINITY ? 0.f : expf(ml[k].x - M);
+    L += ml[k].y * w;
+    acc.x += w * v[k].x;
+    acc.y += w * v[k].y;
+    acc.z += w * v[k].z;
+    acc.w += w * v[k].w;
+  }
+  const float scale = gate / L;
+  out += lane * 4;
+  out[0] = from_f<T>(acc.x * scale);
+  out[1] = from_f<T>(acc.y * scale);
+  out[2] = from_f<T>(acc.z * scale);
+  out[3] = from_f<T>(acc.w * scale);
+}
+
 // Merge of the key splits of one (block row, query head) per warp:
 // M = max m_s, L = sum l_s e^(m_s - M), o = sum O_s e^(m_s - M) / L, then
 // the per-head gate.  Partial rows are [m, l, -, -, O[d]] (16-byte aligned O).
-template <typename T>
+// NSMAX (16 or 32): the most splits merged in one pass; the wider variant
+// holds twice the registers, so it is launched only when a session needs it.
+template <int NSMAX, typename T>
 __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part,
                                                       const int32_t* __restrict__ item_first,
                                                       const int32_t* __restrict__ item_count, AttnParams p, int total,
@@ -543,43 +624,13 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
   const int S = item_count[b];
   const float* base = part + ((int64_t)(item_first[b] + kvh * S) * R + rr) * PD;
   const int64_t sstride = (int64_t)R * PD;
-  if (S <= 16 && d == 128) {
-    // every lane loads every split's (m, l) and its four output columns of
-    // every split at once: one round trip to memory, then the merge in split
-    // order as below
+  if (S <= NSMAX && d == 128) {
     const float gate = Gt ? Gt[(int64_t)bi * p.Hq + hq] : 1.f;
-    float2 ml[16];
-    float4 v[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      if (k < S) {
-        ml[k] = __ldg(reinterpret_cast<const float2*>(base + k * sstride));
-        v[k] = __ldg(reinterpret_cast<const float4*>(base + k * sstride + 4 + lane * 4));
-      } else {
-        ml[k] = make_float2(-INFINITY, 0.f);
-        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) M = fmaxf(M, ml[k].x);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float w = ml[k].x == -INFINITY ? 0.f : expf(ml[k].x - M);
-      L += ml[k].y * w;
-      acc.x += w * v[k].x;
-      acc.y += w * v[k].y;
-      acc.z += w * v[k].z;
-      acc.w += w * v[k].w;
-    }
-    const float scale = gate / L;
-    T* out = O + ((int64_t)bi * p.Hq + hq) * d + lane * 4;
-    out[0] = from_f<T>(acc.x * scale);
-    out[1] = from_f<T>(acc.y * scale);
-    out[2] = from_f<T>(acc.z * scale);
-    out[3] = from_f<T>(acc.w * scale);
+    T* out = O + ((int64_t)bi * p.Hq + hq) * d;
+    if (NSMAX == 16 || S <= 16)
+      combine_d128<16>(base, sstride, S, lane, gate, out);
+    else
+      combine_d128<NSMAX>(base, sstride, S, lane, gate, out);
     return;
   }
   // (m, l) of up to 32 splits in one pass, one split per lane
@@ -1798,10 +1849,15 @@ void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_it
 }
 
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count, int B,
-                              AttnParams p, const float* G, void* O, cudaStream_t st) {
+                              AttnParams p, const float* G, void* O, cudaStream_t st, int max_splits) {
   const int total = B * p.nrows * p.Hq;
-  DFL_DISPATCH(dt, launch_k(k_attn_combine<T>, cdiv(total, 4), 128, 0, st, part, item_first, item_count, p, total, G,
-                                                                      (T*)O));
+  if (max_splits > 16 && max_splits <= 32) {
+    DFL_DISPATCH(dt, launch_k(k_attn_combine<32, T>, cdiv(total, 4), 128, 0, st, part, item_first, item_count, p,
+                              total, G, (T*)O));
+  } else {
+    DFL_DISPATCH(dt, launch_k(k_attn_combine<16, T>, cdiv(total, 4), 128, 0, st, part, item_first, item_count, p,
+                              total, G, (T*)O));
+  }
 }
 
 void launch_trunc_cut(const SampleArgs& a, const Trunc* tr, uint64_t* cut, uint64_t* const* sess_cut,

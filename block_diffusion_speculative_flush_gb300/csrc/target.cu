@@ -419,7 +419,7 @@ DFLASH_API int dflash_target_forward(dflash_target* t, const int32_t* tokens, in
     if (rc != DFLASH_OK) return rc;
     char* tb = t->tables.as<char>();
     SessTables tabs{(void* const*)(tb + o_kv), (const int64_t*)(tb + o_cap), (const int64_t*)(tb + o_fr),
-                    (const int32_t*)(tb + o_seq), (const CUtensorMap* const*)(tb + o_map)};
+                    (const int32_t*)(tb + o_seq), (const CUtensorMap* const*)(tb + o_map), nullptr};
     // buffers
     const size_t f4 = 4;
     cudaError_t e = t->x.ensure((size_t)R * H * f4, st);
