@@ -154,7 +154,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
   // never overwrites a value its partner has not read) and the final sum
   float* xch = (float*)(tmem_slot + 4);
 
-  pdl_trigger();
+  // Merged in-kernel, the output goes to the O product, which reads nothing of
+  // this call's tables early: it may start at once.  Partials go to
+  // k_attn_combine, which does read them early: it starts only once every
+  // thread here is past its wait.
+  if (p.cluster > 1) pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool dual = p.nrows * (p.Hq / p.Hkv) <= 64;
   const int tile_threads = dual ? SOFTMAX_THREADS / 2 : SOFTMAX_THREADS;  // softmax threads per key tile
@@ -210,7 +214,13 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
 
   // everyone but the producers waits here; they first request the tiles of
   // older rows
-  if (warp != 8 && warp != 10) pdl_wait();
+  if (warp != 8 && warp != 10) {
+    pdl_wait();
+    if (p.cluster == 1) pdl_trigger();
+  }
+  // Q (and the gates) come from the kernel just before: read after the wait
+  const bf16* Qw = after_wait(Q);
+  const float* gates = after_wait(p.gates);
   // ---- Q rows of this KV head, zero padded to 128 (two streams: rows 0..63
   // twice), as the MMA's A tile
   if (warp < 8) {
@@ -222,8 +232,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       v[k] = make_uint4(0, 0, 0, 0);
       if (r < R) {
         const int i = r / G, g = r % G;
-        v[k] = __ldg(reinterpret_cast<const uint4*>(
-            Q + (((int64_t)it.sess * p.nrows + i) * p.Hq + it.kvh * G + g) * D + c * 8));
+        v[k] = *reinterpret_cast<const uint4*>(Qw + (((int64_t)it.sess * p.nrows + i) * p.Hq + it.kvh * G + g) * D +
+                                              c * 8);
       }
     }
 #pragma unroll
@@ -264,6 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       for (int t = 0; t < early; ++t) load(t);
     __syncwarp();
     pdl_wait();
+    if (p.cluster == 1) pdl_trigger();
     if (lane == 0) {
       int issued = early;
       for (int t = early; t < T; ++t) {
@@ -585,7 +596,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
       }
       const int i = rr / G, g = rr % G, hq = it.kvh * G + g;
       const int64_t orow = (int64_t)it.sess * p.nrows + i;
-      const float sc = (p.gates ? p.gates[orow * p.Hq + hq] : 1.f) / L;
+      const float sc = (gates ? gates[orow * p.Hq + hq] : 1.f) / L;
       const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * sc, acc.y * sc);
       const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc.z * sc, acc.w * sc);
       uint2 raw;

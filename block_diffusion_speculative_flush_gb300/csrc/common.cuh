@@ -166,5 +166,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// p as the compiler must take it from here on: its value is opaque until this
+// point, so no load through the result can be scheduled before it.  Pointers
+// to what an earlier kernel of the chain writes pass through it right after
+// the wait, and such data is read with plain (coherent) loads: a read-only
+// (__ldg) load is only valid for memory that no kernel writes while this one
+// runs, and with programmatic launch the previous kernel still runs when
+// this one starts.
+template <typename T>
+__device__ __forceinline__ T* after_wait(T* p) {
+  asm volatile("" : "+l"(p)::"memory");
+  return p;
+}
 
 }  // namespace dfl

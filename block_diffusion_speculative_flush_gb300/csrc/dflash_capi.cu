@@ -283,13 +283,14 @@ int check_config(const dflash_config& c) {
 // matrix products: Y[M][N] (fp32) = X[M][K] . W[N][K]^T
 // ---------------------------------------------------------------------------
 int gemm(dflash_model* m, const void* X, int64_t ldx, const void* W, int64_t ldw, float* Y, int64_t ldy, int M, int N,
-         int K, cudaStream_t st) {
+         int K, cudaStream_t st, bool late_trigger = false) {
   if (M <= 0) return DFLASH_OK;
   const double bytes = (double)N * K * m->esz + (double)M * K * m->esz + (double)M * N * 4;
   Timed tm(m, m->use_tc ? kGemmTc : kGemmSimt, bytes, 2.0 * M * N * K, st);
   m->launches++;
   if (m->use_tc) {
-    const int rc = tc_gemm(m->tc, X, ldx, W, nullptr, ldw, Y, ldy, M, N, K, kF32, st);
+    const int rc = tc_gemm(m->tc, X, ldx, W, nullptr, ldw, Y, ldy, M, N, K, kF32, st, nullptr, 0, nullptr,
+                           late_trigger ? 1 : 0);
     if (rc) return fail(DFLASH_ERR_CUDA, "tcgen05 GEMM: %s", tc_last_error());
   } else {
     launch_gemm_simt(m->dt, X, ldx, W, ldw, Y, ldy, M, N, K, st);
@@ -608,8 +609,10 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     launch_rmsnorm(m->dt, false, m->c.p, Mc, m->h.p, H, w.in_norm, m->x.p, H, M, H, M, 0, 0, c.rms_eps, st);
     m->launches++;
     if (block) {
+      // k_qkv_post, next, reads its row and session tables before its wait
+      // (the tensor-core product lets it start only once they are written)
       const void* wq = w.w_qkvg ? w.w_qkvg : w.w_qkv;
-      ST_TRY(gemm(m, m->x.p, H, wq, H, m->qkv.as<float>(), m->qkv_cols, M, m->qkv_cols, H, st));
+      ST_TRY(gemm(m, m->x.p, H, wq, H, m->qkv.as<float>(), m->qkv_cols, M, m->qkv_cols, H, st, true));
     } else {
       // context-only forward: the K/V rows of the fused projection only
       const char* wkv = (const char*)w.w_qkv + (size_t)qd * H * es;
@@ -625,7 +628,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
     }
     m->launches += launch_qkv_post(m->dt, m->qkv.as<float>(), m->qkv_cols, dmeta, M, rope, w.q_norm, w.k_norm, Hq,
                                    Hkv, d, c.gated_attention, c.rms_eps, tabs, c.n_layers, l, m->Q.p,
-                                   m->G.as<float>(), st);
+                                   m->G.as<float>(), st, m->use_tc ? 1 : 0);
     ST_TRY(launch_check("qkv"));
     ap.layer = l;
     {
@@ -642,7 +645,7 @@ int run_forward(dflash_model* m, Forward& fw, cudaStream_t st) {
       if (how != 2)
         launch_attention_combine(m->dt, m->apart.as<float>(), (const int32_t*)(tb + o_ifirst),
                                  (const int32_t*)(tb + o_icount), Bc, ap, c.gated_attention ? m->G.as<float>() : nullptr,
-                                 m->O.p, st, max_splits);
+                                 m->O.p, st, max_splits, how == 1 ? 1 : 0);
       m->launches += 2;
     }
     ST_TRY(launch_check("attention"));

@@ -93,6 +93,10 @@ struct TcParams {
   // [groups * N][K], product g written at Y + g * y_group
   int groups;
   int64_t y_group;
+  // 1: the next kernel may start only once every thread of a CTA is past
+  // its wait (the whole chain before this kernel has finished), so that it
+  // can read that chain's tables before its own wait; 0: at once
+  int late_trigger;
 };
 
 // The tile a unit index names: product g, weight-row tile, activation-row tile.
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();  // the next kernel may be scheduled as this one's CTAs retire
+  if (!p.late_trigger) pdl_trigger();  // the next kernel may be scheduled as this one's CTAs retire
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -350,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
     });
     const int pre = it;
     pdl_wait();
+    if (p.late_trigger) pdl_trigger();
     it = 0;
     bool ok = true;
     for_each_unit<PERSIST>(p, [&](int t, int s) {
@@ -388,6 +393,10 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
     constexpr uint32_t idesc = idesc_bf16(BM, BN);
     int it = 0, j = 0;
     bool ok = true;
+    if (p.late_trigger) {  // this warp reads no memory of earlier kernels: the wait costs it nothing
+      pdl_wait();
+      pdl_trigger();
+    }
     for_each_unit<PERSIST>(p, [&](int, int s) {
       const int b = PERSIST ? (j & 1) : 0;
       if (PERSIST && j >= 2 &&
@@ -430,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
     const int row = q * 32 + lane;
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
     pdl_wait();  // the stores below read (residual) and write memory of earlier kernels
+    if (p.late_trigger) pdl_trigger();
     int j = 0;
     for_each_unit<PERSIST>(p, [&](int t, int s) {
       const int b = PERSIST ? (j & 1) : 0;
@@ -577,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
   if (!PERSIST) {
     // ---- split clusters: sum the partials in split order, then store ----
     pdl_wait();
+    if (p.late_trigger) pdl_trigger();
     const int t = (int)blockIdx.x / p.splits;
     const int m_tile = t / p.n_tiles, tok0 = (t % p.n_tiles) * BN;
     const int E = BN * ROWS / 4;  // 4-feature groups of the tile
@@ -753,12 +764,13 @@ int tc_gemm_grouped(TcContext* c, const void* X, int64_t ldx, const void* W, int
   const size_t fixed = extra_bytes(kWideBN, true, false) + 1024 + kBarrierBytes;
   const int stages = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed) / stage_bytes(kWideBN));
   TcParams p{Y, ldy, M, N, kF32, m_tiles, n_tiles, splits, kb_total, 0, stages, nullptr, 0, c->err, nullptr, groups,
-             y_group};
+             y_group, 0};
   return launch_bn<kWideBN, false, true>(c, mw, mw, mx, p, std::min(tiles, c->num_sms), 1, st, 12);
 }
 
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y,
-            int64_t ldy, int M, int N, int K, int mode, cudaStream_t st, void* const* yseg, int seg_rows, float* ws) {
+            int64_t ldy, int M, int N, int K, int mode, cudaStream_t st, void* const* yseg, int seg_rows, float* ws,
+            int late_trigger) {
   if (M <= 0 || N <= 0) return 0;
   const bool swi = mode == kSwigluBf16;
   if (yseg && (mode != kF32 || seg_rows <= 0)) return tc_fail("tc_gemm: row segments need fp32 output");
@@ -798,7 +810,8 @@ int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void*
   const size_t fixed = extra_bytes(BN, persist, swi) + 1024 + kBarrierBytes;
   const size_t budget = (persist || grid <= c->num_sms) ? kSmemMax : 112 * 1024;
   const int stages = (int)std::min<size_t>(kMaxStages, (budget - fixed) / stage_bytes(BN));
-  TcParams p{Y, ldy, M, N, mode, m_tiles, n_tiles, splits, kb_total, vec, stages, yseg, seg_rows, c->err, ws, 1, 0};
+  TcParams p{Y, ldy, M, N, mode, m_tiles, n_tiles, splits, kb_total, vec, stages, yseg, seg_rows, c->err, ws, 1, 0,
+             late_trigger};
   const int cluster = persist ? 1 : splits;
   return swi ? launch_mode<true>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st)
              : launch_mode<false>(c, BN, persist, mw, mw2, mx, p, grid, cluster, st);

@@ -31,9 +31,12 @@ enum TcMode {
 // Y + row * ldy; Y is then unused.  ws (kResidBf16 only, may be NULL): an
 // fp32 [M][N] scratch that lets many-row calls use 256-wide tiles, holding
 // the running sum of the K splits; its contents are overwritten.
+// late_trigger: the next kernel in the stream starts only once this one's
+// CTAs are past their wait for the previous kernel, so that everything
+// enqueued before this call has finished when it starts.
 int tc_gemm(TcContext* c, const void* X, int64_t ldx, const void* W, const void* W2, int64_t ldw, void* Y, int64_t ldy,
             int M, int N, int K, int mode, cudaStream_t st, void* const* yseg = nullptr, int seg_rows = 0,
-            float* ws = nullptr);
+            float* ws = nullptr, int late_trigger = 0);
 
 // `groups` independent fp32 products of one shape in one persistent launch of
 // 256-wide tiles: X stacked [groups * M][ldx], W stacked [groups * N][ldw],

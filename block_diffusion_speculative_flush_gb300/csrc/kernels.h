@@ -90,9 +90,12 @@ void launch_rmsnorm_layers(DT dt, const void* in, int64_t ld_in, const void* con
 // rows go to the transposed cache planes 32 rows at a time).
 constexpr int kVApartRows = 64;
 // rope: the model's table indexed by position ([pos][d/2]).
+// early: the kernel before this one (the QKV product) lets dependants start
+// only after its own wait, so the row and session tables are read before this
+// kernel's wait
 int launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
                     const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
-                    SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st);
+                    SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st, int early = 0);
 void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_items, SessTables tabs,
                            AttnParams p, float* part, cudaStream_t st);
 // bf16 block attention on tcgen05 tensor cores (key ranges must start on a
@@ -105,9 +108,12 @@ constexpr int kAttnMaxCluster = 16;
 int launch_attention_tc(const void* Q, const AttnItem* items, int n_items, SessTables tabs, AttnParams p, float* part,
                         int* err, cudaStream_t st);
 // max_splits: the largest item count of a session (0: not known); up to 32
-// the merge runs in one pass for d = 128
+// the merge runs in one pass for d = 128.  early: the partials come from
+// k_attn_tc, which lets this kernel start only after its own wait, so the
+// item tables and gates are read before this kernel's wait.
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count,
-                              int B, AttnParams p, const float* G, void* O, cudaStream_t st, int max_splits = 0);
+                              int B, AttnParams p, const float* G, void* O, cudaStream_t st, int max_splits = 0,
+                              int early = 0);
 void launch_residual(DT dt, void* h, const float* delta, int64_t ld_delta, int rows, int H, cudaStream_t st);
 void launch_swiglu(DT dt, const float* gu, int64_t ld, int rows, int I, int up_offset, void* a,
                    cudaStream_t st);

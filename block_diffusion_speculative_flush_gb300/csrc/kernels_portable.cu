@@ -74,7 +74,7 @@ __device__ __forceinline__ void norm_row_vec(const bf16* x, const uint4 (&gw)[kN
 #pragma unroll
   for (int i = 0; i < kNormVec; ++i) {
     const int c = threadIdx.x + i * blockDim.x;
-    w[i] = c < nv ? __ldg(reinterpret_cast<const uint4*>(x) + c) : make_uint4(0, 0, 0, 0);
+    w[i] = c < nv ? reinterpret_cast<const uint4*>(x)[c] : make_uint4(0, 0, 0, 0);
     float v[8];
     unpack8(w[i], v);
 #pragma unroll
@@ -117,13 +117,13 @@ __global__ void __launch_bounds__(128) k_rmsnorm_f32v(const float* __restrict__ 
   }
   pdl_wait();
   __shared__ float red[32];
-  const float4* x = reinterpret_cast<const float4*>(in + (int64_t)j * ld_in);
+  const float4* x = after_wait(reinterpret_cast<const float4*>(in + (int64_t)j * ld_in));
   float4 w[kNormF32Vec];
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < kNormF32Vec; ++i) {
     const int c = threadIdx.x + i * blockDim.x;
-    w[i] = c < nv ? __ldg(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    w[i] = c < nv ? x[c] : make_float4(0.f, 0.f, 0.f, 0.f);
     ss += w[i].x * w[i].x;
     ss += w[i].y * w[i].y;
     ss += w[i].z * w[i].z;
@@ -225,12 +225,12 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const TIn* __restrict__ in0, in
       uint4 gw[kNormVec];
       norm_gain_vec(g, H, gw);
       pdl_wait();
-      norm_row_vec(x, gw, o, H, eps, red);
+      norm_row_vec(after_wait(x), gw, o, H, eps, red);
       return;
     }
   }
   pdl_wait();
-  rmsnorm_row(x, g, o, H, eps, red);
+  rmsnorm_row(after_wait(x), g, o, H, eps, red);
 }
 
 // Every layer's input norm of the same rows at once (a context-only
@@ -289,29 +289,53 @@ template <typename T, int DU>  // DU = d / 32
 __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const RowMeta* __restrict__ meta,
                            const float2* __restrict__ rope, const T* __restrict__ q_norm,
                            const T* __restrict__ k_norm, int Hq, int Hkv, int gated, float eps, SessTables tabs,
-                           int layer, T* __restrict__ Q, float* __restrict__ G, int v_apart) {
+                           int layer, T* __restrict__ Q, float* __restrict__ G, int v_apart, int early) {
   constexpr int d = DU * 32;
   const int m = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const int hh = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const bool is_q = hh < Hq, head = hh < Hq + Hkv;
+  const int kh = hh - Hq;
   // the head-norm gain is a weight: read before the wait
   float gv[DU];
   const T* gn = is_q ? q_norm : k_norm;
 #pragma unroll
   for (int u = 0; u < DU; ++u) gv[u] = head ? to_f(gn[lane + 32 * u]) : 0.f;
+  // The row's table entry, its RoPE pair and the session's cache: written at
+  // the start of the call.  With `early` the product before this kernel let
+  // it start only once everything before that product had finished, so they
+  // are read before the wait.
+  RowMeta rm;
+  float2 cs[DU / 2];
+  int64_t cap = 1;
+  T* base = nullptr;
+  auto tables = [&] {
+    rm = meta[m];
+    if (!head) return;
+    const float2* rt = rope + rm.pos * (d / 2);  // the table is indexed by position
+#pragma unroll
+    for (int u = 0; u < DU / 2; ++u) cs[u] = rt[lane + 32 * u];
+    if (!is_q) {
+      cap = tabs.cap[rm.sess];
+      base = (T*)tabs.kv[rm.sess];
+    }
+  };
+  if (early) tables();
   // The attention kernel that follows reads the session tables and the
   // cache rows older than this forward before its own wait: it may start
   // only once every kernel before this one has finished, so the trigger
   // comes after the wait.
   pdl_wait();
   pdl_trigger();
-  const float* row = qkv + (int64_t)m * ldq;
-  // the head's values are read together with the row's table entry
-  float y[DU];
+  const float* row = after_wait(qkv + (int64_t)m * ldq);  // the product just before
+  // the head's values (and a K head's V values) in one round trip
+  float y[DU], xv[DU];
 #pragma unroll
-  for (int u = 0; u < DU; ++u) y[u] = head ? row[(int64_t)hh * d + lane + 32 * u] : 0.f;
-  const RowMeta rm = meta[m];
+  for (int u = 0; u < DU; ++u) {
+    y[u] = head ? row[(int64_t)hh * d + lane + 32 * u] : 0.f;
+    xv[u] = (head && !is_q && !v_apart) ? row[(int64_t)(Hq + Hkv + kh) * d + lane + 32 * u] : 0.f;
+  }
+  if (!early) tables();
   if (gated && rm.blk >= 0 && blockIdx.y == 0) {
     for (int hq = threadIdx.x; hq < Hq; hq += blockDim.x) {
       const float x = row[(Hq + 2 * Hkv) * d + hq];
@@ -320,7 +344,6 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
   }
   if (!head) return;
   if (is_q && rm.blk < 0) return;  // context rows need only K and V
-  const int kh = hh - Hq;
   float ss = 0.f;
 #pragma unroll
   for (int u = 0; u < DU; ++u) ss += y[u] * y[u];
@@ -328,13 +351,11 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
   const float inv = rsqrtf(ss / (float)d + eps);
 #pragma unroll
   for (int u = 0; u < DU; ++u) y[u] = y[u] * inv * gv[u];
-  const float2* rt = rope + rm.pos * (d / 2);  // the table is indexed by position
 #pragma unroll
   for (int u = 0; u < DU / 2; ++u) {
-    const float2 cs = rt[lane + 32 * u];
     const float a = y[u], b = y[u + DU / 2];
-    y[u] = a * cs.x - b * cs.y;
-    y[u + DU / 2] = b * cs.x + a * cs.y;
+    y[u] = a * cs[u].x - b * cs[u].y;
+    y[u + DU / 2] = b * cs[u].x + a * cs[u].y;
   }
   if (is_q) {
     T* q = Q + ((int64_t)rm.blk * Hq + hh) * d;
@@ -342,16 +363,13 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t ldq, const Row
     for (int u = 0; u < DU; ++u) q[lane + 32 * u] = from_f<T>(y[u]);
     return;
   }
-  const int64_t cap = tabs.cap[rm.sess];
   const int64_t slot = rm.pos % cap;
-  T* base = (T*)tabs.kv[rm.sess];
   T* kd = base + (((int64_t)(2 * layer) * Hkv + kh) * cap + slot) * d;
   T* vd = base + ((int64_t)(2 * layer + 1) * Hkv + kh) * cap * d + slot;  // V^T plane: [d][cap]
-  const float* xv = row + (int64_t)(Hq + Hkv + kh) * d;
 #pragma unroll
   for (int u = 0; u < DU; ++u) {
     kd[lane + 32 * u] = from_f<T>(y[u]);
-    if (!v_apart) vd[(int64_t)(lane + 32 * u) * cap] = from_f<T>(xv[lane + 32 * u]);
+    if (!v_apart) vd[(int64_t)(lane + 32 * u) * cap] = from_f<T>(xv[u]);
   }
 }
 
@@ -572,8 +590,8 @@ __device__ __forceinline__ void combine_d128(const float* __restrict__ base, int
 #pragma unroll
   for (int k = 0; k < NS; ++k) {
     if (k < S) {
-      ml[k] = __ldg(reinterpret_cast<const float2*>(base + k * sstride));
-      v[k] = __ldg(reinterpret_cast<const float4*>(base + k * sstride + 4 + lane * 4));
+      ml[k] = *reinterpret_cast<const float2*>(base + k * sstride);
+      v[k] = *reinterpret_cast<const float4*>(base + k * sstride + 4 + lane * 4);
     } else {
       ml[k] = make_float2(-INFINITY, 0.f);
       v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -610,9 +628,12 @@ template <int NSMAX, typename T>
 __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part,
                                                       const int32_t* __restrict__ item_first,
                                                       const int32_t* __restrict__ item_count, AttnParams p, int total,
-                                                      const float* __restrict__ Gt, T* __restrict__ O) {
+                                                      const float* __restrict__ Gt, T* __restrict__ O, int early) {
   pdl_trigger();
-  pdl_wait();
+  // early: the attention kernel before this one let it start only after its
+  // own wait, so the item tables and the gates (written earlier in the call)
+  // are read before this kernel's wait, the partials after it
+  if (!early) pdl_wait();
   __shared__ float wsm[4][64];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int gw = blockIdx.x * 4 + wl;  // (b, i, hq) flattened
@@ -624,8 +645,10 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
   const int S = item_count[b];
   const float* base = part + ((int64_t)(item_first[b] + kvh * S) * R + rr) * PD;
   const int64_t sstride = (int64_t)R * PD;
+  const float gate = Gt ? Gt[(int64_t)bi * p.Hq + hq] : 1.f;
+  if (early) pdl_wait();
+  base = after_wait(base);  // the partials: written by the kernel just before
   if (S <= NSMAX && d == 128) {
-    const float gate = Gt ? Gt[(int64_t)bi * p.Hq + hq] : 1.f;
     T* out = O + ((int64_t)bi * p.Hq + hq) * d;
     if (NSMAX == 16 || S <= 16)
       combine_d128<16>(base, sstride, S, lane, gate, out);
@@ -656,7 +679,6 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
   }
   L = warp_sum(L);
   __syncwarp();
-  const float gate = Gt ? Gt[(int64_t)bi * p.Hq + hq] : 1.f;
   const float scale = gate / L;
   T* out = O + ((int64_t)bi * p.Hq + hq) * d;
   for (int t4 = lane * 4; t4 < d; t4 += 128) {
@@ -666,7 +688,7 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
       float4 v[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k)
-        v[k] = s0 + k < S ? __ldg(reinterpret_cast<const float4*>(base + (s0 + k) * sstride + 4 + t4))
+        v[k] = s0 + k < S ? *reinterpret_cast<const float4*>(base + (s0 + k) * sstride + 4 + t4)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
@@ -801,6 +823,7 @@ __device__ __forceinline__ RowRef row_ref(const SampleArgs& a, int row) {
                : (const void*)((const float*)a.logits + (int64_t)row * a.ld);
   }
   r.vec = (a.V & 3) == 0 && ((uintptr_t)r.p & (r.bf ? 7u : 15u)) == 0;
+  r.p = after_wait(r.p);  // callers resolve rows after their wait
   return r;
 }
 // Entries 4g..4g+3 scaled by invT (the same product as the draw's); entries
@@ -809,13 +832,13 @@ __device__ __forceinline__ void load_quad(const RowRef& r, int g, int V, float i
   const int v = 4 * g;
   if (r.vec && v < V) {
     if (r.bf) {
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(r.p) + g);
+      const uint2 w = reinterpret_cast<const uint2*>(r.p)[g];
       x[0] = __uint_as_float(w.x << 16) * invT;
       x[1] = __uint_as_float(w.x & 0xffff0000u) * invT;
       x[2] = __uint_as_float(w.y << 16) * invT;
       x[3] = __uint_as_float(w.y & 0xffff0000u) * invT;
     } else {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(r.p) + g);
+      const float4 f = reinterpret_cast<const float4*>(r.p)[g];
       x[0] = f.x * invT;
       x[1] = f.y * invT;
       x[2] = f.z * invT;
@@ -903,7 +926,7 @@ __global__ void __launch_bounds__(256, 4) k_sample_partials(SampleArgs a, int ch
       for (int it = 0; it < kSampleSteps; ++it) {
         const int v4 = base + it * 4 * kSampleThreads;
         if (v4 + 3 < v1) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(rowp + v4));
+          const float4 f = *reinterpret_cast<const float4*>(rowp + v4);
           x[it][0] = f.x * invT;
           x[it][1] = f.y * invT;
           x[it][2] = f.z * invT;
@@ -1812,7 +1835,7 @@ void launch_rmsnorm_layers(DT dt, const void* in, int64_t ld_in, const void* con
 
 int launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, int M, const float2* rope,
                     const void* q_norm, const void* k_norm, int Hq, int Hkv, int d, int gated, float eps,
-                    SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st) {
+                    SessTables tabs, int L, int layer, void* Q, float* G, cudaStream_t st, int early) {
   (void)L;
   if (M <= 0) return 0;
   const int heads = Hq + Hkv;
@@ -1822,14 +1845,14 @@ int launch_qkv_post(DT dt, const float* qkv, int64_t ldq, const RowMeta* meta, i
   if (d == 64) {
     DFL_DISPATCH(dt, launch_k(k_qkv_post<T, 2>, grid, 128, 0, st, qkv, ldq, meta, rope, (const T*)q_norm,
                                                               (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
-                                                              (T*)Q, G, v_apart));
+                                                              (T*)Q, G, v_apart, early));
     if (v_apart)
       DFL_DISPATCH(dt, launch_k(k_v_cache_t<T, 64>, dim3(cdiv(M, 32), Hkv), 256, 0, st, qkv, ldq, meta, M, Hq, Hkv,
                                 tabs, layer));
   } else {
     DFL_DISPATCH(dt, launch_k(k_qkv_post<T, 4>, grid, 128, 0, st, qkv, ldq, meta, rope, (const T*)q_norm,
                                                               (const T*)k_norm, Hq, Hkv, gated, eps, tabs, layer,
-                                                              (T*)Q, G, v_apart));
+                                                              (T*)Q, G, v_apart, early));
     if (v_apart)
       DFL_DISPATCH(dt, launch_k(k_v_cache_t<T, 128>, dim3(cdiv(M, 32), Hkv), 256, 0, st, qkv, ldq, meta, M, Hq, Hkv,
                                 tabs, layer));
@@ -1849,14 +1872,14 @@ void launch_attention_simt(DT dt, const void* Q, const AttnItem* items, int n_it
 }
 
 void launch_attention_combine(DT dt, const float* part, const int32_t* item_first, const int32_t* item_count, int B,
-                              AttnParams p, const float* G, void* O, cudaStream_t st, int max_splits) {
+                              AttnParams p, const float* G, void* O, cudaStream_t st, int max_splits, int early) {
   const int total = B * p.nrows * p.Hq;
   if (max_splits > 16 && max_splits <= 32) {
     DFL_DISPATCH(dt, launch_k(k_attn_combine<32, T>, cdiv(total, 4), 128, 0, st, part, item_first, item_count, p,
-                              total, G, (T*)O));
+                              total, G, (T*)O, early));
   } else {
     DFL_DISPATCH(dt, launch_k(k_attn_combine<16, T>, cdiv(total, 4), 128, 0, st, part, item_first, item_count, p,
-                              total, G, (T*)O));
+                              total, G, (T*)O, early));
   }
 }
 

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(256) k_gemm_rows(const float* __restrict__ X, 
                                                    int64_t ldy, int M, int N, int K) {
   pdl_trigger();
   pdl_wait();
+  X = after_wait(X);  // the previous kernel's rows
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (n >= N) return;
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(256) k_gemm_rows(const float* __restrict__ X, 
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         if (m0 + r < M) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(X + (int64_t)(m0 + r) * ldx) + k);
+          const float4 x = reinterpret_cast<const float4*>(X + (int64_t)(m0 + r) * ldx)[k];
           float a = acc[r];
           a = fmaf(x.x, w.x, a);
           a = fmaf(x.y, w.y, a);
