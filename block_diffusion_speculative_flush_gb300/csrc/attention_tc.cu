@@ -521,10 +521,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_tc(const bf16* __restrict__
     if (dual) {
       if (stream == 1 && live) {
         if (rv && half == 0) *reinterpret_cast<float2*>(xo) = make_float2(m_used, lsum);
+        // Stream 1 owns the odd tiles.  With a single tile it ran no product
+        // and its TMEM O region still holds whatever an earlier kernel left
+        // there, not necessarily finite numbers; its weight below is zero, and
+        // zero times a NaN is a NaN, so it hands over zeros instead.
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
           float o[32];
-          tmem_ld32(tmem + lrow + ocol + c, o);
+          if (T > 1) {
+            tmem_ld32(tmem + lrow + ocol + c, o);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = 0.f;
+          }
           if (rv) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
