@@ -114,6 +114,41 @@ def test_qwen3_8b_round_at_ctx_4096(qwen):
     D.dflash_close(s)
 
 
+def test_single_tile_attention_after_nan_in_every_sms_tmem(qwen):
+    """Tensor memory is not cleared between kernels.  A 2048-row flush of NaN
+    features runs the fc product on persistent 512-column accumulators on
+    every SM, so every SM's TMEM then holds NaN.  A fresh session with 20
+    context rows gives attention work items of one key tile each: with 64
+    query rows the second softmax stream gets no tile, and what it hands to
+    the merge must not come from its unwritten TMEM.  The proposal must be
+    finite and follow the oracle."""
+    D = lib()
+    cfg = qwen.cfg
+    n = cfg.block_size - 1
+    poison = D.dflash_open(qwen.model, max_ctx=2048 + 64)
+    bad = torch.full((2048, cfg.feature_width), float("nan"), device="cuda", dtype=torch.bfloat16)
+    D.dflash_committed(poison, bad, 0)  # 2048 pending rows: flushed in this call
+    torch.cuda.synchronize()
+    D.dflash_close(poison)
+    f_np = S.make_features(cfg, 20, seed=44, name="tmem.features")
+    s = D.dflash_open(qwen.model, max_ctx=128)
+    D.dflash_committed(s, torch.from_numpy(f_np).cuda().to(torch.bfloat16), 0)
+    cur = torch.tensor([5], dtype=torch.int32, device="cuda")
+    tok = torch.empty((1, n), dtype=torch.int32, device="cuda")
+    q = torch.empty((1, n), dtype=torch.float32, device="cuda")
+    lg = torch.empty((1, n, cfg.vocab), dtype=torch.float32, device="cuda")
+    assert D.dflash_propose([s], cur, n, 0.0, 0, 1, tok, q, lg) == [n]
+    torch.cuda.synchronize()
+    g_lg = lg[0].double().cpu().numpy()
+    assert np.isfinite(g_lg).all()
+    o = O.OracleSession(qwen.oracle)
+    o.committed(f_np, 0)
+    ref = o.propose(5, n, 0.0, 0, 1)
+    assert_logits_full(g_lg, ref["logits"])
+    D.dflash_device_status(qwen.model)
+    D.dflash_close(s)
+
+
 def test_flush_8_x_256_rows(qwen):
     """8 sequences at context offsets 0, 1k, ..., 7k each commit 256 rows,
     which flush in one context-only forward after a block rewind; the cursors
