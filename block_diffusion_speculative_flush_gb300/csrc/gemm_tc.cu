@@ -386,6 +386,14 @@ __global__ void __launch_bounds__(kThreads, PERSIST ? 1 : 2) k_gemm_tc(const __g
         }
       }
     }
+  } else if (warp == 0) {
+    // The producer warp's other lanes are idle until the epilogue.  A CTA's
+    // trigger counts once every one of its threads has executed it, so with a
+    // late trigger they wait and trigger at once rather than at the end.
+    if (p.late_trigger) {
+      pdl_wait();
+      pdl_trigger();
+    }
   } else if (warp == 1) {
     // ---- MMA issuer: the whole warp runs the loop (every lane waits on the
     // barriers itself, decisions are taken together) and one elected lane
